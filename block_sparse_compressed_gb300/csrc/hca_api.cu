@@ -1,0 +1,201 @@
+// hca_api.cu -- the exported C ABI of libhca (see include/hca.h): argument
+// validation, workspace carving and kernel dispatch.  Everything is enqueued
+// on the caller's stream; nothing here allocates or synchronises except
+// hca_workspace_status, whose job is to synchronise.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "hca_common.cuh"
+#include "hca_internal.h"
+
+using namespace hca;
+
+namespace {
+
+constexpr int kMaxD = 256;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elt_bytes(int dtype) { return dtype == HCA_F32 ? 4 : 2; }
+
+// Common checks of sizes and scalar arguments.
+int check_dims(int B, int H, int S, int D, int W, int m, int dtype) {
+  if (dtype != HCA_BF16 && dtype != HCA_F32) return HCA_ERR_DTYPE;
+  if (B < 0 || H < 1 || S < 0 || D < 1 || D > kMaxD) return HCA_ERR_SHAPE;
+  // every flat index of the largest tensor must fit in 63 bits and every
+  // position index in 31 bits
+  if ((double)B * H * (double)S * D > 9.0e18 || S > (1 << 30) || H > (1 << 20)) return HCA_ERR_SHAPE;
+  if (W < 1 || m < 1) return HCA_ERR_ARG;
+  if ((D * elt_bytes(dtype)) % 16 != 0) return HCA_ERR_ALIGN;
+  return HCA_OK;
+}
+
+size_t fwd_ws_bytes(int B, int S) { return kHeaderBytes + align_up((size_t)B * S * sizeof(int32_t)); }
+
+size_t bwd_ws_bytes(int B, int H, int S, int D, int W, int m, int dtype) {
+  size_t n = fwd_ws_bytes(B, S) + align_up((size_t)B * H * S * sizeof(float));
+  n += tc_bwd_scratch_bytes(B, H, S, D, W, m, dtype);
+  return n;
+}
+
+struct Carve {
+  char *p;
+  int32_t *status;
+  int32_t *sstart;
+};
+
+Carve carve_fwd(void *ws, int B, int S) {
+  Carve c;
+  c.p = static_cast<char *>(ws);
+  c.status = reinterpret_cast<int32_t *>(c.p);
+  c.sstart = reinterpret_cast<int32_t *>(c.p + kHeaderBytes);
+  return c;
+}
+
+int check_ws(void *ws, size_t have, size_t need) {
+  if (need == 0) return HCA_OK;
+  if (ws == nullptr) return HCA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return HCA_ERR_WORKSPACE;
+  if (have < need) return HCA_ERR_WORKSPACE;
+  return HCA_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? HCA_OK : HCA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *hca_status_string(int s) {
+  switch (s) {
+    case HCA_OK: return "HCA_OK";
+    case HCA_ERR_NULL: return "HCA_ERR_NULL: a required pointer is NULL";
+    case HCA_ERR_SHAPE: return "HCA_ERR_SHAPE: B, H, S or D out of range";
+    case HCA_ERR_DTYPE: return "HCA_ERR_DTYPE: unknown dtype";
+    case HCA_ERR_ALIGN: return "HCA_ERR_ALIGN: pointer not 16-byte aligned or D*element size not a multiple of 16";
+    case HCA_ERR_ARG: return "HCA_ERR_ARG: W < 1, m < 1, non-finite scale or bad tile size";
+    case HCA_ERR_SEG: return "HCA_ERR_SEG: segment ids decrease or padding is not a suffix";
+    case HCA_ERR_WORKSPACE: return "HCA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case HCA_ERR_UNSUPPORTED: return "HCA_ERR_UNSUPPORTED: no kernel for this dtype/D combination";
+    case HCA_ERR_CUDA: return "HCA_ERR_CUDA: a CUDA call or launch failed";
+    case HCA_ERR_TIMEOUT: return "HCA_ERR_TIMEOUT: an on-device wait gave up";
+    default: return "HCA_ERR_UNKNOWN";
+  }
+}
+
+int hca_version(void) { return 1; }
+
+size_t hca_workspace_size(int B, int H, int S, int D, int W, int m, int dtype, int for_backward) {
+  if (check_dims(B, H, S, D, W, m, dtype) != HCA_OK) return 0;
+  return for_backward ? bwd_ws_bytes(B, H, S, D, W, m, dtype) : fwd_ws_bytes(B, S);
+}
+
+int hca_query_tile_positions(int H, int D, int dtype) {
+  if (H < 1) return 0;
+  if (tc_fwd_supported(H, D, dtype)) return tc_query_tile_positions(H);
+  return 1;
+}
+
+int hca_attn_fwd(const void *q, const void *kv, const void *ckv, const int32_t *seg, void *out, float *lse, int B,
+                 int H, int S, int D, int W, int m, float scale, int dtype, void *workspace, size_t workspace_bytes,
+                 void *stream) {
+  int rc = check_dims(B, H, S, D, W, m, dtype);
+  if (rc != HCA_OK) return rc;
+  if (!std::isfinite(scale)) return HCA_ERR_ARG;
+  if (B * (long long)S == 0) return HCA_OK;
+  if (!q || !kv || !ckv || !out || !lse) return HCA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(ckv) || !aligned16(out) || !aligned16(lse) ||
+      (seg && !aligned16(seg)))
+    return HCA_ERR_ALIGN;
+  rc = check_ws(workspace, workspace_bytes, fwd_ws_bytes(B, S));
+  if (rc != HCA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carve c = carve_fwd(workspace, B, S);
+  rc = cuda_status(launch_prep(seg, B, S, c.sstart, c.status, st));
+  if (rc != HCA_OK) return rc;
+  FwdArgs a;
+  a.q = q; a.kv = kv; a.ckv = ckv;
+  a.sstart = seg ? c.sstart : nullptr;
+  a.status = c.status; a.status_rw = c.status;
+  a.out = out; a.lse = lse;
+  a.B = B; a.H = H; a.S = S; a.D = D; a.W = W; a.m = m; a.scale = scale; a.dtype = dtype;
+  if (tc_fwd_supported(H, D, dtype)) return cuda_status(tc_fwd(a, st));
+  return cuda_status(simt_fwd(a, st));
+}
+
+int hca_attn_bwd(const void *q, const void *kv, const void *ckv, const int32_t *seg, const void *out,
+                 const float *lse, const void *dout, void *dq, void *dkv, void *dckv, int B, int H, int S, int D,
+                 int W, int m, float scale, int dtype, void *workspace, size_t workspace_bytes, void *stream) {
+  int rc = check_dims(B, H, S, D, W, m, dtype);
+  if (rc != HCA_OK) return rc;
+  if (!std::isfinite(scale)) return HCA_ERR_ARG;
+  if (B * (long long)S == 0) return HCA_OK;
+  if (!q || !kv || !ckv || !out || !lse || !dout || !dq || !dkv || !dckv) return HCA_ERR_NULL;
+  const void *ptrs[] = {q, kv, ckv, out, lse, dout, dq, dkv, dckv};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return HCA_ERR_ALIGN;
+  if (seg && !aligned16(seg)) return HCA_ERR_ALIGN;
+  rc = check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, S, D, W, m, dtype));
+  if (rc != HCA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carve c = carve_fwd(workspace, B, S);
+  rc = cuda_status(launch_prep(seg, B, S, c.sstart, c.status, st));
+  if (rc != HCA_OK) return rc;
+  char *p = c.p + fwd_ws_bytes(B, S);
+  BwdArgs a;
+  a.q = q; a.kv = kv; a.ckv = ckv; a.out = out; a.dout = dout; a.lse = lse;
+  a.sstart = seg ? c.sstart : nullptr;
+  a.status = c.status; a.status_rw = c.status;
+  a.dq = dq; a.dkv = dkv; a.dckv = dckv;
+  a.delta = reinterpret_cast<float *>(p);
+  p += align_up((size_t)B * H * S * sizeof(float));
+  a.scratch = p;
+  a.scratch_bytes = tc_bwd_scratch_bytes(B, H, S, D, W, m, dtype);
+  a.B = B; a.H = H; a.S = S; a.D = D; a.W = W; a.m = m; a.scale = scale; a.dtype = dtype;
+  if (tc_bwd_supported(H, D, dtype)) return cuda_status(tc_bwd(a, st));
+  return cuda_status(simt_bwd(a, st));
+}
+
+int hca_visible_pairs(const int32_t *seg, int B, int S, int W, int m, int64_t *raw_pairs, int64_t *comp_pairs,
+                      void *workspace, size_t workspace_bytes, void *stream) {
+  if (B < 0 || S < 0 || S > (1 << 30)) return HCA_ERR_SHAPE;
+  if (W < 1 || m < 1) return HCA_ERR_ARG;
+  if (B == 0) return HCA_OK;
+  if (!raw_pairs || !comp_pairs) return HCA_ERR_NULL;
+  if (seg && !aligned16(seg)) return HCA_ERR_ALIGN;
+  int rc = check_ws(workspace, workspace_bytes, fwd_ws_bytes(B, S));
+  if (rc != HCA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carve c = carve_fwd(workspace, B, S);
+  rc = cuda_status(launch_prep(seg, B, S, c.sstart, c.status, st));
+  if (rc != HCA_OK) return rc;
+  return cuda_status(launch_visible_pairs(seg ? c.sstart : nullptr, B, S, W, m, raw_pairs, comp_pairs, st));
+}
+
+int hca_tile_map(const int32_t *seg, int B, int S, int W, int m, int Pq, int32_t *map, void *workspace,
+                 size_t workspace_bytes, void *stream) {
+  if (B < 0 || S < 0 || S > (1 << 30)) return HCA_ERR_SHAPE;
+  if (W < 1 || m < 1 || Pq < 1) return HCA_ERR_ARG;
+  if (B * (long long)S == 0) return HCA_OK;
+  if (!map) return HCA_ERR_NULL;
+  if (!aligned16(map) || (seg && !aligned16(seg))) return HCA_ERR_ALIGN;
+  int rc = check_ws(workspace, workspace_bytes, fwd_ws_bytes(B, S));
+  if (rc != HCA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carve c = carve_fwd(workspace, B, S);
+  rc = cuda_status(launch_prep(seg, B, S, c.sstart, c.status, st));
+  if (rc != HCA_OK) return rc;
+  return cuda_status(launch_tile_map(seg ? c.sstart : nullptr, B, S, W, m, Pq, map, st));
+}
+
+int hca_workspace_status(const void *workspace, void *stream) {
+  if (!workspace) return HCA_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess) return HCA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return HCA_ERR_CUDA;
+  return v;
+}
+
+}  // extern "C"

@@ -1,0 +1,54 @@
+// hca_internal.h -- launch interfaces shared by the translation units of
+// libhca (not part of the public C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace hca {
+
+struct FwdArgs {
+  const void *q, *kv, *ckv;
+  const int32_t *sstart;  // NULL = one segment per row
+  const int32_t *status;  // device status word (non-zero: poison outputs)
+  int32_t *status_rw;     // same word, writable (bounded waits report here)
+  void *out;
+  float *lse;
+  int B, H, S, D, W, m;
+  float scale;
+  int dtype;
+};
+
+struct BwdArgs {
+  const void *q, *kv, *ckv, *out, *dout;
+  const float *lse;
+  const int32_t *sstart;
+  const int32_t *status;
+  int32_t *status_rw;
+  void *dq, *dkv, *dckv;
+  float *delta;  // [B,H,S] workspace
+  void *scratch; // further backward workspace (tensor-core path)
+  size_t scratch_bytes;
+  int B, H, S, D, W, m;
+  float scale;
+  int dtype;
+};
+
+cudaError_t launch_prep(const int32_t *seg, int B, int S, int32_t *sstart, int32_t *status, cudaStream_t st);
+cudaError_t launch_visible_pairs(const int32_t *sstart, int B, int S, int W, int m, int64_t *raw, int64_t *comp,
+                                 cudaStream_t st);
+cudaError_t launch_tile_map(const int32_t *sstart, int B, int S, int W, int m, int Pq, int32_t *map, cudaStream_t st);
+
+cudaError_t simt_fwd(const FwdArgs &a, cudaStream_t st);
+cudaError_t simt_bwd(const BwdArgs &a, cudaStream_t st);
+
+// tensor-core (tcgen05) path
+bool tc_fwd_supported(int H, int D, int dtype);
+int tc_query_tile_positions(int H);
+cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st);
+bool tc_bwd_supported(int H, int D, int dtype);
+size_t tc_bwd_scratch_bytes(int B, int H, int S, int D, int W, int m, int dtype);
+cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st);
+
+}  // namespace hca

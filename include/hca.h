@@ -1,0 +1,142 @@
+/*
+ * hca.h -- C ABI of libhca: DeepSeek-V4 Heavily Compressed Attention (HCA),
+ * forward and backward, on NVIDIA GB300 (sm_103a).
+ *
+ * The operation.  Single-KV-head (MQA) attention in which the one shared kv
+ * tensor is both key and value ("[DeepSeek-V4] Implement Compressed Attention
+ * Layers", review suggestions on the logits and output einsums: k = v = kv,
+ * broadcast over the query heads).  Query position i of batch row b attends,
+ * under one softmax, to
+ *   - the raw kv rows t with i-W < t <= i (causal sliding window), and
+ *   - the compressed entries ckv[j] whose length-m window [j*m, (j+1)*m-1]
+ *     has completed, (j+1)*m <= i+1,
+ * ("Add HCA Static Compilation for Splash Attention [Deepseek v4]",
+ * Description: the HCA pattern is the local sliding window plus the completed
+ * earlier compression windows), restricted to keys of the query's own packed
+ * document: raw rows with the same segment id, compressed entries whose whole
+ * window carries that id (same page, packing and segment-id bullet; "DSV4:
+ * Route compressed and sliding train attention onto the splash kernels",
+ * segment-mask review suggestion).  Sequence lengths need not be multiples of
+ * any tile size (same page, unaligned-length bullet).  No mask tensor is ever
+ * written: visibility is computed from coordinates inside the kernels.
+ *
+ * Conventions shared by every entry point.
+ *   Layout   q, out, dq, dout: [B,H,S,D]; kv, dkv: [B,S,D];
+ *            ckv, dckv: [B,Sc,D] with Sc = ceil(S/m); seg: [B,S] int32;
+ *            lse: [B,H,S] fp32.  All contiguous, row-major.
+ *   dtype    HCA_BF16: q/kv/ckv/out/dout/dq/dkv/dckv are bfloat16, the
+ *            arithmetic is bf16 tensor-core products with fp32 accumulation
+ *            and fp32 softmax.  HCA_F32: everything fp32, fp32 arithmetic.
+ *            lse is fp32 in both.
+ *   seg      NULL means one segment per batch row.  Otherwise non-negative
+ *            ids must be non-decreasing along S and negative ids (padding)
+ *            must form a suffix of each row; padded positions are neither
+ *            queries nor keys (out = 0, lse = -inf, dq = 0).  This ordering
+ *            is checked on the device; a violation is reported through
+ *            hca_workspace_status and the outputs of that call are NaN.
+ *   Memory   Every pointer is a device pointer owned by the caller.  Tensor
+ *            base pointers must be 16-byte aligned and D * element size must
+ *            be a multiple of 16 bytes.  The library allocates and frees
+ *            nothing; scratch comes from the caller's workspace (at least
+ *            hca_workspace_size bytes, 256-byte aligned).
+ *   Streams  Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *            default stream) and the call returns without synchronising.
+ *   Errors   Every entry returns an hca_status.  Argument errors are
+ *            detected on the host before anything is enqueued; launch
+ *            failures return HCA_ERR_CUDA.  Nothing aborts the process.
+ */
+#ifndef HCA_H_
+#define HCA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define HCA_API __attribute__((visibility("default")))
+#else
+#define HCA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HCA_OK = 0,
+  HCA_ERR_NULL = 1,        /* a required pointer is NULL                       */
+  HCA_ERR_SHAPE = 2,       /* B, H, S or D out of range                        */
+  HCA_ERR_DTYPE = 3,       /* unknown dtype code                               */
+  HCA_ERR_ALIGN = 4,       /* pointer not 16-byte aligned, or D*elt % 16 != 0  */
+  HCA_ERR_ARG = 5,         /* W < 1, m < 1, scale not finite, bad tile size    */
+  HCA_ERR_SEG = 6,         /* segment ids out of order (device-side check)     */
+  HCA_ERR_WORKSPACE = 7,   /* workspace NULL, misaligned or too small          */
+  HCA_ERR_UNSUPPORTED = 8, /* no kernel for this dtype / D combination         */
+  HCA_ERR_CUDA = 9,        /* a CUDA runtime call or launch failed             */
+  HCA_ERR_TIMEOUT = 10     /* a bounded on-device wait gave up                 */
+} hca_status;
+
+typedef enum { HCA_BF16 = 0, HCA_F32 = 1 } hca_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+HCA_API const char *hca_status_string(int status);
+
+/* ABI version of this library (increases when an entry point changes). */
+HCA_API int hca_version(void);
+
+/* Bytes of caller-provided workspace that hca_attn_fwd (for_backward = 0)
+ * or hca_attn_bwd (for_backward = 1) needs for these sizes; 0 when the
+ * arguments are invalid.  Grows as O(B*S + B*H*S + Sc*D): never O(S^2). */
+HCA_API size_t hca_workspace_size(int B, int H, int S, int D, int W, int m, int dtype, int for_backward);
+
+/* Number of consecutive query positions the forward kernel packs into one
+ * tile for H heads (all H heads of a position share the tile), i.e. the Pq
+ * argument that makes hca_tile_map describe the forward's own tiles. */
+HCA_API int hca_query_tile_positions(int H, int D, int dtype);
+
+/* Forward.  out[B,H,S,D] = softmax-weighted sum of the visible keys;
+ * lse[B,H,S] = natural-log logsumexp of the scaled visible logits
+ * (scale * <q, key>).  Cited passage: see the header comment.
+ * Returns HCA_OK once the work is enqueued. */
+HCA_API int hca_attn_fwd(const void *q, const void *kv, const void *ckv, const int32_t *seg,
+                 void *out, float *lse,
+                 int B, int H, int S, int D, int W, int m, float scale, int dtype,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward of hca_attn_fwd for the cotangent dout = dL/dout, given the
+ * forward's out and lse.  dq[B,H,S,D]; dkv[B,S,D] and dckv[B,Sc,D] each sum
+ * the key-role and the value-role gradient of the shared rows over every
+ * head and visible query ("[DeepSeek-V4] Implement Compressed Attention
+ * Layers": k and v are the same tensor).  dq, dkv and dckv are fully
+ * overwritten. */
+HCA_API int hca_attn_bwd(const void *q, const void *kv, const void *ckv, const int32_t *seg,
+                 const void *out, const float *lse, const void *dout,
+                 void *dq, void *dkv, void *dckv,
+                 int B, int H, int S, int D, int W, int m, float scale, int dtype,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Visible (query, key) pairs per head of every batch row, from the same
+ * interval arithmetic the attention kernels use: raw_pairs[B] over raw kv
+ * rows and comp_pairs[B] over compressed entries (device int64 arrays,
+ * overwritten).  Needs hca_workspace_size(B,1,S,16,W,m,HCA_F32,0) bytes. */
+HCA_API int hca_visible_pairs(const int32_t *seg, int B, int S, int W, int m,
+                      int64_t *raw_pairs, int64_t *comp_pairs,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* Per query tile of Pq consecutive positions, the half-open key ranges the
+ * kernels visit: map[B][ceil(S/Pq)][4] = {raw_lo, raw_hi, comp_lo, comp_hi}
+ * (device int32, overwritten; 0,0 = no key of that kind).  Keys outside
+ * these ranges are never loaded.  Same workspace as hca_visible_pairs. */
+HCA_API int hca_tile_map(const int32_t *seg, int B, int S, int W, int m, int Pq, int32_t *map,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronises `stream` and returns the status the device recorded in this
+ * workspace during the last call that used it (HCA_OK, HCA_ERR_SEG or
+ * HCA_ERR_TIMEOUT), or HCA_ERR_CUDA if the synchronisation failed.  This is
+ * the one entry point that blocks the host. */
+HCA_API int hca_workspace_status(const void *workspace, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HCA_H_ */
