@@ -59,9 +59,24 @@ def test_edge_windows_bf16(W, m):
     run_case(1, 8, 300, 128, W, m, torch.bfloat16)
 
 
-@pytest.mark.parametrize("H", [1, 4, 16, 64])
+@pytest.mark.parametrize("H", [1, 4, 16, 64, 128, 256])
 def test_heads_bf16(H):
-    run_case(1, H, 260, 128, 64, 32, torch.bfloat16)
+    run_case(1, H, 260, 128, 64, 32, torch.bfloat16, backward=H <= 64)
+
+
+@pytest.mark.parametrize("H,D", [(3, 128), (4, 64), (6, 32)])
+def test_cuda_core_bf16_shapes(H, D):
+    # head counts / dims the tensor-core tiles do not take run on CUDA cores
+    run_case(1, H, 200, D, 48, 16, torch.bfloat16)
+
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_long_window_multiple_raw_blocks(B):
+    # W > 128: a tile's raw range spans several 128-key blocks
+    rng = np.random.Generator(np.random.PCG64(B))
+    S = 700
+    seg = np.stack([I.random_layout(S, rng, allow_pad=True) for _ in range(B)])
+    run_case(B, 16, S, 128, 333, 64, torch.bfloat16, seg, backward=False)
 
 
 def test_segments_off_boundary_and_short_docs_bf16():
