@@ -135,11 +135,19 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk16) {
   return (uint32_t)(half * kHalfTile + row * 128 + ((c ^ (row & 7)) << 4));
 }
 
+// Bounded wait whose outcome is the same for the whole warp, so that a warp
+// never splits around the warp-collective tcgen05.ld / tcgen05.st.
+__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort, int32_t *status) {
+  const bool ok = mbar_wait(bar, parity, abort, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full, s_free;
   uint64_t p_full[2], o_done[2];
+  uint64_t epi;  // softmax-warp rendezvous before the output store
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -168,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.p_full[k], kSoftmaxThreads);
       mbar_init(&bars.o_done[k], 1);
     }
+    mbar_init(&bars.epi, kSoftmaxThreads);
     mbar_init(&bars.drain, 1);
     bars.abort = 0;
     fence_mbar_init();
@@ -320,12 +329,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t done_cnt[2] = {0, 0};
     bool ok = true;
     bool store_pending = false;
+    uint32_t epi_phase = 0;
+    // all 128 softmax threads meet here (bounded; never a bar.sync, so a
+    // CTA that aborted cannot strand a thread)
+    auto rendezvous = [&]() -> bool {
+      mbar_arrive(&bars.epi);
+      const bool r = wait_warp(&bars.epi, epi_phase & 1, abort_flag, p.status);
+      ++epi_phase;
+      return r;
+    };
     // wait until PV number x (global) has completed
     auto wait_pv = [&](uint32_t x) -> bool {
       const int buf = x & 1;
       const uint32_t need = (x >> 1) + 1;
       while (done_cnt[buf] < need) {
-        if (!mbar_wait(&bars.o_done[buf], done_cnt[buf] & 1, abort_flag, p.status)) return false;
+        if (!wait_warp(&bars.o_done[buf], done_cnt[buf] & 1, abort_flag, p.status)) return false;
         ++done_cnt[buf];
       }
       return true;
@@ -364,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           lo_c = max(lo - start, 0);
           hi_c = min(hi - start, n - 1);
         }
-        if (!mbar_wait(&bars.s_full, gb & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_warp(&bars.s_full, gb & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         float s[kBlockKeys];
         {
@@ -429,7 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4 *>(pb + sw128_offset(r, ch)) = v;
           }
         }
-        if (rescale_o) {
+        // the TMEM access below is warp-collective: rescale when any row of the
+        // warp needs it (rows without a new max use f = 1)
+        if (__any_sync(0xffffffffu, rescale_o)) {
           // PV(j) waits for this block's P, so O is stable once PV(j-1) is done
           if (!wait_pv(gb - 1)) { ok = false; break; }
           tc_fence_after();
@@ -453,8 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_pv(gb - 1)) { ok = false; break; }
       tc_fence_after();
       if (store_pending) {
+        // the previous tile's TMA store must have read the staging tile
         if (tid == 0) bulk_wait_read0();
-        named_bar_sync(1, kSoftmaxThreads);
+        if (!rendezvous()) { ok = false; break; }
         store_pending = false;
       }
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -488,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();
       tc_fence_before();
-      named_bar_sync(1, kSoftmaxThreads);
+      if (!rendezvous()) { ok = false; break; }
       if (tid == 0) {
         const int c2 = t.b * p.H + t.g * p.HG;
         tma_store_3d(&map_out, obuf, 0, t.i0, c2);
