@@ -1,0 +1,867 @@
+// hca_bwd_tc.cu -- tensor-core (tcgen05 + TMEM + TMA) HCA backward, sm_103a.
+//
+// Gradient of the forward in hca_fwd_tc.cu (same visibility, K = V):
+//   P = exp(s - lse), dP = dO K^T, Delta = rowsum(dO * out), dS = P (dP - Delta)
+//   dq  = scale * dS K
+//   dkv = sum over heads and visible queries of (scale * dS^T q + P^T dO),
+// i.e. each shared row receives its key-role and its value-role gradient in
+// one accumulator ("[DeepSeek-V4] Implement Compressed Attention Layers",
+// einsum review suggestions: k and v are the same kv tensor).
+//
+// Three kernels on the caller's stream:
+//  1. dq kernel (query-major, the forward's tiles and key blocks).  Per tile
+//     it also forms Delta from the TMA-loaded dO tile and the stored out rows
+//     and writes (lse*log2e, Delta) in tile-row order for kernel 2.  Per key
+//     block: S = Q K^T and dP = dO K^T share the kv tile; the softmax warps
+//     form dS (bf16) straight into TMEM; dq += dS K reads dS from TMEM and the
+//     kv tile through an MN-major descriptor.
+//  2. dkv kernel (key-major).  A work item is one 128-key block (raw kv rows,
+//     or compressed entries with their query range split into kSplit chunks)
+//     and loops over the head-packed query tiles that can see it:
+//       S^T = K Q^T, dP^T = K dO^T  ->  P^T, dS^T (bf16, into TMEM)
+//       acc += P^T dO + (scale dS^T) Q      (one fp32 TMEM accumulator)
+//     Raw blocks write dkv directly; compressed blocks write fp32 partials.
+//     The dQ side needs no atomics: kernel 1 owns dq.  ("Add HCA Static
+//     Compilation for Splash Attention [Deepseek v4]" reduces dQ in an on-chip
+//     ring buffer on TPU; here dq stays in TMEM for a whole query tile.)
+//  3. reduce kernel: dckv = sum of the partials in a fixed order (deterministic).
+#include <cuda_bf16.h>
+
+#include "hca_common.cuh"
+#include "hca_internal.h"
+#include "tc_ptx.cuh"
+#include "tc_tiles.cuh"
+
+namespace hca {
+using namespace tc;
+
+namespace {
+
+constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = 192;
+constexpr int kSplit = 64;  // query chunks per compressed key block
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// kernel 1: dq
+// ---------------------------------------------------------------------------
+namespace dqk {
+constexpr int kStages = 3;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;  // dS: 64 cols of packed bf16
+constexpr int kTmemCols = 512;
+constexpr int kOffQ = 0, kOffDO = kTile, kOffKV = 2 * kTile;
+constexpr int kOffOut = kOffKV + kStages * kTile;
+constexpr int kSmemBytes = kOffOut + kTile + 1024;
+}  // namespace dqk
+
+struct DqParams {
+  QTiling qt;
+  int32_t *status;
+  const __nv_bfloat16 *out;  // forward output (for Delta)
+  const float *lse;
+  float2 *rowstat;           // [ntiles][128]: (lse * log2e, Delta) per tile row
+  __nv_bfloat16 *dq;         // direct stores for poisoned calls / tiles without keys
+  float sl2, scale;
+};
+
+struct DqBars {
+  uint64_t qd_full, qd_empty;
+  uint64_t kv_full[dqk::kStages], kv_empty[dqk::kStages];
+  uint64_t s_full, s_free;
+  uint64_t ds_full, dq_done;
+  uint64_t epi, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ long long tile_linear(const QTiling &q, const Tile &t) {
+  return ((long long)t.b * q.groups + t.g) * q.ntq + t.i0 / q.Pq;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    hca_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+                      const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_ckv,
+                      const __grid_constant__ CUtensorMap map_dq, const DqParams p) {
+  using namespace dqk;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ DqBars bars;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int *abort_flag = &bars.abort;
+  const QTiling &Q = p.qt;
+
+  if (tid == 0) {
+    mbar_init(&bars.qd_full, 1);
+    // released by the last S/dP MMA of a tile and by every softmax thread
+    // once it has read the staged dO tile (Delta)
+    mbar_init(&bars.qd_empty, 1 + kSoftmaxThreads);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
+    }
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.s_free, kSoftmaxThreads);
+    mbar_init(&bars.ds_full, kSoftmaxThreads);
+    mbar_init(&bars.dq_done, 1);
+    mbar_init(&bars.epi, kSoftmaxThreads);
+    mbar_init(&bars.drain, 1);
+    bars.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const bool poisoned = *(volatile const int32_t *)p.status != 0;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA
+    uint32_t gb = 0, tw = 0;
+    int last_par[kStages] = {-1, -1, -1};
+    int q_par = -1;
+    bool ok = !poisoned;
+    for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
+      Tile t;
+      tile_coords(Q, u, t);
+      tile_ranges_warp(Q, t, lane);
+      const int nb = t.nraw + t.ncomp;
+      if (nb == 0) continue;
+      if (lane == 0) {
+        if (tw > 0) ok = mbar_wait(&bars.qd_empty, (tw - 1) & 1, abort_flag, p.status);
+        if (ok) {
+          mbar_arrive_expect_tx(&bars.qd_full, 2 * kTile);
+          const int c2 = t.b * Q.H + t.g * Q.HG;
+          tma_load_3d(&map_q, &bars.qd_full, smem + kOffQ, 0, t.i0, c2);
+          tma_load_3d(&map_q, &bars.qd_full, smem + kOffQ + kHalfTile, 64, t.i0, c2);
+          tma_load_3d(&map_do, &bars.qd_full, smem + kOffDO, 0, t.i0, c2);
+          tma_load_3d(&map_do, &bars.qd_full, smem + kOffDO + kHalfTile, 64, t.i0, c2);
+          q_par = tw & 1;
+        }
+        for (int j = 0; ok && j < nb; ++j, ++gb) {
+          const int s = gb % kStages;
+          if (gb >= (uint32_t)kStages)
+            ok = mbar_wait(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status);
+          if (!ok) break;
+          bool comp;
+          int start, n;
+          block_of(t, j, comp, start, n);
+          const CUtensorMap *mp = comp ? &map_ckv : &map_kv;
+          uint8_t *dst = smem + kOffKV + s * kTile;
+          mbar_arrive_expect_tx(&bars.kv_full[s], kTile);
+          tma_load_3d(mp, &bars.kv_full[s], dst, 0, start, t.b);
+          tma_load_3d(mp, &bars.kv_full[s], dst + kHalfTile, 64, start, t.b);
+          last_par[s] = (gb / kStages) & 1;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      gb = __shfl_sync(0xffffffffu, gb, 0);
+      ++tw;
+    }
+    if (!ok && !poisoned && lane == 0) {
+      volatile int never = 0;
+      for (int s = 0; s < kStages; ++s)
+        if (last_par[s] >= 0) mbar_wait(&bars.kv_full[s], last_par[s], &never, p.status, 100000000ull);
+      if (q_par >= 0) mbar_wait(&bars.qd_full, q_par, &never, p.status, 100000000ull);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA
+    const uint32_t qa = smem_u32(smem + kOffQ), da = smem_u32(smem + kOffDO);
+    uint32_t gb = 0, tw = 0;
+    bool ok = !poisoned, issued = false;
+    for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
+      Tile t;
+      tile_coords(Q, u, t);
+      tile_ranges_warp(Q, t, lane);
+      const int nb = t.nraw + t.ncomp;
+      if (nb == 0) continue;
+      if (lane == 0) {
+        ok = mbar_wait(&bars.qd_full, tw & 1, abort_flag, p.status);
+        auto issue_sdp = [&](int j, uint32_t g) -> bool {
+          const int s = g % kStages;
+          if (!mbar_wait(&bars.kv_full[s], (g / kStages) & 1, abort_flag, p.status)) return false;
+          if (g > 0 && !mbar_wait(&bars.s_free, (g - 1) & 1, abort_flag, p.status)) return false;
+          tc_fence_after();
+          bool comp;
+          int start, n;
+          block_of(t, j, comp, start, n);
+          const int nk = (n + 15) & ~15;
+          const uint32_t idesc = idesc_bf16_f32(kRows, nk, false, false);
+          const uint32_t ka = smem_u32(smem + kOffKV + s * kTile);
+#pragma unroll
+          for (int k = 0; k < kHeadDim / 16; ++k) {
+            const uint32_t off = (k >> 2) * kHalfTile + (k & 3) * 32;
+            const uint64_t bk = smem_desc_sw128(ka + off, 16, 1024);
+            mma_ss(tmem + kColS, smem_desc_sw128(qa + off, 16, 1024), bk, idesc, k > 0);
+            mma_ss(tmem + kColDP, smem_desc_sw128(da + off, 16, 1024), bk, idesc, k > 0);
+          }
+          mma_commit(&bars.s_full);
+          issued = true;
+          return true;
+        };
+        if (ok) ok = issue_sdp(0, gb);
+        if (ok && nb == 1) mma_commit(&bars.qd_empty);
+        for (int j = 0; ok && j < nb; ++j) {
+          const uint32_t g = gb + j;
+          if (j + 1 < nb) {
+            ok = issue_sdp(j + 1, g + 1);
+            if (!ok) break;
+            if (j + 1 == nb - 1) mma_commit(&bars.qd_empty);
+          }
+          ok = mbar_wait(&bars.ds_full, g & 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          bool comp;
+          int start, n;
+          block_of(t, j, comp, start, n);
+          const int nk = (n + 15) & ~15;
+          const int s = g % kStages;
+          const uint32_t ka = smem_u32(smem + kOffKV + s * kTile);
+          const uint32_t idesc = idesc_bf16_f32(kRows, kHeadDim, false, true);
+          for (int kk = 0; kk < nk / 16; ++kk)
+            mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, smem_desc_sw128(ka + kk * 2048, kHalfTile, 1024), idesc,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars.kv_empty[s]);
+          mma_commit(&bars.dq_done);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      gb += nb;
+      ++tw;
+    }
+    if (!ok && issued && lane == 0) {
+      volatile int never = 0;
+      mma_commit(&bars.drain);
+      mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ dS + epilogue
+    const int r = tid;
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    uint8_t *obuf = smem + kOffOut;
+    const uint8_t *dobuf = smem + kOffDO;
+    uint32_t gb = 0, tw = 0, dq_waited = 0, epi_phase = 0;
+    bool ok = true, store_pending = false;
+    auto rendezvous = [&]() -> bool {
+      mbar_arrive(&bars.epi);
+      const bool rr = wait_warp(&bars.epi, epi_phase & 1, abort_flag, p.status);
+      ++epi_phase;
+      return rr;
+    };
+    // dq MMA number x (global) complete
+    auto wait_dq = [&](uint32_t x) -> bool {
+      while (dq_waited <= x) {
+        if (!wait_warp(&bars.dq_done, dq_waited & 1, abort_flag, p.status)) return false;
+        ++dq_waited;
+      }
+      return true;
+    };
+    for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
+      Tile t;
+      tile_coords(Q, u, t);
+      tile_ranges_warp(Q, t, lane);
+      const int nb = t.nraw + t.ncomp;
+      const int pq = r % Q.Pq, hh = r / Q.Pq;
+      const int head = t.g * Q.HG + hh;
+      const int i = t.i0 + pq;
+      const RowIv iv = row_interval(Q.sstart, t.b, Q.S, i, Q.W, Q.m);
+      const size_t lrow = ((size_t)t.b * Q.H + head) * Q.S + i;
+      float2 *rs = p.rowstat + tile_linear(Q, t) * kRows;
+      if (poisoned || nb == 0) {
+        if (i < Q.S) {
+          const __nv_bfloat16 bv = __float2bfloat16_rn(poisoned ? __int_as_float(0x7fc00000) : 0.f);
+          for (int d = 0; d < kHeadDim; ++d) p.dq[lrow * kHeadDim + d] = bv;
+        }
+        rs[r] = make_float2(0.f, 0.f);
+        continue;
+      }
+      // Delta = <dO, out> for this row (dO from the staged tile)
+      if (!wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status)) { ok = false; break; }
+      float lse2 = 0.f, delta = 0.f;
+      if (iv.valid) {
+        const uint4 *orow = reinterpret_cast<const uint4 *>(p.out + lrow * kHeadDim);
+#pragma unroll 4
+        for (int ch = 0; ch < 16; ++ch) {
+          const uint4 ov = orow[ch];
+          const uint4 gv = *reinterpret_cast<const uint4 *>(dobuf + sw128_offset(r, ch));
+          const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            delta = fmaf(__uint_as_float(oa[x] << 16), __uint_as_float(ga[x] << 16), delta);
+            delta = fmaf(__uint_as_float(oa[x] & 0xffff0000u), __uint_as_float(ga[x] & 0xffff0000u), delta);
+          }
+        }
+        lse2 = p.lse[lrow] * kLog2e;
+      }
+      rs[r] = make_float2(lse2, delta);
+      mbar_arrive(&bars.qd_empty);
+      for (int j = 0; j < nb; ++j, ++gb) {
+        bool comp;
+        int start, n;
+        block_of(t, j, comp, start, n);
+        const int nk = (n + 15) & ~15;
+        int lo_c = 0, hi_c = -1;
+        if (iv.valid) {
+          const int lo = comp ? iv.clo : iv.rlo, hi = comp ? iv.chi : iv.rhi;
+          lo_c = max(lo - start, 0);
+          hi_c = min(hi - start, n - 1);
+        }
+        if (!wait_warp(&bars.s_full, gb & 1, abort_flag, p.status)) { ok = false; break; }
+        // dS lives in TMEM: the previous dq MMA must have consumed it
+        if (gb >= 1 && !wait_dq(gb - 1)) { ok = false; break; }
+        tc_fence_after();
+        for (int c0 = 0; c0 < nk; c0 += 32) {
+          uint32_t sr[32], pr[32];
+          const bool full = c0 + 32 <= nk;
+          if (full) {
+            tmem_ld32(lane_addr + kColS + c0, sr);
+            tmem_ld32(lane_addr + kColDP + c0, pr);
+          } else {
+            uint32_t a16[16], b16[16];
+            tmem_ld16(lane_addr + kColS + c0, a16);
+            tmem_ld16(lane_addr + kColDP + c0, b16);
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              sr[x] = a16[x];
+              pr[x] = b16[x];
+            }
+          }
+          tmem_wait_ld();
+          uint32_t packed[16];
+#pragma unroll
+          for (int x = 0; x < 32; x += 2) {
+            float ds2[2];
+#pragma unroll
+            for (int y = 0; y < 2; ++y) {
+              const int c = c0 + x + y;
+              const bool vis = c >= lo_c && c <= hi_c;
+              const float pv = ex2_approx(__uint_as_float(sr[x + y]) * p.sl2 - lse2);
+              ds2[y] = vis ? pv * (__uint_as_float(pr[x + y]) - delta) : 0.f;
+            }
+            packed[x / 2] = pack_bf16x2(ds2[0], ds2[1]);
+          }
+          if (full) {
+            tmem_st16(lane_addr + kColDS + c0 / 2, packed);
+          } else {
+            uint32_t p8[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) p8[x] = packed[x];
+            // only 8 packed columns are meaningful for a 16-key tail
+            tmem_st16(lane_addr + kColDS + c0 / 2, p8);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars.s_free);
+        mbar_arrive(&bars.ds_full);
+      }
+      if (!ok) break;
+      // ---------------- epilogue: dq = scale * acc
+      if (!wait_dq(gb - 1)) { ok = false; break; }
+      tc_fence_after();
+      if (store_pending) {
+        if (tid == 0) bulk_wait_read0();
+        if (!rendezvous()) { ok = false; break; }
+        store_pending = false;
+      }
+      {
+        uint32_t o[32];
+#pragma unroll
+        for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+          tmem_ld32(lane_addr + kColDQ + c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[ch * 8 + 0]) * p.scale, __uint_as_float(o[ch * 8 + 1]) * p.scale);
+            v.y = pack_bf16x2(__uint_as_float(o[ch * 8 + 2]) * p.scale, __uint_as_float(o[ch * 8 + 3]) * p.scale);
+            v.z = pack_bf16x2(__uint_as_float(o[ch * 8 + 4]) * p.scale, __uint_as_float(o[ch * 8 + 5]) * p.scale);
+            v.w = pack_bf16x2(__uint_as_float(o[ch * 8 + 6]) * p.scale, __uint_as_float(o[ch * 8 + 7]) * p.scale);
+            *reinterpret_cast<uint4 *>(obuf + sw128_offset(r, c0 / 8 + ch)) = v;
+          }
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      if (!rendezvous()) { ok = false; break; }
+      if (tid == 0) {
+        const int c2 = t.b * Q.H + t.g * Q.HG;
+        tma_store_3d(&map_dq, obuf, 0, t.i0, c2);
+        tma_store_3d(&map_dq, obuf + kHalfTile, 64, t.i0, c2);
+        bulk_commit();
+      }
+      store_pending = true;
+      ++tw;
+    }
+    if (tid == 0) bulk_wait0();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// kernel 2: dkv / dckv partials
+// ---------------------------------------------------------------------------
+namespace dkk {
+constexpr int kStages = 2;
+constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256, kColP = 384, kColDS = 448;
+constexpr int kTmemCols = 512;
+// stage: Q tile | dO tile | rowstat (128 x float2) | intervals (128 x int2)
+constexpr int kStageBytes = 2 * kTile + 1024 + 1024;
+constexpr int kOffK = 0, kOffStage = kTile;
+constexpr int kSmemBytes = kOffStage + kStages * kStageBytes + 1024;
+}  // namespace dkk
+
+struct DkvParams {
+  QTiling qt;
+  int32_t *status;
+  const float2 *rowstat;
+  __nv_bfloat16 *dkv;
+  float *partial;  // [kSplit][B][Sc_pad][D] fp32
+  int nkb_raw, nkb_comp, Sc_pad;
+  long long nitems;
+  float sl2, scale;
+};
+
+struct Item {
+  int b, comp, k0, n;  // key block [k0, k0+n)
+  int split;
+  int tq_lo, tq_hi;    // query tiles [tq_lo, tq_hi) (each over all head groups)
+};
+
+// items: compressed blocks (all splits, most work first), then raw blocks
+__device__ __forceinline__ void item_of(const DkvParams &p, long long u, Item &it) {
+  const QTiling &Q = p.qt;
+  const long long ncomp_items = (long long)Q.B * p.nkb_comp * kSplit;
+  if (u < ncomp_items) {
+    const int kb = (int)(u / ((long long)Q.B * kSplit));
+    const int rem = (int)(u % ((long long)Q.B * kSplit));
+    it.b = rem / kSplit;
+    it.split = rem % kSplit;
+    it.comp = 1;
+    it.k0 = kb * kBlockKeys;
+    it.n = min(kBlockKeys, Q.Sc - it.k0);
+    const long long first = (long long)(it.k0 + 1) * Q.m - 1;  // first query that sees entry k0
+    const int lo = first >= Q.S ? Q.ntq : (int)(first / Q.Pq);
+    const int len = Q.ntq - lo;
+    it.tq_lo = lo + (int)((long long)len * it.split / kSplit);
+    it.tq_hi = lo + (int)((long long)len * (it.split + 1) / kSplit);
+  } else {
+    const long long v = u - ncomp_items;
+    it.b = (int)(v % Q.B);
+    const int kb = (int)(v / Q.B);
+    it.split = 0;
+    it.comp = 0;
+    it.k0 = kb * kBlockKeys;
+    it.n = min(kBlockKeys, Q.S - it.k0);
+    const long long last = min((long long)Q.S - 1, (long long)it.k0 + it.n - 1 + Q.W - 1);
+    it.tq_lo = it.k0 / Q.Pq;
+    it.tq_hi = (int)(last / Q.Pq) + 1;
+  }
+}
+
+struct DkvBars {
+  uint64_t k_full, k_empty;
+  uint64_t st_full[dkk::kStages], st_empty[dkk::kStages];
+  uint64_t s_full, s_free;
+  uint64_t p_full, acc_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    hca_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+                       const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_ckv,
+                       const DkvParams p) {
+  using namespace dkk;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ DkvBars bars;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int *abort_flag = &bars.abort;
+  const QTiling &Q = p.qt;
+
+  if (tid == 0) {
+    mbar_init(&bars.k_full, 1);
+    mbar_init(&bars.k_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars.st_full[s], 1);
+      mbar_init(&bars.st_empty[s], 1);
+    }
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.s_free, kSoftmaxThreads);
+    mbar_init(&bars.p_full, kSoftmaxThreads);
+    mbar_init(&bars.acc_done, 1);
+    mbar_init(&bars.drain, 1);
+    bars.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const bool poisoned = *(volatile const int32_t *)p.status != 0;
+  const int per_tile = Q.groups;  // query tiles per position tile (one per head group)
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA
+    uint32_t gq = 0, iw = 0;
+    int last_par[kStages] = {-1, -1};
+    int k_par = -1;
+    bool ok = !poisoned;
+    for (long long u = blockIdx.x; ok && u < p.nitems; u += gridDim.x) {
+      Item it;
+      item_of(p, u, it);
+      const int nq = (it.tq_hi - it.tq_lo) * per_tile;
+      if (nq <= 0) continue;
+      if (lane == 0) {
+        if (iw > 0) ok = mbar_wait(&bars.k_empty, (iw - 1) & 1, abort_flag, p.status);
+        if (ok) {
+          const CUtensorMap *mp = it.comp ? &map_ckv : &map_kv;
+          mbar_arrive_expect_tx(&bars.k_full, kTile);
+          tma_load_3d(mp, &bars.k_full, smem + kOffK, 0, it.k0, it.b);
+          tma_load_3d(mp, &bars.k_full, smem + kOffK + kHalfTile, 64, it.k0, it.b);
+          k_par = iw & 1;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      for (int x = 0; ok && x < nq; ++x, ++gq) {
+        const int tq = it.tq_lo + x / per_tile, g = x % per_tile;
+        const int s = gq % kStages;
+        uint8_t *st = smem + kOffStage + s * kStageBytes;
+        if (lane == 0 && gq >= (uint32_t)kStages)
+          ok = mbar_wait(&bars.st_empty[s], ((gq / kStages) - 1) & 1, abort_flag, p.status);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        // per-position key intervals of this query tile, for this key kind
+        int2 *ivs = reinterpret_cast<int2 *>(st + 2 * kTile + 1024);
+        for (int q = lane; q < Q.Pq; q += 32) {
+          RowIv iv = row_interval(Q.sstart, it.b, Q.S, tq * Q.Pq + q, Q.W, Q.m);
+          int lo = 1, hi = 0;
+          if (iv.valid) {
+            lo = it.comp ? iv.clo : iv.rlo;
+            hi = it.comp ? iv.chi : iv.rhi;
+          }
+          ivs[q] = make_int2(lo, hi);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const int c2 = it.b * Q.H + g * Q.HG;
+          const int i0 = tq * Q.Pq;
+          mbar_arrive_expect_tx(&bars.st_full[s], 2 * kTile + 1024);
+          tma_load_3d(&map_q, &bars.st_full[s], st, 0, i0, c2);
+          tma_load_3d(&map_q, &bars.st_full[s], st + kHalfTile, 64, i0, c2);
+          tma_load_3d(&map_do, &bars.st_full[s], st + kTile, 0, i0, c2);
+          tma_load_3d(&map_do, &bars.st_full[s], st + kTile + kHalfTile, 64, i0, c2);
+          const long long tl = ((long long)it.b * Q.groups + g) * Q.ntq + tq;
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                  smem_u32(st + 2 * kTile)),
+              "l"(reinterpret_cast<uint64_t>(p.rowstat + tl * kRows)), "r"(1024), "r"(smem_u32(&bars.st_full[s]))
+              : "memory");
+          last_par[s] = (gq / kStages) & 1;
+        }
+        __syncwarp();
+      }
+      ++iw;
+    }
+    if (!ok && !poisoned && lane == 0) {
+      volatile int never = 0;
+      for (int s = 0; s < kStages; ++s)
+        if (last_par[s] >= 0) mbar_wait(&bars.st_full[s], last_par[s], &never, p.status, 100000000ull);
+      if (k_par >= 0) mbar_wait(&bars.k_full, k_par, &never, p.status, 100000000ull);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA
+    const uint32_t ka = smem_u32(smem + kOffK);
+    uint32_t gq = 0, iw = 0;
+    bool ok = !poisoned, issued = false;
+    for (long long u = blockIdx.x; ok && u < p.nitems; u += gridDim.x) {
+      Item it;
+      item_of(p, u, it);
+      const int nq = (it.tq_hi - it.tq_lo) * per_tile;
+      if (nq <= 0) continue;
+      if (lane == 0) {
+        ok = mbar_wait(&bars.k_full, iw & 1, abort_flag, p.status);
+        const uint32_t id_s = idesc_bf16_f32(kRows, kRows, false, false);
+        const uint32_t id_acc = idesc_bf16_f32(kRows, kHeadDim, false, true);
+        auto issue_s = [&](uint32_t g) -> bool {
+          const int s = g % kStages;
+          if (!mbar_wait(&bars.st_full[s], (g / kStages) & 1, abort_flag, p.status)) return false;
+          if (g > 0 && !mbar_wait(&bars.s_free, (g - 1) & 1, abort_flag, p.status)) return false;
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + kOffStage + s * kStageBytes);
+#pragma unroll
+          for (int k = 0; k < kHeadDim / 16; ++k) {
+            const uint32_t off = (k >> 2) * kHalfTile + (k & 3) * 32;
+            const uint64_t ak = smem_desc_sw128(ka + off, 16, 1024);
+            mma_ss(tmem + kColS, ak, smem_desc_sw128(sa + off, 16, 1024), id_s, k > 0);
+            mma_ss(tmem + kColDP, ak, smem_desc_sw128(sa + kTile + off, 16, 1024), id_s, k > 0);
+          }
+          mma_commit(&bars.s_full);
+          issued = true;
+          return true;
+        };
+        if (ok) ok = issue_s(gq);
+        for (int x = 0; ok && x < nq; ++x) {
+          const uint32_t g = gq + x;
+          if (x + 1 < nq) {
+            ok = issue_s(g + 1);
+            if (!ok) break;
+          }
+          ok = mbar_wait(&bars.p_full, g & 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          const int s = g % kStages;
+          const uint32_t sa = smem_u32(smem + kOffStage + s * kStageBytes);
+          for (int kk = 0; kk < kRows / 16; ++kk) {
+            // acc += P^T dO  (dO tile as an MN-major B operand)
+            mma_ts(tmem + kColAcc, tmem + kColP + kk * 8, smem_desc_sw128(sa + kTile + kk * 2048, kHalfTile, 1024),
+                   id_acc, (x > 0 || kk > 0) ? 1u : 0u);
+            // acc += (scale dS)^T Q
+            mma_ts(tmem + kColAcc, tmem + kColDS + kk * 8, smem_desc_sw128(sa + kk * 2048, kHalfTile, 1024), id_acc,
+                   1u);
+          }
+          mma_commit(&bars.st_empty[s]);
+          mma_commit(&bars.acc_done);
+        }
+        if (ok) mma_commit(&bars.k_empty);
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      gq += nq;
+      ++iw;
+    }
+    if (!ok && issued && lane == 0) {
+      volatile int never = 0;
+      mma_commit(&bars.drain);
+      mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ P^T, dS^T + item epilogue
+    const int kr = tid;  // key row == TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    uint32_t gq = 0, acc_waited = 0;
+    bool ok = true;
+    auto wait_acc = [&](uint32_t x) -> bool {
+      while (acc_waited <= x) {
+        if (!wait_warp(&bars.acc_done, acc_waited & 1, abort_flag, p.status)) return false;
+        ++acc_waited;
+      }
+      return true;
+    };
+    for (long long u = blockIdx.x; ok && u < p.nitems; u += gridDim.x) {
+      Item it;
+      item_of(p, u, it);
+      const int nq = (it.tq_hi - it.tq_lo) * per_tile;
+      const int key = it.k0 + kr;
+      const bool key_ok = kr < it.n;
+      float *prow = it.comp ? p.partial + (((size_t)it.split * Q.B + it.b) * p.Sc_pad + key) * kHeadDim : nullptr;
+      __nv_bfloat16 *drow = it.comp ? nullptr : p.dkv + ((size_t)it.b * Q.S + key) * kHeadDim;
+      if (poisoned || nq <= 0) {
+        const float v = poisoned ? __int_as_float(0x7fc00000) : 0.f;
+        if (it.comp) {
+          for (int d = 0; d < kHeadDim; ++d) prow[d] = v;
+        } else if (key_ok) {
+          const __nv_bfloat16 bv = __float2bfloat16_rn(v);
+          for (int d = 0; d < kHeadDim; ++d) drow[d] = bv;
+        }
+        continue;
+      }
+      for (int x = 0; x < nq; ++x, ++gq) {
+        const int s = gq % kStages;
+        const uint8_t *st = smem + kOffStage + s * kStageBytes;
+        const float2 *rs = reinterpret_cast<const float2 *>(st + 2 * kTile);
+        const int2 *ivs = reinterpret_cast<const int2 *>(st + 2 * kTile + 1024);
+        if (!wait_warp(&bars.s_full, gq & 1, abort_flag, p.status)) { ok = false; break; }
+        // P^T / dS^T live in TMEM: the previous accumulation must be done
+        if (gq >= 1 && !wait_acc(gq - 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < kRows; c0 += 32) {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(lane_addr + kColS + c0, sr);
+          tmem_ld32(lane_addr + kColDP + c0, dr);
+          tmem_wait_ld();
+          uint32_t pp[16], dd[16];
+#pragma unroll
+          for (int xx = 0; xx < 32; xx += 2) {
+            float pv[2], dv[2];
+#pragma unroll
+            for (int y = 0; y < 2; ++y) {
+              const int c = c0 + xx + y;
+              const int2 iv = ivs[c % Q.Pq];
+              const float2 st2 = rs[c];
+              const bool vis = key_ok && key >= iv.x && key <= iv.y;
+              const float e = ex2_approx(__uint_as_float(sr[xx + y]) * p.sl2 - st2.x);
+              pv[y] = vis ? e : 0.f;
+              dv[y] = vis ? p.scale * e * (__uint_as_float(dr[xx + y]) - st2.y) : 0.f;
+            }
+            pp[xx / 2] = pack_bf16x2(pv[0], pv[1]);
+            dd[xx / 2] = pack_bf16x2(dv[0], dv[1]);
+          }
+          tmem_st16(lane_addr + kColP + c0 / 2, pp);
+          tmem_st16(lane_addr + kColDS + c0 / 2, dd);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars.s_free);
+        mbar_arrive(&bars.p_full);
+      }
+      if (!ok) break;
+      // ---------------- item epilogue: the accumulator row of this key
+      if (!wait_acc(gq - 1)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t o[32];
+#pragma unroll
+      for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+        tmem_ld32(lane_addr + kColAcc + c0, o);
+        tmem_wait_ld();
+        if (it.comp) {
+          float4 *dst = reinterpret_cast<float4 *>(prow + c0);
+#pragma unroll
+          for (int x = 0; x < 8; ++x)
+            dst[x] = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]), __uint_as_float(o[4 * x + 2]),
+                                 __uint_as_float(o[4 * x + 3]));
+        } else if (key_ok) {
+          uint4 *dst = reinterpret_cast<uint4 *>(drow + c0);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * x + 0]), __uint_as_float(o[8 * x + 1]));
+            v.y = pack_bf16x2(__uint_as_float(o[8 * x + 2]), __uint_as_float(o[8 * x + 3]));
+            v.z = pack_bf16x2(__uint_as_float(o[8 * x + 4]), __uint_as_float(o[8 * x + 5]));
+            v.w = pack_bf16x2(__uint_as_float(o[8 * x + 6]), __uint_as_float(o[8 * x + 7]));
+            dst[x] = v;
+          }
+        }
+      }
+      tc_fence_before();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// kernel 3: dckv = sum of the split partials (fixed order)
+// ---------------------------------------------------------------------------
+__global__ void hca_bwd_reduce_kernel(const float *__restrict__ partial, __nv_bfloat16 *__restrict__ dckv, int B,
+                                      int Sc, int Sc_pad) {
+  const long long n4 = (long long)B * Sc * (kHeadDim / 4);
+  const size_t split_stride = (size_t)B * Sc_pad * kHeadDim;
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < n4; v += (long long)gridDim.x * blockDim.x) {
+    const int d4 = (int)(v % (kHeadDim / 4));
+    const long long row = v / (kHeadDim / 4);
+    const int b = (int)(row / Sc), j = (int)(row % Sc);
+    const size_t off = ((size_t)b * Sc_pad + j) * kHeadDim + d4 * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < kSplit; ++s) {
+      const float4 x = *reinterpret_cast<const float4 *>(partial + s * split_stride + off);
+      acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+    }
+    uint2 o;
+    o.x = pack_bf16x2(acc.x, acc.y);
+    o.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2 *>(dckv + ((size_t)b * Sc + j) * kHeadDim + d4 * 4) = o;
+  }
+}
+
+size_t rowstat_bytes(const QTiling &q) { return align_up((size_t)q.ntiles * kRows * sizeof(float2)); }
+
+int sc_pad(int Sc) { return (Sc + kBlockKeys - 1) / kBlockKeys * kBlockKeys; }
+
+}  // namespace
+
+bool tc_bwd_supported(int H, int D, int dtype) { return tc_shape_ok(H, D, dtype); }
+
+size_t tc_bwd_scratch_bytes(int B, int H, int S, int D, int W, int m, int dtype) {
+  if (!tc_shape_ok(H, D, dtype)) return 0;
+  QTiling q = make_qtiling(nullptr, B, H, S, W, m);
+  return rowstat_bytes(q) + align_up((size_t)kSplit * B * sc_pad(q.Sc) * kHeadDim * sizeof(float));
+}
+
+cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
+  const QTiling q = make_qtiling(a.sstart, a.B, a.H, a.S, a.W, a.m);
+  const int Spad = sc_pad(q.Sc);
+  char *ws = static_cast<char *>(a.scratch);
+  float2 *rowstat = reinterpret_cast<float2 *>(ws);
+  float *partial = reinterpret_cast<float *>(ws + rowstat_bytes(q));
+  CUtensorMap mq, mdo, mkv, mckv, mdq;
+  if (!make_map_bf16(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mdo, a.dout, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mdq, a.dq, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mkv, a.kv, kHeadDim, a.S, a.B, kBlockKeys, 1) ||
+      !make_map_bf16(&mckv, a.ckv, kHeadDim, q.Sc, a.B, kBlockKeys, 1))
+    return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(hca_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         dqk::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(hca_bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dkk::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorNoDevice;
+  const float sl2 = a.scale * kLog2e;
+
+  DqParams dp;
+  dp.qt = q;
+  dp.status = a.status_rw;
+  dp.out = static_cast<const __nv_bfloat16 *>(a.out);
+  dp.lse = a.lse;
+  dp.rowstat = rowstat;
+  dp.dq = static_cast<__nv_bfloat16 *>(a.dq);
+  dp.sl2 = sl2;
+  dp.scale = a.scale;
+  const long long g1 = q.ntiles < sms ? q.ntiles : sms;
+  if (g1 == 0) return cudaSuccess;
+  hca_bwd_dq_kernel<<<(unsigned)g1, kThreads, dqk::kSmemBytes, st>>>(mq, mdo, mkv, mckv, mdq, dp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  DkvParams kp;
+  kp.qt = q;
+  kp.status = a.status_rw;
+  kp.rowstat = rowstat;
+  kp.dkv = static_cast<__nv_bfloat16 *>(a.dkv);
+  kp.partial = partial;
+  kp.nkb_raw = (a.S + kBlockKeys - 1) / kBlockKeys;
+  kp.nkb_comp = (q.Sc + kBlockKeys - 1) / kBlockKeys;
+  kp.Sc_pad = Spad;
+  kp.nitems = (long long)a.B * kp.nkb_comp * kSplit + (long long)a.B * kp.nkb_raw;
+  kp.sl2 = sl2;
+  kp.scale = a.scale;
+  const long long g2 = kp.nitems < sms ? kp.nitems : sms;
+  hca_bwd_dkv_kernel<<<(unsigned)g2, kThreads, dkk::kSmemBytes, st>>>(mq, mdo, mkv, mckv, kp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  const long long n4 = (long long)a.B * q.Sc * (kHeadDim / 4);
+  if (n4 > 0) {
+    int blocks = (int)((n4 + 255) / 256);
+    if (blocks > 4 * sms) blocks = 4 * sms;
+    hca_bwd_reduce_kernel<<<blocks, 256, 0, st>>>(partial, static_cast<__nv_bfloat16 *>(a.dckv), a.B, q.Sc, Spad);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace hca

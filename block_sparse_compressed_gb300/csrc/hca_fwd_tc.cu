@@ -30,23 +30,17 @@
 // HCA_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
 
-#include <mutex>
-
 #include "hca_common.cuh"
 #include "hca_internal.h"
 #include "tc_ptx.cuh"
+#include "tc_tiles.cuh"
 
 namespace hca {
 using namespace tc;
 
 namespace {
 
-constexpr int kRows = 128;          // MMA M
-constexpr int kHeadDim = 128;       // D handled by this kernel
-constexpr int kBlockKeys = 128;     // keys per block (MMA N of QK^T, K of PV)
 constexpr int kStages = 3;          // kv ring depth
-constexpr int kTile = 32768;        // bytes of a 128 x 128 bf16 tile
-constexpr int kHalfTile = 16384;    // one 64-column SW128 half
 constexpr int kSoftmaxThreads = 128;
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 256;      // S: cols [0,128), O: cols [128,256)
@@ -61,86 +55,12 @@ constexpr int kOffOut = kOffP + 2 * kTile;
 constexpr int kSmemBytes = kOffOut + kTile + 1024;
 
 struct FwdParams {
-  const int32_t *sstart;
+  QTiling qt;
   int32_t *status;
   float *lse;
-  __nv_bfloat16 *out;  // used only for poisoning / all-invalid tiles
-  int B, H, S, W, m, Sc;
-  int HG, Pq, groups, ntq;  // heads per tile, positions per tile, head groups, query tiles per (b, group)
-  long long ntiles;
-  float sl2;  // scale * log2(e)
+  __nv_bfloat16 *out;  // direct stores for poisoned calls / tiles without keys
+  float sl2;           // scale * log2(e)
 };
-
-struct Tile {
-  int b, g, i0;
-  int rlo, rhi, clo, chi;  // half-open unions
-  int nraw, ncomp;         // block counts
-};
-
-__device__ __forceinline__ void tile_coords(const FwdParams &p, long long u, Tile &t) {
-  // longest tiles first: the compressed range grows with the position
-  const long long per = (long long)p.B * p.groups;
-  const int tq = p.ntq - 1 - (int)(u / per);
-  const int rem = (int)(u % per);
-  t.b = rem / p.groups;
-  t.g = rem % p.groups;
-  t.i0 = tq * p.Pq;
-}
-
-// Warp-cooperative union of the row intervals of the tile's positions.
-__device__ __forceinline__ void tile_ranges_warp(const FwdParams &p, Tile &t, int lane) {
-  int rlo = 0x7fffffff, rhi = -1, clo = 0x7fffffff, chi = -1;
-  for (int q = lane; q < p.Pq; q += 32) {
-    RowIv iv = row_interval(p.sstart, t.b, p.S, t.i0 + q, p.W, p.m);
-    if (!iv.valid) continue;
-    rlo = min(rlo, iv.rlo);
-    rhi = max(rhi, iv.rhi);
-    if (iv.chi >= iv.clo) {
-      clo = min(clo, iv.clo);
-      chi = max(chi, iv.chi);
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    rlo = min(rlo, __shfl_xor_sync(0xffffffffu, rlo, off));
-    rhi = max(rhi, __shfl_xor_sync(0xffffffffu, rhi, off));
-    clo = min(clo, __shfl_xor_sync(0xffffffffu, clo, off));
-    chi = max(chi, __shfl_xor_sync(0xffffffffu, chi, off));
-  }
-  t.rlo = rhi < 0 ? 0 : rlo;
-  t.rhi = rhi < 0 ? 0 : rhi + 1;
-  t.clo = chi < 0 ? 0 : clo;
-  t.chi = chi < 0 ? 0 : chi + 1;
-  t.nraw = (t.rhi - t.rlo + kBlockKeys - 1) / kBlockKeys;
-  t.ncomp = (t.chi - t.clo + kBlockKeys - 1) / kBlockKeys;
-}
-
-// block j of a tile: raw blocks first, then compressed blocks
-__device__ __forceinline__ void block_of(const Tile &t, int j, bool &comp, int &start, int &n) {
-  if (j < t.nraw) {
-    comp = false;
-    start = t.rlo + j * kBlockKeys;
-    n = min(kBlockKeys, t.rhi - start);
-  } else {
-    comp = true;
-    start = t.clo + (j - t.nraw) * kBlockKeys;
-    n = min(kBlockKeys, t.chi - start);
-  }
-}
-
-__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk16) {
-  // byte offset of 16-byte chunk `chunk16` (0..15 across both halves) of a
-  // 128-row, 256-byte-per-row tile stored as two 128B-swizzled halves
-  const int half = chunk16 >> 3, c = chunk16 & 7;
-  return (uint32_t)(half * kHalfTile + row * 128 + ((c ^ (row & 7)) << 4));
-}
-
-// Bounded wait whose outcome is the same for the whole warp, so that a warp
-// never splits around the warp-collective tcgen05.ld / tcgen05.st.
-__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort, int32_t *status) {
-  const bool ok = mbar_wait(bar, parity, abort, status);
-  return __all_sync(0xffffffffu, ok);
-}
 
 struct Bars {
   uint64_t q_full, q_empty;
@@ -202,17 +122,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     int last_par[kStages] = {-1, -1, -1};
     int q_par = -1;
     bool ok = !poisoned;
-    for (long long u = blockIdx.x; ok && u < p.ntiles; u += gridDim.x) {
+    for (long long u = blockIdx.x; ok && u < p.qt.ntiles; u += gridDim.x) {
       Tile t;
-      tile_coords(p, u, t);
-      tile_ranges_warp(p, t, lane);
+      tile_coords(p.qt, u, t);
+      tile_ranges_warp(p.qt, t, lane);
       const int nb = t.nraw + t.ncomp;
       if (nb == 0) continue;
       if (lane == 0) {
         if (tiles_with_work > 0) ok = mbar_wait(&bars.q_empty, (tiles_with_work - 1) & 1, abort_flag, p.status);
         if (ok) {
           mbar_arrive_expect_tx(&bars.q_full, kTile);
-          const int c2 = t.b * p.H + t.g * p.HG;
+          const int c2 = t.b * p.qt.H + t.g * p.qt.HG;
           tma_load_3d(&map_q, &bars.q_full, smem + kOffQ, 0, t.i0, c2);
           tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + kHalfTile, 64, t.i0, c2);
           q_par = tiles_with_work & 1;
@@ -250,10 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t gb = 0, tiles_with_work = 0;
     bool ok = !poisoned;
     bool issued = false;
-    for (long long u = blockIdx.x; ok && u < p.ntiles; u += gridDim.x) {
+    for (long long u = blockIdx.x; ok && u < p.qt.ntiles; u += gridDim.x) {
       Tile t;
-      tile_coords(p, u, t);
-      tile_ranges_warp(p, t, lane);
+      tile_coords(p.qt, u, t);
+      tile_ranges_warp(p.qt, t, lane);
       const int nb = t.nraw + t.ncomp;
       if (nb == 0) continue;
       if (lane == 0) {
@@ -348,19 +268,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     };
-    for (long long u = blockIdx.x; ok && u < p.ntiles; u += gridDim.x) {
+    for (long long u = blockIdx.x; ok && u < p.qt.ntiles; u += gridDim.x) {
       Tile t;
-      tile_coords(p, u, t);
-      tile_ranges_warp(p, t, lane);
+      tile_coords(p.qt, u, t);
+      tile_ranges_warp(p.qt, t, lane);
       const int nb = t.nraw + t.ncomp;
-      const int pq = r % p.Pq, hh = r / p.Pq;
-      const int head = t.g * p.HG + hh;
+      const int pq = r % p.qt.Pq, hh = r / p.qt.Pq;
+      const int head = t.g * p.qt.HG + hh;
       const int i = t.i0 + pq;
-      const RowIv iv = row_interval(p.sstart, t.b, p.S, i, p.W, p.m);
-      const size_t lrow = ((size_t)t.b * p.H + head) * p.S + i;
+      const RowIv iv = row_interval(p.qt.sstart, t.b, p.qt.S, i, p.qt.W, p.qt.m);
+      const size_t lrow = ((size_t)t.b * p.qt.H + head) * p.qt.S + i;
       if (poisoned || nb == 0) {
         // whole tile without keys (padding) or poisoned call: direct stores
-        if (i < p.S) {
+        if (i < p.qt.S) {
           const float v = poisoned ? __int_as_float(0x7fc00000) : 0.f;
           __nv_bfloat16 *orow = p.out + lrow * kHeadDim;
           const __nv_bfloat16 bv = __float2bfloat16_rn(v);
@@ -496,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (i < p.S) {
+      if (i < p.qt.S) {
         float lv;
         if (l_run > 0.f) {
           float lg;
@@ -511,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       if (!rendezvous()) { ok = false; break; }
       if (tid == 0) {
-        const int c2 = t.b * p.H + t.g * p.HG;
+        const int c2 = t.b * p.qt.H + t.g * p.qt.HG;
         tma_store_3d(&map_out, obuf, 0, t.i0, c2);
         tma_store_3d(&map_out, obuf + kHalfTile, 64, t.i0, c2);
         bulk_commit();
@@ -529,77 +449,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ---------------------------------------------------------------------------
-// host side
-// ---------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
-
-// 3-D bf16 map {inner, mid, outer} with a {64, box1, box2} box, 128B swizzle
-bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t mid, uint64_t outer, uint32_t box1,
-              uint32_t box2) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {inner, mid, outer};
-  cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
-  cuuint32_t box[3] = {64, box1, box2};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
-}
-
-int heads_per_tile(int H) { return H >= kRows ? kRows : H; }
-
 }  // namespace
 
-bool tc_fwd_supported(int H, int D, int dtype) {
-  if (dtype != HCA_BF16 || D != kHeadDim || H < 1) return false;
-  if (H <= kRows) return (kRows % H) == 0;
-  return (H % kRows) == 0;
-}
+bool tc_fwd_supported(int H, int D, int dtype) { return tc_shape_ok(H, D, dtype); }
 
 int tc_query_tile_positions(int H) { return kRows / heads_per_tile(H); }
 
 cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st) {
-  const int HG = heads_per_tile(a.H);
-  const int Pq = kRows / HG;
-  const int Sc = (a.S + a.m - 1) / a.m;
-  CUtensorMap mq, mkv, mckv, mout;
-  if (!make_map(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, Pq, HG) ||
-      !make_map(&mout, a.out, kHeadDim, a.S, (uint64_t)a.B * a.H, Pq, HG) ||
-      !make_map(&mkv, a.kv, kHeadDim, a.S, a.B, kBlockKeys, 1) ||
-      !make_map(&mckv, a.ckv, kHeadDim, Sc, a.B, kBlockKeys, 1))
-    return cudaErrorInvalidValue;
   FwdParams p;
-  p.sstart = a.sstart;
+  p.qt = make_qtiling(a.sstart, a.B, a.H, a.S, a.W, a.m);
+  const QTiling &q = p.qt;
+  CUtensorMap mq, mkv, mckv, mout;
+  if (!make_map_bf16(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mout, a.out, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mkv, a.kv, kHeadDim, a.S, a.B, kBlockKeys, 1) ||
+      !make_map_bf16(&mckv, a.ckv, kHeadDim, q.Sc, a.B, kBlockKeys, 1))
+    return cudaErrorInvalidValue;
   p.status = a.status_rw;
   p.lse = a.lse;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
-  p.B = a.B; p.H = a.H; p.S = a.S; p.W = a.W; p.m = a.m; p.Sc = Sc;
-  p.HG = HG; p.Pq = Pq; p.groups = a.H / HG; p.ntq = (a.S + Pq - 1) / Pq;
-  p.ntiles = (long long)a.B * p.groups * p.ntq;
   p.sl2 = a.scale * 1.4426950408889634f;
   static bool attr_set = false;
   if (!attr_set) {
@@ -609,14 +477,10 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st) {
   }
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
-  const long long grid = p.ntiles < sms ? p.ntiles : sms;
+  const long long grid = q.ntiles < sms ? q.ntiles : sms;
   if (grid == 0) return cudaSuccess;
   hca_fwd_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mkv, mckv, mout, p);
   return cudaGetLastError();
 }
-
-bool tc_bwd_supported(int, int, int) { return false; }
-size_t tc_bwd_scratch_bytes(int, int, int, int, int, int, int) { return 0; }
-cudaError_t tc_bwd(const BwdArgs &, cudaStream_t) { return cudaErrorNotSupported; }
 
 }  // namespace hca

@@ -61,7 +61,7 @@ def test_edge_windows_bf16(W, m):
 
 @pytest.mark.parametrize("H", [1, 4, 16, 64, 128, 256])
 def test_heads_bf16(H):
-    run_case(1, H, 260, 128, 64, 32, torch.bfloat16, backward=H <= 64)
+    run_case(1, H, 260, 128, 64, 32, torch.bfloat16)
 
 
 @pytest.mark.parametrize("H,D", [(3, 128), (4, 64), (6, 32)])
@@ -76,7 +76,7 @@ def test_long_window_multiple_raw_blocks(B):
     rng = np.random.Generator(np.random.PCG64(B))
     S = 700
     seg = np.stack([I.random_layout(S, rng, allow_pad=True) for _ in range(B)])
-    run_case(B, 16, S, 128, 333, 64, torch.bfloat16, seg, backward=False)
+    run_case(B, 16, S, 128, 333, 64, torch.bfloat16, seg)
 
 
 def test_segments_off_boundary_and_short_docs_bf16():
@@ -102,6 +102,14 @@ def test_random_layouts_f32():
         S = int(rng.integers(20, 200))
         seg = np.stack([I.random_layout(S, rng)])
         run_case(1, 3, S, 64, int(rng.integers(1, 50)), int(rng.integers(1, 20)), torch.float32, seg, seed=k)
+
+
+def test_many_documents_bf16():
+    # more documents than compressed splits need; W > 128 and m < 128
+    lens = [40, 300, 129, 1, 700, 256, 77]
+    S = sum(lens)
+    seg = I.segments_from_lengths(lens, S)
+    run_case(1, 4, S, 128, 200, 32, torch.bfloat16, seg)
 
 
 def test_fwd_4096_two_documents():

@@ -69,11 +69,111 @@ def test_fwd_long_65536():
     check_fwd_sampled(I.LONG_S65536)
 
 
+def cheap_comp_ids(seg_row, S, m, max_queries=1500, count=6, seed=0):
+    """Compressed entries whose exact gradient needs few queries (entries
+    near the end of their document), plus entry ids spread over the row."""
+    Sc = -(-S // m)
+    seg_row = np.zeros(S, np.int32) if seg_row is None else seg_row
+    ends = np.empty(S, np.int64)
+    e = S - 1
+    for x in range(S - 1, -1, -1):
+        if x < S - 1 and seg_row[x] != seg_row[x + 1]:
+            e = x
+        ends[x] = e
+    cands = []
+    for j in range(Sc):
+        lo, hi = j * m, (j + 1) * m - 1
+        if hi >= S or seg_row[lo] < 0 or seg_row[lo] != seg_row[hi]:
+            continue
+        nq = ends[lo] - hi + 1
+        if nq <= max_queries:
+            cands.append(j)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if len(cands) > count:
+        cands = sorted(rng.choice(cands, size=count, replace=False).tolist())
+    return cands
+
+
+def check_bwd_sampled(w, seed=1234, n_raw=24):
+    q, kv, ckv, seg, dout = I.tensors(w, device=DEV, seed=seed)
+    out, lse = hca.hca_attn_fwd(q, kv, ckv, seg, w.W, w.m, w.scale, check=True)
+    dq, dkv, dckv = hca.hca_attn_bwd(q, kv, ckv, seg, out, lse, dout, w.W, w.m, w.scale, check=True)
+    torch.cuda.synchronize()
+    qc, kvc, ckvc, dc = q.cpu(), kv.cpu(), ckv.cpu(), dout.cpu()
+    segc = None if seg is None else seg.cpu()
+    seg_np = None if segc is None else segc.numpy()
+    Pq = hca.hca_query_tile_positions(w.H, w.D, w.dtype)
+    dq_c, dkv_c, dckv_c = to_np(dq), to_np(dkv), to_np(dckv)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    for b in range(w.B):
+        sb = None if segc is None else segc[b:b + 1]
+        srow = None if seg_np is None else seg_np[b]
+        args = (qc[b:b + 1], kvc[b:b + 1], ckvc[b:b + 1], sb)
+        # dq on sampled windows
+        for lo, hi in sample_windows(srow, w.S, Pq, n_random=8, seed=b)[:24]:
+            rdq, _, _ = oracle.bwd(*args, dc[b:b + 1], w.W, w.m, w.scale, rows=(lo, hi))
+            valid = np.ones(hi - lo, bool) if srow is None else srow[lo:hi] >= 0
+            got = dq_c[b][:, lo:hi]
+            assert_close(f"dq b{b} [{lo},{hi})", got[:, valid], rdq[0][:, lo:hi][:, valid], w.dtype)
+            assert np.all(got[:, ~valid] == 0)
+        # dkv rows: document starts, the row ends and random rows
+        n_valid = w.S if srow is None else int((srow >= 0).sum())
+        raw = [0, 1, n_valid - 1, max(0, n_valid - 2)]
+        if srow is not None:
+            raw += (np.flatnonzero(np.diff(srow) != 0) + 1)[:8].tolist()
+        raw += rng.integers(0, n_valid, size=n_raw).tolist()
+        raw = sorted(set(int(x) for x in raw if 0 <= x < n_valid))
+        comp = cheap_comp_ids(srow, w.S, w.m, seed=b)
+        draw, dcomp = oracle.bwd_keys(*args, dc[b:b + 1], w.W, w.m, w.scale, raw_ids=raw, comp_ids=comp)
+        assert_close(f"dkv b{b}", dkv_c[b][raw], draw, w.dtype)
+        if comp:
+            assert_close(f"dckv b{b}", dckv_c[b][comp], dcomp, w.dtype)
+        # any size: the gradients of all keys sum to the sum of dO over valid rows
+        valid = np.ones(w.S, bool) if srow is None else srow >= 0
+        total = dkv_c[b].sum(0) + dckv_c[b].sum(0)
+        expect = to_np(dout[b][:, torch.from_numpy(valid).to(DEV)].sum((0, 1)))
+        assert_close(f"sum identity b{b}", total, expect, w.dtype)
+
+
+def test_bwd_docs_16384():
+    check_bwd_sampled(I.DOCS_S16384)
+
+
+def test_bwd_unaligned_lengths():
+    check_bwd_sampled(I.UNALIGNED)
+
+
+def test_bwd_long_65536():
+    check_bwd_sampled(I.LONG_S65536)
+
+
+def test_bwd_long_131072():
+    check_bwd_sampled(I.LONG_S131072, n_raw=12)
+
+
+def test_backward_is_deterministic():
+    w = I.DOCS_S16384
+    q, kv, ckv, seg, dout = I.tensors(w, device=DEV)
+    out, lse = hca.hca_attn_fwd(q, kv, ckv, seg, w.W, w.m, w.scale)
+    a = hca.hca_attn_bwd(q, kv, ckv, seg, out, lse, dout, w.W, w.m, w.scale)
+    b = hca.hca_attn_bwd(q, kv, ckv, seg, out, lse, dout, w.W, w.m, w.scale)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    o2, l2 = hca.hca_attn_fwd(q, kv, ckv, seg, w.W, w.m, w.scale)
+    assert torch.equal(out, o2) and torch.equal(lse, l2)
+
+
 def test_fwd_489_alone():
     # S = 3*128 + 105: ragged against both the tile and m
     w = I.Workload("S489", 1, 64, 489, 128, 128, 128, torch.bfloat16)
-    q, kv, ckv, seg, _ = I.tensors(w, with_dout=False)
-    out, lse = hca.hca_attn_fwd(q.to(DEV), kv.to(DEV), ckv.to(DEV), None, w.W, w.m, w.scale, check=True)
+    q, kv, ckv, _, dout = I.tensors(w)
+    g = [x.to(DEV) for x in (q, kv, ckv, dout)]
+    out, lse = hca.hca_attn_fwd(g[0], g[1], g[2], None, w.W, w.m, w.scale, check=True)
     ro, rl = oracle.fwd(q, kv, ckv, None, w.W, w.m, w.scale)
     assert_close("out", out, ro, w.dtype)
     assert_close("lse", lse, rl, w.dtype)
+    dq, dkv, dckv = hca.hca_attn_bwd(g[0], g[1], g[2], None, out, lse, g[3], w.W, w.m, w.scale, check=True)
+    rdq, rdkv, rdckv = oracle.bwd(q, kv, ckv, None, dout, w.W, w.m, w.scale)
+    assert_close("dq", dq, rdq, w.dtype)
+    assert_close("dkv", dkv, rdkv, w.dtype)
+    assert_close("dckv", dckv, rdckv, w.dtype)
