@@ -1,0 +1,434 @@
+#!/usr/bin/env python3
+"""Benchmark: HCA attention forward + backward on GB300.
+
+One step = hca_attn_fwd + hca_attn_bwd on one batch of the headline
+workload (B=1, H=64, S=65536, D=128, W=128, m=128, one document, bf16,
+q/kv/ckv/dO ~ N(0,1)).  Throughput counts FLOPs over visible (query, key)
+pairs only: 4*D per pair and head for the forward, 10*D for the backward.
+
+Prints ONE JSON line (rank 0).  With torchrun (N > 1) every rank runs its own
+batch (weak scaling, no collective on the data path); timing is the max over
+ranks of the device-timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (the only other place this file runs the oracle
+is the cpu_baseline leg of the default arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "HCA attn fwd+bwd TFLOP/s (visible pairs) and % bf16 TC peak at S=65536"
+UNIT = "TFLOP/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+PROFILES = os.path.join(ROOT, "profiles")
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+# algorithmic GEMM FLOPs per visible (query, key) pair per head, per kernel
+# (D multiplies each): forward QK^T + PV; dq kernel S + dP + dQ; dkv kernel
+# S^T + dP^T + dK + dV.
+KERNEL_FLOP_PER_PAIR_D = {"hca_fwd_tc": 4, "hca_bwd_dq": 6, "hca_bwd_dkv": 8}
+KERNEL_SOURCES = {"hca_fwd_tc": "hca_fwd_tc.cu", "hca_bwd_dq": "hca_bwd_tc.cu", "hca_bwd_dkv": "hca_bwd_tc.cu"}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload():
+    from block_sparse_compressed_gb300 import inputs as I
+    return I.LONG_S65536
+
+
+def visible_pairs_closed_form(S, W, m):
+    """Per-head visible pairs of one unpadded document of length S."""
+    raw = S * (S + 1) // 2 if S <= W else W * S - W * (W - 1) // 2
+    q, r = divmod(S, m)
+    comp = m * q * (q - 1) // 2 + q * (r + 1)
+    return raw, comp
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxs.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs), "samples": len(sms),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# profiles: DRAM traffic of the dominant kernel from a committed ncu summary
+# ---------------------------------------------------------------------------
+def source_digest(kernel: str) -> str:
+    src = os.path.join(ROOT, "block_sparse_compressed_gb300", "csrc", KERNEL_SOURCES.get(kernel, ""))
+    try:
+        with open(src, "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return ""
+
+
+def profiled_traffic(kernel: str, work_key: str):
+    """traffic bytes per launch recorded for `kernel` on this workload, or
+    None when there is no summary or the kernel source changed since."""
+    if not os.path.isdir(PROFILES):
+        return None
+    digest = source_digest(kernel)
+    for name in sorted(os.listdir(PROFILES)):
+        if not name.startswith(kernel) or not name.endswith((".md", ".txt")):
+            continue
+        text = open(os.path.join(PROFILES, name)).read()
+        m_w = re.search(r"^workload:\s*(.+)$", text, re.M)
+        m_t = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+        m_h = re.search(r"^source_sha256_16:\s*([0-9a-f]+)", text, re.M)
+        if not (m_w and m_t and m_h) or m_w.group(1).strip() != work_key:
+            continue
+        if m_h.group(1) != digest:
+            return None
+        return float(m_t.group(1))
+    return None
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline (oracle) on a bounded sample
+# ---------------------------------------------------------------------------
+def cpu_baseline(w, q, kv, ckv, dout, target_s: float):
+    """Time the fp64 oracle forward+backward on the last R query positions of
+    the workload (the rows with the most keys), R sized to ~target_s."""
+    import oracle
+    S = w.S
+    qc, kvc, ckvc, dc = q.cpu(), kv.cpu(), ckv.cpu(), dout.cpu()
+
+    def pairs_in(lo, hi):
+        raw = sum(min(i + 1, w.W) for i in range(lo, hi))
+        comp = sum((i + 1) // w.m for i in range(lo, hi))
+        return (raw + comp) * w.H
+
+    def run(R):
+        lo = S - R
+        t0 = time.perf_counter()
+        oracle.fwd(qc, kvc, ckvc, None, w.W, w.m, w.scale, rows=(lo, S))
+        oracle.bwd(qc, kvc, ckvc, None, dc, w.W, w.m, w.scale, rows=(lo, S))
+        return time.perf_counter() - t0, pairs_in(lo, S)
+
+    R = 16
+    dt, pairs = run(R)
+    R = int(max(16, min(S, R * target_s / max(dt, 1e-3) * 0.9)))
+    dt, pairs = run(R)
+    flops = 14 * w.D * pairs
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd over query rows [{S - R},{S}) of the workload "
+                      f"({pairs} visible pair-heads, {dt:.1f} s)", "seconds": dt}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle as the reference implementation
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    from block_sparse_compressed_gb300 import inputs as I
+    w = workload()
+    q, kv, ckv, seg, dout = I.tensors(w, device="cpu")
+    import oracle
+    # each step: a bounded sample of the workload sized so the run stays short
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    probe = cpu_baseline(w, q, kv, ckv, dout, per_step)
+    R_rows = int(re.search(r"\[(\d+),", probe["sample"]).group(1))
+    lo = R_rows
+    times, pairs = [], None
+    for k in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.fwd(q, kv, ckv, None, w.W, w.m, w.scale, rows=(lo, w.S))
+        oracle.bwd(q, kv, ckv, None, dout, w.W, w.m, w.scale, rows=(lo, w.S))
+        dt = time.perf_counter() - t0
+        if k >= args.warmup:
+            times.append(dt)
+    raw = sum(min(i + 1, w.W) for i in range(lo, w.S))
+    comp = sum((i + 1) // w.m for i in range(lo, w.S))
+    pairs = (raw + comp) * w.H
+    total = sum(times)
+    value = 14 * w.D * pairs * len(times) / total / 1e12
+    cb = {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+          "sample": f"fp64 oracle fwd+bwd over query rows [{lo},{w.S}) per step"}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(w), "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "W": w.W, "m": w.m, "segments": "one",
+            "l2": "no flush: q/dO/out/dq are 1.07 GB each, far above the 129 MB L2",
+            "parallelism": "replicas (one independent batch per GPU)"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}), flush=True)
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    from block_sparse_compressed_gb300 import hca
+    from block_sparse_compressed_gb300 import inputs as I
+    w = workload()
+    hca.load()
+    q, kv, ckv, seg, dout = I.tensors(w, device=dev, seed=I.SEED + 100 * rank)
+    raw, comp = visible_pairs_closed_form(w.S, w.W, w.m)
+    pairs = (raw + comp) * w.H * w.B
+    gr, gc = hca.hca_visible_pairs(seg, w.B, w.S, w.W, w.m, device=dev)
+    assert int((gr + gc).sum().item()) * w.H == pairs, "visible-pair count mismatch"
+    flop_fwd, flop_bwd = 4 * w.D * pairs, 10 * w.D * pairs
+    out = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.S, dtype=torch.float32, device=dev)
+    dq, dkv, dckv = torch.empty_like(q), torch.empty_like(kv), torch.empty_like(ckv)
+    wsf = hca.workspace(w.B, w.H, w.S, w.D, w.W, w.m, w.dtype, False, dev)
+    wsb = hca.workspace(w.B, w.H, w.S, w.D, w.W, w.m, w.dtype, True, dev)
+
+    def step():
+        hca.hca_attn_fwd(q, kv, ckv, seg, w.W, w.m, w.scale, out=out, lse=lse, ws=wsf)
+        hca.hca_attn_bwd(q, kv, ckv, seg, out, lse, dout, w.W, w.m, w.scale, dq=dq, dkv=dkv, dckv=dckv, ws=wsb)
+
+    step()
+    if hca.hca_workspace_status(wsf) != 0 or hca.hca_workspace_status(wsb) != 0:
+        raise RuntimeError("device reported an error status")
+    for _ in range(max(0, args.warmup - 1)):
+        step()
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local) if rank == 0 else None
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    hca.hca_profile_enable(True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    prof = hca.hca_profile_read()
+    hca.hca_profile_enable(False)
+    barrier(dist)
+    ms_total = ev0.elapsed_time(ev1)
+    clk = clocks.stop() if clocks else None
+    ms_total = max_over_ranks(ms_total, dist, dev)
+    ms_step = ms_total / args.steps
+    value = (flop_fwd + flop_bwd) * world / (ms_step * 1e-3) / 1e12
+
+    # per-kernel share and the dominant kernel's roofline
+    launches = sum(n for n, _ in prof.values())
+    tot_ms = sum(ms for _, ms in prof.values()) or 1.0
+    kernels = {k: {"launches": n, "ms_total": round(ms, 4), "share": round(ms / tot_ms, 4)}
+               for k, (n, ms) in prof.items() if n}
+    dom = max((k for k in kernels if k in KERNEL_FLOP_PER_PAIR_D), key=lambda k: kernels[k]["ms_total"])
+    n_dom, ms_dom = prof[dom]
+    avg_ms = ms_dom / n_dom
+    alg_flops = KERNEL_FLOP_PER_PAIR_D[dom] * w.D * pairs
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved = alg_flops / (avg_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(dom, w.name),
+                "peak_source": f"{peak_src} bf16_tflops_sustained",
+                "algorithmic": f"{KERNEL_FLOP_PER_PAIR_D[dom]}*D FLOP per visible pair-head"}
+    per_phase = {}
+    fwd_ms = prof.get("hca_fwd_tc", (0, 0.0))[1] / args.steps
+    bwd_ms = sum(prof.get(k, (0, 0.0))[1] for k in ("hca_bwd_dq", "hca_bwd_dkv", "hca_bwd_reduce")) / args.steps
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    if fwd_ms > 0:
+        per_phase["fwd"] = {"ms": round(fwd_ms, 4), "tflops": round(flop_fwd / fwd_ms / 1e9, 2),
+                            "pct_bf16_peak": round(100 * flop_fwd / fwd_ms / 1e9 / burst, 2)}
+    if bwd_ms > 0:
+        per_phase["bwd"] = {"ms": round(bwd_ms, 4), "tflops": round(flop_bwd / bwd_ms / 1e9, 2),
+                            "pct_bf16_peak": round(100 * flop_bwd / bwd_ms / 1e9 / burst, 2)}
+
+    # end to end: host buffers in, results back to host, through the API
+    e2e = run_e2e(args, w, q, kv, ckv, dout, dev, dist, flop_fwd + flop_bwd, world)
+
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(w),
+            "pct_bf16_peak": round(100 * value / world / burst, 2), "peak_tflops": burst,
+            "phases": per_phase, "kernels": kernels, "gpu_launches": launches, "roofline": roofline,
+            "clocks": clk, "e2e": e2e}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, q, kv, ckv, dout, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, w, q, kv, ckv, dout, dev, dist, flops_step, world):
+    import torch
+    from block_sparse_compressed_gb300 import hca
+    hq, hkv, hckv, hdo = (x.cpu().pin_memory() for x in (q, kv, ckv, dout))
+    houts = [torch.empty(q.shape, dtype=q.dtype).pin_memory(), torch.empty(w.B, w.H, w.S).pin_memory(),
+             torch.empty(q.shape, dtype=q.dtype).pin_memory(), torch.empty(kv.shape, dtype=kv.dtype).pin_memory(),
+             torch.empty(ckv.shape, dtype=ckv.dtype).pin_memory()]
+    dq_, dkv_, dckv_ = torch.empty_like(q), torch.empty_like(kv), torch.empty_like(ckv)
+    gq, gkv, gckv, gdo = torch.empty_like(q), torch.empty_like(kv), torch.empty_like(ckv), torch.empty_like(dout)
+    out = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.S, dtype=torch.float32, device=dev)
+    wsf = hca.workspace(w.B, w.H, w.S, w.D, w.W, w.m, w.dtype, False, dev)
+    wsb = hca.workspace(w.B, w.H, w.S, w.D, w.W, w.m, w.dtype, True, dev)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hkv, hckv, hdo))
+    d2h = sum(x.numel() * x.element_size() for x in houts)
+
+    def step():
+        for g, h in ((gq, hq), (gkv, hkv), (gckv, hckv), (gdo, hdo)):
+            g.copy_(h, non_blocking=True)
+        hca.hca_attn_fwd(gq, gkv, gckv, None, w.W, w.m, w.scale, out=out, lse=lse, ws=wsf)
+        hca.hca_attn_bwd(gq, gkv, gckv, None, out, lse, gdo, w.W, w.m, w.scale, dq=dq_, dkv=dkv_, dckv=dckv_,
+                         ws=wsb)
+        for h, g in zip(houts, (out, lse, dq_, dkv_, dckv_)):
+            h.copy_(g, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    steps = max(3, args.steps // 4)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / steps
+    return {"value": round(flops_step * world / (ms * 1e-3) / 1e12, 3), "unit": UNIT, "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "path": "pinned host tensors -> hca_attn_fwd/hca_attn_bwd (C ABI) -> pinned host tensors"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

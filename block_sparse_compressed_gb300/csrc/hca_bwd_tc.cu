@@ -833,8 +833,12 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   dp.scale = a.scale;
   const long long g1 = q.ntiles < sms ? q.ntiles : sms;
   if (g1 == 0) return cudaSuccess;
-  hca_bwd_dq_kernel<<<(unsigned)g1, kThreads, dqk::kSmemBytes, st>>>(mq, mdo, mkv, mckv, mdq, dp);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  {
+    ProfScope prof(kKBwdDq, st);
+    hca_bwd_dq_kernel<<<(unsigned)g1, kThreads, dqk::kSmemBytes, st>>>(mq, mdo, mkv, mckv, mdq, dp);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
 
   DkvParams kp;
@@ -850,14 +854,18 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   kp.sl2 = sl2;
   kp.scale = a.scale;
   const long long g2 = kp.nitems < sms ? kp.nitems : sms;
-  hca_bwd_dkv_kernel<<<(unsigned)g2, kThreads, dkk::kSmemBytes, st>>>(mq, mdo, mkv, mckv, kp);
-  e = cudaGetLastError();
+  {
+    ProfScope prof(kKBwdDkv, st);
+    hca_bwd_dkv_kernel<<<(unsigned)g2, kThreads, dkk::kSmemBytes, st>>>(mq, mdo, mkv, mckv, kp);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
 
   const long long n4 = (long long)a.B * q.Sc * (kHeadDim / 4);
   if (n4 > 0) {
     int blocks = (int)((n4 + 255) / 256);
     if (blocks > 4 * sms) blocks = 4 * sms;
+    ProfScope prof(kKBwdReduce, st);
     hca_bwd_reduce_kernel<<<blocks, 256, 0, st>>>(partial, static_cast<__nv_bfloat16 *>(a.dckv), a.B, q.Sc, Spad);
     e = cudaGetLastError();
   }

@@ -479,6 +479,7 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st) {
   if (sms <= 0) return cudaErrorNoDevice;
   const long long grid = q.ntiles < sms ? q.ntiles : sms;
   if (grid == 0) return cudaSuccess;
+  ProfScope prof(kKFwdTc, st);
   hca_fwd_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mkv, mckv, mout, p);
   return cudaGetLastError();
 }

@@ -8,6 +8,26 @@
 
 namespace hca {
 
+// kernels the optional profiler distinguishes (hca_profile_read ids)
+enum KernelId {
+  kKPrep = 0, kKFwdTc, kKBwdDq, kKBwdDkv, kKBwdReduce, kKSimtFwd, kKSimtBwd, kKVisibility, kNumKernels
+};
+
+// Brackets the launches issued during its lifetime with CUDA events on `st`
+// when profiling is enabled (hca_profile_enable); otherwise does nothing.
+class ProfScope {
+ public:
+  ProfScope(int kernel, cudaStream_t st);
+  ~ProfScope();
+  ProfScope(const ProfScope &) = delete;
+  ProfScope &operator=(const ProfScope &) = delete;
+
+ private:
+  int kernel_;
+  cudaStream_t st_;
+  cudaEvent_t start_;
+};
+
 struct FwdArgs {
   const void *q, *kv, *ckv;
   const int32_t *sstart;  // NULL = one segment per row

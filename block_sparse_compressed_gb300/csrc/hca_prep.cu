@@ -105,6 +105,7 @@ cudaError_t launch_prep(const int32_t *seg, int B, int S, int32_t *sstart, int32
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), st);
   if (e != cudaSuccess) return e;
   if (seg == nullptr || B == 0 || S == 0) return cudaSuccess;
+  ProfScope prof(kKPrep, st);
   hca_prep_kernel<<<B, kPrepThreads, 0, st>>>(seg, S, sstart, status);
   return cudaGetLastError();
 }
@@ -116,6 +117,7 @@ cudaError_t launch_visible_pairs(const int32_t *sstart, int B, int S, int W, int
   if (e != cudaSuccess || B == 0 || S == 0) return e;
   int blocks = (S + 255) / 256;
   if (blocks > 1024) blocks = 1024;
+  ProfScope prof(kKVisibility, st);
   hca_visible_pairs_kernel<<<dim3(blocks, B), 256, 0, st>>>(sstart, S, W, m,
                                                             reinterpret_cast<unsigned long long *>(raw),
                                                             reinterpret_cast<unsigned long long *>(comp));
@@ -127,6 +129,7 @@ cudaError_t launch_tile_map(const int32_t *sstart, int B, int S, int W, int m, i
   const int nt = (S + Pq - 1) / Pq;
   int blocks = (nt + 127) / 128;
   if (blocks > 1024) blocks = 1024;
+  ProfScope prof(kKVisibility, st);
   hca_tile_map_kernel<<<dim3(blocks, B), 128, 0, st>>>(sstart, S, W, m, Pq, nt, map);
   return cudaGetLastError();
 }

@@ -250,6 +250,7 @@ template <typename T, int DPL>
 static cudaError_t fwd_t(const FwdArgs &a, cudaStream_t st) {
   const long long rows = (long long)a.B * a.H * a.S;
   if (rows == 0) return cudaSuccess;
+  ProfScope prof(kKSimtFwd, st);
   simt_fwd_kernel<T, DPL><<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(
       (const T *)a.q, (const T *)a.kv, (const T *)a.ckv, a.sstart, a.status, (T *)a.out, a.lse, a.B, a.H, a.S, a.D,
       a.W, a.m, a.scale);
@@ -261,6 +262,7 @@ static cudaError_t bwd_t(const BwdArgs &a, cudaStream_t st) {
   const long long rows = (long long)a.B * a.H * a.S;
   if (rows == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((rows + 3) / 4);
+  ProfScope prof(kKSimtBwd, st);
   simt_delta_kernel<T, DPL><<<grid, 128, 0, st>>>((const T *)a.out, (const T *)a.dout, a.delta, rows, a.D);
   simt_dq_kernel<T, DPL><<<grid, 128, 0, st>>>((const T *)a.q, (const T *)a.kv, (const T *)a.ckv, a.sstart, a.status,
                                                a.lse, a.delta, (const T *)a.dout, (T *)a.dq, a.B, a.H, a.S, a.D, a.W,

@@ -26,7 +26,8 @@ _lock = threading.Lock()
 _lib = None
 
 EXPORTS = ("hca_status_string", "hca_version", "hca_workspace_size", "hca_query_tile_positions", "hca_attn_fwd",
-           "hca_attn_bwd", "hca_visible_pairs", "hca_tile_map", "hca_workspace_status")
+           "hca_attn_bwd", "hca_visible_pairs", "hca_tile_map", "hca_workspace_status", "hca_profile_enable",
+           "hca_profile_read", "hca_num_kernels", "hca_kernel_name")
 
 
 class HCAError(RuntimeError):
@@ -63,6 +64,14 @@ def load(path: str = LIB_PATH):
             lib.hca_tile_map.restype = I
             lib.hca_workspace_status.argtypes = [P, P]
             lib.hca_workspace_status.restype = I
+            lib.hca_profile_enable.argtypes = [I]
+            lib.hca_profile_enable.restype = I
+            lib.hca_profile_read.argtypes = [I, ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_double)]
+            lib.hca_profile_read.restype = I
+            lib.hca_num_kernels.argtypes = []
+            lib.hca_num_kernels.restype = I
+            lib.hca_kernel_name.argtypes = [I]
+            lib.hca_kernel_name.restype = ctypes.c_char_p
             _lib = lib
     return _lib
 
@@ -218,3 +227,18 @@ def hca_tile_map(seg: Optional[torch.Tensor], B: int, S: int, W: int, m: int, Pq
     rc = lib.hca_tile_map(_ptr(seg), B, S, W, m, Pq, _ptr(out), _ptr(ws), ws.numel(), _stream(device))
     _check(rc, "hca_tile_map")
     return out
+
+
+def hca_profile_enable(on: bool = True) -> None:
+    _check(load().hca_profile_enable(int(on)), "hca_profile_enable")
+
+
+def hca_profile_read() -> dict:
+    """{kernel name: (launches, total_ms)} since the last enable (syncs)."""
+    lib = load()
+    res = {}
+    for k in range(lib.hca_num_kernels()):
+        n, ms = ctypes.c_longlong(0), ctypes.c_double(0.0)
+        _check(lib.hca_profile_read(k, ctypes.byref(n), ctypes.byref(ms)), "hca_profile_read")
+        res[lib.hca_kernel_name(k).decode()] = (int(n.value), float(ms.value))
+    return res

@@ -135,6 +135,17 @@ HCA_API int hca_tile_map(const int32_t *seg, int B, int S, int W, int m, int Pq,
  * the one entry point that blocks the host. */
 HCA_API int hca_workspace_status(const void *workspace, void *stream);
 
+/* Optional per-kernel timing.  hca_profile_enable(1) resets the counters and
+ * makes every later kernel launch of the library record a pair of CUDA events
+ * on its stream (0 stops recording).  hca_profile_read synchronises on the
+ * recorded events and returns, for kernel id `kernel` (0 <= kernel <
+ * hca_num_kernels()), the number of launches and their total device time in
+ * milliseconds since the last enable.  hca_kernel_name gives the id's name. */
+HCA_API int hca_profile_enable(int on);
+HCA_API int hca_profile_read(int kernel, long long *launches, double *total_ms);
+HCA_API int hca_num_kernels(void);
+HCA_API const char *hca_kernel_name(int kernel);
+
 #ifdef __cplusplus
 }
 #endif
