@@ -272,8 +272,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float2 *rs = p.rowstat + tile_linear(Q, t) * kRows;
       if (poisoned || nb == 0) {
         if (i < Q.S) {
-          const __nv_bfloat16 bv = __float2bfloat16_rn(poisoned ? __int_as_float(0x7fc00000) : 0.f);
-          for (int d = 0; d < kHeadDim; ++d) p.dq[lrow * kHeadDim + d] = bv;
+          const float v = poisoned ? __int_as_float(0x7fc00000) : 0.f;
+          const uint32_t w2 = pack_bf16x2(v, v);
+          uint4 *grow = reinterpret_cast<uint4 *>(p.dq + lrow * kHeadDim);
+#pragma unroll
+          for (int c = 0; c < kHeadDim / 8; ++c) grow[c] = make_uint4(w2, w2, w2, w2);
         }
         rs[r] = make_float2(0.f, 0.f);
         continue;
@@ -672,10 +675,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (poisoned || nq <= 0) {
         const float v = poisoned ? __int_as_float(0x7fc00000) : 0.f;
         if (it.comp) {
-          for (int d = 0; d < kHeadDim; ++d) prow[d] = v;
+          float4 *dst = reinterpret_cast<float4 *>(prow);
+#pragma unroll
+          for (int c = 0; c < kHeadDim / 4; ++c) dst[c] = make_float4(v, v, v, v);
         } else if (key_ok) {
-          const __nv_bfloat16 bv = __float2bfloat16_rn(v);
-          for (int d = 0; d < kHeadDim; ++d) drow[d] = bv;
+          const uint32_t w2 = pack_bf16x2(v, v);
+          uint4 *dst = reinterpret_cast<uint4 *>(drow);
+#pragma unroll
+          for (int c = 0; c < kHeadDim / 8; ++c) dst[c] = make_uint4(w2, w2, w2, w2);
         }
         continue;
       }

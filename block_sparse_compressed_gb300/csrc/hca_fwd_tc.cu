@@ -282,9 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // whole tile without keys (padding) or poisoned call: direct stores
         if (i < p.qt.S) {
           const float v = poisoned ? __int_as_float(0x7fc00000) : 0.f;
-          __nv_bfloat16 *orow = p.out + lrow * kHeadDim;
-          const __nv_bfloat16 bv = __float2bfloat16_rn(v);
-          for (int d = 0; d < kHeadDim; ++d) orow[d] = bv;
+          const uint32_t w2 = pack_bf16x2(v, v);
+          uint4 *orow = reinterpret_cast<uint4 *>(p.out + lrow * kHeadDim);
+#pragma unroll
+          for (int c = 0; c < kHeadDim / 8; ++c) orow[c] = make_uint4(w2, w2, w2, w2);
           p.lse[lrow] = poisoned ? v : -INFINITY;
         }
         continue;
