@@ -27,7 +27,7 @@ _lib = None
 
 EXPORTS = ("hca_status_string", "hca_version", "hca_workspace_size", "hca_query_tile_positions", "hca_attn_fwd",
            "hca_attn_bwd", "hca_visible_pairs", "hca_tile_map", "hca_workspace_status", "hca_profile_enable",
-           "hca_profile_read", "hca_num_kernels", "hca_kernel_name")
+           "hca_profile_read", "hca_num_kernels", "hca_kernel_name", "hca_attn_fwd_noalloc")
 
 
 class HCAError(RuntimeError):
@@ -72,6 +72,8 @@ def load(path: str = LIB_PATH):
             lib.hca_num_kernels.restype = I
             lib.hca_kernel_name.argtypes = [I]
             lib.hca_kernel_name.restype = ctypes.c_char_p
+            lib.hca_attn_fwd_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, I, P]
+            lib.hca_attn_fwd_noalloc.restype = I
             _lib = lib
     return _lib
 
@@ -242,3 +244,25 @@ def hca_profile_read() -> dict:
         _check(lib.hca_profile_read(k, ctypes.byref(n), ctypes.byref(ms)), "hca_profile_read")
         res[lib.hca_kernel_name(k).decode()] = (int(n.value), float(ms.value))
     return res
+
+
+NOALLOC_MAX_POSITIONS = 1 << 20
+
+
+def hca_attn_fwd_noalloc(q, kv, ckv, seg, W: int, m: int, scale: float, out=None, lse=None):
+    """Forward through the entry point that uses the library's built-in
+    scratch instead of a workspace (for callers that cannot allocate device
+    memory; B*S <= NOALLOC_MAX_POSITIONS).  Returns (out, lse)."""
+    lib = load()
+    if m < 1:
+        raise ValueError("m must be >= 1")
+    B, H, S, D, Sc = _shapes(q, kv, ckv, seg, m)
+    dt = _dtype_code(q)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(out, "out", q.shape, q.dtype, q.device)
+    _need(lse, "lse", (B, H, S), torch.float32, q.device)
+    rc = lib.hca_attn_fwd_noalloc(_ptr(q), _ptr(kv), _ptr(ckv), _ptr(seg), _ptr(out), _ptr(lse), B, H, S, D, W, m,
+                                  float(scale), dt, _stream(q.device))
+    _check(rc, "hca_attn_fwd_noalloc")
+    return out, lse

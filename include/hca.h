@@ -135,6 +135,24 @@ HCA_API int hca_tile_map(const int32_t *seg, int B, int S, int W, int m, int Pq,
  * the one entry point that blocks the host. */
 HCA_API int hca_workspace_status(const void *workspace, void *stream);
 
+/* Forward for callers that cannot allocate device memory.  The paper has no
+ * counterpart: this is a convenience of this library.  Plugin hooks of
+ * inference runtimes, real-time loops that cannot afford cudaMalloc's implicit
+ * synchronisation, and hosts without an allocator can call it with only their
+ * inputs and outputs; arguments, layouts, outputs and errors are those of
+ * hca_attn_fwd.  Its scratch is a fixed array inside the library (every GPU
+ * that loads the library keeps it until exit, about 4 MB), which caps B * S at
+ * HCA_NOALLOC_MAX_POSITIONS; larger problems return HCA_ERR_WORKSPACE before
+ * anything is enqueued.  The first call on a device looks the array up (make
+ * it before any stream capture).  All calls share the array: calls that
+ * overlap on the GPU race and must be serialised by the caller.  A segment
+ * ordering error poisons that call's outputs with NaN (there is no workspace
+ * to read a status from).  Nothing is allocated or freed. */
+#define HCA_NOALLOC_MAX_POSITIONS (1 << 20)
+HCA_API int hca_attn_fwd_noalloc(const void *q, const void *kv, const void *ckv, const int32_t *seg,
+                                 void *out, float *lse,
+                                 int B, int H, int S, int D, int W, int m, float scale, int dtype, void *stream);
+
 /* Optional per-kernel timing.  hca_profile_enable(1) resets the counters and
  * makes every later kernel launch of the library record a pair of CUDA events
  * on its stream (0 stops recording).  hca_profile_read synchronises on the
