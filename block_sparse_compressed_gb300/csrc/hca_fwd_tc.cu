@@ -1,4 +1,4 @@
-// hca_tc.cu -- tensor-core (tcgen05 + TMEM + TMA) HCA forward for sm_103a.
+// hca_fwd_tc.cu -- tensor-core (tcgen05 + TMEM + TMA) HCA forward for sm_103a.
 //
 // Operation ("Add HCA Static Compilation for Splash Attention [Deepseek v4]",
 // Description: sliding window + completed compression windows, MQA dispatch
@@ -6,26 +6,36 @@
 // Layers", einsum review suggestions: k = v = kv broadcast over heads).
 //
 // Tiling.  All heads of a query position share every key row (one kv head),
-// so a tile packs Pq consecutive positions x HG heads into the M = 128 rows
-// of the MMA (row r = head*Pq + p), loaded by one 3-D TMA box {64, Pq, HG}
-// per 64-column half of q.  For every tile the key ranges of the union of its
-// rows' intervals (hca_common.cuh) are cut into blocks of <= 128 keys: raw kv
-// blocks first, then compressed ckv blocks.  Keys outside those ranges are
-// never loaded and no mask exists in memory; inside a block each row masks by
-// its own interval.
+// so a query tile packs Pq consecutive positions x HG heads into the M = 128
+// rows of the MMA (row r = head*Pq + p), loaded by one 3-D TMA box
+// {64, Pq, HG} per 64-column half of q.  A CTA works on a *pair* of adjacent
+// query tiles (A and B) that share one stream of key blocks: the union of the
+// 2*Pq positions' intervals (hca_common.cuh) cut into blocks of <= 128 keys,
+// raw kv blocks first, then compressed ckv blocks.  Keys outside those ranges
+// are never loaded and no mask exists in memory; inside a block every row
+// masks by its own interval.
 //
-// Per key block: S = Q K^T (tcgen05, fp32 in TMEM) -> softmax warps load S,
-// mask, online softmax in fp32 with exp2 (the running max is only raised when
-// a block's max exceeds it by more than 2^8, so O in TMEM is rarely rescaled)
-// -> P (bf16) in shared memory -> O += P V with V = the same shared-memory
-// kv tile read through an MN-major descriptor (K = V: one load serves both).
-// Epilogue: out = O / l through a 128B-swizzled staging tile and a TMA store;
-// lse = ln-domain logsumexp.
+// Per key block j and tile X in {A, B}:
+//   S_X = Q_X K^T            tcgen05 SS, fp32 accumulator in TMEM
+//   softmax warpgroup X      loads S_X, masks, online softmax in fp32 with
+//                            exp2 (the running max is raised only when a
+//                            block beats it by more than 2^8, so O_X is
+//                            rarely rescaled), writes P_X (bf16) back into
+//                            the first half of S_X's TMEM columns
+//   O_X += P_X V             tcgen05 TS: A = P_X from TMEM, B = the same kv
+//                            tile through an MN-major descriptor (K = V)
+// The MMA warp interleaves S_A, S_B, PV_A, PV_B so that each softmax
+// warpgroup works while the tensor core runs the other tile's GEMMs.  The
+// tensor pipe executes one thread's MMAs in order, so the commit of S_X(j+1)
+// also means PV_X(j) is done: that is what lets P alias S and lets the
+// softmax rescale O_X right after S_X(j+1) arrives.
 //
-// Warp roles (192 threads, persistent CTAs):
-//   warps 0-3  softmax + epilogue, thread r owns row r (TMEM lane r)
-//   warp 4     TMA producer (Q once per tile, kv/ckv blocks into a 3-stage ring)
-//   warp 5     MMA issuer (one elected lane)
+// Warp roles (512 threads, persistent CTAs; registers rebalanced with
+// setmaxnreg to 168 / 168 / 96 / 80 per thread):
+//   warpgroup 0   softmax of tile A (thread r owns row r = TMEM lane r)
+//   warpgroup 1   softmax of tile B
+//   warpgroup 2   epilogue: O_X * (1/l) -> bf16 -> swizzled smem -> TMA store
+//   warpgroup 3   warp 12 TMA producer, warp 13 MMA issuer, warps 14-15 idle
 // Every wait is bounded (tc_ptx.cuh): on a timeout the CTA records
 // HCA_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -40,39 +50,84 @@ using namespace tc;
 
 namespace {
 
-constexpr int kStages = 3;          // kv ring depth
-constexpr int kSoftmaxThreads = 128;
-constexpr int kThreads = 192;
-constexpr int kTmemCols = 256;      // S: cols [0,128), O: cols [128,256)
-constexpr uint32_t kColS = 0, kColO = 128;
+constexpr int kStages = 3;        // kv ring depth
+constexpr int kWG = 128;          // threads per warpgroup
+constexpr int kThreads = 4 * kWG;
+constexpr int kTmemCols = 512;    // S_A | S_B | O_A | O_B, 128 columns each
+__host__ __device__ constexpr uint32_t col_s(int x) { return (uint32_t)x * 128u; }        // S_X (P_X aliases it)
+__host__ __device__ constexpr uint32_t col_o(int x) { return 256u + (uint32_t)x * 128u; }  // O_X
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kRegSoftmax = 168, kRegEpilogue = 96, kRegProducer = 80;
+static_assert(2 * kRegSoftmax + kRegEpilogue + kRegProducer == 512, "register split must fit the launch");
 
-// dynamic shared memory: Q | kv ring | P x2 | out staging  (+1 KB alignment)
+// dynamic shared memory: Q_A | Q_B | kv ring | out staging A | B (+1 KB align)
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kTile;
-constexpr int kOffP = kOffKV + kStages * kTile;
-constexpr int kOffOut = kOffP + 2 * kTile;
-constexpr int kSmemBytes = kOffOut + kTile + 1024;
+constexpr int kOffKV = 2 * kTile;
+constexpr int kOffOut = kOffKV + kStages * kTile;
+constexpr int kSmemBytes = kOffOut + 2 * kTile + 1024;
 
 struct FwdParams {
-  QTiling qt;
+  QTiling qt;          // per query tile (Pq positions)
+  long long npairs;    // pair tiles over (b, head group, pair index)
+  int ntp;             // pairs per (b, group)
   int32_t *status;
   float *lse;
-  __nv_bfloat16 *out;  // direct stores for poisoned calls / tiles without keys
+  __nv_bfloat16 *out;  // direct stores for poisoned calls / pairs without keys
   float sl2;           // scale * log2(e)
 };
+
+struct Pair {
+  int b, g, i0;           // tile A starts at i0, tile B at i0 + Pq
+  int rlo, rhi, clo, chi; // union of both tiles' key ranges (half-open)
+  int nraw, ncomp;
+};
+
+__device__ __forceinline__ void pair_coords(const FwdParams &p, long long u, Pair &t) {
+  // longest pairs first: the compressed range grows with the position
+  const long long per = (long long)p.qt.B * p.qt.groups;
+  const int tp = p.ntp - 1 - (int)(u / per);
+  const int rem = (int)(u % per);
+  t.b = rem / p.qt.groups;
+  t.g = rem % p.qt.groups;
+  t.i0 = tp * 2 * p.qt.Pq;
+}
+
+__device__ __forceinline__ void pair_ranges_warp(const FwdParams &p, Pair &t, int lane) {
+  Tile tt;
+  tt.b = t.b;
+  tt.g = t.g;
+  tt.i0 = t.i0;
+  QTiling q2 = p.qt;
+  q2.Pq = 2 * p.qt.Pq;
+  tile_ranges_warp(q2, tt, lane);
+  t.rlo = tt.rlo; t.rhi = tt.rhi; t.clo = tt.clo; t.chi = tt.chi;
+  t.nraw = tt.nraw; t.ncomp = tt.ncomp;
+}
+
+__device__ __forceinline__ void pair_block(const Pair &t, int j, bool &comp, int &start, int &n) {
+  Tile tt;
+  tt.rlo = t.rlo; tt.rhi = t.rhi; tt.clo = t.clo; tt.chi = t.chi;
+  tt.nraw = t.nraw; tt.ncomp = t.ncomp;
+  block_of(tt, j, comp, start, n);
+}
+
+__device__ __forceinline__ void setmaxnreg_inc_softmax() { asm volatile("setmaxnreg.inc.sync.aligned.u32 168;"); }
+__device__ __forceinline__ void setmaxnreg_dec_epilogue() { asm volatile("setmaxnreg.dec.sync.aligned.u32 96;"); }
+__device__ __forceinline__ void setmaxnreg_dec_producer() { asm volatile("setmaxnreg.dec.sync.aligned.u32 80;"); }
 
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full, s_free;
-  uint64_t p_full[2], o_done[2];
-  uint64_t epi;  // softmax-warp rendezvous before the output store
-  uint64_t drain;
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_final[2], o_free[2];
+  uint64_t st_full[2], st_free[2];
+  uint64_t epi, drain;
+  float inv_l[2][kRows];
   uint32_t tmem_base;
   int abort;
 };
 
+template <bool kPosScale>
 __global__ void __launch_bounds__(kThreads, 1)
     hca_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
                       const __grid_constant__ CUtensorMap map_ckv, const __grid_constant__ CUtensorMap map_out,
@@ -81,7 +136,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Bars bars;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wg = warp >> 2;
   volatile int *abort_flag = &bars.abort;
+  const QTiling &Q = p.qt;
 
   if (tid == 0) {
     mbar_init(&bars.q_full, 1);
@@ -90,18 +147,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.kv_full[s], 1);
       mbar_init(&bars.kv_empty[s], 1);
     }
-    mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.s_free, kSoftmaxThreads);
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(&bars.p_full[k], kSoftmaxThreads);
-      mbar_init(&bars.o_done[k], 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars.s_full[x], 1);
+      mbar_init(&bars.p_full[x], kWG);
+      mbar_init(&bars.o_final[x], 1);
+      mbar_init(&bars.o_free[x], kWG);
+      mbar_init(&bars.st_full[x], kWG);
+      mbar_init(&bars.st_free[x], kWG);
     }
-    mbar_init(&bars.epi, kSoftmaxThreads);
+    mbar_init(&bars.epi, kWG);
     mbar_init(&bars.drain, 1);
     bars.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
+  if (warp == 8) {
     tmem_alloc(&bars.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -111,301 +170,191 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   const bool poisoned = *(volatile const int32_t *)p.status != 0;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ TMA
-    if (!poisoned && lane == 0) {
-      tma_prefetch_map(&map_q);
-      tma_prefetch_map(&map_kv);
-      tma_prefetch_map(&map_ckv);
-    }
-    uint32_t gb = 0, tiles_with_work = 0;
-    int last_par[kStages] = {-1, -1, -1};
-    int q_par = -1;
-    bool ok = !poisoned;
-    for (long long u = blockIdx.x; ok && u < p.qt.ntiles; u += gridDim.x) {
-      Tile t;
-      tile_coords(p.qt, u, t);
-      tile_ranges_warp(p.qt, t, lane);
-      const int nb = t.nraw + t.ncomp;
-      if (nb == 0) continue;
-      if (lane == 0) {
-        if (tiles_with_work > 0) ok = mbar_wait(&bars.q_empty, (tiles_with_work - 1) & 1, abort_flag, p.status);
-        if (ok) {
-          mbar_arrive_expect_tx(&bars.q_full, kTile);
-          const int c2 = t.b * p.qt.H + t.g * p.qt.HG;
-          tma_load_3d(&map_q, &bars.q_full, smem + kOffQ, 0, t.i0, c2);
-          tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + kHalfTile, 64, t.i0, c2);
-          q_par = tiles_with_work & 1;
-        }
-        for (int j = 0; ok && j < nb; ++j, ++gb) {
-          const int s = gb % kStages;
-          if (gb >= (uint32_t)kStages) ok = mbar_wait(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status);
-          if (!ok) break;
-          bool comp;
-          int start, n;
-          block_of(t, j, comp, start, n);
-          const CUtensorMap *mp = comp ? &map_ckv : &map_kv;
-          uint8_t *dst = smem + kOffKV + s * kTile;
-          mbar_arrive_expect_tx(&bars.kv_full[s], kTile);
-          tma_load_3d(mp, &bars.kv_full[s], dst, 0, start, t.b);
-          tma_load_3d(mp, &bars.kv_full[s], dst + kHalfTile, 64, start, t.b);
-          last_par[s] = (gb / kStages) & 1;
-        }
+  if (wg == 3) {
+    setmaxnreg_dec_producer();
+    if (warp == 12) {
+      // ---------------------------------------------------------- TMA
+      if (!poisoned && lane == 0) {
+        tma_prefetch_map(&map_q);
+        tma_prefetch_map(&map_kv);
+        tma_prefetch_map(&map_ckv);
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      gb = __shfl_sync(0xffffffffu, gb, 0);
-      ++tiles_with_work;
-    }
-    if (!ok && !poisoned && lane == 0) {
-      // drain own copies before leaving (bounded, ignores the abort flag)
-      volatile int never = 0;
-      for (int s = 0; s < kStages; ++s)
-        if (last_par[s] >= 0) mbar_wait(&bars.kv_full[s], last_par[s], &never, p.status, 100000000ull);
-      if (q_par >= 0) mbar_wait(&bars.q_full, q_par, &never, p.status, 100000000ull);
-    }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA
-    const uint32_t qa = smem_u32(smem + kOffQ);
-    const uint32_t pa0 = smem_u32(smem + kOffP);
-    uint32_t gb = 0, tiles_with_work = 0;
-    bool ok = !poisoned;
-    bool issued = false;
-    for (long long u = blockIdx.x; ok && u < p.qt.ntiles; u += gridDim.x) {
-      Tile t;
-      tile_coords(p.qt, u, t);
-      tile_ranges_warp(p.qt, t, lane);
-      const int nb = t.nraw + t.ncomp;
-      if (nb == 0) continue;
-      if (lane == 0) {
-        ok = mbar_wait(&bars.q_full, tiles_with_work & 1, abort_flag, p.status);
-        // S(j) for the first block, then S(j+1) ahead of PV(j)
-        auto issue_s = [&](int j, uint32_t g) -> bool {
-          const int s = g % kStages;
-          if (!mbar_wait(&bars.kv_full[s], (g / kStages) & 1, abort_flag, p.status)) return false;
-          if (g > 0 && !mbar_wait(&bars.s_free, (g - 1) & 1, abort_flag, p.status)) return false;
-          tc_fence_after();
-          bool comp;
-          int start, n;
-          block_of(t, j, comp, start, n);
-          const int nk = (n + 15) & ~15;
-          const uint32_t idesc = idesc_bf16_f32(kRows, nk, false, false);
-          const uint32_t ka = smem_u32(smem + kOffKV + s * kTile);
-#pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k) {
-            const uint32_t off = (k >> 2) * kHalfTile + (k & 3) * 32;
-            mma_ss(tmem + kColS, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), idesc,
-                   k > 0);
+      uint32_t gb = 0, gq = 0;
+      uint32_t issued = 0;  // bit s: stage s loaded at least once; bit 8+s: parity of its last load
+      int q_par = -1;
+      bool ok = !poisoned;
+      for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
+        Pair t;
+        pair_coords(p, u, t);
+        pair_ranges_warp(p, t, lane);
+        const int nb = t.nraw + t.ncomp;
+        if (nb == 0) continue;
+        if (lane == 0) {
+          if (gq > 0) ok = mbar_wait(&bars.q_empty, (gq - 1) & 1, abort_flag, p.status);
+          if (ok) {
+            const bool has_b = t.i0 + Q.Pq < Q.S;
+            mbar_arrive_expect_tx(&bars.q_full, has_b ? 2 * kTile : kTile);
+            const int c2 = t.b * Q.H + t.g * Q.HG;
+            tma_load_3d(&map_q, &bars.q_full, smem + kOffQ, 0, t.i0, c2);
+            tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + kHalfTile, 64, t.i0, c2);
+            if (has_b) {
+              tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + kTile, 0, t.i0 + Q.Pq, c2);
+              tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + kTile + kHalfTile, 64, t.i0 + Q.Pq, c2);
+            }
+            q_par = gq & 1;
           }
-          mma_commit(&bars.s_full);
-          issued = true;
-          return true;
-        };
-        if (ok) ok = issue_s(0, gb);
-        if (ok && nb == 1) mma_commit(&bars.q_empty);
-        for (int j = 0; ok && j < nb; ++j) {
-          const uint32_t g = gb + j;
-          if (j + 1 < nb) {
-            ok = issue_s(j + 1, g + 1);
+          for (int j = 0; ok && j < nb; ++j, ++gb) {
+            const int s = gb % kStages;
+            if (gb >= (uint32_t)kStages)
+              ok = mbar_wait(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status);
             if (!ok) break;
-            if (j + 1 == nb - 1) mma_commit(&bars.q_empty);
+            bool comp;
+            int start, n;
+            pair_block(t, j, comp, start, n);
+            const CUtensorMap *mp = comp ? &map_ckv : &map_kv;
+            uint8_t *dst = smem + kOffKV + s * kTile;
+            mbar_arrive_expect_tx(&bars.kv_full[s], kTile);
+            tma_load_3d(mp, &bars.kv_full[s], dst, 0, start, t.b);
+            tma_load_3d(mp, &bars.kv_full[s], dst + kHalfTile, 64, start, t.b);
+            issued = (issued | (1u << s)) & ~(1u << (8 + s));
+            issued |= ((gb / kStages) & 1u) << (8 + s);
           }
-          const int pb = g & 1;
-          ok = mbar_wait(&bars.p_full[pb], (g >> 1) & 1, abort_flag, p.status);
-          if (!ok) break;
-          tc_fence_after();
-          bool comp;
-          int start, n;
-          block_of(t, j, comp, start, n);
-          const int nk = (n + 15) & ~15;
-          const int s = g % kStages;
-          const uint32_t va = smem_u32(smem + kOffKV + s * kTile);
-          const uint32_t pa = pa0 + pb * kTile;
-          const uint32_t idesc = idesc_bf16_f32(kRows, kHeadDim, false, true);
-          for (int kk = 0; kk < nk / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kHalfTile + (kk & 3) * 32;
-            mma_ss(tmem + kColO, smem_desc_sw128(pa + aoff, 16, 1024),
-                   smem_desc_sw128(va + kk * 2048, kHalfTile, 1024), idesc, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&bars.kv_empty[s]);
-          mma_commit(&bars.o_done[pb]);
         }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        gb = __shfl_sync(0xffffffffu, gb, 0);
+        ++gq;
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      gb += nb;
-      ++tiles_with_work;
+      if (!ok && !poisoned && lane == 0) {
+        volatile int never = 0;
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s)) mbar_wait(&bars.kv_full[s], (issued >> (8 + s)) & 1u, &never, p.status, 100000000ull);
+        if (q_par >= 0) mbar_wait(&bars.q_full, q_par, &never, p.status, 100000000ull);
+      }
+    } else if (warp == 13) {
+      // ---------------------------------------------------------- MMA
+      const uint32_t qa0 = smem_u32(smem + kOffQ), qa1 = smem_u32(smem + kOffQ + kTile);
+      uint32_t gb = 0, gq = 0, pcnt = 0;
+      bool ok = !poisoned, issued = false;
+      for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
+        Pair t;
+        pair_coords(p, u, t);
+        pair_ranges_warp(p, t, lane);
+        const int nb = t.nraw + t.ncomp;
+        if (nb == 0) continue;
+        if (lane == 0) {
+          ok = mbar_wait(&bars.q_full, gq & 1, abort_flag, p.status);
+          auto issue_s = [&](int x, int j, uint32_t g) {
+            bool comp;
+            int start, n;
+            pair_block(t, j, comp, start, n);
+            const int nk = (n + 15) & ~15;
+            const uint32_t idesc = idesc_bf16_f32(kRows, nk, false, false);
+            const uint32_t ka = smem_u32(smem + kOffKV + (g % kStages) * kTile);
+#pragma unroll
+            for (int k = 0; k < kHeadDim / 16; ++k) {
+              const uint32_t off = (k >> 2) * kHalfTile + (k & 3) * 32;
+              mma_ss(tmem + col_s(x), smem_desc_sw128((x ? qa1 : qa0) + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                     idesc, k > 0);
+            }
+            mma_commit(&bars.s_full[x]);
+            issued = true;
+          };
+          auto issue_pv = [&](int x, int j, uint32_t g) {
+            bool comp;
+            int start, n;
+            pair_block(t, j, comp, start, n);
+            const int nk = (n + 15) & ~15;
+            const uint32_t va = smem_u32(smem + kOffKV + (g % kStages) * kTile);
+            const uint32_t idesc = idesc_bf16_f32(kRows, kHeadDim, false, true);
+            for (int kk = 0; kk < nk / 16; ++kk)
+              mma_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, smem_desc_sw128(va + kk * 2048, kHalfTile, 1024),
+                     idesc, (j > 0 || kk > 0) ? 1u : 0u);
+          };
+          if (ok) ok = mbar_wait(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status);
+          if (ok) {
+            tc_fence_after();
+            issue_s(0, 0, gb);
+            issue_s(1, 0, gb);
+            if (nb == 1) mma_commit(&bars.q_empty);
+          }
+          for (int j = 0; ok && j < nb; ++j) {
+            const uint32_t g = gb + j;
+            const bool next = j + 1 < nb;
+            for (int x = 0; ok && x < 2; ++x) {
+              ok = mbar_wait(&bars.p_full[x], pcnt & 1, abort_flag, p.status);
+              if (ok && j == 0 && gq > 0) ok = mbar_wait(&bars.o_free[x], (gq - 1) & 1, abort_flag, p.status);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(x, j, g);
+              if (j == nb - 1) mma_commit(&bars.o_final[x]);
+              if (x == 1) mma_commit(&bars.kv_empty[g % kStages]);
+              if (next) {
+                if (x == 0) {
+                  ok = mbar_wait(&bars.kv_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag, p.status);
+                  if (!ok) break;
+                  tc_fence_after();
+                }
+                issue_s(x, j + 1, g + 1);
+                if (x == 1 && j + 1 == nb - 1) mma_commit(&bars.q_empty);
+              }
+            }
+            ++pcnt;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        pcnt = __shfl_sync(0xffffffffu, pcnt, 0);
+        gb += nb;
+        ++gq;
+      }
+      if (!ok && issued && lane == 0) {
+        volatile int never = 0;
+        mma_commit(&bars.drain);
+        mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+      }
     }
-    if (!ok && issued && lane == 0) {
-      volatile int never = 0;
-      mma_commit(&bars.drain);
-      mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
-    }
-  } else {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int r = tid;  // row == TMEM lane
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    uint8_t *pbuf = smem + kOffP;
-    uint8_t *obuf = smem + kOffOut;
-    uint32_t gb = 0;
-    uint32_t done_cnt[2] = {0, 0};
+  } else if (wg == 2) {
+    setmaxnreg_dec_epilogue();
+    // ------------------------------------------------------------ epilogue
+    const int r = tid - 2 * kWG;
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    uint32_t gq = 0, epi_phase = 0;
     bool ok = true;
-    bool store_pending = false;
-    uint32_t epi_phase = 0;
-    // all 128 softmax threads meet here (bounded; never a bar.sync, so a
-    // CTA that aborted cannot strand a thread)
+    uint32_t pending = 0;  // bit x: a store from staging tile x may still be reading it
     auto rendezvous = [&]() -> bool {
       mbar_arrive(&bars.epi);
-      const bool r = wait_warp(&bars.epi, epi_phase & 1, abort_flag, p.status);
+      const bool rr = wait_warp(&bars.epi, epi_phase & 1, abort_flag, p.status);
       ++epi_phase;
-      return r;
+      return rr;
     };
-    // wait until PV number x (global) has completed
-    auto wait_pv = [&](uint32_t x) -> bool {
-      const int buf = x & 1;
-      const uint32_t need = (x >> 1) + 1;
-      while (done_cnt[buf] < need) {
-        if (!wait_warp(&bars.o_done[buf], done_cnt[buf] & 1, abort_flag, p.status)) return false;
-        ++done_cnt[buf];
-      }
-      return true;
-    };
-    for (long long u = blockIdx.x; ok && u < p.qt.ntiles; u += gridDim.x) {
-      Tile t;
-      tile_coords(p.qt, u, t);
-      tile_ranges_warp(p.qt, t, lane);
+    for (long long u = blockIdx.x; ok && !poisoned && u < p.npairs; u += gridDim.x) {
+      Pair t;
+      pair_coords(p, u, t);
+      pair_ranges_warp(p, t, lane);
       const int nb = t.nraw + t.ncomp;
-      const int pq = r % p.qt.Pq, hh = r / p.qt.Pq;
-      const int head = t.g * p.qt.HG + hh;
-      const int i = t.i0 + pq;
-      const RowIv iv = row_interval(p.qt.sstart, t.b, p.qt.S, i, p.qt.W, p.qt.m);
-      const size_t lrow = ((size_t)t.b * p.qt.H + head) * p.qt.S + i;
-      if (poisoned || nb == 0) {
-        // whole tile without keys (padding) or poisoned call: direct stores
-        if (i < p.qt.S) {
-          const float v = poisoned ? __int_as_float(0x7fc00000) : 0.f;
-          const uint32_t w2 = pack_bf16x2(v, v);
-          uint4 *orow = reinterpret_cast<uint4 *>(p.out + lrow * kHeadDim);
-#pragma unroll
-          for (int c = 0; c < kHeadDim / 8; ++c) orow[c] = make_uint4(w2, w2, w2, w2);
-          p.lse[lrow] = poisoned ? v : -INFINITY;
-        }
-        continue;
-      }
-      float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < nb; ++j, ++gb) {
-        bool comp;
-        int start, n;
-        block_of(t, j, comp, start, n);
-        const int nk = (n + 15) & ~15;
-        // visible columns of this row inside the block
-        int lo_c = 0, hi_c = -1;
-        if (iv.valid) {
-          const int lo = comp ? iv.clo : iv.rlo, hi = comp ? iv.chi : iv.rhi;
-          lo_c = max(lo - start, 0);
-          hi_c = min(hi - start, n - 1);
-        }
-        if (!wait_warp(&bars.s_full, gb & 1, abort_flag, p.status)) { ok = false; break; }
+      if (nb == 0) continue;
+      for (int x = 0; ok && x < 2; ++x) {
+        const int i0 = t.i0 + x * Q.Pq;
+        uint8_t *obuf = smem + kOffOut + x * kTile;
+        if (!wait_warp(&bars.o_final[x], gq & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_warp(&bars.st_full[x], gq & 1, abort_flag, p.status)) { ok = false; break; }
+        const float inv = bars.inv_l[x][r];
+        mbar_arrive(&bars.st_free[x]);
         tc_fence_after();
-        float s[kBlockKeys];
-        {
-          uint32_t rr[32];
-#pragma unroll
-          for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
-            if (c0 < nk) {
-              if (c0 + 32 <= nk) {
-                tmem_ld32(lane_addr + kColS + c0, rr);
-              } else {
-                uint32_t r16[16];
-                tmem_ld16(lane_addr + kColS + c0, r16);
-#pragma unroll
-                for (int x = 0; x < 16; ++x) rr[x] = r16[x];
-              }
-              tmem_wait_ld();
-#pragma unroll
-              for (int x = 0; x < 32; ++x) s[c0 + x] = __uint_as_float(rr[x]);
-            }
-          }
+        if (pending & (1u << x)) {
+          // the store issued from this staging tile one pair ago must have read it
+          if (r == 0) bulk_wait_read1();
+          if (!rendezvous()) { ok = false; break; }
+          pending &= ~(1u << x);
         }
-        tc_fence_before();
-        mbar_arrive(&bars.s_free);
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kBlockKeys; ++c) {
-          const float v = (c >= lo_c && c <= hi_c) ? s[c] * p.sl2 : -INFINITY;
-          s[c] = v;
-          mx = fmaxf(mx, v);
-        }
-        // raise the running max only when this block exceeds it by > 2^8
-        float f = 1.f;
-        bool rescale_o = false;
-        if (mx > m_run + kRescaleLog2 || (m_run == -INFINITY && mx > -INFINITY)) {
-          if (m_run > -INFINITY) {
-            f = ex2_approx(m_run - mx);
-            l_run *= f;
-            rescale_o = j > 0;  // O holds PV(0..j-1) of this tile
-          }
-          m_run = mx;
-        }
-        const float m_use = m_run == -INFINITY ? 0.f : m_run;
-        float rs = 0.f;
-#pragma unroll
-        for (int c = 0; c < kBlockKeys; ++c) {
-          const float e = ex2_approx(s[c] - m_use);
-          s[c] = e;
-          rs += e;
-        }
-        l_run += rs;
-        // P buffer gb&1 was last read by PV(gb-2)
-        if (gb >= 2 && !wait_pv(gb - 2)) { ok = false; break; }
-        uint8_t *pb = pbuf + (gb & 1) * kTile;
-#pragma unroll
-        for (int ch = 0; ch < kBlockKeys / 8; ++ch) {
-          if (ch * 8 < nk) {
-            uint4 v;
-            v.x = pack_bf16x2(s[ch * 8 + 0], s[ch * 8 + 1]);
-            v.y = pack_bf16x2(s[ch * 8 + 2], s[ch * 8 + 3]);
-            v.z = pack_bf16x2(s[ch * 8 + 4], s[ch * 8 + 5]);
-            v.w = pack_bf16x2(s[ch * 8 + 6], s[ch * 8 + 7]);
-            *reinterpret_cast<uint4 *>(pb + sw128_offset(r, ch)) = v;
-          }
-        }
-        // the TMEM access below is warp-collective: rescale when any row of the
-        // warp needs it (rows without a new max use f = 1)
-        if (__any_sync(0xffffffffu, rescale_o)) {
-          // PV(j) waits for this block's P, so O is stable once PV(j-1) is done
-          if (!wait_pv(gb - 1)) { ok = false; break; }
-          tc_fence_after();
-          uint32_t o[32];
-#pragma unroll
-          for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
-            tmem_ld32(lane_addr + kColO + c0, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
-            tmem_st32(lane_addr + kColO + c0, o);
-          }
-          tmem_wait_st();
-        }
-        fence_async_smem();
-        tc_fence_before();
-        mbar_arrive(&bars.p_full[gb & 1]);
-      }
-      if (!ok) break;
-      // ---------------- epilogue
-      if (!wait_pv(gb - 1)) { ok = false; break; }
-      tc_fence_after();
-      if (store_pending) {
-        // the previous tile's TMA store must have read the staging tile
-        if (tid == 0) bulk_wait_read0();
-        if (!rendezvous()) { ok = false; break; }
-        store_pending = false;
-      }
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      {
         uint32_t o[32];
 #pragma unroll
         for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
-          tmem_ld32(lane_addr + kColO + c0, o);
+          tmem_ld32(lane_addr + col_o(x) + c0, o);
           tmem_wait_ld();
+          if (c0 == kHeadDim - 32) {
+            tc_fence_before();
+            mbar_arrive(&bars.o_free[x]);  // O_X may now be overwritten
+          }
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             uint4 v;
@@ -416,35 +365,187 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4 *>(obuf + sw128_offset(r, c0 / 8 + ch)) = v;
           }
         }
+        fence_async_smem();
+        if (!rendezvous()) { ok = false; break; }
+        if (i0 < Q.S) {
+          if (r == 0) {
+            const int c2 = t.b * Q.H + t.g * Q.HG;
+            tma_store_3d(&map_out, obuf, 0, i0, c2);
+            tma_store_3d(&map_out, obuf + kHalfTile, 64, i0, c2);
+          }
+        }
+        if (r == 0) bulk_commit();  // one group per staging tile (possibly empty)
+        pending |= 1u << x;
       }
-      if (i < p.qt.S) {
-        float lv;
+      ++gq;
+    }
+    if (r == 0) bulk_wait0();
+  } else {
+    setmaxnreg_inc_softmax();
+    // ------------------------------------------------------------ softmax of tile X
+    const int x = wg;  // 0: tile A, 1: tile B
+    const int r = tid - x * kWG;
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    uint32_t scnt = 0, gq = 0;
+    bool ok = true;
+    for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
+      Pair t;
+      pair_coords(p, u, t);
+      pair_ranges_warp(p, t, lane);
+      const int nb = t.nraw + t.ncomp;
+      const int pq = r % Q.Pq, hh = r / Q.Pq;
+      const int head = t.g * Q.HG + hh;
+      const int i = t.i0 + x * Q.Pq + pq;
+      const RowIv iv = row_interval(Q.sstart, t.b, Q.S, i, Q.W, Q.m);
+      const size_t lrow = ((size_t)t.b * Q.H + head) * Q.S + i;
+      if (poisoned || nb == 0) {
+        if (i < Q.S) {
+          const float v = poisoned ? __int_as_float(0x7fc00000) : 0.f;
+          const uint32_t w2 = pack_bf16x2(v, v);
+          uint4 *orow = reinterpret_cast<uint4 *>(p.out + lrow * kHeadDim);
+#pragma unroll
+          for (int c = 0; c < kHeadDim / 8; ++c) orow[c] = make_uint4(w2, w2, w2, w2);
+          p.lse[lrow] = poisoned ? v : -INFINITY;
+        }
+        continue;
+      }
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < nb; ++j) {
+        bool comp;
+        int start, n;
+        pair_block(t, j, comp, start, n);
+        const int nk = (n + 15) & ~15;
+        int lo_c = 0, hi_c = -1;
+        if (iv.valid) {
+          const int lo = comp ? iv.clo : iv.rlo, hi = comp ? iv.chi : iv.rhi;
+          lo_c = max(lo - start, 0);
+          hi_c = min(hi - start, n - 1);
+        }
+        // S_X(j) ready; since S_X(j) was issued after PV_X(j-1), O_X is stable
+        if (!wait_warp(&bars.s_full[x], scnt & 1, abort_flag, p.status)) { ok = false; break; }
+        ++scnt;
+        tc_fence_after();
+        // Two passes over S_X in TMEM keep register pressure low: pass 1 takes
+        // the masked row max, pass 2 re-reads 32 columns at a time to form P.
+        const bool full = lo_c == 0 && hi_c == nk - 1;
+        const bool warp_full = __all_sync(0xffffffffu, full);
+        float mx;
+        {
+          float m8[8];
+#pragma unroll
+          for (int y = 0; y < 8; ++y) m8[y] = -INFINITY;
+#pragma unroll
+          for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
+            if (c0 < nk) {
+              uint32_t rr[32];
+              if (c0 + 32 <= nk) {
+                tmem_ld32(lane_addr + col_s(x) + c0, rr);
+              } else {
+                uint32_t r16[16];
+                tmem_ld16(lane_addr + col_s(x) + c0, r16);
+#pragma unroll
+                for (int y = 0; y < 16; ++y) rr[y] = r16[y];
+#pragma unroll
+                for (int y = 16; y < 32; ++y) rr[y] = 0xff800000u;  // -inf
+              }
+              tmem_wait_ld();
+#pragma unroll
+              for (int y = 0; y < 32; ++y) {
+                const int c = c0 + y;
+                float v = __uint_as_float(rr[y]);
+                if (!warp_full && (c < lo_c || c > hi_c)) v = -INFINITY;
+                if (!kPosScale) v *= p.sl2;
+                m8[y & 7] = fmaxf(m8[y & 7], v);
+              }
+            }
+          }
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          if (kPosScale) mx *= p.sl2;
+        }
+        float f = 1.f;
+        bool rescale_o = false;
+        if (mx > m_run + kRescaleLog2 || (m_run == -INFINITY && mx > -INFINITY)) {
+          if (m_run > -INFINITY) {
+            f = ex2_approx(m_run - mx);
+            l_run *= f;
+            rescale_o = j > 0;
+          }
+          m_run = mx;
+        }
+        const float m_use = m_run == -INFINITY ? 0.f : m_run;
+        // pass 2: exp2, row sum, bf16 packing; P_X overwrites the first nk/2
+        // columns of S_X, which pass 2 has already read (chunk k writes columns
+        // [16k, 16k+16), inside chunks 0..k/2 of S)
+        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
+          if (c0 < nk) {
+            uint32_t rr[32];
+            if (c0 + 32 <= nk) {
+              tmem_ld32(lane_addr + col_s(x) + c0, rr);
+            } else {
+              uint32_t r16[16];
+              tmem_ld16(lane_addr + col_s(x) + c0, r16);
+#pragma unroll
+              for (int y = 0; y < 16; ++y) rr[y] = r16[y];
+#pragma unroll
+              for (int y = 16; y < 32; ++y) rr[y] = 0u;
+            }
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int y = 0; y < 32; y += 2) {
+              float e[2];
+#pragma unroll
+              for (int z = 0; z < 2; ++z) {
+                const int c = c0 + y + z;
+                const float sv = __uint_as_float(rr[y + z]);
+                e[z] = kPosScale ? ex2_approx(fmaf(sv, p.sl2, -m_use)) : ex2_approx(sv * p.sl2 - m_use);
+                if (c >= nk || (!warp_full && (c < lo_c || c > hi_c))) e[z] = 0.f;
+              }
+              rs4[(y >> 1) & 3] += e[0] + e[1];
+              pk[y >> 1] = pack_bf16x2(e[0], e[1]);
+            }
+            tmem_st16(lane_addr + col_s(x) + c0 / 2, pk);
+          }
+        }
+        l_run += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          uint32_t o[32];
+#pragma unroll
+          for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+            tmem_ld32(lane_addr + col_o(x) + c0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int y = 0; y < 32; ++y) o[y] = __float_as_uint(__uint_as_float(o[y]) * f);
+            tmem_st32(lane_addr + col_o(x) + c0, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars.p_full[x]);
+      }
+      if (!ok) break;
+      // row statistics: lse to global, 1/l to the epilogue
+      if (gq > 0 && !wait_warp(&bars.st_free[x], (gq - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      bars.inv_l[x][r] = l_run > 0.f ? 1.f / l_run : 0.f;
+      mbar_arrive(&bars.st_full[x]);
+      if (i < Q.S) {
+        float lv = -INFINITY;
         if (l_run > 0.f) {
           float lg;
           asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(l_run));
           lv = (m_run + lg) * 0.69314718055994531f;
-        } else {
-          lv = -INFINITY;
         }
         p.lse[lrow] = lv;
       }
-      fence_async_smem();
-      tc_fence_before();
-      if (!rendezvous()) { ok = false; break; }
-      if (tid == 0) {
-        const int c2 = t.b * p.qt.H + t.g * p.qt.HG;
-        tma_store_3d(&map_out, obuf, 0, t.i0, c2);
-        tma_store_3d(&map_out, obuf + kHalfTile, 64, t.i0, c2);
-        bulk_commit();
-      }
-      store_pending = true;
+      ++gq;
     }
-    if (tid == 0) bulk_wait0();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -460,6 +561,8 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st) {
   FwdParams p;
   p.qt = make_qtiling(a.sstart, a.B, a.H, a.S, a.W, a.m);
   const QTiling &q = p.qt;
+  p.ntp = (q.ntq + 1) / 2;
+  p.npairs = (long long)a.B * q.groups * p.ntp;
   CUtensorMap mq, mkv, mckv, mout;
   if (!make_map_bf16(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mout, a.out, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
@@ -470,18 +573,20 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st) {
   p.lse = a.lse;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.sl2 = a.scale * 1.4426950408889634f;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(hca_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const bool pos = p.sl2 > 0.f;
+  auto kern = pos ? hca_fwd_tc_kernel<true> : hca_fwd_tc_kernel<false>;
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[pos]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[pos] = true;
   }
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
-  const long long grid = q.ntiles < sms ? q.ntiles : sms;
+  const long long grid = p.npairs < sms ? p.npairs : sms;
   if (grid == 0) return cudaSuccess;
   ProfScope prof(kKFwdTc, st);
-  hca_fwd_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mkv, mckv, mout, p);
+  kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mkv, mckv, mout, p);
   return cudaGetLastError();
 }
 
