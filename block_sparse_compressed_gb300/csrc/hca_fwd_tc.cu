@@ -427,8 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // Two passes over S_X in TMEM keep register pressure low: pass 1 takes
         // the masked row max, pass 2 re-reads 32 columns at a time to form P.
-        const bool full = lo_c == 0 && hi_c == nk - 1;
-        const bool warp_full = __all_sync(0xffffffffu, full);
+        // Columns outside [lo_c, hi_c] are masked; a chunk that every row of
+        // the warp sees whole skips the per-element test (warp-uniform).
+        const int wlo = __reduce_max_sync(0xffffffffu, lo_c);
+        const int whi = __reduce_min_sync(0xffffffffu, hi_c);
         float mx;
         {
           float m8[8];
@@ -437,25 +439,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
             if (c0 < nk) {
+              const bool tail = c0 + 32 > nk;  // 16 live columns
               uint32_t rr[32];
-              if (c0 + 32 <= nk) {
+              if (!tail) {
                 tmem_ld32(lane_addr + col_s(x) + c0, rr);
               } else {
                 uint32_t r16[16];
                 tmem_ld16(lane_addr + col_s(x) + c0, r16);
 #pragma unroll
                 for (int y = 0; y < 16; ++y) rr[y] = r16[y];
-#pragma unroll
-                for (int y = 16; y < 32; ++y) rr[y] = 0xff800000u;  // -inf
               }
               tmem_wait_ld();
+              const int w = tail ? 16 : 32;
+              if (c0 >= wlo && c0 + w - 1 <= whi) {
 #pragma unroll
-              for (int y = 0; y < 32; ++y) {
-                const int c = c0 + y;
-                float v = __uint_as_float(rr[y]);
-                if (!warp_full && (c < lo_c || c > hi_c)) v = -INFINITY;
-                if (!kPosScale) v *= p.sl2;
-                m8[y & 7] = fmaxf(m8[y & 7], v);
+                for (int y = 0; y < 32; ++y) {
+                  if (y < 16 || !tail) {
+                    float v = __uint_as_float(rr[y]);
+                    if (!kPosScale) v *= p.sl2;
+                    m8[y & 7] = fmaxf(m8[y & 7], v);
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int y = 0; y < 32; ++y) {
+                  if (y < 16 || !tail) {
+                    float v = __uint_as_float(rr[y]);
+                    if (c0 + y < lo_c || c0 + y > hi_c) v = -INFINITY;
+                    if (!kPosScale) v *= p.sl2;
+                    m8[y & 7] = fmaxf(m8[y & 7], v);
+                  }
+                }
               }
             }
           }
@@ -473,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = mx;
         }
         const float m_use = m_run == -INFINITY ? 0.f : m_run;
+        const float neg_m = -m_use;
         // pass 2: exp2, row sum, bf16 packing; P_X overwrites the first nk/2
         // columns of S_X, which pass 2 has already read (chunk k writes columns
         // [16k, 16k+16), inside chunks 0..k/2 of S)
@@ -480,28 +495,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
           if (c0 < nk) {
+            const bool tail = c0 + 32 > nk;
             uint32_t rr[32];
-            if (c0 + 32 <= nk) {
+            if (!tail) {
               tmem_ld32(lane_addr + col_s(x) + c0, rr);
             } else {
               uint32_t r16[16];
               tmem_ld16(lane_addr + col_s(x) + c0, r16);
 #pragma unroll
               for (int y = 0; y < 16; ++y) rr[y] = r16[y];
-#pragma unroll
-              for (int y = 16; y < 32; ++y) rr[y] = 0u;
             }
             tmem_wait_ld();
+            const int w = tail ? 16 : 32;
+            const bool whole = c0 >= wlo && c0 + w - 1 <= whi;
             uint32_t pk[16];
 #pragma unroll
             for (int y = 0; y < 32; y += 2) {
               float e[2];
 #pragma unroll
               for (int z = 0; z < 2; ++z) {
-                const int c = c0 + y + z;
                 const float sv = __uint_as_float(rr[y + z]);
-                e[z] = kPosScale ? ex2_approx(fmaf(sv, p.sl2, -m_use)) : ex2_approx(sv * p.sl2 - m_use);
-                if (c >= nk || (!warp_full && (c < lo_c || c > hi_c))) e[z] = 0.f;
+                e[z] = kPosScale ? ex2_approx(fmaf(sv, p.sl2, neg_m)) : ex2_approx(fmaf(sv, p.sl2, neg_m));
+                if (!whole && (c0 + y + z < lo_c || c0 + y + z > hi_c)) e[z] = 0.f;
+                if (tail && y + z >= 16) e[z] = 0.f;
               }
               rs4[(y >> 1) & 3] += e[0] + e[1];
               pk[y >> 1] = pack_bf16x2(e[0], e[1]);
