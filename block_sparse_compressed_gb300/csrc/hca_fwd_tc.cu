@@ -426,55 +426,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++scnt;
         tc_fence_after();
         // Two passes over S_X in TMEM keep register pressure low: pass 1 takes
-        // the masked row max, pass 2 re-reads 32 columns at a time to form P.
-        // Columns outside [lo_c, hi_c] are masked; a chunk that every row of
-        // the warp sees whole skips the per-element test (warp-uniform).
+        // the masked row max (two 32-column loads per round trip), pass 2
+        // re-reads 32 columns at a time (the next load overlaps the current
+        // chunk's math) to form P.  Columns outside [lo_c, hi_c] are masked --
+        // that also covers the columns past n of a short block -- and a chunk
+        // that every row of the warp sees whole skips the per-element test.
         const int wlo = __reduce_max_sync(0xffffffffu, lo_c);
         const int whi = __reduce_min_sync(0xffffffffu, hi_c);
+        const uint32_t sbase = lane_addr + col_s(x);
         float mx;
         {
-          float m8[8];
+          // kPosScale: max of s, scaled after; otherwise min of s (scale < 0)
+          const float ninf = kPosScale ? -INFINITY : INFINITY;
+          float ma = ninf, mb = ninf;
+          auto reduce_chunk = [&](const uint32_t(&rr)[32], int c0) {
+            const bool whole = c0 >= wlo && c0 + 31 <= whi;
+            float v[32];
 #pragma unroll
-          for (int y = 0; y < 8; ++y) m8[y] = -INFINITY;
+            for (int y = 0; y < 32; ++y) {
+              v[y] = __uint_as_float(rr[y]);
+              if (!whole && (c0 + y < lo_c || c0 + y > hi_c)) v[y] = ninf;
+            }
 #pragma unroll
-          for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
-            if (c0 < nk) {
-              const bool tail = c0 + 32 > nk;  // 16 live columns
-              uint32_t rr[32];
-              if (!tail) {
-                tmem_ld32(lane_addr + col_s(x) + c0, rr);
+            for (int y = 0; y < 32; y += 4) {
+              if (kPosScale) {
+                ma = fmax3(ma, v[y], v[y + 1]);
+                mb = fmax3(mb, v[y + 2], v[y + 3]);
               } else {
-                uint32_t r16[16];
-                tmem_ld16(lane_addr + col_s(x) + c0, r16);
-#pragma unroll
-                for (int y = 0; y < 16; ++y) rr[y] = r16[y];
-              }
-              tmem_wait_ld();
-              const int w = tail ? 16 : 32;
-              if (c0 >= wlo && c0 + w - 1 <= whi) {
-#pragma unroll
-                for (int y = 0; y < 32; ++y) {
-                  if (y < 16 || !tail) {
-                    float v = __uint_as_float(rr[y]);
-                    if (!kPosScale) v *= p.sl2;
-                    m8[y & 7] = fmaxf(m8[y & 7], v);
-                  }
-                }
-              } else {
-#pragma unroll
-                for (int y = 0; y < 32; ++y) {
-                  if (y < 16 || !tail) {
-                    float v = __uint_as_float(rr[y]);
-                    if (c0 + y < lo_c || c0 + y > hi_c) v = -INFINITY;
-                    if (!kPosScale) v *= p.sl2;
-                    m8[y & 7] = fmaxf(m8[y & 7], v);
-                  }
-                }
+                ma = fmin3(ma, v[y], v[y + 1]);
+                mb = fmin3(mb, v[y + 2], v[y + 3]);
               }
             }
+          };
+#pragma unroll
+          for (int c0 = 0; c0 < kBlockKeys; c0 += 64) {
+            if (c0 < nk) {
+              uint32_t ra[32], rb[32];
+              const bool two = c0 + 32 < nk;
+              tmem_ld32(sbase + c0, ra);
+              if (two) tmem_ld32(sbase + c0 + 32, rb);
+              tmem_wait_ld();
+              reduce_chunk(ra, c0);
+              if (two) reduce_chunk(rb, c0 + 32);
+            }
           }
-          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-          if (kPosScale) mx *= p.sl2;
+          const float m = kPosScale ? fmaxf(ma, mb) : fminf(ma, mb);
+          mx = (m == ninf) ? -INFINITY : m * p.sl2;
         }
         float f = 1.f;
         bool rescale_o = false;
@@ -487,45 +484,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = mx;
         }
         const float m_use = m_run == -INFINITY ? 0.f : m_run;
-        const float neg_m = -m_use;
         // pass 2: exp2, row sum, bf16 packing; P_X overwrites the first nk/2
         // columns of S_X, which pass 2 has already read (chunk k writes columns
-        // [16k, 16k+16), inside chunks 0..k/2 of S)
-        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+        // [16k, 16k+16), inside S chunks 0..k/2; the load in flight is chunk k+1)
+        {
+          const uint64_t sl2x2 = f32x2(__float_as_uint(p.sl2), __float_as_uint(p.sl2));
+          const uint64_t nm2 = f32x2(__float_as_uint(-m_use), __float_as_uint(-m_use));
+          uint64_t acc0 = 0, acc1 = 0;  // packed row sums (+0.0f bit patterns)
+          uint32_t buf[2][32];
+          tmem_ld32(sbase, buf[0]);
 #pragma unroll
-        for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
-          if (c0 < nk) {
-            const bool tail = c0 + 32 > nk;
-            uint32_t rr[32];
-            if (!tail) {
-              tmem_ld32(lane_addr + col_s(x) + c0, rr);
-            } else {
-              uint32_t r16[16];
-              tmem_ld16(lane_addr + col_s(x) + c0, r16);
+          for (int k = 0; k < kBlockKeys / 32; ++k) {
+            const int c0 = 32 * k;
+            if (c0 < nk) {
+              tmem_wait_ld();
+              if (c0 + 32 < nk) tmem_ld32(sbase + c0 + 32, buf[(k + 1) & 1]);
+              const uint32_t(&rr)[32] = buf[k & 1];
+              const bool whole = c0 >= wlo && c0 + 31 <= whi;
+              uint32_t pk[16];
 #pragma unroll
-              for (int y = 0; y < 16; ++y) rr[y] = r16[y];
-            }
-            tmem_wait_ld();
-            const int w = tail ? 16 : 32;
-            const bool whole = c0 >= wlo && c0 + w - 1 <= whi;
-            uint32_t pk[16];
-#pragma unroll
-            for (int y = 0; y < 32; y += 2) {
-              float e[2];
-#pragma unroll
-              for (int z = 0; z < 2; ++z) {
-                const float sv = __uint_as_float(rr[y + z]);
-                e[z] = kPosScale ? ex2_approx(fmaf(sv, p.sl2, neg_m)) : ex2_approx(fmaf(sv, p.sl2, neg_m));
-                if (!whole && (c0 + y + z < lo_c || c0 + y + z > hi_c)) e[z] = 0.f;
-                if (tail && y + z >= 16) e[z] = 0.f;
+              for (int y = 0; y < 32; y += 2) {
+                float t0, t1;
+                f32x2_split(ffma2(f32x2(rr[y], rr[y + 1]), sl2x2, nm2), t0, t1);
+                float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
+                if (!whole) {
+                  if (c0 + y < lo_c || c0 + y > hi_c) e0 = 0.f;
+                  if (c0 + y + 1 < lo_c || c0 + y + 1 > hi_c) e1 = 0.f;
+                }
+                const uint64_t e2 = f32x2(__float_as_uint(e0), __float_as_uint(e1));
+                if ((y >> 1) & 1) acc1 = fadd2(acc1, e2); else acc0 = fadd2(acc0, e2);
+                pk[y >> 1] = pack_bf16x2(e0, e1);
               }
-              rs4[(y >> 1) & 3] += e[0] + e[1];
-              pk[y >> 1] = pack_bf16x2(e[0], e[1]);
+              tmem_st16(lane_addr + col_s(x) + c0 / 2, pk);
             }
-            tmem_st16(lane_addr + col_s(x) + c0 / 2, pk);
           }
+          float a0, a1, b0, b1;
+          f32x2_split(acc0, a0, a1);
+          f32x2_split(acc1, b0, b1);
+          l_run += (a0 + a1) + (b0 + b1);
         }
-        l_run += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
         if (__any_sync(0xffffffffu, rescale_o)) {
           uint32_t o[32];
 #pragma unroll
