@@ -169,7 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA
-    const uint32_t qa = smem_u32(smem + kOffQ), da = smem_u32(smem + kOffDO);
+    const uint64_t dQ = smem_desc_sw128(smem_u32(smem + kOffQ), 16, 1024);
+    const uint64_t dDO = smem_desc_sw128(smem_u32(smem + kOffDO), 16, 1024);
+    const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + kOffKV), 16, 1024);
+    const uint64_t dV0 = smem_desc_sw128(smem_u32(smem + kOffKV), kHalfTile, 1024);
     uint32_t gb = 0, tw = 0;
     bool ok = !poisoned, issued = false;
     for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
@@ -190,13 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           block_of(t, j, comp, start, n);
           const int nk = (n + 15) & ~15;
           const uint32_t idesc = idesc_bf16_f32(kRows, nk, false, false);
-          const uint32_t ka = smem_u32(smem + kOffKV + s * kTile);
+          const uint64_t bk = dK0 + desc_bytes(s * kTile);
 #pragma unroll
           for (int k = 0; k < kHeadDim / 16; ++k) {
-            const uint32_t off = (k >> 2) * kHalfTile + (k & 3) * 32;
-            const uint64_t bk = smem_desc_sw128(ka + off, 16, 1024);
-            mma_ss(tmem + kColS, smem_desc_sw128(qa + off, 16, 1024), bk, idesc, k > 0);
-            mma_ss(tmem + kColDP, smem_desc_sw128(da + off, 16, 1024), bk, idesc, k > 0);
+            mma_ss(tmem + kColS, dQ + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
+            mma_ss(tmem + kColDP, dDO + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
           }
           mma_commit(&bars.s_full);
           issued = true;
@@ -219,11 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           block_of(t, j, comp, start, n);
           const int nk = (n + 15) & ~15;
           const int s = g % kStages;
-          const uint32_t ka = smem_u32(smem + kOffKV + s * kTile);
+          const uint64_t bv = dV0 + desc_bytes(s * kTile);
           const uint32_t idesc = idesc_bf16_f32(kRows, kHeadDim, false, true);
           for (int kk = 0; kk < nk / 16; ++kk)
-            mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, smem_desc_sw128(ka + kk * 2048, kHalfTile, 1024), idesc,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, bv + mnmaj_step(kk), idesc, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars.kv_empty[s]);
           mma_commit(&bars.dq_done);
         }
@@ -588,7 +588,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA
-    const uint32_t ka = smem_u32(smem + kOffK);
+    const uint64_t dK = smem_desc_sw128(smem_u32(smem + kOffK), 16, 1024);
+    const uint64_t dS0 = smem_desc_sw128(smem_u32(smem + kOffStage), 16, 1024);          // K-major view of stage 0
+    const uint64_t dM0 = smem_desc_sw128(smem_u32(smem + kOffStage), kHalfTile, 1024);   // MN-major view of stage 0
     uint32_t gq = 0, iw = 0;
     bool ok = !poisoned, issued = false;
     for (long long u = blockIdx.x; ok && u < p.nitems; u += gridDim.x) {
@@ -605,13 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&bars.st_full[s], (g / kStages) & 1, abort_flag, p.status)) return false;
           if (g > 0 && !mbar_wait(&bars.s_free, (g - 1) & 1, abort_flag, p.status)) return false;
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + kOffStage + s * kStageBytes);
+          const uint64_t bq = dS0 + desc_bytes(s * kStageBytes);
+          const uint64_t bdo = bq + desc_bytes(kTile);
 #pragma unroll
           for (int k = 0; k < kHeadDim / 16; ++k) {
-            const uint32_t off = (k >> 2) * kHalfTile + (k & 3) * 32;
-            const uint64_t ak = smem_desc_sw128(ka + off, 16, 1024);
-            mma_ss(tmem + kColS, ak, smem_desc_sw128(sa + off, 16, 1024), id_s, k > 0);
-            mma_ss(tmem + kColDP, ak, smem_desc_sw128(sa + kTile + off, 16, 1024), id_s, k > 0);
+            mma_ss(tmem + kColS, dK + kmaj_step(k), bq + kmaj_step(k), id_s, k > 0);
+            mma_ss(tmem + kColDP, dK + kmaj_step(k), bdo + kmaj_step(k), id_s, k > 0);
           }
           mma_commit(&bars.s_full);
           issued = true;
@@ -628,14 +629,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const int s = g % kStages;
-          const uint32_t sa = smem_u32(smem + kOffStage + s * kStageBytes);
+          const uint64_t mq = dM0 + desc_bytes(s * kStageBytes);
+          const uint64_t mdo = mq + desc_bytes(kTile);
+#pragma unroll
           for (int kk = 0; kk < kRows / 16; ++kk) {
             // acc += P^T dO  (dO tile as an MN-major B operand)
-            mma_ts(tmem + kColAcc, tmem + kColP + kk * 8, smem_desc_sw128(sa + kTile + kk * 2048, kHalfTile, 1024),
-                   id_acc, (x > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + kColAcc, tmem + kColP + kk * 8, mdo + mnmaj_step(kk), id_acc, (x > 0 || kk > 0) ? 1u : 0u);
             // acc += (scale dS)^T Q
-            mma_ts(tmem + kColAcc, tmem + kColDS + kk * 8, smem_desc_sw128(sa + kk * 2048, kHalfTile, 1024), id_acc,
-                   1u);
+            mma_ts(tmem + kColAcc, tmem + kColDS + kk * 8, mq + mnmaj_step(kk), id_acc, 1u);
           }
           mma_commit(&bars.st_empty[s]);
           mma_commit(&bars.acc_done);

@@ -31,7 +31,7 @@
 // softmax rescale O_X right after S_X(j+1) arrives.
 //
 // Warp roles (512 threads, persistent CTAs; registers rebalanced with
-// setmaxnreg to 168 / 168 / 96 / 80 per thread):
+// setmaxnreg to 176 / 176 / 72 / 88 per thread):
 //   warpgroup 0   softmax of tile A (thread r owns row r = TMEM lane r)
 //   warpgroup 1   softmax of tile B
 //   warpgroup 2   epilogue: O_X * (1/l) -> bf16 -> swizzled smem -> TMA store
@@ -57,7 +57,7 @@ constexpr int kTmemCols = 512;    // S_A | S_B | O_A | O_B, 128 columns each
 __host__ __device__ constexpr uint32_t col_s(int x) { return (uint32_t)x * 128u; }        // S_X (P_X aliases it)
 __host__ __device__ constexpr uint32_t col_o(int x) { return 256u + (uint32_t)x * 128u; }  // O_X
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kRegSoftmax = 168, kRegEpilogue = 96, kRegProducer = 80;
+constexpr int kRegSoftmax = 176, kRegEpilogue = 72, kRegProducer = 88;
 static_assert(2 * kRegSoftmax + kRegEpilogue + kRegProducer == 512, "register split must fit the launch");
 
 // dynamic shared memory: Q_A | Q_B | kv ring | out staging A | B (+1 KB align)
@@ -111,9 +111,9 @@ __device__ __forceinline__ void pair_block(const Pair &t, int j, bool &comp, int
   block_of(tt, j, comp, start, n);
 }
 
-__device__ __forceinline__ void setmaxnreg_inc_softmax() { asm volatile("setmaxnreg.inc.sync.aligned.u32 168;"); }
-__device__ __forceinline__ void setmaxnreg_dec_epilogue() { asm volatile("setmaxnreg.dec.sync.aligned.u32 96;"); }
-__device__ __forceinline__ void setmaxnreg_dec_producer() { asm volatile("setmaxnreg.dec.sync.aligned.u32 80;"); }
+__device__ __forceinline__ void setmaxnreg_inc_softmax() { asm volatile("setmaxnreg.inc.sync.aligned.u32 176;"); }
+__device__ __forceinline__ void setmaxnreg_dec_epilogue() { asm volatile("setmaxnreg.dec.sync.aligned.u32 72;"); }
+__device__ __forceinline__ void setmaxnreg_dec_producer() { asm volatile("setmaxnreg.dec.sync.aligned.u32 88;"); }
 
 struct Bars {
   uint64_t q_full, q_empty;
@@ -232,7 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 13) {
       // ---------------------------------------------------------- MMA
-      const uint32_t qa0 = smem_u32(smem + kOffQ), qa1 = smem_u32(smem + kOffQ + kTile);
+      // descriptors are built once; an MMA only adds a constant offset
+      const uint64_t dq0 = smem_desc_sw128(smem_u32(smem + kOffQ), 16, 1024);
+      const uint64_t dq1 = smem_desc_sw128(smem_u32(smem + kOffQ + kTile), 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(smem_u32(smem + kOffKV), 16, 1024);         // K view of stage 0
+      const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + kOffKV), kHalfTile, 1024);  // V view of stage 0
       uint32_t gb = 0, gq = 0, pcnt = 0;
       bool ok = !poisoned, issued = false;
       for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
@@ -249,13 +253,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             pair_block(t, j, comp, start, n);
             const int nk = (n + 15) & ~15;
             const uint32_t idesc = idesc_bf16_f32(kRows, nk, false, false);
-            const uint32_t ka = smem_u32(smem + kOffKV + (g % kStages) * kTile);
+            const uint64_t da = x ? dq1 : dq0;
+            const uint64_t db = dk0 + desc_bytes((g % kStages) * kTile);
 #pragma unroll
-            for (int k = 0; k < kHeadDim / 16; ++k) {
-              const uint32_t off = (k >> 2) * kHalfTile + (k & 3) * 32;
-              mma_ss(tmem + col_s(x), smem_desc_sw128((x ? qa1 : qa0) + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                     idesc, k > 0);
-            }
+            for (int k = 0; k < kHeadDim / 16; ++k)
+              mma_ss(tmem + col_s(x), da + kmaj_step(k), db + kmaj_step(k), idesc, k > 0);
             mma_commit(&bars.s_full[x]);
             issued = true;
           };
@@ -264,11 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int start, n;
             pair_block(t, j, comp, start, n);
             const int nk = (n + 15) & ~15;
-            const uint32_t va = smem_u32(smem + kOffKV + (g % kStages) * kTile);
+            const uint64_t db = dv0 + desc_bytes((g % kStages) * kTile);
             const uint32_t idesc = idesc_bf16_f32(kRows, kHeadDim, false, true);
             for (int kk = 0; kk < nk / 16; ++kk)
-              mma_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, smem_desc_sw128(va + kk * 2048, kHalfTile, 1024),
-                     idesc, (j > 0 || kk > 0) ? 1u : 0u);
+              mma_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, db + mnmaj_step(kk), idesc, (j > 0 || kk > 0) ? 1u : 0u);
           };
           if (ok) ok = mbar_wait(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status);
           if (ok) {
@@ -425,49 +426,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(&bars.s_full[x], scnt & 1, abort_flag, p.status)) { ok = false; break; }
         ++scnt;
         tc_fence_after();
-        // Two passes over S_X in TMEM keep register pressure low: pass 1 takes
-        // the masked row max (two 32-column loads per round trip), pass 2
-        // re-reads 32 columns at a time (the next load overlaps the current
-        // chunk's math) to form P.  Columns outside [lo_c, hi_c] are masked --
-        // that also covers the columns past n of a short block -- and a chunk
-        // that every row of the warp sees whole skips the per-element test.
+        // One TMEM round trip brings the row's nk scores into registers; the
+        // masked row max, then exp2 / row sum / bf16 packing 32 columns at a
+        // time.  P_X overwrites the first nk/2 columns of S_X.  Columns outside
+        // [lo_c, hi_c] are masked -- that also covers the columns past n of a
+        // short block -- and a chunk that every row of the warp sees whole
+        // skips the per-element test (warp-uniform).
         const int wlo = __reduce_max_sync(0xffffffffu, lo_c);
         const int whi = __reduce_min_sync(0xffffffffu, hi_c);
         const uint32_t sbase = lane_addr + col_s(x);
+        uint32_t sv[kBlockKeys];
+        {
+          uint32_t* c0p = sv;
+          tmem_ld32(sbase, *reinterpret_cast<uint32_t(*)[32]>(c0p));
+          if (32 < nk) tmem_ld32(sbase + 32, *reinterpret_cast<uint32_t(*)[32]>(c0p + 32));
+          if (64 < nk) tmem_ld32(sbase + 64, *reinterpret_cast<uint32_t(*)[32]>(c0p + 64));
+          if (96 < nk) tmem_ld32(sbase + 96, *reinterpret_cast<uint32_t(*)[32]>(c0p + 96));
+          tmem_wait_ld();
+        }
         float mx;
         {
           // kPosScale: max of s, scaled after; otherwise min of s (scale < 0)
           const float ninf = kPosScale ? -INFINITY : INFINITY;
           float ma = ninf, mb = ninf;
-          auto reduce_chunk = [&](const uint32_t(&rr)[32], int c0) {
-            const bool whole = c0 >= wlo && c0 + 31 <= whi;
-            float v[32];
 #pragma unroll
-            for (int y = 0; y < 32; ++y) {
-              v[y] = __uint_as_float(rr[y]);
-              if (!whole && (c0 + y < lo_c || c0 + y > hi_c)) v[y] = ninf;
-            }
-#pragma unroll
-            for (int y = 0; y < 32; y += 4) {
-              if (kPosScale) {
-                ma = fmax3(ma, v[y], v[y + 1]);
-                mb = fmax3(mb, v[y + 2], v[y + 3]);
-              } else {
-                ma = fmin3(ma, v[y], v[y + 1]);
-                mb = fmin3(mb, v[y + 2], v[y + 3]);
-              }
-            }
-          };
-#pragma unroll
-          for (int c0 = 0; c0 < kBlockKeys; c0 += 64) {
+          for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
             if (c0 < nk) {
-              uint32_t ra[32], rb[32];
-              const bool two = c0 + 32 < nk;
-              tmem_ld32(sbase + c0, ra);
-              if (two) tmem_ld32(sbase + c0 + 32, rb);
-              tmem_wait_ld();
-              reduce_chunk(ra, c0);
-              if (two) reduce_chunk(rb, c0 + 32);
+              const bool whole = c0 >= wlo && c0 + 31 <= whi;
+              if (!whole) {
+#pragma unroll
+                for (int y = 0; y < 32; ++y)
+                  if (c0 + y < lo_c || c0 + y > hi_c) sv[c0 + y] = __float_as_uint(ninf);
+              }
+#pragma unroll
+              for (int y = 0; y < 32; y += 4) {
+                if (kPosScale) {
+                  ma = fmax3(ma, __uint_as_float(sv[c0 + y]), __uint_as_float(sv[c0 + y + 1]));
+                  mb = fmax3(mb, __uint_as_float(sv[c0 + y + 2]), __uint_as_float(sv[c0 + y + 3]));
+                } else {
+                  ma = fmin3(ma, __uint_as_float(sv[c0 + y]), __uint_as_float(sv[c0 + y + 1]));
+                  mb = fmin3(mb, __uint_as_float(sv[c0 + y + 2]), __uint_as_float(sv[c0 + y + 3]));
+                }
+              }
             }
           }
           const float m = kPosScale ? fmaxf(ma, mb) : fminf(ma, mb);
@@ -484,33 +484,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = mx;
         }
         const float m_use = m_run == -INFINITY ? 0.f : m_run;
-        // pass 2: exp2, row sum, bf16 packing; P_X overwrites the first nk/2
-        // columns of S_X, which pass 2 has already read (chunk k writes columns
-        // [16k, 16k+16), inside S chunks 0..k/2; the load in flight is chunk k+1)
         {
           const uint64_t sl2x2 = f32x2(__float_as_uint(p.sl2), __float_as_uint(p.sl2));
           const uint64_t nm2 = f32x2(__float_as_uint(-m_use), __float_as_uint(-m_use));
           uint64_t acc0 = 0, acc1 = 0;  // packed row sums (+0.0f bit patterns)
-          uint32_t buf[2][32];
-          tmem_ld32(sbase, buf[0]);
 #pragma unroll
-          for (int k = 0; k < kBlockKeys / 32; ++k) {
-            const int c0 = 32 * k;
+          for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
             if (c0 < nk) {
-              tmem_wait_ld();
-              if (c0 + 32 < nk) tmem_ld32(sbase + c0 + 32, buf[(k + 1) & 1]);
-              const uint32_t(&rr)[32] = buf[k & 1];
-              const bool whole = c0 >= wlo && c0 + 31 <= whi;
               uint32_t pk[16];
 #pragma unroll
               for (int y = 0; y < 32; y += 2) {
+                // masked scores are already +-inf, so exp2 gives exactly 0
                 float t0, t1;
-                f32x2_split(ffma2(f32x2(rr[y], rr[y + 1]), sl2x2, nm2), t0, t1);
-                float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
-                if (!whole) {
-                  if (c0 + y < lo_c || c0 + y > hi_c) e0 = 0.f;
-                  if (c0 + y + 1 < lo_c || c0 + y + 1 > hi_c) e1 = 0.f;
-                }
+                f32x2_split(ffma2(f32x2(sv[c0 + y], sv[c0 + y + 1]), sl2x2, nm2), t0, t1);
+                const float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
                 const uint64_t e2 = f32x2(__float_as_uint(e0), __float_as_uint(e1));
                 if ((y >> 1) & 1) acc1 = fadd2(acc1, e2); else acc0 = fadd2(acc0, e2);
                 pk[y >> 1] = pack_bf16x2(e0, e1);

@@ -100,10 +100,21 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk16) {
   return (uint32_t)(half * kHalfTile + row * 128 + ((c ^ (row & 7)) << 4));
 }
 
+// UMMA descriptor offsets (in the descriptor's 16-byte units) of k-step k
+// (16 bf16 of K) inside a 128-row tile stored as two 128B-swizzled halves:
+// K-major operands advance 32 bytes inside a half, then jump to the next half;
+// MN-major operands (K along the rows) advance 16 rows = 2048 bytes.
+__host__ __device__ constexpr uint64_t kmaj_step(int k) {
+  return (uint64_t)(((k >> 2) * kHalfTile + (k & 3) * 32) >> 4);
+}
+__host__ __device__ constexpr uint64_t mnmaj_step(int k) { return (uint64_t)((k * 2048) >> 4); }
+__host__ __device__ constexpr uint64_t desc_bytes(uint32_t bytes) { return (uint64_t)(bytes >> 4); }
+
 // Bounded wait whose outcome is the same for the whole warp, so that a warp
 // never splits around warp-collective tcgen05.ld / tcgen05.st.
-__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort, int32_t *status) {
-  const bool ok = mbar_wait(bar, parity, abort, status);
+__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort, int32_t *status,
+                                          uint32_t spin = 4096) {
+  const bool ok = mbar_wait(bar, parity, abort, status, kWaitLimitNs, spin);
   return __all_sync(0xffffffffu, ok);
 }
 
