@@ -59,7 +59,7 @@ struct DqParams {
   int32_t *status;
   const __nv_bfloat16 *out;  // forward output (for Delta)
   const float *lse;
-  float2 *rowstat;           // [ntiles][128]: (lse * log2e, Delta) per tile row
+  float *rowstat;            // [ntiles][2][128]: -lse*log2e, then Delta, per tile row
   __nv_bfloat16 *dq;         // direct stores for poisoned calls / tiles without keys
   float sl2, scale;
 };
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i = t.i0 + pq;
       const RowIv iv = row_interval(Q.sstart, t.b, Q.S, i, Q.W, Q.m);
       const size_t lrow = ((size_t)t.b * Q.H + head) * Q.S + i;
-      float2 *rs = p.rowstat + tile_linear(Q, t) * kRows;
+      float *rs = p.rowstat + tile_linear(Q, t) * 2 * kRows;
       if (poisoned || nb == 0) {
         if (i < Q.S) {
           const float v = poisoned ? __int_as_float(0x7fc00000) : 0.f;
@@ -278,7 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kHeadDim / 8; ++c) grow[c] = make_uint4(w2, w2, w2, w2);
         }
-        rs[r] = make_float2(0.f, 0.f);
+        rs[r] = 0.f;
+        rs[kRows + r] = 0.f;
         continue;
       }
       // Delta = <dO, out> for this row (dO from the staged tile)
@@ -299,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         lse2 = p.lse[lrow] * kLog2e;
       }
-      rs[r] = make_float2(lse2, delta);
+      rs[r] = -lse2;
+      rs[kRows + r] = delta;
       mbar_arrive(&bars.qd_empty);
       for (int j = 0; j < nb; ++j, ++gb) {
         bool comp;
@@ -413,22 +415,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 // kernel 2: dkv / dckv partials
 // ---------------------------------------------------------------------------
 namespace dkk {
-constexpr int kStages = 2;
-constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256, kColP = 384, kColDS = 448;
-constexpr int kTmemCols = 512;
-// stage: Q tile | dO tile | rowstat (128 x float2) | intervals (128 x int2)
-constexpr int kStageBytes = 2 * kTile + 1024 + 1024;
+// A query tile is processed as two 64-row sub-tiles.  Shared memory holds a
+// sub-tile as one 128-row operand R = [Q_sub ; dO_sub] (64 rows each, per
+// 64-column half), so a single N = 128 MMA K R^T yields S^T (columns 0-63) and
+// dP^T (columns 64-127) of the sub-tile.
+constexpr int kStages = 2;                 // query tiles in flight
+constexpr int kSubBytes = kTile;           // one 128-row operand R (two halves)
+constexpr int kHalfRows = 64;              // rows of Q_sub (and of dO_sub) per half
+constexpr int kOffRowstat = 2 * kSubBytes; // -lse*log2e [128] then Delta [128]
+constexpr int kOffIv = kOffRowstat + 1024; // per-position key interval (int2)
+constexpr int kStageBytes = kOffIv + 1024;
 constexpr int kOffK = 0, kOffStage = kTile;
 constexpr int kSmemBytes = kOffStage + kStages * kStageBytes + 1024;
+// TMEM: two [S^T | dP^T] buffers (P^T and dS^T overwrite their first 64
+// columns as packed bf16), then the fp32 dkv accumulator
+constexpr uint32_t kColAcc = 256;
+constexpr int kTmemCols = 512;
+__host__ __device__ constexpr uint32_t col_buf(uint32_t g) { return (g & 1u) * 128u; }
 }  // namespace dkk
 
 struct DkvParams {
   QTiling qt;
   int32_t *status;
-  const float2 *rowstat;
+  const float *rowstat;
   __nv_bfloat16 *dkv;
   float *partial;  // [kSplit][B][Sc_pad][D] fp32
   int nkb_raw, nkb_comp, Sc_pad;
+  int sub_pq, sub_hg;  // TMA box of a 64-row sub-tile: positions x heads
   long long nitems;
   float sl2, scale;
 };
@@ -473,15 +486,15 @@ __device__ __forceinline__ void item_of(const DkvParams &p, long long u, Item &i
 struct DkvBars {
   uint64_t k_full, k_empty;
   uint64_t st_full[dkk::kStages], st_empty[dkk::kStages];
-  uint64_t s_full, s_free;
-  uint64_t p_full, acc_done;
+  uint64_t s_full[2], p_full[2];  // per TMEM buffer
+  uint64_t acc_full, acc_free;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-    hca_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+    hca_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_qs, const __grid_constant__ CUtensorMap map_dos,
                        const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_ckv,
                        const DkvParams p) {
   using namespace dkk;
@@ -499,10 +512,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.st_full[s], 1);
       mbar_init(&bars.st_empty[s], 1);
     }
-    mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.s_free, kSoftmaxThreads);
-    mbar_init(&bars.p_full, kSoftmaxThreads);
-    mbar_init(&bars.acc_done, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars.s_full[x], 1);
+      mbar_init(&bars.p_full[x], kSoftmaxThreads);
+    }
+    mbar_init(&bars.acc_full, 1);
+    mbar_init(&bars.acc_free, kSoftmaxThreads);
     mbar_init(&bars.drain, 1);
     bars.abort = 0;
     fence_mbar_init();
@@ -521,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 4) {
     // ------------------------------------------------------------ TMA
     uint32_t gq = 0, iw = 0;
-    int last_par[kStages] = {-1, -1};
+    uint32_t issued = 0;  // bit s: stage loaded at least once; bit 8+s: parity of its last load
     int k_par = -1;
     bool ok = !poisoned;
     for (long long u = blockIdx.x; ok && u < p.nitems; u += gridDim.x) {
@@ -549,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
         // per-position key intervals of this query tile, for this key kind
-        int2 *ivs = reinterpret_cast<int2 *>(st + 2 * kTile + 1024);
+        int2 *ivs = reinterpret_cast<int2 *>(st + kOffIv);
         for (int q = lane; q < Q.Pq; q += 32) {
           RowIv iv = row_interval(Q.sstart, it.b, Q.S, tq * Q.Pq + q, Q.W, Q.m);
           int lo = 1, hi = 0;
@@ -563,18 +578,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           const int c2 = it.b * Q.H + g * Q.HG;
           const int i0 = tq * Q.Pq;
-          mbar_arrive_expect_tx(&bars.st_full[s], 2 * kTile + 1024);
-          tma_load_3d(&map_q, &bars.st_full[s], st, 0, i0, c2);
-          tma_load_3d(&map_q, &bars.st_full[s], st + kHalfTile, 64, i0, c2);
-          tma_load_3d(&map_do, &bars.st_full[s], st + kTile, 0, i0, c2);
-          tma_load_3d(&map_do, &bars.st_full[s], st + kTile + kHalfTile, 64, i0, c2);
+          mbar_arrive_expect_tx(&bars.st_full[s], 2 * kSubBytes + 1024);
+#pragma unroll
+          for (int sub = 0; sub < 2; ++sub) {
+            // rows [64 sub, 64 sub + 64) of the tile: a head range when HG >= 2,
+            // a position range when one head fills the tile
+            const int pos = p.sub_hg == Q.HG ? i0 + sub * p.sub_pq : i0;
+            const int hd = p.sub_hg == Q.HG ? c2 : c2 + sub * p.sub_hg;
+            uint8_t *r0 = st + sub * kSubBytes;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              tma_load_3d(&map_qs, &bars.st_full[s], r0 + h * kHalfTile, 64 * h, pos, hd);
+              tma_load_3d(&map_dos, &bars.st_full[s], r0 + h * kHalfTile + kHalfRows * 128, 64 * h, pos, hd);
+            }
+          }
           const long long tl = ((long long)it.b * Q.groups + g) * Q.ntq + tq;
           asm volatile(
               "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                  smem_u32(st + 2 * kTile)),
-              "l"(reinterpret_cast<uint64_t>(p.rowstat + tl * kRows)), "r"(1024), "r"(smem_u32(&bars.st_full[s]))
+                  smem_u32(st + kOffRowstat)),
+              "l"(reinterpret_cast<uint64_t>(p.rowstat + tl * 2 * kRows)), "r"(1024),
+              "r"(smem_u32(&bars.st_full[s]))
               : "memory");
-          last_par[s] = (gq / kStages) & 1;
+          issued = (issued | (1u << s)) & ~(1u << (8 + s));
+          issued |= ((gq / kStages) & 1u) << (8 + s);
         }
         __syncwarp();
       }
@@ -583,15 +609,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && !poisoned && lane == 0) {
       volatile int never = 0;
       for (int s = 0; s < kStages; ++s)
-        if (last_par[s] >= 0) mbar_wait(&bars.st_full[s], last_par[s], &never, p.status, 100000000ull);
+        if (issued & (1u << s)) mbar_wait(&bars.st_full[s], (issued >> (8 + s)) & 1u, &never, p.status, 100000000ull);
       if (k_par >= 0) mbar_wait(&bars.k_full, k_par, &never, p.status, 100000000ull);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA
     const uint64_t dK = smem_desc_sw128(smem_u32(smem + kOffK), 16, 1024);
-    const uint64_t dS0 = smem_desc_sw128(smem_u32(smem + kOffStage), 16, 1024);          // K-major view of stage 0
-    const uint64_t dM0 = smem_desc_sw128(smem_u32(smem + kOffStage), kHalfTile, 1024);   // MN-major view of stage 0
-    uint32_t gq = 0, iw = 0;
+    const uint64_t dR0 = smem_desc_sw128(smem_u32(smem + kOffStage), 16, 1024);          // R, K-major
+    const uint64_t dM0 = smem_desc_sw128(smem_u32(smem + kOffStage), kHalfTile, 1024);   // R rows, MN-major
+    const uint32_t id_sd = idesc_bf16_f32(kRows, kRows, false, false);
+    const uint32_t id_acc = idesc_bf16_f32(kRows, kHeadDim, false, true);
+    uint32_t gq = 0, gs = 0, iw = 0;  // query tiles, sub-tiles and items with work so far
     bool ok = !poisoned, issued = false;
     for (long long u = blockIdx.x; ok && u < p.nitems; u += gridDim.x) {
       Item it;
@@ -599,52 +627,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nq = (it.tq_hi - it.tq_lo) * per_tile;
       if (nq <= 0) continue;
       if (lane == 0) {
+        const int nsub = 2 * nq;
         ok = mbar_wait(&bars.k_full, iw & 1, abort_flag, p.status);
-        const uint32_t id_s = idesc_bf16_f32(kRows, kRows, false, false);
-        const uint32_t id_acc = idesc_bf16_f32(kRows, kHeadDim, false, true);
-        auto issue_s = [&](uint32_t g) -> bool {
-          const int s = g % kStages;
-          if (!mbar_wait(&bars.st_full[s], (g / kStages) & 1, abort_flag, p.status)) return false;
-          if (g > 0 && !mbar_wait(&bars.s_free, (g - 1) & 1, abort_flag, p.status)) return false;
+        // S^T | dP^T of sub-tile v (item-local), into TMEM buffer of global sub-tile gs+v
+        auto issue_sd = [&](int v) -> bool {
+          const uint32_t qg = gq + v / 2;
+          const int s = qg % kStages;
+          if ((v & 1) == 0 && !mbar_wait(&bars.st_full[s], (qg / kStages) & 1, abort_flag, p.status)) return false;
           tc_fence_after();
-          const uint64_t bq = dS0 + desc_bytes(s * kStageBytes);
-          const uint64_t bdo = bq + desc_bytes(kTile);
+          const uint64_t br = dR0 + desc_bytes(s * kStageBytes + (v & 1) * kSubBytes);
 #pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k) {
-            mma_ss(tmem + kColS, dK + kmaj_step(k), bq + kmaj_step(k), id_s, k > 0);
-            mma_ss(tmem + kColDP, dK + kmaj_step(k), bdo + kmaj_step(k), id_s, k > 0);
-          }
-          mma_commit(&bars.s_full);
+          for (int k = 0; k < kHeadDim / 16; ++k)
+            mma_ss(tmem + col_buf(gs + v), dK + kmaj_step(k), br + kmaj_step(k), id_sd, k > 0);
+          mma_commit(&bars.s_full[(gs + v) & 1]);
+          if (v == nsub - 1) mma_commit(&bars.k_empty);  // the K tile is read by these MMAs only
           issued = true;
           return true;
         };
-        if (ok) ok = issue_s(gq);
-        for (int x = 0; ok && x < nq; ++x) {
-          const uint32_t g = gq + x;
-          if (x + 1 < nq) {
-            ok = issue_s(g + 1);
-            if (!ok) break;
-          }
-          ok = mbar_wait(&bars.p_full, g & 1, abort_flag, p.status);
+        if (ok) ok = issue_sd(0);
+        if (ok) ok = issue_sd(1);
+        for (int v = 0; ok && v < nsub; ++v) {
+          const uint32_t g = gs + v;
+          ok = mbar_wait(&bars.p_full[g & 1], (g >> 1) & 1, abort_flag, p.status);
+          if (ok && v == 0 && iw > 0) ok = mbar_wait(&bars.acc_free, (iw - 1) & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          const int s = g % kStages;
-          const uint64_t mq = dM0 + desc_bytes(s * kStageBytes);
-          const uint64_t mdo = mq + desc_bytes(kTile);
+          const uint32_t qg = gq + v / 2;
+          const int s = qg % kStages;
+          const uint64_t mr = dM0 + desc_bytes(s * kStageBytes + (v & 1) * kSubBytes);
+          const uint64_t mq = mr, mdo = mr + desc_bytes(kHalfRows * 128);
+          const uint32_t buf = tmem + col_buf(g);
 #pragma unroll
-          for (int kk = 0; kk < kRows / 16; ++kk) {
-            // acc += P^T dO  (dO tile as an MN-major B operand)
-            mma_ts(tmem + kColAcc, tmem + kColP + kk * 8, mdo + mnmaj_step(kk), id_acc, (x > 0 || kk > 0) ? 1u : 0u);
-            // acc += (scale dS)^T Q
-            mma_ts(tmem + kColAcc, tmem + kColDS + kk * 8, mq + mnmaj_step(kk), id_acc, 1u);
+          for (int kk = 0; kk < kHalfRows / 16; ++kk) {
+            // acc += P^T dO_sub  and  acc += (scale dS)^T Q_sub
+            mma_ts(tmem + kColAcc, buf + kk * 8, mdo + mnmaj_step(kk), id_acc, (v > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + kColAcc, buf + 32 + kk * 8, mq + mnmaj_step(kk), id_acc, 1u);
           }
-          mma_commit(&bars.st_empty[s]);
-          mma_commit(&bars.acc_done);
+          if (v & 1) mma_commit(&bars.st_empty[s]);
+          if (v + 2 < nsub) {
+            ok = issue_sd(v + 2);
+            if (!ok) break;
+          }
         }
-        if (ok) mma_commit(&bars.k_empty);
+        if (ok) mma_commit(&bars.acc_full);
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       gq += nq;
+      gs += 2 * nq;
       ++iw;
     }
     if (!ok && issued && lane == 0) {
@@ -656,15 +685,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ P^T, dS^T + item epilogue
     const int kr = tid;  // key row == TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    uint32_t gq = 0, acc_waited = 0;
+    const uint64_t sl2x2 = f32x2(__float_as_uint(p.sl2), __float_as_uint(p.sl2));
+    uint32_t gq = 0, gs = 0, iw = 0;
     bool ok = true;
-    auto wait_acc = [&](uint32_t x) -> bool {
-      while (acc_waited <= x) {
-        if (!wait_warp(&bars.acc_done, acc_waited & 1, abort_flag, p.status)) return false;
-        ++acc_waited;
-      }
-      return true;
-    };
     for (long long u = blockIdx.x; ok && u < p.nitems; u += gridDim.x) {
       Item it;
       item_of(p, u, it);
@@ -687,75 +710,101 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      for (int x = 0; x < nq; ++x, ++gq) {
-        const int s = gq % kStages;
-        const uint8_t *st = smem + kOffStage + s * kStageBytes;
-        const float2 *rs = reinterpret_cast<const float2 *>(st + 2 * kTile);
-        const int2 *ivs = reinterpret_cast<const int2 *>(st + 2 * kTile + 1024);
-        if (!wait_warp(&bars.s_full, gq & 1, abort_flag, p.status)) { ok = false; break; }
-        // P^T / dS^T live in TMEM: the previous accumulation must be done
-        if (gq >= 1 && !wait_acc(gq - 1)) { ok = false; break; }
+      const int nsub = 2 * nq;
+      for (int v = 0; v < nsub; ++v) {
+        const uint32_t g = gs + v;
+        const uint32_t qg = gq + v / 2;
+        const uint8_t *st = smem + kOffStage + (qg % kStages) * kStageBytes;
+        const float *rs_nl = reinterpret_cast<const float *>(st + kOffRowstat) + (v & 1) * kHalfRows;
+        const float *rs_d = rs_nl + kRows;
+        const int2 *ivs = reinterpret_cast<const int2 *>(st + kOffIv);
+        if ((v & 1) == 0 &&
+            !wait_warp(&bars.st_full[qg % kStages], (qg / kStages) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_warp(&bars.s_full[g & 1], (g >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-#pragma unroll 1
-        for (int c0 = 0; c0 < kRows; c0 += 32) {
-          uint32_t sr[32], dr[32];
-          tmem_ld32(lane_addr + kColS + c0, sr);
-          tmem_ld32(lane_addr + kColDP + c0, dr);
-          tmem_wait_ld();
-          uint32_t pp[16], dd[16];
-#pragma unroll
-          for (int xx = 0; xx < 32; xx += 2) {
-            float pv[2], dv[2];
-#pragma unroll
-            for (int y = 0; y < 2; ++y) {
-              const int c = c0 + xx + y;
-              const int2 iv = ivs[c % Q.Pq];
-              const float2 st2 = rs[c];
-              const bool vis = key_ok && key >= iv.x && key <= iv.y;
-              const float e = ex2_approx(__uint_as_float(sr[xx + y]) * p.sl2 - st2.x);
-              pv[y] = vis ? e : 0.f;
-              dv[y] = vis ? p.scale * e * (__uint_as_float(dr[xx + y]) - st2.y) : 0.f;
+        const uint32_t base = lane_addr + col_buf(g);
+        uint32_t sv[128];
+        tmem_ld32(base, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        tmem_ld32(base + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        tmem_ld32(base + 64, *reinterpret_cast<uint32_t(*)[32]>(sv + 64));
+        tmem_ld32(base + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 96));
+        // visibility of this key for the 64 columns (query rows) of the sub-tile:
+        // row r = 64 sub + c sits at position r mod Pq
+        uint64_t vis = 0;
+        if (key_ok) {
+          const int row0 = (v & 1) * kHalfRows;
+          if (Q.Pq <= kHalfRows) {
+            uint64_t pat = 0;
+            for (int q = 0; q < Q.Pq; ++q) {
+              const int2 iv = ivs[q];
+              if (key >= iv.x && key <= iv.y) pat |= 1ull << q;
             }
-            pp[xx / 2] = pack_bf16x2(pv[0], pv[1]);
-            dd[xx / 2] = pack_bf16x2(dv[0], dv[1]);
+            for (int w = Q.Pq; w < kHalfRows; w *= 2) pat |= pat << w;
+            vis = pat;
+          } else {
+            for (int c = 0; c < kHalfRows; ++c) {
+              const int2 iv = ivs[(row0 + c) % Q.Pq];
+              if (key >= iv.x && key <= iv.y) vis |= 1ull << c;
+            }
           }
-          tmem_st16(lane_addr + kColP + c0 / 2, pp);
-          tmem_st16(lane_addr + kColDS + c0 / 2, dd);
         }
+        tmem_wait_ld();
+        uint32_t pk[32], dk[32];
+        const float scale = p.scale;
+#pragma unroll
+        for (int c = 0; c < kHalfRows; c += 2) {
+          const float2 nl = *reinterpret_cast<const float2 *>(rs_nl + c);
+          const float2 dl = *reinterpret_cast<const float2 *>(rs_d + c);
+          float t0, t1;
+          f32x2_split(ffma2(f32x2(sv[c], sv[c + 1]), sl2x2, f32x2(__float_as_uint(nl.x), __float_as_uint(nl.y))),
+                      t0, t1);
+          float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
+          if (!((vis >> c) & 1ull)) e0 = 0.f;
+          if (!((vis >> (c + 1)) & 1ull)) e1 = 0.f;
+          const float d0 = scale * e0 * (__uint_as_float(sv[64 + c]) - dl.x);
+          const float d1 = scale * e1 * (__uint_as_float(sv[64 + c + 1]) - dl.y);
+          pk[c >> 1] = pack_bf16x2(e0, e1);
+          dk[c >> 1] = pack_bf16x2(d0, d1);
+        }
+        tmem_st32(base, pk);
+        tmem_st32(base + 32, dk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars.s_free);
-        mbar_arrive(&bars.p_full);
+        mbar_arrive(&bars.p_full[g & 1]);
       }
       if (!ok) break;
       // ---------------- item epilogue: the accumulator row of this key
-      if (!wait_acc(gq - 1)) { ok = false; break; }
+      if (!wait_warp(&bars.acc_full, iw & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
-      uint32_t o[32];
+      uint32_t o[128];
+      tmem_ld32(lane_addr + kColAcc, *reinterpret_cast<uint32_t(*)[32]>(o));
+      tmem_ld32(lane_addr + kColAcc + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+      tmem_ld32(lane_addr + kColAcc + 64, *reinterpret_cast<uint32_t(*)[32]>(o + 64));
+      tmem_ld32(lane_addr + kColAcc + 96, *reinterpret_cast<uint32_t(*)[32]>(o + 96));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bars.acc_free);  // the next item's accumulation may start
+      if (it.comp) {
+        float4 *dst = reinterpret_cast<float4 *>(prow);
 #pragma unroll
-      for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
-        tmem_ld32(lane_addr + kColAcc + c0, o);
-        tmem_wait_ld();
-        if (it.comp) {
-          float4 *dst = reinterpret_cast<float4 *>(prow + c0);
+        for (int x = 0; x < 32; ++x)
+          dst[x] = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]), __uint_as_float(o[4 * x + 2]),
+                               __uint_as_float(o[4 * x + 3]));
+      } else if (key_ok) {
+        uint4 *dst = reinterpret_cast<uint4 *>(drow);
 #pragma unroll
-          for (int x = 0; x < 8; ++x)
-            dst[x] = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]), __uint_as_float(o[4 * x + 2]),
-                                 __uint_as_float(o[4 * x + 3]));
-        } else if (key_ok) {
-          uint4 *dst = reinterpret_cast<uint4 *>(drow + c0);
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[8 * x + 0]), __uint_as_float(o[8 * x + 1]));
-            v.y = pack_bf16x2(__uint_as_float(o[8 * x + 2]), __uint_as_float(o[8 * x + 3]));
-            v.z = pack_bf16x2(__uint_as_float(o[8 * x + 4]), __uint_as_float(o[8 * x + 5]));
-            v.w = pack_bf16x2(__uint_as_float(o[8 * x + 6]), __uint_as_float(o[8 * x + 7]));
-            dst[x] = v;
-          }
+        for (int x = 0; x < 16; ++x) {
+          uint4 w4;
+          w4.x = pack_bf16x2(__uint_as_float(o[8 * x + 0]), __uint_as_float(o[8 * x + 1]));
+          w4.y = pack_bf16x2(__uint_as_float(o[8 * x + 2]), __uint_as_float(o[8 * x + 3]));
+          w4.z = pack_bf16x2(__uint_as_float(o[8 * x + 4]), __uint_as_float(o[8 * x + 5]));
+          w4.w = pack_bf16x2(__uint_as_float(o[8 * x + 6]), __uint_as_float(o[8 * x + 7]));
+          dst[x] = w4;
         }
       }
-      tc_fence_before();
+      gq += nq;
+      gs += 2 * nq;
+      ++iw;
     }
   }
   tc_fence_before();
@@ -790,7 +839,7 @@ __global__ void hca_bwd_reduce_kernel(const float *__restrict__ partial, __nv_bf
   }
 }
 
-size_t rowstat_bytes(const QTiling &q) { return align_up((size_t)q.ntiles * kRows * sizeof(float2)); }
+size_t rowstat_bytes(const QTiling &q) { return align_up((size_t)q.ntiles * 2 * kRows * sizeof(float)); }
 
 int sc_pad(int Sc) { return (Sc + kBlockKeys - 1) / kBlockKeys * kBlockKeys; }
 
@@ -808,12 +857,18 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   const QTiling q = make_qtiling(a.sstart, a.B, a.H, a.S, a.W, a.m);
   const int Spad = sc_pad(q.Sc);
   char *ws = static_cast<char *>(a.scratch);
-  float2 *rowstat = reinterpret_cast<float2 *>(ws);
+  float *rowstat = reinterpret_cast<float *>(ws);
   float *partial = reinterpret_cast<float *>(ws + rowstat_bytes(q));
-  CUtensorMap mq, mdo, mkv, mckv, mdq;
+  // dkv kernel: a 64-row half of a query tile is a head range when HG >= 2,
+  // a position range when one head fills the tile
+  const int sub_hg = q.HG >= 2 ? q.HG / 2 : 1;
+  const int sub_pq = q.HG >= 2 ? q.Pq : q.Pq / 2;
+  CUtensorMap mq, mdo, mkv, mckv, mdq, mqs, mdos;
   if (!make_map_bf16(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mdo, a.dout, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mdq, a.dq, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mqs, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, sub_pq, sub_hg) ||
+      !make_map_bf16(&mdos, a.dout, kHeadDim, a.S, (uint64_t)a.B * a.H, sub_pq, sub_hg) ||
       !make_map_bf16(&mkv, a.kv, kHeadDim, a.S, a.B, kBlockKeys, 1) ||
       !make_map_bf16(&mckv, a.ckv, kHeadDim, q.Sc, a.B, kBlockKeys, 1))
     return cudaErrorInvalidValue;
@@ -858,13 +913,15 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   kp.nkb_raw = (a.S + kBlockKeys - 1) / kBlockKeys;
   kp.nkb_comp = (q.Sc + kBlockKeys - 1) / kBlockKeys;
   kp.Sc_pad = Spad;
+  kp.sub_pq = sub_pq;
+  kp.sub_hg = sub_hg;
   kp.nitems = (long long)a.B * kp.nkb_comp * kSplit + (long long)a.B * kp.nkb_raw;
   kp.sl2 = sl2;
   kp.scale = a.scale;
   const long long g2 = kp.nitems < sms ? kp.nitems : sms;
   {
     ProfScope prof(kKBwdDkv, st);
-    hca_bwd_dkv_kernel<<<(unsigned)g2, kThreads, dkk::kSmemBytes, st>>>(mq, mdo, mkv, mckv, kp);
+    hca_bwd_dkv_kernel<<<(unsigned)g2, kThreads, dkk::kSmemBytes, st>>>(mqs, mdos, mkv, mckv, kp);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;
