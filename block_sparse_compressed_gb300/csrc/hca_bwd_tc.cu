@@ -437,6 +437,7 @@ __host__ __device__ constexpr uint32_t col_buf(uint32_t g) { return (g & 1u) * 1
 struct DkvParams {
   QTiling qt;
   int32_t *status;
+  int32_t *next_item;  // work counter (zeroed before the launch)
   const float *rowstat;
   __nv_bfloat16 *dkv;
   float *partial;  // [kSplit][B][Sc_pad][D] fp32
@@ -483,7 +484,11 @@ __device__ __forceinline__ void item_of(const DkvParams &p, long long u, Item &i
   }
 }
 
+constexpr int kItemRing = 4;
+
 struct DkvBars {
+  uint64_t item_full[kItemRing], item_empty[kItemRing];  // dynamic item queue
+  long long item[kItemRing];
   uint64_t k_full, k_empty;
   uint64_t st_full[dkk::kStages], st_empty[dkk::kStages];
   uint64_t s_full[2], p_full[2];  // per TMEM buffer
@@ -506,6 +511,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const QTiling &Q = p.qt;
 
   if (tid == 0) {
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(&bars.item_full[i], 1);
+      mbar_init(&bars.item_empty[i], 1 + kSoftmaxThreads);
+    }
     mbar_init(&bars.k_full, 1);
     mbar_init(&bars.k_empty, 1);
     for (int s = 0; s < kStages; ++s) {
@@ -538,8 +547,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t gq = 0, iw = 0;
     uint32_t issued = 0;  // bit s: stage loaded at least once; bit 8+s: parity of its last load
     int k_par = -1;
-    bool ok = !poisoned;
-    for (long long u = blockIdx.x; ok && u < p.nitems; u += gridDim.x) {
+    bool ok = true;
+    // Items are handed out dynamically (largest first) through a global
+    // counter; this warp fetches them and publishes each to the other roles.
+    for (uint32_t k = 0; ok; ++k) {
+      const int slot = k % kItemRing;
+      long long u = -1;
+      if (lane == 0) {
+        if (k >= (uint32_t)kItemRing)
+          ok = mbar_wait(&bars.item_empty[slot], ((k / kItemRing) - 1) & 1, abort_flag, p.status);
+        if (ok) {
+          u = atomicAdd(p.next_item, 1);
+          if (u >= p.nitems) u = -1;
+          bars.item[slot] = u;
+          mbar_arrive(&bars.item_full[slot]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (!ok || u < 0) break;
+      if (poisoned) continue;
       Item it;
       item_of(p, u, it);
       const int nq = (it.tq_hi - it.tq_lo) * per_tile;
@@ -620,8 +647,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t id_sd = idesc_bf16_f32(kRows, kRows, false, false);
     const uint32_t id_acc = idesc_bf16_f32(kRows, kHeadDim, false, true);
     uint32_t gq = 0, gs = 0, iw = 0;  // query tiles, sub-tiles and items with work so far
-    bool ok = !poisoned, issued = false;
-    for (long long u = blockIdx.x; ok && u < p.nitems; u += gridDim.x) {
+    bool ok = true, issued = false;
+    for (uint32_t kq = 0; ok; ++kq) {
+      const int slot = kq % kItemRing;
+      long long u = -1;
+      if (lane == 0) {
+        ok = mbar_wait(&bars.item_full[slot], (kq / kItemRing) & 1, abort_flag, p.status);
+        if (ok) {
+          u = bars.item[slot];
+          mbar_arrive(&bars.item_empty[slot]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (!ok || u < 0) break;
+      if (poisoned) continue;
       Item it;
       item_of(p, u, it);
       const int nq = (it.tq_hi - it.tq_lo) * per_tile;
@@ -688,7 +728,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t sl2x2 = f32x2(__float_as_uint(p.sl2), __float_as_uint(p.sl2));
     uint32_t gq = 0, gs = 0, iw = 0;
     bool ok = true;
-    for (long long u = blockIdx.x; ok && u < p.nitems; u += gridDim.x) {
+    for (uint32_t kq = 0; ok; ++kq) {
+      const int slot = kq % kItemRing;
+      if (!wait_warp(&bars.item_full[slot], (kq / kItemRing) & 1, abort_flag, p.status)) { ok = false; break; }
+      const long long u = *(volatile long long *)&bars.item[slot];
+      mbar_arrive(&bars.item_empty[slot]);
+      if (u < 0) break;
       Item it;
       item_of(p, u, it);
       const int nq = (it.tq_hi - it.tq_lo) * per_tile;
@@ -913,12 +958,15 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   kp.nkb_raw = (a.S + kBlockKeys - 1) / kBlockKeys;
   kp.nkb_comp = (q.Sc + kBlockKeys - 1) / kBlockKeys;
   kp.Sc_pad = Spad;
+  kp.next_item = a.status_rw + 16;  // in the workspace header (64 bytes past the status word)
   kp.sub_pq = sub_pq;
   kp.sub_hg = sub_hg;
   kp.nitems = (long long)a.B * kp.nkb_comp * kSplit + (long long)a.B * kp.nkb_raw;
   kp.sl2 = sl2;
   kp.scale = a.scale;
   const long long g2 = kp.nitems < sms ? kp.nitems : sms;
+  e = cudaMemsetAsync(kp.next_item, 0, sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
   {
     ProfScope prof(kKBwdDkv, st);
     hca_bwd_dkv_kernel<<<(unsigned)g2, kThreads, dkk::kSmemBytes, st>>>(mqs, mdos, mkv, mckv, kp);
