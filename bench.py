@@ -221,10 +221,13 @@ def cpu_baseline(w, q, kv, ckv, dout, target_s: float):
         oracle.bwd(qc, kvc, ckvc, None, dc, w.W, w.m, w.scale, rows=(lo, S))
         return time.perf_counter() - t0, pairs_in(lo, S)
 
+    # grow the sample until it takes about target_s (the fixed cost of a call
+    # makes the first small samples a poor predictor)
     R = 16
     dt, pairs = run(R)
-    R = int(max(16, min(S, R * target_s / max(dt, 1e-3) * 0.9)))
-    dt, pairs = run(R)
+    while dt < 0.6 * target_s and R < S:
+        R = int(min(S, R * min(8.0, max(1.5, 0.9 * target_s / max(dt, 1e-3)))))
+        dt, pairs = run(R)
     flops = 14 * w.D * pairs
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"fp64 oracle fwd+bwd over query rows [{S - R},{S}) of the workload "
