@@ -169,73 +169,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA
+    // Whole warp, warp-uniform values, one elect.sync lane issues (cheap
+    // tcgen05.mma issue from uniform registers; see the forward kernel).
     const uint64_t dQ = smem_desc_sw128(smem_u32(smem + kOffQ), 16, 1024);
     const uint64_t dDO = smem_desc_sw128(smem_u32(smem + kOffDO), 16, 1024);
     const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + kOffKV), 16, 1024);
     const uint64_t dV0 = smem_desc_sw128(smem_u32(smem + kOffKV), kHalfTile, 1024);
+    const uint32_t id_dq = idesc_bf16_f32(kRows, kHeadDim, false, true);
     uint32_t gb = 0, tw = 0;
     bool ok = !poisoned, issued = false;
     for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
       Tile t;
       tile_coords(Q, u, t);
       tile_ranges_warp(Q, t, lane);
+      uniform_tile(t);
       const int nb = t.nraw + t.ncomp;
       if (nb == 0) continue;
-      if (lane == 0) {
-        ok = mbar_wait(&bars.qd_full, tw & 1, abort_flag, p.status);
-        auto issue_sdp = [&](int j, uint32_t g) -> bool {
-          const int s = g % kStages;
-          if (!mbar_wait(&bars.kv_full[s], (g / kStages) & 1, abort_flag, p.status)) return false;
-          if (g > 0 && !mbar_wait(&bars.s_free, (g - 1) & 1, abort_flag, p.status)) return false;
-          tc_fence_after();
-          bool comp;
-          int start, n;
-          block_of(t, j, comp, start, n);
-          const int nk = (n + 15) & ~15;
-          const uint32_t idesc = idesc_bf16_f32(kRows, nk, false, false);
-          const uint64_t bk = dK0 + desc_bytes(s * kTile);
+      auto issue_sdp = [&](int j, uint32_t g, bool last_q_use) -> bool {
+        const int s = g % kStages;
+        if (!wait_warp(&bars.kv_full[s], (g / kStages) & 1, abort_flag, p.status)) return false;
+        if (g > 0 && !wait_warp(&bars.s_free, (g - 1) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        bool comp;
+        int start, n;
+        block_of(t, j, comp, start, n);
+        const uint32_t idesc = idesc_bf16_f32(kRows, (n + 15) & ~15, false, false);
+        const uint64_t bk = dK0 + desc_bytes(s * kTile);
+        if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < kHeadDim / 16; ++k) {
             mma_ss(tmem + kColS, dQ + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
             mma_ss(tmem + kColDP, dDO + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
           }
           mma_commit(&bars.s_full);
-          issued = true;
-          return true;
-        };
-        if (ok) ok = issue_sdp(0, gb);
-        if (ok && nb == 1) mma_commit(&bars.qd_empty);
-        for (int j = 0; ok && j < nb; ++j) {
-          const uint32_t g = gb + j;
-          if (j + 1 < nb) {
-            ok = issue_sdp(j + 1, g + 1);
-            if (!ok) break;
-            if (j + 1 == nb - 1) mma_commit(&bars.qd_empty);
-          }
-          ok = mbar_wait(&bars.ds_full, g & 1, abort_flag, p.status);
+          if (last_q_use) mma_commit(&bars.qd_empty);
+        }
+        __syncwarp();
+        issued = true;
+        return true;
+      };
+      ok = wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status);
+      if (ok) ok = issue_sdp(0, gb, nb == 1);
+      for (int j = 0; ok && j < nb; ++j) {
+        const uint32_t g = gb + j;
+        if (j + 1 < nb) {
+          ok = issue_sdp(j + 1, g + 1, j + 1 == nb - 1);
           if (!ok) break;
-          tc_fence_after();
-          bool comp;
-          int start, n;
-          block_of(t, j, comp, start, n);
-          const int nk = (n + 15) & ~15;
-          const int s = g % kStages;
-          const uint64_t bv = dV0 + desc_bytes(s * kTile);
-          const uint32_t idesc = idesc_bf16_f32(kRows, kHeadDim, false, true);
-          for (int kk = 0; kk < nk / 16; ++kk)
-            mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, bv + mnmaj_step(kk), idesc, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        ok = wait_warp(&bars.ds_full, g & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        bool comp;
+        int start, n;
+        block_of(t, j, comp, start, n);
+        const int nks = (n + 15) >> 4;
+        const int s = g % kStages;
+        const uint64_t bv = dV0 + desc_bytes(s * kTile);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < kBlockKeys / 16; ++kk)
+            if (kk < nks)
+              mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, bv + mnmaj_step(kk), id_dq, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars.kv_empty[s]);
           mma_commit(&bars.dq_done);
         }
+        __syncwarp();
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       gb += nb;
       ++tw;
     }
-    if (!ok && issued && lane == 0) {
+    if (!ok && issued) {
       volatile int never = 0;
-      mma_commit(&bars.drain);
-      mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+      if (elect_one()) mma_commit(&bars.drain);
+      __syncwarp();
+      if (lane == 0) mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ dS + epilogue
@@ -666,37 +674,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       item_of(p, u, it);
       const int nq = (it.tq_hi - it.tq_lo) * per_tile;
       if (nq <= 0) continue;
-      if (lane == 0) {
-        const int nsub = 2 * nq;
-        ok = mbar_wait(&bars.k_full, iw & 1, abort_flag, p.status);
-        // S^T | dP^T of sub-tile v (item-local), into TMEM buffer of global sub-tile gs+v
-        auto issue_sd = [&](int v) -> bool {
-          const uint32_t qg = gq + v / 2;
-          const int s = qg % kStages;
-          if ((v & 1) == 0 && !mbar_wait(&bars.st_full[s], (qg / kStages) & 1, abort_flag, p.status)) return false;
-          tc_fence_after();
-          const uint64_t br = dR0 + desc_bytes(s * kStageBytes + (v & 1) * kSubBytes);
+      // whole warp on warp-uniform values; one elect.sync lane issues
+      const int nsub = 2 * nq;
+      ok = wait_warp(&bars.k_full, iw & 1, abort_flag, p.status);
+      // S^T | dP^T of sub-tile v (item-local), into TMEM buffer of global sub-tile gs+v
+      auto issue_sd = [&](int v) -> bool {
+        const uint32_t qg = gq + v / 2;
+        const int s = qg % kStages;
+        if ((v & 1) == 0 && !wait_warp(&bars.st_full[s], (qg / kStages) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint64_t br = dR0 + desc_bytes(s * kStageBytes + (v & 1) * kSubBytes);
+        const uint32_t d = tmem + col_buf(gs + v);
+        if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k)
-            mma_ss(tmem + col_buf(gs + v), dK + kmaj_step(k), br + kmaj_step(k), id_sd, k > 0);
+          for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, dK + kmaj_step(k), br + kmaj_step(k), id_sd, k > 0);
           mma_commit(&bars.s_full[(gs + v) & 1]);
           if (v == nsub - 1) mma_commit(&bars.k_empty);  // the K tile is read by these MMAs only
-          issued = true;
-          return true;
-        };
-        if (ok) ok = issue_sd(0);
-        if (ok) ok = issue_sd(1);
-        for (int v = 0; ok && v < nsub; ++v) {
-          const uint32_t g = gs + v;
-          ok = mbar_wait(&bars.p_full[g & 1], (g >> 1) & 1, abort_flag, p.status);
-          if (ok && v == 0 && iw > 0) ok = mbar_wait(&bars.acc_free, (iw - 1) & 1, abort_flag, p.status);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t qg = gq + v / 2;
-          const int s = qg % kStages;
-          const uint64_t mr = dM0 + desc_bytes(s * kStageBytes + (v & 1) * kSubBytes);
-          const uint64_t mq = mr, mdo = mr + desc_bytes(kHalfRows * 128);
-          const uint32_t buf = tmem + col_buf(g);
+        }
+        __syncwarp();
+        issued = true;
+        return true;
+      };
+      if (ok) ok = issue_sd(0);
+      if (ok) ok = issue_sd(1);
+      for (int v = 0; ok && v < nsub; ++v) {
+        const uint32_t g = gs + v;
+        ok = wait_warp(&bars.p_full[g & 1], (g >> 1) & 1, abort_flag, p.status);
+        if (ok && v == 0 && iw > 0) ok = wait_warp(&bars.acc_free, (iw - 1) & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qg = gq + v / 2;
+        const int s = qg % kStages;
+        const uint64_t mr = dM0 + desc_bytes(s * kStageBytes + (v & 1) * kSubBytes);
+        const uint64_t mq = mr, mdo = mr + desc_bytes(kHalfRows * 128);
+        const uint32_t buf = tmem + col_buf(g);
+        if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kHalfRows / 16; ++kk) {
             // acc += P^T dO_sub  and  acc += (scale dS)^T Q_sub
@@ -704,22 +716,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(tmem + kColAcc, buf + 32 + kk * 8, mq + mnmaj_step(kk), id_acc, 1u);
           }
           if (v & 1) mma_commit(&bars.st_empty[s]);
-          if (v + 2 < nsub) {
-            ok = issue_sd(v + 2);
-            if (!ok) break;
-          }
+          if (v == nsub - 1) mma_commit(&bars.acc_full);
         }
-        if (ok) mma_commit(&bars.acc_full);
+        __syncwarp();
+        if (v + 2 < nsub) {
+          ok = issue_sd(v + 2);
+          if (!ok) break;
+        }
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       gq += nq;
       gs += 2 * nq;
       ++iw;
     }
-    if (!ok && issued && lane == 0) {
+    if (!ok && issued) {
       volatile int never = 0;
-      mma_commit(&bars.drain);
-      mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+      if (elect_one()) mma_commit(&bars.drain);
+      __syncwarp();
+      if (lane == 0) mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ P^T, dS^T + item epilogue

@@ -111,6 +111,17 @@ __device__ __forceinline__ void pair_block(const Pair &t, int j, bool &comp, int
   block_of(tt, j, comp, start, n);
 }
 
+// Broadcast a pair's ranges from lane 0 so the compiler treats them (and
+// everything derived from them) as warp-uniform.
+__device__ __forceinline__ void uniform_pair(Pair &t) {
+  t.rlo = __shfl_sync(0xffffffffu, t.rlo, 0);
+  t.rhi = __shfl_sync(0xffffffffu, t.rhi, 0);
+  t.clo = __shfl_sync(0xffffffffu, t.clo, 0);
+  t.chi = __shfl_sync(0xffffffffu, t.chi, 0);
+  t.nraw = __shfl_sync(0xffffffffu, t.nraw, 0);
+  t.ncomp = __shfl_sync(0xffffffffu, t.ncomp, 0);
+}
+
 __device__ __forceinline__ void setmaxnreg_inc_softmax() { asm volatile("setmaxnreg.inc.sync.aligned.u32 176;"); }
 __device__ __forceinline__ void setmaxnreg_dec_epilogue() { asm volatile("setmaxnreg.dec.sync.aligned.u32 72;"); }
 __device__ __forceinline__ void setmaxnreg_dec_producer() { asm volatile("setmaxnreg.dec.sync.aligned.u32 88;"); }
@@ -232,85 +243,93 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 13) {
       // ---------------------------------------------------------- MMA
-      // descriptors are built once; an MMA only adds a constant offset
+      // The whole warp runs this loop on warp-uniform values (the pair's
+      // ranges are broadcast from lane 0) and one elect.sync lane issues each
+      // group of MMAs with its commits.  Operands that the compiler can keep
+      // in uniform registers cost ~19 cycles per tcgen05.mma to issue; the
+      // same MMAs issued from a lane-0 branch cost 50-80 cycles, more than
+      // the tensor pipe needs to execute an M=128, N=128, K=16 step (~65).
+      // Descriptors are built once; an MMA only adds a constant offset.
       const uint64_t dq0 = smem_desc_sw128(smem_u32(smem + kOffQ), 16, 1024);
       const uint64_t dq1 = smem_desc_sw128(smem_u32(smem + kOffQ + kTile), 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(smem + kOffKV), 16, 1024);         // K view of stage 0
       const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + kOffKV), kHalfTile, 1024);  // V view of stage 0
+      const uint32_t id_pv = idesc_bf16_f32(kRows, kHeadDim, false, true);
       uint32_t gb = 0, gq = 0, pcnt = 0;
       bool ok = !poisoned, issued = false;
       for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
         Pair t;
         pair_coords(p, u, t);
         pair_ranges_warp(p, t, lane);
+        uniform_pair(t);
         const int nb = t.nraw + t.ncomp;
         if (nb == 0) continue;
-        if (lane == 0) {
-          ok = mbar_wait(&bars.q_full, gq & 1, abort_flag, p.status);
-          auto issue_s = [&](int x, int j, uint32_t g) {
-            bool comp;
-            int start, n;
-            pair_block(t, j, comp, start, n);
-            const int nk = (n + 15) & ~15;
-            const uint32_t idesc = idesc_bf16_f32(kRows, nk, false, false);
-            const uint64_t da = x ? dq1 : dq0;
-            const uint64_t db = dk0 + desc_bytes((g % kStages) * kTile);
+        auto issue_s = [&](int x, int j, uint32_t g, uint64_t *extra) {
+          bool comp;
+          int start, n;
+          pair_block(t, j, comp, start, n);
+          const uint32_t idesc = idesc_bf16_f32(kRows, (n + 15) & ~15, false, false);
+          const uint64_t da = x ? dq1 : dq0;
+          const uint64_t db = dk0 + desc_bytes((g % kStages) * kTile);
+          const uint32_t d = tmem + col_s(x);
+          if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < kHeadDim / 16; ++k)
-              mma_ss(tmem + col_s(x), da + kmaj_step(k), db + kmaj_step(k), idesc, k > 0);
+            for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, da + kmaj_step(k), db + kmaj_step(k), idesc, k > 0);
             mma_commit(&bars.s_full[x]);
-            issued = true;
-          };
-          auto issue_pv = [&](int x, int j, uint32_t g) {
-            bool comp;
-            int start, n;
-            pair_block(t, j, comp, start, n);
-            const int nk = (n + 15) & ~15;
-            const uint64_t db = dv0 + desc_bytes((g % kStages) * kTile);
-            const uint32_t idesc = idesc_bf16_f32(kRows, kHeadDim, false, true);
-            for (int kk = 0; kk < nk / 16; ++kk)
-              mma_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, db + mnmaj_step(kk), idesc, (j > 0 || kk > 0) ? 1u : 0u);
-          };
-          if (ok) ok = mbar_wait(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status);
-          if (ok) {
-            tc_fence_after();
-            issue_s(0, 0, gb);
-            issue_s(1, 0, gb);
-            if (nb == 1) mma_commit(&bars.q_empty);
+            if (extra) mma_commit(extra);
           }
-          for (int j = 0; ok && j < nb; ++j) {
-            const uint32_t g = gb + j;
-            const bool next = j + 1 < nb;
-            for (int x = 0; ok && x < 2; ++x) {
-              ok = mbar_wait(&bars.p_full[x], pcnt & 1, abort_flag, p.status);
-              if (ok && j == 0 && gq > 0) ok = mbar_wait(&bars.o_free[x], (gq - 1) & 1, abort_flag, p.status);
-              if (!ok) break;
-              tc_fence_after();
-              issue_pv(x, j, g);
+          __syncwarp();
+          issued = true;
+        };
+        ok = wait_warp(&bars.q_full, gq & 1, abort_flag, p.status);
+        if (ok) ok = wait_warp(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0, gb, nullptr);
+          issue_s(1, 0, gb, nb == 1 ? &bars.q_empty : nullptr);
+        }
+        for (int j = 0; ok && j < nb; ++j) {
+          const uint32_t g = gb + j;
+          const bool next = j + 1 < nb;
+          bool comp;
+          int start, n;
+          pair_block(t, j, comp, start, n);
+          const int nks = (n + 15) >> 4;
+          const uint64_t dbv = dv0 + desc_bytes((g % kStages) * kTile);
+          for (int x = 0; ok && x < 2; ++x) {
+            ok = wait_warp(&bars.p_full[x], pcnt & 1, abort_flag, p.status);
+            if (ok && j == 0 && gq > 0) ok = wait_warp(&bars.o_free[x], (gq - 1) & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d = tmem + col_o(x), a = tmem + col_s(x);
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < kBlockKeys / 16; ++kk)
+                if (kk < nks) mma_ts(d, a + kk * 8, dbv + mnmaj_step(kk), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
               if (j == nb - 1) mma_commit(&bars.o_final[x]);
               if (x == 1) mma_commit(&bars.kv_empty[g % kStages]);
-              if (next) {
-                if (x == 0) {
-                  ok = mbar_wait(&bars.kv_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag, p.status);
-                  if (!ok) break;
-                  tc_fence_after();
-                }
-                issue_s(x, j + 1, g + 1);
-                if (x == 1 && j + 1 == nb - 1) mma_commit(&bars.q_empty);
-              }
             }
-            ++pcnt;
+            __syncwarp();
+            if (next) {
+              if (x == 0) {
+                ok = wait_warp(&bars.kv_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag, p.status);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              issue_s(x, j + 1, g + 1, (x == 1 && j + 1 == nb - 1) ? &bars.q_empty : nullptr);
+            }
           }
+          ++pcnt;
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        pcnt = __shfl_sync(0xffffffffu, pcnt, 0);
         gb += nb;
         ++gq;
       }
-      if (!ok && issued && lane == 0) {
+      if (!ok && issued) {
         volatile int never = 0;
-        mma_commit(&bars.drain);
-        mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+        if (elect_one()) mma_commit(&bars.drain);
+        __syncwarp();
+        if (lane == 0) mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+        __syncwarp();
       }
     }
   } else if (wg == 2) {

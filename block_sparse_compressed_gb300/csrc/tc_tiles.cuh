@@ -78,6 +78,17 @@ __device__ __forceinline__ void tile_ranges_warp(const QTiling &p, Tile &t, int 
   t.ncomp = (t.chi - t.clo + kBlockKeys - 1) / kBlockKeys;
 }
 
+// Broadcast a tile's ranges from lane 0: the compiler then treats them and
+// everything derived from them as warp-uniform (uniform registers).
+__device__ __forceinline__ void uniform_tile(Tile &t) {
+  t.rlo = __shfl_sync(0xffffffffu, t.rlo, 0);
+  t.rhi = __shfl_sync(0xffffffffu, t.rhi, 0);
+  t.clo = __shfl_sync(0xffffffffu, t.clo, 0);
+  t.chi = __shfl_sync(0xffffffffu, t.chi, 0);
+  t.nraw = __shfl_sync(0xffffffffu, t.nraw, 0);
+  t.ncomp = __shfl_sync(0xffffffffu, t.ncomp, 0);
+}
+
 // Block j of a tile: raw kv blocks first, then compressed ckv blocks.
 __device__ __forceinline__ void block_of(const Tile &t, int j, bool &comp, int &start, int &n) {
   if (j < t.nraw) {
