@@ -49,7 +49,11 @@ namespace dqk {
 constexpr int kStages = 3;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;  // dS: 64 cols of packed bf16
 constexpr int kTmemCols = 512;
-constexpr int kOffQ = 0, kOffDO = kTile, kOffKV = 2 * kTile;
+// two dS warpgroups (each owns 64 of a row's 128 key columns), TMA warp, MMA warp
+constexpr int kEW = 256;
+constexpr int kThreads = kEW + 64;
+// shared memory: Q | dO | out (for Delta) | kv ring | dq staging (+1 KB align)
+constexpr int kOffQ = 0, kOffDO = kTile, kOffO = 2 * kTile, kOffKV = 3 * kTile;
 constexpr int kOffOut = kOffKV + kStages * kTile;
 constexpr int kSmemBytes = kOffOut + kTile + 1024;
 }  // namespace dqk
@@ -57,7 +61,6 @@ constexpr int kSmemBytes = kOffOut + kTile + 1024;
 struct DqParams {
   QTiling qt;
   int32_t *status;
-  const __nv_bfloat16 *out;  // forward output (for Delta)
   const float *lse;
   float *rowstat;            // [ntiles][2][128]: -lse*log2e, then Delta, per tile row
   __nv_bfloat16 *dq;         // direct stores for poisoned calls / tiles without keys
@@ -67,8 +70,9 @@ struct DqParams {
 struct DqBars {
   uint64_t qd_full, qd_empty;
   uint64_t kv_full[dqk::kStages], kv_empty[dqk::kStages];
-  uint64_t s_full, s_free;
-  uint64_t ds_full, dq_done;
+  uint64_t s_full, s_free;   // S of a block in TMEM / read out by the dS warps
+  uint64_t dp_full, ds_full; // dP in TMEM / dS stored (and dP read out)
+  uint64_t dq_done;          // a tile's last dq MMA complete
   uint64_t epi, drain;
   uint32_t tmem_base;
   int abort;
@@ -78,8 +82,9 @@ __device__ __forceinline__ long long tile_linear(const QTiling &q, const Tile &t
   return ((long long)t.b * q.groups + t.g) * q.ntq + t.i0 / q.Pq;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(dqk::kThreads, 1)
     hca_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+                      const __grid_constant__ CUtensorMap map_out,
                       const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_ckv,
                       const __grid_constant__ CUtensorMap map_dq, const DqParams p) {
   using namespace dqk;
@@ -94,16 +99,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.qd_full, 1);
     // released by the last S/dP MMA of a tile and by every softmax thread
     // once it has read the staged dO tile (Delta)
-    mbar_init(&bars.qd_empty, 1 + kSoftmaxThreads);
+    mbar_init(&bars.qd_empty, 1 + kEW);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars.kv_full[s], 1);
       mbar_init(&bars.kv_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.s_free, kSoftmaxThreads);
-    mbar_init(&bars.ds_full, kSoftmaxThreads);
+    mbar_init(&bars.s_free, kEW);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.ds_full, kEW);
     mbar_init(&bars.dq_done, 1);
-    mbar_init(&bars.epi, kSoftmaxThreads);
+    mbar_init(&bars.epi, kEW);
     mbar_init(&bars.drain, 1);
     bars.abort = 0;
     fence_mbar_init();
@@ -118,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   const bool poisoned = *(volatile const int32_t *)p.status != 0;
 
-  if (warp == 4) {
+  if (warp == kEW / 32) {
     // ------------------------------------------------------------ TMA
     uint32_t gb = 0, tw = 0;
     int last_par[kStages] = {-1, -1, -1};
@@ -133,12 +139,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         if (tw > 0) ok = mbar_wait(&bars.qd_empty, (tw - 1) & 1, abort_flag, p.status);
         if (ok) {
-          mbar_arrive_expect_tx(&bars.qd_full, 2 * kTile);
+          mbar_arrive_expect_tx(&bars.qd_full, 3 * kTile);
           const int c2 = t.b * Q.H + t.g * Q.HG;
           tma_load_3d(&map_q, &bars.qd_full, smem + kOffQ, 0, t.i0, c2);
           tma_load_3d(&map_q, &bars.qd_full, smem + kOffQ + kHalfTile, 64, t.i0, c2);
           tma_load_3d(&map_do, &bars.qd_full, smem + kOffDO, 0, t.i0, c2);
           tma_load_3d(&map_do, &bars.qd_full, smem + kOffDO + kHalfTile, 64, t.i0, c2);
+          tma_load_3d(&map_out, &bars.qd_full, smem + kOffO, 0, t.i0, c2);
+          tma_load_3d(&map_out, &bars.qd_full, smem + kOffO + kHalfTile, 64, t.i0, c2);
           q_par = tw & 1;
         }
         for (int j = 0; ok && j < nb; ++j, ++gb) {
@@ -167,10 +175,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (last_par[s] >= 0) mbar_wait(&bars.kv_full[s], last_par[s], &never, p.status, 100000000ull);
       if (q_par >= 0) mbar_wait(&bars.qd_full, q_par, &never, p.status, 100000000ull);
     }
-  } else if (warp == 5) {
+  } else if (warp == kEW / 32 + 1) {
     // ------------------------------------------------------------ MMA
     // Whole warp, warp-uniform values, one elect.sync lane issues (cheap
     // tcgen05.mma issue from uniform registers; see the forward kernel).
+    // Per key block j the order is  S(j+1) | dq(j) | dP(j+1):  S(j+1) goes
+    // out as soon as the dS warps hold P(j) in registers, so the tensor pipe
+    // runs it while they form dS(j).  dP(j+1) overwrites dP(j) only after
+    // dS(j) is stored, and its commit also covers dq(j) (one thread's MMAs
+    // complete in order), so dS(j+1) never overwrites a dS that an
+    // unfinished dq MMA still reads.
     const uint64_t dQ = smem_desc_sw128(smem_u32(smem + kOffQ), 16, 1024);
     const uint64_t dDO = smem_desc_sw128(smem_u32(smem + kOffDO), 16, 1024);
     const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + kOffKV), 16, 1024);
@@ -185,36 +199,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       uniform_tile(t);
       const int nb = t.nraw + t.ncomp;
       if (nb == 0) continue;
-      auto issue_sdp = [&](int j, uint32_t g, bool last_q_use) -> bool {
-        const int s = g % kStages;
-        if (!wait_warp(&bars.kv_full[s], (g / kStages) & 1, abort_flag, p.status)) return false;
-        if (g > 0 && !wait_warp(&bars.s_free, (g - 1) & 1, abort_flag, p.status)) return false;
-        tc_fence_after();
+      // S (x = 0) or dP (x = 1) of block j into its TMEM columns
+      auto issue_sdp = [&](int x, int j, uint32_t g, bool last_q_use) {
         bool comp;
         int start, n;
         block_of(t, j, comp, start, n);
         const uint32_t idesc = idesc_bf16_f32(kRows, (n + 15) & ~15, false, false);
-        const uint64_t bk = dK0 + desc_bytes(s * kTile);
+        const uint64_t bk = dK0 + desc_bytes((g % kStages) * kTile);
+        const uint64_t da = x ? dDO : dQ;
+        const uint32_t d = tmem + (x ? kColDP : kColS);
         if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k) {
-            mma_ss(tmem + kColS, dQ + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
-            mma_ss(tmem + kColDP, dDO + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
-          }
-          mma_commit(&bars.s_full);
+          for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, da + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
+          mma_commit(x ? &bars.dp_full : &bars.s_full);
           if (last_q_use) mma_commit(&bars.qd_empty);
         }
         __syncwarp();
         issued = true;
-        return true;
       };
       ok = wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status);
-      if (ok) ok = issue_sdp(0, gb, nb == 1);
+      if (ok) ok = wait_warp(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status);
+      // the previous tile's last S must have been read out
+      if (ok && gb > 0) ok = wait_warp(&bars.s_free, (gb - 1) & 1, abort_flag, p.status);
+      if (ok) {
+        tc_fence_after();
+        issue_sdp(0, 0, gb, false);
+        issue_sdp(1, 0, gb, nb == 1);
+      }
       for (int j = 0; ok && j < nb; ++j) {
         const uint32_t g = gb + j;
-        if (j + 1 < nb) {
-          ok = issue_sdp(j + 1, g + 1, j + 1 == nb - 1);
+        const bool next = j + 1 < nb;
+        if (next) {
+          ok = wait_warp(&bars.s_free, g & 1, abort_flag, p.status);
+          if (ok) ok = wait_warp(&bars.kv_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag, p.status);
           if (!ok) break;
+          tc_fence_after();
+          issue_sdp(0, j + 1, g + 1, false);
         }
         ok = wait_warp(&bars.ds_full, g & 1, abort_flag, p.status);
         if (!ok) break;
@@ -231,9 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kk < nks)
               mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, bv + mnmaj_step(kk), id_dq, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bars.kv_empty[s]);
-          mma_commit(&bars.dq_done);
+          if (!next) mma_commit(&bars.dq_done);
         }
         __syncwarp();
+        if (next) issue_sdp(1, j + 1, g + 1, j + 1 == nb - 1);
       }
       gb += nb;
       ++tw;
@@ -247,25 +268,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dS + epilogue
-    const int r = tid;
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    // thread r of warpgroup wg owns row r (TMEM lane r) and key columns
+    // [64 wg, 64 wg + 64) of every block (and dq columns [64 wg, 64 wg + 64))
+    const int r = tid & (kRows - 1), wg = tid >> 7;
+    const int cb = wg * 64;
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     uint8_t *obuf = smem + kOffOut;
     const uint8_t *dobuf = smem + kOffDO;
-    uint32_t gb = 0, tw = 0, dq_waited = 0, epi_phase = 0;
+    const uint8_t *outbuf = smem + kOffO;
+    uint32_t gb = 0, tw = 0, epi_phase = 0;
+    const uint64_t sl2x2 = f32x2(__float_as_uint(p.sl2), __float_as_uint(p.sl2));
     bool ok = true, store_pending = false;
     auto rendezvous = [&]() -> bool {
       mbar_arrive(&bars.epi);
       const bool rr = wait_warp(&bars.epi, epi_phase & 1, abort_flag, p.status);
       ++epi_phase;
       return rr;
-    };
-    // dq MMA number x (global) complete
-    auto wait_dq = [&](uint32_t x) -> bool {
-      while (dq_waited <= x) {
-        if (!wait_warp(&bars.dq_done, dq_waited & 1, abort_flag, p.status)) return false;
-        ++dq_waited;
-      }
-      return true;
     };
     for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
       Tile t;
@@ -282,22 +300,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i < Q.S) {
           const float v = poisoned ? __int_as_float(0x7fc00000) : 0.f;
           const uint32_t w2 = pack_bf16x2(v, v);
-          uint4 *grow = reinterpret_cast<uint4 *>(p.dq + lrow * kHeadDim);
+          uint4 *grow = reinterpret_cast<uint4 *>(p.dq + lrow * kHeadDim + cb);
 #pragma unroll
-          for (int c = 0; c < kHeadDim / 8; ++c) grow[c] = make_uint4(w2, w2, w2, w2);
+          for (int c = 0; c < kHeadDim / 16; ++c) grow[c] = make_uint4(w2, w2, w2, w2);
         }
-        rs[r] = 0.f;
-        rs[kRows + r] = 0.f;
+        if (wg == 0) {
+          rs[r] = 0.f;
+          rs[kRows + r] = 0.f;
+        }
         continue;
       }
-      // Delta = <dO, out> for this row (dO from the staged tile)
+      // Delta = <dO, out> for this row, from the staged dO and out tiles
+      // (both warpgroups form it; the first one publishes it)
+      const float lse_row = iv.valid ? p.lse[lrow] : 0.f;
       if (!wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status)) { ok = false; break; }
       float lse2 = 0.f, delta = 0.f;
       if (iv.valid) {
-        const uint4 *orow = reinterpret_cast<const uint4 *>(p.out + lrow * kHeadDim);
-#pragma unroll 4
+#pragma unroll
         for (int ch = 0; ch < 16; ++ch) {
-          const uint4 ov = orow[ch];
+          const uint4 ov = *reinterpret_cast<const uint4 *>(outbuf + sw128_offset(r, ch));
           const uint4 gv = *reinterpret_cast<const uint4 *>(dobuf + sw128_offset(r, ch));
           const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
@@ -306,74 +327,78 @@ __global__ void __launch_bounds__(kThreads, 1)
             delta = fmaf(__uint_as_float(oa[x] & 0xffff0000u), __uint_as_float(ga[x] & 0xffff0000u), delta);
           }
         }
-        lse2 = p.lse[lrow] * kLog2e;
+        lse2 = lse_row * kLog2e;
       }
-      rs[r] = -lse2;
-      rs[kRows + r] = delta;
+      if (wg == 0) {
+        rs[r] = -lse2;
+        rs[kRows + r] = delta;
+      }
       mbar_arrive(&bars.qd_empty);
       for (int j = 0; j < nb; ++j, ++gb) {
         bool comp;
         int start, n;
         block_of(t, j, comp, start, n);
         const int nk = (n + 15) & ~15;
-        int lo_c = 0, hi_c = -1;
+        // visible columns [cb, cb + 64) of this row: one contiguous range
+        uint64_t vis = 0;
         if (iv.valid) {
           const int lo = comp ? iv.clo : iv.rlo, hi = comp ? iv.chi : iv.rhi;
-          lo_c = max(lo - start, 0);
-          hi_c = min(hi - start, n - 1);
+          vis = range_mask64(max(lo - start, 0), min(hi - start, n - 1), cb);
         }
         if (!wait_warp(&bars.s_full, gb & 1, abort_flag, p.status)) { ok = false; break; }
-        // dS lives in TMEM: the previous dq MMA must have consumed it
-        if (gb >= 1 && !wait_dq(gb - 1)) { ok = false; break; }
         tc_fence_after();
-        for (int c0 = 0; c0 < nk; c0 += 32) {
-          uint32_t sr[32], pr[32];
-          const bool full = c0 + 32 <= nk;
-          if (full) {
-            tmem_ld32(lane_addr + kColS + c0, sr);
-            tmem_ld32(lane_addr + kColDP + c0, pr);
-          } else {
-            uint32_t a16[16], b16[16];
-            tmem_ld16(lane_addr + kColS + c0, a16);
-            tmem_ld16(lane_addr + kColDP + c0, b16);
+        // P = exp2(S * scale * log2e - lse * log2e), kept in registers so the
+        // S columns can take the next block's scores right away
+        uint32_t pv[64];
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-              sr[x] = a16[x];
-              pr[x] = b16[x];
-            }
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          if (cb + c0 < nk) {
+            tmem_ld32(lane_addr + kColS + cb + c0, *reinterpret_cast<uint32_t(*)[32]>(pv + c0));
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) pv[c0 + x] = 0u;
           }
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars.s_free);
+        const uint64_t nl2 = f32x2(__float_as_uint(-lse2), __float_as_uint(-lse2));
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float t0, t1;
+          f32x2_split(ffma2(f32x2(pv[c], pv[c + 1]), sl2x2, nl2), t0, t1);
+          pv[c] = ((vis >> c) & 1ull) ? __float_as_uint(ex2_approx(t0)) : 0u;
+          pv[c + 1] = ((vis >> (c + 1)) & 1ull) ? __float_as_uint(ex2_approx(t1)) : 0u;
+        }
+        if (!wait_warp(&bars.dp_full, gb & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t ndl2 = f32x2(__float_as_uint(-delta), __float_as_uint(-delta));
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          if (cb + c0 >= nk) break;
+          uint32_t dr[32];
+          tmem_ld32(lane_addr + kColDP + cb + c0, dr);
           tmem_wait_ld();
           uint32_t packed[16];
 #pragma unroll
           for (int x = 0; x < 32; x += 2) {
-            float ds2[2];
-#pragma unroll
-            for (int y = 0; y < 2; ++y) {
-              const int c = c0 + x + y;
-              const bool vis = c >= lo_c && c <= hi_c;
-              const float pv = ex2_approx(__uint_as_float(sr[x + y]) * p.sl2 - lse2);
-              ds2[y] = vis ? pv * (__uint_as_float(pr[x + y]) - delta) : 0.f;
-            }
-            packed[x / 2] = pack_bf16x2(ds2[0], ds2[1]);
+            const int c = c0 + x;
+            // dS = P (dP - Delta); columns past the block (stale TMEM) are zero
+            float d0, d1;
+            f32x2_split(fmul2(f32x2(pv[c], pv[c + 1]), fadd2(f32x2(dr[x], dr[x + 1]), ndl2)), d0, d1);
+            d0 = ((vis >> c) & 1ull) ? d0 : 0.f;
+            d1 = ((vis >> (c + 1)) & 1ull) ? d1 : 0.f;
+            packed[x / 2] = pack_bf16x2(d0, d1);
           }
-          if (full) {
-            tmem_st16(lane_addr + kColDS + c0 / 2, packed);
-          } else {
-            uint32_t p8[16];
-#pragma unroll
-            for (int x = 0; x < 16; ++x) p8[x] = packed[x];
-            // only 8 packed columns are meaningful for a 16-key tail
-            tmem_st16(lane_addr + kColDS + c0 / 2, p8);
-          }
+          tmem_st16(lane_addr + kColDS + (cb + c0) / 2, packed);
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars.s_free);
         mbar_arrive(&bars.ds_full);
       }
       if (!ok) break;
       // ---------------- epilogue: dq = scale * acc
-      if (!wait_dq(gb - 1)) { ok = false; break; }
+      if (!wait_warp(&bars.dq_done, tw & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       if (store_pending) {
         if (tid == 0) bulk_wait_read0();
@@ -383,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         uint32_t o[32];
 #pragma unroll
-        for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+        for (int c0 = cb; c0 < cb + 64; c0 += 32) {
           tmem_ld32(lane_addr + kColDQ + c0, o);
           tmem_wait_ld();
 #pragma unroll
@@ -922,8 +947,9 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   // a position range when one head fills the tile
   const int sub_hg = q.HG >= 2 ? q.HG / 2 : 1;
   const int sub_pq = q.HG >= 2 ? q.Pq : q.Pq / 2;
-  CUtensorMap mq, mdo, mkv, mckv, mdq, mqs, mdos;
+  CUtensorMap mq, mdo, mout, mkv, mckv, mdq, mqs, mdos;
   if (!make_map_bf16(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mout, a.out, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mdo, a.dout, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mdq, a.dq, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mqs, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, sub_pq, sub_hg) ||
@@ -947,7 +973,6 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   DqParams dp;
   dp.qt = q;
   dp.status = a.status_rw;
-  dp.out = static_cast<const __nv_bfloat16 *>(a.out);
   dp.lse = a.lse;
   dp.rowstat = rowstat;
   dp.dq = static_cast<__nv_bfloat16 *>(a.dq);
@@ -958,7 +983,7 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   cudaError_t e;
   {
     ProfScope prof(kKBwdDq, st);
-    hca_bwd_dq_kernel<<<(unsigned)g1, kThreads, dqk::kSmemBytes, st>>>(mq, mdo, mkv, mckv, mdq, dp);
+    hca_bwd_dq_kernel<<<(unsigned)g1, dqk::kThreads, dqk::kSmemBytes, st>>>(mq, mdo, mout, mkv, mckv, mdq, dp);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;

@@ -102,6 +102,14 @@ __device__ __forceinline__ void block_of(const Tile &t, int j, bool &comp, int &
   }
 }
 
+// Bits c of a 64-bit mask for which lo <= base + c <= hi.
+__device__ __forceinline__ uint64_t range_mask64(int lo, int hi, int base) {
+  const int l = max(lo - base, 0), h = min(hi - base, 63);
+  if (h < l) return 0ull;
+  const int w = h - l + 1;
+  return (w >= 64 ? ~0ull : ((1ull << w) - 1ull)) << l;
+}
+
 // Byte offset of 16-byte chunk `chunk16` (0..15 over both halves) of row
 // `row` in a 128-row x 256-byte tile stored as two 128B-swizzled halves --
 // the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B and the UMMA
