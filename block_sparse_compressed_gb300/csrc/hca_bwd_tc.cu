@@ -15,16 +15,19 @@
 //     block: S = Q K^T and dP = dO K^T share the kv tile; the softmax warps
 //     form dS (bf16) straight into TMEM; dq += dS K reads dS from TMEM and the
 //     kv tile through an MN-major descriptor.
-//  2. dkv kernel (key-major).  A work item is one 128-key block (raw kv rows,
-//     or compressed entries with their query range split into kSplit chunks)
-//     and loops over the head-packed query tiles that can see it:
+//  2. dkv kernel (key-major).  A work item is a range of head-packed query
+//     tiles and one or two 128-key blocks of one kind; each 64-row query
+//     sub-tile is loaded once and serves both blocks:
 //       S^T = K Q^T, dP^T = K dO^T  ->  P^T, dS^T (bf16, into TMEM)
-//       acc += P^T dO + (scale dS^T) Q      (one fp32 TMEM accumulator)
-//     Raw blocks write dkv directly; compressed blocks write fp32 partials.
+//       acc_a += P^T dO + (scale dS^T) Q    (one fp32 TMEM accumulator per block)
+//     Raw items cover 128 query positions and the (up to two) raw blocks they
+//     see; compressed items cover a slice of the queries that see a pair of
+//     compressed blocks.  Every item writes fp32 partial sums.
 //     The dQ side needs no atomics: kernel 1 owns dq.  ("Add HCA Static
 //     Compilation for Splash Attention [Deepseek v4]" reduces dQ in an on-chip
 //     ring buffer on TPU; here dq stays in TMEM for a whole query tile.)
-//  3. reduce kernel: dckv = sum of the partials in a fixed order (deterministic).
+//  3. reduce kernel: dkv and dckv = sums of their partials in a fixed order
+//     (deterministic).
 #include <cuda_bf16.h>
 
 #include "hca_common.cuh"
@@ -39,7 +42,6 @@ namespace {
 
 constexpr int kSoftmaxThreads = 128;
 constexpr int kThreads = 192;
-constexpr int kSplit = 64;  // query chunks per compressed key block
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -448,23 +450,33 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
 // kernel 2: dkv / dckv partials
 // ---------------------------------------------------------------------------
 namespace dkk {
-// A query tile is processed as two 64-row sub-tiles.  Shared memory holds a
-// sub-tile as one 128-row operand R = [Q_sub ; dO_sub] (64 rows each, per
-// 64-column half), so a single N = 128 MMA K R^T yields S^T (columns 0-63) and
-// dP^T (columns 64-127) of the sub-tile.
-constexpr int kStages = 2;                 // query tiles in flight
-constexpr int kSubBytes = kTile;           // one 128-row operand R (two halves)
-constexpr int kHalfRows = 64;              // rows of Q_sub (and of dO_sub) per half
-constexpr int kOffRowstat = 2 * kSubBytes; // -lse*log2e [128] then Delta [128]
-constexpr int kOffIv = kOffRowstat + 1024; // per-position key interval (int2)
-constexpr int kStageBytes = kOffIv + 1024;
-constexpr int kOffK = 0, kOffStage = kTile;
+// A work item is a range of query tiles and one or two 128-key blocks of one
+// kind (raw or compressed).  The item streams 64-row query sub-tiles through
+// shared memory once and uses each for both key blocks, so a query row is
+// fetched about half as often as with one key block per item.  Shared memory
+// holds a sub-tile as one 128-row operand R = [Q_sub ; dO_sub] (64 rows each,
+// per 64-column half): a single N = 128 MMA K R^T yields S^T (columns 0-63)
+// and dP^T (columns 64-127) of the sub-tile for one key block.
+constexpr int kStages = 4;                     // sub-tiles in flight
+constexpr int kSubBytes = kTile;               // one operand R (two halves)
+constexpr int kHalfRows = 64;                  // rows of Q_sub (and of dO_sub)
+constexpr int kOffRowstat = kSubBytes;         // -lse*log2e [64] then Delta [64]
+constexpr int kOffIv = kOffRowstat + 512;      // per-position intervals (rlo, rhi, clo, chi) [<= 64]
+constexpr int kStageBytes = kOffIv + 1024 + 512;  // 34 KB: every stage stays 1 KB aligned
+constexpr int kOffK = 0;                       // key block tiles A | B
+constexpr int kOffStage = 2 * kTile;
 constexpr int kSmemBytes = kOffStage + kStages * kStageBytes + 1024;
 // TMEM: two [S^T | dP^T] buffers (P^T and dS^T overwrite their first 64
-// columns as packed bf16), then the fp32 dkv accumulator
+// columns as packed bf16), then one fp32 accumulator per key block
 constexpr uint32_t kColAcc = 256;
 constexpr int kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_buf(uint32_t g) { return (g & 1u) * 128u; }
+__host__ __device__ constexpr uint32_t col_acc(int a) { return kColAcc + (uint32_t)a * 128u; }
+// Query-range splits of the compressed items.  They are fixed numbers so
+// the partial buffers grow linearly with the sequence length.
+constexpr int kSplitBoth = 128;  // compressed blocks 2c, 2c+1 where both are visible
+constexpr int kSplitLead = 32;   // block 2c alone, before block 2c+1 is visible
+constexpr int kSlotsComp = kSplitLead + kSplitBoth;
 }  // namespace dkk
 
 struct DkvParams {
@@ -472,48 +484,98 @@ struct DkvParams {
   int32_t *status;
   int32_t *next_item;  // work counter (zeroed before the launch)
   const float *rowstat;
-  __nv_bfloat16 *dkv;
-  float *partial;  // [kSplit][B][Sc_pad][D] fp32
-  int nkb_raw, nkb_comp, Sc_pad;
+  float *rpart;  // raw partials [nslot][B][S_pad][D] fp32: slot = query range - key block
+                 // (one slot, accumulated with atomics, when raw_atomic)
+  float *cpart;  // compressed partials [kSlotsComp][B][Sc_pad][D] fp32
+  int nrb, nkb_comp, S_pad, Sc_pad, nslot, npr;
+  int raw_atomic;      // raw partials summed with fp32 atomics into slot 0 (long windows)
   int sub_pq, sub_hg;  // TMA box of a 64-row sub-tile: positions x heads
-  long long nitems;
+  long long n_both, n_lead, nitems;
   float sl2, scale;
 };
 
 struct Item {
-  int b, comp, k0, n;  // key block [k0, k0+n)
-  int split;
-  int tq_lo, tq_hi;    // query tiles [tq_lo, tq_hi) (each over all head groups)
+  int b, comp, nkb;   // nkb key blocks of one kind (0: nothing to do)
+  int k0[2], n[2];    // key blocks [k0, k0 + n)
+  int slot[2];        // partial slot of each block
+  int tq_lo, tq_hi;   // query tiles [tq_lo, tq_hi), each over all head groups
 };
 
-// items: compressed blocks (all splits, most work first), then raw blocks
+// First query tile with a query that can see compressed entry e (the entry's
+// window completes at query (e + 1) m - 1).
+__device__ __forceinline__ int first_tile_comp(const QTiling &Q, int e) {
+  const long long first = (long long)(e + 1) * Q.m - 1;
+  return first >= Q.S ? Q.ntq : (int)(first / Q.Pq);
+}
+
+// Items, most work first: compressed pairs, lone even compressed blocks, raw.
+//  - compressed pair c: blocks 2c and 2c+1 over the tiles from the first one
+//    that sees block 2c+1 on, split kSplitBoth ways (slots kSplitLead + s);
+//  - compressed lead c: block 2c over the tiles before that, split kSplitLead
+//    ways (slots s);
+//  - raw (b, j, pr): query positions [128 j, 128 j + 128) with raw blocks
+//    j - 2 pr and j - 2 pr - 1 (the blocks that range can see, two at a time);
+//    block kb's partial goes to slot j - kb.
 __device__ __forceinline__ void item_of(const DkvParams &p, long long u, Item &it) {
   const QTiling &Q = p.qt;
-  const long long ncomp_items = (long long)Q.B * p.nkb_comp * kSplit;
-  if (u < ncomp_items) {
-    const int kb = (int)(u / ((long long)Q.B * kSplit));
-    const int rem = (int)(u % ((long long)Q.B * kSplit));
-    it.b = rem / kSplit;
-    it.split = rem % kSplit;
+  it.nkb = 0;
+  it.tq_lo = it.tq_hi = 0;
+  it.b = 0;
+  it.comp = 0;
+  if (u < p.n_both) {
+    const long long per = (long long)Q.B * dkk::kSplitBoth;
+    const int pc = (int)(u / per);
+    const int rem = (int)(u % per);
+    it.b = rem / dkk::kSplitBoth;
+    const int split = rem % dkk::kSplitBoth;
     it.comp = 1;
-    it.k0 = kb * kBlockKeys;
-    it.n = min(kBlockKeys, Q.Sc - it.k0);
-    const long long first = (long long)(it.k0 + 1) * Q.m - 1;  // first query that sees entry k0
-    const int lo = first >= Q.S ? Q.ntq : (int)(first / Q.Pq);
+    it.nkb = 2;
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      it.k0[a] = (2 * pc + a) * kBlockKeys;
+      it.n[a] = min(kBlockKeys, Q.Sc - it.k0[a]);
+      it.slot[a] = dkk::kSplitLead + split;
+    }
+    const int lo = first_tile_comp(Q, it.k0[1]);
     const int len = Q.ntq - lo;
-    it.tq_lo = lo + (int)((long long)len * it.split / kSplit);
-    it.tq_hi = lo + (int)((long long)len * (it.split + 1) / kSplit);
+    it.tq_lo = lo + (int)((long long)len * split / dkk::kSplitBoth);
+    it.tq_hi = lo + (int)((long long)len * (split + 1) / dkk::kSplitBoth);
+  } else if (u < p.n_both + p.n_lead) {
+    const long long v = u - p.n_both;
+    const long long per = (long long)Q.B * dkk::kSplitLead;
+    const int pc = (int)(v / per);
+    const int rem = (int)(v % per);
+    it.b = rem / dkk::kSplitLead;
+    const int split = rem % dkk::kSplitLead;
+    it.comp = 1;
+    it.nkb = 1;
+    it.k0[0] = 2 * pc * kBlockKeys;
+    it.n[0] = min(kBlockKeys, Q.Sc - it.k0[0]);
+    it.slot[0] = split;
+    const int lo = first_tile_comp(Q, it.k0[0]);
+    const int hi = 2 * pc + 1 < p.nkb_comp ? first_tile_comp(Q, it.k0[0] + kBlockKeys) : Q.ntq;
+    const int len = hi - lo;
+    it.tq_lo = lo + (int)((long long)len * split / dkk::kSplitLead);
+    it.tq_hi = lo + (int)((long long)len * (split + 1) / dkk::kSplitLead);
   } else {
-    const long long v = u - ncomp_items;
-    it.b = (int)(v % Q.B);
-    const int kb = (int)(v / Q.B);
-    it.split = 0;
-    it.comp = 0;
-    it.k0 = kb * kBlockKeys;
-    it.n = min(kBlockKeys, Q.S - it.k0);
-    const long long last = min((long long)Q.S - 1, (long long)it.k0 + it.n - 1 + Q.W - 1);
-    it.tq_lo = it.k0 / Q.Pq;
-    it.tq_hi = (int)(last / Q.Pq) + 1;
+    const long long v = u - p.n_both - p.n_lead;
+    const int pr = (int)(v % p.npr);
+    const long long w = v / p.npr;
+    it.b = (int)(w % Q.B);
+    const int j = (int)(w / Q.B);
+    const long long lo_key = (long long)j * kBlockKeys - Q.W + 1;  // oldest key the range can see
+    const int kb_lo = lo_key <= 0 ? 0 : (int)(lo_key / kBlockKeys);
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      const int kb = j - 2 * pr - a;
+      if (kb < kb_lo || 2 * pr + a >= p.nslot) break;
+      it.k0[a] = kb * kBlockKeys;
+      it.n[a] = min(kBlockKeys, Q.S - it.k0[a]);
+      it.slot[a] = 2 * pr + a;
+      it.nkb = a + 1;
+    }
+    it.tq_lo = j * kBlockKeys / Q.Pq;
+    it.tq_hi = (min(j * kBlockKeys + kBlockKeys, Q.S) + Q.Pq - 1) / Q.Pq;
   }
 }
 
@@ -574,10 +636,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   const bool poisoned = *(volatile const int32_t *)p.status != 0;
   const int per_tile = Q.groups;  // query tiles per position tile (one per head group)
+  // a sub-tile is a head range of its query tile when HG >= 2, a position range when one head fills it
+  const bool pos_split = p.sub_hg == Q.HG;
 
   if (warp == 4) {
     // ------------------------------------------------------------ TMA
-    uint32_t gq = 0, iw = 0;
+    uint32_t gsub = 0, iw = 0;
     uint32_t issued = 0;  // bit s: stage loaded at least once; bit 8+s: parity of its last load
     int k_par = -1;
     bool ok = true;
@@ -602,65 +666,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (poisoned) continue;
       Item it;
       item_of(p, u, it);
-      const int nq = (it.tq_hi - it.tq_lo) * per_tile;
-      if (nq <= 0) continue;
+      const int nsub = 2 * (it.tq_hi - it.tq_lo) * per_tile;
+      if (it.nkb == 0 || nsub <= 0) continue;
       if (lane == 0) {
         if (iw > 0) ok = mbar_wait(&bars.k_empty, (iw - 1) & 1, abort_flag, p.status);
         if (ok) {
           const CUtensorMap *mp = it.comp ? &map_ckv : &map_kv;
-          mbar_arrive_expect_tx(&bars.k_full, kTile);
-          tma_load_3d(mp, &bars.k_full, smem + kOffK, 0, it.k0, it.b);
-          tma_load_3d(mp, &bars.k_full, smem + kOffK + kHalfTile, 64, it.k0, it.b);
+          mbar_arrive_expect_tx(&bars.k_full, it.nkb * kTile);
+          for (int a = 0; a < it.nkb; ++a) {
+            uint8_t *dst = smem + kOffK + a * kTile;
+            tma_load_3d(mp, &bars.k_full, dst, 0, it.k0[a], it.b);
+            tma_load_3d(mp, &bars.k_full, dst + kHalfTile, 64, it.k0[a], it.b);
+          }
           k_par = iw & 1;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      for (int x = 0; ok && x < nq; ++x, ++gq) {
+      for (int v = 0; ok && v < nsub; ++v, ++gsub) {
+        const int x = v >> 1, sub = v & 1;
         const int tq = it.tq_lo + x / per_tile, g = x % per_tile;
-        const int s = gq % kStages;
+        const int s = gsub % kStages;
         uint8_t *st = smem + kOffStage + s * kStageBytes;
-        if (lane == 0 && gq >= (uint32_t)kStages)
-          ok = mbar_wait(&bars.st_empty[s], ((gq / kStages) - 1) & 1, abort_flag, p.status);
+        if (lane == 0 && gsub >= (uint32_t)kStages)
+          ok = mbar_wait(&bars.st_empty[s], ((gsub / kStages) - 1) & 1, abort_flag, p.status);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        // per-position key intervals of this query tile, for this key kind
-        int2 *ivs = reinterpret_cast<int2 *>(st + kOffIv);
-        for (int q = lane; q < Q.Pq; q += 32) {
-          RowIv iv = row_interval(Q.sstart, it.b, Q.S, tq * Q.Pq + q, Q.W, Q.m);
-          int lo = 1, hi = 0;
-          if (iv.valid) {
-            lo = it.comp ? iv.clo : iv.rlo;
-            hi = it.comp ? iv.chi : iv.rhi;
-          }
-          ivs[q] = make_int2(lo, hi);
+        const int i0 = tq * Q.Pq;
+        const int pos0 = pos_split ? i0 + sub * p.sub_pq : i0;
+        const int hd = it.b * Q.H + g * Q.HG + (pos_split ? 0 : sub * p.sub_hg);
+        // key intervals of the sub-tile's positions (both kinds)
+        int4 *ivs = reinterpret_cast<int4 *>(st + kOffIv);
+        for (int c = lane; c < p.sub_pq; c += 32) {
+          const RowIv iv = row_interval(Q.sstart, it.b, Q.S, pos0 + c, Q.W, Q.m);
+          ivs[c] = iv.valid ? make_int4(iv.rlo, iv.rhi, iv.clo, iv.chi) : make_int4(1, 0, 1, 0);
         }
         __syncwarp();
         if (lane == 0) {
-          const int c2 = it.b * Q.H + g * Q.HG;
-          const int i0 = tq * Q.Pq;
-          mbar_arrive_expect_tx(&bars.st_full[s], 2 * kSubBytes + 1024);
+          mbar_arrive_expect_tx(&bars.st_full[s], kSubBytes + 512);
 #pragma unroll
-          for (int sub = 0; sub < 2; ++sub) {
-            // rows [64 sub, 64 sub + 64) of the tile: a head range when HG >= 2,
-            // a position range when one head fills the tile
-            const int pos = p.sub_hg == Q.HG ? i0 + sub * p.sub_pq : i0;
-            const int hd = p.sub_hg == Q.HG ? c2 : c2 + sub * p.sub_hg;
-            uint8_t *r0 = st + sub * kSubBytes;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              tma_load_3d(&map_qs, &bars.st_full[s], r0 + h * kHalfTile, 64 * h, pos, hd);
-              tma_load_3d(&map_dos, &bars.st_full[s], r0 + h * kHalfTile + kHalfRows * 128, 64 * h, pos, hd);
-            }
+          for (int h = 0; h < 2; ++h) {
+            tma_load_3d(&map_qs, &bars.st_full[s], st + h * kHalfTile, 64 * h, pos0, hd);
+            tma_load_3d(&map_dos, &bars.st_full[s], st + h * kHalfTile + kHalfRows * 128, 64 * h, pos0, hd);
           }
+          // rows [64 sub, 64 sub + 64) of the tile's (-lse*log2e, Delta) record
           const long long tl = ((long long)it.b * Q.groups + g) * Q.ntq + tq;
-          asm volatile(
-              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                  smem_u32(st + kOffRowstat)),
-              "l"(reinterpret_cast<uint64_t>(p.rowstat + tl * 2 * kRows)), "r"(1024),
-              "r"(smem_u32(&bars.st_full[s]))
-              : "memory");
+          const float *rs = p.rowstat + tl * 2 * kRows + sub * kHalfRows;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(st + kOffRowstat + h * 256)),
+                "l"(reinterpret_cast<uint64_t>(rs + h * kRows)), "r"(256), "r"(smem_u32(&bars.st_full[s]))
+                : "memory");
           issued = (issued | (1u << s)) & ~(1u << (8 + s));
-          issued |= ((gq / kStages) & 1u) << (8 + s);
+          issued |= ((gsub / kStages) & 1u) << (8 + s);
         }
         __syncwarp();
       }
@@ -674,12 +733,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA
-    const uint64_t dK = smem_desc_sw128(smem_u32(smem + kOffK), 16, 1024);
+    // Whole warp on warp-uniform values; one elect.sync lane issues.  Work
+    // unit u of an item is (sub-tile u / nkb, key block u % nkb); its
+    // S^T | dP^T goes to TMEM buffer (global unit count) & 1, so the dS warps
+    // form P^T, dS^T of one unit while the tensor pipe runs the next.
+    const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + kOffK), 16, 1024);
     const uint64_t dR0 = smem_desc_sw128(smem_u32(smem + kOffStage), 16, 1024);          // R, K-major
     const uint64_t dM0 = smem_desc_sw128(smem_u32(smem + kOffStage), kHalfTile, 1024);   // R rows, MN-major
     const uint32_t id_sd = idesc_bf16_f32(kRows, kRows, false, false);
     const uint32_t id_acc = idesc_bf16_f32(kRows, kHeadDim, false, true);
-    uint32_t gq = 0, gs = 0, iw = 0;  // query tiles, sub-tiles and items with work so far
+    uint32_t gsub = 0, gu = 0, iw = 0;  // sub-tiles, units and items with work so far
     bool ok = true, issued = false;
     for (uint32_t kq = 0; ok; ++kq) {
       const int slot = kq % kItemRing;
@@ -697,60 +760,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (poisoned) continue;
       Item it;
       item_of(p, u, it);
-      const int nq = (it.tq_hi - it.tq_lo) * per_tile;
-      if (nq <= 0) continue;
-      // whole warp on warp-uniform values; one elect.sync lane issues
-      const int nsub = 2 * nq;
+      const int nsub = 2 * (it.tq_hi - it.tq_lo) * per_tile;
+      if (it.nkb == 0 || nsub <= 0) continue;
+      const int nkb = it.nkb;
+      const int nu = nsub * nkb;
       ok = wait_warp(&bars.k_full, iw & 1, abort_flag, p.status);
-      // S^T | dP^T of sub-tile v (item-local), into TMEM buffer of global sub-tile gs+v
-      auto issue_sd = [&](int v) -> bool {
-        const uint32_t qg = gq + v / 2;
-        const int s = qg % kStages;
-        if ((v & 1) == 0 && !wait_warp(&bars.st_full[s], (qg / kStages) & 1, abort_flag, p.status)) return false;
+      // S^T | dP^T of unit w into TMEM buffer (gu + w) & 1
+      auto issue_sd = [&](int w) -> bool {
+        const int v = nkb == 2 ? (w >> 1) : w, a = nkb == 2 ? (w & 1) : 0;
+        const uint32_t sg = gsub + v;
+        const int s = sg % kStages;
+        if (a == 0 && !wait_warp(&bars.st_full[s], (sg / kStages) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint64_t br = dR0 + desc_bytes(s * kStageBytes + (v & 1) * kSubBytes);
-        const uint32_t d = tmem + col_buf(gs + v);
+        const uint64_t br = dR0 + desc_bytes(s * kStageBytes);
+        const uint64_t bk = dK0 + desc_bytes(a * kTile);
+        const uint32_t d = tmem + col_buf(gu + w);
         if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, dK + kmaj_step(k), br + kmaj_step(k), id_sd, k > 0);
-          mma_commit(&bars.s_full[(gs + v) & 1]);
-          if (v == nsub - 1) mma_commit(&bars.k_empty);  // the K tile is read by these MMAs only
+          for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, bk + kmaj_step(k), br + kmaj_step(k), id_sd, k > 0);
+          mma_commit(&bars.s_full[(gu + w) & 1]);
+          if (w == nu - 1) mma_commit(&bars.k_empty);  // the key tiles are read by these MMAs only
         }
         __syncwarp();
         issued = true;
         return true;
       };
       if (ok) ok = issue_sd(0);
-      if (ok) ok = issue_sd(1);
-      for (int v = 0; ok && v < nsub; ++v) {
-        const uint32_t g = gs + v;
+      if (ok && nu > 1) ok = issue_sd(1);
+      for (int w = 0; ok && w < nu; ++w) {
+        const uint32_t g = gu + w;
         ok = wait_warp(&bars.p_full[g & 1], (g >> 1) & 1, abort_flag, p.status);
-        if (ok && v == 0 && iw > 0) ok = wait_warp(&bars.acc_free, (iw - 1) & 1, abort_flag, p.status);
+        if (ok && w == 0 && iw > 0) ok = wait_warp(&bars.acc_free, (iw - 1) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t qg = gq + v / 2;
-        const int s = qg % kStages;
-        const uint64_t mr = dM0 + desc_bytes(s * kStageBytes + (v & 1) * kSubBytes);
-        const uint64_t mq = mr, mdo = mr + desc_bytes(kHalfRows * 128);
-        const uint32_t buf = tmem + col_buf(g);
+        const int v = nkb == 2 ? (w >> 1) : w, a = nkb == 2 ? (w & 1) : 0;
+        const int s = (gsub + v) % kStages;
+        const uint64_t mq = dM0 + desc_bytes(s * kStageBytes), mdo = mq + desc_bytes(kHalfRows * 128);
+        const uint32_t buf = tmem + col_buf(g), acc = tmem + col_acc(a);
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kHalfRows / 16; ++kk) {
             // acc += P^T dO_sub  and  acc += (scale dS)^T Q_sub
-            mma_ts(tmem + kColAcc, buf + kk * 8, mdo + mnmaj_step(kk), id_acc, (v > 0 || kk > 0) ? 1u : 0u);
-            mma_ts(tmem + kColAcc, buf + 32 + kk * 8, mq + mnmaj_step(kk), id_acc, 1u);
+            mma_ts(acc, buf + kk * 8, mdo + mnmaj_step(kk), id_acc, (v > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(acc, buf + 32 + kk * 8, mq + mnmaj_step(kk), id_acc, 1u);
           }
-          if (v & 1) mma_commit(&bars.st_empty[s]);
-          if (v == nsub - 1) mma_commit(&bars.acc_full);
+          if (a == nkb - 1) mma_commit(&bars.st_empty[s]);  // the sub-tile's last reader
+          if (w == nu - 1) mma_commit(&bars.acc_full);
         }
         __syncwarp();
-        if (v + 2 < nsub) {
-          ok = issue_sd(v + 2);
+        if (w + 2 < nu) {
+          ok = issue_sd(w + 2);
           if (!ok) break;
         }
       }
-      gq += nq;
-      gs += 2 * nq;
+      gsub += nsub;
+      gu += nu;
       ++iw;
     }
     if (!ok && issued) {
@@ -765,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kr = tid;  // key row == TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
     const uint64_t sl2x2 = f32x2(__float_as_uint(p.sl2), __float_as_uint(p.sl2));
-    uint32_t gq = 0, gs = 0, iw = 0;
+    uint32_t gsub = 0, gu = 0, iw = 0;
     bool ok = true;
     for (uint32_t kq = 0; ok; ++kq) {
       const int slot = kq % kItemRing;
@@ -775,35 +839,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u < 0) break;
       Item it;
       item_of(p, u, it);
-      const int nq = (it.tq_hi - it.tq_lo) * per_tile;
-      const int key = it.k0 + kr;
-      const bool key_ok = kr < it.n;
-      float *prow = it.comp ? p.partial + (((size_t)it.split * Q.B + it.b) * p.Sc_pad + key) * kHeadDim : nullptr;
-      __nv_bfloat16 *drow = it.comp ? nullptr : p.dkv + ((size_t)it.b * Q.S + key) * kHeadDim;
-      if (poisoned || nq <= 0) {
-        const float v = poisoned ? __int_as_float(0x7fc00000) : 0.f;
-        if (it.comp) {
-          float4 *dst = reinterpret_cast<float4 *>(prow);
+      const int nkb = it.nkb;
+      if (nkb == 0) continue;
+      const int nsub = 2 * (it.tq_hi - it.tq_lo) * per_tile;
+      float *prow[2];
 #pragma unroll
-          for (int c = 0; c < kHeadDim / 4; ++c) dst[c] = make_float4(v, v, v, v);
-        } else if (key_ok) {
-          const uint32_t w2 = pack_bf16x2(v, v);
-          uint4 *dst = reinterpret_cast<uint4 *>(drow);
+      for (int a = 0; a < 2; ++a) {
+        const size_t rows = it.comp ? (size_t)p.Sc_pad : (size_t)p.S_pad;
+        float *base = it.comp ? p.cpart : p.rpart;
+        const int sl = (it.comp || !p.raw_atomic) ? it.slot[a] : 0;
+        prow[a] = a < nkb ? base + (((size_t)sl * Q.B + it.b) * rows + it.k0[a] + kr) * kHeadDim : nullptr;
+      }
+      const bool atomic_rows = !it.comp && p.raw_atomic;
+      if (poisoned || nsub <= 0) {
+        const float val = poisoned ? __int_as_float(0x7fc00000) : 0.f;
+        for (int a = 0; a < nkb; ++a) {
+          float4 *dst = reinterpret_cast<float4 *>(prow[a]);
+          if (atomic_rows) {
+            if (poisoned)
+              for (int c = 0; c < kHeadDim / 4; ++c) atomicAdd(dst + c, make_float4(val, val, val, val));
+          } else {
 #pragma unroll
-          for (int c = 0; c < kHeadDim / 8; ++c) dst[c] = make_uint4(w2, w2, w2, w2);
+            for (int c = 0; c < kHeadDim / 4; ++c) dst[c] = make_float4(val, val, val, val);
+          }
         }
         continue;
       }
-      const int nsub = 2 * nq;
-      for (int v = 0; v < nsub; ++v) {
-        const uint32_t g = gs + v;
-        const uint32_t qg = gq + v / 2;
-        const uint8_t *st = smem + kOffStage + (qg % kStages) * kStageBytes;
-        const float *rs_nl = reinterpret_cast<const float *>(st + kOffRowstat) + (v & 1) * kHalfRows;
-        const float *rs_d = rs_nl + kRows;
-        const int2 *ivs = reinterpret_cast<const int2 *>(st + kOffIv);
-        if ((v & 1) == 0 &&
-            !wait_warp(&bars.st_full[qg % kStages], (qg / kStages) & 1, abort_flag, p.status)) { ok = false; break; }
+      const int nu = nsub * nkb;
+      for (int w = 0; w < nu; ++w) {
+        const int v = nkb == 2 ? (w >> 1) : w, a = nkb == 2 ? (w & 1) : 0;
+        const uint32_t g = gu + w;
+        const uint32_t sg = gsub + v;
+        const uint8_t *st = smem + kOffStage + (sg % kStages) * kStageBytes;
+        if (a == 0 &&
+            !wait_warp(&bars.st_full[sg % kStages], (sg / kStages) & 1, abort_flag, p.status)) { ok = false; break; }
         if (!wait_warp(&bars.s_full[g & 1], (g >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t base = lane_addr + col_buf(g);
@@ -812,27 +881,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(base + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
         tmem_ld32(base + 64, *reinterpret_cast<uint32_t(*)[32]>(sv + 64));
         tmem_ld32(base + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 96));
-        // visibility of this key for the 64 columns (query rows) of the sub-tile:
-        // row r = 64 sub + c sits at position r mod Pq
+        // visibility of this key for the 64 columns (query rows) of the
+        // sub-tile: column c sits at position c mod sub_pq of the sub-tile
+        const int key = it.k0[a] + kr;
         uint64_t vis = 0;
-        if (key_ok) {
-          const int row0 = (v & 1) * kHalfRows;
-          if (Q.Pq <= kHalfRows) {
-            uint64_t pat = 0;
-            for (int q = 0; q < Q.Pq; ++q) {
-              const int2 iv = ivs[q];
-              if (key >= iv.x && key <= iv.y) pat |= 1ull << q;
-            }
-            for (int w = Q.Pq; w < kHalfRows; w *= 2) pat |= pat << w;
-            vis = pat;
-          } else {
-            for (int c = 0; c < kHalfRows; ++c) {
-              const int2 iv = ivs[(row0 + c) % Q.Pq];
-              if (key >= iv.x && key <= iv.y) vis |= 1ull << c;
-            }
+        if (kr < it.n[a]) {
+          const int4 *ivs = reinterpret_cast<const int4 *>(st + kOffIv);
+          uint64_t pat = 0;
+          for (int q = 0; q < p.sub_pq; ++q) {
+            const int4 iv = ivs[q];
+            const int lo = it.comp ? iv.z : iv.x, hi = it.comp ? iv.w : iv.y;
+            if (key >= lo && key <= hi) pat |= 1ull << q;
           }
+          for (int wd = p.sub_pq; wd < kHalfRows; wd *= 2) pat |= pat << wd;
+          vis = pat;
         }
         tmem_wait_ld();
+        const float *rs_nl = reinterpret_cast<const float *>(st + kOffRowstat);
+        const float *rs_d = rs_nl + kHalfRows;
         uint32_t pk[32], dk[32];
         const float scale = p.scale;
 #pragma unroll
@@ -842,11 +908,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float t0, t1;
           f32x2_split(ffma2(f32x2(sv[c], sv[c + 1]), sl2x2, f32x2(__float_as_uint(nl.x), __float_as_uint(nl.y))),
                       t0, t1);
-          float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
-          if (!((vis >> c) & 1ull)) e0 = 0.f;
-          if (!((vis >> (c + 1)) & 1ull)) e1 = 0.f;
-          const float d0 = scale * e0 * (__uint_as_float(sv[64 + c]) - dl.x);
-          const float d1 = scale * e1 * (__uint_as_float(sv[64 + c + 1]) - dl.y);
+          const bool v0 = (vis >> c) & 1ull, v1 = (vis >> (c + 1)) & 1ull;
+          const float e0 = v0 ? ex2_approx(t0) : 0.f, e1 = v1 ? ex2_approx(t1) : 0.f;
+          const float d0 = v0 ? scale * e0 * (__uint_as_float(sv[64 + c]) - dl.x) : 0.f;
+          const float d1 = v1 ? scale * e1 * (__uint_as_float(sv[64 + c + 1]) - dl.y) : 0.f;
           pk[c >> 1] = pack_bf16x2(e0, e1);
           dk[c >> 1] = pack_bf16x2(d0, d1);
         }
@@ -857,37 +922,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars.p_full[g & 1]);
       }
       if (!ok) break;
-      // ---------------- item epilogue: the accumulator row of this key
+      // ---------------- item epilogue: this key's accumulator rows
       if (!wait_warp(&bars.acc_full, iw & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
-      uint32_t o[128];
-      tmem_ld32(lane_addr + kColAcc, *reinterpret_cast<uint32_t(*)[32]>(o));
-      tmem_ld32(lane_addr + kColAcc + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
-      tmem_ld32(lane_addr + kColAcc + 64, *reinterpret_cast<uint32_t(*)[32]>(o + 64));
-      tmem_ld32(lane_addr + kColAcc + 96, *reinterpret_cast<uint32_t(*)[32]>(o + 96));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars.acc_free);  // the next item's accumulation may start
-      if (it.comp) {
-        float4 *dst = reinterpret_cast<float4 *>(prow);
+      for (int a = 0; a < nkb; ++a) {
+        uint32_t o[128];
+        const uint32_t ab = lane_addr + col_acc(a);
+        tmem_ld32(ab, *reinterpret_cast<uint32_t(*)[32]>(o));
+        tmem_ld32(ab + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+        tmem_ld32(ab + 64, *reinterpret_cast<uint32_t(*)[32]>(o + 64));
+        tmem_ld32(ab + 96, *reinterpret_cast<uint32_t(*)[32]>(o + 96));
+        tmem_wait_ld();
+        if (a == nkb - 1) {
+          tc_fence_before();
+          mbar_arrive(&bars.acc_free);  // the next item's accumulation may start
+        }
+        float4 *dst = reinterpret_cast<float4 *>(prow[a]);
+        if (atomic_rows) {
 #pragma unroll
-        for (int x = 0; x < 32; ++x)
-          dst[x] = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]), __uint_as_float(o[4 * x + 2]),
-                               __uint_as_float(o[4 * x + 3]));
-      } else if (key_ok) {
-        uint4 *dst = reinterpret_cast<uint4 *>(drow);
+          for (int x = 0; x < 32; ++x)
+            atomicAdd(dst + x, make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
+                                           __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3])));
+        } else {
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          uint4 w4;
-          w4.x = pack_bf16x2(__uint_as_float(o[8 * x + 0]), __uint_as_float(o[8 * x + 1]));
-          w4.y = pack_bf16x2(__uint_as_float(o[8 * x + 2]), __uint_as_float(o[8 * x + 3]));
-          w4.z = pack_bf16x2(__uint_as_float(o[8 * x + 4]), __uint_as_float(o[8 * x + 5]));
-          w4.w = pack_bf16x2(__uint_as_float(o[8 * x + 6]), __uint_as_float(o[8 * x + 7]));
-          dst[x] = w4;
+          for (int x = 0; x < 32; ++x)
+            dst[x] = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]), __uint_as_float(o[4 * x + 2]),
+                                 __uint_as_float(o[4 * x + 3]));
         }
       }
-      gq += nq;
-      gs += 2 * nq;
+      gsub += nsub;
+      gu += nu;
       ++iw;
     }
   }
@@ -900,32 +964,85 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// kernel 3: dckv = sum of the split partials (fixed order)
+// kernel 3: dkv and dckv = sums of their partial slots, in a fixed order
 // ---------------------------------------------------------------------------
-__global__ void hca_bwd_reduce_kernel(const float *__restrict__ partial, __nv_bfloat16 *__restrict__ dckv, int B,
-                                      int Sc, int Sc_pad) {
-  const long long n4 = (long long)B * Sc * (kHeadDim / 4);
-  const size_t split_stride = (size_t)B * Sc_pad * kHeadDim;
-  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < n4; v += (long long)gridDim.x * blockDim.x) {
-    const int d4 = (int)(v % (kHeadDim / 4));
-    const long long row = v / (kHeadDim / 4);
-    const int b = (int)(row / Sc), j = (int)(row % Sc);
-    const size_t off = ((size_t)b * Sc_pad + j) * kHeadDim + d4 * 4;
+struct ReduceParams {
+  const float *rpart, *cpart;
+  __nv_bfloat16 *dkv, *dckv;
+  int B, S, Sc, S_pad, Sc_pad, nslot, nrb, nkb_comp, raw_atomic;
+};
+
+__global__ void hca_bwd_reduce_kernel(const ReduceParams p) {
+  const long long nraw4 = (long long)p.B * p.S * (kHeadDim / 4);
+  const long long ncomp4 = (long long)p.B * p.Sc * (kHeadDim / 4);
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nraw4 + ncomp4;
+       v += (long long)gridDim.x * blockDim.x) {
+    const bool comp = v >= nraw4;
+    const long long x = comp ? v - nraw4 : v;
+    const int d4 = (int)(x % (kHeadDim / 4));
+    const long long row = x / (kHeadDim / 4);
+    const int rows = comp ? p.Sc : p.S;
+    const int b = (int)(row / rows), key = (int)(row % rows);
+    const int kb = key / kBlockKeys;
+    int s_lo, s_hi;
+    size_t stride, off;
+    const float *base;
+    if (comp) {
+      // odd blocks only have pair slots; even blocks have lead slots and,
+      // when their odd partner exists, pair slots
+      s_lo = (kb & 1) ? dkk::kSplitLead : 0;
+      s_hi = ((kb & 1) || kb + 1 < p.nkb_comp) ? dkk::kSlotsComp : dkk::kSplitLead;
+      stride = (size_t)p.B * p.Sc_pad * kHeadDim;
+      off = ((size_t)b * p.Sc_pad + key) * kHeadDim + d4 * 4;
+      base = p.cpart;
+    } else {
+      // slot s holds query range kb + s; ranges past the sequence do not exist
+      s_lo = 0;
+      s_hi = p.raw_atomic ? 1 : min(p.nslot, p.nrb - kb);
+      stride = (size_t)p.B * p.S_pad * kHeadDim;
+      off = ((size_t)b * p.S_pad + key) * kHeadDim + d4 * 4;
+      base = p.rpart;
+    }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < kSplit; ++s) {
-      const float4 x = *reinterpret_cast<const float4 *>(partial + s * split_stride + off);
-      acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+    for (int s = s_lo; s < s_hi; ++s) {
+      const float4 y = *reinterpret_cast<const float4 *>(base + s * stride + off);
+      acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
     }
     uint2 o;
     o.x = pack_bf16x2(acc.x, acc.y);
     o.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2 *>(dckv + ((size_t)b * Sc + j) * kHeadDim + d4 * 4) = o;
+    __nv_bfloat16 *dst = comp ? p.dckv + ((size_t)b * p.Sc + key) * kHeadDim : p.dkv + ((size_t)b * p.S + key) * kHeadDim;
+    *reinterpret_cast<uint2 *>(dst + d4 * 4) = o;
   }
 }
 
 size_t rowstat_bytes(const QTiling &q) { return align_up((size_t)q.ntiles * 2 * kRows * sizeof(float)); }
 
 int sc_pad(int Sc) { return (Sc + kBlockKeys - 1) / kBlockKeys * kBlockKeys; }
+
+// Raw key blocks: query range j (positions [128 j, 128 j + 128)) sees blocks
+// j - nslot + 1 .. j, so a block collects nslot partial sums.  Windows longer
+// than a few blocks accumulate into one fp32 buffer with atomics instead.
+constexpr int kMaxRawSlots = 4;
+struct RawGeom {
+  int nrb, S_pad, nslot, npr, atomic;
+};
+RawGeom raw_geom(int S, int W) {
+  RawGeom g;
+  g.nrb = (S + kBlockKeys - 1) / kBlockKeys;
+  g.S_pad = g.nrb * kBlockKeys;
+  int ns = (int)(((long long)W + kBlockKeys - 2) / kBlockKeys) + 1;
+  if (ns > g.nrb) ns = g.nrb;
+  if (ns < 1) ns = 1;
+  g.nslot = ns;
+  g.npr = (ns + 1) / 2;
+  g.atomic = ns > kMaxRawSlots;
+  return g;
+}
+size_t rpart_bytes(int B, const RawGeom &g) {
+  return align_up((size_t)(g.atomic ? 1 : g.nslot) * B * g.S_pad * kHeadDim * sizeof(float));
+}
+size_t cpart_bytes(int B, int Sc) { return align_up((size_t)dkk::kSlotsComp * B * sc_pad(Sc) * kHeadDim * sizeof(float)); }
 
 }  // namespace
 
@@ -934,15 +1051,17 @@ bool tc_bwd_supported(int H, int D, int dtype) { return tc_shape_ok(H, D, dtype)
 size_t tc_bwd_scratch_bytes(int B, int H, int S, int D, int W, int m, int dtype) {
   if (!tc_shape_ok(H, D, dtype)) return 0;
   QTiling q = make_qtiling(nullptr, B, H, S, W, m);
-  return rowstat_bytes(q) + align_up((size_t)kSplit * B * sc_pad(q.Sc) * kHeadDim * sizeof(float));
+  return rowstat_bytes(q) + cpart_bytes(B, q.Sc) + rpart_bytes(B, raw_geom(S, W));
 }
 
 cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   const QTiling q = make_qtiling(a.sstart, a.B, a.H, a.S, a.W, a.m);
   const int Spad = sc_pad(q.Sc);
+  const RawGeom rg = raw_geom(a.S, a.W);
   char *ws = static_cast<char *>(a.scratch);
   float *rowstat = reinterpret_cast<float *>(ws);
-  float *partial = reinterpret_cast<float *>(ws + rowstat_bytes(q));
+  float *cpart = reinterpret_cast<float *>(ws + rowstat_bytes(q));
+  float *rpart = reinterpret_cast<float *>(ws + rowstat_bytes(q) + cpart_bytes(a.B, q.Sc));
   // dkv kernel: a 64-row half of a query tile is a head range when HG >= 2,
   // a position range when one head fills the tile
   const int sub_hg = q.HG >= 2 ? q.HG / 2 : 1;
@@ -991,20 +1110,27 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   DkvParams kp;
   kp.qt = q;
   kp.status = a.status_rw;
-  kp.rowstat = rowstat;
-  kp.dkv = static_cast<__nv_bfloat16 *>(a.dkv);
-  kp.partial = partial;
-  kp.nkb_raw = (a.S + kBlockKeys - 1) / kBlockKeys;
-  kp.nkb_comp = (q.Sc + kBlockKeys - 1) / kBlockKeys;
-  kp.Sc_pad = Spad;
   kp.next_item = a.status_rw + 16;  // in the workspace header (64 bytes past the status word)
+  kp.rowstat = rowstat;
+  kp.rpart = rpart;
+  kp.cpart = cpart;
+  kp.nrb = rg.nrb;
+  kp.nkb_comp = (q.Sc + kBlockKeys - 1) / kBlockKeys;
+  kp.S_pad = rg.S_pad;
+  kp.Sc_pad = Spad;
+  kp.nslot = rg.nslot;
+  kp.npr = rg.npr;
+  kp.raw_atomic = rg.atomic;
   kp.sub_pq = sub_pq;
   kp.sub_hg = sub_hg;
-  kp.nitems = (long long)a.B * kp.nkb_comp * kSplit + (long long)a.B * kp.nkb_raw;
+  kp.n_both = (long long)a.B * (kp.nkb_comp / 2) * dkk::kSplitBoth;
+  kp.n_lead = (long long)a.B * ((kp.nkb_comp + 1) / 2) * dkk::kSplitLead;
+  kp.nitems = kp.n_both + kp.n_lead + (long long)a.B * rg.nrb * rg.npr;
   kp.sl2 = sl2;
   kp.scale = a.scale;
   const long long g2 = kp.nitems < sms ? kp.nitems : sms;
   e = cudaMemsetAsync(kp.next_item, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess && rg.atomic) e = cudaMemsetAsync(rpart, 0, rpart_bytes(a.B, rg), st);
   if (e != cudaSuccess) return e;
   {
     ProfScope prof(kKBwdDkv, st);
@@ -1013,12 +1139,26 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   }
   if (e != cudaSuccess) return e;
 
-  const long long n4 = (long long)a.B * q.Sc * (kHeadDim / 4);
+  ReduceParams rp;
+  rp.rpart = rpart;
+  rp.cpart = cpart;
+  rp.dkv = static_cast<__nv_bfloat16 *>(a.dkv);
+  rp.dckv = static_cast<__nv_bfloat16 *>(a.dckv);
+  rp.B = a.B;
+  rp.S = a.S;
+  rp.Sc = q.Sc;
+  rp.S_pad = rg.S_pad;
+  rp.Sc_pad = Spad;
+  rp.nslot = rg.nslot;
+  rp.nrb = rg.nrb;
+  rp.nkb_comp = kp.nkb_comp;
+  rp.raw_atomic = rg.atomic;
+  const long long n4 = (long long)a.B * (a.S + q.Sc) * (kHeadDim / 4);
   if (n4 > 0) {
     int blocks = (int)((n4 + 255) / 256);
-    if (blocks > 4 * sms) blocks = 4 * sms;
+    if (blocks > 8 * sms) blocks = 8 * sms;
     ProfScope prof(kKBwdReduce, st);
-    hca_bwd_reduce_kernel<<<blocks, 256, 0, st>>>(partial, static_cast<__nv_bfloat16 *>(a.dckv), a.B, q.Sc, Spad);
+    hca_bwd_reduce_kernel<<<blocks, 256, 0, st>>>(rp);
     e = cudaGetLastError();
   }
   return e;

@@ -50,8 +50,9 @@ def test_workspace_is_linear_not_quadratic(lib):
     for bwd in (0, 1):
         a, b = f(65536, bwd), f(131072, bwd)
         assert 0 < a < b <= 2 * a + 4096 * 1024, (a, b)
-        # far below one byte per (query, key) pair
-        assert b < 131072 * 131072 // 64
+        # far below one byte per (query, key) pair (the backward keeps fp32
+        # partial sums per key block: a fixed number of slots per row)
+        assert b < 131072 * 131072 // 32
     assert lib.hca_workspace_size(1, 64, 1024, 128, 0, 128, 0, 0) == 0   # W < 1
     assert lib.hca_workspace_size(1, 64, 1024, 128, 128, 0, 0, 0) == 0   # m < 1
     assert lib.hca_workspace_size(1, 64, 1024, 128, 128, 128, 7, 0) == 0  # dtype
