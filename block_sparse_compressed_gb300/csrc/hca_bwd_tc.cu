@@ -40,8 +40,6 @@ using namespace tc;
 
 namespace {
 
-constexpr int kSoftmaxThreads = 128;
-constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -365,12 +363,28 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         tc_fence_before();
         mbar_arrive(&bars.s_free);
         const uint64_t nl2 = f32x2(__float_as_uint(-lse2), __float_as_uint(-lse2));
+        // warp-uniform cases: nothing visible, everything visible, or a mix
+        const bool none = __all_sync(0xffffffffu, vis == 0ull);
+        const bool all = __all_sync(0xffffffffu, vis == ~0ull);
+        if (none) {
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float t0, t1;
-          f32x2_split(ffma2(f32x2(pv[c], pv[c + 1]), sl2x2, nl2), t0, t1);
-          pv[c] = ((vis >> c) & 1ull) ? __float_as_uint(ex2_approx(t0)) : 0u;
-          pv[c + 1] = ((vis >> (c + 1)) & 1ull) ? __float_as_uint(ex2_approx(t1)) : 0u;
+          for (int c = 0; c < 64; ++c) pv[c] = 0u;
+        } else if (all) {
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            float t0, t1;
+            f32x2_split(ffma2(f32x2(pv[c], pv[c + 1]), sl2x2, nl2), t0, t1);
+            pv[c] = __float_as_uint(ex2_approx(t0));
+            pv[c + 1] = __float_as_uint(ex2_approx(t1));
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            float t0, t1;
+            f32x2_split(ffma2(f32x2(pv[c], pv[c + 1]), sl2x2, nl2), t0, t1);
+            pv[c] = ((vis >> c) & 1ull) ? __float_as_uint(ex2_approx(t0)) : 0u;
+            pv[c + 1] = ((vis >> (c + 1)) & 1ull) ? __float_as_uint(ex2_approx(t1)) : 0u;
+          }
         }
         if (!wait_warp(&bars.dp_full, gb & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
@@ -378,19 +392,26 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 32) {
           if (cb + c0 >= nk) break;
-          uint32_t dr[32];
-          tmem_ld32(lane_addr + kColDP + cb + c0, dr);
-          tmem_wait_ld();
           uint32_t packed[16];
+          if (none) {
 #pragma unroll
-          for (int x = 0; x < 32; x += 2) {
-            const int c = c0 + x;
-            // dS = P (dP - Delta); columns past the block (stale TMEM) are zero
-            float d0, d1;
-            f32x2_split(fmul2(f32x2(pv[c], pv[c + 1]), fadd2(f32x2(dr[x], dr[x + 1]), ndl2)), d0, d1);
-            d0 = ((vis >> c) & 1ull) ? d0 : 0.f;
-            d1 = ((vis >> (c + 1)) & 1ull) ? d1 : 0.f;
-            packed[x / 2] = pack_bf16x2(d0, d1);
+            for (int x = 0; x < 16; ++x) packed[x] = 0u;
+          } else {
+            uint32_t dr[32];
+            tmem_ld32(lane_addr + kColDP + cb + c0, dr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; x += 2) {
+              const int c = c0 + x;
+              // dS = P (dP - Delta); columns past the block (stale TMEM) are zero
+              float d0, d1;
+              f32x2_split(fmul2(f32x2(pv[c], pv[c + 1]), fadd2(f32x2(dr[x], dr[x + 1]), ndl2)), d0, d1);
+              if (!all) {
+                d0 = ((vis >> c) & 1ull) ? d0 : 0.f;
+                d1 = ((vis >> (c + 1)) & 1ull) ? d1 : 0.f;
+              }
+              packed[x / 2] = pack_bf16x2(d0, d1);
+            }
           }
           tmem_st16(lane_addr + kColDS + (cb + c0) / 2, packed);
         }
@@ -457,6 +478,10 @@ namespace dkk {
 // holds a sub-tile as one 128-row operand R = [Q_sub ; dO_sub] (64 rows each,
 // per 64-column half): a single N = 128 MMA K R^T yields S^T (columns 0-63)
 // and dP^T (columns 64-127) of the sub-tile for one key block.
+// two P^T/dS^T warpgroups (each owns 32 of a unit's 64 query columns and 64
+// of a key row's 128 accumulator columns), TMA warp, MMA warp
+constexpr int kEW = 256;
+constexpr int kThreads = kEW + 64;
 constexpr int kStages = 4;                     // sub-tiles in flight
 constexpr int kSubBytes = kTile;               // one operand R (two halves)
 constexpr int kHalfRows = 64;                  // rows of Q_sub (and of dO_sub)
@@ -466,8 +491,9 @@ constexpr int kStageBytes = kOffIv + 1024 + 512;  // 34 KB: every stage stays 1 
 constexpr int kOffK = 0;                       // key block tiles A | B
 constexpr int kOffStage = 2 * kTile;
 constexpr int kSmemBytes = kOffStage + kStages * kStageBytes + 1024;
-// TMEM: two [S^T | dP^T] buffers (P^T and dS^T overwrite their first 64
-// columns as packed bf16), then one fp32 accumulator per key block
+// TMEM: two [S^T | dP^T] buffers (packed bf16 P^T and dS^T overwrite the
+// S^T columns: query rows 0-31 at columns 0-15 / 16-31, rows 32-63 at 32-47 /
+// 48-63), then one fp32 accumulator per key block
 constexpr uint32_t kColAcc = 256;
 constexpr int kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_buf(uint32_t g) { return (g & 1u) * 128u; }
@@ -579,6 +605,44 @@ __device__ __forceinline__ void item_of(const DkvParams &p, long long u, Item &i
   }
 }
 
+// P^T and (scale dS^T) of one key row for 32 query columns of a unit:
+//   p = exp2(s * scale * log2e - lse * log2e),  ds = p * (scale dP - scale Delta)
+// sv holds the 32 S^T values then the 32 matching dP^T values; rs4 points at
+// the columns' (-lse*log2e) records, their Delta records 16 float4 further.
+// kMasked zeroes the columns whose bit in vis is clear.
+template <bool kMasked>
+__device__ __forceinline__ void ew_unit(const uint32_t (&sv)[64], const float4 *rs4, uint32_t vis, uint64_t sl2x2,
+                                        uint64_t sc2, uint32_t (&pk)[16], uint32_t (&dk)[16]) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 4) {
+    const float4 nl = rs4[c / 4];
+    const float4 dl = rs4[16 + c / 4];
+#pragma unroll
+    for (int h = 0; h < 4; h += 2) {
+      const float n0 = h ? nl.z : nl.x, n1 = h ? nl.w : nl.y;
+      const float d0 = h ? dl.z : dl.x, d1 = h ? dl.w : dl.y;
+      float t0, t1;
+      f32x2_split(ffma2(f32x2(sv[c + h], sv[c + h + 1]), sl2x2, f32x2(__float_as_uint(n0), __float_as_uint(n1))), t0,
+                  t1);
+      float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
+      // scale dP - scale Delta, then times p
+      const uint64_t g2 = ffma2(f32x2(sv[32 + c + h], sv[32 + c + h + 1]), sc2,
+                                fmul2(f32x2(__float_as_uint(-d0), __float_as_uint(-d1)), sc2));
+      float g0, g1;
+      f32x2_split(fmul2(f32x2(__float_as_uint(e0), __float_as_uint(e1)), g2), g0, g1);
+      if (kMasked) {
+        const bool v0 = (vis >> (c + h)) & 1u, v1 = (vis >> (c + h + 1)) & 1u;
+        e0 = v0 ? e0 : 0.f;
+        e1 = v1 ? e1 : 0.f;
+        g0 = v0 ? g0 : 0.f;
+        g1 = v1 ? g1 : 0.f;
+      }
+      pk[(c + h) >> 1] = pack_bf16x2(e0, e1);
+      dk[(c + h) >> 1] = pack_bf16x2(g0, g1);
+    }
+  }
+}
+
 constexpr int kItemRing = 4;
 
 struct DkvBars {
@@ -593,7 +657,7 @@ struct DkvBars {
   int abort;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(dkk::kThreads, 1)
     hca_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_qs, const __grid_constant__ CUtensorMap map_dos,
                        const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_ckv,
                        const DkvParams p) {
@@ -608,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kItemRing; ++i) {
       mbar_init(&bars.item_full[i], 1);
-      mbar_init(&bars.item_empty[i], 1 + kSoftmaxThreads);
+      mbar_init(&bars.item_empty[i], 1 + kEW);
     }
     mbar_init(&bars.k_full, 1);
     mbar_init(&bars.k_empty, 1);
@@ -618,10 +682,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars.s_full[x], 1);
-      mbar_init(&bars.p_full[x], kSoftmaxThreads);
+      mbar_init(&bars.p_full[x], kEW);
     }
     mbar_init(&bars.acc_full, 1);
-    mbar_init(&bars.acc_free, kSoftmaxThreads);
+    mbar_init(&bars.acc_free, kEW);
     mbar_init(&bars.drain, 1);
     bars.abort = 0;
     fence_mbar_init();
@@ -639,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // a sub-tile is a head range of its query tile when HG >= 2, a position range when one head fills it
   const bool pos_split = p.sub_hg == Q.HG;
 
-  if (warp == 4) {
+  if (warp == kEW / 32) {
     // ------------------------------------------------------------ TMA
     uint32_t gsub = 0, iw = 0;
     uint32_t issued = 0;  // bit s: stage loaded at least once; bit 8+s: parity of its last load
@@ -731,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (issued & (1u << s)) mbar_wait(&bars.st_full[s], (issued >> (8 + s)) & 1u, &never, p.status, 100000000ull);
       if (k_par >= 0) mbar_wait(&bars.k_full, k_par, &never, p.status, 100000000ull);
     }
-  } else if (warp == 5) {
+  } else if (warp == kEW / 32 + 1) {
     // ------------------------------------------------------------ MMA
     // Whole warp on warp-uniform values; one elect.sync lane issues.  Work
     // unit u of an item is (sub-tile u / nkb, key block u % nkb); its
@@ -800,9 +864,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kHalfRows / 16; ++kk) {
-            // acc += P^T dO_sub  and  acc += (scale dS)^T Q_sub
-            mma_ts(acc, buf + kk * 8, mdo + mnmaj_step(kk), id_acc, (v > 0 || kk > 0) ? 1u : 0u);
-            mma_ts(acc, buf + 32 + kk * 8, mq + mnmaj_step(kk), id_acc, 1u);
+            // acc += P^T dO_sub  and  acc += (scale dS)^T Q_sub; query rows
+            // [32 h, 32 h + 32) have P^T at columns 32 h .. 32 h + 15 and dS^T
+            // at 32 h + 16 .. 32 h + 31 (8 packed columns per k-step)
+            const uint32_t pc = (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8);
+            mma_ts(acc, buf + pc, mdo + mnmaj_step(kk), id_acc, (v > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(acc, buf + pc + 16, mq + mnmaj_step(kk), id_acc, 1u);
           }
           if (a == nkb - 1) mma_commit(&bars.st_empty[s]);  // the sub-tile's last reader
           if (w == nu - 1) mma_commit(&bars.acc_full);
@@ -826,9 +893,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ P^T, dS^T + item epilogue
-    const int kr = tid;  // key row == TMEM lane
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    // thread kr of warpgroup wg owns key row kr (TMEM lane kr), query columns
+    // [32 wg, 32 wg + 32) of every unit and accumulator columns [64 wg, 64 wg + 64)
+    const int kr = tid & (kRows - 1), wg = tid >> 7;
+    const int cq = wg * 32;
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint64_t sl2x2 = f32x2(__float_as_uint(p.sl2), __float_as_uint(p.sl2));
+    const uint64_t sc2 = f32x2(__float_as_uint(p.scale), __float_as_uint(p.scale));
     uint32_t gsub = 0, gu = 0, iw = 0;
     bool ok = true;
     for (uint32_t kq = 0; ok; ++kq) {
@@ -848,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t rows = it.comp ? (size_t)p.Sc_pad : (size_t)p.S_pad;
         float *base = it.comp ? p.cpart : p.rpart;
         const int sl = (it.comp || !p.raw_atomic) ? it.slot[a] : 0;
-        prow[a] = a < nkb ? base + (((size_t)sl * Q.B + it.b) * rows + it.k0[a] + kr) * kHeadDim : nullptr;
+        prow[a] = a < nkb ? base + (((size_t)sl * Q.B + it.b) * rows + it.k0[a] + kr) * kHeadDim + wg * 64 : nullptr;
       }
       const bool atomic_rows = !it.comp && p.raw_atomic;
       if (poisoned || nsub <= 0) {
@@ -857,10 +928,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float4 *dst = reinterpret_cast<float4 *>(prow[a]);
           if (atomic_rows) {
             if (poisoned)
-              for (int c = 0; c < kHeadDim / 4; ++c) atomicAdd(dst + c, make_float4(val, val, val, val));
+              for (int c = 0; c < 16; ++c) atomicAdd(dst + c, make_float4(val, val, val, val));
           } else {
 #pragma unroll
-            for (int c = 0; c < kHeadDim / 4; ++c) dst[c] = make_float4(val, val, val, val);
+            for (int c = 0; c < 16; ++c) dst[c] = make_float4(val, val, val, val);
           }
         }
         continue;
@@ -876,11 +947,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(&bars.s_full[g & 1], (g >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t base = lane_addr + col_buf(g);
-        uint32_t sv[128];
-        tmem_ld32(base, *reinterpret_cast<uint32_t(*)[32]>(sv));
-        tmem_ld32(base + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-        tmem_ld32(base + 64, *reinterpret_cast<uint32_t(*)[32]>(sv + 64));
-        tmem_ld32(base + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 96));
+        uint32_t sv[64];  // S^T columns [cq, cq + 32), then dP^T columns [64 + cq, 64 + cq + 32)
+        tmem_ld32(base + cq, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        tmem_ld32(base + 64 + cq, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
         // visibility of this key for the 64 columns (query rows) of the
         // sub-tile: column c sits at position c mod sub_pq of the sub-tile
         const int key = it.k0[a] + kr;
@@ -896,27 +965,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int wd = p.sub_pq; wd < kHalfRows; wd *= 2) pat |= pat << wd;
           vis = pat;
         }
+        const uint32_t vis32 = (uint32_t)(vis >> cq);
         tmem_wait_ld();
-        const float *rs_nl = reinterpret_cast<const float *>(st + kOffRowstat);
-        const float *rs_d = rs_nl + kHalfRows;
-        uint32_t pk[32], dk[32];
-        const float scale = p.scale;
+        // -lse*log2e [64] then Delta [64] of the sub-tile's rows, from column cq
+        const float4 *rs4 = reinterpret_cast<const float4 *>(st + kOffRowstat) + cq / 4;
+        uint32_t pk[16], dk[16];
+        // warp-uniform cases: no visible pair (P^T = dS^T = 0), every pair
+        // visible (no masking), or a mix
+        const bool none = __all_sync(0xffffffffu, vis32 == 0u);
+        const bool all = __all_sync(0xffffffffu, vis32 == ~0u);
+        if (none) {
 #pragma unroll
-        for (int c = 0; c < kHalfRows; c += 2) {
-          const float2 nl = *reinterpret_cast<const float2 *>(rs_nl + c);
-          const float2 dl = *reinterpret_cast<const float2 *>(rs_d + c);
-          float t0, t1;
-          f32x2_split(ffma2(f32x2(sv[c], sv[c + 1]), sl2x2, f32x2(__float_as_uint(nl.x), __float_as_uint(nl.y))),
-                      t0, t1);
-          const bool v0 = (vis >> c) & 1ull, v1 = (vis >> (c + 1)) & 1ull;
-          const float e0 = v0 ? ex2_approx(t0) : 0.f, e1 = v1 ? ex2_approx(t1) : 0.f;
-          const float d0 = v0 ? scale * e0 * (__uint_as_float(sv[64 + c]) - dl.x) : 0.f;
-          const float d1 = v1 ? scale * e1 * (__uint_as_float(sv[64 + c + 1]) - dl.y) : 0.f;
-          pk[c >> 1] = pack_bf16x2(e0, e1);
-          dk[c >> 1] = pack_bf16x2(d0, d1);
+          for (int c = 0; c < 16; ++c) pk[c] = dk[c] = 0u;
+        } else if (all) {
+          ew_unit<false>(sv, rs4, 0u, sl2x2, sc2, pk, dk);
+        } else {
+          ew_unit<true>(sv, rs4, vis32, sl2x2, sc2, pk, dk);
         }
-        tmem_st32(base, pk);
-        tmem_st32(base + 32, dk);
+        // packed P^T and dS^T of these 32 query rows go over the 32 S^T
+        // columns this thread read (the other warpgroup reads other columns)
+        tmem_st16(base + cq, pk);
+        tmem_st16(base + cq + 16, dk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars.p_full[g & 1]);
@@ -926,12 +995,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_warp(&bars.acc_full, iw & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       for (int a = 0; a < nkb; ++a) {
-        uint32_t o[128];
-        const uint32_t ab = lane_addr + col_acc(a);
+        uint32_t o[64];
+        const uint32_t ab = lane_addr + col_acc(a) + wg * 64;
         tmem_ld32(ab, *reinterpret_cast<uint32_t(*)[32]>(o));
         tmem_ld32(ab + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
-        tmem_ld32(ab + 64, *reinterpret_cast<uint32_t(*)[32]>(o + 64));
-        tmem_ld32(ab + 96, *reinterpret_cast<uint32_t(*)[32]>(o + 96));
         tmem_wait_ld();
         if (a == nkb - 1) {
           tc_fence_before();
@@ -940,12 +1007,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float4 *dst = reinterpret_cast<float4 *>(prow[a]);
         if (atomic_rows) {
 #pragma unroll
-          for (int x = 0; x < 32; ++x)
+          for (int x = 0; x < 16; ++x)
             atomicAdd(dst + x, make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
                                            __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3])));
         } else {
 #pragma unroll
-          for (int x = 0; x < 32; ++x)
+          for (int x = 0; x < 16; ++x)
             dst[x] = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]), __uint_as_float(o[4 * x + 2]),
                                  __uint_as_float(o[4 * x + 3]));
         }
@@ -1134,7 +1201,7 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   {
     ProfScope prof(kKBwdDkv, st);
-    hca_bwd_dkv_kernel<<<(unsigned)g2, kThreads, dkk::kSmemBytes, st>>>(mqs, mdos, mkv, mckv, kp);
+    hca_bwd_dkv_kernel<<<(unsigned)g2, dkk::kThreads, dkk::kSmemBytes, st>>>(mqs, mdos, mkv, mckv, kp);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;

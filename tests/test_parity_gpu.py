@@ -79,6 +79,16 @@ def test_long_window_multiple_raw_blocks(B):
     run_case(B, 16, S, 128, 333, 64, torch.bfloat16, seg)
 
 
+@pytest.mark.parametrize("W", [390, 600])
+def test_long_window_atomic_raw_partials(W):
+    # windows longer than four 128-key blocks: the key-major backward sums the
+    # raw blocks' partials with fp32 atomics instead of per-range slots
+    rng = np.random.Generator(np.random.PCG64(W))
+    S = 900
+    seg = np.stack([I.random_layout(S, rng, allow_pad=True) for _ in range(2)])
+    run_case(2, 16, S, 128, W, 64, torch.bfloat16, seg)
+
+
 def test_segments_off_boundary_and_short_docs_bf16():
     # documents starting off an m-boundary, one shorter than W and than m,
     # and padding at the end
