@@ -51,7 +51,11 @@ constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;  // dS: 
 constexpr int kTmemCols = 512;
 // two dS warpgroups (each owns 64 of a row's 128 key columns), TMA warp, MMA warp
 constexpr int kEW = 256;
-constexpr int kThreads = kEW + 64;
+constexpr int kThreads = kEW + 128;
+// 12 warps put 3 on each SM sub-partition (16K registers each): 168 per
+// thread at launch; the TMA/MMA warpgroup gives registers to the other two
+constexpr int kRegEW = 208, kRegProducer = 88;
+static_assert(2 * 128 * kRegEW + 128 * kRegProducer <= kThreads * 168, "register split must fit the launch");
 // shared memory: Q | dO | out (for Delta) | kv ring | dq staging (+1 KB align)
 constexpr int kOffQ = 0, kOffDO = kTile, kOffO = 2 * kTile, kOffKV = 3 * kTile;
 constexpr int kOffOut = kOffKV + kStages * kTile;
@@ -124,149 +128,153 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   const bool poisoned = *(volatile const int32_t *)p.status != 0;
 
-  if (warp == kEW / 32) {
-    // ------------------------------------------------------------ TMA
-    uint32_t gb = 0, tw = 0;
-    int last_par[kStages] = {-1, -1, -1};
-    int q_par = -1;
-    bool ok = !poisoned;
-    for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
-      Tile t;
-      tile_coords(Q, u, t);
-      tile_ranges_warp(Q, t, lane);
-      const int nb = t.nraw + t.ncomp;
-      if (nb == 0) continue;
-      if (lane == 0) {
-        if (tw > 0) ok = mbar_wait(&bars.qd_empty, (tw - 1) & 1, abort_flag, p.status);
-        if (ok) {
-          mbar_arrive_expect_tx(&bars.qd_full, 3 * kTile);
-          const int c2 = t.b * Q.H + t.g * Q.HG;
-          tma_load_3d(&map_q, &bars.qd_full, smem + kOffQ, 0, t.i0, c2);
-          tma_load_3d(&map_q, &bars.qd_full, smem + kOffQ + kHalfTile, 64, t.i0, c2);
-          tma_load_3d(&map_do, &bars.qd_full, smem + kOffDO, 0, t.i0, c2);
-          tma_load_3d(&map_do, &bars.qd_full, smem + kOffDO + kHalfTile, 64, t.i0, c2);
-          tma_load_3d(&map_out, &bars.qd_full, smem + kOffO, 0, t.i0, c2);
-          tma_load_3d(&map_out, &bars.qd_full, smem + kOffO + kHalfTile, 64, t.i0, c2);
-          q_par = tw & 1;
+  if (warp >= kEW / 32) {
+    setmaxnreg_dec<kRegProducer>();
+    if (warp == kEW / 32) {
+      // ------------------------------------------------------------ TMA
+      uint32_t gb = 0, tw = 0;
+      int last_par[kStages] = {-1, -1, -1};
+      int q_par = -1;
+      bool ok = !poisoned;
+      for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
+        Tile t;
+        tile_coords(Q, u, t);
+        tile_ranges_warp(Q, t, lane);
+        const int nb = t.nraw + t.ncomp;
+        if (nb == 0) continue;
+        if (lane == 0) {
+          if (tw > 0) ok = mbar_wait(&bars.qd_empty, (tw - 1) & 1, abort_flag, p.status);
+          if (ok) {
+            mbar_arrive_expect_tx(&bars.qd_full, 3 * kTile);
+            const int c2 = t.b * Q.H + t.g * Q.HG;
+            tma_load_3d(&map_q, &bars.qd_full, smem + kOffQ, 0, t.i0, c2);
+            tma_load_3d(&map_q, &bars.qd_full, smem + kOffQ + kHalfTile, 64, t.i0, c2);
+            tma_load_3d(&map_do, &bars.qd_full, smem + kOffDO, 0, t.i0, c2);
+            tma_load_3d(&map_do, &bars.qd_full, smem + kOffDO + kHalfTile, 64, t.i0, c2);
+            tma_load_3d(&map_out, &bars.qd_full, smem + kOffO, 0, t.i0, c2);
+            tma_load_3d(&map_out, &bars.qd_full, smem + kOffO + kHalfTile, 64, t.i0, c2);
+            q_par = tw & 1;
+          }
+          for (int j = 0; ok && j < nb; ++j, ++gb) {
+            const int s = gb % kStages;
+            if (gb >= (uint32_t)kStages)
+              ok = mbar_wait(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status);
+            if (!ok) break;
+            bool comp;
+            int start, n;
+            block_of(t, j, comp, start, n);
+            const CUtensorMap *mp = comp ? &map_ckv : &map_kv;
+            uint8_t *dst = smem + kOffKV + s * kTile;
+            mbar_arrive_expect_tx(&bars.kv_full[s], kTile);
+            tma_load_3d(mp, &bars.kv_full[s], dst, 0, start, t.b);
+            tma_load_3d(mp, &bars.kv_full[s], dst + kHalfTile, 64, start, t.b);
+            last_par[s] = (gb / kStages) & 1;
+          }
         }
-        for (int j = 0; ok && j < nb; ++j, ++gb) {
-          const int s = gb % kStages;
-          if (gb >= (uint32_t)kStages)
-            ok = mbar_wait(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status);
-          if (!ok) break;
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        gb = __shfl_sync(0xffffffffu, gb, 0);
+        ++tw;
+      }
+      if (!ok && !poisoned && lane == 0) {
+        volatile int never = 0;
+        for (int s = 0; s < kStages; ++s)
+          if (last_par[s] >= 0) mbar_wait(&bars.kv_full[s], last_par[s], &never, p.status, 100000000ull);
+        if (q_par >= 0) mbar_wait(&bars.qd_full, q_par, &never, p.status, 100000000ull);
+      }
+    } else if (warp == kEW / 32 + 1) {
+      // ------------------------------------------------------------ MMA
+      // Whole warp, warp-uniform values, one elect.sync lane issues (cheap
+      // tcgen05.mma issue from uniform registers; see the forward kernel).
+      // Per key block j the order is  S(j+1) | dq(j) | dP(j+1):  S(j+1) goes
+      // out as soon as the dS warps hold P(j) in registers, so the tensor pipe
+      // runs it while they form dS(j).  dP(j+1) overwrites dP(j) only after
+      // dS(j) is stored, and its commit also covers dq(j) (one thread's MMAs
+      // complete in order), so dS(j+1) never overwrites a dS that an
+      // unfinished dq MMA still reads.
+      const uint64_t dQ = smem_desc_sw128(smem_u32(smem + kOffQ), 16, 1024);
+      const uint64_t dDO = smem_desc_sw128(smem_u32(smem + kOffDO), 16, 1024);
+      const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + kOffKV), 16, 1024);
+      const uint64_t dV0 = smem_desc_sw128(smem_u32(smem + kOffKV), kHalfTile, 1024);
+      const uint32_t id_dq = idesc_bf16_f32(kRows, kHeadDim, false, true);
+      uint32_t gb = 0, tw = 0;
+      bool ok = !poisoned, issued = false;
+      for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
+        Tile t;
+        tile_coords(Q, u, t);
+        tile_ranges_warp(Q, t, lane);
+        uniform_tile(t);
+        const int nb = t.nraw + t.ncomp;
+        if (nb == 0) continue;
+        // S (x = 0) or dP (x = 1) of block j into its TMEM columns
+        auto issue_sdp = [&](int x, int j, uint32_t g, bool last_q_use) {
           bool comp;
           int start, n;
           block_of(t, j, comp, start, n);
-          const CUtensorMap *mp = comp ? &map_ckv : &map_kv;
-          uint8_t *dst = smem + kOffKV + s * kTile;
-          mbar_arrive_expect_tx(&bars.kv_full[s], kTile);
-          tma_load_3d(mp, &bars.kv_full[s], dst, 0, start, t.b);
-          tma_load_3d(mp, &bars.kv_full[s], dst + kHalfTile, 64, start, t.b);
-          last_par[s] = (gb / kStages) & 1;
+          const uint32_t idesc = idesc_bf16_f32(kRows, (n + 15) & ~15, false, false);
+          const uint64_t bk = dK0 + desc_bytes((g % kStages) * kTile);
+          const uint64_t da = x ? dDO : dQ;
+          const uint32_t d = tmem + (x ? kColDP : kColS);
+          if (elect_one()) {
+  #pragma unroll
+            for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, da + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
+            mma_commit(x ? &bars.dp_full : &bars.s_full);
+            if (last_q_use) mma_commit(&bars.qd_empty);
+          }
+          __syncwarp();
+          issued = true;
+        };
+        ok = wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status);
+        if (ok) ok = wait_warp(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status);
+        // the previous tile's last S must have been read out
+        if (ok && gb > 0) ok = wait_warp(&bars.s_free, (gb - 1) & 1, abort_flag, p.status);
+        if (ok) {
+          tc_fence_after();
+          issue_sdp(0, 0, gb, false);
+          issue_sdp(1, 0, gb, nb == 1);
         }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      gb = __shfl_sync(0xffffffffu, gb, 0);
-      ++tw;
-    }
-    if (!ok && !poisoned && lane == 0) {
-      volatile int never = 0;
-      for (int s = 0; s < kStages; ++s)
-        if (last_par[s] >= 0) mbar_wait(&bars.kv_full[s], last_par[s], &never, p.status, 100000000ull);
-      if (q_par >= 0) mbar_wait(&bars.qd_full, q_par, &never, p.status, 100000000ull);
-    }
-  } else if (warp == kEW / 32 + 1) {
-    // ------------------------------------------------------------ MMA
-    // Whole warp, warp-uniform values, one elect.sync lane issues (cheap
-    // tcgen05.mma issue from uniform registers; see the forward kernel).
-    // Per key block j the order is  S(j+1) | dq(j) | dP(j+1):  S(j+1) goes
-    // out as soon as the dS warps hold P(j) in registers, so the tensor pipe
-    // runs it while they form dS(j).  dP(j+1) overwrites dP(j) only after
-    // dS(j) is stored, and its commit also covers dq(j) (one thread's MMAs
-    // complete in order), so dS(j+1) never overwrites a dS that an
-    // unfinished dq MMA still reads.
-    const uint64_t dQ = smem_desc_sw128(smem_u32(smem + kOffQ), 16, 1024);
-    const uint64_t dDO = smem_desc_sw128(smem_u32(smem + kOffDO), 16, 1024);
-    const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + kOffKV), 16, 1024);
-    const uint64_t dV0 = smem_desc_sw128(smem_u32(smem + kOffKV), kHalfTile, 1024);
-    const uint32_t id_dq = idesc_bf16_f32(kRows, kHeadDim, false, true);
-    uint32_t gb = 0, tw = 0;
-    bool ok = !poisoned, issued = false;
-    for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
-      Tile t;
-      tile_coords(Q, u, t);
-      tile_ranges_warp(Q, t, lane);
-      uniform_tile(t);
-      const int nb = t.nraw + t.ncomp;
-      if (nb == 0) continue;
-      // S (x = 0) or dP (x = 1) of block j into its TMEM columns
-      auto issue_sdp = [&](int x, int j, uint32_t g, bool last_q_use) {
-        bool comp;
-        int start, n;
-        block_of(t, j, comp, start, n);
-        const uint32_t idesc = idesc_bf16_f32(kRows, (n + 15) & ~15, false, false);
-        const uint64_t bk = dK0 + desc_bytes((g % kStages) * kTile);
-        const uint64_t da = x ? dDO : dQ;
-        const uint32_t d = tmem + (x ? kColDP : kColS);
-        if (elect_one()) {
-#pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, da + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
-          mma_commit(x ? &bars.dp_full : &bars.s_full);
-          if (last_q_use) mma_commit(&bars.qd_empty);
-        }
-        __syncwarp();
-        issued = true;
-      };
-      ok = wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status);
-      if (ok) ok = wait_warp(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status);
-      // the previous tile's last S must have been read out
-      if (ok && gb > 0) ok = wait_warp(&bars.s_free, (gb - 1) & 1, abort_flag, p.status);
-      if (ok) {
-        tc_fence_after();
-        issue_sdp(0, 0, gb, false);
-        issue_sdp(1, 0, gb, nb == 1);
-      }
-      for (int j = 0; ok && j < nb; ++j) {
-        const uint32_t g = gb + j;
-        const bool next = j + 1 < nb;
-        if (next) {
-          ok = wait_warp(&bars.s_free, g & 1, abort_flag, p.status);
-          if (ok) ok = wait_warp(&bars.kv_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag, p.status);
+        for (int j = 0; ok && j < nb; ++j) {
+          const uint32_t g = gb + j;
+          const bool next = j + 1 < nb;
+          if (next) {
+            ok = wait_warp(&bars.s_free, g & 1, abort_flag, p.status);
+            if (ok) ok = wait_warp(&bars.kv_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_sdp(0, j + 1, g + 1, false);
+          }
+          ok = wait_warp(&bars.ds_full, g & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          issue_sdp(0, j + 1, g + 1, false);
+          bool comp;
+          int start, n;
+          block_of(t, j, comp, start, n);
+          const int nks = (n + 15) >> 4;
+          const int s = g % kStages;
+          const uint64_t bv = dV0 + desc_bytes(s * kTile);
+          if (elect_one()) {
+  #pragma unroll
+            for (int kk = 0; kk < kBlockKeys / 16; ++kk)
+              if (kk < nks)
+                mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, bv + mnmaj_step(kk), id_dq, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bars.kv_empty[s]);
+            if (!next) mma_commit(&bars.dq_done);
+          }
+          __syncwarp();
+          if (next) issue_sdp(1, j + 1, g + 1, j + 1 == nb - 1);
         }
-        ok = wait_warp(&bars.ds_full, g & 1, abort_flag, p.status);
-        if (!ok) break;
-        tc_fence_after();
-        bool comp;
-        int start, n;
-        block_of(t, j, comp, start, n);
-        const int nks = (n + 15) >> 4;
-        const int s = g % kStages;
-        const uint64_t bv = dV0 + desc_bytes(s * kTile);
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < kBlockKeys / 16; ++kk)
-            if (kk < nks)
-              mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, bv + mnmaj_step(kk), id_dq, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars.kv_empty[s]);
-          if (!next) mma_commit(&bars.dq_done);
-        }
-        __syncwarp();
-        if (next) issue_sdp(1, j + 1, g + 1, j + 1 == nb - 1);
+        gb += nb;
+        ++tw;
       }
-      gb += nb;
-      ++tw;
-    }
-    if (!ok && issued) {
-      volatile int never = 0;
-      if (elect_one()) mma_commit(&bars.drain);
-      __syncwarp();
-      if (lane == 0) mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
-      __syncwarp();
+      if (!ok && issued) {
+        volatile int never = 0;
+        if (elect_one()) mma_commit(&bars.drain);
+        __syncwarp();
+        if (lane == 0) mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+        __syncwarp();
+      }
     }
   } else {
+    setmaxnreg_inc<kRegEW>();
     // ------------------------------------------------------------ dS + epilogue
     // thread r of warpgroup wg owns row r (TMEM lane r) and key columns
     // [64 wg, 64 wg + 64) of every block (and dq columns [64 wg, 64 wg + 64))
@@ -478,10 +486,14 @@ namespace dkk {
 // holds a sub-tile as one 128-row operand R = [Q_sub ; dO_sub] (64 rows each,
 // per 64-column half): a single N = 128 MMA K R^T yields S^T (columns 0-63)
 // and dP^T (columns 64-127) of the sub-tile for one key block.
-// two P^T/dS^T warpgroups (each owns 32 of a unit's 64 query columns and 64
-// of a key row's 128 accumulator columns), TMA warp, MMA warp
+// two P^T/dS^T warpgroups (each takes every other work unit, i.e. one TMEM
+// buffer, and 64 of a key row's 128 accumulator columns), TMA warp, MMA warp
 constexpr int kEW = 256;
-constexpr int kThreads = kEW + 64;
+constexpr int kThreads = kEW + 128;
+// 12 warps put 3 on each SM sub-partition (16K registers each): 168 per
+// thread at launch; the TMA/MMA warpgroup gives registers to the other two
+constexpr int kRegEW = 208, kRegProducer = 88;
+static_assert(2 * 128 * kRegEW + 128 * kRegProducer <= kThreads * 168, "register split must fit the launch");
 constexpr int kStages = 4;                     // sub-tiles in flight
 constexpr int kSubBytes = kTile;               // one operand R (two halves)
 constexpr int kHalfRows = 64;                  // rows of Q_sub (and of dO_sub)
@@ -682,7 +694,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars.s_full[x], 1);
-      mbar_init(&bars.p_full[x], kEW);
+      mbar_init(&bars.p_full[x], kEW / 2);  // one warpgroup per buffer
     }
     mbar_init(&bars.acc_full, 1);
     mbar_init(&bars.acc_free, kEW);
@@ -703,200 +715,204 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
   // a sub-tile is a head range of its query tile when HG >= 2, a position range when one head fills it
   const bool pos_split = p.sub_hg == Q.HG;
 
-  if (warp == kEW / 32) {
-    // ------------------------------------------------------------ TMA
-    uint32_t gsub = 0, iw = 0;
-    uint32_t issued = 0;  // bit s: stage loaded at least once; bit 8+s: parity of its last load
-    int k_par = -1;
-    bool ok = true;
-    // Items are handed out dynamically (largest first) through a global
-    // counter; this warp fetches them and publishes each to the other roles.
-    for (uint32_t k = 0; ok; ++k) {
-      const int slot = k % kItemRing;
-      long long u = -1;
-      if (lane == 0) {
-        if (k >= (uint32_t)kItemRing)
-          ok = mbar_wait(&bars.item_empty[slot], ((k / kItemRing) - 1) & 1, abort_flag, p.status);
-        if (ok) {
-          u = atomicAdd(p.next_item, 1);
-          if (u >= p.nitems) u = -1;
-          bars.item[slot] = u;
-          mbar_arrive(&bars.item_full[slot]);
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      u = __shfl_sync(0xffffffffu, u, 0);
-      if (!ok || u < 0) break;
-      if (poisoned) continue;
-      Item it;
-      item_of(p, u, it);
-      const int nsub = 2 * (it.tq_hi - it.tq_lo) * per_tile;
-      if (it.nkb == 0 || nsub <= 0) continue;
-      if (lane == 0) {
-        if (iw > 0) ok = mbar_wait(&bars.k_empty, (iw - 1) & 1, abort_flag, p.status);
-        if (ok) {
-          const CUtensorMap *mp = it.comp ? &map_ckv : &map_kv;
-          mbar_arrive_expect_tx(&bars.k_full, it.nkb * kTile);
-          for (int a = 0; a < it.nkb; ++a) {
-            uint8_t *dst = smem + kOffK + a * kTile;
-            tma_load_3d(mp, &bars.k_full, dst, 0, it.k0[a], it.b);
-            tma_load_3d(mp, &bars.k_full, dst + kHalfTile, 64, it.k0[a], it.b);
-          }
-          k_par = iw & 1;
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      for (int v = 0; ok && v < nsub; ++v, ++gsub) {
-        const int x = v >> 1, sub = v & 1;
-        const int tq = it.tq_lo + x / per_tile, g = x % per_tile;
-        const int s = gsub % kStages;
-        uint8_t *st = smem + kOffStage + s * kStageBytes;
-        if (lane == 0 && gsub >= (uint32_t)kStages)
-          ok = mbar_wait(&bars.st_empty[s], ((gsub / kStages) - 1) & 1, abort_flag, p.status);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        const int i0 = tq * Q.Pq;
-        const int pos0 = pos_split ? i0 + sub * p.sub_pq : i0;
-        const int hd = it.b * Q.H + g * Q.HG + (pos_split ? 0 : sub * p.sub_hg);
-        // key intervals of the sub-tile's positions (both kinds)
-        int4 *ivs = reinterpret_cast<int4 *>(st + kOffIv);
-        for (int c = lane; c < p.sub_pq; c += 32) {
-          const RowIv iv = row_interval(Q.sstart, it.b, Q.S, pos0 + c, Q.W, Q.m);
-          ivs[c] = iv.valid ? make_int4(iv.rlo, iv.rhi, iv.clo, iv.chi) : make_int4(1, 0, 1, 0);
-        }
-        __syncwarp();
+  if (warp >= kEW / 32) {
+    setmaxnreg_dec<kRegProducer>();
+    if (warp == kEW / 32) {
+      // ------------------------------------------------------------ TMA
+      uint32_t gsub = 0, iw = 0;
+      uint32_t issued = 0;  // bit s: stage loaded at least once; bit 8+s: parity of its last load
+      int k_par = -1;
+      bool ok = true;
+      // Items are handed out dynamically (largest first) through a global
+      // counter; this warp fetches them and publishes each to the other roles.
+      for (uint32_t k = 0; ok; ++k) {
+        const int slot = k % kItemRing;
+        long long u = -1;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bars.st_full[s], kSubBytes + 512);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tma_load_3d(&map_qs, &bars.st_full[s], st + h * kHalfTile, 64 * h, pos0, hd);
-            tma_load_3d(&map_dos, &bars.st_full[s], st + h * kHalfTile + kHalfRows * 128, 64 * h, pos0, hd);
+          if (k >= (uint32_t)kItemRing)
+            ok = mbar_wait(&bars.item_empty[slot], ((k / kItemRing) - 1) & 1, abort_flag, p.status);
+          if (ok) {
+            u = atomicAdd(p.next_item, 1);
+            if (u >= p.nitems) u = -1;
+            bars.item[slot] = u;
+            mbar_arrive(&bars.item_full[slot]);
           }
-          // rows [64 sub, 64 sub + 64) of the tile's (-lse*log2e, Delta) record
-          const long long tl = ((long long)it.b * Q.groups + g) * Q.ntq + tq;
-          const float *rs = p.rowstat + tl * 2 * kRows + sub * kHalfRows;
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    smem_u32(st + kOffRowstat + h * 256)),
-                "l"(reinterpret_cast<uint64_t>(rs + h * kRows)), "r"(256), "r"(smem_u32(&bars.st_full[s]))
-                : "memory");
-          issued = (issued | (1u << s)) & ~(1u << (8 + s));
-          issued |= ((gsub / kStages) & 1u) << (8 + s);
         }
-        __syncwarp();
-      }
-      ++iw;
-    }
-    if (!ok && !poisoned && lane == 0) {
-      volatile int never = 0;
-      for (int s = 0; s < kStages; ++s)
-        if (issued & (1u << s)) mbar_wait(&bars.st_full[s], (issued >> (8 + s)) & 1u, &never, p.status, 100000000ull);
-      if (k_par >= 0) mbar_wait(&bars.k_full, k_par, &never, p.status, 100000000ull);
-    }
-  } else if (warp == kEW / 32 + 1) {
-    // ------------------------------------------------------------ MMA
-    // Whole warp on warp-uniform values; one elect.sync lane issues.  Work
-    // unit u of an item is (sub-tile u / nkb, key block u % nkb); its
-    // S^T | dP^T goes to TMEM buffer (global unit count) & 1, so the dS warps
-    // form P^T, dS^T of one unit while the tensor pipe runs the next.
-    const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + kOffK), 16, 1024);
-    const uint64_t dR0 = smem_desc_sw128(smem_u32(smem + kOffStage), 16, 1024);          // R, K-major
-    const uint64_t dM0 = smem_desc_sw128(smem_u32(smem + kOffStage), kHalfTile, 1024);   // R rows, MN-major
-    const uint32_t id_sd = idesc_bf16_f32(kRows, kRows, false, false);
-    const uint32_t id_acc = idesc_bf16_f32(kRows, kHeadDim, false, true);
-    uint32_t gsub = 0, gu = 0, iw = 0;  // sub-tiles, units and items with work so far
-    bool ok = true, issued = false;
-    for (uint32_t kq = 0; ok; ++kq) {
-      const int slot = kq % kItemRing;
-      long long u = -1;
-      if (lane == 0) {
-        ok = mbar_wait(&bars.item_full[slot], (kq / kItemRing) & 1, abort_flag, p.status);
-        if (ok) {
-          u = bars.item[slot];
-          mbar_arrive(&bars.item_empty[slot]);
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      u = __shfl_sync(0xffffffffu, u, 0);
-      if (!ok || u < 0) break;
-      if (poisoned) continue;
-      Item it;
-      item_of(p, u, it);
-      const int nsub = 2 * (it.tq_hi - it.tq_lo) * per_tile;
-      if (it.nkb == 0 || nsub <= 0) continue;
-      const int nkb = it.nkb;
-      const int nu = nsub * nkb;
-      ok = wait_warp(&bars.k_full, iw & 1, abort_flag, p.status);
-      // S^T | dP^T of unit w into TMEM buffer (gu + w) & 1
-      auto issue_sd = [&](int w) -> bool {
-        const int v = nkb == 2 ? (w >> 1) : w, a = nkb == 2 ? (w & 1) : 0;
-        const uint32_t sg = gsub + v;
-        const int s = sg % kStages;
-        if (a == 0 && !wait_warp(&bars.st_full[s], (sg / kStages) & 1, abort_flag, p.status)) return false;
-        tc_fence_after();
-        const uint64_t br = dR0 + desc_bytes(s * kStageBytes);
-        const uint64_t bk = dK0 + desc_bytes(a * kTile);
-        const uint32_t d = tmem + col_buf(gu + w);
-        if (elect_one()) {
-#pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, bk + kmaj_step(k), br + kmaj_step(k), id_sd, k > 0);
-          mma_commit(&bars.s_full[(gu + w) & 1]);
-          if (w == nu - 1) mma_commit(&bars.k_empty);  // the key tiles are read by these MMAs only
-        }
-        __syncwarp();
-        issued = true;
-        return true;
-      };
-      if (ok) ok = issue_sd(0);
-      if (ok && nu > 1) ok = issue_sd(1);
-      for (int w = 0; ok && w < nu; ++w) {
-        const uint32_t g = gu + w;
-        ok = wait_warp(&bars.p_full[g & 1], (g >> 1) & 1, abort_flag, p.status);
-        if (ok && w == 0 && iw > 0) ok = wait_warp(&bars.acc_free, (iw - 1) & 1, abort_flag, p.status);
-        if (!ok) break;
-        tc_fence_after();
-        const int v = nkb == 2 ? (w >> 1) : w, a = nkb == 2 ? (w & 1) : 0;
-        const int s = (gsub + v) % kStages;
-        const uint64_t mq = dM0 + desc_bytes(s * kStageBytes), mdo = mq + desc_bytes(kHalfRows * 128);
-        const uint32_t buf = tmem + col_buf(g), acc = tmem + col_acc(a);
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < kHalfRows / 16; ++kk) {
-            // acc += P^T dO_sub  and  acc += (scale dS)^T Q_sub; query rows
-            // [32 h, 32 h + 32) have P^T at columns 32 h .. 32 h + 15 and dS^T
-            // at 32 h + 16 .. 32 h + 31 (8 packed columns per k-step)
-            const uint32_t pc = (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8);
-            mma_ts(acc, buf + pc, mdo + mnmaj_step(kk), id_acc, (v > 0 || kk > 0) ? 1u : 0u);
-            mma_ts(acc, buf + pc + 16, mq + mnmaj_step(kk), id_acc, 1u);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        u = __shfl_sync(0xffffffffu, u, 0);
+        if (!ok || u < 0) break;
+        if (poisoned) continue;
+        Item it;
+        item_of(p, u, it);
+        const int nsub = 2 * (it.tq_hi - it.tq_lo) * per_tile;
+        if (it.nkb == 0 || nsub <= 0) continue;
+        if (lane == 0) {
+          if (iw > 0) ok = mbar_wait(&bars.k_empty, (iw - 1) & 1, abort_flag, p.status);
+          if (ok) {
+            const CUtensorMap *mp = it.comp ? &map_ckv : &map_kv;
+            mbar_arrive_expect_tx(&bars.k_full, it.nkb * kTile);
+            for (int a = 0; a < it.nkb; ++a) {
+              uint8_t *dst = smem + kOffK + a * kTile;
+              tma_load_3d(mp, &bars.k_full, dst, 0, it.k0[a], it.b);
+              tma_load_3d(mp, &bars.k_full, dst + kHalfTile, 64, it.k0[a], it.b);
+            }
+            k_par = iw & 1;
           }
-          if (a == nkb - 1) mma_commit(&bars.st_empty[s]);  // the sub-tile's last reader
-          if (w == nu - 1) mma_commit(&bars.acc_full);
         }
-        __syncwarp();
-        if (w + 2 < nu) {
-          ok = issue_sd(w + 2);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        for (int v = 0; ok && v < nsub; ++v, ++gsub) {
+          const int x = v >> 1, sub = v & 1;
+          const int tq = it.tq_lo + x / per_tile, g = x % per_tile;
+          const int s = gsub % kStages;
+          uint8_t *st = smem + kOffStage + s * kStageBytes;
+          if (lane == 0 && gsub >= (uint32_t)kStages)
+            ok = mbar_wait(&bars.st_empty[s], ((gsub / kStages) - 1) & 1, abort_flag, p.status);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
+          const int i0 = tq * Q.Pq;
+          const int pos0 = pos_split ? i0 + sub * p.sub_pq : i0;
+          const int hd = it.b * Q.H + g * Q.HG + (pos_split ? 0 : sub * p.sub_hg);
+          // key intervals of the sub-tile's positions (both kinds)
+          int4 *ivs = reinterpret_cast<int4 *>(st + kOffIv);
+          for (int c = lane; c < p.sub_pq; c += 32) {
+            const RowIv iv = row_interval(Q.sstart, it.b, Q.S, pos0 + c, Q.W, Q.m);
+            ivs[c] = iv.valid ? make_int4(iv.rlo, iv.rhi, iv.clo, iv.chi) : make_int4(1, 0, 1, 0);
+          }
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars.st_full[s], kSubBytes + 512);
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              tma_load_3d(&map_qs, &bars.st_full[s], st + h * kHalfTile, 64 * h, pos0, hd);
+              tma_load_3d(&map_dos, &bars.st_full[s], st + h * kHalfTile + kHalfRows * 128, 64 * h, pos0, hd);
+            }
+            // rows [64 sub, 64 sub + 64) of the tile's (-lse*log2e, Delta) record
+            const long long tl = ((long long)it.b * Q.groups + g) * Q.ntq + tq;
+            const float *rs = p.rowstat + tl * 2 * kRows + sub * kHalfRows;
+  #pragma unroll
+            for (int h = 0; h < 2; ++h)
+              asm volatile(
+                  "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                      smem_u32(st + kOffRowstat + h * 256)),
+                  "l"(reinterpret_cast<uint64_t>(rs + h * kRows)), "r"(256), "r"(smem_u32(&bars.st_full[s]))
+                  : "memory");
+            issued = (issued | (1u << s)) & ~(1u << (8 + s));
+            issued |= ((gsub / kStages) & 1u) << (8 + s);
+          }
+          __syncwarp();
         }
+        ++iw;
       }
-      gsub += nsub;
-      gu += nu;
-      ++iw;
-    }
-    if (!ok && issued) {
-      volatile int never = 0;
-      if (elect_one()) mma_commit(&bars.drain);
-      __syncwarp();
-      if (lane == 0) mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
-      __syncwarp();
+      if (!ok && !poisoned && lane == 0) {
+        volatile int never = 0;
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s)) mbar_wait(&bars.st_full[s], (issued >> (8 + s)) & 1u, &never, p.status, 100000000ull);
+        if (k_par >= 0) mbar_wait(&bars.k_full, k_par, &never, p.status, 100000000ull);
+      }
+    } else if (warp == kEW / 32 + 1) {
+      // ------------------------------------------------------------ MMA
+      // Whole warp on warp-uniform values; one elect.sync lane issues.  Work
+      // unit u of an item is (sub-tile u / nkb, key block u % nkb); its
+      // S^T | dP^T goes to TMEM buffer (global unit count) & 1, so the dS warps
+      // form P^T, dS^T of one unit while the tensor pipe runs the next.
+      const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + kOffK), 16, 1024);
+      const uint64_t dR0 = smem_desc_sw128(smem_u32(smem + kOffStage), 16, 1024);          // R, K-major
+      const uint64_t dM0 = smem_desc_sw128(smem_u32(smem + kOffStage), kHalfTile, 1024);   // R rows, MN-major
+      const uint32_t id_sd = idesc_bf16_f32(kRows, kRows, false, false);
+      const uint32_t id_acc = idesc_bf16_f32(kRows, kHeadDim, false, true);
+      uint32_t gsub = 0, gu = 0, iw = 0;  // sub-tiles, units and items with work so far
+      bool ok = true, issued = false;
+      for (uint32_t kq = 0; ok; ++kq) {
+        const int slot = kq % kItemRing;
+        long long u = -1;
+        if (lane == 0) {
+          ok = mbar_wait(&bars.item_full[slot], (kq / kItemRing) & 1, abort_flag, p.status);
+          if (ok) {
+            u = bars.item[slot];
+            mbar_arrive(&bars.item_empty[slot]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        u = __shfl_sync(0xffffffffu, u, 0);
+        if (!ok || u < 0) break;
+        if (poisoned) continue;
+        Item it;
+        item_of(p, u, it);
+        const int nsub = 2 * (it.tq_hi - it.tq_lo) * per_tile;
+        if (it.nkb == 0 || nsub <= 0) continue;
+        const int nkb = it.nkb;
+        const int nu = nsub * nkb;
+        ok = wait_warp(&bars.k_full, iw & 1, abort_flag, p.status);
+        // S^T | dP^T of unit w into TMEM buffer (gu + w) & 1
+        auto issue_sd = [&](int w) -> bool {
+          const int v = nkb == 2 ? (w >> 1) : w, a = nkb == 2 ? (w & 1) : 0;
+          const uint32_t sg = gsub + v;
+          const int s = sg % kStages;
+          if (a == 0 && !wait_warp(&bars.st_full[s], (sg / kStages) & 1, abort_flag, p.status)) return false;
+          tc_fence_after();
+          const uint64_t br = dR0 + desc_bytes(s * kStageBytes);
+          const uint64_t bk = dK0 + desc_bytes(a * kTile);
+          const uint32_t d = tmem + col_buf(gu + w);
+          if (elect_one()) {
+  #pragma unroll
+            for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, bk + kmaj_step(k), br + kmaj_step(k), id_sd, k > 0);
+            mma_commit(&bars.s_full[(gu + w) & 1]);
+            if (w == nu - 1) mma_commit(&bars.k_empty);  // the key tiles are read by these MMAs only
+          }
+          __syncwarp();
+          issued = true;
+          return true;
+        };
+        if (ok) ok = issue_sd(0);
+        if (ok && nu > 1) ok = issue_sd(1);
+        for (int w = 0; ok && w < nu; ++w) {
+          const uint32_t g = gu + w;
+          ok = wait_warp(&bars.p_full[g & 1], (g >> 1) & 1, abort_flag, p.status);
+          if (ok && w == 0 && iw > 0) ok = wait_warp(&bars.acc_free, (iw - 1) & 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          const int v = nkb == 2 ? (w >> 1) : w, a = nkb == 2 ? (w & 1) : 0;
+          const int s = (gsub + v) % kStages;
+          const uint64_t mq = dM0 + desc_bytes(s * kStageBytes), mdo = mq + desc_bytes(kHalfRows * 128);
+          const uint32_t buf = tmem + col_buf(g), acc = tmem + col_acc(a);
+          if (elect_one()) {
+  #pragma unroll
+            for (int kk = 0; kk < kHalfRows / 16; ++kk) {
+              // acc += P^T dO_sub  and  acc += (scale dS)^T Q_sub; query rows
+              // [32 h, 32 h + 32) have P^T at columns 32 h .. 32 h + 15 and dS^T
+              // at 32 h + 16 .. 32 h + 31 (8 packed columns per k-step)
+              const uint32_t pc = (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8);
+              mma_ts(acc, buf + pc, mdo + mnmaj_step(kk), id_acc, (v > 0 || kk > 0) ? 1u : 0u);
+              mma_ts(acc, buf + pc + 16, mq + mnmaj_step(kk), id_acc, 1u);
+            }
+            if (a == nkb - 1) mma_commit(&bars.st_empty[s]);  // the sub-tile's last reader
+            if (w == nu - 1) mma_commit(&bars.acc_full);
+          }
+          __syncwarp();
+          if (w + 2 < nu) {
+            ok = issue_sd(w + 2);
+            if (!ok) break;
+          }
+        }
+        gsub += nsub;
+        gu += nu;
+        ++iw;
+      }
+      if (!ok && issued) {
+        volatile int never = 0;
+        if (elect_one()) mma_commit(&bars.drain);
+        __syncwarp();
+        if (lane == 0) mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+        __syncwarp();
+      }
     }
   } else {
+    setmaxnreg_inc<kRegEW>();
     // ------------------------------------------------------------ P^T, dS^T + item epilogue
-    // thread kr of warpgroup wg owns key row kr (TMEM lane kr), query columns
-    // [32 wg, 32 wg + 32) of every unit and accumulator columns [64 wg, 64 wg + 64)
+    // thread kr of warpgroup wg owns key row kr (TMEM lane kr) of the units
+    // in TMEM buffer wg (every other unit) and accumulator columns
+    // [64 wg, 64 wg + 64) of the item epilogue
     const int kr = tid & (kRows - 1), wg = tid >> 7;
-    const int cq = wg * 32;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint64_t sl2x2 = f32x2(__float_as_uint(p.sl2), __float_as_uint(p.sl2));
     const uint64_t sc2 = f32x2(__float_as_uint(p.scale), __float_as_uint(p.scale));
@@ -937,19 +953,21 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
         continue;
       }
       const int nu = nsub * nkb;
-      for (int w = 0; w < nu; ++w) {
+      // units alternate between the warpgroups (and TMEM buffers): one
+      // warpgroup's exp/dS math overlaps the other's TMEM traffic and waits
+      for (int w = wg; w < nu; w += 2) {
         const int v = nkb == 2 ? (w >> 1) : w, a = nkb == 2 ? (w & 1) : 0;
         const uint32_t g = gu + w;
         const uint32_t sg = gsub + v;
         const uint8_t *st = smem + kOffStage + (sg % kStages) * kStageBytes;
-        if (a == 0 &&
-            !wait_warp(&bars.st_full[sg % kStages], (sg / kStages) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_warp(&bars.st_full[sg % kStages], (sg / kStages) & 1, abort_flag, p.status)) { ok = false; break; }
         if (!wait_warp(&bars.s_full[g & 1], (g >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t base = lane_addr + col_buf(g);
-        uint32_t sv[64];  // S^T columns [cq, cq + 32), then dP^T columns [64 + cq, 64 + cq + 32)
-        tmem_ld32(base + cq, *reinterpret_cast<uint32_t(*)[32]>(sv));
-        tmem_ld32(base + 64 + cq, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        // query rows [32 h, 32 h + 32): S^T columns 32 h.., dP^T columns 64 + 32 h..
+        uint32_t sv0[64], sv1[64];
+        tmem_ld32(base, *reinterpret_cast<uint32_t(*)[32]>(sv0));
+        tmem_ld32(base + 64, *reinterpret_cast<uint32_t(*)[32]>(sv0 + 32));
         // visibility of this key for the 64 columns (query rows) of the
         // sub-tile: column c sits at position c mod sub_pq of the sub-tile
         const int key = it.k0[a] + kr;
@@ -965,27 +983,33 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
           for (int wd = p.sub_pq; wd < kHalfRows; wd *= 2) pat |= pat << wd;
           vis = pat;
         }
-        const uint32_t vis32 = (uint32_t)(vis >> cq);
         tmem_wait_ld();
-        // -lse*log2e [64] then Delta [64] of the sub-tile's rows, from column cq
-        const float4 *rs4 = reinterpret_cast<const float4 *>(st + kOffRowstat) + cq / 4;
-        uint32_t pk[16], dk[16];
-        // warp-uniform cases: no visible pair (P^T = dS^T = 0), every pair
-        // visible (no masking), or a mix
-        const bool none = __all_sync(0xffffffffu, vis32 == 0u);
-        const bool all = __all_sync(0xffffffffu, vis32 == ~0u);
-        if (none) {
+        tmem_ld32(base + 32, *reinterpret_cast<uint32_t(*)[32]>(sv1));
+        tmem_ld32(base + 96, *reinterpret_cast<uint32_t(*)[32]>(sv1 + 32));
+        // -lse*log2e [64] then Delta [64] of the sub-tile's rows
+        const float4 *rs4 = reinterpret_cast<const float4 *>(st + kOffRowstat);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) pk[c] = dk[c] = 0u;
-        } else if (all) {
-          ew_unit<false>(sv, rs4, 0u, sl2x2, sc2, pk, dk);
-        } else {
-          ew_unit<true>(sv, rs4, vis32, sl2x2, sc2, pk, dk);
+        for (int h = 0; h < 2; ++h) {
+          if (h == 1) tmem_wait_ld();
+          const uint32_t vis32 = (uint32_t)(vis >> (32 * h));
+          uint32_t pk[16], dk[16];
+          // warp-uniform cases: no visible pair (P^T = dS^T = 0), every pair
+          // visible (no masking), or a mix
+          const bool none = __all_sync(0xffffffffu, vis32 == 0u);
+          const bool all = __all_sync(0xffffffffu, vis32 == ~0u);
+          if (none) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) pk[c] = dk[c] = 0u;
+          } else if (all) {
+            ew_unit<false>(h ? sv1 : sv0, rs4 + 8 * h, 0u, sl2x2, sc2, pk, dk);
+          } else {
+            ew_unit<true>(h ? sv1 : sv0, rs4 + 8 * h, vis32, sl2x2, sc2, pk, dk);
+          }
+          // packed P^T and dS^T of query rows [32 h, 32 h + 32) go over S^T
+          // columns 32 h .. 32 h + 31, which this thread has read
+          tmem_st16(base + 32 * h, pk);
+          tmem_st16(base + 32 * h + 16, dk);
         }
-        // packed P^T and dS^T of these 32 query rows go over the 32 S^T
-        // columns this thread read (the other warpgroup reads other columns)
-        tmem_st16(base + cq, pk);
-        tmem_st16(base + cq + 16, dk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars.p_full[g & 1]);
