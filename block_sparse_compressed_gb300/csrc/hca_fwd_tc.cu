@@ -467,7 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           // kPosScale: max of s, scaled after; otherwise min of s (scale < 0)
           const float ninf = kPosScale ? -INFINITY : INFINITY;
-          float ma = ninf, mb = ninf;
+          // eight independent 3-input max chains keep the dependency depth short
+          float mc[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mc[k] = ninf;
 #pragma unroll
           for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
             if (c0 < nk) {
@@ -478,18 +481,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                   if (c0 + y < lo_c || c0 + y > hi_c) sv[c0 + y] = __float_as_uint(ninf);
               }
 #pragma unroll
-              for (int y = 0; y < 32; y += 4) {
-                if (kPosScale) {
-                  ma = fmax3(ma, __uint_as_float(sv[c0 + y]), __uint_as_float(sv[c0 + y + 1]));
-                  mb = fmax3(mb, __uint_as_float(sv[c0 + y + 2]), __uint_as_float(sv[c0 + y + 3]));
-                } else {
-                  ma = fmin3(ma, __uint_as_float(sv[c0 + y]), __uint_as_float(sv[c0 + y + 1]));
-                  mb = fmin3(mb, __uint_as_float(sv[c0 + y + 2]), __uint_as_float(sv[c0 + y + 3]));
+              for (int y = 0; y < 32; y += 16) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  const float a0 = __uint_as_float(sv[c0 + y + 2 * k]), a1 = __uint_as_float(sv[c0 + y + 2 * k + 1]);
+                  mc[k] = kPosScale ? fmax3(mc[k], a0, a1) : fmin3(mc[k], a0, a1);
                 }
               }
             }
           }
-          const float m = kPosScale ? fmaxf(ma, mb) : fminf(ma, mb);
+          float m;
+          if (kPosScale) {
+            const float m0 = fmax3(mc[0], mc[1], mc[2]), m1 = fmax3(mc[3], mc[4], mc[5]);
+            m = fmax3(m0, m1, fmaxf(mc[6], mc[7]));
+          } else {
+            const float m0 = fmin3(mc[0], mc[1], mc[2]), m1 = fmin3(mc[3], mc[4], mc[5]);
+            m = fmin3(m0, m1, fminf(mc[6], mc[7]));
+          }
           mx = (m == ninf) ? -INFINITY : m * p.sl2;
         }
         float f = 1.f;
@@ -506,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           const uint64_t sl2x2 = f32x2(__float_as_uint(p.sl2), __float_as_uint(p.sl2));
           const uint64_t nm2 = f32x2(__float_as_uint(-m_use), __float_as_uint(-m_use));
-          uint64_t acc0 = 0, acc1 = 0;  // packed row sums (+0.0f bit patterns)
+          uint64_t acc[4] = {0, 0, 0, 0};  // packed row sums (+0.0f bit patterns), four chains
 #pragma unroll
           for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
             if (c0 < nk) {
@@ -518,15 +526,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 f32x2_split(ffma2(f32x2(sv[c0 + y], sv[c0 + y + 1]), sl2x2, nm2), t0, t1);
                 const float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
                 const uint64_t e2 = f32x2(__float_as_uint(e0), __float_as_uint(e1));
-                if ((y >> 1) & 1) acc1 = fadd2(acc1, e2); else acc0 = fadd2(acc0, e2);
+                acc[(y >> 1) & 3] = fadd2(acc[(y >> 1) & 3], e2);
                 pk[y >> 1] = pack_bf16x2(e0, e1);
               }
               tmem_st16(lane_addr + col_s(x) + c0 / 2, pk);
             }
           }
           float a0, a1, b0, b1;
-          f32x2_split(acc0, a0, a1);
-          f32x2_split(acc1, b0, b1);
+          f32x2_split(fadd2(acc[0], acc[1]), a0, a1);
+          f32x2_split(fadd2(acc[2], acc[3]), b0, b1);
           l_run += (a0 + a1) + (b0 + b1);
         }
         if (__any_sync(0xffffffffu, rescale_o)) {
