@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--mode", choices=("hca", "local"), default="hca",
+                    help="local: time the local sliding-window entry points (no compressed set) on the same shape")
     ap.add_argument("--ncu-case", type=int, default=0, metavar="S",
                     help="profiling case: run --warmup + 1 untimed fwd+bwd steps of the headline shape at sequence "
                          "length S and exit (for ncu captures; prints nothing to time)")
@@ -429,6 +431,57 @@ def run_e2e(args, w, q, kv, ckv, dout, dev, dist, flops_step, world):
             "path": "pinned host tensors -> hca_attn_fwd/hca_attn_bwd (C ABI) -> pinned host tensors"}
 
 
+def run_local(args):
+    """Local sliding-window attention (no compressed set) on the headline
+    shape: same timing rules, FLOPs over the raw visible pairs."""
+    import torch
+    from block_sparse_compressed_gb300 import hca
+    from block_sparse_compressed_gb300 import inputs as I
+    w = workload()
+    dev = torch.device("cuda", 0)
+    q, kv, _, seg, dout = I.tensors(w, device=dev)
+    raw, _ = visible_pairs_closed_form(w.S, w.W, w.S + 1)
+    pairs = raw * w.H * w.B
+    out = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.S, dtype=torch.float32, device=dev)
+    dq, dkv = torch.empty_like(q), torch.empty_like(kv)
+    wsf = hca.local_workspace(w.B, w.H, w.S, w.D, w.W, w.dtype, False, dev)
+    wsb = hca.local_workspace(w.B, w.H, w.S, w.D, w.W, w.dtype, True, dev)
+
+    def step():
+        hca.hca_local_attn_fwd(q, kv, seg, w.W, w.scale, out=out, lse=lse, ws=wsf)
+        hca.hca_local_attn_bwd(q, kv, seg, out, lse, dout, w.W, w.scale, dq=dq, dkv=dkv, ws=wsb)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    if hca.hca_workspace_status(wsf) != 0 or hca.hca_workspace_status(wsb) != 0:
+        raise RuntimeError("device reported an error status")
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    hca.hca_profile_enable(True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    prof = hca.hca_profile_read()
+    hca.hca_profile_enable(False)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    flops = 14 * w.D * pairs
+    fwd_ms = prof.get("hca_fwd_tc", (0, 0.0))[1] / args.steps
+    bwd_ms = sum(prof.get(k, (0, 0.0))[1] for k in ("hca_bwd_dq", "hca_bwd_dkv", "hca_bwd_reduce")) / args.steps
+    line = {"metric": "LOCAL_SLIDING attn fwd+bwd TFLOP/s (visible pairs) at S=65536", "value": round(
+        flops / (ms * 1e-3) / 1e12, 3), "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"local fwd+bwd bf16 B{w.B} H{w.H} S{w.S} D{w.D} W{w.W}", "pairs_per_head": raw},
+        "phases": {"fwd": {"ms": round(fwd_ms, 4), "tflops": round(4 * w.D * pairs / fwd_ms / 1e9, 2)},
+                   "bwd": {"ms": round(bwd_ms, 4), "tflops": round(10 * w.D * pairs / bwd_ms / 1e9, 2)}},
+        "kernels": {k: {"launches": n, "ms_total": round(t, 4)} for k, (n, t) in prof.items() if n}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_ncu_case(args):
     import torch
     from block_sparse_compressed_gb300 import hca
@@ -451,6 +504,8 @@ def main(argv=None):
         return run_ncu_case(args)
     if args.impl == "reference":
         return run_reference(args)
+    if args.mode == "local":
+        return run_local(args)
     return run_ours(args)
 
 

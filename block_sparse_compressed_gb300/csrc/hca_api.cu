@@ -157,6 +157,38 @@ int hca_attn_bwd(const void *q, const void *kv, const void *ckv, const int32_t *
   return cuda_status(simt_bwd(a, st));
 }
 
+// Local sliding attention: the HCA calls with a compression ratio larger
+// than the sequence (no window of length m completes, so the compressed set
+// is empty).  The one ckv row that this ratio implies is never visible; kv
+// stands in for it, and its gradient row lands in scratch at the end of the
+// backward workspace.
+size_t hca_local_workspace_size(int B, int H, int S, int D, int W, int dtype, int for_backward) {
+  const int m = S + 1;
+  if (check_dims(B, H, S, D, W, m, dtype) != HCA_OK) return 0;
+  if (!for_backward) return fwd_ws_bytes(B, S);
+  return bwd_ws_bytes(B, H, S, D, W, m, dtype) + align_up((size_t)B * D * elt_bytes(dtype));
+}
+
+int hca_local_attn_fwd(const void *q, const void *kv, const int32_t *seg, void *out, float *lse, int B, int H, int S,
+                       int D, int W, float scale, int dtype, void *workspace, size_t workspace_bytes, void *stream) {
+  return hca_attn_fwd(q, kv, kv, seg, out, lse, B, H, S, D, W, S + 1, scale, dtype, workspace, workspace_bytes,
+                      stream);
+}
+
+int hca_local_attn_bwd(const void *q, const void *kv, const int32_t *seg, const void *out, const float *lse,
+                       const void *dout, void *dq, void *dkv, int B, int H, int S, int D, int W, float scale, int dtype,
+                       void *workspace, size_t workspace_bytes, void *stream) {
+  const int m = S + 1;
+  int rc = check_dims(B, H, S, D, W, m, dtype);
+  if (rc != HCA_OK) return rc;
+  const size_t need = bwd_ws_bytes(B, H, S, D, W, m, dtype);
+  rc = check_ws(workspace, workspace_bytes, need + align_up((size_t)B * D * elt_bytes(dtype)));
+  if (rc != HCA_OK) return rc;
+  void *dckv = static_cast<char *>(workspace) + need;  // [B, 1, D], discarded
+  return hca_attn_bwd(q, kv, kv, seg, out, lse, dout, dq, dkv, dckv, B, H, S, D, W, m, scale, dtype, workspace,
+                      need, stream);
+}
+
 int hca_visible_pairs(const int32_t *seg, int B, int S, int W, int m, int64_t *raw_pairs, int64_t *comp_pairs,
                       void *workspace, size_t workspace_bytes, void *stream) {
   if (B < 0 || S < 0 || S > (1 << 30)) return HCA_ERR_SHAPE;

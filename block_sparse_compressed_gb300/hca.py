@@ -27,7 +27,8 @@ _lib = None
 
 EXPORTS = ("hca_status_string", "hca_version", "hca_workspace_size", "hca_query_tile_positions", "hca_attn_fwd",
            "hca_attn_bwd", "hca_visible_pairs", "hca_tile_map", "hca_workspace_status", "hca_profile_enable",
-           "hca_profile_read", "hca_num_kernels", "hca_kernel_name", "hca_attn_fwd_noalloc")
+           "hca_profile_read", "hca_num_kernels", "hca_kernel_name", "hca_attn_fwd_noalloc",
+           "hca_local_workspace_size", "hca_local_attn_fwd", "hca_local_attn_bwd")
 
 
 class HCAError(RuntimeError):
@@ -74,6 +75,12 @@ def load(path: str = LIB_PATH):
             lib.hca_kernel_name.restype = ctypes.c_char_p
             lib.hca_attn_fwd_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, I, P]
             lib.hca_attn_fwd_noalloc.restype = I
+            lib.hca_local_workspace_size.argtypes = [I, I, I, I, I, I, I]
+            lib.hca_local_workspace_size.restype = Z
+            lib.hca_local_attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P, Z, P]
+            lib.hca_local_attn_fwd.restype = I
+            lib.hca_local_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, P, Z, P]
+            lib.hca_local_attn_bwd.restype = I
             _lib = lib
     return _lib
 
@@ -205,6 +212,69 @@ def hca_attn_bwd(q, kv, ckv, seg, out, lse, dout, W: int, m: int, scale: float, 
     if check:
         _check(hca_workspace_status(ws), "hca_attn_bwd (device)")
     return dq, dkv, dckv
+
+
+def hca_local_workspace_size(B: int, H: int, S: int, D: int, W: int, dtype: torch.dtype, for_backward: bool) -> int:
+    return load().hca_local_workspace_size(B, H, S, D, W, _DTYPES[dtype], int(for_backward))
+
+
+def local_workspace(B, H, S, D, W, dtype, for_backward, device) -> torch.Tensor:
+    n = hca_local_workspace_size(B, H, S, D, W, dtype, for_backward)
+    if n == 0:
+        raise ValueError("invalid sizes for hca_local_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _local_shapes(q, kv, seg):
+    if q.dim() != 4:
+        raise ValueError("q must be [B,H,S,D]")
+    B, H, S, D = q.shape
+    _need(kv, "kv", (B, S, D), q.dtype, q.device)
+    if seg is not None:
+        _need(seg, "seg", (B, S), torch.int32, q.device)
+    return B, H, S, D
+
+
+def hca_local_attn_fwd(q, kv, seg, W: int, scale: float, out=None, lse=None, ws=None, check: bool = False):
+    """Local sliding-window attention forward: returns (out, lse)."""
+    lib = load()
+    B, H, S, D = _local_shapes(q, kv, seg)
+    dt = _dtype_code(q)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(out, "out", q.shape, q.dtype, q.device)
+    _need(lse, "lse", (B, H, S), torch.float32, q.device)
+    if ws is None:
+        ws = local_workspace(B, H, S, D, W, q.dtype, False, q.device)
+    rc = lib.hca_local_attn_fwd(_ptr(q), _ptr(kv), _ptr(seg), _ptr(out), _ptr(lse), B, H, S, D, W, float(scale), dt,
+                                _ptr(ws), ws.numel(), _stream(q.device))
+    _check(rc, "hca_local_attn_fwd")
+    if check:
+        _check(hca_workspace_status(ws), "hca_local_attn_fwd (device)")
+    return out, lse
+
+
+def hca_local_attn_bwd(q, kv, seg, out, lse, dout, W: int, scale: float, dq=None, dkv=None, ws=None,
+                       check: bool = False):
+    """Local sliding-window attention backward: returns (dq, dkv)."""
+    lib = load()
+    B, H, S, D = _local_shapes(q, kv, seg)
+    _need(out, "out", q.shape, q.dtype, q.device)
+    _need(dout, "dout", q.shape, q.dtype, q.device)
+    _need(lse, "lse", (B, H, S), torch.float32, q.device)
+    dt = _dtype_code(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dkv = torch.empty_like(kv) if dkv is None else dkv
+    _need(dq, "dq", q.shape, q.dtype, q.device)
+    _need(dkv, "dkv", kv.shape, q.dtype, q.device)
+    if ws is None:
+        ws = local_workspace(B, H, S, D, W, q.dtype, True, q.device)
+    rc = lib.hca_local_attn_bwd(_ptr(q), _ptr(kv), _ptr(seg), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dkv),
+                                B, H, S, D, W, float(scale), dt, _ptr(ws), ws.numel(), _stream(q.device))
+    _check(rc, "hca_local_attn_bwd")
+    if check:
+        _check(hca_workspace_status(ws), "hca_local_attn_bwd (device)")
+    return dq, dkv
 
 
 def hca_visible_pairs(seg: Optional[torch.Tensor], B: int, S: int, W: int, m: int, device=None):

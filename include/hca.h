@@ -135,6 +135,24 @@ HCA_API int hca_tile_map(const int32_t *seg, int B, int S, int W, int m, int Pq,
  * the one entry point that blocks the host. */
 HCA_API int hca_workspace_status(const void *workspace, void *stream);
 
+/* Local sliding-window attention (the LOCAL_SLIDING layers of "DSV4: Route
+ * compressed and sliding train attention onto the splash kernels", local
+ * sliding mask: window plus segment ids, no compressed set).  Query i
+ * attends under one softmax to the raw kv rows t with i - W < t <= i of its
+ * own document and to nothing else.  Arguments, layouts, ownership and
+ * errors are those of hca_attn_fwd / hca_attn_bwd without ckv, dckv and m;
+ * the same kernels run with the compressed set empty.  The workspace size
+ * comes from hca_local_workspace_size (for_backward as in
+ * hca_workspace_size); dq and dkv are fully overwritten. */
+HCA_API size_t hca_local_workspace_size(int B, int H, int S, int D, int W, int dtype, int for_backward);
+HCA_API int hca_local_attn_fwd(const void *q, const void *kv, const int32_t *seg, void *out, float *lse,
+                               int B, int H, int S, int D, int W, float scale, int dtype,
+                               void *workspace, size_t workspace_bytes, void *stream);
+HCA_API int hca_local_attn_bwd(const void *q, const void *kv, const int32_t *seg,
+                               const void *out, const float *lse, const void *dout, void *dq, void *dkv,
+                               int B, int H, int S, int D, int W, float scale, int dtype,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
 /* Forward for callers that cannot allocate device memory.  The paper has no
  * counterpart: this is a convenience of this library.  Plugin hooks of
  * inference runtimes, real-time loops that cannot afford cudaMalloc's implicit

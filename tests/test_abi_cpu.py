@@ -111,6 +111,25 @@ def test_backward_argument_errors(lib):
     assert call(ptrs=p, wsb=64) == E_WS
 
 
+def test_local_attention_host_checks(lib):
+    # the local entry points are the HCA calls with an empty compressed set:
+    # same argument checks, a workspace that exists for every valid size
+    P = ctypes.c_void_p
+    for bwd in (0, 1):
+        assert lib.hca_local_workspace_size(1, 64, 65536, 128, 128, 0, bwd) > 0
+        assert lib.hca_local_workspace_size(1, 64, 65536, 128, 0, 0, bwd) == 0   # W < 1
+    rc = lib.hca_local_attn_fwd(P(16), P(16), None, P(16), P(16), 1, 4, 64, 128, 0, 0.1, 0, P(256), 1 << 20, None)
+    assert rc == E_ARG
+    rc = lib.hca_local_attn_fwd(P(16), P(16), None, P(16), P(16), 1, 4, 64, 128, 8, 0.1, 0, P(256), 16, None)
+    assert rc == E_WS
+    rc = lib.hca_local_attn_bwd(P(16), P(16), None, P(16), P(16), P(16), P(16), P(16), 1, 4, 64, 128, 8, 0.1, 0,
+                                P(256), 64, None)
+    assert rc == E_WS
+    rc = lib.hca_local_attn_bwd(P(16), P(16), None, P(16), P(16), P(16), None, P(16), 1, 4, 64, 128, 8, 0.1, 0,
+                                P(256), 1 << 26, None)
+    assert rc == E_NULL
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="uses fake device addresses; only meaningful without a GPU")
 def test_valid_call_without_a_device_reports_cuda_error(lib):
     # with no GPU the first CUDA call fails: the ABI reports HCA_ERR_CUDA and
