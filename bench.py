@@ -44,6 +44,12 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # S^T + dP^T + dK + dV.
 KERNEL_FLOP_PER_PAIR_D = {"hca_fwd_tc": 4, "hca_bwd_dq": 6, "hca_bwd_dkv": 8}
 KERNEL_SOURCES = {"hca_fwd_tc": "hca_fwd_tc.cu", "hca_bwd_dq": "hca_bwd_tc.cu", "hca_bwd_dkv": "hca_bwd_tc.cu"}
+# secondary roof: exponentials.  ex2.approx.f32 issues at 32 per clock per SM
+# on GB300 (measured with 1024 threads x 8 independent chains per SM); the
+# path needs one exp per visible pair and head in the forward and one in each
+# backward kernel (dq and dkv both form P).
+EX2_PER_CLK_PER_SM = 32
+EXP_PER_PAIR = {"fwd": 1, "bwd": 2}
 
 
 def parse_args(argv=None):
@@ -373,11 +379,21 @@ def run_ours(args):
     # end to end: host buffers in, results back to host, through the API
     e2e = run_e2e(args, w, q, kv, ckv, dout, dev, dist, flop_fwd + flop_bwd, world)
 
+    sm_mhz = (clk or {}).get("sm_mhz") or 2070.0
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    ex2_rate = EX2_PER_CLK_PER_SM * n_sm * sm_mhz * 1e6
+    mufu = {"unit": "exp/s", "peak": ex2_rate, "peak_source": "32 ex2.approx per clock per SM (probe) x SMs x sm_mhz"}
+    for ph, ph_ms in (("fwd", fwd_ms), ("bwd", bwd_ms)):
+        n_exp = EXP_PER_PAIR[ph] * pairs
+        mufu[ph] = {"exp": n_exp, "floor_ms": round(n_exp / ex2_rate * 1e3, 4),
+                    "tensor_floor_ms": round((flop_fwd if ph == "fwd" else flop_bwd) / (peak * 1e12) * 1e3, 4),
+                    "frac": round(n_exp / (ph_ms * 1e-3) / ex2_rate, 4) if ph_ms > 0 else None}
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(w),
             "pct_bf16_peak": round(100 * value / world / burst, 2), "peak_tflops": burst,
             "phases": per_phase, "kernels": kernels, "gpu_launches": launches, "roofline": roofline,
+            "secondary_roof_exp": mufu,
             "clocks": clk, "e2e": e2e}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, q, kv, ckv, dout, args.cpu_seconds)
