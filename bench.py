@@ -326,6 +326,15 @@ def run_ours(args):
         raise RuntimeError("device reported an error status")
     for _ in range(max(0, args.warmup - 1)):
         step()
+    # no hidden allocation in a step: peak memory before/after one more step
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    base_alloc = torch.cuda.memory_allocated(dev)
+    step()
+    torch.cuda.synchronize(dev)
+    memory = {"workspace_fwd_bytes": wsf.numel(), "workspace_bwd_bytes": wsb.numel(),
+              "step_peak_delta_bytes": torch.cuda.max_memory_allocated(dev) - base_alloc,
+              "mask_bytes": 0, "note": "workspace is O(B*S + B*H*S + slots*Sc*D); no (query, key) mask in memory"}
     stream = torch.cuda.current_stream(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local) if rank == 0 else None
@@ -393,7 +402,7 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(w),
             "pct_bf16_peak": round(100 * value / world / burst, 2), "peak_tflops": burst,
             "phases": per_phase, "kernels": kernels, "gpu_launches": launches, "roofline": roofline,
-            "secondary_roof_exp": mufu,
+            "secondary_roof_exp": mufu, "memory": memory,
             "clocks": clk, "e2e": e2e}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, q, kv, ckv, dout, args.cpu_seconds)
