@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
           const uint64_t da = x ? dDO : dQ;
           const uint32_t d = tmem + (x ? kColDP : kColS);
           if (elect_one()) {
-  #pragma unroll
+#pragma unroll
             for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, da + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
             mma_commit(x ? &bars.dp_full : &bars.s_full);
             if (last_q_use) mma_commit(&bars.qd_empty);
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
           const int s = g % kStages;
           const uint64_t bv = dV0 + desc_bytes(s * kTile);
           if (elect_one()) {
-  #pragma unroll
+#pragma unroll
             for (int kk = 0; kk < kBlockKeys / 16; ++kk)
               if (kk < nks)
                 mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, bv + mnmaj_step(kk), id_dq, (j > 0 || kk > 0) ? 1u : 0u);
@@ -781,7 +781,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
           __syncwarp();
           if (lane == 0) {
             mbar_arrive_expect_tx(&bars.st_full[s], kSubBytes + 512);
-  #pragma unroll
+#pragma unroll
             for (int h = 0; h < 2; ++h) {
               tma_load_3d(&map_qs, &bars.st_full[s], st + h * kHalfTile, 64 * h, pos0, hd);
               tma_load_3d(&map_dos, &bars.st_full[s], st + h * kHalfTile + kHalfRows * 128, 64 * h, pos0, hd);
@@ -789,7 +789,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
             // rows [64 sub, 64 sub + 64) of the tile's (-lse*log2e, Delta) record
             const long long tl = ((long long)it.b * Q.groups + g) * Q.ntq + tq;
             const float *rs = p.rowstat + tl * 2 * kRows + sub * kHalfRows;
-  #pragma unroll
+#pragma unroll
             for (int h = 0; h < 2; ++h)
               asm volatile(
                   "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -854,7 +854,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
           const uint64_t bk = dK0 + desc_bytes(a * kTile);
           const uint32_t d = tmem + col_buf(gu + w);
           if (elect_one()) {
-  #pragma unroll
+#pragma unroll
             for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, bk + kmaj_step(k), br + kmaj_step(k), id_sd, k > 0);
             mma_commit(&bars.s_full[(gu + w) & 1]);
             if (w == nu - 1) mma_commit(&bars.k_empty);  // the key tiles are read by these MMAs only
@@ -876,7 +876,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
           const uint64_t mq = dM0 + desc_bytes(s * kStageBytes), mdo = mq + desc_bytes(kHalfRows * 128);
           const uint32_t buf = tmem + col_buf(g), acc = tmem + col_acc(a);
           if (elect_one()) {
-  #pragma unroll
+#pragma unroll
             for (int kk = 0; kk < kHalfRows / 16; ++kk) {
               // acc += P^T dO_sub  and  acc += (scale dS)^T Q_sub; query rows
               // [32 h, 32 h + 32) have P^T at columns 32 h .. 32 h + 15 and dS^T
@@ -974,14 +974,22 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
         uint64_t vis = 0;
         if (kr < it.n[a]) {
           const int4 *ivs = reinterpret_cast<const int4 *>(st + kOffIv);
-          uint64_t pat = 0;
-          for (int q = 0; q < p.sub_pq; ++q) {
+          auto sees = [&](int q) -> bool {
             const int4 iv = ivs[q];
             const int lo = it.comp ? iv.z : iv.x, hi = it.comp ? iv.w : iv.y;
-            if (key >= lo && key <= hi) pat |= 1ull << q;
+            return key >= lo && key <= hi;
+          };
+          if (p.sub_pq == 1) {  // one position: all 64 columns alike
+            vis = sees(0) ? ~0ull : 0ull;
+          } else if (p.sub_pq == 2) {  // two positions alternate over the columns
+            vis = (sees(0) ? 0x5555555555555555ull : 0ull) | (sees(1) ? 0xAAAAAAAAAAAAAAAAull : 0ull);
+          } else {
+            uint64_t pat = 0;
+            for (int q = 0; q < p.sub_pq; ++q)
+              if (sees(q)) pat |= 1ull << q;
+            for (int wd = p.sub_pq; wd < kHalfRows; wd *= 2) pat |= pat << wd;
+            vis = pat;
           }
-          for (int wd = p.sub_pq; wd < kHalfRows; wd *= 2) pat |= pat << wd;
-          vis = pat;
         }
         tmem_wait_ld();
         tmem_ld32(base + 32, *reinterpret_cast<uint32_t(*)[32]>(sv1));
