@@ -66,7 +66,7 @@ struct DqParams {
   QTiling qt;
   int32_t *status;
   const float *lse;
-  float *rowstat;            // [ntiles][2][128]: -lse*log2e, then Delta, per tile row
+  float *rowstat;            // [ntiles][2][128]: -lse*log2e, then -scale*Delta, per tile row
   __nv_bfloat16 *dq;         // direct stores for poisoned calls / tiles without keys
   float sl2, scale;
 };
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       }
       if (wg == 0) {
         rs[r] = -lse2;
-        rs[kRows + r] = delta;
+        rs[kRows + r] = -p.scale * delta;
       }
       mbar_arrive(&bars.qd_empty);
       for (int j = 0; j < nb; ++j, ++gb) {
@@ -497,7 +497,7 @@ static_assert(2 * 128 * kRegEW + 128 * kRegProducer <= kThreads * 168, "register
 constexpr int kStages = 4;                     // sub-tiles in flight
 constexpr int kSubBytes = kTile;               // one operand R (two halves)
 constexpr int kHalfRows = 64;                  // rows of Q_sub (and of dO_sub)
-constexpr int kOffRowstat = kSubBytes;         // -lse*log2e [64] then Delta [64]
+constexpr int kOffRowstat = kSubBytes;         // -lse*log2e [64] then -scale*Delta [64]
 constexpr int kOffIv = kOffRowstat + 512;      // per-position intervals (rlo, rhi, clo, chi) [<= 64]
 constexpr int kStageBytes = kOffIv + 1024 + 512;  // 34 KB: every stage stays 1 KB aligned
 constexpr int kOffK = 0;                       // key block tiles A | B
@@ -620,7 +620,8 @@ __device__ __forceinline__ void item_of(const DkvParams &p, long long u, Item &i
 // P^T and (scale dS^T) of one key row for 32 query columns of a unit:
 //   p = exp2(s * scale * log2e - lse * log2e),  ds = p * (scale dP - scale Delta)
 // sv holds the 32 S^T values then the 32 matching dP^T values; rs4 points at
-// the columns' (-lse*log2e) records, their Delta records 16 float4 further.
+// the columns' (-lse*log2e) records, their (-scale*Delta) records 16 float4
+// further.
 // kMasked zeroes the columns whose bit in vis is clear.
 template <bool kMasked>
 __device__ __forceinline__ void ew_unit(const uint32_t (&sv)[64], const float4 *rs4, uint32_t vis, uint64_t sl2x2,
@@ -632,14 +633,14 @@ __device__ __forceinline__ void ew_unit(const uint32_t (&sv)[64], const float4 *
 #pragma unroll
     for (int h = 0; h < 4; h += 2) {
       const float n0 = h ? nl.z : nl.x, n1 = h ? nl.w : nl.y;
-      const float d0 = h ? dl.z : dl.x, d1 = h ? dl.w : dl.y;
+      const float d0 = h ? dl.z : dl.x, d1 = h ? dl.w : dl.y;  // -scale * Delta
       float t0, t1;
       f32x2_split(ffma2(f32x2(sv[c + h], sv[c + h + 1]), sl2x2, f32x2(__float_as_uint(n0), __float_as_uint(n1))), t0,
                   t1);
       float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
       // scale dP - scale Delta, then times p
-      const uint64_t g2 = ffma2(f32x2(sv[32 + c + h], sv[32 + c + h + 1]), sc2,
-                                fmul2(f32x2(__float_as_uint(-d0), __float_as_uint(-d1)), sc2));
+      const uint64_t g2 =
+          ffma2(f32x2(sv[32 + c + h], sv[32 + c + h + 1]), sc2, f32x2(__float_as_uint(d0), __float_as_uint(d1)));
       float g0, g1;
       f32x2_split(fmul2(f32x2(__float_as_uint(e0), __float_as_uint(e1)), g2), g0, g1);
       if (kMasked) {
@@ -994,7 +995,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
         tmem_wait_ld();
         tmem_ld32(base + 32, *reinterpret_cast<uint32_t(*)[32]>(sv1));
         tmem_ld32(base + 96, *reinterpret_cast<uint32_t(*)[32]>(sv1 + 32));
-        // -lse*log2e [64] then Delta [64] of the sub-tile's rows
+        // -lse*log2e [64] then -scale*Delta [64] of the sub-tile's rows
         const float4 *rs4 = reinterpret_cast<const float4 *>(st + kOffRowstat);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
