@@ -251,11 +251,19 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
           const int nks = (n + 15) >> 4;
           const int s = g % kStages;
           const uint64_t bv = dV0 + desc_bytes(s * kTile);
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
           if (elect_one()) {
+            // a full block goes out as one straight run of MMAs: a branch
+            // between tcgen05.mma instructions slows their issue
+            if (nks == kBlockKeys / 16) {
+              mma_ts(tmem + kColDQ, tmem + kColDS, bv, id_dq, acc0);
 #pragma unroll
-            for (int kk = 0; kk < kBlockKeys / 16; ++kk)
-              if (kk < nks)
-                mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, bv + mnmaj_step(kk), id_dq, (j > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 1; kk < kBlockKeys / 16; ++kk)
+                mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, bv + mnmaj_step(kk), id_dq, 1u);
+            } else {
+              for (int kk = 0; kk < nks; ++kk)
+                mma_ts(tmem + kColDQ, tmem + kColDS + kk * 8, bv + mnmaj_step(kk), id_dq, kk > 0 ? 1u : acc0);
+            }
             mma_commit(&bars.kv_empty[s]);
             if (!next) mma_commit(&bars.dq_done);
           }

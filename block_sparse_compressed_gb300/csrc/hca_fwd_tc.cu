@@ -302,10 +302,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t d = tmem + col_o(x), a = tmem + col_s(x);
+            const uint32_t acc0 = j > 0 ? 1u : 0u;
             if (elect_one()) {
+              // a full block goes out as one straight run of MMAs: a branch
+              // between tcgen05.mma instructions slows their issue
+              if (nks == kBlockKeys / 16) {
+                mma_ts(d, a, dbv, id_pv, acc0);
 #pragma unroll
-              for (int kk = 0; kk < kBlockKeys / 16; ++kk)
-                if (kk < nks) mma_ts(d, a + kk * 8, dbv + mnmaj_step(kk), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 1; kk < kBlockKeys / 16; ++kk) mma_ts(d, a + kk * 8, dbv + mnmaj_step(kk), id_pv, 1u);
+              } else {
+                for (int kk = 0; kk < nks; ++kk) mma_ts(d, a + kk * 8, dbv + mnmaj_step(kk), id_pv, kk > 0 ? 1u : acc0);
+              }
               if (j == nb - 1) mma_commit(&bars.o_final[x]);
               if (x == 1) mma_commit(&bars.kv_empty[g % kStages]);
             }
