@@ -177,3 +177,36 @@ def test_fwd_489_alone():
     assert_close("dq", dq, rdq, w.dtype)
     assert_close("dkv", dkv, rdkv, w.dtype)
     assert_close("dckv", dckv, rdckv, w.dtype)
+
+
+def visible_comp_ids(seg_row, S, m):
+    """Compressed entries that some query sees: the window lies in one
+    document and completes before that document ends."""
+    Sc = -(-S // m)
+    out = []
+    for j in range(Sc):
+        lo, hi = j * m, (j + 1) * m - 1
+        if hi >= S or seg_row[lo] < 0 or seg_row[lo] != seg_row[hi]:
+            continue
+        out.append(j)
+    return out
+
+
+def test_bwd_dckv_entries_exact_16384():
+    # compressed entries 0, 1, the last visible one and random ones, each
+    # exact over every query that sees it (no cap on the query count)
+    w = I.DOCS_S16384
+    q, kv, ckv, seg, dout = I.tensors(w, device=DEV)
+    out, lse = hca.hca_attn_fwd(q, kv, ckv, seg, w.W, w.m, w.scale, check=True)
+    _, _, dckv = hca.hca_attn_bwd(q, kv, ckv, seg, out, lse, dout, w.W, w.m, w.scale, check=True)
+    qc, kvc, ckvc, dc, segc = q.cpu(), kv.cpu(), ckv.cpu(), dout.cpu(), seg.cpu()
+    dckv_c = to_np(dckv)
+    rng = np.random.Generator(np.random.PCG64(7))
+    for b in range(w.B):
+        vis = visible_comp_ids(segc[b].numpy(), w.S, w.m)
+        assert len(vis) >= 3
+        ids = {vis[0], vis[1], vis[-1]} | set(rng.choice(vis, size=min(4, len(vis)), replace=False).tolist())
+        ids = sorted(int(x) for x in ids)
+        _, ref = oracle.bwd_keys(qc[b:b + 1], kvc[b:b + 1], ckvc[b:b + 1], segc[b:b + 1], dc[b:b + 1], w.W, w.m,
+                                 w.scale, comp_ids=ids)
+        assert_close(f"dckv b{b} entries {ids}", dckv_c[b][ids], ref, w.dtype)
