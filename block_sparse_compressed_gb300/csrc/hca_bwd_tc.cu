@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
     hca_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                       const __grid_constant__ CUtensorMap map_out,
                       const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_ckv,
+                      const __grid_constant__ CUtensorMap map_kv16, const __grid_constant__ CUtensorMap map_ckv16,
                       const __grid_constant__ CUtensorMap map_dq, const DqParams p) {
   using namespace dqk;
   extern __shared__ uint8_t smem_raw[];
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         Tile t;
         tile_coords(Q, u, t);
         tile_ranges_warp(Q, t, lane);
-        const int nb = t.nraw + t.ncomp;
+        const int nb = t.nb;
         if (nb == 0) continue;
         if (lane == 0) {
           if (tw > 0) ok = mbar_wait(&bars.qd_empty, (tw - 1) & 1, abort_flag, p.status);
@@ -160,14 +161,11 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
             if (gb >= (uint32_t)kStages)
               ok = mbar_wait(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status);
             if (!ok) break;
-            bool comp;
-            int start, n;
-            block_of(t, j, comp, start, n);
-            const CUtensorMap *mp = comp ? &map_ckv : &map_kv;
-            uint8_t *dst = smem + kOffKV + s * kTile;
-            mbar_arrive_expect_tx(&bars.kv_full[s], kTile);
-            tma_load_3d(mp, &bars.kv_full[s], dst, 0, start, t.b);
-            tma_load_3d(mp, &bars.kv_full[s], dst + kHalfTile, 64, start, t.b);
+            int n, nc;
+            block_cols(t, j, n, nc);
+            mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes(n, nc));
+            load_block(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
+                       smem + kOffKV + s * kTile);
             last_par[s] = (gb / kStages) & 1;
           }
         }
@@ -203,13 +201,12 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         tile_coords(Q, u, t);
         tile_ranges_warp(Q, t, lane);
         uniform_tile(t);
-        const int nb = t.nraw + t.ncomp;
+        const int nb = t.nb;
         if (nb == 0) continue;
         // S (x = 0) or dP (x = 1) of block j into its TMEM columns
         auto issue_sdp = [&](int x, int j, uint32_t g, bool last_q_use) {
-          bool comp;
-          int start, n;
-          block_of(t, j, comp, start, n);
+          int n, nc;
+          block_cols(t, j, n, nc);
           const uint32_t idesc = idesc_bf16_f32(kRows, (n + 15) & ~15, false, false);
           const uint64_t bk = dK0 + desc_bytes((g % kStages) * kTile);
           const uint64_t da = x ? dDO : dQ;
@@ -245,9 +242,8 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
           ok = wait_warp(&bars.ds_full, g & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          bool comp;
-          int start, n;
-          block_of(t, j, comp, start, n);
+          int n, nc;
+          block_cols(t, j, n, nc);
           const int nks = (n + 15) >> 4;
           const int s = g % kStages;
           const uint64_t bv = dV0 + desc_bytes(s * kTile);
@@ -305,7 +301,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       Tile t;
       tile_coords(Q, u, t);
       tile_ranges_warp(Q, t, lane);
-      const int nb = t.nraw + t.ncomp;
+      const int nb = t.nb;
       const int pq = r % Q.Pq, hh = r / Q.Pq;
       const int head = t.g * Q.HG + hh;
       const int i = t.i0 + pq;
@@ -351,16 +347,14 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       }
       mbar_arrive(&bars.qd_empty);
       for (int j = 0; j < nb; ++j, ++gb) {
-        bool comp;
-        int start, n;
-        block_of(t, j, comp, start, n);
+        int n, nc;
+        block_cols(t, j, n, nc);
         const int nk = (n + 15) & ~15;
-        // visible columns [cb, cb + 64) of this row: one contiguous range
-        uint64_t vis = 0;
-        if (iv.valid) {
-          const int lo = comp ? iv.clo : iv.rlo, hi = comp ? iv.chi : iv.rhi;
-          vis = range_mask64(max(lo - start, 0), min(hi - start, n - 1), cb);
-        }
+        // visible columns [cb, cb + 64) of this row: its compressed range and
+        // its raw range in the block
+        int a1, b1, a2, b2;
+        row_cols(t, iv, j, n, nc, a1, b1, a2, b2);
+        const uint64_t vis = range_mask64(a1, b1, cb) | range_mask64(a2, b2, cb);
         if (!wait_warp(&bars.s_full, gb & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         // P = exp2(S * scale * log2e - lse * log2e), kept in registers so the
@@ -1174,7 +1168,7 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   // a position range when one head fills the tile
   const int sub_hg = q.HG >= 2 ? q.HG / 2 : 1;
   const int sub_pq = q.HG >= 2 ? q.Pq : q.Pq / 2;
-  CUtensorMap mq, mdo, mout, mkv, mckv, mdq, mqs, mdos;
+  CUtensorMap mq, mdo, mout, mkv, mckv, mkv16, mckv16, mdq, mqs, mdos;
   if (!make_map_bf16(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mout, a.out, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mdo, a.dout, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
@@ -1182,7 +1176,9 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
       !make_map_bf16(&mqs, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, sub_pq, sub_hg) ||
       !make_map_bf16(&mdos, a.dout, kHeadDim, a.S, (uint64_t)a.B * a.H, sub_pq, sub_hg) ||
       !make_map_bf16(&mkv, a.kv, kHeadDim, a.S, a.B, kBlockKeys, 1) ||
-      !make_map_bf16(&mckv, a.ckv, kHeadDim, q.Sc, a.B, kBlockKeys, 1))
+      !make_map_bf16(&mckv, a.ckv, kHeadDim, q.Sc, a.B, kBlockKeys, 1) ||
+      !make_map_bf16(&mkv16, a.kv, kHeadDim, a.S, a.B, 16, 1) ||
+      !make_map_bf16(&mckv16, a.ckv, kHeadDim, q.Sc, a.B, 16, 1))
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
@@ -1210,7 +1206,8 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   cudaError_t e;
   {
     ProfScope prof(kKBwdDq, st);
-    hca_bwd_dq_kernel<<<(unsigned)g1, dqk::kThreads, dqk::kSmemBytes, st>>>(mq, mdo, mout, mkv, mckv, mdq, dp);
+    hca_bwd_dq_kernel<<<(unsigned)g1, dqk::kThreads, dqk::kSmemBytes, st>>>(mq, mdo, mout, mkv, mckv, mkv16, mckv16, mdq,
+                                                                            dp);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;

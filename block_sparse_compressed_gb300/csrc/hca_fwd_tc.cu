@@ -10,10 +10,11 @@
 // rows of the MMA (row r = head*Pq + p), loaded by one 3-D TMA box
 // {64, Pq, HG} per 64-column half of q.  A CTA works on a *pair* of adjacent
 // query tiles (A and B) that share one stream of key blocks: the union of the
-// 2*Pq positions' intervals (hca_common.cuh) cut into blocks of <= 128 keys,
-// raw kv blocks first, then compressed ckv blocks.  Keys outside those ranges
-// are never loaded and no mask exists in memory; inside a block every row
-// masks by its own interval.
+// 2*Pq positions' intervals (hca_common.cuh) as one list of columns, the
+// compressed ckv entries then the raw kv keys, cut into blocks of <= 128
+// columns (a block may hold both kinds; tc_tiles.cuh).  Keys outside those
+// ranges are never loaded and no mask exists in memory; inside a block every
+// row masks by its own two intervals.
 //
 // Per key block j and tile X in {A, B}:
 //   S_X = Q_X K^T            tcgen05 SS, fp32 accumulator in TMEM
@@ -76,13 +77,9 @@ struct FwdParams {
   float sl2;           // scale * log2(e)
 };
 
-struct Pair {
-  int b, g, i0;           // tile A starts at i0, tile B at i0 + Pq
-  int rlo, rhi, clo, chi; // union of both tiles' key ranges (half-open)
-  int nraw, ncomp;
-};
-
-__device__ __forceinline__ void pair_coords(const FwdParams &p, long long u, Pair &t) {
+// A pair of adjacent query tiles (A at i0, B at i0 + Pq) shares one key list:
+// the union of both tiles' key ranges, i.e. a Tile of 2 Pq positions.
+__device__ __forceinline__ void pair_coords(const FwdParams &p, long long u, Tile &t) {
   // longest pairs first: the compressed range grows with the position
   const long long per = (long long)p.qt.B * p.qt.groups;
   const int tp = p.ntp - 1 - (int)(u / per);
@@ -92,34 +89,10 @@ __device__ __forceinline__ void pair_coords(const FwdParams &p, long long u, Pai
   t.i0 = tp * 2 * p.qt.Pq;
 }
 
-__device__ __forceinline__ void pair_ranges_warp(const FwdParams &p, Pair &t, int lane) {
-  Tile tt;
-  tt.b = t.b;
-  tt.g = t.g;
-  tt.i0 = t.i0;
+__device__ __forceinline__ void pair_ranges_warp(const FwdParams &p, Tile &t, int lane) {
   QTiling q2 = p.qt;
   q2.Pq = 2 * p.qt.Pq;
-  tile_ranges_warp(q2, tt, lane);
-  t.rlo = tt.rlo; t.rhi = tt.rhi; t.clo = tt.clo; t.chi = tt.chi;
-  t.nraw = tt.nraw; t.ncomp = tt.ncomp;
-}
-
-__device__ __forceinline__ void pair_block(const Pair &t, int j, bool &comp, int &start, int &n) {
-  Tile tt;
-  tt.rlo = t.rlo; tt.rhi = t.rhi; tt.clo = t.clo; tt.chi = t.chi;
-  tt.nraw = t.nraw; tt.ncomp = t.ncomp;
-  block_of(tt, j, comp, start, n);
-}
-
-// Broadcast a pair's ranges from lane 0 so the compiler treats them (and
-// everything derived from them) as warp-uniform.
-__device__ __forceinline__ void uniform_pair(Pair &t) {
-  t.rlo = __shfl_sync(0xffffffffu, t.rlo, 0);
-  t.rhi = __shfl_sync(0xffffffffu, t.rhi, 0);
-  t.clo = __shfl_sync(0xffffffffu, t.clo, 0);
-  t.chi = __shfl_sync(0xffffffffu, t.chi, 0);
-  t.nraw = __shfl_sync(0xffffffffu, t.nraw, 0);
-  t.ncomp = __shfl_sync(0xffffffffu, t.ncomp, 0);
+  tile_ranges_warp(q2, t, lane);
 }
 
 __device__ __forceinline__ void setmaxnreg_inc_softmax() { asm volatile("setmaxnreg.inc.sync.aligned.u32 176;"); }
@@ -141,7 +114,8 @@ struct Bars {
 template <bool kPosScale>
 __global__ void __launch_bounds__(kThreads, 1)
     hca_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
-                      const __grid_constant__ CUtensorMap map_ckv, const __grid_constant__ CUtensorMap map_out,
+                      const __grid_constant__ CUtensorMap map_ckv, const __grid_constant__ CUtensorMap map_kv16,
+                      const __grid_constant__ CUtensorMap map_ckv16, const __grid_constant__ CUtensorMap map_out,
                       const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -189,16 +163,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&map_q);
         tma_prefetch_map(&map_kv);
         tma_prefetch_map(&map_ckv);
+        tma_prefetch_map(&map_kv16);
+        tma_prefetch_map(&map_ckv16);
       }
       uint32_t gb = 0, gq = 0;
       uint32_t issued = 0;  // bit s: stage s loaded at least once; bit 8+s: parity of its last load
       int q_par = -1;
       bool ok = !poisoned;
       for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
-        Pair t;
+        Tile t;
         pair_coords(p, u, t);
         pair_ranges_warp(p, t, lane);
-        const int nb = t.nraw + t.ncomp;
+        const int nb = t.nb;
         if (nb == 0) continue;
         if (lane == 0) {
           if (gq > 0) ok = mbar_wait(&bars.q_empty, (gq - 1) & 1, abort_flag, p.status);
@@ -219,14 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (gb >= (uint32_t)kStages)
               ok = mbar_wait(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status);
             if (!ok) break;
-            bool comp;
-            int start, n;
-            pair_block(t, j, comp, start, n);
-            const CUtensorMap *mp = comp ? &map_ckv : &map_kv;
-            uint8_t *dst = smem + kOffKV + s * kTile;
-            mbar_arrive_expect_tx(&bars.kv_full[s], kTile);
-            tma_load_3d(mp, &bars.kv_full[s], dst, 0, start, t.b);
-            tma_load_3d(mp, &bars.kv_full[s], dst + kHalfTile, 64, start, t.b);
+            int n, nc;
+            block_cols(t, j, n, nc);
+            mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes(n, nc));
+            load_block(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
+                       smem + kOffKV + s * kTile);
             issued = (issued | (1u << s)) & ~(1u << (8 + s));
             issued |= ((gb / kStages) & 1u) << (8 + s);
           }
@@ -258,16 +231,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t gb = 0, gq = 0, pcnt = 0;
       bool ok = !poisoned, issued = false;
       for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
-        Pair t;
+        Tile t;
         pair_coords(p, u, t);
         pair_ranges_warp(p, t, lane);
-        uniform_pair(t);
-        const int nb = t.nraw + t.ncomp;
+        uniform_tile(t);
+        const int nb = t.nb;
         if (nb == 0) continue;
         auto issue_s = [&](int x, int j, uint32_t g, uint64_t *extra) {
-          bool comp;
-          int start, n;
-          pair_block(t, j, comp, start, n);
+          int n, nc;
+          block_cols(t, j, n, nc);
           const uint32_t idesc = idesc_bf16_f32(kRows, (n + 15) & ~15, false, false);
           const uint64_t da = x ? dq1 : dq0;
           const uint64_t db = dk0 + desc_bytes((g % kStages) * kTile);
@@ -291,9 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; ok && j < nb; ++j) {
           const uint32_t g = gb + j;
           const bool next = j + 1 < nb;
-          bool comp;
-          int start, n;
-          pair_block(t, j, comp, start, n);
+          int n, nc;
+          block_cols(t, j, n, nc);
           const int nks = (n + 15) >> 4;
           const uint64_t dbv = dv0 + desc_bytes((g % kStages) * kTile);
           for (int x = 0; ok && x < 2; ++x) {
@@ -354,10 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       return rr;
     };
     for (long long u = blockIdx.x; ok && !poisoned && u < p.npairs; u += gridDim.x) {
-      Pair t;
+      Tile t;
       pair_coords(p, u, t);
       pair_ranges_warp(p, t, lane);
-      const int nb = t.nraw + t.ncomp;
+      const int nb = t.nb;
       if (nb == 0) continue;
       for (int x = 0; ok && x < 2; ++x) {
         const int i0 = t.i0 + x * Q.Pq;
@@ -416,10 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t scnt = 0, gq = 0;
     bool ok = true;
     for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
-      Pair t;
+      Tile t;
       pair_coords(p, u, t);
       pair_ranges_warp(p, t, lane);
-      const int nb = t.nraw + t.ncomp;
+      const int nb = t.nb;
       const int pq = r % Q.Pq, hh = r / Q.Pq;
       const int head = t.g * Q.HG + hh;
       const int i = t.i0 + x * Q.Pq + pq;
@@ -438,16 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < nb; ++j) {
-        bool comp;
-        int start, n;
-        pair_block(t, j, comp, start, n);
+        int n, nc;
+        block_cols(t, j, n, nc);
         const int nk = (n + 15) & ~15;
-        int lo_c = 0, hi_c = -1;
-        if (iv.valid) {
-          const int lo = comp ? iv.clo : iv.rlo, hi = comp ? iv.chi : iv.rhi;
-          lo_c = max(lo - start, 0);
-          hi_c = min(hi - start, n - 1);
-        }
+        // the row's visible columns: [a1, b1] compressed, [a2, b2] raw
+        int a1, b1, a2, b2;
+        row_cols(t, iv, j, n, nc, a1, b1, a2, b2);
         // S_X(j) ready; since S_X(j) was issued after PV_X(j-1), O_X is stable
         if (!wait_warp(&bars.s_full[x], scnt & 1, abort_flag, p.status)) { ok = false; break; }
         ++scnt;
@@ -455,11 +422,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // One TMEM round trip brings the row's nk scores into registers; the
         // masked row max, then exp2 / row sum / bf16 packing 32 columns at a
         // time.  P_X overwrites the first nk/2 columns of S_X.  Columns outside
-        // [lo_c, hi_c] are masked -- that also covers the columns past n of a
-        // short block -- and a chunk that every row of the warp sees whole
-        // skips the per-element test (warp-uniform).
-        const int wlo = __reduce_max_sync(0xffffffffu, lo_c);
-        const int whi = __reduce_min_sync(0xffffffffu, hi_c);
+        // the row's two ranges are masked -- that also covers the padding
+        // entries and the columns past n of a short block -- and a chunk that
+        // every row of the warp sees whole skips the per-element test
+        // (warp-uniform).
         const uint32_t sbase = lane_addr + col_s(x);
         uint32_t sv[kBlockKeys];
         {
@@ -481,11 +447,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
             if (c0 < nk) {
-              const bool whole = c0 >= wlo && c0 + 31 <= whi;
-              if (!whole) {
+              const bool whole = (c0 >= a1 && c0 + 31 <= b1) || (c0 >= a2 && c0 + 31 <= b2);
+              if (!__all_sync(0xffffffffu, whole)) {
+                const uint32_t vm = (uint32_t)(range_mask64(a1, b1, c0) | range_mask64(a2, b2, c0));
 #pragma unroll
                 for (int y = 0; y < 32; ++y)
-                  if (c0 + y < lo_c || c0 + y > hi_c) sv[c0 + y] = __float_as_uint(ninf);
+                  if (!((vm >> y) & 1u)) sv[c0 + y] = __float_as_uint(ninf);
               }
 #pragma unroll
               for (int y = 0; y < 32; y += 16) {
@@ -597,11 +564,13 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st) {
   const QTiling &q = p.qt;
   p.ntp = (q.ntq + 1) / 2;
   p.npairs = (long long)a.B * q.groups * p.ntp;
-  CUtensorMap mq, mkv, mckv, mout;
+  CUtensorMap mq, mkv, mckv, mkv16, mckv16, mout;
   if (!make_map_bf16(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mout, a.out, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mkv, a.kv, kHeadDim, a.S, a.B, kBlockKeys, 1) ||
-      !make_map_bf16(&mckv, a.ckv, kHeadDim, q.Sc, a.B, kBlockKeys, 1))
+      !make_map_bf16(&mckv, a.ckv, kHeadDim, q.Sc, a.B, kBlockKeys, 1) ||
+      !make_map_bf16(&mkv16, a.kv, kHeadDim, a.S, a.B, 16, 1) ||
+      !make_map_bf16(&mckv16, a.ckv, kHeadDim, q.Sc, a.B, 16, 1))
     return cudaErrorInvalidValue;
   p.status = a.status_rw;
   p.lse = a.lse;
@@ -620,7 +589,7 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st) {
   const long long grid = p.npairs < sms ? p.npairs : sms;
   if (grid == 0) return cudaSuccess;
   ProfScope prof(kKFwdTc, st);
-  kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mkv, mckv, mout, p);
+  kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mkv, mckv, mkv16, mckv16, mout, p);
   return cudaGetLastError();
 }
 

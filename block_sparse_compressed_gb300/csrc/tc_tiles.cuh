@@ -33,10 +33,17 @@ struct QTiling {
   long long ntiles;
 };
 
+// A tile's keys form one list of columns: the compressed entries
+// [clo, clo + cpad) (cpad = chi - clo rounded up to 16; the extra entries are
+// masked) followed by the raw keys [rlo, rhi).  Blocks are consecutive
+// 128-column slices of that list, so the few raw keys past a 128-key window
+// share a block with the last compressed entries instead of taking a block
+// of their own.
 struct Tile {
   int b, g, i0;
   int rlo, rhi, clo, chi;  // half-open key ranges (union over the tile's rows)
-  int nraw, ncomp;         // blocks of <= kBlockKeys keys
+  int cpad;                // column where the raw keys start (multiple of 16)
+  int ncols, nb;           // columns of the key list, blocks of <= kBlockKeys columns
 };
 
 // Tile u of the schedule: positions descending, so the tiles with the most
@@ -74,8 +81,9 @@ __device__ __forceinline__ void tile_ranges_warp(const QTiling &p, Tile &t, int 
   t.rhi = rhi < 0 ? 0 : rhi + 1;
   t.clo = chi < 0 ? 0 : clo;
   t.chi = chi < 0 ? 0 : chi + 1;
-  t.nraw = (t.rhi - t.rlo + kBlockKeys - 1) / kBlockKeys;
-  t.ncomp = (t.chi - t.clo + kBlockKeys - 1) / kBlockKeys;
+  t.cpad = (t.chi - t.clo + 15) & ~15;
+  t.ncols = t.cpad + (t.rhi - t.rlo);
+  t.nb = (t.ncols + kBlockKeys - 1) / kBlockKeys;
 }
 
 // Broadcast a tile's ranges from lane 0: the compiler then treats them and
@@ -85,20 +93,66 @@ __device__ __forceinline__ void uniform_tile(Tile &t) {
   t.rhi = __shfl_sync(0xffffffffu, t.rhi, 0);
   t.clo = __shfl_sync(0xffffffffu, t.clo, 0);
   t.chi = __shfl_sync(0xffffffffu, t.chi, 0);
-  t.nraw = __shfl_sync(0xffffffffu, t.nraw, 0);
-  t.ncomp = __shfl_sync(0xffffffffu, t.ncomp, 0);
+  t.cpad = __shfl_sync(0xffffffffu, t.cpad, 0);
+  t.ncols = __shfl_sync(0xffffffffu, t.ncols, 0);
+  t.nb = __shfl_sync(0xffffffffu, t.nb, 0);
 }
 
-// Block j of a tile: raw kv blocks first, then compressed ckv blocks.
-__device__ __forceinline__ void block_of(const Tile &t, int j, bool &comp, int &start, int &n) {
-  if (j < t.nraw) {
-    comp = false;
-    start = t.rlo + j * kBlockKeys;
-    n = min(kBlockKeys, t.rhi - start);
+// Block j of a tile: columns [128 j, 128 j + n) of the key list, of which
+// the first nc (a multiple of 16) are compressed entries and the rest raw keys.
+__device__ __forceinline__ void block_cols(const Tile &t, int j, int &n, int &nc) {
+  const int c0 = j * kBlockKeys;
+  n = min(kBlockKeys, t.ncols - c0);
+  nc = min(max(t.cpad - c0, 0), n);
+}
+
+// Columns of block j that a row sees, as two inclusive ranges: [a1, b1] of
+// compressed entries and [a2, b2] of raw keys (either may be empty; b1 < a2).
+__device__ __forceinline__ void row_cols(const Tile &t, const RowIv &iv, int j, int n, int nc, int &a1, int &b1,
+                                         int &a2, int &b2) {
+  if (!iv.valid) {
+    a1 = a2 = 0;
+    b1 = b2 = -1;
+    return;
+  }
+  const int c0 = j * kBlockKeys;
+  a1 = max(iv.clo - t.clo - c0, 0);
+  b1 = min(iv.chi - t.clo - c0, nc - 1);
+  const int off = t.rlo + c0 - t.cpad;  // raw key of column c: off + c
+  a2 = max(iv.rlo - off, nc);
+  b2 = min(iv.rhi - off, n - 1);
+}
+
+// Bytes that load_block delivers for a block of n columns, nc compressed.
+__device__ __forceinline__ uint32_t block_load_bytes(int n, int nc) {
+  if (nc == n || nc == 0) return (uint32_t)kTile;
+  return (uint32_t)(nc / 16 + (n - nc + 15) / 16) * 16u * 256u;
+}
+
+// TMA loads of block j's key rows into a 128-row tile at dst (two 64-column
+// swizzled halves).  A block of one kind is one 128-row box per half; a block
+// that holds both kinds is loaded in 16-row boxes (2 KB, so every box starts
+// on a 1 KB swizzle atom), compressed rows first.
+__device__ __forceinline__ void load_block(const Tile &t, int j, int n, int nc, const CUtensorMap *kv,
+                                           const CUtensorMap *ckv, const CUtensorMap *kv16, const CUtensorMap *ckv16,
+                                           uint64_t *bar, uint8_t *dst) {
+  const int c0 = j * kBlockKeys;
+  const int off = t.rlo + c0 - t.cpad;
+  if (nc == n) {
+    tma_load_3d(ckv, bar, dst, 0, t.clo + c0, t.b);
+    tma_load_3d(ckv, bar, dst + kHalfTile, 64, t.clo + c0, t.b);
+  } else if (nc == 0) {
+    tma_load_3d(kv, bar, dst, 0, off, t.b);
+    tma_load_3d(kv, bar, dst + kHalfTile, 64, off, t.b);
   } else {
-    comp = true;
-    start = t.clo + (j - t.nraw) * kBlockKeys;
-    n = min(kBlockKeys, t.chi - start);
+    for (int r = 0; r < nc; r += 16) {
+      tma_load_3d(ckv16, bar, dst + r * 128, 0, t.clo + c0 + r, t.b);
+      tma_load_3d(ckv16, bar, dst + kHalfTile + r * 128, 64, t.clo + c0 + r, t.b);
+    }
+    for (int r = nc; r < n; r += 16) {
+      tma_load_3d(kv16, bar, dst + r * 128, 0, off + r, t.b);
+      tma_load_3d(kv16, bar, dst + kHalfTile + r * 128, 64, off + r, t.b);
+    }
   }
 }
 
