@@ -488,8 +488,8 @@ namespace dkk {
 // holds a sub-tile as one 128-row operand R = [Q_sub ; dO_sub] (64 rows each,
 // per 64-column half): a single N = 128 MMA K R^T yields S^T (columns 0-63)
 // and dP^T (columns 64-127) of the sub-tile for one key block.
-// two P^T/dS^T warpgroups (each takes every other work unit, i.e. one TMEM
-// buffer, and 64 of a key row's 128 accumulator columns), TMA warp, MMA warp
+// two P^T/dS^T warpgroups (each takes 32 of every unit's 64 query columns
+// and 64 of a key row's 128 accumulator columns), TMA warp, MMA warp
 constexpr int kEW = 256;
 constexpr int kThreads = kEW + 128;
 // 12 warps put 3 on each SM sub-partition (16K registers each): 168 per
@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars.s_full[x], 1);
-      mbar_init(&bars.p_full[x], kEW / 2);  // one warpgroup per buffer
+      mbar_init(&bars.p_full[x], kEW);  // both warpgroups write every unit
     }
     mbar_init(&bars.acc_full, 1);
     mbar_init(&bars.acc_free, kEW);
@@ -912,8 +912,8 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
   } else {
     setmaxnreg_inc<kRegEW>();
     // ------------------------------------------------------------ P^T, dS^T + item epilogue
-    // thread kr of warpgroup wg owns key row kr (TMEM lane kr) of the units
-    // in TMEM buffer wg (every other unit) and accumulator columns
+    // thread kr of warpgroup wg owns key row kr (TMEM lane kr), query columns
+    // [32 wg, 32 wg + 32) of every unit and accumulator columns
     // [64 wg, 64 wg + 64) of the item epilogue
     const int kr = tid & (kRows - 1), wg = tid >> 7;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -956,9 +956,11 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
         continue;
       }
       const int nu = nsub * nkb;
-      // units alternate between the warpgroups (and TMEM buffers): one
-      // warpgroup's exp/dS math overlaps the other's TMEM traffic and waits
-      for (int w = wg; w < nu; w += 2) {
+      // both warpgroups work on every unit, warpgroup h on query rows
+      // [32 h, 32 h + 32) of its sub-tile: half the latency per unit, which
+      // is what the tensor pipe waits on with two TMEM buffers in flight
+      const int h = wg;
+      for (int w = 0; w < nu; ++w) {
         const int v = nkb == 2 ? (w >> 1) : w, a = nkb == 2 ? (w & 1) : 0;
         const uint32_t g = gu + w;
         const uint32_t sg = gsub + v;
@@ -968,9 +970,9 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
         tc_fence_after();
         const uint32_t base = lane_addr + col_buf(g);
         // query rows [32 h, 32 h + 32): S^T columns 32 h.., dP^T columns 64 + 32 h..
-        uint32_t sv0[64], sv1[64];
-        tmem_ld32(base, *reinterpret_cast<uint32_t(*)[32]>(sv0));
-        tmem_ld32(base + 64, *reinterpret_cast<uint32_t(*)[32]>(sv0 + 32));
+        uint32_t sv[64];
+        tmem_ld32(base + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        tmem_ld32(base + 64 + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
         // visibility of this key for the 64 columns (query rows) of the
         // sub-tile: column c sits at position c mod sub_pq of the sub-tile
         const int key = it.k0[a] + kr;
@@ -994,33 +996,27 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
             vis = pat;
           }
         }
-        tmem_wait_ld();
-        tmem_ld32(base + 32, *reinterpret_cast<uint32_t(*)[32]>(sv1));
-        tmem_ld32(base + 96, *reinterpret_cast<uint32_t(*)[32]>(sv1 + 32));
+        const uint32_t vis32 = (uint32_t)(vis >> (32 * h));
         // -lse*log2e [64] then -scale*Delta [64] of the sub-tile's rows
         const float4 *rs4 = reinterpret_cast<const float4 *>(st + kOffRowstat);
+        uint32_t pk[16], dk[16];
+        // warp-uniform cases: no visible pair (P^T = dS^T = 0), every pair
+        // visible (no masking), or a mix
+        const bool none = __all_sync(0xffffffffu, vis32 == 0u);
+        const bool all = __all_sync(0xffffffffu, vis32 == ~0u);
+        tmem_wait_ld();
+        if (none) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (h == 1) tmem_wait_ld();
-          const uint32_t vis32 = (uint32_t)(vis >> (32 * h));
-          uint32_t pk[16], dk[16];
-          // warp-uniform cases: no visible pair (P^T = dS^T = 0), every pair
-          // visible (no masking), or a mix
-          const bool none = __all_sync(0xffffffffu, vis32 == 0u);
-          const bool all = __all_sync(0xffffffffu, vis32 == ~0u);
-          if (none) {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) pk[c] = dk[c] = 0u;
-          } else if (all) {
-            ew_unit<false>(h ? sv1 : sv0, rs4 + 8 * h, 0u, sl2x2, sc2, pk, dk);
-          } else {
-            ew_unit<true>(h ? sv1 : sv0, rs4 + 8 * h, vis32, sl2x2, sc2, pk, dk);
-          }
-          // packed P^T and dS^T of query rows [32 h, 32 h + 32) go over S^T
-          // columns 32 h .. 32 h + 31, which this thread has read
-          tmem_st16(base + 32 * h, pk);
-          tmem_st16(base + 32 * h + 16, dk);
+          for (int c = 0; c < 16; ++c) pk[c] = dk[c] = 0u;
+        } else if (all) {
+          ew_unit<false>(sv, rs4 + 8 * h, 0u, sl2x2, sc2, pk, dk);
+        } else {
+          ew_unit<true>(sv, rs4 + 8 * h, vis32, sl2x2, sc2, pk, dk);
         }
+        // packed P^T and dS^T of query rows [32 h, 32 h + 32) go over S^T
+        // columns 32 h .. 32 h + 31, which this thread has read
+        tmem_st16(base + 32 * h, pk);
+        tmem_st16(base + 32 * h + 16, dk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars.p_full[g & 1]);
