@@ -79,6 +79,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   // fastest without it (polling warps take issue slots from warps with work)
   for (uint32_t it = 0; it < spin; ++it)
     if (mbar_try_wait(a, parity)) return true;
+  // the clock is read only once the phase is found incomplete
+  if (mbar_try_wait_suspend(a, parity, kSuspendHintNs)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_suspend(a, parity, kSuspendHintNs)) return true;
