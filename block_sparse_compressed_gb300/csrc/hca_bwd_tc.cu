@@ -155,6 +155,20 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
             tma_load_3d(&map_out, &bars.qd_full, smem + kOffO, 0, t.i0, c2);
             tma_load_3d(&map_out, &bars.qd_full, smem + kOffO + kHalfTile, 64, t.i0, c2);
             q_par = tw & 1;
+            // this CTA's next tile: its q, dO and out rows go to L2 now, so
+            // the loads at the tile boundary do not wait on HBM
+            const long long un = u + gridDim.x;
+            if (un < Q.ntiles) {
+              Tile tn;
+              tile_coords(Q, un, tn);
+              const int cn = tn.b * Q.H + tn.g * Q.HG;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                tma_prefetch_3d(&map_q, 64 * hh, tn.i0, cn);
+                tma_prefetch_3d(&map_do, 64 * hh, tn.i0, cn);
+                tma_prefetch_3d(&map_out, 64 * hh, tn.i0, cn);
+              }
+            }
           }
           for (int j = 0; ok && j < nb; ++j, ++gb) {
             const int s = gb % kStages;

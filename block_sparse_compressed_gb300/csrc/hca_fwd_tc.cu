@@ -189,6 +189,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + kTile + kHalfTile, 64, t.i0 + Q.Pq, c2);
             }
             q_par = gq & 1;
+            // this CTA's next pair: its q rows go to L2 now
+            const long long un = u + gridDim.x;
+            if (un < p.npairs) {
+              Tile tn;
+              pair_coords(p, un, tn);
+              const int cn = tn.b * Q.H + tn.g * Q.HG;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                tma_prefetch_3d(&map_q, 64 * hh, tn.i0, cn);
+                if (tn.i0 + Q.Pq < Q.S) tma_prefetch_3d(&map_q, 64 * hh, tn.i0 + Q.Pq, cn);
+              }
+            }
           }
           for (int j = 0; ok && j < nb; ++j, ++gb) {
             const int s = gb % kStages;
