@@ -44,6 +44,8 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # S^T + dP^T + dK + dV.
 KERNEL_FLOP_PER_PAIR_D = {"hca_fwd_tc": 4, "hca_bwd_dq": 6, "hca_bwd_dkv": 8}
 KERNEL_SOURCES = {"hca_fwd_tc": "hca_fwd_tc.cu", "hca_bwd_dq": "hca_bwd_tc.cu", "hca_bwd_dkv": "hca_bwd_tc.cu"}
+# headers every tensor-core kernel is built from (part of a kernel's digest)
+KERNEL_HEADERS = ("hca_common.cuh", "tc_ptx.cuh", "tc_tiles.cuh")
 # secondary roof: exponentials.  ex2.approx.f32 issues at 32 per clock per SM
 # on GB300 (measured with 1024 threads x 8 independent chains per SM); the
 # path needs one exp per visible pair and head in the forward and one in each
@@ -178,12 +180,17 @@ class ClockSampler:
 # profiles: DRAM traffic of the dominant kernel from a committed ncu summary
 # ---------------------------------------------------------------------------
 def source_digest(kernel: str) -> str:
-    src = os.path.join(ROOT, "block_sparse_compressed_gb300", "csrc", KERNEL_SOURCES.get(kernel, ""))
+    csrc = os.path.join(ROOT, "block_sparse_compressed_gb300", "csrc")
+    if kernel not in KERNEL_SOURCES:
+        return ""
+    h = hashlib.sha256()
     try:
-        with open(src, "rb") as f:
-            return hashlib.sha256(f.read()).hexdigest()[:16]
+        for name in (KERNEL_SOURCES[kernel],) + KERNEL_HEADERS:
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
     except OSError:
         return ""
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel: str, work_key: str):

@@ -185,9 +185,8 @@ __host__ __device__ constexpr uint64_t desc_bytes(uint32_t bytes) { return (uint
 
 // Bounded wait whose outcome is the same for the whole warp, so that a warp
 // never splits around warp-collective tcgen05.ld / tcgen05.st.
-__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort, int32_t *status,
-                                          uint32_t spin = 0) {
-  const bool ok = mbar_wait(bar, parity, abort, status, kWaitLimitNs, spin);
+__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort, int32_t *status) {
+  const bool ok = mbar_wait(bar, parity, abort, status, kWaitLimitNs);
   return __all_sync(0xffffffffu, ok);
 }
 
