@@ -59,6 +59,15 @@ def test_edge_windows_bf16(W, m):
     run_case(1, 8, 300, 128, W, m, torch.bfloat16)
 
 
+@pytest.mark.parametrize("H,W,m", [(64, 16, 1), (64, 113, 2), (64, 128, 8), (64, 200, 1), (128, 128, 1), (16, 48, 2)])
+def test_key_list_block_boundaries_bf16(H, W, m):
+    # a tile's key list is its compressed entries (padded to 16) then its raw
+    # keys, cut into 128-column blocks: over 700 positions the compressed
+    # count takes every residue mod 16 and mod 128, so blocks hold compressed
+    # rows only, raw rows only, or both (16-row loads), and last blocks are short
+    run_case(1, H, 700, 128, W, m, torch.bfloat16)
+
+
 @pytest.mark.parametrize("H", [1, 4, 16, 64, 128, 256])
 def test_heads_bf16(H):
     run_case(1, H, 260, 128, 64, 32, torch.bfloat16)
