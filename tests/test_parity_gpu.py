@@ -68,6 +68,14 @@ def test_key_list_block_boundaries_bf16(H, W, m):
     run_case(1, H, 700, 128, W, m, torch.bfloat16)
 
 
+@pytest.mark.parametrize("scale", [2.0, -1.0 / math.sqrt(128)])
+def test_rescale_and_negative_scale_bf16(scale):
+    # scale 2 spreads the logits (std ~ 23), so a row's running max grows by
+    # more than 2^8 between key blocks and O is rescaled; a negative scale
+    # runs the forward's min-based instantiation
+    run_case(1, 64, 600, 128, 128, 16, torch.bfloat16, scale=scale)
+
+
 @pytest.mark.parametrize("H", [1, 4, 16, 64, 128, 256])
 def test_heads_bf16(H):
     run_case(1, H, 260, 128, 64, 32, torch.bfloat16)
