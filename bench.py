@@ -26,6 +26,7 @@ import os
 import re
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -134,7 +135,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples go to $HCA_BENCH_CLOCKS_DIR when set (to keep them), else a temporary directory
+        out_dir = os.environ.get("HCA_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"hca_bench_clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:
