@@ -1,4 +1,6 @@
-"""fp64 CPU oracle for Heavily Compressed Attention (HCA).
+"""fp64 CPU oracle for Heavily Compressed Attention (HCA) and for its sparse
+variant (CSA: the same sets, compressed entries also selected per query by an
+indexer keep mask that is an input here).
 
 TEST INFRASTRUCTURE ONLY.  This package is imported by ``tests/``, by
 ``__graft_entry__.smoke()`` and by the CPU-baseline leg of ``bench.py``; the
@@ -57,8 +59,12 @@ def _load():
             lib.hca_oracle_visible_pairs.argtypes = [P, i, i, i, i, P, P]
             lib.hca_oracle_tile_ranges.argtypes = [P, i, i, i, i, i, P]
             lib.hca_oracle_num_threads.argtypes = [i]
+            lib.hca_oracle_csa_fwd.argtypes = [P, P, P, P, P, i, i, i, i, i, i, i, d, i, i, P, P, i]
+            lib.hca_oracle_csa_bwd.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, i, d, i, i, P, P, P, i]
+            lib.hca_oracle_csa_visible_pairs.argtypes = [P, P, i, i, i, i, P, P]
             for f in ("hca_oracle_fwd", "hca_oracle_bwd", "hca_oracle_bwd_keys",
-                      "hca_oracle_visible_pairs", "hca_oracle_tile_ranges", "hca_oracle_num_threads"):
+                      "hca_oracle_visible_pairs", "hca_oracle_tile_ranges", "hca_oracle_num_threads",
+                      "hca_oracle_csa_fwd", "hca_oracle_csa_bwd", "hca_oracle_csa_visible_pairs"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -199,3 +205,77 @@ def tile_ranges(seg, B: int, S: int, W: int, m: int, Pq: int):
     if rc != 0:
         raise RuntimeError(f"hca_oracle_tile_ranges failed ({rc})")
     return out
+
+
+# --------------------------------------------------------------------------
+# compressed sparse attention (CSA): the HCA sets with an indexer selection
+# --------------------------------------------------------------------------
+
+def topk_mask(topk, Sc: int):
+    """Dense keep mask uint8[B,S,Sc] from per-query index lists int[B,S,k]
+    (entries outside [0, Sc), e.g. -1 padding, select nothing)."""
+    try:
+        import torch
+        if isinstance(topk, torch.Tensor):
+            topk = topk.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    t = np.asarray(topk, dtype=np.int64)
+    B, S, _ = t.shape
+    sel = np.zeros((B, S, Sc), dtype=np.uint8)
+    b, i, _k = np.nonzero((t >= 0) & (t < Sc))
+    sel[b, i, t[b, i, _k]] = 1
+    return sel
+
+
+def _sel(sel, B, S, Sc):
+    s = np.ascontiguousarray(np.asarray(sel) != 0, dtype=np.uint8)
+    assert s.shape == (B, S, Sc), s.shape
+    return s
+
+
+def csa_fwd(q, kv, ckv, seg, sel, W: int, m: int, scale: float, rows=None, nthreads: int = 0):
+    """CSA out[B,H,S,D], lse[B,H,S] (float64); sel[B,S,Sc] keeps (query,
+    compressed entry) pairs (see ``topk_mask``)."""
+    qa, kva, ca, _, dt = _inputs(q, kv, ckv)
+    B, H, S, D = qa.shape
+    sg = _seg(seg, B, S)
+    sl = _sel(sel, B, S, -(-S // m))
+    lo, hi = rows if rows is not None else (0, S)
+    out = np.full((B, H, S, D), np.nan)
+    lse = np.full((B, H, S), np.nan)
+    rc = _load().hca_oracle_csa_fwd(_ptr(qa), _ptr(kva), _ptr(ca), _ptr(sg), _ptr(sl), dt, B, H, S, D, W, m,
+                                    float(scale), lo, hi, _ptr(out), _ptr(lse), nthreads)
+    if rc != 0:
+        raise RuntimeError(f"hca_oracle_csa_fwd failed ({rc})")
+    return out, lse
+
+
+def csa_bwd(q, kv, ckv, seg, sel, dout, W: int, m: int, scale: float, rows=None, nthreads: int = 0):
+    """CSA dq[B,H,S,D], dkv[B,S,D], dckv[B,Sc,D] (float64)."""
+    qa, kva, ca, da, dt = _inputs(q, kv, ckv, dout)
+    B, H, S, D = qa.shape
+    Sc = -(-S // m)
+    sg = _seg(seg, B, S)
+    sl = _sel(sel, B, S, Sc)
+    lo, hi = rows if rows is not None else (0, S)
+    dq = np.full((B, H, S, D), np.nan)
+    dkv = np.zeros((B, S, D))
+    dckv = np.zeros((B, Sc, D))
+    rc = _load().hca_oracle_csa_bwd(_ptr(qa), _ptr(kva), _ptr(ca), _ptr(sg), _ptr(sl), _ptr(da), dt, B, H, S, D,
+                                    W, m, float(scale), lo, hi, _ptr(dq), _ptr(dkv), _ptr(dckv), nthreads)
+    if rc != 0:
+        raise RuntimeError(f"hca_oracle_csa_bwd failed ({rc})")
+    return dq, dkv, dckv
+
+
+def csa_visible_pairs(seg, sel, B: int, S: int, W: int, m: int):
+    """CSA (raw_pairs[B], comp_pairs[B]) int64, counted per element."""
+    sg = _seg(seg, B, S)
+    sl = _sel(sel, B, S, -(-S // m))
+    raw = np.zeros(B, dtype=np.int64)
+    comp = np.zeros(B, dtype=np.int64)
+    rc = _load().hca_oracle_csa_visible_pairs(_ptr(sg), _ptr(sl), B, S, W, m, _ptr(raw), _ptr(comp))
+    if rc != 0:
+        raise RuntimeError(f"hca_oracle_csa_visible_pairs failed ({rc})")
+    return raw, comp

@@ -37,6 +37,17 @@
  *   Positions with seg < 0 are padding: they are neither queries nor keys;
  *   their out and dq rows are 0 and their lse is -inf.
  *
+ *   Compressed sparse attention (CSA) takes the same two sets, except that a
+ *   compressed entry also has to be kept by the indexer's top-k selection for
+ *   that query ("Add HCA Static Compilation for Splash Attention [Deepseek
+ *   v4]", Description: CSA, compress ratio 4, needs a top-k step and runtime
+ *   indexer masks; "DSV4: Route compressed and sliding train attention onto
+ *   the splash kernels": the indexer mask keeps or discards a (query,
+ *   compressed entry) pair).  The hca_oracle_csa_* entry points take that
+ *   selection as a dense keep mask sel[B,S,Sc]; the pages do not define the
+ *   indexer, so the selection is an input.  Completion and document rules are
+ *   those above (the plainest reading: selection narrows the HCA set).
+ *
  * Inputs are read in their stored type (bf16 bits, fp32 or fp64) and widened
  * exactly to double; every result is double.  Parallelism is plain pthreads
  * over independent rows; each output element is produced by one thread in a
@@ -72,6 +83,8 @@ typedef struct {
   int32_t *win_id;    /* [B,Sc]: the id shared by all m positions of
                          window j, or INT32_MIN when the window mixes ids,
                          touches padding or runs past S               */
+  const uint8_t *sel; /* [B,S,Sc] CSA keep mask (nonzero = the indexer
+                         kept entry j for query i); NULL for HCA      */
 } vis_t;
 
 static int32_t seg_at(const vis_t *v, int b, int x) {
@@ -81,6 +94,7 @@ static int32_t seg_at(const vis_t *v, int b, int x) {
 static int vis_init(vis_t *v, const int32_t *seg, int B, int S, int W, int m) {
   v->seg = seg; v->B = B; v->S = S; v->W = W; v->m = m;
   v->Sc = (S + m - 1) / m;
+  v->sel = NULL;
   v->win_id = (int32_t *)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1) * (v->Sc > 0 ? v->Sc : 1));
   if (!v->win_id) return -1;
   for (int b = 0; b < B; ++b)
@@ -110,6 +124,7 @@ static int comp_visible(const vis_t *v, int b, int i, int j) {
   int32_t si = seg_at(v, b, i);
   if (si < 0 || j < 0 || j >= v->Sc) return 0;
   if ((long)(j + 1) * v->m > (long)i + 1) return 0;
+  if (v->sel && !v->sel[((size_t)b * v->S + i) * v->Sc + j]) return 0;
   return v->win_id[(size_t)b * v->Sc + j] == si;
 }
 
@@ -265,19 +280,34 @@ static int check_rows(int S, int *rb, int *re) {
 
 /* out[B,H,S,D] and lse[B,H,S] for query positions [row_begin,row_end) of
  * every batch row (other rows are left untouched). */
-int hca_oracle_fwd(const void *q, const void *kv, const void *ckv, const int32_t *seg, int dtype,
-                   int B, int H, int S, int D, int W, int m, double scale,
-                   int row_begin, int row_end, double *out, double *lse, int nthreads) {
+static int fwd_impl(const void *q, const void *kv, const void *ckv, const int32_t *seg, const uint8_t *sel,
+                    int dtype, int B, int H, int S, int D, int W, int m, double scale,
+                    int row_begin, int row_end, double *out, double *lse, int nthreads) {
   if (B < 0 || H < 1 || S < 0 || D < 1 || W < 1 || m < 1) return -2;
   if (!check_rows(S, &row_begin, &row_end)) return -2;
   prob_t P;
   memset(&P, 0, sizeof P);
   if (vis_init(&P.v, seg, B, S, W, m)) return -1;
+  P.v.sel = sel;
   P.q = q; P.kv = kv; P.ckv = ckv; P.dt = dtype; P.H = H; P.D = D; P.scale = scale;
   P.row_begin = row_begin; P.row_end = row_end; P.out = out; P.lse = lse;
   int rc = run_pool(fwd_task, &P, (long)B * (row_end - row_begin), keys_scratch(&P), nthreads);
   free(P.v.win_id);
   return rc;
+}
+
+int hca_oracle_fwd(const void *q, const void *kv, const void *ckv, const int32_t *seg, int dtype,
+                   int B, int H, int S, int D, int W, int m, double scale,
+                   int row_begin, int row_end, double *out, double *lse, int nthreads) {
+  return fwd_impl(q, kv, ckv, seg, NULL, dtype, B, H, S, D, W, m, scale, row_begin, row_end, out, lse, nthreads);
+}
+
+/* CSA forward: as hca_oracle_fwd, compressed entries also need sel[b,i,j]. */
+int hca_oracle_csa_fwd(const void *q, const void *kv, const void *ckv, const int32_t *seg, const uint8_t *sel,
+                       int dtype, int B, int H, int S, int D, int W, int m, double scale,
+                       int row_begin, int row_end, double *out, double *lse, int nthreads) {
+  if (!sel) return -2;
+  return fwd_impl(q, kv, ckv, seg, sel, dtype, B, H, S, D, W, m, scale, row_begin, row_end, out, lse, nthreads);
 }
 
 /* ------------------------------------------------------------------ */
@@ -376,14 +406,15 @@ static void bwd_key_task(void *ctx, long item, double *scr) {
 /* dq[B,H,S,D] for query positions [row_begin,row_end) and dkv[B,S,D],
  * dckv[B,Sc,D] holding the contributions of exactly those queries (the
  * full gradient when the range is [0,S)). */
-int hca_oracle_bwd(const void *q, const void *kv, const void *ckv, const int32_t *seg, const void *dout, int dtype,
-                   int B, int H, int S, int D, int W, int m, double scale, int row_begin, int row_end,
-                   double *dq, double *dkv, double *dckv, int nthreads) {
+static int bwd_impl(const void *q, const void *kv, const void *ckv, const int32_t *seg, const uint8_t *sel,
+                    const void *dout, int dtype, int B, int H, int S, int D, int W, int m, double scale,
+                    int row_begin, int row_end, double *dq, double *dkv, double *dckv, int nthreads) {
   if (B < 0 || H < 1 || S < 0 || D < 1 || W < 1 || m < 1) return -2;
   if (!check_rows(S, &row_begin, &row_end)) return -2;
   prob_t P;
   memset(&P, 0, sizeof P);
   if (vis_init(&P.v, seg, B, S, W, m)) return -1;
+  P.v.sel = sel;
   P.q = q; P.kv = kv; P.ckv = ckv; P.dout = dout; P.dt = dtype; P.H = H; P.D = D; P.scale = scale;
   P.row_begin = row_begin; P.row_end = row_end; P.dq = dq; P.dkv = dkv; P.dckv = dckv;
   size_t nrow = (size_t)B * H * (S > 0 ? S : 1);
@@ -404,6 +435,22 @@ int hca_oracle_bwd(const void *q, const void *kv, const void *ckv, const int32_t
   free(P.delta_all);
   free(P.v.win_id);
   return rc;
+}
+
+int hca_oracle_bwd(const void *q, const void *kv, const void *ckv, const int32_t *seg, const void *dout, int dtype,
+                   int B, int H, int S, int D, int W, int m, double scale, int row_begin, int row_end,
+                   double *dq, double *dkv, double *dckv, int nthreads) {
+  return bwd_impl(q, kv, ckv, seg, NULL, dout, dtype, B, H, S, D, W, m, scale, row_begin, row_end, dq, dkv, dckv,
+                  nthreads);
+}
+
+/* CSA backward: as hca_oracle_bwd, compressed entries also need sel[b,i,j]. */
+int hca_oracle_csa_bwd(const void *q, const void *kv, const void *ckv, const int32_t *seg, const uint8_t *sel,
+                       const void *dout, int dtype, int B, int H, int S, int D, int W, int m, double scale,
+                       int row_begin, int row_end, double *dq, double *dkv, double *dckv, int nthreads) {
+  if (!sel) return -2;
+  return bwd_impl(q, kv, ckv, seg, sel, dout, dtype, B, H, S, D, W, m, scale, row_begin, row_end, dq, dkv, dckv,
+                  nthreads);
 }
 
 static void key_list_task(void *ctx, long item, double *scr) {
@@ -475,10 +522,12 @@ int hca_oracle_bwd_keys(const void *q, const void *kv, const void *ckv, const in
 /* Visible (query, key) pairs of every batch row, per head, counted element
  * by element: raw_pairs[b] over raw rows, comp_pairs[b] over compressed
  * entries. */
-int hca_oracle_visible_pairs(const int32_t *seg, int B, int S, int W, int m, int64_t *raw_pairs, int64_t *comp_pairs) {
+static int pairs_impl(const int32_t *seg, const uint8_t *sel, int B, int S, int W, int m, int64_t *raw_pairs,
+                      int64_t *comp_pairs) {
   if (B < 0 || S < 0 || W < 1 || m < 1) return -2;
   vis_t v;
   if (vis_init(&v, seg, B, S, W, m)) return -1;
+  v.sel = sel;
   for (int b = 0; b < B; ++b) {
     int64_t nr = 0, nc = 0;
     for (int i = 0; i < S; ++i) {
@@ -491,6 +540,17 @@ int hca_oracle_visible_pairs(const int32_t *seg, int B, int S, int W, int m, int
   }
   free(v.win_id);
   return 0;
+}
+
+int hca_oracle_visible_pairs(const int32_t *seg, int B, int S, int W, int m, int64_t *raw_pairs, int64_t *comp_pairs) {
+  return pairs_impl(seg, NULL, B, S, W, m, raw_pairs, comp_pairs);
+}
+
+/* CSA pair counts: compressed pairs also need sel[b,i,j]. */
+int hca_oracle_csa_visible_pairs(const int32_t *seg, const uint8_t *sel, int B, int S, int W, int m,
+                                 int64_t *raw_pairs, int64_t *comp_pairs) {
+  if (!sel) return -2;
+  return pairs_impl(seg, sel, B, S, W, m, raw_pairs, comp_pairs);
 }
 
 /* For query tiles of Pq consecutive positions, the smallest range of keys
