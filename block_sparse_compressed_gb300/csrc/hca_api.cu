@@ -2,6 +2,7 @@
 // validation, workspace carving and kernel dispatch.  Everything is enqueued
 // on the caller's stream; nothing here allocates or synchronises except
 // hca_workspace_status, whose job is to synchronise.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -63,7 +64,28 @@ int check_ws(void *ws, size_t have, size_t need) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? HCA_OK : HCA_ERR_CUDA; }
 
+// bf16 runs on the tensor-core kernels only; fp32 on the CUDA-core kernels
+bool supported(int H, int D, int dtype) { return dtype == HCA_F32 || tc_fwd_supported(H, D, dtype); }
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+std::atomic<long long> g_inject_launch_failures{0};
+std::atomic<int> g_inject_stall_mask{0};
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+
+bool take_counter(std::atomic<long long> &c) {
+  long long v = c.load();
+  while (v > 0)
+    if (c.compare_exchange_weak(v, v - 1)) return true;
+  return false;
+}
+
 }  // namespace
+
+namespace hca {
+bool take_launch_failure() { return take_counter(g_inject_launch_failures); }
+int take_stall_mask() { return g_inject_stall_mask.exchange(0); }
+uint64_t wait_limit_ns() { return g_wait_ns.load(); }
+}  // namespace hca
 
 extern "C" {
 
@@ -91,6 +113,24 @@ size_t hca_workspace_size(int B, int H, int S, int D, int W, int m, int dtype, i
   return for_backward ? bwd_ws_bytes(B, H, S, D, W, m, dtype) : fwd_ws_bytes(B, S);
 }
 
+int hca_test_inject(int what, long long value) {
+  if (value < 0) return HCA_ERR_ARG;
+  switch (what) {
+    case HCA_INJECT_RESET:
+      g_inject_launch_failures = 0;
+      g_inject_stall_mask = 0;
+      g_wait_ns = kDefaultWaitNs;
+      return HCA_OK;
+    case HCA_INJECT_LAUNCH_FAILURE: g_inject_launch_failures = value; return HCA_OK;
+    case HCA_INJECT_STALL:
+      if (value > (HCA_STALL_FWD | HCA_STALL_DQ | HCA_STALL_DKV)) return HCA_ERR_ARG;
+      g_inject_stall_mask = (int)value;
+      return HCA_OK;
+    case HCA_INJECT_WAIT_LIMIT_NS: g_wait_ns = value == 0 ? kDefaultWaitNs : (unsigned long long)value; return HCA_OK;
+    default: return HCA_ERR_ARG;
+  }
+}
+
 int hca_query_tile_positions(int H, int D, int dtype) {
   if (H < 1) return 0;
   if (tc_fwd_supported(H, D, dtype)) return tc_query_tile_positions(H);
@@ -103,6 +143,7 @@ int hca_attn_fwd(const void *q, const void *kv, const void *ckv, const int32_t *
   int rc = check_dims(B, H, S, D, W, m, dtype);
   if (rc != HCA_OK) return rc;
   if (!std::isfinite(scale)) return HCA_ERR_ARG;
+  if (!supported(H, D, dtype)) return HCA_ERR_UNSUPPORTED;
   if (B * (long long)S == 0) return HCA_OK;
   if (!q || !kv || !ckv || !out || !lse) return HCA_ERR_NULL;
   if (!aligned16(q) || !aligned16(kv) || !aligned16(ckv) || !aligned16(out) || !aligned16(lse) ||
@@ -110,6 +151,7 @@ int hca_attn_fwd(const void *q, const void *kv, const void *ckv, const int32_t *
     return HCA_ERR_ALIGN;
   rc = check_ws(workspace, workspace_bytes, fwd_ws_bytes(B, S));
   if (rc != HCA_OK) return rc;
+  if (take_launch_failure()) return HCA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Carve c = carve_fwd(workspace, B, S);
   rc = cuda_status(launch_prep(seg, B, S, c.sstart, c.status, st));
@@ -120,7 +162,12 @@ int hca_attn_fwd(const void *q, const void *kv, const void *ckv, const int32_t *
   a.status = c.status; a.status_rw = c.status;
   a.out = out; a.lse = lse;
   a.B = B; a.H = H; a.S = S; a.D = D; a.W = W; a.m = m; a.scale = scale; a.dtype = dtype;
-  if (tc_fwd_supported(H, D, dtype)) return cuda_status(tc_fwd(a, st));
+  a.wait_ns = wait_limit_ns();
+  a.stall = 0;
+  if (dtype == HCA_BF16) {
+    a.stall = take_stall_mask() & HCA_STALL_FWD;
+    return cuda_status(tc_fwd(a, st));
+  }
   return cuda_status(simt_fwd(a, st));
 }
 
@@ -130,6 +177,7 @@ int hca_attn_bwd(const void *q, const void *kv, const void *ckv, const int32_t *
   int rc = check_dims(B, H, S, D, W, m, dtype);
   if (rc != HCA_OK) return rc;
   if (!std::isfinite(scale)) return HCA_ERR_ARG;
+  if (!supported(H, D, dtype)) return HCA_ERR_UNSUPPORTED;
   if (B * (long long)S == 0) return HCA_OK;
   if (!q || !kv || !ckv || !out || !lse || !dout || !dq || !dkv || !dckv) return HCA_ERR_NULL;
   const void *ptrs[] = {q, kv, ckv, out, lse, dout, dq, dkv, dckv};
@@ -138,6 +186,7 @@ int hca_attn_bwd(const void *q, const void *kv, const void *ckv, const int32_t *
   if (seg && !aligned16(seg)) return HCA_ERR_ALIGN;
   rc = check_ws(workspace, workspace_bytes, bwd_ws_bytes(B, H, S, D, W, m, dtype));
   if (rc != HCA_OK) return rc;
+  if (take_launch_failure()) return HCA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Carve c = carve_fwd(workspace, B, S);
   rc = cuda_status(launch_prep(seg, B, S, c.sstart, c.status, st));
@@ -153,7 +202,12 @@ int hca_attn_bwd(const void *q, const void *kv, const void *ckv, const int32_t *
   a.scratch = p;
   a.scratch_bytes = tc_bwd_scratch_bytes(B, H, S, D, W, m, dtype);
   a.B = B; a.H = H; a.S = S; a.D = D; a.W = W; a.m = m; a.scale = scale; a.dtype = dtype;
-  if (tc_bwd_supported(H, D, dtype)) return cuda_status(tc_bwd(a, st));
+  a.wait_ns = wait_limit_ns();
+  a.stall = 0;
+  if (dtype == HCA_BF16) {
+    a.stall = take_stall_mask() & (HCA_STALL_DQ | HCA_STALL_DKV);
+    return cuda_status(tc_bwd(a, st));
+  }
   return cuda_status(simt_bwd(a, st));
 }
 

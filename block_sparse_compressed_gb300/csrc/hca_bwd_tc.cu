@@ -69,6 +69,8 @@ struct DqParams {
   float *rowstat;            // [ntiles][2][128]: -lse*log2e, then -scale*Delta, per tile row
   __nv_bfloat16 *dq;         // direct stores for poisoned calls / tiles without keys
   float sl2, scale;
+  uint64_t wait_ns;          // limit of every bounded wait
+  int stall;                 // failure-path test: the MMA warp first waits on a barrier nothing arrives at
 };
 
 struct DqBars {
@@ -77,7 +79,7 @@ struct DqBars {
   uint64_t s_full, s_free;   // S of a block in TMEM / read out by the dS warps
   uint64_t dp_full, ds_full; // dP in TMEM / dS stored (and dP read out)
   uint64_t dq_done;          // a tile's last dq MMA complete
-  uint64_t epi, drain;
+  uint64_t epi, drain, never;
   uint32_t tmem_base;
   int abort;
 };
@@ -116,6 +118,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
     mbar_init(&bars.dq_done, 1);
     mbar_init(&bars.epi, kEW);
     mbar_init(&bars.drain, 1);
+    mbar_init(&bars.never, 1);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -144,7 +147,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         const int nb = t.nb;
         if (nb == 0) continue;
         if (lane == 0) {
-          if (tw > 0) ok = mbar_wait(&bars.qd_empty, (tw - 1) & 1, abort_flag, p.status);
+          if (tw > 0) ok = mbar_wait(&bars.qd_empty, (tw - 1) & 1, abort_flag, p.status, p.wait_ns);
           if (ok) {
             mbar_arrive_expect_tx(&bars.qd_full, 3 * kTile);
             const int c2 = t.b * Q.H + t.g * Q.HG;
@@ -173,7 +176,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
           for (int j = 0; ok && j < nb; ++j, ++gb) {
             const int s = gb % kStages;
             if (gb >= (uint32_t)kStages)
-              ok = mbar_wait(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status);
+              ok = mbar_wait(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
             if (!ok) break;
             int n, nc;
             block_cols(t, j, n, nc);
@@ -210,6 +213,10 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       const uint32_t id_dq = idesc_bf16_f32(kRows, kHeadDim, false, true);
       uint32_t gb = 0, tw = 0;
       bool ok = !poisoned, issued = false;
+      if (ok && p.stall) {
+        injected_stall(&bars.never, abort_flag, p.status, p.wait_ns);
+        ok = false;
+      }
       for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
         Tile t;
         tile_coords(Q, u, t);
@@ -234,10 +241,10 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
           __syncwarp();
           issued = true;
         };
-        ok = wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status);
-        if (ok) ok = wait_warp(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status);
+        ok = wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status, p.wait_ns);
+        if (ok) ok = wait_warp(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status, p.wait_ns);
         // the previous tile's last S must have been read out
-        if (ok && gb > 0) ok = wait_warp(&bars.s_free, (gb - 1) & 1, abort_flag, p.status);
+        if (ok && gb > 0) ok = wait_warp(&bars.s_free, (gb - 1) & 1, abort_flag, p.status, p.wait_ns);
         if (ok) {
           tc_fence_after();
           issue_sdp(0, 0, gb, false);
@@ -247,13 +254,13 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
           const uint32_t g = gb + j;
           const bool next = j + 1 < nb;
           if (next) {
-            ok = wait_warp(&bars.s_free, g & 1, abort_flag, p.status);
-            if (ok) ok = wait_warp(&bars.kv_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag, p.status);
+            ok = wait_warp(&bars.s_free, g & 1, abort_flag, p.status, p.wait_ns);
+            if (ok) ok = wait_warp(&bars.kv_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag, p.status, p.wait_ns);
             if (!ok) break;
             tc_fence_after();
             issue_sdp(0, j + 1, g + 1, false);
           }
-          ok = wait_warp(&bars.ds_full, g & 1, abort_flag, p.status);
+          ok = wait_warp(&bars.ds_full, g & 1, abort_flag, p.status, p.wait_ns);
           if (!ok) break;
           tc_fence_after();
           int n, nc;
@@ -307,7 +314,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
     bool ok = true, store_pending = false;
     auto rendezvous = [&]() -> bool {
       mbar_arrive(&bars.epi);
-      const bool rr = wait_warp(&bars.epi, epi_phase & 1, abort_flag, p.status);
+      const bool rr = wait_warp(&bars.epi, epi_phase & 1, abort_flag, p.status, p.wait_ns);
       ++epi_phase;
       return rr;
     };
@@ -339,7 +346,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       // Delta = <dO, out> for this row, from the staged dO and out tiles
       // (both warpgroups form it; the first one publishes it)
       const float lse_row = iv.valid ? p.lse[lrow] : 0.f;
-      if (!wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
       float lse2 = 0.f, delta = 0.f;
       if (iv.valid) {
 #pragma unroll
@@ -369,7 +376,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         int a1, b1, a2, b2;
         row_cols(t, iv, j, n, nc, a1, b1, a2, b2);
         const uint64_t vis = range_mask64(a1, b1, cb) | range_mask64(a2, b2, cb);
-        if (!wait_warp(&bars.s_full, gb & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_warp(&bars.s_full, gb & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         // P = exp2(S * scale * log2e - lse * log2e), kept in registers so the
         // S columns can take the next block's scores right away
@@ -410,7 +417,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
             pv[c + 1] = ((vis >> (c + 1)) & 1ull) ? __float_as_uint(ex2_approx(t1)) : 0u;
           }
         }
-        if (!wait_warp(&bars.dp_full, gb & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_warp(&bars.dp_full, gb & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         const uint64_t ndl2 = f32x2(__float_as_uint(-delta), __float_as_uint(-delta));
 #pragma unroll
@@ -445,7 +452,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       }
       if (!ok) break;
       // ---------------- epilogue: dq = scale * acc
-      if (!wait_warp(&bars.dq_done, tw & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!wait_warp(&bars.dq_done, tw & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
       tc_fence_after();
       if (store_pending) {
         if (tid == 0) bulk_wait_read0();
@@ -546,6 +553,8 @@ struct DkvParams {
   int sub_pq, sub_hg;  // TMA box of a 64-row sub-tile: positions x heads
   long long n_both, n_lead, nitems;
   float sl2, scale;
+  uint64_t wait_ns;    // limit of every bounded wait
+  int stall;           // failure-path test: the MMA warp first waits on a barrier nothing arrives at
 };
 
 struct Item {
@@ -681,7 +690,7 @@ struct DkvBars {
   uint64_t st_full[dkk::kStages], st_empty[dkk::kStages];
   uint64_t s_full[2], p_full[2];  // per TMEM buffer
   uint64_t acc_full, acc_free;
-  uint64_t drain;
+  uint64_t drain, never;
   uint32_t tmem_base;
   int abort;
 };
@@ -716,6 +725,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
     mbar_init(&bars.acc_full, 1);
     mbar_init(&bars.acc_free, kEW);
     mbar_init(&bars.drain, 1);
+    mbar_init(&bars.never, 1);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -747,7 +757,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
         long long u = -1;
         if (lane == 0) {
           if (k >= (uint32_t)kItemRing)
-            ok = mbar_wait(&bars.item_empty[slot], ((k / kItemRing) - 1) & 1, abort_flag, p.status);
+            ok = mbar_wait(&bars.item_empty[slot], ((k / kItemRing) - 1) & 1, abort_flag, p.status, p.wait_ns);
           if (ok) {
             u = atomicAdd(p.next_item, 1);
             if (u >= p.nitems) u = -1;
@@ -764,7 +774,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
         const int nsub = 2 * (it.tq_hi - it.tq_lo) * per_tile;
         if (it.nkb == 0 || nsub <= 0) continue;
         if (lane == 0) {
-          if (iw > 0) ok = mbar_wait(&bars.k_empty, (iw - 1) & 1, abort_flag, p.status);
+          if (iw > 0) ok = mbar_wait(&bars.k_empty, (iw - 1) & 1, abort_flag, p.status, p.wait_ns);
           if (ok) {
             const CUtensorMap *mp = it.comp ? &map_ckv : &map_kv;
             mbar_arrive_expect_tx(&bars.k_full, it.nkb * kTile);
@@ -783,7 +793,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
           const int s = gsub % kStages;
           uint8_t *st = smem + kOffStage + s * kStageBytes;
           if (lane == 0 && gsub >= (uint32_t)kStages)
-            ok = mbar_wait(&bars.st_empty[s], ((gsub / kStages) - 1) & 1, abort_flag, p.status);
+            ok = mbar_wait(&bars.st_empty[s], ((gsub / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
           const int i0 = tq * Q.Pq;
@@ -839,11 +849,15 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
       const uint32_t id_acc = idesc_bf16_f32(kRows, kHeadDim, false, true);
       uint32_t gsub = 0, gu = 0, iw = 0;  // sub-tiles, units and items with work so far
       bool ok = true, issued = false;
+      if (p.stall && !poisoned) {
+        injected_stall(&bars.never, abort_flag, p.status, p.wait_ns);
+        ok = false;
+      }
       for (uint32_t kq = 0; ok; ++kq) {
         const int slot = kq % kItemRing;
         long long u = -1;
         if (lane == 0) {
-          ok = mbar_wait(&bars.item_full[slot], (kq / kItemRing) & 1, abort_flag, p.status);
+          ok = mbar_wait(&bars.item_full[slot], (kq / kItemRing) & 1, abort_flag, p.status, p.wait_ns);
           if (ok) {
             u = bars.item[slot];
             mbar_arrive(&bars.item_empty[slot]);
@@ -859,13 +873,13 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
         if (it.nkb == 0 || nsub <= 0) continue;
         const int nkb = it.nkb;
         const int nu = nsub * nkb;
-        ok = wait_warp(&bars.k_full, iw & 1, abort_flag, p.status);
+        ok = wait_warp(&bars.k_full, iw & 1, abort_flag, p.status, p.wait_ns);
         // S^T | dP^T of unit w into TMEM buffer (gu + w) & 1
         auto issue_sd = [&](int w) -> bool {
           const int v = nkb == 2 ? (w >> 1) : w, a = nkb == 2 ? (w & 1) : 0;
           const uint32_t sg = gsub + v;
           const int s = sg % kStages;
-          if (a == 0 && !wait_warp(&bars.st_full[s], (sg / kStages) & 1, abort_flag, p.status)) return false;
+          if (a == 0 && !wait_warp(&bars.st_full[s], (sg / kStages) & 1, abort_flag, p.status, p.wait_ns)) return false;
           tc_fence_after();
           const uint64_t br = dR0 + desc_bytes(s * kStageBytes);
           const uint64_t bk = dK0 + desc_bytes(a * kTile);
@@ -884,8 +898,8 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
         if (ok && nu > 1) ok = issue_sd(1);
         for (int w = 0; ok && w < nu; ++w) {
           const uint32_t g = gu + w;
-          ok = wait_warp(&bars.p_full[g & 1], (g >> 1) & 1, abort_flag, p.status);
-          if (ok && w == 0 && iw > 0) ok = wait_warp(&bars.acc_free, (iw - 1) & 1, abort_flag, p.status);
+          ok = wait_warp(&bars.p_full[g & 1], (g >> 1) & 1, abort_flag, p.status, p.wait_ns);
+          if (ok && w == 0 && iw > 0) ok = wait_warp(&bars.acc_free, (iw - 1) & 1, abort_flag, p.status, p.wait_ns);
           if (!ok) break;
           tc_fence_after();
           const int v = nkb == 2 ? (w >> 1) : w, a = nkb == 2 ? (w & 1) : 0;
@@ -937,7 +951,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
     bool ok = true;
     for (uint32_t kq = 0; ok; ++kq) {
       const int slot = kq % kItemRing;
-      if (!wait_warp(&bars.item_full[slot], (kq / kItemRing) & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!wait_warp(&bars.item_full[slot], (kq / kItemRing) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
       const long long u = *(volatile long long *)&bars.item[slot];
       mbar_arrive(&bars.item_empty[slot]);
       if (u < 0) break;
@@ -979,8 +993,8 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
         const uint32_t g = gu + w;
         const uint32_t sg = gsub + v;
         const uint8_t *st = smem + kOffStage + (sg % kStages) * kStageBytes;
-        if (!wait_warp(&bars.st_full[sg % kStages], (sg / kStages) & 1, abort_flag, p.status)) { ok = false; break; }
-        if (!wait_warp(&bars.s_full[g & 1], (g >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_warp(&bars.st_full[sg % kStages], (sg / kStages) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+        if (!wait_warp(&bars.s_full[g & 1], (g >> 1) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         const uint32_t base = lane_addr + col_buf(g);
         // query rows [32 h, 32 h + 32): S^T columns 32 h.., dP^T columns 64 + 32 h..
@@ -1037,7 +1051,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
       }
       if (!ok) break;
       // ---------------- item epilogue: this key's accumulator rows
-      if (!wait_warp(&bars.acc_full, iw & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!wait_warp(&bars.acc_full, iw & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
       tc_fence_after();
       for (int a = 0; a < nkb; ++a) {
         uint32_t o[64];
@@ -1190,14 +1204,11 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
       !make_map_bf16(&mkv16, a.kv, kHeadDim, a.S, a.B, 16, 1) ||
       !make_map_bf16(&mckv16, a.ckv, kHeadDim, q.Sc, a.B, 16, 1))
     return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(hca_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         dqk::kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(hca_bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dkk::kSmemBytes);
+  static SmemAttrOnce attr_dq, attr_dkv;
+  {
+    cudaError_t e = attr_dq.ensure(reinterpret_cast<const void *>(hca_bwd_dq_kernel), dqk::kSmemBytes);
+    if (e == cudaSuccess) e = attr_dkv.ensure(reinterpret_cast<const void *>(hca_bwd_dkv_kernel), dkk::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
@@ -1211,6 +1222,8 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   dp.dq = static_cast<__nv_bfloat16 *>(a.dq);
   dp.sl2 = sl2;
   dp.scale = a.scale;
+  dp.wait_ns = a.wait_ns;
+  dp.stall = (a.stall & HCA_STALL_DQ) != 0;
   const long long g1 = q.ntiles < sms ? q.ntiles : sms;
   if (g1 == 0) return cudaSuccess;
   cudaError_t e;
@@ -1243,6 +1256,8 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   kp.nitems = kp.n_both + kp.n_lead + (long long)a.B * rg.nrb * rg.npr;
   kp.sl2 = sl2;
   kp.scale = a.scale;
+  kp.wait_ns = a.wait_ns;
+  kp.stall = (a.stall & HCA_STALL_DKV) != 0;
   const long long g2 = kp.nitems < sms ? kp.nitems : sms;
   e = cudaMemsetAsync(kp.next_item, 0, sizeof(int32_t), st);
   if (e == cudaSuccess && rg.atomic) e = cudaMemsetAsync(rpart, 0, rpart_bytes(a.B, rg), st);

@@ -75,6 +75,8 @@ struct FwdParams {
   float *lse;
   __nv_bfloat16 *out;  // direct stores for poisoned calls / pairs without keys
   float sl2;           // scale * log2(e)
+  uint64_t wait_ns;    // limit of every bounded wait
+  int stall;           // failure-path test: the MMA warp first waits on a barrier nothing arrives at
 };
 
 // A pair of adjacent query tiles (A at i0, B at i0 + Pq) shares one key list:
@@ -105,7 +107,7 @@ struct Bars {
   uint64_t s_full[2], p_full[2];
   uint64_t o_final[2], o_free[2];
   uint64_t st_full[2], st_free[2];
-  uint64_t epi, drain;
+  uint64_t epi, drain, never;
   float inv_l[2][kRows];
   uint32_t tmem_base;
   int abort;
@@ -142,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars.epi, kWG);
     mbar_init(&bars.drain, 1);
+    mbar_init(&bars.never, 1);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nb = t.nb;
         if (nb == 0) continue;
         if (lane == 0) {
-          if (gq > 0) ok = mbar_wait(&bars.q_empty, (gq - 1) & 1, abort_flag, p.status);
+          if (gq > 0) ok = mbar_wait(&bars.q_empty, (gq - 1) & 1, abort_flag, p.status, p.wait_ns);
           if (ok) {
             const bool has_b = t.i0 + Q.Pq < Q.S;
             mbar_arrive_expect_tx(&bars.q_full, has_b ? 2 * kTile : kTile);
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; ok && j < nb; ++j, ++gb) {
             const int s = gb % kStages;
             if (gb >= (uint32_t)kStages)
-              ok = mbar_wait(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status);
+              ok = mbar_wait(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
             if (!ok) break;
             int n, nc;
             block_cols(t, j, n, nc);
@@ -242,6 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_pv = idesc_bf16_f32(kRows, kHeadDim, false, true);
       uint32_t gb = 0, gq = 0, pcnt = 0;
       bool ok = !poisoned, issued = false;
+      if (ok && p.stall) {
+        injected_stall(&bars.never, abort_flag, p.status, p.wait_ns);
+        ok = false;
+      }
       for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
         Tile t;
         pair_coords(p, u, t);
@@ -265,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           issued = true;
         };
-        ok = wait_warp(&bars.q_full, gq & 1, abort_flag, p.status);
-        if (ok) ok = wait_warp(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status);
+        ok = wait_warp(&bars.q_full, gq & 1, abort_flag, p.status, p.wait_ns);
+        if (ok) ok = wait_warp(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status, p.wait_ns);
         if (ok) {
           tc_fence_after();
           issue_s(0, 0, gb, nullptr);
@@ -280,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nks = (n + 15) >> 4;
           const uint64_t dbv = dv0 + desc_bytes((g % kStages) * kTile);
           for (int x = 0; ok && x < 2; ++x) {
-            ok = wait_warp(&bars.p_full[x], pcnt & 1, abort_flag, p.status);
-            if (ok && j == 0 && gq > 0) ok = wait_warp(&bars.o_free[x], (gq - 1) & 1, abort_flag, p.status);
+            ok = wait_warp(&bars.p_full[x], pcnt & 1, abort_flag, p.status, p.wait_ns);
+            if (ok && j == 0 && gq > 0) ok = wait_warp(&bars.o_free[x], (gq - 1) & 1, abort_flag, p.status, p.wait_ns);
             if (!ok) break;
             tc_fence_after();
             const uint32_t d = tmem + col_o(x), a = tmem + col_s(x);
@@ -302,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (next) {
               if (x == 0) {
-                ok = wait_warp(&bars.kv_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag, p.status);
+                ok = wait_warp(&bars.kv_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag, p.status, p.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
               }
@@ -332,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t pending = 0;  // bit x: a store from staging tile x may still be reading it
     auto rendezvous = [&]() -> bool {
       mbar_arrive(&bars.epi);
-      const bool rr = wait_warp(&bars.epi, epi_phase & 1, abort_flag, p.status);
+      const bool rr = wait_warp(&bars.epi, epi_phase & 1, abort_flag, p.status, p.wait_ns);
       ++epi_phase;
       return rr;
     };
@@ -345,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int x = 0; ok && x < 2; ++x) {
         const int i0 = t.i0 + x * Q.Pq;
         uint8_t *obuf = smem + kOffOut + x * kTile;
-        if (!wait_warp(&bars.o_final[x], gq & 1, abort_flag, p.status)) { ok = false; break; }
-        if (!wait_warp(&bars.st_full[x], gq & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_warp(&bars.o_final[x], gq & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+        if (!wait_warp(&bars.st_full[x], gq & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         const float inv = bars.inv_l[x][r];
         mbar_arrive(&bars.st_free[x]);
         tc_fence_after();
@@ -428,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int a1, b1, a2, b2;
         row_cols(t, iv, j, n, nc, a1, b1, a2, b2);
         // S_X(j) ready; since S_X(j) was issued after PV_X(j-1), O_X is stable
-        if (!wait_warp(&bars.s_full[x], scnt & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!wait_warp(&bars.s_full[x], scnt & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         ++scnt;
         tc_fence_after();
         // One TMEM round trip brings the row's nk scores into registers; the
@@ -540,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // row statistics: lse to global, 1/l to the epilogue
-      if (gq > 0 && !wait_warp(&bars.st_free[x], (gq - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      if (gq > 0 && !wait_warp(&bars.st_free[x], (gq - 1) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
       bars.inv_l[x][r] = l_run > 0.f ? 1.f / l_run : 0.f;
       mbar_arrive(&bars.st_full[x]);
       if (i < Q.S) {
@@ -588,14 +595,13 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st) {
   p.lse = a.lse;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.sl2 = a.scale * 1.4426950408889634f;
+  p.wait_ns = a.wait_ns;
+  p.stall = a.stall;
   const bool pos = p.sl2 > 0.f;
   auto kern = pos ? hca_fwd_tc_kernel<true> : hca_fwd_tc_kernel<false>;
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[pos]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set[pos] = true;
-  }
+  static SmemAttrOnce attr[2];
+  cudaError_t e = attr[pos].ensure(reinterpret_cast<const void *>(kern), kSmemBytes);
+  if (e != cudaSuccess) return e;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;
   const long long grid = p.npairs < sms ? p.npairs : sms;

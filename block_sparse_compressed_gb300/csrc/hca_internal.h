@@ -38,6 +38,8 @@ struct FwdArgs {
   int B, H, S, D, W, m;
   float scale;
   int dtype;
+  uint64_t wait_ns;  // limit of the kernels' bounded waits
+  int stall;         // failure-path test (hca_test_inject): HCA_STALL_* mask of kernels whose MMA warp stalls
 };
 
 struct BwdArgs {
@@ -53,7 +55,18 @@ struct BwdArgs {
   int B, H, S, D, W, m;
   float scale;
   int dtype;
+  uint64_t wait_ns;
+  int stall;
 };
+
+// Failure-path test hooks (hca_test_inject).  take_launch_failure() is true
+// when an injected launch failure is pending (and consumes it);
+// take_stall_mask() returns (and clears) the HCA_STALL_* mask of kernels
+// whose MMA warp stalls in the next call; wait_limit_ns() is the bounded wait
+// limit for the next launch (2 s unless a test shortened it).
+bool take_launch_failure();
+int take_stall_mask();
+uint64_t wait_limit_ns();
 
 cudaError_t launch_prep(const int32_t *seg, int B, int S, int32_t *sstart, int32_t *status, cudaStream_t st);
 cudaError_t launch_visible_pairs(const int32_t *sstart, int B, int S, int W, int m, int64_t *raw, int64_t *comp,

@@ -1,8 +1,7 @@
 // hca_simt.cu -- CUDA-core (SIMT) HCA forward and backward.
 //
 // These kernels carry the fp32 mode (fp32 inputs, fp32 arithmetic; a 1e-5
-// accuracy target rules out TF32 tensor cores) and bf16 head dims that the
-// tensor-core kernels do not instantiate.  One warp owns one (b, h, i) query
+// accuracy target rules out TF32 tensor cores).  One warp owns one (b, h, i) query
 // row for the forward and dq, or one key row for dkv / dckv; each lane holds
 // D/32 coordinates.  The key ranges come from the analytic intervals in
 // hca_common.cuh, so no mask is read or written.
@@ -291,12 +290,14 @@ static cudaError_t bwd_dispatch(const BwdArgs &a, cudaStream_t st) {
   return bwd_t<T, 8>(a, st);
 }
 
+// fp32 mode only: bf16 runs on the tensor-core kernels (hca_api.cu rejects
+// the bf16 shapes they do not take with HCA_ERR_UNSUPPORTED)
 cudaError_t simt_fwd(const FwdArgs &a, cudaStream_t st) {
-  return a.dtype == HCA_F32 ? fwd_dispatch<float>(a, st) : fwd_dispatch<__nv_bfloat16>(a, st);
+  return a.dtype == HCA_F32 ? fwd_dispatch<float>(a, st) : cudaErrorInvalidValue;
 }
 
 cudaError_t simt_bwd(const BwdArgs &a, cudaStream_t st) {
-  return a.dtype == HCA_F32 ? bwd_dispatch<float>(a, st) : bwd_dispatch<__nv_bfloat16>(a, st);
+  return a.dtype == HCA_F32 ? bwd_dispatch<float>(a, st) : cudaErrorInvalidValue;
 }
 
 }  // namespace hca

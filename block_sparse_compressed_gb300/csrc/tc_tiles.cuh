@@ -185,9 +185,18 @@ __host__ __device__ constexpr uint64_t desc_bytes(uint32_t bytes) { return (uint
 
 // Bounded wait whose outcome is the same for the whole warp, so that a warp
 // never splits around warp-collective tcgen05.ld / tcgen05.st.
-__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort, int32_t *status) {
-  const bool ok = mbar_wait(bar, parity, abort, status, kWaitLimitNs);
+__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort, int32_t *status,
+                                          uint64_t limit_ns) {
+  const bool ok = mbar_wait(bar, parity, abort, status, limit_ns);
   return __all_sync(0xffffffffu, ok);
+}
+
+// A wait on a barrier that nothing ever arrives at: it always runs out after
+// limit_ns and takes the same abort path as a real wait that gave up.  The
+// failure-path tests reach it through hca_test_inject (HCA_INJECT_STALL).
+__device__ __forceinline__ void injected_stall(uint64_t *never_bar, volatile int *abort, int32_t *status,
+                                               uint64_t limit_ns) {
+  (void)wait_warp(never_bar, 0, abort, status, limit_ns);
 }
 
 // ---------------------------------------------------------------------------
@@ -232,13 +241,39 @@ inline int sm_count() {
   return n;
 }
 
-inline int heads_per_tile(int H) { return H >= kRows ? kRows : H; }
-
-inline bool tc_shape_ok(int H, int D, int dtype) {
-  if (dtype != HCA_BF16 || D != kHeadDim || H < 1) return false;
-  if (H <= kRows) return (kRows % H) == 0;
-  return (H % kRows) == 0;
+// Heads packed into one 128-row tile: the largest power of two that divides
+// both H and 128, so any head count tiles exactly (H = 48: 16 heads x 8
+// positions per tile, three head groups).
+inline int heads_per_tile(int H) {
+  int hg = 1;
+  while (hg < kRows && H % (2 * hg) == 0) hg *= 2;
+  return hg;
 }
+
+inline bool tc_shape_ok(int H, int D, int dtype) { return dtype == HCA_BF16 && D == kHeadDim && H >= 1; }
+
+// Dynamic shared-memory limit of a kernel, raised once per device: the
+// attribute belongs to the (function, device) pair, so a process that drives
+// several GPUs needs it on each of them.  Guarded for concurrent first calls.
+class SmemAttrOnce {
+ public:
+  cudaError_t ensure(const void *kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu_);
+    if (done_[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done_[dev] = true;
+    return e;
+  }
+
+ private:
+  static constexpr int kMaxDev = 64;
+  std::mutex mu_;
+  bool done_[kMaxDev] = {};
+};
 
 inline QTiling make_qtiling(const int32_t *sstart, int B, int H, int S, int W, int m) {
   QTiling q;

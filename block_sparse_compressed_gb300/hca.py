@@ -9,6 +9,7 @@ and a missing library is an error.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -28,7 +29,10 @@ _lib = None
 EXPORTS = ("hca_status_string", "hca_version", "hca_workspace_size", "hca_query_tile_positions", "hca_attn_fwd",
            "hca_attn_bwd", "hca_visible_pairs", "hca_tile_map", "hca_workspace_status", "hca_profile_enable",
            "hca_profile_read", "hca_num_kernels", "hca_kernel_name", "hca_attn_fwd_noalloc",
-           "hca_local_workspace_size", "hca_local_attn_fwd", "hca_local_attn_bwd")
+           "hca_local_workspace_size", "hca_local_attn_fwd", "hca_local_attn_bwd", "hca_test_inject")
+
+# failure-path test hooks (hca_test_inject)
+INJECT_RESET, INJECT_LAUNCH_FAILURE, INJECT_STALL, INJECT_WAIT_LIMIT_NS = 0, 1, 2, 3
 
 
 class HCAError(RuntimeError):
@@ -81,6 +85,8 @@ def load(path: str = LIB_PATH):
             lib.hca_local_attn_fwd.restype = I
             lib.hca_local_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, P, Z, P]
             lib.hca_local_attn_bwd.restype = I
+            lib.hca_test_inject.argtypes = [I, ctypes.c_longlong]
+            lib.hca_test_inject.restype = I
             _lib = lib
     return _lib
 
@@ -105,6 +111,14 @@ def _ptr(t: Optional[torch.Tensor]):
 
 def _stream(device) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _on(device):
+    """Make `device` the current CUDA device for the C call: the library
+    resolves per-device state (kernel attributes, the built-in scratch of the
+    no-allocation entry point) on the current device."""
+    device = torch.device(device)
+    return torch.cuda.device(device) if device.type == "cuda" else contextlib.nullcontext()
 
 
 def _check(rc: int, where: str):
@@ -143,7 +157,13 @@ def workspace(B, H, S, D, W, m, dtype, for_backward, device) -> torch.Tensor:
 
 def hca_workspace_status(ws: torch.Tensor) -> int:
     """Synchronise the current stream and return the device-recorded status."""
-    return load().hca_workspace_status(_ptr(ws), _stream(ws.device))
+    with _on(ws.device):
+        return load().hca_workspace_status(_ptr(ws), _stream(ws.device))
+
+
+def hca_test_inject(what: int, value: int = 0) -> None:
+    """Failure-path test hook (include/hca.h, hca_test_inject)."""
+    _check(load().hca_test_inject(int(what), int(value)), "hca_test_inject")
 
 
 def _shapes(q, kv, ckv, seg, m):
@@ -177,8 +197,9 @@ def hca_attn_fwd(q: torch.Tensor, kv: torch.Tensor, ckv: torch.Tensor, seg: Opti
     _need(lse, "lse", (B, H, S), torch.float32, q.device)
     if ws is None:
         ws = workspace(B, H, S, D, W, m, q.dtype, False, q.device)
-    rc = lib.hca_attn_fwd(_ptr(q), _ptr(kv), _ptr(ckv), _ptr(seg), _ptr(out), _ptr(lse), B, H, S, D, W, m,
-                          float(scale), dt, _ptr(ws), ws.numel(), _stream(q.device))
+    with _on(q.device):
+        rc = lib.hca_attn_fwd(_ptr(q), _ptr(kv), _ptr(ckv), _ptr(seg), _ptr(out), _ptr(lse), B, H, S, D, W, m,
+                              float(scale), dt, _ptr(ws), ws.numel(), _stream(q.device))
     _check(rc, "hca_attn_fwd")
     if check:
         _check(hca_workspace_status(ws), "hca_attn_fwd (device)")
@@ -205,9 +226,10 @@ def hca_attn_bwd(q, kv, ckv, seg, out, lse, dout, W: int, m: int, scale: float, 
     _need(dckv, "dckv", ckv.shape, q.dtype, q.device)
     if ws is None:
         ws = workspace(B, H, S, D, W, m, q.dtype, True, q.device)
-    rc = lib.hca_attn_bwd(_ptr(q), _ptr(kv), _ptr(ckv), _ptr(seg), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
-                          _ptr(dkv), _ptr(dckv), B, H, S, D, W, m, float(scale), dt, _ptr(ws), ws.numel(),
-                          _stream(q.device))
+    with _on(q.device):
+        rc = lib.hca_attn_bwd(_ptr(q), _ptr(kv), _ptr(ckv), _ptr(seg), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                              _ptr(dkv), _ptr(dckv), B, H, S, D, W, m, float(scale), dt, _ptr(ws), ws.numel(),
+                              _stream(q.device))
     _check(rc, "hca_attn_bwd")
     if check:
         _check(hca_workspace_status(ws), "hca_attn_bwd (device)")
@@ -246,8 +268,9 @@ def hca_local_attn_fwd(q, kv, seg, W: int, scale: float, out=None, lse=None, ws=
     _need(lse, "lse", (B, H, S), torch.float32, q.device)
     if ws is None:
         ws = local_workspace(B, H, S, D, W, q.dtype, False, q.device)
-    rc = lib.hca_local_attn_fwd(_ptr(q), _ptr(kv), _ptr(seg), _ptr(out), _ptr(lse), B, H, S, D, W, float(scale), dt,
-                                _ptr(ws), ws.numel(), _stream(q.device))
+    with _on(q.device):
+        rc = lib.hca_local_attn_fwd(_ptr(q), _ptr(kv), _ptr(seg), _ptr(out), _ptr(lse), B, H, S, D, W, float(scale), dt,
+                                    _ptr(ws), ws.numel(), _stream(q.device))
     _check(rc, "hca_local_attn_fwd")
     if check:
         _check(hca_workspace_status(ws), "hca_local_attn_fwd (device)")
@@ -269,8 +292,9 @@ def hca_local_attn_bwd(q, kv, seg, out, lse, dout, W: int, scale: float, dq=None
     _need(dkv, "dkv", kv.shape, q.dtype, q.device)
     if ws is None:
         ws = local_workspace(B, H, S, D, W, q.dtype, True, q.device)
-    rc = lib.hca_local_attn_bwd(_ptr(q), _ptr(kv), _ptr(seg), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dkv),
-                                B, H, S, D, W, float(scale), dt, _ptr(ws), ws.numel(), _stream(q.device))
+    with _on(q.device):
+        rc = lib.hca_local_attn_bwd(_ptr(q), _ptr(kv), _ptr(seg), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dkv),
+                                    B, H, S, D, W, float(scale), dt, _ptr(ws), ws.numel(), _stream(q.device))
     _check(rc, "hca_local_attn_bwd")
     if check:
         _check(hca_workspace_status(ws), "hca_local_attn_bwd (device)")
@@ -284,7 +308,8 @@ def hca_visible_pairs(seg: Optional[torch.Tensor], B: int, S: int, W: int, m: in
     raw = torch.empty(B, dtype=torch.int64, device=device)
     comp = torch.empty(B, dtype=torch.int64, device=device)
     ws = workspace(B, 1, S, 16, W, m, torch.float32, False, device)
-    rc = lib.hca_visible_pairs(_ptr(seg), B, S, W, m, _ptr(raw), _ptr(comp), _ptr(ws), ws.numel(), _stream(device))
+    with _on(device):
+        rc = lib.hca_visible_pairs(_ptr(seg), B, S, W, m, _ptr(raw), _ptr(comp), _ptr(ws), ws.numel(), _stream(device))
     _check(rc, "hca_visible_pairs")
     return raw, comp
 
@@ -296,7 +321,8 @@ def hca_tile_map(seg: Optional[torch.Tensor], B: int, S: int, W: int, m: int, Pq
     nt = -(-S // Pq)
     out = torch.empty(B, nt, 4, dtype=torch.int32, device=device)
     ws = workspace(B, 1, S, 16, W, m, torch.float32, False, device)
-    rc = lib.hca_tile_map(_ptr(seg), B, S, W, m, Pq, _ptr(out), _ptr(ws), ws.numel(), _stream(device))
+    with _on(device):
+        rc = lib.hca_tile_map(_ptr(seg), B, S, W, m, Pq, _ptr(out), _ptr(ws), ws.numel(), _stream(device))
     _check(rc, "hca_tile_map")
     return out
 
@@ -327,12 +353,14 @@ def hca_attn_fwd_noalloc(q, kv, ckv, seg, W: int, m: int, scale: float, out=None
     if m < 1:
         raise ValueError("m must be >= 1")
     B, H, S, D, Sc = _shapes(q, kv, ckv, seg, m)
+    _need(q, "q", q.shape, q.dtype, q.device)
     dt = _dtype_code(q)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty(B, H, S, dtype=torch.float32, device=q.device) if lse is None else lse
     _need(out, "out", q.shape, q.dtype, q.device)
     _need(lse, "lse", (B, H, S), torch.float32, q.device)
-    rc = lib.hca_attn_fwd_noalloc(_ptr(q), _ptr(kv), _ptr(ckv), _ptr(seg), _ptr(out), _ptr(lse), B, H, S, D, W, m,
-                                  float(scale), dt, _stream(q.device))
+    with _on(q.device):
+        rc = lib.hca_attn_fwd_noalloc(_ptr(q), _ptr(kv), _ptr(ckv), _ptr(seg), _ptr(out), _ptr(lse), B, H, S, D, W, m,
+                                      float(scale), dt, _stream(q.device))
     _check(rc, "hca_attn_fwd_noalloc")
     return out, lse

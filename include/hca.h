@@ -70,7 +70,8 @@ typedef enum {
   HCA_ERR_ARG = 5,         /* W < 1, m < 1, scale not finite, bad tile size    */
   HCA_ERR_SEG = 6,         /* segment ids out of order (device-side check)     */
   HCA_ERR_WORKSPACE = 7,   /* workspace NULL, misaligned or too small          */
-  HCA_ERR_UNSUPPORTED = 8, /* no kernel for this dtype / D combination         */
+  HCA_ERR_UNSUPPORTED = 8, /* no kernel for this dtype / D combination (bf16
+                              runs on tensor cores only, for D = 128)        */
   HCA_ERR_CUDA = 9,        /* a CUDA runtime call or launch failed             */
   HCA_ERR_TIMEOUT = 10     /* a bounded on-device wait gave up                 */
 } hca_status;
@@ -89,8 +90,9 @@ HCA_API int hca_version(void);
 HCA_API size_t hca_workspace_size(int B, int H, int S, int D, int W, int m, int dtype, int for_backward);
 
 /* Number of consecutive query positions the forward kernel packs into one
- * tile for H heads (all H heads of a position share the tile), i.e. the Pq
- * argument that makes hca_tile_map describe the forward's own tiles. */
+ * 128-row tile for H heads (the tile holds Pq positions of 128 / Pq heads,
+ * the largest power of two dividing both H and 128), i.e. the Pq argument
+ * that makes hca_tile_map describe the forward's own tiles; 1 for fp32. */
 HCA_API int hca_query_tile_positions(int H, int D, int dtype);
 
 /* Forward.  out[B,H,S,D] = softmax-weighted sum of the visible keys;
@@ -165,11 +167,46 @@ HCA_API int hca_local_attn_bwd(const void *q, const void *kv, const int32_t *seg
  * it before any stream capture).  All calls share the array: calls that
  * overlap on the GPU race and must be serialised by the caller.  A segment
  * ordering error poisons that call's outputs with NaN (there is no workspace
- * to read a status from).  Nothing is allocated or freed. */
+ * to read a status from).  A bounded on-device wait that gives up (see
+ * HCA_ERR_TIMEOUT) leaves that call's outputs undefined, and this entry point
+ * cannot report it: callers that need to detect it use hca_attn_fwd with a
+ * workspace.  Nothing is allocated or freed. */
 #define HCA_NOALLOC_MAX_POSITIONS (1 << 20)
 HCA_API int hca_attn_fwd_noalloc(const void *q, const void *kv, const void *ckv, const int32_t *seg,
                                  void *out, float *lse,
                                  int B, int H, int S, int D, int W, int m, float scale, int dtype, void *stream);
+
+/* Failure-path test hooks.  "Add HCA Static Compilation for Splash Attention
+ * [Deepseek v4]" (Description, validation-guard bullet) wants unsupported or
+ * failing cases reported as errors rather than crashes; the tests that check
+ * this need failures on demand, and these hooks make them without faulting
+ * the GPU.  `what` is one of
+ *   HCA_INJECT_RESET          clear every injection below (value ignored);
+ *   HCA_INJECT_LAUNCH_FAILURE the next `value` attention calls return
+ *                             HCA_ERR_CUDA after checking their arguments and
+ *                             before enqueuing anything;
+ *   HCA_INJECT_STALL          in the next bf16 attention call, the kernels
+ *                             named by the mask `value` (HCA_STALL_FWD,
+ *                             HCA_STALL_DQ, HCA_STALL_DKV) start with their
+ *                             MMA warp waiting on a barrier that nothing
+ *                             arrives at: the wait gives up after the wait
+ *                             limit, every CTA drains its own copies and
+ *                             MMAs, frees its tensor memory and exits, later
+ *                             kernels of the call see the error and poison
+ *                             their outputs, and the call's workspace status
+ *                             reads HCA_ERR_TIMEOUT;
+ *   HCA_INJECT_WAIT_LIMIT_NS  limit of every bounded on-device wait, in ns,
+ *                             for later launches (0 restores the default 2 s).
+ * The settings are process-wide.  Returns HCA_OK, or HCA_ERR_ARG for an
+ * unknown `what` or a negative value. */
+#define HCA_INJECT_RESET 0
+#define HCA_INJECT_LAUNCH_FAILURE 1
+#define HCA_INJECT_STALL 2
+#define HCA_INJECT_WAIT_LIMIT_NS 3
+#define HCA_STALL_FWD 1
+#define HCA_STALL_DQ 2
+#define HCA_STALL_DKV 4
+HCA_API int hca_test_inject(int what, long long value);
 
 /* Optional per-kernel timing.  hca_profile_enable(1) resets the counters and
  * makes every later kernel launch of the library record a pair of CUDA events

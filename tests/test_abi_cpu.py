@@ -88,6 +88,11 @@ def test_argument_errors_are_caught_on_the_host(lib):
     assert _fwd(lib, wsb=16) == E_WS               # too small
     assert _fwd(lib, B=0) == OK                     # empty problem: nothing to do
     assert _fwd(lib, S=0) == OK
+    # bf16 runs on the tensor-core kernels only (D = 128): other head dims
+    # are rejected before anything is enqueued, never sent to CUDA cores
+    assert _fwd(lib, D=64) == E_UNSUP
+    assert _fwd(lib, D=256) == E_UNSUP
+    assert _fwd(lib, D=64, dt=1) != E_UNSUP         # fp32 runs every D
 
 
 def test_backward_argument_errors(lib):
@@ -109,6 +114,23 @@ def test_backward_argument_errors(lib):
     assert call(wsb=64) == E_WS
     p = list(args); p[3] = None            # seg = NULL is allowed: one segment
     assert call(ptrs=p, wsb=64) == E_WS
+
+
+def test_test_hooks_argument_checks(lib):
+    # the failure-path hooks validate their arguments on the host
+    assert lib.hca_test_inject(0, 0) == OK
+    assert lib.hca_test_inject(1, -1) == E_ARG
+    assert lib.hca_test_inject(2, 8) == E_ARG       # not a mask of the three kernels
+    assert lib.hca_test_inject(99, 0) == E_ARG
+    assert lib.hca_test_inject(3, 1000) == OK
+    assert lib.hca_test_inject(0, 0) == OK
+
+
+def test_head_packing_covers_every_head_count(lib):
+    # Pq = 128 / (largest power of two dividing H and 128)
+    for H, pq in ((1, 128), (3, 128), (6, 64), (48, 8), (64, 2), (96, 4), (128, 1), (256, 1), (384, 1)):
+        assert lib.hca_query_tile_positions(H, 128, 0) == pq, H
+    assert lib.hca_query_tile_positions(64, 64, 1) == 1   # fp32: one row per warp
 
 
 def test_local_attention_host_checks(lib):

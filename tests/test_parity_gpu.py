@@ -81,10 +81,27 @@ def test_heads_bf16(H):
     run_case(1, H, 260, 128, 64, 32, torch.bfloat16)
 
 
-@pytest.mark.parametrize("H,D", [(3, 128), (4, 64), (6, 32)])
-def test_cuda_core_bf16_shapes(H, D):
-    # head counts / dims the tensor-core tiles do not take run on CUDA cores
-    run_case(1, H, 200, D, 48, 16, torch.bfloat16)
+@pytest.mark.parametrize("H", [3, 6, 48, 96, 24])
+def test_any_head_count_on_tensor_cores(H):
+    # a tile packs the largest power of two dividing H and 128 (H = 3: one
+    # head x 128 positions; 48: 16 heads x 8 positions; 96: 32 x 4)
+    assert hca.hca_query_tile_positions(H, 128, torch.bfloat16) == 128 // math.gcd(H, 128)
+    run_case(1, H, 300, 128, 48, 16, torch.bfloat16)
+
+
+@pytest.mark.parametrize("D", [64, 32, 256])
+def test_bf16_head_dims_without_a_tensor_core_tile_are_rejected(D):
+    # bf16 runs on the tensor-core kernels only: other head dims are an
+    # error, never a silent CUDA-core fallback
+    q, kv, ckv, _, dout = (x.to(DEV) for x in I.small(1, 4, 64, D, 16, 8, dtype=torch.bfloat16))
+    with pytest.raises(hca.HCAError) as e:
+        hca.hca_attn_fwd(q, kv, ckv, None, 16, 8, 0.1)
+    assert e.value.status == 8
+    out = torch.zeros_like(q)
+    lse = torch.zeros(q.shape[:3], dtype=torch.float32, device=DEV)
+    with pytest.raises(hca.HCAError) as e:
+        hca.hca_attn_bwd(q, kv, ckv, None, out, lse, dout, 16, 8, 0.1)
+    assert e.value.status == 8
 
 
 @pytest.mark.parametrize("B", [1, 3])

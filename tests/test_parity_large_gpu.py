@@ -210,3 +210,34 @@ def test_bwd_dckv_entries_exact_16384():
         _, ref = oracle.bwd_keys(qc[b:b + 1], kvc[b:b + 1], ckvc[b:b + 1], segc[b:b + 1], dc[b:b + 1], w.W, w.m,
                                  w.scale, comp_ids=ids)
         assert_close(f"dckv b{b} entries {ids}", dckv_c[b][ids], ref, w.dtype)
+
+
+def check_dckv_high_fan_in(w, seed=1234):
+    """dckv entries that collect gradient from the most queries, each exact
+    over every query that sees it: entry 0 (all queries from m - 1 on), entry
+    1, the middle entry and the last visible one.  At this size those entries
+    are summed through the split partial slots and the fixed-order reduce."""
+    q, kv, ckv, seg, dout = I.tensors(w, device=DEV, seed=seed)
+    assert seg is None or bool((seg >= 0).all())
+    out, lse = hca.hca_attn_fwd(q, kv, ckv, seg, w.W, w.m, w.scale, check=True)
+    _, _, dckv = hca.hca_attn_bwd(q, kv, ckv, seg, out, lse, dout, w.W, w.m, w.scale, check=True)
+    torch.cuda.synchronize()
+    Sc = w.Sc
+    last = w.S // w.m - 1                       # last window that completes
+    ids = sorted({0, 1, Sc // 2, last})
+    _, ref = oracle.bwd_keys(q.cpu(), kv.cpu(), ckv.cpu(), None if seg is None else seg.cpu(), dout.cpu(), w.W,
+                             w.m, w.scale, comp_ids=ids)
+    got = to_np(dckv)[0][ids]
+    err = assert_close(f"dckv entries {ids}", got, ref, w.dtype)
+    tol = 1e-2 * float(np.max(np.abs(ref))) + 1e-3
+    per_entry = [float(np.max(np.abs(got[k] - ref[k]))) for k in range(len(ids))]
+    print(f"{w.name}: dckv entries {ids} max|err| {err:.3e} of bound {tol:.3e} ({100 * err / tol:.1f} %); "
+          f"per entry {[f'{e:.2e}' for e in per_entry]}")
+
+
+def test_bwd_dckv_high_fan_in_65536():
+    check_dckv_high_fan_in(I.LONG_S65536)
+
+
+def test_bwd_dckv_high_fan_in_131072():
+    check_dckv_high_fan_in(I.LONG_S131072)

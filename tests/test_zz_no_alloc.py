@@ -10,13 +10,11 @@ contents, so the second call checks that nothing stale leaks through).
 import ctypes
 import math
 
-import numpy as np
 import pytest
 import torch
 
 from block_sparse_compressed_gb300 import hca
 from block_sparse_compressed_gb300 import inputs as I
-from _util import assert_close, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -48,12 +46,10 @@ def _compare(q, kv, ckv, seg, W, m):
     ref_out, ref_lse = hca.hca_attn_fwd(q, kv, ckv, seg, W, m, scale, check=True)
     out, lse = _noalloc_c_abi(q, kv, ckv, seg, W, m, scale)
     torch.cuda.synchronize()
-    B, H, S, _ = q.shape
-    valid = np.ones((B, H, S), bool) if seg is None else np.broadcast_to(to_np(seg)[:, None, :] >= 0, (B, H, S))
-    assert_close("out", out, to_np(ref_out), torch.bfloat16)
-    assert_close("lse", lse[torch.from_numpy(np.ascontiguousarray(valid)).to(DEV)],
-                 to_np(ref_lse)[valid], torch.bfloat16)
-    assert torch.equal(torch.isinf(lse), torch.isinf(ref_lse))
+    # the same kernels on the same inputs: any difference at all would be
+    # stale state leaking out of the shared scratch array
+    assert torch.equal(out, ref_out)
+    assert torch.equal(lse, ref_lse)
 
 
 def test_noalloc_matches_workspace_entry_point_twice():
@@ -72,8 +68,8 @@ def test_noalloc_without_segments_and_fp32():
     q32, kv32, ckv32 = q32.to(DEV), kv32.to(DEV), ckv32.to(DEV)
     ref_out, ref_lse = hca.hca_attn_fwd(q32, kv32, ckv32, None, 30, 8, 0.125)
     out, lse = hca.hca_attn_fwd_noalloc(q32, kv32, ckv32, None, 30, 8, 0.125)
-    assert_close("out f32", out, to_np(ref_out), torch.float32)
-    assert_close("lse f32", lse, to_np(ref_lse), torch.float32)
+    assert torch.equal(out, ref_out)
+    assert torch.equal(lse, ref_lse)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
