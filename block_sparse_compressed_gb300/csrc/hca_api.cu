@@ -131,6 +131,82 @@ int hca_test_inject(int what, long long value) {
   }
 }
 
+size_t hca_compress_workspace_size(int B, int S, int m) {
+  if (B < 0 || S < 0 || m < 1 || S > (1 << 30)) return 0;
+  const size_t n = compress_workspace_bytes(B, S, m);
+  return n ? n : kAlign;
+}
+
+static int compress_checks(const void *x, const float *g, const float *bias, const int32_t *seg, const void *out,
+                           int B, int S, int D, int m, int dtype) {
+  if (dtype != HCA_BF16 && dtype != HCA_F32) return HCA_ERR_DTYPE;
+  if (B < 0 || S < 0 || D < 1 || S > (1 << 30) || (double)B * S * D > 9.0e18) return HCA_ERR_SHAPE;
+  if (m < 1) return HCA_ERR_ARG;
+  if (D % 32 != 0 || D > 256) return HCA_ERR_UNSUPPORTED;
+  if (B * (long long)S == 0) return HCA_OK;
+  if (!x || !g || !bias || !out) return HCA_ERR_NULL;
+  if (!aligned16(x) || !aligned16(out) || (seg && !aligned16(seg))) return HCA_ERR_ALIGN;
+  return HCA_OK;
+}
+
+int hca_compress_fwd(const void *x, const float *g, const float *bias, const int32_t *seg, void *ckv, int B, int S,
+                     int D, int m, int dtype, void *stream) {
+  int rc = compress_checks(x, g, bias, seg, ckv, B, S, D, m, dtype);
+  if (rc != HCA_OK || B * (long long)S == 0) return rc;
+  if (take_launch_failure()) return HCA_ERR_CUDA;
+  return cuda_status(compress_fwd(x, g, bias, seg, ckv, B, S, D, m, dtype, static_cast<cudaStream_t>(stream)));
+}
+
+int hca_compress_bwd(const void *x, const float *g, const float *bias, const int32_t *seg, const void *dckv, void *dx,
+                     float *dg, float *dbias, int B, int S, int D, int m, int dtype, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+  int rc = compress_checks(x, g, bias, seg, dckv, B, S, D, m, dtype);
+  if (rc != HCA_OK) return rc;
+  if (!dbias) return HCA_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (B * (long long)S == 0) return cuda_status(cudaMemsetAsync(dbias, 0, sizeof(float) * m, st));
+  if (!dx || !dg) return HCA_ERR_NULL;
+  if (!aligned16(dx)) return HCA_ERR_ALIGN;
+  rc = check_ws(workspace, workspace_bytes, compress_workspace_bytes(B, S, m));
+  if (rc != HCA_OK) return rc;
+  if (take_launch_failure()) return HCA_ERR_CUDA;
+  return cuda_status(compress_bwd(x, g, bias, seg, dckv, dx, dg, dbias, static_cast<float *>(workspace), B, S, D, m,
+                                  dtype, st));
+}
+
+size_t hca_indexer_workspace_size(int B, int S, int m) {
+  if (B < 0 || S < 0 || m < 1 || S > (1 << 30)) return 0;
+  return indexer_workspace_bytes(B, S, m);
+}
+
+int hca_indexer_topk(const void *qi, const void *ki, const float *w, const int32_t *seg, int32_t *sel, float *scores,
+                     int B, int S, int Hi, int Di, int m, int k, void *workspace, size_t workspace_bytes,
+                     void *stream) {
+  if (B < 0 || S < 0 || Hi < 1 || S > (1 << 30) || (double)B * S * Hi * Di > 9.0e18) return HCA_ERR_SHAPE;
+  if (m < 1 || k < 1) return HCA_ERR_ARG;
+  if (Di != 128) return HCA_ERR_UNSUPPORTED;
+  const long long Sc = ((long long)S + m - 1) / m;
+  if (Sc > 57344) return HCA_ERR_UNSUPPORTED;
+  if (B * (long long)S == 0) return HCA_OK;
+  if (!qi || !ki || !w || !sel) return HCA_ERR_NULL;
+  if (!aligned16(qi) || !aligned16(ki) || (seg && !aligned16(seg))) return HCA_ERR_ALIGN;
+  int rc = check_ws(workspace, workspace_bytes, indexer_workspace_bytes(B, S, m));
+  if (rc != HCA_OK) return rc;
+  if (take_launch_failure()) return HCA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carve c = carve_fwd(workspace, B, S);
+  rc = cuda_status(launch_prep(seg, B, S, c.sstart, c.status, st));
+  if (rc != HCA_OK) return rc;
+  char *p = c.p + fwd_ws_bytes(B, S);
+  IndexerArgs a;
+  a.qi = qi; a.ki = ki; a.w = w; a.sstart = seg ? c.sstart : nullptr; a.sel = sel; a.scores = scores;
+  a.qc = p;
+  a.buf = reinterpret_cast<float *>(p + align_up((size_t)B * S * 128 * 2));
+  a.status = c.status; a.wait_ns = wait_limit_ns();
+  a.B = B; a.S = S; a.Hi = Hi; a.m = m; a.k = k;
+  return cuda_status(indexer_topk(a, st));
+}
+
 int hca_query_tile_positions(int H, int D, int dtype) {
   if (H < 1) return 0;
   if (tc_fwd_supported(H, D, dtype)) return tc_query_tile_positions(H);

@@ -49,7 +49,8 @@ namespace dqk {
 constexpr int kStages = 3;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;  // dS: 64 cols of packed bf16
 constexpr int kTmemCols = 512;
-// two dS warpgroups (each owns 64 of a row's 128 key columns), TMA warp, MMA warp
+// two dS warpgroups (each owns 64 of a row's 128 key columns); warpgroup 2:
+// TMA warp (also the tile descriptors), MMA warp, two Delta warps
 constexpr int kEW = 256;
 constexpr int kThreads = kEW + 128;
 // 12 warps put 3 on each SM sub-partition (16K registers each): 168 per
@@ -60,6 +61,9 @@ static_assert(2 * 128 * kRegEW + 128 * kRegProducer <= kThreads * 168, "register
 constexpr int kOffQ = 0, kOffDO = kTile, kOffO = 2 * kTile, kOffKV = 3 * kTile;
 constexpr int kOffOut = kOffKV + kStages * kTile;
 constexpr int kSmemBytes = kOffOut + kTile + 1024;
+constexpr int kDescSlots = 8;
+constexpr int kDescReaders = 11;  // dS warps 0-7, MMA warp 9, Delta warps 10-11
+constexpr int kDeltaThreads = 64;
 }  // namespace dqk
 
 struct DqParams {
@@ -69,8 +73,15 @@ struct DqParams {
   float *rowstat;            // [ntiles][2][128]: -lse*log2e, then -scale*Delta, per tile row
   __nv_bfloat16 *dq;         // direct stores for poisoned calls / tiles without keys
   float sl2, scale;
+  int pq_shift;              // log2(Pq)
   uint64_t wait_ns;          // limit of every bounded wait
   int stall;                 // failure-path test: the MMA warp first waits on a barrier nothing arrives at
+};
+
+// One query tile of the CTA's schedule as every role needs it (u < 0 ends it).
+struct DqDesc {
+  long long u;
+  int b, g, i0, rlo, rhi, clo, chi, cpad, ncols, nb;
 };
 
 struct DqBars {
@@ -79,13 +90,33 @@ struct DqBars {
   uint64_t s_full, s_free;   // S of a block in TMEM / read out by the dS warps
   uint64_t dp_full, ds_full; // dP in TMEM / dS stored (and dP read out)
   uint64_t dq_done;          // a tile's last dq MMA complete
+  uint64_t stat_full, stat_empty;  // a tile's Delta in shared memory / read by the dS warps
+  uint64_t desc_full[dqk::kDescSlots], desc_empty[dqk::kDescSlots];
   uint64_t epi, drain, never;
+  DqDesc desc[dqk::kDescSlots];
+  float delta[kRows];
   uint32_t tmem_base;
   int abort;
 };
 
 __device__ __forceinline__ long long tile_linear(const QTiling &q, const Tile &t) {
   return ((long long)t.b * q.groups + t.g) * q.ntq + t.i0 / q.Pq;
+}
+
+// Reads tile descriptor kd (bounded wait) and releases its slot; false when
+// the wait gave up.
+__device__ __forceinline__ bool read_dq_desc(DqBars &bars, uint32_t kd, Tile &t, long long &u, volatile int *abort,
+                                             int32_t *status, uint64_t wait_ns) {
+  const int slot = kd % dqk::kDescSlots;
+  if (!wait_warp(&bars.desc_full[slot], (kd / dqk::kDescSlots) & 1, abort, status, wait_ns)) return false;
+  const volatile DqDesc &d = bars.desc[slot];
+  u = d.u;
+  t.b = d.b; t.g = d.g; t.i0 = d.i0;
+  t.rlo = d.rlo; t.rhi = d.rhi; t.clo = d.clo; t.chi = d.chi;
+  t.cpad = d.cpad; t.ncols = d.ncols; t.nb = d.nb;
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&bars.desc_empty[slot]);
+  return true;
 }
 
 __global__ void __launch_bounds__(dqk::kThreads, 1)
@@ -104,9 +135,9 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&bars.qd_full, 1);
-    // released by the last S/dP MMA of a tile and by every softmax thread
-    // once it has read the staged dO tile (Delta)
-    mbar_init(&bars.qd_empty, 1 + kEW);
+    // released by the last S/dP MMA of a tile and by every Delta thread once
+    // it has read the staged dO and out tiles
+    mbar_init(&bars.qd_empty, 1 + kDeltaThreads);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars.kv_full[s], 1);
       mbar_init(&bars.kv_empty[s], 1);
@@ -116,6 +147,12 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.ds_full, kEW);
     mbar_init(&bars.dq_done, 1);
+    mbar_init(&bars.stat_full, kDeltaThreads);
+    mbar_init(&bars.stat_empty, kEW);
+    for (int s = 0; s < kDescSlots; ++s) {
+      mbar_init(&bars.desc_full[s], 32);
+      mbar_init(&bars.desc_empty[s], kDescReaders);
+    }
     mbar_init(&bars.epi, kEW);
     mbar_init(&bars.drain, 1);
     mbar_init(&bars.never, 1);
@@ -135,17 +172,42 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
   if (warp >= kEW / 32) {
     setmaxnreg_dec<kRegProducer>();
     if (warp == kEW / 32) {
-      // ------------------------------------------------------------ TMA
+      // ------------------------------------------------------------ TMA + tile descriptors
+      // Every tile of the CTA's schedule (then an end marker) is published
+      // to the other roles through a shared-memory ring, so its key ranges
+      // are computed once; then its operands are loaded.
       uint32_t gb = 0, tw = 0;
       int last_par[kStages] = {-1, -1, -1};
       int q_par = -1;
-      bool ok = !poisoned;
-      for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
+      bool ok = true;
+      for (uint32_t k = 0; ok; ++k) {
+        const long long u = (long long)blockIdx.x + (long long)k * gridDim.x;
+        const bool end = u >= Q.ntiles;
         Tile t;
-        tile_coords(Q, u, t);
-        tile_ranges_warp(Q, t, lane);
+        t.b = t.g = t.i0 = 0;
+        t.rlo = t.rhi = t.clo = t.chi = t.cpad = t.ncols = t.nb = 0;
+        if (!end) {
+          tile_coords(Q, u, t);
+          tile_ranges_warp(Q, t, lane);
+        }
+        const int slot = k % kDescSlots;
+        if (k >= (uint32_t)kDescSlots &&
+            !wait_warp(&bars.desc_empty[slot], ((k / kDescSlots) - 1) & 1, abort_flag, p.status, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          volatile DqDesc &d = bars.desc[slot];
+          d.u = end ? -1 : u;
+          d.b = t.b; d.g = t.g; d.i0 = t.i0;
+          d.rlo = t.rlo; d.rhi = t.rhi; d.clo = t.clo; d.chi = t.chi;
+          d.cpad = t.cpad; d.ncols = t.ncols; d.nb = t.nb;
+        }
+        __syncwarp();
+        mbar_arrive(&bars.desc_full[slot]);
+        if (end) break;
         const int nb = t.nb;
-        if (nb == 0) continue;
+        if (poisoned || nb == 0) continue;
         if (lane == 0) {
           if (tw > 0) ok = mbar_wait(&bars.qd_empty, (tw - 1) & 1, abort_flag, p.status, p.wait_ns);
           if (ok) {
@@ -211,19 +273,19 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + kOffKV), 16, 1024);
       const uint64_t dV0 = smem_desc_sw128(smem_u32(smem + kOffKV), kHalfTile, 1024);
       const uint32_t id_dq = idesc_bf16_f32(kRows, kHeadDim, false, true);
-      uint32_t gb = 0, tw = 0;
-      bool ok = !poisoned, issued = false;
-      if (ok && p.stall) {
+      uint32_t gb = 0, tw = 0, kd = 0;
+      bool ok = true, issued = false;
+      if (!poisoned && p.stall) {
         injected_stall(&bars.never, abort_flag, p.status, p.wait_ns);
         ok = false;
       }
-      for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
+      while (ok) {
         Tile t;
-        tile_coords(Q, u, t);
-        tile_ranges_warp(Q, t, lane);
-        uniform_tile(t);
+        long long u;
+        ok = read_dq_desc(bars, kd++, t, u, abort_flag, p.status, p.wait_ns);
+        if (!ok || u < 0) break;
         const int nb = t.nb;
-        if (nb == 0) continue;
+        if (poisoned || nb == 0) continue;
         // S (x = 0) or dP (x = 1) of block j into its TMEM columns
         auto issue_sdp = [&](int x, int j, uint32_t g, bool last_q_use) {
           int n, nc;
@@ -297,6 +359,51 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         if (lane == 0) mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
         __syncwarp();
       }
+    } else {
+      // ------------------------------------------------------------ Delta
+      // Delta = <dO, out> of every tile row from the staged dO and out tiles
+      // (two warps, 64 rows each, two rows per lane), off the dS warps'
+      // critical path; published in shared memory and, as -scale*Delta, in
+      // the row records the dkv kernel reads.
+      const int dt = tid - (kEW + 64);  // 0..63
+      uint32_t tw = 0, kd = 0;
+      bool ok = true;
+      const uint8_t *dobuf = smem + kOffDO;
+      const uint8_t *outbuf = smem + kOffO;
+      while (ok) {
+        Tile t;
+        long long u;
+        ok = read_dq_desc(bars, kd++, t, u, abort_flag, p.status, p.wait_ns);
+        if (!ok || u < 0) break;
+        if (poisoned || t.nb == 0) continue;
+        if (!wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+        float dl[2] = {0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = dt + 64 * h;
+#pragma unroll 4
+          for (int ch = 0; ch < 16; ++ch) {
+            const uint4 ov = *reinterpret_cast<const uint4 *>(outbuf + sw128_offset(r, ch));
+            const uint4 gv = *reinterpret_cast<const uint4 *>(dobuf + sw128_offset(r, ch));
+            const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              dl[h] = fmaf(__uint_as_float(oa[x] << 16), __uint_as_float(ga[x] << 16), dl[h]);
+              dl[h] = fmaf(__uint_as_float(oa[x] & 0xffff0000u), __uint_as_float(ga[x] & 0xffff0000u), dl[h]);
+            }
+          }
+        }
+        mbar_arrive(&bars.qd_empty);  // dO and out of this tile are read
+        float *rs = p.rowstat + tile_linear(Q, t) * 2 * kRows;
+        rs[kRows + dt] = -p.scale * dl[0];
+        rs[kRows + dt + 64] = -p.scale * dl[1];
+        // the dS warps have read the previous tile's Delta
+        if (tw > 0 && !wait_warp(&bars.stat_empty, (tw - 1) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+        bars.delta[dt] = dl[0];
+        bars.delta[dt + 64] = dl[1];
+        mbar_arrive(&bars.stat_full);
+        ++tw;
+      }
     }
   } else {
     setmaxnreg_inc<kRegEW>();
@@ -305,11 +412,10 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
     // [64 wg, 64 wg + 64) of every block (and dq columns [64 wg, 64 wg + 64))
     const int r = tid & (kRows - 1), wg = tid >> 7;
     const int cb = wg * 64;
+    const int pq = r & (Q.Pq - 1), hh = r >> p.pq_shift;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     uint8_t *obuf = smem + kOffOut;
-    const uint8_t *dobuf = smem + kOffDO;
-    const uint8_t *outbuf = smem + kOffO;
-    uint32_t gb = 0, tw = 0, epi_phase = 0;
+    uint32_t gb = 0, tw = 0, epi_phase = 0, kd = 0;
     const uint64_t sl2x2 = f32x2(__float_as_uint(p.sl2), __float_as_uint(p.sl2));
     bool ok = true, store_pending = false;
     auto rendezvous = [&]() -> bool {
@@ -318,12 +424,12 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       ++epi_phase;
       return rr;
     };
-    for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
+    while (ok) {
       Tile t;
-      tile_coords(Q, u, t);
-      tile_ranges_warp(Q, t, lane);
+      long long u;
+      ok = read_dq_desc(bars, kd++, t, u, abort_flag, p.status, p.wait_ns);
+      if (!ok || u < 0) break;
       const int nb = t.nb;
-      const int pq = r % Q.Pq, hh = r / Q.Pq;
       const int head = t.g * Q.HG + hh;
       const int i = t.i0 + pq;
       const RowIv iv = row_interval(Q.sstart, t.b, Q.S, i, Q.W, Q.m);
@@ -343,30 +449,9 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         }
         continue;
       }
-      // Delta = <dO, out> for this row, from the staged dO and out tiles
-      // (both warpgroups form it; the first one publishes it)
-      const float lse_row = iv.valid ? p.lse[lrow] : 0.f;
-      if (!wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
-      float lse2 = 0.f, delta = 0.f;
-      if (iv.valid) {
-#pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          const uint4 ov = *reinterpret_cast<const uint4 *>(outbuf + sw128_offset(r, ch));
-          const uint4 gv = *reinterpret_cast<const uint4 *>(dobuf + sw128_offset(r, ch));
-          const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            delta = fmaf(__uint_as_float(oa[x] << 16), __uint_as_float(ga[x] << 16), delta);
-            delta = fmaf(__uint_as_float(oa[x] & 0xffff0000u), __uint_as_float(ga[x] & 0xffff0000u), delta);
-          }
-        }
-        lse2 = lse_row * kLog2e;
-      }
-      if (wg == 0) {
-        rs[r] = -lse2;
-        rs[kRows + r] = -p.scale * delta;
-      }
-      mbar_arrive(&bars.qd_empty);
+      const float lse2 = iv.valid ? p.lse[lrow] * kLog2e : 0.f;
+      if (wg == 0) rs[r] = -lse2;
+      float delta = 0.f;
       for (int j = 0; j < nb; ++j, ++gb) {
         int n, nc;
         block_cols(t, j, n, nc);
@@ -416,6 +501,12 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
             pv[c] = ((vis >> c) & 1ull) ? __float_as_uint(ex2_approx(t0)) : 0u;
             pv[c + 1] = ((vis >> (c + 1)) & 1ull) ? __float_as_uint(ex2_approx(t1)) : 0u;
           }
+        }
+        if (j == 0) {
+          // this tile's Delta, from the Delta warps
+          if (!wait_warp(&bars.stat_full, tw & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+          delta = bars.delta[r];
+          mbar_arrive(&bars.stat_empty);
         }
         if (!wait_warp(&bars.dp_full, gb & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
@@ -1224,6 +1315,8 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   dp.scale = a.scale;
   dp.wait_ns = a.wait_ns;
   dp.stall = (a.stall & HCA_STALL_DQ) != 0;
+  dp.pq_shift = 0;
+  while ((1 << dp.pq_shift) < q.Pq) ++dp.pq_shift;
   const long long g1 = q.ntiles < sms ? q.ntiles : sms;
   if (g1 == 0) return cudaSuccess;
   cudaError_t e;

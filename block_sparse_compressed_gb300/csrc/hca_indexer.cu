@@ -1,0 +1,442 @@
+// hca_indexer.cu -- the Lightning Indexer: index scores of the compressed
+// entries per query, sentinel masking and top-k selection, feeding CSA.
+//
+// "[DeepSeek-V4] Implement Compressed Attention Layers": the LightningIndexer
+// implements sentinel masking (Description), and its scores are the matmul
+// of the indexer queries with the transposed compressed kv, [B, S, H, W] per
+// head (review suggestion on the indexer); "Add HCA Static Compilation for
+// Splash Attention [Deepseek v4]", Description: CSA needs a top-k step.
+// The per-head scores are combined by a weighted sum over heads:
+//   score[b,s,j] = sum_h w[b,s,h] <qi[b,s,h,:], ki[b,j,:]>
+//                = < sum_h w[b,s,h] qi[b,s,h,:], ki[b,j,:] >
+// (linear in the query, so the heads collapse into one query vector first;
+// the pages name no activation between the two steps).  Entry j is visible
+// to query i under the HCA compressed rule (window complete at i, inside i's
+// document, hca_common.cuh), a contiguous range [clo(i), chi(i)]; every
+// other entry carries the sentinel -inf and is never selected.  top-k keeps
+// the k largest scores (ties: smaller entry index), written in ascending
+// entry order and padded with -1.
+//
+// Three kernels per chunk of query rows:
+//   1. collapse   q~[b,s,:] = sum_h w qi  (fp32 accumulation -> bf16), HBM-bound
+//   2. scores     tcgen05 GEMM of 128-position tiles of q~ against 128-entry
+//                 blocks of ki (TMA -> smem -> MMA -> TMEM -> fp32 rows in a
+//                 chunk buffer); blocks past a tile's last visible entry are
+//                 skipped
+//   3. top-k      one CTA per query row: 4-pass radix select (8-bit digits)
+//                 on order-preserving integer keys in shared memory, then an
+//                 ordered compaction of the winners
+#include <cuda_bf16.h>
+
+#include "hca_common.cuh"
+#include "hca_internal.h"
+#include "tc_ptx.cuh"
+#include "tc_tiles.cuh"
+
+namespace hca {
+using namespace tc;
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// 1. head collapse
+// ---------------------------------------------------------------------------
+constexpr int kCollapseWarps = 8;
+
+__global__ void __launch_bounds__(32 * kCollapseWarps)
+    hca_index_collapse_kernel(const __nv_bfloat16 *__restrict__ qi, const float *__restrict__ w,
+                              __nv_bfloat16 *__restrict__ qc, long long rows, int Hi) {
+  const int lane = threadIdx.x & 31;
+  const long long r = (long long)blockIdx.x * kCollapseWarps + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  // lane holds dims [4 lane, 4 lane + 4) of the 128
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const __nv_bfloat16 *base = qi + (size_t)r * Hi * kHeadDim;
+  const float *wr = w + (size_t)r * Hi;
+  for (int h = 0; h < Hi; ++h) {
+    const float wh = __ldg(wr + h);
+    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(base + (size_t)h * kHeadDim) + lane);
+    acc[0] = fmaf(wh, __uint_as_float(v.x << 16), acc[0]);
+    acc[1] = fmaf(wh, __uint_as_float(v.x & 0xffff0000u), acc[1]);
+    acc[2] = fmaf(wh, __uint_as_float(v.y << 16), acc[2]);
+    acc[3] = fmaf(wh, __uint_as_float(v.y & 0xffff0000u), acc[3]);
+  }
+  uint2 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  reinterpret_cast<uint2 *>(qc + (size_t)r * kHeadDim)[lane] = o;
+}
+
+// ---------------------------------------------------------------------------
+// 2. scores: 128 query positions x 128 entries per MMA tile
+// ---------------------------------------------------------------------------
+namespace isk {
+constexpr int kStages = 2;
+constexpr int kThreads = 192;  // warps 0-3 epilogue (one TMEM lane quarter each), 4 TMA, 5 MMA
+constexpr int kOffA = 0, kOffB = kTile;
+constexpr int kSmemBytes = kTile + kStages * kTile + 1024;
+constexpr int kTmemCols = 256;  // two 128-column accumulators
+}  // namespace isk
+
+struct ScoreParams {
+  const int32_t *sstart;  // NULL = one document per row
+  float *buf;             // [B][rows][ld] fp32 chunk buffer
+  int B, S, m, Sc, row0, rows, ld;
+  int32_t *status;
+  uint64_t wait_ns;
+};
+
+struct ScoreBars {
+  uint64_t a_full;
+  uint64_t b_full[isk::kStages], b_empty[isk::kStages];
+  uint64_t acc_full[2], acc_free[2], drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Last entry (exclusive) any position of [p0, p1) can see: entries complete
+// at position p1 - 1.
+__device__ __forceinline__ int entries_upto(int p1, int m) { return p1 / m; }
+
+__global__ void __launch_bounds__(isk::kThreads, 1)
+    hca_index_score_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                           const ScoreParams p) {
+  using namespace isk;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ ScoreBars bars;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int *abort_flag = &bars.abort;
+  // tile: batch row b, positions [p0, p0 + 128) of the chunk
+  const int tiles_per_b = (p.rows + kRows - 1) / kRows;
+  const int b = blockIdx.x / tiles_per_b;
+  const int p0 = p.row0 + (blockIdx.x % tiles_per_b) * kRows;
+  const int p1 = min(p0 + kRows, min(p.row0 + p.rows, p.S));
+  const int nent = min(entries_upto(p1, p.m), p.Sc);
+  const int nblk = (nent + kBlockKeys - 1) / kBlockKeys;
+
+  if (tid == 0) {
+    mbar_init(&bars.a_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars.b_full[s], 1);
+      mbar_init(&bars.b_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars.acc_full[x], 1);
+      mbar_init(&bars.acc_free[x], 128);
+    }
+    mbar_init(&bars.drain, 1);
+    bars.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA
+    bool ok = true;
+    int b_par[kStages] = {-1, -1};
+    if (lane == 0 && nblk > 0) {
+      mbar_arrive_expect_tx(&bars.a_full, kTile);
+      tma_load_3d(&map_q, &bars.a_full, smem + kOffA, 0, p0, b);
+      tma_load_3d(&map_q, &bars.a_full, smem + kOffA + kHalfTile, 64, p0, b);
+      for (int j = 0; ok && j < nblk; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages) ok = mbar_wait(&bars.b_empty[s], ((j / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars.b_full[s], kTile);
+        tma_load_3d(&map_k, &bars.b_full[s], smem + kOffB + s * kTile, 0, j * kBlockKeys, b);
+        tma_load_3d(&map_k, &bars.b_full[s], smem + kOffB + s * kTile + kHalfTile, 64, j * kBlockKeys, b);
+        b_par[s] = (j / kStages) & 1;
+      }
+      if (!ok) {
+        volatile int never = 0;
+        mbar_wait(&bars.a_full, 0, &never, p.status, 100000000ull);
+        for (int s = 0; s < kStages; ++s)
+          if (b_par[s] >= 0) mbar_wait(&bars.b_full[s], b_par[s], &never, p.status, 100000000ull);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA
+    const uint64_t da = smem_desc_sw128(smem_u32(smem + kOffA), 16, 1024);
+    const uint64_t db0 = smem_desc_sw128(smem_u32(smem + kOffB), 16, 1024);
+    const uint32_t idesc = idesc_bf16_f32(kRows, kBlockKeys, false, false);
+    bool ok = nblk > 0, issued = false;
+    if (ok) ok = wait_warp(&bars.a_full, 0, abort_flag, p.status, p.wait_ns);
+    for (int j = 0; ok && j < nblk; ++j) {
+      const int s = j % kStages, x = j & 1;
+      ok = wait_warp(&bars.b_full[s], (j / kStages) & 1, abort_flag, p.status, p.wait_ns);
+      if (ok && j >= 2) ok = wait_warp(&bars.acc_free[x], ((j / 2) - 1) & 1, abort_flag, p.status, p.wait_ns);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t db = db0 + desc_bytes(s * kTile);
+      if (elect_one()) {
+#pragma unroll
+        for (int k = 0; k < kHeadDim / 16; ++k)
+          mma_ss(tmem + x * 128, da + kmaj_step(k), db + kmaj_step(k), idesc, k > 0);
+        mma_commit(&bars.acc_full[x]);
+        mma_commit(&bars.b_empty[s]);
+      }
+      __syncwarp();
+      issued = true;
+    }
+    if (!ok && issued) {
+      volatile int never = 0;
+      if (elect_one()) mma_commit(&bars.drain);
+      __syncwarp();
+      if (lane == 0) mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // thread r = row r of the tile (TMEM lane r): its 128 scores of a block
+    // go to the chunk buffer as 32 16-byte stores
+    const int r = tid;
+    const int pos = p0 + r;
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    float *dst = p.buf + ((size_t)b * p.rows + (pos - p.row0)) * p.ld;
+    const bool live = pos < p1;
+    for (int j = 0; j < nblk; ++j) {
+      const int x = j & 1;
+      if (!wait_warp(&bars.acc_full[x], (j / 2) & 1, abort_flag, p.status, p.wait_ns)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(lane_addr + x * 128 + c0, v);
+        tmem_wait_ld();
+        if (live) {
+          float4 *d4 = reinterpret_cast<float4 *>(dst + j * kBlockKeys + c0);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars.acc_free[x]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. top-k per query row
+// ---------------------------------------------------------------------------
+constexpr int kTopkThreads = 256;
+
+// Order-preserving map of a float to an unsigned key (larger float, larger key).
+__device__ __forceinline__ uint32_t fkey(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive block scan of one int per thread; returns the block total.
+__device__ __forceinline__ int block_excl_scan(int v, int &excl, int *wsum) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[wid] = x;
+  __syncthreads();
+  int base = 0, total = 0;
+#pragma unroll
+  for (int k = 0; k < kTopkThreads / 32; ++k) {
+    const int s = wsum[k];
+    if (k < wid) base += s;
+    total += s;
+  }
+  __syncthreads();
+  excl = base + x - v;
+  return total;
+}
+
+struct TopkParams {
+  const float *buf;
+  const int32_t *sstart;
+  const int32_t *status;  // non-zero (segment ids out of order): nothing is selected
+  int32_t *sel;      // [B,S,k]
+  float *scores;     // optional [B,S,Sc] with -inf outside the visible range
+  int B, S, m, Sc, row0, rows, ld, k;
+};
+
+__global__ void __launch_bounds__(kTopkThreads) hca_index_topk_kernel(const TopkParams p) {
+  extern __shared__ uint32_t keys[];
+  __shared__ int hist[256];
+  __shared__ int wsum[kTopkThreads / 32];
+  __shared__ int sh_digit, sh_rem;
+  const int tid = threadIdx.x;
+  const int b = blockIdx.x / p.rows;
+  const int i = p.row0 + blockIdx.x % p.rows;
+  if (i >= p.S) return;
+  const float *row = p.buf + ((size_t)b * p.rows + (i - p.row0)) * p.ld;
+  int32_t *out = p.sel + ((size_t)b * p.S + i) * p.k;
+  const RowIv iv = row_interval(p.sstart, b, p.S, i, 1, p.m);
+  const int lo = iv.valid ? iv.clo : 0;
+  const int hi = iv.valid ? min(iv.chi, p.Sc - 1) : -1;
+  const int n = hi >= lo ? hi - lo + 1 : 0;
+  if (p.scores) {
+    float *sr = p.scores + ((size_t)b * p.S + i) * p.Sc;
+    for (int j = tid; j < p.Sc; j += kTopkThreads) sr[j] = (j >= lo && j <= hi) ? row[j] : -INFINITY;
+  }
+  if (*(volatile const int32_t *)p.status != 0) {
+    for (int t = tid; t < p.k; t += kTopkThreads) out[t] = -1;
+    return;
+  }
+  if (n <= p.k) {
+    for (int t = tid; t < p.k; t += kTopkThreads) out[t] = t < n ? lo + t : -1;
+    return;
+  }
+  for (int t = tid; t < n; t += kTopkThreads) keys[t] = fkey(row[lo + t]);
+  // radix select of the k-th largest key, 8 bits at a time from the top
+  uint32_t prefix = 0, mask = 0;
+  int rem = p.k;  // winners still to place at or below the current prefix
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int d = tid; d < 256; d += kTopkThreads) hist[d] = 0;
+    __syncthreads();
+    for (int t = tid; t < n; t += kTopkThreads) {
+      const uint32_t kv = keys[t];
+      if ((kv & mask) == prefix) atomicAdd(&hist[(kv >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      // digit from the top where the running count reaches rem (one warp:
+      // each lane owns 8 consecutive digits, highest lanes first)
+      int c[8], s = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        c[q] = hist[255 - (tid * 8 + q)];
+        s += c[q];
+      }
+      int incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += y;
+      }
+      const int before = incl - s;  // keys in higher digits than this lane's
+      const bool here = before < rem && incl >= rem;
+      const unsigned ball = __ballot_sync(0xffffffffu, here);
+      if (here) {
+        int run = before, dsel = 0, rsel = rem;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (run + c[q] >= rem) {
+            dsel = 255 - (tid * 8 + q);
+            rsel = rem - run;
+            break;
+          }
+          run += c[q];
+        }
+        sh_digit = dsel;
+        sh_rem = rsel;
+      }
+      (void)ball;
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sh_digit << shift;
+    mask |= 255u << shift;
+    rem = sh_rem;
+    __syncthreads();
+  }
+  // prefix is the k-th largest key; rem of the keys equal to it are taken,
+  // the ones with the smallest entry index.  Ordered compaction:
+  int placed = 0, ties = 0;
+  for (int t0 = 0; t0 < n; t0 += kTopkThreads) {
+    const int t = t0 + tid;
+    const uint32_t kv = t < n ? keys[t] : 0u;
+    const bool eq = t < n && kv == prefix;
+    int eq_before;
+    const int eq_total = block_excl_scan(eq ? 1 : 0, eq_before, wsum);
+    const bool take = t < n && (kv > prefix || (eq && ties + eq_before < rem));
+    int pos;
+    const int take_total = block_excl_scan(take ? 1 : 0, pos, wsum);
+    if (take) out[placed + pos] = lo + t;
+    placed += take_total;
+    ties += eq_total;
+  }
+}
+
+}  // namespace
+
+size_t indexer_chunk_rows(int B, int S, int Sc) {
+  // rows of query positions per pass: the fp32 score buffer stays <= 256 MB
+  const size_t ld = (size_t)((Sc + kBlockKeys - 1) / kBlockKeys) * kBlockKeys;
+  size_t rows = (size_t)256 << 20;
+  rows /= (size_t)(B > 0 ? B : 1) * ld * sizeof(float);
+  rows = rows / kRows * kRows;
+  if (rows < kRows) rows = kRows;
+  if (rows > (size_t)S) rows = ((size_t)S + kRows - 1) / kRows * kRows;
+  return rows;
+}
+
+size_t indexer_workspace_bytes(int B, int S, int m) {
+  const int Sc = (S + m - 1) / m;
+  const size_t ld = (size_t)((Sc + kBlockKeys - 1) / kBlockKeys) * kBlockKeys;
+  const size_t rows = indexer_chunk_rows(B, S, Sc);
+  return kHeaderBytes + align_up((size_t)B * S * sizeof(int32_t)) + align_up((size_t)B * S * kHeadDim * 2) +
+         align_up((size_t)B * rows * ld * sizeof(float));
+}
+
+cudaError_t indexer_topk(const IndexerArgs &a, cudaStream_t st) {
+  const int Sc = (a.S + a.m - 1) / a.m;
+  const int ld = (Sc + kBlockKeys - 1) / kBlockKeys * kBlockKeys;
+  const int rows_chunk = (int)indexer_chunk_rows(a.B, a.S, Sc);
+  __nv_bfloat16 *qc = static_cast<__nv_bfloat16 *>(a.qc);
+  // 1. collapse the heads
+  {
+    const long long rows = (long long)a.B * a.S;
+    ProfScope prof(kKIndexScore, st);
+    hca_index_collapse_kernel<<<(unsigned)((rows + kCollapseWarps - 1) / kCollapseWarps), 32 * kCollapseWarps, 0,
+                                st>>>(static_cast<const __nv_bfloat16 *>(a.qi), a.w, qc, rows, a.Hi);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap mq, mk;
+  if (!make_map_bf16(&mq, qc, kHeadDim, a.S, a.B, kRows, 1) || !make_map_bf16(&mk, a.ki, kHeadDim, Sc, a.B, kBlockKeys, 1))
+    return cudaErrorInvalidValue;
+  static SmemAttrOnce attr_s, attr_t;
+  const int topk_smem = ld * (int)sizeof(uint32_t);
+  cudaError_t e = attr_s.ensure(reinterpret_cast<const void *>(hca_index_score_kernel), isk::kSmemBytes);
+  if (e == cudaSuccess) e = attr_t.ensure(reinterpret_cast<const void *>(hca_index_topk_kernel), 227 * 1024);
+  if (e != cudaSuccess) return e;
+  for (int row0 = 0; row0 < a.S; row0 += rows_chunk) {
+    const int rows = min(rows_chunk, a.S - row0);
+    ScoreParams sp;
+    sp.sstart = a.sstart; sp.buf = a.buf; sp.B = a.B; sp.S = a.S; sp.m = a.m; sp.Sc = Sc;
+    sp.row0 = row0; sp.rows = rows; sp.ld = ld; sp.status = a.status; sp.wait_ns = a.wait_ns;
+    const int tiles = a.B * ((rows + kRows - 1) / kRows);
+    {
+      ProfScope prof(kKIndexScore, st);
+      hca_index_score_kernel<<<tiles, isk::kThreads, isk::kSmemBytes, st>>>(mq, mk, sp);
+      e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
+    TopkParams tp;
+    tp.buf = a.buf; tp.sstart = a.sstart; tp.status = a.status; tp.sel = a.sel; tp.scores = a.scores;
+    tp.B = a.B; tp.S = a.S; tp.m = a.m; tp.Sc = Sc; tp.row0 = row0; tp.rows = rows; tp.ld = ld; tp.k = a.k;
+    {
+      ProfScope prof(kKIndexTopk, st);
+      hca_index_topk_kernel<<<a.B * rows, kTopkThreads, topk_smem, st>>>(tp);
+      e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace hca

@@ -10,7 +10,8 @@ namespace hca {
 
 // kernels the optional profiler distinguishes (hca_profile_read ids)
 enum KernelId {
-  kKPrep = 0, kKFwdTc, kKBwdDq, kKBwdDkv, kKBwdReduce, kKSimtFwd, kKSimtBwd, kKVisibility, kNumKernels
+  kKPrep = 0, kKFwdTc, kKBwdDq, kKBwdDkv, kKBwdReduce, kKSimtFwd, kKSimtBwd, kKVisibility, kKCompress,
+  kKIndexScore, kKIndexTopk, kNumKernels
 };
 
 // Brackets the launches issued during its lifetime with CUDA events on `st`
@@ -75,6 +76,30 @@ cudaError_t launch_tile_map(const int32_t *sstart, int B, int S, int W, int m, i
 
 cudaError_t simt_fwd(const FwdArgs &a, cudaStream_t st);
 cudaError_t simt_bwd(const BwdArgs &a, cudaStream_t st);
+
+// HCA compressor (hca_compress.cu)
+size_t compress_workspace_bytes(int B, int S, int m);
+cudaError_t compress_fwd(const void *x, const float *g, const float *bias, const int32_t *seg, void *ckv, int B, int S,
+                         int D, int m, int dtype, cudaStream_t st);
+cudaError_t compress_bwd(const void *x, const float *g, const float *bias, const int32_t *seg, const void *dckv,
+                         void *dx, float *dg, float *dbias, float *dz, int B, int S, int D, int m, int dtype,
+                         cudaStream_t st);
+
+// Lightning Indexer (hca_indexer.cu)
+struct IndexerArgs {
+  const void *qi, *ki;       // [B,S,Hi,128], [B,Sc,128] bf16
+  const float *w;            // [B,S,Hi]
+  const int32_t *sstart;     // document starts (NULL = one document)
+  int32_t *sel;              // [B,S,k]
+  float *scores;             // optional [B,S,Sc]
+  void *qc;                  // workspace: collapsed queries [B,S,128] bf16
+  float *buf;                // workspace: chunk score buffer
+  int32_t *status;
+  uint64_t wait_ns;
+  int B, S, Hi, m, k;
+};
+size_t indexer_workspace_bytes(int B, int S, int m);
+cudaError_t indexer_topk(const IndexerArgs &a, cudaStream_t st);
 
 // tensor-core (tcgen05) path
 bool tc_fwd_supported(int H, int D, int dtype);

@@ -29,7 +29,9 @@ _lib = None
 EXPORTS = ("hca_status_string", "hca_version", "hca_workspace_size", "hca_query_tile_positions", "hca_attn_fwd",
            "hca_attn_bwd", "hca_visible_pairs", "hca_tile_map", "hca_workspace_status", "hca_profile_enable",
            "hca_profile_read", "hca_num_kernels", "hca_kernel_name", "hca_attn_fwd_noalloc",
-           "hca_local_workspace_size", "hca_local_attn_fwd", "hca_local_attn_bwd", "hca_test_inject")
+           "hca_local_workspace_size", "hca_local_attn_fwd", "hca_local_attn_bwd", "hca_test_inject",
+           "hca_compress_fwd", "hca_compress_workspace_size", "hca_compress_bwd", "hca_indexer_workspace_size",
+           "hca_indexer_topk")
 
 # failure-path test hooks (hca_test_inject)
 INJECT_RESET, INJECT_LAUNCH_FAILURE, INJECT_STALL, INJECT_WAIT_LIMIT_NS = 0, 1, 2, 3
@@ -87,6 +89,16 @@ def load(path: str = LIB_PATH):
             lib.hca_local_attn_bwd.restype = I
             lib.hca_test_inject.argtypes = [I, ctypes.c_longlong]
             lib.hca_test_inject.restype = I
+            lib.hca_compress_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
+            lib.hca_compress_fwd.restype = I
+            lib.hca_compress_workspace_size.argtypes = [I, I, I]
+            lib.hca_compress_workspace_size.restype = Z
+            lib.hca_compress_bwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, Z, P]
+            lib.hca_compress_bwd.restype = I
+            lib.hca_indexer_workspace_size.argtypes = [I, I, I]
+            lib.hca_indexer_workspace_size.restype = Z
+            lib.hca_indexer_topk.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, Z, P]
+            lib.hca_indexer_topk.restype = I
             _lib = lib
     return _lib
 
@@ -364,3 +376,70 @@ def hca_attn_fwd_noalloc(q, kv, ckv, seg, W: int, m: int, scale: float, out=None
                                       float(scale), dt, _stream(q.device))
     _check(rc, "hca_attn_fwd_noalloc")
     return out, lse
+
+
+def hca_compress_fwd(x: torch.Tensor, g: torch.Tensor, bias: torch.Tensor, seg: Optional[torch.Tensor], m: int,
+                     ckv: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """HCA compressor: ckv[B, ceil(S/m), D] from x[B,S,D], gates g[B,S] fp32,
+    block bias[m] fp32 (include/hca.h, hca_compress_fwd)."""
+    lib = load()
+    B, S, D = x.shape
+    Sc = -(-S // m)
+    dev = x.device
+    _need(x, "x", (B, S, D), x.dtype, dev)
+    _need(g, "g", (B, S), torch.float32, dev)
+    _need(bias, "bias", (m,), torch.float32, dev)
+    if seg is not None:
+        _need(seg, "seg", (B, S), torch.int32, dev)
+    ckv = torch.empty(B, Sc, D, dtype=x.dtype, device=dev) if ckv is None else ckv
+    _need(ckv, "ckv", (B, Sc, D), x.dtype, dev)
+    with _on(dev):
+        rc = lib.hca_compress_fwd(_ptr(x), _ptr(g), _ptr(bias), _ptr(seg), _ptr(ckv), B, S, D, m, _dtype_code(x),
+                                  _stream(dev))
+    _check(rc, "hca_compress_fwd")
+    return ckv
+
+
+def hca_compress_bwd(x, g, bias, seg, m: int, dckv, dx=None, dg=None, dbias=None, ws=None):
+    """Backward of the compressor: (dx[B,S,D], dg[B,S] fp32, dbias[m] fp32)."""
+    lib = load()
+    B, S, D = x.shape
+    Sc = -(-S // m)
+    dev = x.device
+    _need(dckv, "dckv", (B, Sc, D), x.dtype, dev)
+    dx = torch.empty_like(x) if dx is None else dx
+    dg = torch.empty(B, S, dtype=torch.float32, device=dev) if dg is None else dg
+    dbias = torch.empty(m, dtype=torch.float32, device=dev) if dbias is None else dbias
+    if ws is None:
+        ws = torch.empty(lib.hca_compress_workspace_size(B, S, m), dtype=torch.uint8, device=dev)
+    with _on(dev):
+        rc = lib.hca_compress_bwd(_ptr(x), _ptr(g), _ptr(bias), _ptr(seg), _ptr(dckv), _ptr(dx), _ptr(dg),
+                                  _ptr(dbias), B, S, D, m, _dtype_code(x), _ptr(ws), ws.numel(), _stream(dev))
+    _check(rc, "hca_compress_bwd")
+    return dx, dg, dbias
+
+
+def hca_indexer_topk(qi: torch.Tensor, ki: torch.Tensor, w: torch.Tensor, seg: Optional[torch.Tensor], m: int,
+                     k: int, with_scores: bool = False, ws: Optional[torch.Tensor] = None, check: bool = False):
+    """Lightning Indexer top-k: (sel[B,S,k] int32, scores[B,S,Sc] fp32 or
+    None) from qi[B,S,Hi,128], ki[B,ceil(S/m),128] (bf16), w[B,S,Hi] fp32."""
+    lib = load()
+    B, S, Hi, Di = qi.shape
+    Sc = -(-S // m)
+    dev = qi.device
+    _need(qi, "qi", (B, S, Hi, Di), torch.bfloat16, dev)
+    _need(ki, "ki", (B, Sc, Di), torch.bfloat16, dev)
+    _need(w, "w", (B, S, Hi), torch.float32, dev)
+    if seg is not None:
+        _need(seg, "seg", (B, S), torch.int32, dev)
+    sel = torch.empty(B, S, k, dtype=torch.int32, device=dev)
+    scores = torch.empty(B, S, Sc, dtype=torch.float32, device=dev) if with_scores else None
+    if ws is None:
+        ws = torch.empty(lib.hca_indexer_workspace_size(B, S, m), dtype=torch.uint8, device=dev)
+    with _on(dev):
+        rc = lib.hca_indexer_topk(_ptr(qi), _ptr(ki), _ptr(w), _ptr(seg), _ptr(sel), _ptr(scores), B, S, Hi, Di, m, k,
+                                  _ptr(ws), ws.numel(), _stream(dev))
+    _check(rc, "hca_indexer_topk")
+    if check:
+        _check(hca_workspace_status(ws), "hca_indexer_topk (device)")
+    return sel, scores

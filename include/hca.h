@@ -176,6 +176,62 @@ HCA_API int hca_attn_fwd_noalloc(const void *q, const void *kv, const void *ckv,
                                  void *out, float *lse,
                                  int B, int H, int S, int D, int W, int m, float scale, int dtype, void *stream);
 
+/* HCA compressor: pooling of length-m windows of rows into compressed
+ * entries ("[DeepSeek-V4] Implement Compressed Attention Layers",
+ * Description: the compressors pool with a causal block bias; "Add HCA Static
+ * Compilation for Splash Attention [Deepseek v4]": compressed entries are
+ * the length-m windows).  For window j of batch row b and its positions
+ * t = j*m + r (r < m) that exist and are not padding (seg >= 0):
+ *   a = softmax_r(g[b,t] + bias[r]),   ckv[b,j,:] = sum_r a_r x[b,t,:];
+ * a window with no such position gives a zero row.
+ *   x     [B,S,D]  dtype (bf16 or fp32), D a multiple of 32, D <= 256
+ *   g     [B,S]    fp32 gate logits;  bias [m] fp32 (offset in the block)
+ *   seg   [B,S]    int32 or NULL (padding is skipped; documents are not:
+ *                  a window that crosses documents is never visible to the
+ *                  attention, whatever its value)
+ *   ckv   [B,ceil(S/m),D] dtype, fully overwritten.
+ * No workspace.  Errors as for hca_attn_fwd (HCA_ERR_UNSUPPORTED for D). */
+HCA_API int hca_compress_fwd(const void *x, const float *g, const float *bias, const int32_t *seg, void *ckv,
+                             int B, int S, int D, int m, int dtype, void *stream);
+
+/* Backward of hca_compress_fwd for the cotangent dckv [B,ceil(S/m),D]:
+ * dx [B,S,D] (dtype; 0 at padding), dg [B,S] fp32 (0 at padding), dbias [m]
+ * fp32 (summed over every window in a fixed order, so run-to-run identical).
+ * All three are fully overwritten.  Needs hca_compress_workspace_size(B,S,m)
+ * bytes of workspace (one logit gradient per window position). */
+HCA_API size_t hca_compress_workspace_size(int B, int S, int m);
+HCA_API int hca_compress_bwd(const void *x, const float *g, const float *bias, const int32_t *seg,
+                             const void *dckv, void *dx, float *dg, float *dbias,
+                             int B, int S, int D, int m, int dtype,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/* Lightning Indexer with top-k selection, the step that feeds CSA
+ * ("[DeepSeek-V4] Implement Compressed Attention Layers": the indexer's
+ * per-head scores are the matmul of its queries with the transposed
+ * compressed kv, and it masks with a sentinel; "Add HCA Static Compilation
+ * for Splash Attention [Deepseek v4]", Description: CSA needs a top-k step).
+ *   score[b,s,j] = sum_h w[b,s,h] <qi[b,s,h,:], ki[b,j,:]>   (bf16 inputs,
+ *                  heads collapsed first in fp32, tensor-core products with
+ *                  fp32 accumulation)
+ * for the entries j that query s may see under the HCA compressed rule
+ * (window complete at s, inside s's document); the others carry the
+ * sentinel -inf and are never selected.  sel[b,s,:] receives the k entries
+ * with the largest scores (ties: smaller index), in ascending entry order,
+ * padded with -1 when fewer than k are visible.
+ *   qi [B,S,Hi,Di] bf16, Di = 128;  ki [B,ceil(S/m),Di] bf16;  w [B,S,Hi] fp32
+ *   seg [B,S] int32 or NULL;  sel [B,S,k] int32 (overwritten)
+ *   scores [B,S,ceil(S/m)] fp32 or NULL: when given, every score with the
+ *                  sentinel -inf outside the visible range (for checking)
+ * ceil(S/m) must be at most 57344 and k at least 1.  Workspace:
+ * hca_indexer_workspace_size(B,S,m) bytes (status word, document starts,
+ * collapsed queries and a score buffer of at most 256 MB).  Segment ids out
+ * of order are reported through hca_workspace_status (HCA_ERR_SEG) and that
+ * call selects nothing (every entry of sel is -1). */
+HCA_API size_t hca_indexer_workspace_size(int B, int S, int m);
+HCA_API int hca_indexer_topk(const void *qi, const void *ki, const float *w, const int32_t *seg,
+                             int32_t *sel, float *scores, int B, int S, int Hi, int Di, int m, int k,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
 /* Failure-path test hooks.  "Add HCA Static Compilation for Splash Attention
  * [Deepseek v4]" (Description, validation-guard bullet) wants unsupported or
  * failing cases reported as errors rather than crashes; the tests that check

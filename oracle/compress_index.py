@@ -133,12 +133,14 @@ def compress_bwd(x, g, bias, seg, m: int, dckv):
 # Lightning Indexer: scores, sentinel masking, top-k
 # --------------------------------------------------------------------------
 
-def comp_visible(seg, B: int, S: int, m: int):
-    """bool [B, S, Sc]: compressed entry j may be seen by query i (its window
-    [j*m, (j+1)*m - 1] has completed at i and lies in i's document)."""
+def comp_visible(seg, B: int, S: int, m: int, rows=None):
+    """bool [B, R, Sc]: compressed entry j may be seen by query i (its window
+    [j*m, (j+1)*m - 1] has completed at i and lies in i's document), for the
+    query positions i in rows = (r0, r1) (default: all S)."""
     sg = _seg(seg, B, S)
     Sc = -(-S // m)
-    vis = np.zeros((B, S, Sc), dtype=bool)
+    r0, r1 = rows if rows is not None else (0, S)
+    vis = np.zeros((B, r1 - r0, Sc), dtype=bool)
     for b in range(B):
         for j in range(Sc):
             lo, hi = j * m, (j + 1) * m - 1
@@ -147,26 +149,29 @@ def comp_visible(seg, B: int, S: int, m: int):
             d = sg[b, lo]
             if d < 0 or not np.all(sg[b, lo:hi + 1] == d):
                 continue
-            for i in range(hi, S):
+            for i in range(max(hi, r0), r1):
                 if sg[b, i] == d:
-                    vis[b, i, j] = True
+                    vis[b, i - r0, j] = True
     return vis
 
 
-def index_scores(qi, ki, w, seg, m: int, relu: bool = False):
-    """float64 [B, S, Sc]: sum_h w[b,s,h] * act(<qi[b,s,h,:], ki[b,j,:]>) for
-    visible entries, -inf (the sentinel) elsewhere."""
-    qi = _f64(qi)
+def index_scores(qi, ki, w, seg, m: int, relu: bool = False, rows=None):
+    """float64 [B, R, Sc]: sum_h w[b,s,h] * act(<qi[b,s,h,:], ki[b,j,:]>) for
+    visible entries, -inf (the sentinel) elsewhere; query positions s in
+    rows = (r0, r1) (default: all)."""
+    B, S = qi.shape[0], qi.shape[1]
+    r0, r1 = rows if rows is not None else (0, S)
+    qi = _f64(qi[:, r0:r1])
     ki = _f64(ki)
-    w = _f64(w)
-    B, S, Hi, Di = qi.shape
+    w = _f64(w[:, r0:r1])
+    Hi, Di = qi.shape[2], qi.shape[3]
     Sc = ki.shape[1]
-    assert ki.shape == (B, Sc, Di) and w.shape == (B, S, Hi)
+    assert ki.shape == (B, Sc, Di) and w.shape == (B, r1 - r0, Hi)
     per_head = np.einsum("bshd,bjd->bshj", qi, ki)
     if relu:
         per_head = np.maximum(per_head, 0.0)
     sc = np.einsum("bsh,bshj->bsj", w, per_head)
-    vis = comp_visible(seg, B, S, m)
+    vis = comp_visible(seg, B, S, m, rows=(r0, r1))
     assert vis.shape == sc.shape
     return np.where(vis, sc, -np.inf)
 

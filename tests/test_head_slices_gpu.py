@@ -47,10 +47,11 @@ def test_head_slices_sum_to_the_full_call(group):
         dkv_sum += b.float()
         dckv_sum += c.float()
     v = valid_rows(seg, B, H, S)
-    # the forward and dq do not depend on the other heads at all
-    assert torch.equal(torch.cat(outs, 1), out)
-    assert torch.equal(torch.cat(lses, 1), lse)
-    assert torch.equal(torch.cat(dqs, 1), dq)
+    # the forward and dq of a head do not depend on the other heads (a slice
+    # packs its heads into tiles differently, so only rounding may differ)
+    assert_close("out (slices) vs full call", torch.cat(outs, 1), to_np(out), torch.bfloat16, v)
+    assert_close("lse (slices) vs full call", torch.cat(lses, 1), to_np(lse), torch.bfloat16, v)
+    assert_close("dq (slices) vs full call", torch.cat(dqs, 1), to_np(dq), torch.bfloat16, v)
     # the summed slices match the full call and the oracle
     rdq, rdkv, rdckv = oracle.bwd(q, kv, ckv, seg, dout, W, m, scale)
     assert_close("dkv (slices summed) vs full call", dkv_sum, to_np(dkv), torch.bfloat16)

@@ -93,7 +93,8 @@ def test_any_head_count_on_tensor_cores(H):
 def test_bf16_head_dims_without_a_tensor_core_tile_are_rejected(D):
     # bf16 runs on the tensor-core kernels only: other head dims are an
     # error, never a silent CUDA-core fallback
-    q, kv, ckv, _, dout = (x.to(DEV) for x in I.small(1, 4, 64, D, 16, 8, dtype=torch.bfloat16))
+    q, kv, ckv, _, dout = I.small(1, 4, 64, D, 16, 8, dtype=torch.bfloat16)
+    q, kv, ckv, dout = (x.to(DEV) for x in (q, kv, ckv, dout))
     with pytest.raises(hca.HCAError) as e:
         hca.hca_attn_fwd(q, kv, ckv, None, 16, 8, 0.1)
     assert e.value.status == 8
