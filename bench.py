@@ -64,8 +64,10 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
-    ap.add_argument("--mode", choices=("hca", "local"), default="hca",
-                    help="local: time the local sliding-window entry points (no compressed set) on the same shape")
+    ap.add_argument("--mode", choices=("hca", "local", "compress", "indexer"), default="hca",
+                    help="local: the local sliding-window entry points (no compressed set) on the same shape; "
+                         "compress: the HCA compressor (m=128) and its backward; indexer: the Lightning Indexer "
+                         "scores + top-k on the CSA shape (m=4)")
     ap.add_argument("--ncu-case", type=int, default=0, metavar="S",
                     help="profiling case: run --warmup + 1 untimed fwd+bwd steps of the headline shape at sequence "
                          "length S and exit (for ncu captures; prints nothing to time)")
@@ -553,6 +555,89 @@ def run_local(args):
     return 0
 
 
+def _time_cuda(fn, steps, warmup):
+    import torch
+    for _ in range(max(3, warmup)):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_compress(args):
+    """HCA compressor forward and backward on 16 sequences of the headline
+    length (kv [16, 65536, 128] bf16, 268 MB: above L2, so no flush needed);
+    HBM-bound, reported against the measured copy bandwidth."""
+    import torch
+    from block_sparse_compressed_gb300 import hca
+    from block_sparse_compressed_gb300 import inputs as I
+    B, S, D, m = 16, 65536, 128, 128
+    dev = torch.device("cuda", 0)
+    x = I.normal((B, S, D), 1, torch.bfloat16, dev)
+    g = I.normal((B, S), 2, torch.float32, dev)
+    bias = I.normal((m,), 3, torch.float32, dev)
+    Sc = S // m
+    dck = I.normal((B, Sc, D), 4, torch.bfloat16, dev)
+    ckv = torch.empty(B, Sc, D, dtype=torch.bfloat16, device=dev)
+    dx, dg, db = torch.empty_like(x), torch.empty_like(g), torch.empty_like(bias)
+    ws = torch.empty(hca.load().hca_compress_workspace_size(B, S, m), dtype=torch.uint8, device=dev)
+    f_ms = _time_cuda(lambda: hca.hca_compress_fwd(x, g, bias, None, m, ckv=ckv), args.steps, args.warmup)
+    b_ms = _time_cuda(lambda: hca.hca_compress_bwd(x, g, bias, None, m, dck, dx=dx, dg=dg, dbias=db, ws=ws),
+                      args.steps, args.warmup)
+    fwd_bytes = x.numel() * 2 + g.numel() * 4 + ckv.numel() * 2
+    # backward: x and g read, dckv read, dx and dg written, per-window logit grads written + read
+    bwd_bytes = x.numel() * 2 + g.numel() * 4 + dck.numel() * 2 + dx.numel() * 2 + dg.numel() * 4 + 2 * 4 * B * S
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    line = {"metric": "HCA compressor GB/s (algorithmic bytes) fwd and bwd", "unit": "GB/s",
+            "value": round(fwd_bytes / f_ms / 1e6, 1), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"compressor B{B} S{S} D{D} m{m}"},
+            "fwd": {"ms": round(f_ms, 4), "bytes": fwd_bytes, "gbs": round(fwd_bytes / f_ms / 1e6, 1),
+                    "frac_hbm": round(fwd_bytes / f_ms / 1e6 / hbm, 4)},
+            "bwd": {"ms": round(b_ms, 4), "bytes": bwd_bytes, "gbs": round(bwd_bytes / b_ms / 1e6, 1),
+                    "frac_hbm": round(bwd_bytes / b_ms / 1e6 / hbm, 4)},
+            "peak_hbm_gbs": hbm, "peak_source": f"{src} hbm_gbs"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_indexer(args):
+    """Lightning Indexer scores + top-k on the CSA shape: S = 65536, m = 4
+    (16384 compressed entries), 64 index heads of dim 128, k = 512."""
+    import torch
+    from block_sparse_compressed_gb300 import hca
+    from block_sparse_compressed_gb300 import inputs as I
+    B, S, Hi, m, k = 1, 65536, 64, 4, 512
+    dev = torch.device("cuda", 0)
+    Sc = S // m
+    qi = I.normal((B, S, Hi, 128), 1, torch.bfloat16, dev)
+    ki = I.normal((B, Sc, 128), 2, torch.bfloat16, dev)
+    w = I.normal((B, S, Hi), 3, torch.float32, dev)
+    ws = torch.empty(hca.load().hca_indexer_workspace_size(B, S, m), dtype=torch.uint8, device=dev)
+    hca.hca_profile_enable(True)
+    ms = _time_cuda(lambda: hca.hca_indexer_topk(qi, ki, w, None, m, k, ws=ws), args.steps, args.warmup)
+    prof = hca.hca_profile_read()
+    hca.hca_profile_enable(False)
+    # visible (query, entry) pairs: entry j is complete at query (j+1)m-1
+    q_, r_ = divmod(S, m)
+    pairs = m * q_ * (q_ - 1) // 2 + q_ * (r_ + 1)
+    flops_def = 2 * Hi * 128 * pairs   # the per-head definition
+    flops_gemm = 2 * 128 * pairs       # after collapsing the heads (what the GEMM executes on visible pairs)
+    line = {"metric": "Lightning Indexer scores + top-k, ms per call", "unit": "ms", "value": round(ms, 4),
+            "higher_is_better": False, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"indexer B{B} S{S} Hi{Hi} Di128 m{m} k{k}"},
+            "visible_pairs": pairs, "definition_tflops": round(flops_def / ms / 1e9, 2),
+            "collapsed_gemm_tflops": round(flops_gemm / ms / 1e9, 2),
+            "kernels": {kk: {"launches": n, "ms_total": round(t, 4)} for kk, (n, t) in prof.items() if n}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_ncu_case(args):
     import torch
     from block_sparse_compressed_gb300 import hca
@@ -577,6 +662,10 @@ def main(argv=None):
         return run_reference(args)
     if args.mode == "local":
         return run_local(args)
+    if args.mode == "compress":
+        return run_compress(args)
+    if args.mode == "indexer":
+        return run_indexer(args)
     return run_ours(args)
 
 

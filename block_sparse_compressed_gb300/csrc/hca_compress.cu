@@ -14,9 +14,9 @@
 //   dbias[r] = sum over (b, j) of dz_r   (fixed-order reduction: deterministic)
 //
 // One warp per window.  Lanes first hold the window's logits (32 positions at
-// a time), then D/32 columns each for the weighted row sum, so every row is
-// read as one coalesced 2*D- or 4*D-byte line.  HBM-bound: x is read once
-// (twice in the backward: forward weights and da), ckv / dx written once.
+// a time), then D/32 consecutive columns each (one vector load per row) for
+// the weighted row sum, several rows in flight per lane.  HBM-bound: x is
+// read once per pass, ckv / dx written once.
 #include <cuda_bf16.h>
 
 #include "hca_common.cuh"
@@ -26,7 +26,6 @@ namespace hca {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
-constexpr int kMaxCols = 8;  // D <= 256: 8 columns per lane
 
 template <typename T>
 __device__ __forceinline__ float ldf(const T *p);
@@ -40,6 +39,42 @@ template <>
 __device__ __forceinline__ void stf<float>(float *p, float v) { *p = v; }
 template <>
 __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+
+// NC consecutive columns of a row per lane: one vector load / store.
+template <typename T, int NC>
+__device__ __forceinline__ void load_cols(const T *row, int lane, float (&v)[NC]) {
+  if constexpr (sizeof(T) == 4) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) v[c] = row[NC * lane + c];
+  } else {
+    const uint16_t *h = reinterpret_cast<const uint16_t *>(row) + NC * lane;
+    if constexpr (NC == 1) {
+      v[0] = __uint_as_float((uint32_t)h[0] << 16);
+    } else if constexpr (NC == 2) {
+      const uint32_t u = *reinterpret_cast<const uint32_t *>(h);
+      v[0] = __uint_as_float(u << 16);
+      v[1] = __uint_as_float(u & 0xffff0000u);
+    } else if constexpr (NC == 4) {
+      const uint2 u = *reinterpret_cast<const uint2 *>(h);
+      v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xffff0000u);
+      v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xffff0000u);
+    } else {
+      const uint4 u = *reinterpret_cast<const uint4 *>(h);
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[2 * q] = __uint_as_float(w4[q] << 16);
+        v[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
+      }
+    }
+  }
+}
+
+template <typename T, int NC>
+__device__ __forceinline__ void store_cols(T *row, int lane, const float (&v)[NC]) {
+#pragma unroll
+  for (int c = 0; c < NC; ++c) stf(row + NC * lane + c, v[c]);
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -88,7 +123,7 @@ __device__ __forceinline__ float window_weight(const CompressArgs &a, int b, int
   return expf(a.g[(size_t)b * a.S + t] + a.bias[r] - mx) * inv;
 }
 
-template <typename T>
+template <typename T, int NC>
 __global__ void __launch_bounds__(32 * kWarpsPerBlock) hca_compress_fwd_kernel(const CompressArgs a) {
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -97,32 +132,46 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) hca_compress_fwd_kernel(c
   float mx, sum;
   window_stats(a, b, j, lane, mx, sum);
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
-  const int nc = a.D / 32;  // columns per lane (D is a multiple of 32 here)
-  float acc[kMaxCols];
+  float acc[NC];
 #pragma unroll
-  for (int c = 0; c < kMaxCols; ++c) acc[c] = 0.f;
+  for (int c = 0; c < NC; ++c) acc[c] = 0.f;
   const T *x = static_cast<const T *>(a.x);
   if (sum > 0.f) {
     for (int r0 = 0; r0 < a.m; r0 += 32) {
       const float my = r0 + lane < a.m ? window_weight(a, b, j, r0 + lane, mx, inv) : 0.f;
-      const int rn = min(32, a.m - r0);
-      for (int rr = 0; rr < rn; ++rr) {
-        const float wr = __shfl_sync(0xffffffffu, my, rr);
-        if (wr == 0.f) continue;  // warp-uniform
-        const T *row = x + ((size_t)b * a.S + j * a.m + r0 + rr) * a.D;
+      const int rn = min(32, min(a.m - r0, a.S - (j * a.m + r0)));
+      const T *rows = x + ((size_t)b * a.S + j * a.m + r0) * a.D;
+      // eight rows in flight per lane
+      int rr = 0;
+      for (; rr + 8 <= rn; rr += 8) {
+        float v[8][NC];
 #pragma unroll
-        for (int c = 0; c < kMaxCols; ++c)
-          if (c < nc) acc[c] = fmaf(wr, ldf(row + lane + 32 * c), acc[c]);
+        for (int u = 0; u < 8; ++u) load_cols<T, NC>(rows + (size_t)(rr + u) * a.D, lane, v[u]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          // padding rows (weight 0) are skipped, not multiplied: their values are arbitrary
+          const float wr = __shfl_sync(0xffffffffu, my, rr + u);
+          if (wr != 0.f) {
+#pragma unroll
+            for (int c = 0; c < NC; ++c) acc[c] = fmaf(wr, v[u][c], acc[c]);
+          }
+        }
+      }
+      for (; rr < rn; ++rr) {
+        float v[NC];
+        load_cols<T, NC>(rows + (size_t)rr * a.D, lane, v);
+        const float wr = __shfl_sync(0xffffffffu, my, rr);
+        if (wr != 0.f) {
+#pragma unroll
+          for (int c = 0; c < NC; ++c) acc[c] = fmaf(wr, v[c], acc[c]);
+        }
       }
     }
   }
-  T *out = static_cast<T *>(a.ckv) + ((size_t)b * a.Sc + j) * a.D;
-#pragma unroll
-  for (int c = 0; c < kMaxCols; ++c)
-    if (c < nc) stf(out + lane + 32 * c, acc[c]);
+  store_cols<T, NC>(static_cast<T *>(a.ckv) + ((size_t)b * a.Sc + j) * a.D, lane, acc);
 }
 
-template <typename T>
+template <typename T, int NC>
 __global__ void __launch_bounds__(32 * kWarpsPerBlock) hca_compress_bwd_kernel(const CompressArgs a) {
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -131,40 +180,60 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) hca_compress_bwd_kernel(c
   float mx, sum;
   window_stats(a, b, j, lane, mx, sum);
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
-  const int nc = a.D / 32;
   const T *x = static_cast<const T *>(a.x);
-  const T *dck = static_cast<const T *>(a.dckv) + ((size_t)b * a.Sc + j) * a.D;
   T *dx = static_cast<T *>(a.dx);
-  float gv[kMaxCols];
-#pragma unroll
-  for (int c = 0; c < kMaxCols; ++c) gv[c] = c < nc ? ldf(dck + lane + 32 * c) : 0.f;
-  // pass 1: da_r = <dckv, x_r> and s = sum_r a_r da_r; dx_r = a_r dckv
+  float gv[NC];
+  load_cols<T, NC>(static_cast<const T *>(a.dckv) + ((size_t)b * a.Sc + j) * a.D, lane, gv);
+  // pass 1: da_r = <dckv, x_r>, s = sum_r a_r da_r, dx_r = a_r dckv
   float s = 0.f;
   for (int r0 = 0; r0 < a.m; r0 += 32) {
     const float my = r0 + lane < a.m && sum > 0.f ? window_weight(a, b, j, r0 + lane, mx, inv) : 0.f;
     float my_da = 0.f;
-    const int rn = min(32, a.m - r0);
-    for (int rr = 0; rr < rn; ++rr) {
-      const int t = j * a.m + r0 + rr;
-      if (t >= a.S) break;
+    const int rn = max(0, min(32, min(a.m - r0, a.S - (j * a.m + r0))));
+    const size_t base = (size_t)b * a.S + j * a.m + r0;
+    int rr = 0;
+    for (; rr + 4 <= rn; rr += 4) {
+      float v[4][NC], d[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) load_cols<T, NC>(x + (base + rr + u) * a.D, lane, v[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float wr = __shfl_sync(0xffffffffu, my, rr + u);
+        float o[NC];
+        d[u] = 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          d[u] = fmaf(gv[c], v[u][c], d[u]);
+          o[c] = wr * gv[c];
+        }
+        store_cols<T, NC>(dx + (base + rr + u) * a.D, lane, o);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float t = warp_sum(d[u]);
+        if (lane == rr + u) my_da = t;
+      }
+    }
+    for (; rr < rn; ++rr) {
+      float v[NC], o[NC];
+      load_cols<T, NC>(x + (base + rr) * a.D, lane, v);
       const float wr = __shfl_sync(0xffffffffu, my, rr);
-      const T *row = x + ((size_t)b * a.S + t) * a.D;
-      T *drow = dx + ((size_t)b * a.S + t) * a.D;
       float d = 0.f;
 #pragma unroll
-      for (int c = 0; c < kMaxCols; ++c)
-        if (c < nc) {
-          d = fmaf(gv[c], ldf(row + lane + 32 * c), d);
-          stf(drow + lane + 32 * c, wr * gv[c]);
-        }
+      for (int c = 0; c < NC; ++c) {
+        d = fmaf(gv[c], v[c], d);
+        o[c] = wr * gv[c];
+      }
+      store_cols<T, NC>(dx + (base + rr) * a.D, lane, o);
       d = warp_sum(d);
       if (lane == rr) my_da = d;
     }
+    // positions without weight (padding) hold arbitrary values: their da is dropped
+    if (my == 0.f) my_da = 0.f;
     s += warp_sum(my * my_da);
-    // keep this chunk's (a_r, da_r) for pass 2 in the logit-gradient buffer
+    // this chunk's da_r, kept for pass 2 in the logit-gradient buffer
     if (r0 + lane < a.m) a.dz[w * a.m + r0 + lane] = my_da;
   }
-  __syncwarp();
   // pass 2: dz_r = a_r (da_r - s)
   for (int r = lane; r < a.m; r += 32) {
     const int t = j * a.m + r;
@@ -191,12 +260,32 @@ __global__ void __launch_bounds__(256) hca_compress_dbias_kernel(const float *dz
   if (threadIdx.x == 0) dbias[r] = part[0];
 }
 
-template <typename T>
-cudaError_t launch_fwd(const CompressArgs &a, cudaStream_t st) {
+template <typename T, int NC>
+cudaError_t launch_fwd_nc(const CompressArgs &a, cudaStream_t st) {
   const long long nwin = (long long)a.B * a.Sc;
   if (nwin == 0) return cudaSuccess;
   ProfScope prof(kKCompress, st);
-  hca_compress_fwd_kernel<T><<<(unsigned)((nwin + kWarpsPerBlock - 1) / kWarpsPerBlock), 32 * kWarpsPerBlock, 0, st>>>(a);
+  hca_compress_fwd_kernel<T, NC><<<(unsigned)((nwin + kWarpsPerBlock - 1) / kWarpsPerBlock), 32 * kWarpsPerBlock, 0,
+                                   st>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_fwd(const CompressArgs &a, cudaStream_t st) {
+  switch (a.D / 32) {
+    case 1: return launch_fwd_nc<T, 1>(a, st);
+    case 2: return launch_fwd_nc<T, 2>(a, st);
+    case 4: return launch_fwd_nc<T, 4>(a, st);
+    case 8: return launch_fwd_nc<T, 8>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T, int NC>
+cudaError_t launch_bwd_nc(const CompressArgs &a, cudaStream_t st) {
+  const long long nwin = (long long)a.B * a.Sc;
+  hca_compress_bwd_kernel<T, NC><<<(unsigned)((nwin + kWarpsPerBlock - 1) / kWarpsPerBlock), 32 * kWarpsPerBlock, 0,
+                                   st>>>(a);
   return cudaGetLastError();
 }
 
@@ -205,7 +294,15 @@ cudaError_t launch_bwd(const CompressArgs &a, float *dbias, cudaStream_t st) {
   const long long nwin = (long long)a.B * a.Sc;
   if (nwin == 0) return cudaMemsetAsync(dbias, 0, sizeof(float) * a.m, st);
   ProfScope prof(kKCompress, st);
-  hca_compress_bwd_kernel<T><<<(unsigned)((nwin + kWarpsPerBlock - 1) / kWarpsPerBlock), 32 * kWarpsPerBlock, 0, st>>>(a);
+  cudaError_t e0 = cudaErrorInvalidValue;
+  switch (a.D / 32) {
+    case 1: e0 = launch_bwd_nc<T, 1>(a, st); break;
+    case 2: e0 = launch_bwd_nc<T, 2>(a, st); break;
+    case 4: e0 = launch_bwd_nc<T, 4>(a, st); break;
+    case 8: e0 = launch_bwd_nc<T, 8>(a, st); break;
+    default: break;
+  }
+  if (e0 != cudaSuccess) return e0;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   hca_compress_dbias_kernel<<<a.m, 256, 0, st>>>(a.dz, nwin, a.m, dbias);

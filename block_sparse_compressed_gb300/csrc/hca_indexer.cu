@@ -412,7 +412,7 @@ cudaError_t indexer_topk(const IndexerArgs &a, cudaStream_t st) {
   static SmemAttrOnce attr_s, attr_t;
   const int topk_smem = ld * (int)sizeof(uint32_t);
   cudaError_t e = attr_s.ensure(reinterpret_cast<const void *>(hca_index_score_kernel), isk::kSmemBytes);
-  if (e == cudaSuccess) e = attr_t.ensure(reinterpret_cast<const void *>(hca_index_topk_kernel), 227 * 1024);
+  if (e == cudaSuccess) e = attr_t.ensure(reinterpret_cast<const void *>(hca_index_topk_kernel), 57344 * (int)sizeof(uint32_t));
   if (e != cudaSuccess) return e;
   for (int row0 = 0; row0 < a.S; row0 += rows_chunk) {
     const int rows = min(rows_chunk, a.S - row0);

@@ -72,3 +72,24 @@ def test_compressor_feeds_the_attention():
     # checked above); out must match within the bf16 bound
     ro, _ = oracle.fwd(q, x, ckv.cpu(), None, W, m, 1 / math.sqrt(D))
     assert_close("out", out, ro, torch.bfloat16)
+
+
+def test_compressor_ignores_values_at_padding():
+    # padding positions may hold anything (here NaN); they must not leak into
+    # any output of the forward or the backward
+    B, S, D, m = 1, 300, 128, 16
+    x, g, bias, dck = _inputs(B, S, D, m, torch.bfloat16, 12)
+    seg = I.segments_from_lengths([120, 130], S, pad=50)
+    xn = x.clone()
+    xn[0, 250:] = float("nan")
+    gn = g.clone()
+    gn[0, 250:] = float("nan")
+    gd = [t.to(DEV) for t in (xn, gn, bias, seg, dck)]
+    ckv = hca.hca_compress_fwd(gd[0], gd[1], gd[2], gd[3], m)
+    dx, dg, db = hca.hca_compress_bwd(gd[0], gd[1], gd[2], gd[3], m, gd[4])
+    torch.cuda.synchronize()
+    assert_close("ckv", ckv, CI.compress_fwd(x, g, bias, seg, m), torch.bfloat16)
+    rdx, rdg, rdb = CI.compress_bwd(x, g, bias, seg, m, dck)
+    assert_close("dx", dx, rdx, torch.bfloat16)
+    assert_close("dg", dg, rdg, torch.bfloat16)
+    assert_close("dbias", db, rdb, torch.bfloat16)
