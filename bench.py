@@ -64,10 +64,11 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
-    ap.add_argument("--mode", choices=("hca", "local", "compress", "indexer"), default="hca",
+    ap.add_argument("--mode", choices=("hca", "local", "compress", "indexer", "csa"), default="hca",
                     help="local: the local sliding-window entry points (no compressed set) on the same shape; "
                          "compress: the HCA compressor (m=128) and its backward; indexer: the Lightning Indexer "
-                         "scores + top-k on the CSA shape (m=4)")
+                         "scores + top-k on the CSA shape (m=4); csa: compressed sparse attention fwd+bwd "
+                         "(m=4, k=256 selected entries per query)")
     ap.add_argument("--ncu-case", type=int, default=0, metavar="S",
                     help="profiling case: run --warmup + 1 untimed fwd+bwd steps of the headline shape at sequence "
                          "length S and exit (for ncu captures; prints nothing to time)")
@@ -638,6 +639,67 @@ def run_indexer(args):
     return 0
 
 
+def run_csa(args):
+    """Compressed sparse attention forward + backward: B=1, H=64, S=65536,
+    D=128, W=128, m=4 (16384 compressed entries), k=256 selected entries per
+    query (uniform random among the completed ones, with repeats and
+    padding: the indexer's output on random inputs has no locality either).
+    FLOPs over visible pairs as the HCA metric (4*D fwd, 10*D bwd per pair
+    and head)."""
+    import torch
+    from block_sparse_compressed_gb300 import hca
+    from block_sparse_compressed_gb300 import inputs as I
+    B, H, S, D, W, m, k = 1, 64, 65536, 128, 128, 4, 256
+    dev = torch.device("cuda", 0)
+    w = I.Workload(f"csa fwd+bwd bf16 B{B} H{H} S{S} D{D} W{W} m{m} k{k}", B, H, S, D, W, m, torch.bfloat16)
+    q, kv, ckv, seg, dout = I.tensors(w, device=dev)
+    sel = I.random_selection(B, S, m, k, 77, extra=0).to(dev)
+    # visible pairs per head: raw window + distinct selected entries that are complete
+    i = torch.arange(S, device=dev)
+    srt = torch.sort(sel[0].long(), dim=1).values
+    valid = (srt >= 0) & (srt <= ((i + 1) // m - 1)[:, None])
+    first = torch.ones_like(valid)
+    first[:, 1:] = srt[:, 1:] != srt[:, :-1]
+    comp_pairs = int((valid & first).sum().item())
+    raw_pairs, _ = visible_pairs_closed_form(S, W, m)
+    pairs = (raw_pairs + comp_pairs) * H
+    out = torch.empty_like(q)
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=dev)
+    dq, dkv, dckv = torch.empty_like(q), torch.empty_like(kv), torch.empty_like(ckv)
+    wsf = hca.csa_workspace(B, H, S, D, W, m, k, torch.bfloat16, False, dev)
+    wsb = hca.csa_workspace(B, H, S, D, W, m, k, torch.bfloat16, True, dev)
+
+    def fwd():
+        hca.hca_csa_attn_fwd(q, kv, ckv, None, sel, W, m, w.scale, out=out, lse=lse, ws=wsf)
+
+    def bwd():
+        hca.hca_csa_attn_bwd(q, kv, ckv, None, sel, out, lse, dout, W, m, w.scale, dq=dq, dkv=dkv, dckv=dckv, ws=wsb)
+
+    fwd()
+    bwd()
+    if hca.hca_workspace_status(wsf) != 0 or hca.hca_workspace_status(wsb) != 0:
+        raise RuntimeError("device reported an error status")
+    hca.hca_profile_enable(True)
+    f_ms = _time_cuda(fwd, args.steps, args.warmup)
+    b_ms = _time_cuda(bwd, args.steps, args.warmup)
+    prof = hca.hca_profile_read()
+    hca.hca_profile_enable(False)
+    peaks, src = load_peaks()
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    ff, fb = 4 * D * pairs, 10 * D * pairs
+    line = {"metric": "CSA attn fwd+bwd TFLOP/s (visible pairs) at S=65536", "unit": "TFLOP/s",
+            "value": round((ff + fb) / ((f_ms + b_ms) * 1e-3) / 1e12, 3), "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": w.name, "selected_pairs_per_head": comp_pairs,
+                                            "raw_pairs_per_head": raw_pairs},
+            "fwd": {"ms": round(f_ms, 4), "tflops": round(ff / f_ms / 1e9, 2),
+                    "pct_bf16_peak": round(100 * ff / f_ms / 1e9 / burst, 2)},
+            "bwd": {"ms": round(b_ms, 4), "tflops": round(fb / b_ms / 1e9, 2),
+                    "pct_bf16_peak": round(100 * fb / b_ms / 1e9 / burst, 2)},
+            "kernels": {kk: {"launches": n, "ms_total": round(t, 4)} for kk, (n, t) in prof.items() if n}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_ncu_case(args):
     import torch
     from block_sparse_compressed_gb300 import hca
@@ -666,6 +728,8 @@ def main(argv=None):
         return run_compress(args)
     if args.mode == "indexer":
         return run_indexer(args)
+    if args.mode == "csa":
+        return run_csa(args)
     return run_ours(args)
 
 

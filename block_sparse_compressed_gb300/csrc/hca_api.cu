@@ -34,10 +34,20 @@ int check_dims(int B, int H, int S, int D, int W, int m, int dtype) {
 
 size_t fwd_ws_bytes(int B, int S) { return kHeaderBytes + align_up((size_t)B * S * sizeof(int32_t)); }
 
-size_t bwd_ws_bytes(int B, int H, int S, int D, int W, int m, int dtype) {
+size_t bwd_ws_bytes(int B, int H, int S, int D, int W, int m, int dtype, bool csa = false) {
   size_t n = fwd_ws_bytes(B, S) + align_up((size_t)B * H * S * sizeof(float));
-  n += tc_bwd_scratch_bytes(B, H, S, D, W, m, dtype);
+  n += tc_bwd_scratch_bytes(B, H, S, D, W, m, dtype, csa);
   return n;
+}
+
+// CSA workspace: the attention's, then the union of selections (per forward
+// pair of 2*Pq positions, or per dq tile of Pq), then (backward) the fp32
+// dckv accumulator.
+int csa_pq(int H) { return tc_query_tile_positions(H); }
+size_t csa_fwd_ws_bytes(int B, int H, int S, int k) { return fwd_ws_bytes(B, S) + csa_union_bytes(B, S, 2 * csa_pq(H), k); }
+size_t csa_bwd_ws_bytes(int B, int H, int S, int D, int W, int m, int k) {
+  return bwd_ws_bytes(B, H, S, D, W, m, HCA_BF16, true) + csa_union_bytes(B, S, csa_pq(H), k) +
+         csa_dckv_acc_bytes(B, (S + m - 1) / m);
 }
 
 struct Carve {
@@ -186,7 +196,7 @@ int hca_indexer_topk(const void *qi, const void *ki, const float *w, const int32
   if (m < 1 || k < 1) return HCA_ERR_ARG;
   if (Di != 128) return HCA_ERR_UNSUPPORTED;
   const long long Sc = ((long long)S + m - 1) / m;
-  if (Sc > 57344) return HCA_ERR_UNSUPPORTED;
+  if (Sc > (long long)indexer_max_entries()) return HCA_ERR_UNSUPPORTED;
   if (B * (long long)S == 0) return HCA_OK;
   if (!qi || !ki || !w || !sel) return HCA_ERR_NULL;
   if (!aligned16(qi) || !aligned16(ki) || (seg && !aligned16(seg))) return HCA_ERR_ALIGN;
@@ -285,6 +295,94 @@ int hca_attn_bwd(const void *q, const void *kv, const void *ckv, const int32_t *
     return cuda_status(tc_bwd(a, st));
   }
   return cuda_status(simt_bwd(a, st));
+}
+
+size_t hca_csa_workspace_size(int B, int H, int S, int D, int W, int m, int k, int dtype, int for_backward) {
+  if (check_dims(B, H, S, D, W, m, dtype) != HCA_OK || k < 1) return 0;
+  if (dtype != HCA_BF16 || !tc_fwd_supported(H, D, dtype) || !csa_shape_ok(H, k)) return 0;
+  return for_backward ? csa_bwd_ws_bytes(B, H, S, D, W, m, k) : csa_fwd_ws_bytes(B, H, S, k);
+}
+
+static int csa_checks(int B, int H, int S, int D, int W, int m, int k, float scale, int dtype) {
+  int rc = check_dims(B, H, S, D, W, m, dtype);
+  if (rc != HCA_OK) return rc;
+  if (!std::isfinite(scale) || k < 1) return HCA_ERR_ARG;
+  // CSA runs on the tensor-core kernels only (bf16, D = 128, H a multiple of 32)
+  if (dtype != HCA_BF16 || !tc_fwd_supported(H, D, dtype) || !csa_shape_ok(H, k)) return HCA_ERR_UNSUPPORTED;
+  return HCA_OK;
+}
+
+int hca_csa_attn_fwd(const void *q, const void *kv, const void *ckv, const int32_t *seg, const int32_t *sel,
+                     void *out, float *lse, int B, int H, int S, int D, int W, int m, int k, float scale, int dtype,
+                     void *workspace, size_t workspace_bytes, void *stream) {
+  int rc = csa_checks(B, H, S, D, W, m, k, scale, dtype);
+  if (rc != HCA_OK) return rc;
+  if (B * (long long)S == 0) return HCA_OK;
+  if (!q || !kv || !ckv || !sel || !out || !lse) return HCA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(ckv) || !aligned16(out) || !aligned16(lse) ||
+      (seg && !aligned16(seg)) || !aligned16(sel))
+    return HCA_ERR_ALIGN;
+  rc = check_ws(workspace, workspace_bytes, csa_fwd_ws_bytes(B, H, S, k));
+  if (rc != HCA_OK) return rc;
+  if (take_launch_failure()) return HCA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carve c = carve_fwd(workspace, B, S);
+  rc = cuda_status(launch_prep(seg, B, S, c.sstart, c.status, st));
+  if (rc != HCA_OK) return rc;
+  CsaUnion u;
+  rc = cuda_status(csa_build_union(sel, seg ? c.sstart : nullptr, B, S, m, k, 2 * csa_pq(H), u,
+                                   c.p + fwd_ws_bytes(B, S), st));
+  if (rc != HCA_OK) return rc;
+  FwdArgs a;
+  a.q = q; a.kv = kv; a.ckv = ckv;
+  a.sstart = seg ? c.sstart : nullptr;
+  a.status = c.status; a.status_rw = c.status;
+  a.out = out; a.lse = lse;
+  a.B = B; a.H = H; a.S = S; a.D = D; a.W = W; a.m = m; a.scale = scale; a.dtype = dtype;
+  a.wait_ns = wait_limit_ns();
+  a.stall = take_stall_mask() & HCA_STALL_FWD;
+  return cuda_status(tc_fwd(a, st, &u));
+}
+
+int hca_csa_attn_bwd(const void *q, const void *kv, const void *ckv, const int32_t *seg, const int32_t *sel,
+                     const void *out, const float *lse, const void *dout, void *dq, void *dkv, void *dckv, int B,
+                     int H, int S, int D, int W, int m, int k, float scale, int dtype, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+  int rc = csa_checks(B, H, S, D, W, m, k, scale, dtype);
+  if (rc != HCA_OK) return rc;
+  if (B * (long long)S == 0) return HCA_OK;
+  if (!q || !kv || !ckv || !sel || !out || !lse || !dout || !dq || !dkv || !dckv) return HCA_ERR_NULL;
+  const void *ptrs[] = {q, kv, ckv, sel, out, lse, dout, dq, dkv, dckv};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return HCA_ERR_ALIGN;
+  if (seg && !aligned16(seg)) return HCA_ERR_ALIGN;
+  rc = check_ws(workspace, workspace_bytes, csa_bwd_ws_bytes(B, H, S, D, W, m, k));
+  if (rc != HCA_OK) return rc;
+  if (take_launch_failure()) return HCA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carve c = carve_fwd(workspace, B, S);
+  rc = cuda_status(launch_prep(seg, B, S, c.sstart, c.status, st));
+  if (rc != HCA_OK) return rc;
+  char *p = c.p + fwd_ws_bytes(B, S);
+  BwdArgs a;
+  a.q = q; a.kv = kv; a.ckv = ckv; a.out = out; a.dout = dout; a.lse = lse;
+  a.sstart = seg ? c.sstart : nullptr;
+  a.status = c.status; a.status_rw = c.status;
+  a.dq = dq; a.dkv = dkv; a.dckv = dckv;
+  a.delta = reinterpret_cast<float *>(p);
+  p += align_up((size_t)B * H * S * sizeof(float));
+  a.scratch = p;
+  a.scratch_bytes = tc_bwd_scratch_bytes(B, H, S, D, W, m, dtype, true);
+  p += a.scratch_bytes;
+  a.B = B; a.H = H; a.S = S; a.D = D; a.W = W; a.m = m; a.scale = scale; a.dtype = dtype;
+  a.wait_ns = wait_limit_ns();
+  a.stall = take_stall_mask() & (HCA_STALL_DQ | HCA_STALL_DKV);
+  CsaBwd cb;
+  rc = cuda_status(csa_build_union(sel, a.sstart, B, S, m, k, csa_pq(H), cb.u, p, st));
+  if (rc != HCA_OK) return rc;
+  p += csa_union_bytes(B, S, csa_pq(H), k);
+  cb.acc = reinterpret_cast<float *>(p);
+  return cuda_status(tc_bwd(a, st, &cb));
 }
 
 // Local sliding attention: the HCA calls with a compression ratio larger

@@ -62,12 +62,18 @@ constexpr int kOffQ = 0, kOffDO = kTile, kOffO = 2 * kTile, kOffKV = 3 * kTile;
 constexpr int kOffOut = kOffKV + kStages * kTile;
 constexpr int kSmemBytes = kOffOut + kTile + 1024;
 constexpr int kDescSlots = 8;
-constexpr int kDescReaders = 11;  // dS warps 0-7, MMA warp 9, Delta warps 10-11
+constexpr int kDescReaders = 11;  // dS warps 0-7, MMA warp 9, Delta warps 10-11 (CSA: gather warp 10, Delta warp 11)
 constexpr int kDeltaThreads = 64;
+constexpr int kCsaMaxPos = 4;     // CSA: positions per tile whose bits are kept (Pq <= 4)
 }  // namespace dqk
 
 struct DqParams {
   QTiling qt;
+  // CSA: per tile, the union of its positions' selected entries (hca_csa.cu)
+  const int32_t *u_cnt, *u_ent;
+  const uint32_t *u_mask;
+  int u_cap;
+  const __nv_bfloat16 *ckv;
   int32_t *status;
   const float *lse;
   float *rowstat;            // [ntiles][2][128]: -lse*log2e, then -scale*Delta, per tile row
@@ -95,6 +101,7 @@ struct DqBars {
   uint64_t epi, drain, never;
   DqDesc desc[dqk::kDescSlots];
   float delta[kRows];
+  uint32_t vis[dqk::kStages][dqk::kCsaMaxPos][4];  // CSA: per block, each position's bits of the compressed columns
   uint32_t tmem_base;
   int abort;
 };
@@ -119,6 +126,7 @@ __device__ __forceinline__ bool read_dq_desc(DqBars &bars, uint32_t kd, Tile &t,
   return true;
 }
 
+template <bool kCsa>
 __global__ void __launch_bounds__(dqk::kThreads, 1)
     hca_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                       const __grid_constant__ CUtensorMap map_out,
@@ -137,9 +145,10 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
     mbar_init(&bars.qd_full, 1);
     // released by the last S/dP MMA of a tile and by every Delta thread once
     // it has read the staged dO and out tiles
-    mbar_init(&bars.qd_empty, 1 + kDeltaThreads);
+    mbar_init(&bars.qd_empty, 1 + (kCsa ? 32 : kDeltaThreads));
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars.kv_full[s], 1);
+      // CSA: the gather warp also arrives once its rows have landed
+      mbar_init(&bars.kv_full[s], kCsa ? 1 + 32 : 1);
       mbar_init(&bars.kv_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
@@ -147,7 +156,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.ds_full, kEW);
     mbar_init(&bars.dq_done, 1);
-    mbar_init(&bars.stat_full, kDeltaThreads);
+    mbar_init(&bars.stat_full, kCsa ? 32 : kDeltaThreads);
     mbar_init(&bars.stat_empty, kEW);
     for (int s = 0; s < kDescSlots; ++s) {
       mbar_init(&bars.desc_full[s], 32);
@@ -189,6 +198,15 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         if (!end) {
           tile_coords(Q, u, t);
           tile_ranges_warp(Q, t, lane);
+          if (kCsa) {
+            // compressed columns: the tile's union of selected entries
+            const int cnt = p.u_cnt[(long long)t.b * Q.ntq + t.i0 / Q.Pq];
+            t.clo = 0;
+            t.chi = cnt;
+            t.cpad = (cnt + 15) & ~15;
+            t.ncols = t.cpad + (t.rhi - t.rlo);
+            t.nb = (t.ncols + kBlockKeys - 1) / kBlockKeys;
+          }
         }
         const int slot = k % kDescSlots;
         if (k >= (uint32_t)kDescSlots &&
@@ -242,9 +260,15 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
             if (!ok) break;
             int n, nc;
             block_cols(t, j, n, nc);
-            mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes(n, nc));
-            load_block(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
-                       smem + kOffKV + s * kTile);
+            if (kCsa) {
+              // raw rows only: the gather warp brings the compressed ones
+              mbar_arrive_expect_tx(&bars.kv_full[s], nc == n ? 0u : raw_load_bytes(n, nc));
+              if (nc < n) load_block_raw(t, j, n, nc, &map_kv, &map_kv16, &bars.kv_full[s], smem + kOffKV + s * kTile);
+            } else {
+              mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes(n, nc));
+              load_block(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
+                         smem + kOffKV + s * kTile);
+            }
             last_par[s] = (gb / kStages) & 1;
           }
         }
@@ -359,13 +383,46 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         if (lane == 0) mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
         __syncwarp();
       }
+    } else if (kCsa && warp == kEW / 32 + 2) {
+      // ------------------------------------------------------------ CSA gather
+      // The compressed columns of every block are the tile's union of
+      // selected entries: their ckv rows go into the key tile in the swizzled
+      // layout the TMA gives the raw rows, each position's bits for them to
+      // shared memory, then the warp joins the block's kv_full arrival.
+      uint32_t gb = 0, kd = 0;
+      bool ok = true;
+      while (ok) {
+        Tile t;
+        long long u;
+        ok = read_dq_desc(bars, kd++, t, u, abort_flag, p.status, p.wait_ns);
+        if (!ok || u < 0) break;
+        if (poisoned || t.nb == 0) continue;
+        const long long grp = (long long)t.b * Q.ntq + t.i0 / Q.Pq;
+        const int32_t *ent = p.u_ent + grp * p.u_cap;
+        const uint32_t *msk = p.u_mask + grp * p.u_cap;
+        const __nv_bfloat16 *ckv_b = p.ckv + (size_t)t.b * Q.Sc * kHeadDim;
+        for (int j = 0; ok && j < t.nb; ++j, ++gb) {
+          const int s = gb % kStages;
+          if (gb >= (uint32_t)kStages)
+            ok = wait_warp(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
+          if (!ok) break;
+          int n, nc;
+          block_cols(t, j, n, nc);
+          gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, 0, 1, Q.Pq, 0, 4,
+                       &bars.vis[s][0][0], lane);
+          cp_async_wait_all();
+          fence_async_smem();
+          mbar_arrive(&bars.kv_full[s]);
+        }
+      }
     } else {
       // ------------------------------------------------------------ Delta
       // Delta = <dO, out> of every tile row from the staged dO and out tiles
-      // (two warps, 64 rows each, two rows per lane), off the dS warps'
-      // critical path; published in shared memory and, as -scale*Delta, in
-      // the row records the dkv kernel reads.
-      const int dt = tid - (kEW + 64);  // 0..63
+      // (two warps, 64 rows each, two rows per lane; CSA: one warp, four rows
+      // per lane), off the dS warps' critical path; published in shared
+      // memory and, as -scale*Delta, in the row records the dkv kernel reads.
+      constexpr int kRowsPerLane = kCsa ? 4 : 2;
+      const int dt = kCsa ? lane : tid - (kEW + 64);
       uint32_t tw = 0, kd = 0;
       bool ok = true;
       const uint8_t *dobuf = smem + kOffDO;
@@ -377,10 +434,11 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         if (!ok || u < 0) break;
         if (poisoned || t.nb == 0) continue;
         if (!wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
-        float dl[2] = {0.f, 0.f};
+        float dl[kRowsPerLane];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = dt + 64 * h;
+        for (int h = 0; h < kRowsPerLane; ++h) {
+          dl[h] = 0.f;
+          const int r = dt + (kRows / kRowsPerLane) * h;
 #pragma unroll 4
           for (int ch = 0; ch < 16; ++ch) {
             const uint4 ov = *reinterpret_cast<const uint4 *>(outbuf + sw128_offset(r, ch));
@@ -395,12 +453,12 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         }
         mbar_arrive(&bars.qd_empty);  // dO and out of this tile are read
         float *rs = p.rowstat + tile_linear(Q, t) * 2 * kRows;
-        rs[kRows + dt] = -p.scale * dl[0];
-        rs[kRows + dt + 64] = -p.scale * dl[1];
+#pragma unroll
+        for (int h = 0; h < kRowsPerLane; ++h) rs[kRows + dt + (kRows / kRowsPerLane) * h] = -p.scale * dl[h];
         // the dS warps have read the previous tile's Delta
         if (tw > 0 && !wait_warp(&bars.stat_empty, (tw - 1) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
-        bars.delta[dt] = dl[0];
-        bars.delta[dt + 64] = dl[1];
+#pragma unroll
+        for (int h = 0; h < kRowsPerLane; ++h) bars.delta[dt + (kRows / kRowsPerLane) * h] = dl[h];
         mbar_arrive(&bars.stat_full);
         ++tw;
       }
@@ -460,8 +518,15 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         // its raw range in the block
         int a1, b1, a2, b2;
         row_cols(t, iv, j, n, nc, a1, b1, a2, b2);
-        const uint64_t vis = range_mask64(a1, b1, cb) | range_mask64(a2, b2, cb);
+        uint64_t vis = kCsa ? range_mask64(a2, b2, cb) : (range_mask64(a1, b1, cb) | range_mask64(a2, b2, cb));
         if (!wait_warp(&bars.s_full, gb & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+        if (kCsa) {
+          // the block's key tile (with the gather warp's bits) has landed;
+          // this wait orders the bits' reads
+          const int s = gb % kStages;
+          if (!wait_warp(&bars.kv_full[s], (gb / kStages) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+          if (iv.valid) vis |= (uint64_t)bars.vis[s][pq][2 * wg] | ((uint64_t)bars.vis[s][pq][2 * wg + 1] << 32);
+        }
         tc_fence_after();
         // P = exp2(S * scale * log2e - lse * log2e), kept in registers so the
         // S columns can take the next block's scores right away
@@ -1187,11 +1252,12 @@ struct ReduceParams {
   const float *rpart, *cpart;
   __nv_bfloat16 *dkv, *dckv;
   int B, S, Sc, S_pad, Sc_pad, nslot, nrb, nkb_comp, raw_atomic;
+  int with_comp;  // 0: dkv only (CSA writes dckv itself)
 };
 
 __global__ void hca_bwd_reduce_kernel(const ReduceParams p) {
   const long long nraw4 = (long long)p.B * p.S * (kHeadDim / 4);
-  const long long ncomp4 = (long long)p.B * p.Sc * (kHeadDim / 4);
+  const long long ncomp4 = p.with_comp ? (long long)p.B * p.Sc * (kHeadDim / 4) : 0;
   for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nraw4 + ncomp4;
        v += (long long)gridDim.x * blockDim.x) {
     const bool comp = v >= nraw4;
@@ -1265,20 +1331,21 @@ size_t cpart_bytes(int B, int Sc) { return align_up((size_t)dkk::kSlotsComp * B 
 
 bool tc_bwd_supported(int H, int D, int dtype) { return tc_shape_ok(H, D, dtype); }
 
-size_t tc_bwd_scratch_bytes(int B, int H, int S, int D, int W, int m, int dtype) {
+size_t tc_bwd_scratch_bytes(int B, int H, int S, int D, int W, int m, int dtype, bool csa) {
   if (!tc_shape_ok(H, D, dtype)) return 0;
   QTiling q = make_qtiling(nullptr, B, H, S, W, m);
-  return rowstat_bytes(q) + cpart_bytes(B, q.Sc) + rpart_bytes(B, raw_geom(S, W));
+  // CSA keeps no compressed partial slots: its dckv is accumulated query-major
+  return rowstat_bytes(q) + (csa ? 0 : cpart_bytes(B, q.Sc)) + rpart_bytes(B, raw_geom(S, W));
 }
 
-cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
+cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st, const CsaBwd *csa) {
   const QTiling q = make_qtiling(a.sstart, a.B, a.H, a.S, a.W, a.m);
   const int Spad = sc_pad(q.Sc);
   const RawGeom rg = raw_geom(a.S, a.W);
   char *ws = static_cast<char *>(a.scratch);
   float *rowstat = reinterpret_cast<float *>(ws);
-  float *cpart = reinterpret_cast<float *>(ws + rowstat_bytes(q));
-  float *rpart = reinterpret_cast<float *>(ws + rowstat_bytes(q) + cpart_bytes(a.B, q.Sc));
+  float *cpart = csa ? nullptr : reinterpret_cast<float *>(ws + rowstat_bytes(q));
+  float *rpart = reinterpret_cast<float *>(ws + rowstat_bytes(q) + (csa ? 0 : cpart_bytes(a.B, q.Sc)));
   // dkv kernel: a 64-row half of a query tile is a head range when HG >= 2,
   // a position range when one head fills the tile
   const int sub_hg = q.HG >= 2 ? q.HG / 2 : 1;
@@ -1295,9 +1362,10 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
       !make_map_bf16(&mkv16, a.kv, kHeadDim, a.S, a.B, 16, 1) ||
       !make_map_bf16(&mckv16, a.ckv, kHeadDim, q.Sc, a.B, 16, 1))
     return cudaErrorInvalidValue;
-  static SmemAttrOnce attr_dq, attr_dkv;
+  auto dq_kern = csa ? hca_bwd_dq_kernel<true> : hca_bwd_dq_kernel<false>;
+  static SmemAttrOnce attr_dq[2], attr_dkv;
   {
-    cudaError_t e = attr_dq.ensure(reinterpret_cast<const void *>(hca_bwd_dq_kernel), dqk::kSmemBytes);
+    cudaError_t e = attr_dq[csa ? 1 : 0].ensure(reinterpret_cast<const void *>(dq_kern), dqk::kSmemBytes);
     if (e == cudaSuccess) e = attr_dkv.ensure(reinterpret_cast<const void *>(hca_bwd_dkv_kernel), dkk::kSmemBytes);
     if (e != cudaSuccess) return e;
   }
@@ -1307,6 +1375,11 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
 
   DqParams dp;
   dp.qt = q;
+  dp.u_cnt = csa ? csa->u.cnt : nullptr;
+  dp.u_ent = csa ? csa->u.ent : nullptr;
+  dp.u_mask = csa ? csa->u.mask : nullptr;
+  dp.u_cap = csa ? csa->u.cap : 0;
+  dp.ckv = static_cast<const __nv_bfloat16 *>(a.ckv);
   dp.status = a.status_rw;
   dp.lse = a.lse;
   dp.rowstat = rowstat;
@@ -1322,8 +1395,7 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   cudaError_t e;
   {
     ProfScope prof(kKBwdDq, st);
-    hca_bwd_dq_kernel<<<(unsigned)g1, dqk::kThreads, dqk::kSmemBytes, st>>>(mq, mdo, mout, mkv, mckv, mkv16, mckv16, mdq,
-                                                                            dp);
+    dq_kern<<<(unsigned)g1, dqk::kThreads, dqk::kSmemBytes, st>>>(mq, mdo, mout, mkv, mckv, mkv16, mckv16, mdq, dp);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;
@@ -1344,8 +1416,9 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   kp.raw_atomic = rg.atomic;
   kp.sub_pq = sub_pq;
   kp.sub_hg = sub_hg;
-  kp.n_both = (long long)a.B * (kp.nkb_comp / 2) * dkk::kSplitBoth;
-  kp.n_lead = (long long)a.B * ((kp.nkb_comp + 1) / 2) * dkk::kSplitLead;
+  // CSA: raw items only (its compressed entries are handled query-major)
+  kp.n_both = csa ? 0 : (long long)a.B * (kp.nkb_comp / 2) * dkk::kSplitBoth;
+  kp.n_lead = csa ? 0 : (long long)a.B * ((kp.nkb_comp + 1) / 2) * dkk::kSplitLead;
   kp.nitems = kp.n_both + kp.n_lead + (long long)a.B * rg.nrb * rg.npr;
   kp.sl2 = sl2;
   kp.scale = a.scale;
@@ -1376,7 +1449,8 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
   rp.nrb = rg.nrb;
   rp.nkb_comp = kp.nkb_comp;
   rp.raw_atomic = rg.atomic;
-  const long long n4 = (long long)a.B * (a.S + q.Sc) * (kHeadDim / 4);
+  rp.with_comp = csa ? 0 : 1;
+  const long long n4 = (long long)a.B * (a.S + (csa ? 0 : q.Sc)) * (kHeadDim / 4);
   if (n4 > 0) {
     int blocks = (int)((n4 + 255) / 256);
     if (blocks > 8 * sms) blocks = 8 * sms;
@@ -1384,7 +1458,8 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st) {
     hca_bwd_reduce_kernel<<<blocks, 256, 0, st>>>(rp);
     e = cudaGetLastError();
   }
-  return e;
+  if (e != cudaSuccess || !csa) return e;
+  return csa_dckv(a, csa->u, rowstat, csa->acc, st);
 }
 
 }  // namespace hca

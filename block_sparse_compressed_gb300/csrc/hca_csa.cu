@@ -1,0 +1,576 @@
+// hca_csa.cu -- compressed sparse attention (CSA): the HCA sets with the
+// compressed entries narrowed to the indexer's per-query top-k selection.
+//
+// "Add HCA Static Compilation for Splash Attention [Deepseek v4]",
+// Description: CSA (compress ratio 4) needs a top-k step and runtime indexer
+// masks that keep or discard (query, compressed entry) pairs; "DSV4: Route
+// compressed and sliding train attention onto the splash kernels" routes the
+// compressed attention the same way.  Query i attends, under one softmax, to
+// its raw window (as in HCA) and to the selected entries j in sel[b,i,:]
+// that HCA would let it see (window complete at i, inside i's document);
+// selections outside that set, repeats and -1 padding are ignored.
+//
+// This file holds the CSA-only parts:
+//   - csa_union_kernel: per group of P consecutive positions (a forward
+//     pair or a dq tile), the sorted set of entries any of them selected
+//     and may see, each with the bit mask of the positions that selected it.
+//     The attention kernels gather those ckv rows into their key blocks and
+//     mask each row by its position's bit.
+//   - hca_csa_dckv_kernel: dckv, query-major.  Per query tile and block of
+//     its union: S = Q K^T and dP = dO K^T (tcgen05, TMEM), P and scale*dS
+//     (bf16) into shared memory, then D = P^T dO + (scale dS)^T Q with both
+//     A operands read transposed (MN-major) from those tiles, and each
+//     entry's row of D added into an fp32 accumulator with float4 atomics
+//     (a random selection gives no key-major block structure to reduce in).
+//   - a finalize kernel: dckv = bf16(accumulator).
+// The raw-key gradients come from the HCA key-major kernel (raw items only).
+#include <cuda_bf16.h>
+
+#include "hca_common.cuh"
+#include "hca_internal.h"
+#include "tc_ptx.cuh"
+#include "tc_tiles.cuh"
+
+namespace hca {
+using namespace tc;
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// union of the selections of a group of positions
+// ---------------------------------------------------------------------------
+constexpr int kUnionThreads = 256;
+constexpr uint32_t kInvalidKey = 0xffffffffu;
+
+struct UnionArgs {
+  const int32_t *sel;     // [B,S,k]
+  const int32_t *sstart;  // NULL = one document
+  int32_t *cnt;           // [B*ngroups]
+  int32_t *ent;           // [B*ngroups][cap]
+  uint32_t *mask;         // [B*ngroups][cap]
+  int B, S, m, Sc, k, P, ngroups, cap, sortn;
+};
+
+__global__ void __launch_bounds__(kUnionThreads) csa_union_kernel(const UnionArgs a) {
+  extern __shared__ uint32_t keys[];
+  __shared__ int wsum[kUnionThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int g = blockIdx.x;
+  const int b = g / a.ngroups, pos0 = (g % a.ngroups) * a.P;
+  // key = entry * 32 + position in the group; invalid selections sort last
+  for (int t = tid; t < a.sortn; t += kUnionThreads) {
+    uint32_t key = kInvalidKey;
+    if (t < a.P * a.k) {
+      const int p = t / a.k, i = pos0 + p;
+      if (i < a.S) {
+        const int e = a.sel[((size_t)b * a.S + i) * a.k + t % a.k];
+        const RowIv iv = row_interval(a.sstart, b, a.S, i, 1, a.m);
+        if (iv.valid && e >= iv.clo && e <= iv.chi && e < a.Sc) key = ((uint32_t)e << 5) | (uint32_t)p;
+      }
+    }
+    keys[t] = key;
+  }
+  __syncthreads();
+  // bitonic sort, ascending
+  for (int size = 2; size <= a.sortn; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = tid; t < a.sortn / 2; t += kUnionThreads) {
+        const int lo = 2 * t - (t & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const uint32_t x = keys[lo], y = keys[hi];
+        if ((x > y) == up) {
+          keys[lo] = y;
+          keys[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // one output per run of equal entries, in order, with the OR of the
+  // positions' bits
+  const size_t base = (size_t)g * a.cap;
+  int out = 0;
+  for (int t0 = 0; t0 < a.sortn; t0 += kUnionThreads) {
+    const int t = t0 + tid;
+    const uint32_t key = t < a.sortn ? keys[t] : kInvalidKey;
+    const bool start = key != kInvalidKey && (t == 0 || (keys[t - 1] >> 5) != (key >> 5));
+    int x = start ? 1 : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[wid] = x;
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kUnionThreads / 32; ++w) {
+      if (w < wid) before += wsum[w];
+      total += wsum[w];
+    }
+    __syncthreads();
+    if (start) {
+      uint32_t msk = 0;
+      for (int u = t; u < a.sortn && keys[u] != kInvalidKey && (keys[u] >> 5) == (key >> 5); ++u)
+        msk |= 1u << (keys[u] & 31u);
+      const int pos = out + before + x - 1;
+      a.ent[base + pos] = (int32_t)(key >> 5);
+      a.mask[base + pos] = msk;
+    }
+    out += total;
+  }
+  // pad to a multiple of 16 with a loadable row that no position sees
+  const int padded = (out + 15) & ~15;
+  for (int t = out + tid; t < padded; t += kUnionThreads) {
+    a.ent[base + t] = 0;
+    a.mask[base + t] = 0u;
+  }
+  if (tid == 0) a.cnt[g] = out;
+}
+
+// ---------------------------------------------------------------------------
+// dckv, query-major
+// ---------------------------------------------------------------------------
+namespace ckk {
+constexpr int kStages = 2;
+constexpr int kEW = 256;                  // two warpgroups, 64 key columns each
+constexpr int kThreads = kEW + 128;       // + TMA warp, MMA warp, gather warp, idle warp
+constexpr int kRegEW = 192, kRegProducer = 120;
+static_assert(2 * 128 * kRegEW + 128 * kRegProducer <= kThreads * 168, "register split must fit the launch");
+constexpr uint32_t kColS = 0, kColDP = 128, kColD = 256;  // D: two 128-column buffers
+constexpr int kTmemCols = 512;
+constexpr int kOffQ = 0, kOffDO = kTile, kOffKV = 2 * kTile;
+constexpr int kOffP = kOffKV + kStages * kTile, kOffDS = kOffP + kTile;
+constexpr int kSmemBytes = kOffDS + kTile + 1024;
+constexpr int kMaxPos = 4;                // positions per tile (H a multiple of 32)
+constexpr int kGather = 32;               // gather threads
+}  // namespace ckk
+
+struct DckvParams {
+  QTiling qt;
+  const __nv_bfloat16 *ckv;
+  const float *rowstat;       // [ntiles][2][128] from the dq kernel
+  const int32_t *u_cnt, *u_ent;
+  const uint32_t *u_mask;
+  int u_cap;
+  float *acc;                 // [B][Sc][D] fp32
+  int32_t *status;
+  float sl2, scale;
+  int pq_shift;
+  uint64_t wait_ns;
+};
+
+struct DckvBars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[ckk::kStages], kv_empty[ckk::kStages];
+  uint64_t s_full, s_free;
+  uint64_t pds_full, pds_free;
+  uint64_t d_full[2], d_free[2];
+  uint64_t drain;
+  uint32_t vis[ckk::kStages][ckk::kMaxPos][4];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__global__ void __launch_bounds__(ckk::kThreads, 1)
+    hca_csa_dckv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+                        const DckvParams p) {
+  using namespace ckk;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ DckvBars bars;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int *abort_flag = &bars.abort;
+  const QTiling &Q = p.qt;
+
+  if (tid == 0) {
+    mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.q_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars.kv_full[s], kGather);
+      // the S/dP MMAs' commit and every dS thread once it has read the block's bits
+      mbar_init(&bars.kv_empty[s], 1 + kEW);
+    }
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.s_free, kEW);
+    mbar_init(&bars.pds_full, kEW);
+    mbar_init(&bars.pds_free, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars.d_full[x], 1);
+      mbar_init(&bars.d_free[x], kEW);
+    }
+    mbar_init(&bars.drain, 1);
+    bars.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const bool poisoned = *(volatile const int32_t *)p.status != 0;
+
+  // the tiles this CTA owns, and the number of key blocks of each
+  auto tile_blocks = [&](long long u, Tile &t, int &cnt) -> int {
+    tile_coords(Q, u, t);
+    const long long grp = (long long)t.b * Q.ntq + t.i0 / Q.Pq;
+    cnt = p.u_cnt[grp];
+    return (cnt + kBlockKeys - 1) / kBlockKeys;
+  };
+
+  if (warp >= kEW / 32) {
+    setmaxnreg_dec<kRegProducer>();
+    if (warp == kEW / 32) {
+      // ------------------------------------------------------------ TMA: Q and dO tiles
+      uint32_t tw = 0;
+      int q_par = -1;
+      bool ok = !poisoned;
+      for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
+        Tile t;
+        int cnt;
+        if (tile_blocks(u, t, cnt) == 0) continue;
+        if (lane == 0) {
+          if (tw > 0) ok = mbar_wait(&bars.q_empty, (tw - 1) & 1, abort_flag, p.status, p.wait_ns);
+          if (ok) {
+            mbar_arrive_expect_tx(&bars.q_full, 2 * kTile);
+            const int c2 = t.b * Q.H + t.g * Q.HG;
+            tma_load_3d(&map_q, &bars.q_full, smem + kOffQ, 0, t.i0, c2);
+            tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + kHalfTile, 64, t.i0, c2);
+            tma_load_3d(&map_do, &bars.q_full, smem + kOffDO, 0, t.i0, c2);
+            tma_load_3d(&map_do, &bars.q_full, smem + kOffDO + kHalfTile, 64, t.i0, c2);
+            q_par = tw & 1;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        ++tw;
+      }
+      if (!ok && !poisoned && lane == 0 && q_par >= 0) {
+        volatile int never = 0;
+        mbar_wait(&bars.q_full, q_par, &never, p.status, 100000000ull);
+      }
+    } else if (warp == kEW / 32 + 2) {
+      // ------------------------------------------------------------ gather: the union's ckv rows
+      // Each block's entries are copied 16 bytes at a time into the 128B-
+      // swizzled tile layout the MMA descriptors read; the per-position
+      // visibility bits of the block go to shared memory beside them.
+      uint32_t gb = 0;
+      bool ok = !poisoned;
+      for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
+        Tile t;
+        int cnt;
+        const int nb = tile_blocks(u, t, cnt);
+        const long long grp = (long long)t.b * Q.ntq + t.i0 / Q.Pq;
+        const int32_t *ent = p.u_ent + grp * p.u_cap;
+        const uint32_t *msk = p.u_mask + grp * p.u_cap;
+        for (int j = 0; ok && j < nb; ++j, ++gb) {
+          const int s = gb % kStages;
+          if (gb >= (uint32_t)kStages)
+            ok = wait_warp(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
+          if (!ok) break;
+          const int c0 = j * kBlockKeys;
+          const int n = min(kBlockKeys, ((cnt + 15) & ~15) - c0);
+          uint8_t *dst = smem + kOffKV + s * kTile;
+          for (int q = lane; q < n * 16; q += 32) {
+            const int r = q >> 4, ch = q & 15;
+            const __nv_bfloat16 *src = p.ckv + ((size_t)t.b * Q.Sc + ent[c0 + r]) * kHeadDim + ch * 8;
+            cp_async16(smem_u32(dst + sw128_offset(r, ch)), src);
+          }
+          // visibility bits: word w of position pp = columns [32 w, 32 w + 32)
+          for (int w = 0; w < 4; ++w) {
+            const int c = c0 + 32 * w + lane;
+            const uint32_t mk = (32 * w + lane < n && c < cnt) ? msk[c] : 0u;
+            for (int pp = 0; pp < Q.Pq; ++pp) {
+              const uint32_t bits = __ballot_sync(0xffffffffu, (mk >> pp) & 1u);
+              if (lane == 0) bars.vis[s][pp][w] = bits;
+            }
+          }
+          cp_async_wait_all();
+          fence_async_smem();
+          mbar_arrive(&bars.kv_full[s]);
+        }
+      }
+    } else if (warp == kEW / 32 + 1) {
+      // ------------------------------------------------------------ MMA
+      const uint64_t dQk = smem_desc_sw128(smem_u32(smem + kOffQ), 16, 1024);          // K-major (S)
+      const uint64_t dDOk = smem_desc_sw128(smem_u32(smem + kOffDO), 16, 1024);        // K-major (dP)
+      const uint64_t dQm = smem_desc_sw128(smem_u32(smem + kOffQ), kHalfTile, 1024);   // MN-major (D)
+      const uint64_t dDOm = smem_desc_sw128(smem_u32(smem + kOffDO), kHalfTile, 1024);
+      const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + kOffKV), 16, 1024);
+      const uint64_t dP = smem_desc_sw128(smem_u32(smem + kOffP), kHalfTile, 1024);    // P^T: MN-major A
+      const uint64_t dDS = smem_desc_sw128(smem_u32(smem + kOffDS), kHalfTile, 1024);  // dS^T: MN-major A
+      const uint32_t id_d = idesc_bf16_f32(kRows, kHeadDim, true, true);
+      uint32_t gb = 0, tw = 0;
+      bool ok = !poisoned, issued = false;
+      for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
+        Tile t;
+        int cnt;
+        const int nb = tile_blocks(u, t, cnt);
+        if (nb == 0) continue;
+        ok = wait_warp(&bars.q_full, tw & 1, abort_flag, p.status, p.wait_ns);
+        for (int j = 0; ok && j < nb; ++j) {
+          const uint32_t g = gb + j;
+          const int s = g % kStages;
+          const int n = min(kBlockKeys, ((cnt + 15) & ~15) - j * kBlockKeys);
+          ok = wait_warp(&bars.kv_full[s], (g / kStages) & 1, abort_flag, p.status, p.wait_ns);
+          // the previous block's S and dP have been read out
+          if (ok && g > 0) ok = wait_warp(&bars.s_free, (g - 1) & 1, abort_flag, p.status, p.wait_ns);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t idesc = idesc_bf16_f32(kRows, n, false, false);
+          const uint64_t bk = dK0 + desc_bytes(s * kTile);
+          if (elect_one()) {
+#pragma unroll
+            for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(tmem + kColS, dQk + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
+#pragma unroll
+            for (int k = 0; k < kHeadDim / 16; ++k)
+              mma_ss(tmem + kColDP, dDOk + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
+            mma_commit(&bars.s_full);
+            mma_commit(&bars.kv_empty[s]);  // the key block's last readers (with the dS warps' read of its bits)
+          }
+          __syncwarp();
+          issued = true;
+          // D = P^T dO + (scale dS)^T Q once P and dS are in shared memory
+          const int x = g & 1;
+          ok = wait_warp(&bars.pds_full, g & 1, abort_flag, p.status, p.wait_ns);
+          if (ok && g >= 2) ok = wait_warp(&bars.d_free[x], ((g / 2) - 1) & 1, abort_flag, p.status, p.wait_ns);
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) {
+            const uint32_t d = tmem + kColD + x * 128;
+#pragma unroll
+            for (int k = 0; k < kRows / 16; ++k) mma_ss(d, dP + mnmaj_step(k), dDOm + mnmaj_step(k), id_d, k > 0);
+#pragma unroll
+            for (int k = 0; k < kRows / 16; ++k) mma_ss(d, dDS + mnmaj_step(k), dQm + mnmaj_step(k), id_d, 1u);
+            mma_commit(&bars.d_full[x]);
+            mma_commit(&bars.pds_free);
+            if (j == nb - 1) mma_commit(&bars.q_empty);  // Q and dO are last read by the D MMAs
+          }
+          __syncwarp();
+        }
+        gb += nb;
+        ++tw;
+      }
+      if (!ok && issued) {
+        volatile int never = 0;
+        if (elect_one()) mma_commit(&bars.drain);
+        __syncwarp();
+        if (lane == 0) mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+        __syncwarp();
+      }
+    }
+  } else {
+    setmaxnreg_inc<kRegEW>();
+    // ------------------------------------------------------------ P, dS and the dckv rows
+    // thread r of warpgroup wg: query row r (TMEM lane r) and key columns
+    // [64 wg, 64 wg + 64) of every block; then entry column r of the block's
+    // D, its dims [64 wg, 64 wg + 64), into the fp32 accumulator.
+    const int r = tid & (kRows - 1), wg = tid >> 7;
+    const int cb = wg * 64;
+    const int pq = r & (Q.Pq - 1);
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint64_t sl2x2 = f32x2(__float_as_uint(p.sl2), __float_as_uint(p.sl2));
+    uint32_t gb = 0;
+    bool ok = !poisoned;
+    for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
+      Tile t;
+      int cnt;
+      const int nb = tile_blocks(u, t, cnt);
+      if (nb == 0) continue;
+      const long long tl = ((long long)t.b * Q.groups + t.g) * Q.ntq + t.i0 / Q.Pq;
+      const float nl2 = p.rowstat[tl * 2 * kRows + r];             // -lse*log2e (0 for invalid rows)
+      const float ndl = p.rowstat[tl * 2 * kRows + kRows + r];     // -scale*Delta
+      const int i = t.i0 + pq;
+      const bool row_valid = i < Q.S && (Q.sstart == nullptr || Q.sstart[(size_t)t.b * Q.S + i] >= 0);
+      const long long grp = (long long)t.b * Q.ntq + t.i0 / Q.Pq;
+      const int32_t *ent = p.u_ent + grp * p.u_cap;
+      for (int j = 0; j < nb; ++j, ++gb) {
+        const int s = gb % kStages;
+        const int c0 = j * kBlockKeys;
+        if (!wait_warp(&bars.s_full, gb & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+        tc_fence_after();
+        // S and dP of the row's 64 columns, 32 at a time, into P and scale*dS
+        // (bf16) in shared memory; the bits say which columns the row sees
+        if (!wait_warp(&bars.kv_full[s], (gb / kStages) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+        const uint64_t vis = row_valid ? ((uint64_t)bars.vis[s][pq][2 * wg] | ((uint64_t)bars.vis[s][pq][2 * wg + 1] << 32))
+                                       : 0ull;
+        mbar_arrive(&bars.kv_empty[s]);
+        // the previous block's D MMAs must have read the P and dS tiles
+        if (gb > 0 && !wait_warp(&bars.pds_free, (gb - 1) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+        const uint64_t nl2x2 = f32x2(__float_as_uint(nl2), __float_as_uint(nl2));
+        const uint64_t sc2 = f32x2(__float_as_uint(p.scale), __float_as_uint(p.scale));
+        const uint64_t nd2 = f32x2(__float_as_uint(ndl), __float_as_uint(ndl));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sv[32], dv[32];
+          tmem_ld32(lane_addr + kColS + cb + 32 * h, sv);
+          tmem_ld32(lane_addr + kColDP + cb + 32 * h, dv);
+          tmem_wait_ld();
+          if (h == 1) {
+            tc_fence_before();
+            mbar_arrive(&bars.s_free);
+          }
+          const uint32_t vh = (uint32_t)(vis >> (32 * h));
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t pw[4], dw[4];
+#pragma unroll
+            for (int y = 0; y < 8; y += 2) {
+              const int c = ch * 8 + y;
+              float t0, t1;
+              f32x2_split(ffma2(f32x2(sv[c], sv[c + 1]), sl2x2, nl2x2), t0, t1);
+              float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
+              // scale dP - scale Delta, times P
+              float g0, g1;
+              f32x2_split(fmul2(f32x2(__float_as_uint(e0), __float_as_uint(e1)), ffma2(f32x2(dv[c], dv[c + 1]), sc2, nd2)),
+                          g0, g1);
+              const bool v0 = (vh >> c) & 1u, v1 = (vh >> (c + 1)) & 1u;
+              e0 = v0 ? e0 : 0.f;
+              e1 = v1 ? e1 : 0.f;
+              g0 = v0 ? g0 : 0.f;
+              g1 = v1 ? g1 : 0.f;
+              pw[y >> 1] = pack_bf16x2(e0, e1);
+              dw[y >> 1] = pack_bf16x2(g0, g1);
+            }
+            const uint32_t off = sw128_offset(r, (cb + 32 * h) / 8 + ch);
+            *reinterpret_cast<uint4 *>(smem + kOffP + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            *reinterpret_cast<uint4 *>(smem + kOffDS + off) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+          }
+        }
+        fence_async_smem();
+        mbar_arrive(&bars.pds_full);
+        // D of this block: entry column r of the block, dims [64 wg, 64 wg + 64)
+        const int x = gb & 1;
+        if (!wait_warp(&bars.d_full[x], (gb / 2) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t o[64];
+        tmem_ld32(lane_addr + kColD + x * 128 + cb, *reinterpret_cast<uint32_t(*)[32]>(o));
+        tmem_ld32(lane_addr + kColD + x * 128 + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars.d_free[x]);
+        if (c0 + r < cnt) {
+          float4 *dst = reinterpret_cast<float4 *>(p.acc + ((size_t)t.b * Q.Sc + ent[c0 + r]) * kHeadDim + cb);
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            atomicAdd(dst + q, make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                           __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3])));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+__global__ void csa_dckv_finalize_kernel(const float *acc, __nv_bfloat16 *dckv, long long n4, const int32_t *status) {
+  const bool poisoned = *(volatile const int32_t *)status != 0;
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < n4; v += (long long)gridDim.x * blockDim.x) {
+    float4 a = reinterpret_cast<const float4 *>(acc)[v];
+    if (poisoned) a = make_float4(NAN, NAN, NAN, NAN);
+    uint2 o;
+    o.x = pack_bf16x2(a.x, a.y);
+    o.y = pack_bf16x2(a.z, a.w);
+    reinterpret_cast<uint2 *>(dckv)[v] = o;
+  }
+}
+
+int next_pow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+size_t csa_union_bytes(int B, int S, int P, int k) {
+  const long long ng = ((long long)S + P - 1) / P;
+  const long long cap = ((long long)P * k + 15) / 16 * 16;
+  return align_up((size_t)B * ng * sizeof(int32_t)) + 2 * align_up((size_t)B * ng * cap * sizeof(int32_t));
+}
+
+bool csa_shape_ok(int H, int k) {
+  // masks carry one bit per position of a forward pair: Pq <= 4 (H a multiple of 32)
+  if (H < 1 || (H % 32) != 0 || k < 1) return false;
+  const int Pq = kRows / heads_per_tile(H);
+  return Pq <= ckk::kMaxPos && 2 * Pq * k <= 32768;
+}
+
+cudaError_t csa_build_union(const int32_t *sel, const int32_t *sstart, int B, int S, int m, int k, int P,
+                            CsaUnion &u, void *mem, cudaStream_t st) {
+  const int ng = (S + P - 1) / P;
+  u.P = P;
+  u.cap = (P * k + 15) / 16 * 16;
+  u.ngroups = ng;
+  char *c = static_cast<char *>(mem);
+  u.cnt = reinterpret_cast<int32_t *>(c);
+  c += align_up((size_t)B * ng * sizeof(int32_t));
+  u.ent = reinterpret_cast<int32_t *>(c);
+  c += align_up((size_t)B * ng * u.cap * sizeof(int32_t));
+  u.mask = reinterpret_cast<uint32_t *>(c);
+  if ((long long)B * ng == 0) return cudaSuccess;
+  UnionArgs a;
+  a.sel = sel; a.sstart = sstart; a.cnt = u.cnt; a.ent = u.ent; a.mask = u.mask;
+  a.B = B; a.S = S; a.m = m; a.Sc = (S + m - 1) / m; a.k = k; a.P = P; a.ngroups = ng; a.cap = u.cap;
+  a.sortn = next_pow2(P * k);
+  if (a.sortn < 2) a.sortn = 2;
+  static SmemAttrOnce attr;
+  cudaError_t e = attr.ensure(reinterpret_cast<const void *>(csa_union_kernel), 32768 * (int)sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  ProfScope prof(kKCsaUnion, st);
+  csa_union_kernel<<<B * ng, kUnionThreads, a.sortn * sizeof(uint32_t), st>>>(a);
+  return cudaGetLastError();
+}
+
+size_t csa_dckv_acc_bytes(int B, int Sc) { return align_up((size_t)B * Sc * kHeadDim * sizeof(float)); }
+
+cudaError_t csa_dckv(const BwdArgs &a, const CsaUnion &u, const float *rowstat, float *acc, cudaStream_t st) {
+  const QTiling q = make_qtiling(a.sstart, a.B, a.H, a.S, a.W, a.m);
+  CUtensorMap mq, mdo;
+  if (!make_map_bf16(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mdo, a.dout, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(acc, 0, (size_t)a.B * q.Sc * kHeadDim * sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  static SmemAttrOnce attr;
+  e = attr.ensure(reinterpret_cast<const void *>(hca_csa_dckv_kernel), ckk::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  DckvParams p;
+  p.qt = q;
+  p.ckv = static_cast<const __nv_bfloat16 *>(a.ckv);
+  p.rowstat = rowstat;
+  p.u_cnt = u.cnt; p.u_ent = u.ent; p.u_mask = u.mask; p.u_cap = u.cap;
+  p.acc = acc;
+  p.status = a.status_rw;
+  p.sl2 = a.scale * 1.4426950408889634f;
+  p.scale = a.scale;
+  p.pq_shift = 0;
+  while ((1 << p.pq_shift) < q.Pq) ++p.pq_shift;
+  p.wait_ns = a.wait_ns;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorNoDevice;
+  const long long grid = q.ntiles < sms ? q.ntiles : sms;
+  if (grid > 0) {
+    ProfScope prof(kKCsaDckv, st);
+    hca_csa_dckv_kernel<<<(unsigned)grid, ckk::kThreads, ckk::kSmemBytes, st>>>(mq, mdo, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const long long n4 = (long long)a.B * q.Sc * kHeadDim / 4;
+  if (n4 > 0) {
+    int blocks = (int)((n4 + 255) / 256);
+    if (blocks > 8 * sms) blocks = 8 * sms;
+    csa_dckv_finalize_kernel<<<blocks, 256, 0, st>>>(acc, static_cast<__nv_bfloat16 *>(a.dckv), n4, a.status_rw);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace hca

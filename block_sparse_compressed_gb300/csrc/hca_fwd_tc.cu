@@ -66,9 +66,16 @@ constexpr int kOffQ = 0;
 constexpr int kOffKV = 2 * kTile;
 constexpr int kOffOut = kOffKV + kStages * kTile;
 constexpr int kSmemBytes = kOffOut + 2 * kTile + 1024;
+constexpr int kCsaMaxPos = 8;     // positions of a pair whose bits CSA keeps (Pq <= 4)
+constexpr int kGatherThreads = 64;  // CSA: warps 14 and 15 gather the compressed rows
 
 struct FwdParams {
   QTiling qt;          // per query tile (Pq positions)
+  // CSA: per pair, the union of its positions' selected entries (hca_csa.cu)
+  const int32_t *u_cnt, *u_ent;
+  const uint32_t *u_mask;
+  int u_cap;
+  const __nv_bfloat16 *ckv;
   long long npairs;    // pair tiles over (b, head group, pair index)
   int ntp;             // pairs per (b, group)
   int32_t *status;
@@ -91,10 +98,20 @@ __device__ __forceinline__ void pair_coords(const FwdParams &p, long long u, Til
   t.i0 = tp * 2 * p.qt.Pq;
 }
 
+template <bool kCsa>
 __device__ __forceinline__ void pair_ranges_warp(const FwdParams &p, Tile &t, int lane) {
   QTiling q2 = p.qt;
   q2.Pq = 2 * p.qt.Pq;
   tile_ranges_warp(q2, t, lane);
+  if (kCsa) {
+    // compressed columns: the pair's union of selected entries
+    const int cnt = p.u_cnt[(long long)t.b * p.ntp + t.i0 / (2 * p.qt.Pq)];
+    t.clo = 0;
+    t.chi = cnt;
+    t.cpad = (cnt + 15) & ~15;
+    t.ncols = t.cpad + (t.rhi - t.rlo);
+    t.nb = (t.ncols + kBlockKeys - 1) / kBlockKeys;
+  }
 }
 
 __device__ __forceinline__ void setmaxnreg_inc_softmax() { asm volatile("setmaxnreg.inc.sync.aligned.u32 176;"); }
@@ -109,11 +126,12 @@ struct Bars {
   uint64_t st_full[2], st_free[2];
   uint64_t epi, drain, never;
   float inv_l[2][kRows];
+  uint32_t vis[kStages][kCsaMaxPos][4];  // CSA: per block, each pair position's bits of the compressed columns
   uint32_t tmem_base;
   int abort;
 };
 
-template <bool kPosScale>
+template <bool kPosScale, bool kCsa>
 __global__ void __launch_bounds__(kThreads, 1)
     hca_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
                       const __grid_constant__ CUtensorMap map_ckv, const __grid_constant__ CUtensorMap map_kv16,
@@ -131,7 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.q_full, 1);
     mbar_init(&bars.q_empty, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars.kv_full[s], 1);
+      // CSA: the gather warps also arrive once their rows have landed
+      mbar_init(&bars.kv_full[s], kCsa ? 1 + kGatherThreads : 1);
       mbar_init(&bars.kv_empty[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
@@ -176,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
         Tile t;
         pair_coords(p, u, t);
-        pair_ranges_warp(p, t, lane);
+        pair_ranges_warp<kCsa>(p, t, lane);
         const int nb = t.nb;
         if (nb == 0) continue;
         if (lane == 0) {
@@ -212,9 +231,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             int n, nc;
             block_cols(t, j, n, nc);
-            mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes(n, nc));
-            load_block(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
-                       smem + kOffKV + s * kTile);
+            if (kCsa) {
+              // raw rows only: the gather warps bring the compressed ones
+              mbar_arrive_expect_tx(&bars.kv_full[s], nc == n ? 0u : raw_load_bytes(n, nc));
+              if (nc < n) load_block_raw(t, j, n, nc, &map_kv, &map_kv16, &bars.kv_full[s], smem + kOffKV + s * kTile);
+            } else {
+              mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes(n, nc));
+              load_block(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
+                         smem + kOffKV + s * kTile);
+            }
             issued = (issued | (1u << s)) & ~(1u << (8 + s));
             issued |= ((gb / kStages) & 1u) << (8 + s);
           }
@@ -228,6 +253,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s)
           if (issued & (1u << s)) mbar_wait(&bars.kv_full[s], (issued >> (8 + s)) & 1u, &never, p.status, 100000000ull);
         if (q_par >= 0) mbar_wait(&bars.q_full, q_par, &never, p.status, 100000000ull);
+      }
+    } else if (kCsa && warp >= 14) {
+      // ---------------------------------------------------------- CSA gather
+      // The compressed columns of every block are the pair's union of
+      // selected entries: their ckv rows are copied into the key tile (the
+      // swizzled layout the TMA gives the raw rows) and each pair position's
+      // bits for them go to shared memory; the warps then join the block's
+      // kv_full arrival.  They follow the TMA warp's schedule.
+      const int part = warp - 14;
+      uint32_t gb = 0;
+      bool ok = !poisoned;
+      for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
+        Tile t;
+        pair_coords(p, u, t);
+        pair_ranges_warp<kCsa>(p, t, lane);
+        const int nb = t.nb;
+        const long long grp = (long long)t.b * p.ntp + t.i0 / (2 * Q.Pq);
+        const int32_t *ent = p.u_ent + grp * p.u_cap;
+        const uint32_t *msk = p.u_mask + grp * p.u_cap;
+        const __nv_bfloat16 *ckv_b = p.ckv + (size_t)t.b * Q.Sc * kHeadDim;
+        for (int j = 0; ok && j < nb; ++j, ++gb) {
+          const int s = gb % kStages;
+          if (gb >= (uint32_t)kStages)
+            ok = wait_warp(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
+          if (!ok) break;
+          int n, nc;
+          block_cols(t, j, n, nc);
+          gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, part, 2,
+                       2 * Q.Pq, 2 * part, 2 * part + 2, &bars.vis[s][0][0], lane);
+          cp_async_wait_all();
+          fence_async_smem();
+          mbar_arrive(&bars.kv_full[s]);
+        }
       }
     } else if (warp == 13) {
       // ---------------------------------------------------------- MMA
@@ -252,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
         Tile t;
         pair_coords(p, u, t);
-        pair_ranges_warp(p, t, lane);
+        pair_ranges_warp<kCsa>(p, t, lane);
         uniform_tile(t);
         const int nb = t.nb;
         if (nb == 0) continue;
@@ -346,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (long long u = blockIdx.x; ok && !poisoned && u < p.npairs; u += gridDim.x) {
       Tile t;
       pair_coords(p, u, t);
-      pair_ranges_warp(p, t, lane);
+      pair_ranges_warp<kCsa>(p, t, lane);
       const int nb = t.nb;
       if (nb == 0) continue;
       for (int x = 0; ok && x < 2; ++x) {
@@ -408,9 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
       Tile t;
       pair_coords(p, u, t);
-      pair_ranges_warp(p, t, lane);
+      pair_ranges_warp<kCsa>(p, t, lane);
       const int nb = t.nb;
       const int pq = r % Q.Pq, hh = r / Q.Pq;
+      const int ppos = x * Q.Pq + pq;  // this row's position in the pair (CSA bits)
       const int head = t.g * Q.HG + hh;
       const int i = t.i0 + x * Q.Pq + pq;
       const RowIv iv = row_interval(Q.sstart, t.b, Q.S, i, Q.W, Q.m);
@@ -436,6 +495,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         row_cols(t, iv, j, n, nc, a1, b1, a2, b2);
         // S_X(j) ready; since S_X(j) was issued after PV_X(j-1), O_X is stable
         if (!wait_warp(&bars.s_full[x], scnt & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+        uint32_t cbits[4] = {0u, 0u, 0u, 0u};
+        if (kCsa) {
+          // the block's key tile (with the gather warps' bits) has landed:
+          // the MMA waited for it before S; this wait orders the bits' reads
+          const uint32_t sst = scnt % kStages;
+          if (!wait_warp(&bars.kv_full[sst], (scnt / kStages) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+          if (iv.valid) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) cbits[w] = bars.vis[sst][ppos][w];
+          }
+        }
         ++scnt;
         tc_fence_after();
         // One TMEM round trip brings the row's nk scores into registers; the
@@ -466,9 +536,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
             if (c0 < nk) {
-              const bool whole = (c0 >= a1 && c0 + 31 <= b1) || (c0 >= a2 && c0 + 31 <= b2);
+              uint32_t vm;
+              bool whole;
+              if (kCsa) {
+                // compressed columns: this position's selection bits; raw: its window
+                vm = cbits[c0 >> 5] | (uint32_t)range_mask64(a2, b2, c0);
+                whole = vm == 0xffffffffu;
+              } else {
+                whole = (c0 >= a1 && c0 + 31 <= b1) || (c0 >= a2 && c0 + 31 <= b2);
+              }
               if (!__all_sync(0xffffffffu, whole)) {
-                const uint32_t vm = (uint32_t)(range_mask64(a1, b1, c0) | range_mask64(a2, b2, c0));
+                if (!kCsa) vm = (uint32_t)(range_mask64(a1, b1, c0) | range_mask64(a2, b2, c0));
 #pragma unroll
                 for (int y = 0; y < 32; ++y)
                   if (!((vm >> y) & 1u)) sv[c0 + y] = __float_as_uint(ninf);
@@ -577,12 +655,17 @@ bool tc_fwd_supported(int H, int D, int dtype) { return tc_shape_ok(H, D, dtype)
 
 int tc_query_tile_positions(int H) { return kRows / heads_per_tile(H); }
 
-cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st) {
+cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st, const CsaUnion *csa) {
   FwdParams p;
   p.qt = make_qtiling(a.sstart, a.B, a.H, a.S, a.W, a.m);
   const QTiling &q = p.qt;
   p.ntp = (q.ntq + 1) / 2;
   p.npairs = (long long)a.B * q.groups * p.ntp;
+  p.u_cnt = csa ? csa->cnt : nullptr;
+  p.u_ent = csa ? csa->ent : nullptr;
+  p.u_mask = csa ? csa->mask : nullptr;
+  p.u_cap = csa ? csa->cap : 0;
+  p.ckv = static_cast<const __nv_bfloat16 *>(a.ckv);
   CUtensorMap mq, mkv, mckv, mkv16, mckv16, mout;
   if (!make_map_bf16(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mout, a.out, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
@@ -598,9 +681,15 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st) {
   p.wait_ns = a.wait_ns;
   p.stall = a.stall;
   const bool pos = p.sl2 > 0.f;
-  auto kern = pos ? hca_fwd_tc_kernel<true> : hca_fwd_tc_kernel<false>;
-  static SmemAttrOnce attr[2];
-  cudaError_t e = attr[pos].ensure(reinterpret_cast<const void *>(kern), kSmemBytes);
+  const int which = (pos ? 1 : 0) + (csa ? 2 : 0);
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+               const CUtensorMap, const FwdParams) =
+      which == 0   ? hca_fwd_tc_kernel<false, false>
+      : which == 1 ? hca_fwd_tc_kernel<true, false>
+      : which == 2 ? hca_fwd_tc_kernel<false, true>
+                   : hca_fwd_tc_kernel<true, true>;
+  static SmemAttrOnce attr[4];
+  cudaError_t e = attr[which].ensure(reinterpret_cast<const void *>(kern), kSmemBytes);
   if (e != cudaSuccess) return e;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorNoDevice;

@@ -74,7 +74,9 @@ namespace isk {
 constexpr int kStages = 2;
 constexpr int kThreads = 192;  // warps 0-3 epilogue (one TMEM lane quarter each), 4 TMA, 5 MMA
 constexpr int kOffA = 0, kOffB = kTile;
-constexpr int kSmemBytes = kTile + kStages * kTile + 1024;
+constexpr int kStageLd = kBlockKeys + 4;  // staging row pitch in floats (bank-conflict padding)
+constexpr int kOffStage = kTile + kStages * kTile;
+constexpr int kSmemBytes = kOffStage + kRows * kStageLd * 4 + 1024;
 constexpr int kTmemCols = 256;  // two 128-column accumulators
 }  // namespace isk
 
@@ -89,7 +91,7 @@ struct ScoreParams {
 struct ScoreBars {
   uint64_t a_full;
   uint64_t b_full[isk::kStages], b_empty[isk::kStages];
-  uint64_t acc_full[2], acc_free[2], drain;
+  uint64_t acc_full[2], acc_free[2], drain, epi;
   uint32_t tmem_base;
   int abort;
 };
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(isk::kThreads, 1)
       mbar_init(&bars.acc_free[x], 128);
     }
     mbar_init(&bars.drain, 1);
+    mbar_init(&bars.epi, 128);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -195,13 +198,20 @@ __global__ void __launch_bounds__(isk::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // thread r = row r of the tile (TMEM lane r): its 128 scores of a block
-    // go to the chunk buffer as 32 16-byte stores
+    // thread r = row r of the tile (TMEM lane r) stages its 128 scores of a
+    // block in shared memory; then every warp writes whole rows, so each
+    // store instruction covers one contiguous 512-byte row segment
     const int r = tid;
-    const int pos = p0 + r;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    float *dst = p.buf + ((size_t)b * p.rows + (pos - p.row0)) * p.ld;
-    const bool live = pos < p1;
+    float *stage = reinterpret_cast<float *>(smem + kOffStage);
+    uint32_t epi_phase = 0;
+    // bounded rendezvous of the four epilogue warps (an abort ends it too)
+    auto rendezvous = [&]() -> bool {
+      mbar_arrive(&bars.epi);
+      const bool rr = wait_warp(&bars.epi, epi_phase & 1, abort_flag, p.status, p.wait_ns);
+      ++epi_phase;
+      return rr;
+    };
     for (int j = 0; j < nblk; ++j) {
       const int x = j & 1;
       if (!wait_warp(&bars.acc_full[x], (j / 2) & 1, abort_flag, p.status, p.wait_ns)) break;
@@ -211,16 +221,22 @@ __global__ void __launch_bounds__(isk::kThreads, 1)
         uint32_t v[32];
         tmem_ld32(lane_addr + x * 128 + c0, v);
         tmem_wait_ld();
-        if (live) {
-          float4 *d4 = reinterpret_cast<float4 *>(dst + j * kBlockKeys + c0);
+        float4 *d4 = reinterpret_cast<float4 *>(stage + r * kStageLd + c0);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-        }
+        for (int q = 0; q < 8; ++q)
+          d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                              __uint_as_float(v[4 * q + 3]));
       }
       tc_fence_before();
       mbar_arrive(&bars.acc_free[x]);
+      if (!rendezvous()) break;
+      for (int rr = warp * 32; rr < warp * 32 + 32; ++rr) {
+        if (p0 + rr >= p1) break;
+        const float4 v = reinterpret_cast<const float4 *>(stage + rr * kStageLd)[lane];
+        float *dst = p.buf + ((size_t)b * p.rows + (p0 + rr - p.row0)) * p.ld + j * kBlockKeys;
+        reinterpret_cast<float4 *>(dst)[lane] = v;
+      }
+      if (!rendezvous()) break;
     }
   }
   tc_fence_before();
@@ -235,6 +251,10 @@ __global__ void __launch_bounds__(isk::kThreads, 1)
 // 3. top-k per query row
 // ---------------------------------------------------------------------------
 constexpr int kTopkThreads = 256;
+constexpr int kRadixBins = 2048;  // 11-bit digits
+// a query row's visible scores are staged in shared memory (with the 8 KB
+// histogram, within the 227 KB a block may use)
+constexpr int kMaxEntries = 55296;
 
 // Order-preserving map of a float to an unsigned key (larger float, larger key).
 __device__ __forceinline__ uint32_t fkey(float f) {
@@ -276,10 +296,10 @@ struct TopkParams {
 
 __global__ void __launch_bounds__(kTopkThreads) hca_index_topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t keys[];
-  __shared__ int hist[256];
+  __shared__ int hist[kRadixBins];
   __shared__ int wsum[kTopkThreads / 32];
   __shared__ int sh_digit, sh_rem;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int b = blockIdx.x / p.rows;
   const int i = p.row0 + blockIdx.x % p.rows;
   if (i >= p.S) return;
@@ -302,54 +322,55 @@ __global__ void __launch_bounds__(kTopkThreads) hca_index_topk_kernel(const Topk
     return;
   }
   for (int t = tid; t < n; t += kTopkThreads) keys[t] = fkey(row[lo + t]);
-  // radix select of the k-th largest key, 8 bits at a time from the top
+  // radix select of the k-th largest key: digits of 11, 11 and 10 bits from
+  // the top.  Lanes whose digit agrees add to the histogram once per group
+  // (match.any), so bins that most keys share (the exponent bits of similar
+  // scores) do not serialise the block on one shared-memory address.
   uint32_t prefix = 0, mask = 0;
   int rem = p.k;  // winners still to place at or below the current prefix
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int d = tid; d < 256; d += kTopkThreads) hist[d] = 0;
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const int bits = pass == 2 ? 10 : 11;
+    const uint32_t dmask = (1u << bits) - 1u;
+    for (int d = tid; d < kRadixBins; d += kTopkThreads) hist[d] = 0;
     __syncthreads();
-    for (int t = tid; t < n; t += kTopkThreads) {
-      const uint32_t kv = keys[t];
-      if ((kv & mask) == prefix) atomicAdd(&hist[(kv >> shift) & 255u], 1);
+    for (int t0 = 0; t0 < n; t0 += kTopkThreads) {
+      const int t = t0 + tid;
+      const uint32_t kv = t < n ? keys[t] : 0u;
+      const bool in = t < n && (kv & mask) == prefix;
+      const uint32_t dg = in ? (kv >> shift) & dmask : 0xffffffffu;
+      const unsigned peers = __match_any_sync(0xffffffffu, dg);
+      if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
     }
     __syncthreads();
-    if (tid < 32) {
-      // digit from the top where the running count reaches rem (one warp:
-      // each lane owns 8 consecutive digits, highest lanes first)
-      int c[8], s = 0;
+    // digit from the top where the running count reaches rem: thread t owns
+    // the 8 bins [top - 8t - 7, top - 8t] (top = 2^bits - 1)
+    const int top = (int)dmask;
+    int c[8], sum = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int d = top - (tid * 8 + q);
+      c[q] = d >= 0 ? hist[d] : 0;
+      sum += c[q];
+    }
+    int before;
+    block_excl_scan(sum, before, wsum);
+    if (before < rem && before + sum >= rem) {
+      int run = before;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        c[q] = hist[255 - (tid * 8 + q)];
-        s += c[q];
-      }
-      int incl = s;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (tid >= o) incl += y;
-      }
-      const int before = incl - s;  // keys in higher digits than this lane's
-      const bool here = before < rem && incl >= rem;
-      const unsigned ball = __ballot_sync(0xffffffffu, here);
-      if (here) {
-        int run = before, dsel = 0, rsel = rem;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (run + c[q] >= rem) {
-            dsel = 255 - (tid * 8 + q);
-            rsel = rem - run;
-            break;
-          }
-          run += c[q];
+        if (run + c[q] >= rem) {
+          sh_digit = top - (tid * 8 + q);
+          sh_rem = rem - run;
+          break;
         }
-        sh_digit = dsel;
-        sh_rem = rsel;
+        run += c[q];
       }
-      (void)ball;
     }
     __syncthreads();
     prefix |= (uint32_t)sh_digit << shift;
-    mask |= 255u << shift;
+    mask |= dmask << shift;
     rem = sh_rem;
     __syncthreads();
   }
@@ -372,6 +393,8 @@ __global__ void __launch_bounds__(kTopkThreads) hca_index_topk_kernel(const Topk
 }
 
 }  // namespace
+
+size_t indexer_max_entries() { return kMaxEntries; }
 
 size_t indexer_chunk_rows(int B, int S, int Sc) {
   // rows of query positions per pass: the fp32 score buffer stays <= 256 MB
@@ -412,7 +435,7 @@ cudaError_t indexer_topk(const IndexerArgs &a, cudaStream_t st) {
   static SmemAttrOnce attr_s, attr_t;
   const int topk_smem = ld * (int)sizeof(uint32_t);
   cudaError_t e = attr_s.ensure(reinterpret_cast<const void *>(hca_index_score_kernel), isk::kSmemBytes);
-  if (e == cudaSuccess) e = attr_t.ensure(reinterpret_cast<const void *>(hca_index_topk_kernel), 57344 * (int)sizeof(uint32_t));
+  if (e == cudaSuccess) e = attr_t.ensure(reinterpret_cast<const void *>(hca_index_topk_kernel), kMaxEntries * (int)sizeof(uint32_t));
   if (e != cudaSuccess) return e;
   for (int row0 = 0; row0 < a.S; row0 += rows_chunk) {
     const int rows = min(rows_chunk, a.S - row0);

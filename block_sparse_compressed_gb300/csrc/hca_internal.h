@@ -11,7 +11,7 @@ namespace hca {
 // kernels the optional profiler distinguishes (hca_profile_read ids)
 enum KernelId {
   kKPrep = 0, kKFwdTc, kKBwdDq, kKBwdDkv, kKBwdReduce, kKSimtFwd, kKSimtBwd, kKVisibility, kKCompress,
-  kKIndexScore, kKIndexTopk, kNumKernels
+  kKIndexScore, kKIndexTopk, kKCsaUnion, kKCsaDckv, kNumKernels
 };
 
 // Brackets the launches issued during its lifetime with CUDA events on `st`
@@ -99,14 +99,35 @@ struct IndexerArgs {
   int B, S, Hi, m, k;
 };
 size_t indexer_workspace_bytes(int B, int S, int m);
+size_t indexer_max_entries();
 cudaError_t indexer_topk(const IndexerArgs &a, cudaStream_t st);
+
+// CSA (hca_csa.cu): per group of P positions, the union of their valid
+// selections with one position bit per entry
+struct CsaUnion {
+  int32_t *cnt;    // [B*ngroups] entries in the union
+  int32_t *ent;    // [B*ngroups][cap] entry ids, ascending, padded to 16 with 0
+  uint32_t *mask;  // [B*ngroups][cap] bit p: position p of the group selected it
+  int P, cap, ngroups;
+};
+bool csa_shape_ok(int H, int k);
+size_t csa_union_bytes(int B, int S, int P, int k);
+cudaError_t csa_build_union(const int32_t *sel, const int32_t *sstart, int B, int S, int m, int k, int P,
+                            CsaUnion &u, void *mem, cudaStream_t st);
+size_t csa_dckv_acc_bytes(int B, int Sc);
+struct BwdArgs;
+cudaError_t csa_dckv(const BwdArgs &a, const CsaUnion &u, const float *rowstat, float *acc, cudaStream_t st);
 
 // tensor-core (tcgen05) path
 bool tc_fwd_supported(int H, int D, int dtype);
 int tc_query_tile_positions(int H);
-cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st);
+cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st, const CsaUnion *csa = nullptr);
 bool tc_bwd_supported(int H, int D, int dtype);
-size_t tc_bwd_scratch_bytes(int B, int H, int S, int D, int W, int m, int dtype);
-cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st);
+struct CsaBwd {
+  CsaUnion u;  // per dq tile (Pq positions)
+  float *acc;  // [B][Sc][D] fp32 dckv accumulator
+};
+size_t tc_bwd_scratch_bytes(int B, int H, int S, int D, int W, int m, int dtype, bool csa = false);
+cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st, const CsaBwd *csa = nullptr);
 
 }  // namespace hca

@@ -40,7 +40,8 @@ cudaEvent_t take_event() {
 
 const char *kNames[kNumKernels] = {"hca_prep",       "hca_fwd_tc",   "hca_bwd_dq",       "hca_bwd_dkv",
                                    "hca_bwd_reduce", "hca_simt_fwd", "hca_simt_bwd",     "hca_visibility",
-                                   "hca_compress",   "hca_index_score", "hca_index_topk"};
+                                   "hca_compress",   "hca_index_score", "hca_index_topk",   "hca_csa_union",
+                                   "hca_csa_dckv"};
 
 }  // namespace
 

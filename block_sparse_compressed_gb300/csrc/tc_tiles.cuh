@@ -173,6 +173,64 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk16) {
   return (uint32_t)(half * kHalfTile + row * 128 + ((c ^ (row & 7)) << 4));
 }
 
+// ---------------------------------------------------------------------------
+// CSA key blocks: compressed columns are the tile's union of selected
+// entries (gathered), raw columns as in HCA (TMA)
+// ---------------------------------------------------------------------------
+// Bytes the TMA delivers for the raw rows of block j (n columns, nc of them
+// gathered compressed entries).
+__device__ __forceinline__ uint32_t raw_load_bytes(int n, int nc) {
+  if (nc == 0) return (uint32_t)kTile;
+  return (uint32_t)((n - nc + 15) / 16) * 16u * 256u;
+}
+
+// TMA loads of the raw rows [nc, n) of block j (16-row boxes after the
+// compressed rows, one 128-row box per half when the block is all raw).
+__device__ __forceinline__ void load_block_raw(const Tile &t, int j, int n, int nc, const CUtensorMap *kv,
+                                               const CUtensorMap *kv16, uint64_t *bar, uint8_t *dst) {
+  const int c0 = j * kBlockKeys;
+  const int off = t.rlo + c0 - t.cpad;
+  if (nc == 0) {
+    tma_load_3d(kv, bar, dst, 0, off, t.b);
+    tma_load_3d(kv, bar, dst + kHalfTile, 64, off, t.b);
+    return;
+  }
+  for (int r = nc; r < n; r += 16) {
+    tma_load_3d(kv16, bar, dst + r * 128, 0, off + r, t.b);
+    tma_load_3d(kv16, bar, dst + kHalfTile + r * 128, 64, off + r, t.b);
+  }
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// One gather warp's share of block j's compressed columns [c0, c0 + nc):
+// rows ent[c0 + r] of ckv[b] copied 16 bytes at a time into the swizzled
+// tile at dst (warp `part` of `nparts` takes rows r = part, part + nparts,
+// ...), and words [wlo, whi) of the per-position visibility bits: word w of
+// position p holds bit (c - 32 w) for the block's columns c in [32 w, 32 w +
+// 32) that position p selected.  The caller waits for the copies
+// (cp_async_wait_all) and fences them for the tensor core before it signals.
+__device__ __forceinline__ void gather_block(const int32_t *ent, const uint32_t *msk, int cnt, int c0, int nc,
+                                             const __nv_bfloat16 *ckv_b, uint8_t *dst, int part, int nparts,
+                                             int npos, int wlo, int whi, uint32_t *vis /* [npos][4] */, int lane) {
+  for (int q = lane; q < 16 * ((nc + nparts - 1) / nparts); q += 32) {
+    const int r = part + nparts * (q >> 4), ch = q & 15;
+    if (r < nc) cp_async16(smem_u32(dst + sw128_offset(r, ch)), ckv_b + (size_t)ent[c0 + r] * kHeadDim + ch * 8);
+  }
+  for (int w = wlo; w < whi; ++w) {
+    const int c = 32 * w + lane;
+    const uint32_t mk = (c < nc && c0 + c < cnt) ? msk[c0 + c] : 0u;
+    for (int pp = 0; pp < npos; ++pp) {
+      const uint32_t bits = __ballot_sync(0xffffffffu, (mk >> pp) & 1u);
+      if (lane == 0) vis[pp * 4 + w] = bits;
+    }
+  }
+}
+
+
 // UMMA descriptor offsets (in the descriptor's 16-byte units) of k-step k
 // (16 bf16 of K) inside a 128-row tile stored as two 128B-swizzled halves:
 // K-major operands advance 32 bytes inside a half, then jump to the next half;

@@ -31,7 +31,7 @@ EXPORTS = ("hca_status_string", "hca_version", "hca_workspace_size", "hca_query_
            "hca_profile_read", "hca_num_kernels", "hca_kernel_name", "hca_attn_fwd_noalloc",
            "hca_local_workspace_size", "hca_local_attn_fwd", "hca_local_attn_bwd", "hca_test_inject",
            "hca_compress_fwd", "hca_compress_workspace_size", "hca_compress_bwd", "hca_indexer_workspace_size",
-           "hca_indexer_topk")
+           "hca_indexer_topk", "hca_csa_workspace_size", "hca_csa_attn_fwd", "hca_csa_attn_bwd")
 
 # failure-path test hooks (hca_test_inject)
 INJECT_RESET, INJECT_LAUNCH_FAILURE, INJECT_STALL, INJECT_WAIT_LIMIT_NS = 0, 1, 2, 3
@@ -99,6 +99,12 @@ def load(path: str = LIB_PATH):
             lib.hca_indexer_workspace_size.restype = Z
             lib.hca_indexer_topk.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, Z, P]
             lib.hca_indexer_topk.restype = I
+            lib.hca_csa_workspace_size.argtypes = [I, I, I, I, I, I, I, I, I]
+            lib.hca_csa_workspace_size.restype = Z
+            lib.hca_csa_attn_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, Z, P]
+            lib.hca_csa_attn_fwd.restype = I
+            lib.hca_csa_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, Z, P]
+            lib.hca_csa_attn_bwd.restype = I
             _lib = lib
     return _lib
 
@@ -443,3 +449,52 @@ def hca_indexer_topk(qi: torch.Tensor, ki: torch.Tensor, w: torch.Tensor, seg: O
     if check:
         _check(hca_workspace_status(ws), "hca_indexer_topk (device)")
     return sel, scores
+
+
+def csa_workspace(B, H, S, D, W, m, k, dtype, for_backward, device) -> torch.Tensor:
+    n = load().hca_csa_workspace_size(B, H, S, D, W, m, k, _DTYPES[dtype], int(for_backward))
+    if n == 0:
+        raise HCAError(8, "hca_csa_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def hca_csa_attn_fwd(q, kv, ckv, seg, sel, W: int, m: int, scale: float, out=None, lse=None, ws=None,
+                     check: bool = False):
+    """CSA forward: (out, lse); sel[B,S,k] int32 selected compressed entries."""
+    lib = load()
+    B, H, S, D, Sc = _shapes(q, kv, ckv, seg, m)
+    k = sel.shape[-1]
+    _need(sel, "sel", (B, S, k), torch.int32, q.device)
+    dt = _dtype_code(q)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(B, H, S, dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = csa_workspace(B, H, S, D, W, m, k, q.dtype, False, q.device) if ws is None else ws
+    with _on(q.device):
+        rc = lib.hca_csa_attn_fwd(_ptr(q), _ptr(kv), _ptr(ckv), _ptr(seg), _ptr(sel), _ptr(out), _ptr(lse), B, H, S,
+                                  D, W, m, k, float(scale), dt, _ptr(ws), ws.numel(), _stream(q.device))
+    _check(rc, "hca_csa_attn_fwd")
+    if check:
+        _check(hca_workspace_status(ws), "hca_csa_attn_fwd (device)")
+    return out, lse
+
+
+def hca_csa_attn_bwd(q, kv, ckv, seg, sel, out, lse, dout, W: int, m: int, scale: float, dq=None, dkv=None,
+                     dckv=None, ws=None, check: bool = False):
+    """CSA backward: (dq, dkv, dckv)."""
+    lib = load()
+    B, H, S, D, Sc = _shapes(q, kv, ckv, seg, m)
+    k = sel.shape[-1]
+    _need(sel, "sel", (B, S, k), torch.int32, q.device)
+    dt = _dtype_code(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dkv = torch.empty_like(kv) if dkv is None else dkv
+    dckv = torch.empty_like(ckv) if dckv is None else dckv
+    ws = csa_workspace(B, H, S, D, W, m, k, q.dtype, True, q.device) if ws is None else ws
+    with _on(q.device):
+        rc = lib.hca_csa_attn_bwd(_ptr(q), _ptr(kv), _ptr(ckv), _ptr(seg), _ptr(sel), _ptr(out), _ptr(lse),
+                                  _ptr(dout), _ptr(dq), _ptr(dkv), _ptr(dckv), B, H, S, D, W, m, k, float(scale), dt,
+                                  _ptr(ws), ws.numel(), _stream(q.device))
+    _check(rc, "hca_csa_attn_bwd")
+    if check:
+        _check(hca_workspace_status(ws), "hca_csa_attn_bwd (device)")
+    return dq, dkv, dckv

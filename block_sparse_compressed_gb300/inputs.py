@@ -154,3 +154,18 @@ def random_layout(S: int, rng: np.random.Generator, max_docs: int = 6, allow_pad
         ids[bounds[k]:bounds[k + 1]] = k
     ids[n:] = -1
     return ids
+
+
+def random_selection(B: int, S: int, m: int, k: int, seed: int, extra: int = 2) -> torch.Tensor:
+    """int32 [B,S,k] per-query compressed-entry selections for CSA tests and
+    benchmarks (a stand-in for the indexer's top-k): entries drawn uniformly
+    from [0, (i+1)//m + extra) for query i, so a few are not yet complete (the
+    attention must ignore them), with repeats; the first and last slot of
+    every fifth query are -1 (padding)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    hi = (np.arange(S) + 1) // m + extra
+    u = rng.random((B, S, k))
+    sel = np.floor(u * hi[None, :, None]).astype(np.int32)
+    sel[:, ::5, 0] = -1
+    sel[:, ::5, -1] = -1
+    return torch.from_numpy(sel)

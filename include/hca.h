@@ -176,6 +176,34 @@ HCA_API int hca_attn_fwd_noalloc(const void *q, const void *kv, const void *ckv,
                                  void *out, float *lse,
                                  int B, int H, int S, int D, int W, int m, float scale, int dtype, void *stream);
 
+/* Compressed sparse attention (CSA): HCA's two sets with the compressed
+ * entries narrowed to a per-query selection ("Add HCA Static Compilation
+ * for Splash Attention [Deepseek v4]", Description: CSA, compress ratio 4,
+ * needs a top-k step and runtime indexer masks that keep or discard (query,
+ * compressed entry) pairs; "DSV4: Route compressed and sliding train
+ * attention onto the splash kernels", indexer-mask review).  Query i attends
+ * under one softmax to its raw window (as hca_attn_fwd) and to the entries
+ * j listed in sel[b,i,:] that hca_attn_fwd would let it see (window complete
+ * at i, inside i's document).  Entries outside that set, repeats and
+ * negative ids (padding) in sel are ignored, so sel can be the output of
+ * hca_indexer_topk directly.
+ *   sel   [B,S,k] int32 (device), k >= 1
+ * Other arguments, layouts and outputs as hca_attn_fwd / hca_attn_bwd; dckv
+ * rows of entries nobody selected are 0.  bf16 only, D = 128, H a multiple
+ * of 32 and 2*Pq*k <= 32768 (Pq = hca_query_tile_positions); anything else
+ * returns HCA_ERR_UNSUPPORTED.  Workspace: hca_csa_workspace_size bytes
+ * (for_backward as in hca_workspace_size); 0 for unsupported sizes.  The
+ * backward's dckv is summed with fp32 atomics (reproducible only up to
+ * summation order); dq and dkv are deterministic. */
+HCA_API size_t hca_csa_workspace_size(int B, int H, int S, int D, int W, int m, int k, int dtype, int for_backward);
+HCA_API int hca_csa_attn_fwd(const void *q, const void *kv, const void *ckv, const int32_t *seg, const int32_t *sel,
+                             void *out, float *lse, int B, int H, int S, int D, int W, int m, int k, float scale,
+                             int dtype, void *workspace, size_t workspace_bytes, void *stream);
+HCA_API int hca_csa_attn_bwd(const void *q, const void *kv, const void *ckv, const int32_t *seg, const int32_t *sel,
+                             const void *out, const float *lse, const void *dout, void *dq, void *dkv, void *dckv,
+                             int B, int H, int S, int D, int W, int m, int k, float scale, int dtype,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
 /* HCA compressor: pooling of length-m windows of rows into compressed
  * entries ("[DeepSeek-V4] Implement Compressed Attention Layers",
  * Description: the compressors pool with a causal block bias; "Add HCA Static
@@ -222,7 +250,7 @@ HCA_API int hca_compress_bwd(const void *x, const float *g, const float *bias, c
  *   seg [B,S] int32 or NULL;  sel [B,S,k] int32 (overwritten)
  *   scores [B,S,ceil(S/m)] fp32 or NULL: when given, every score with the
  *                  sentinel -inf outside the visible range (for checking)
- * ceil(S/m) must be at most 57344 and k at least 1.  Workspace:
+ * ceil(S/m) must be at most 55296 and k at least 1.  Workspace:
  * hca_indexer_workspace_size(B,S,m) bytes (status word, document starts,
  * collapsed queries and a score buffer of at most 256 MB).  Segment ids out
  * of order are reported through hca_workspace_status (HCA_ERR_SEG) and that
