@@ -69,13 +69,18 @@ constexpr int kSmemBytes = kOffOut + 2 * kTile + 1024;
 constexpr int kCsaMaxPos = 8;     // positions of a pair whose bits CSA keeps (Pq <= 4)
 constexpr int kGatherThreads = 64;  // CSA: warps 14 and 15 gather the compressed rows
 
-struct FwdParams {
-  QTiling qt;          // per query tile (Pq positions)
-  // CSA: per pair, the union of its positions' selected entries (hca_csa.cu)
+// CSA: per pair, the union of its positions' selected entries (hca_csa.cu).
+// A kernel argument of its own: growing FwdParams changes how the HCA
+// instantiation keeps its parameters and costs it registers.
+struct CsaParams {
   const int32_t *u_cnt, *u_ent;
   const uint32_t *u_mask;
   int u_cap;
   const __nv_bfloat16 *ckv;
+};
+
+struct FwdParams {
+  QTiling qt;          // per query tile (Pq positions)
   long long npairs;    // pair tiles over (b, head group, pair index)
   int ntp;             // pairs per (b, group)
   int32_t *status;
@@ -99,13 +104,13 @@ __device__ __forceinline__ void pair_coords(const FwdParams &p, long long u, Til
 }
 
 template <bool kCsa>
-__device__ __forceinline__ void pair_ranges_warp(const FwdParams &p, Tile &t, int lane) {
+__device__ __forceinline__ void pair_ranges_warp(const FwdParams &p, const CsaParams &cp, Tile &t, int lane) {
   QTiling q2 = p.qt;
   q2.Pq = 2 * p.qt.Pq;
   tile_ranges_warp(q2, t, lane);
   if (kCsa) {
     // compressed columns: the pair's union of selected entries
-    const int cnt = p.u_cnt[(long long)t.b * p.ntp + t.i0 / (2 * p.qt.Pq)];
+    const int cnt = cp.u_cnt[(long long)t.b * p.ntp + t.i0 / (2 * p.qt.Pq)];
     t.clo = 0;
     t.chi = cnt;
     t.cpad = (cnt + 15) & ~15;
@@ -136,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     hca_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
                       const __grid_constant__ CUtensorMap map_ckv, const __grid_constant__ CUtensorMap map_kv16,
                       const __grid_constant__ CUtensorMap map_ckv16, const __grid_constant__ CUtensorMap map_out,
-                      const FwdParams p) {
+                      const FwdParams p, const CsaParams cp) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Bars bars;
@@ -195,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
         Tile t;
         pair_coords(p, u, t);
-        pair_ranges_warp<kCsa>(p, t, lane);
+        pair_ranges_warp<kCsa>(p, cp, t, lane);
         const int nb = t.nb;
         if (nb == 0) continue;
         if (lane == 0) {
@@ -267,12 +272,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
         Tile t;
         pair_coords(p, u, t);
-        pair_ranges_warp<kCsa>(p, t, lane);
+        pair_ranges_warp<kCsa>(p, cp, t, lane);
         const int nb = t.nb;
         const long long grp = (long long)t.b * p.ntp + t.i0 / (2 * Q.Pq);
-        const int32_t *ent = p.u_ent + grp * p.u_cap;
-        const uint32_t *msk = p.u_mask + grp * p.u_cap;
-        const __nv_bfloat16 *ckv_b = p.ckv + (size_t)t.b * Q.Sc * kHeadDim;
+        const int32_t *ent = cp.u_ent + grp * cp.u_cap;
+        const uint32_t *msk = cp.u_mask + grp * cp.u_cap;
+        const __nv_bfloat16 *ckv_b = cp.ckv + (size_t)t.b * Q.Sc * kHeadDim;
         for (int j = 0; ok && j < nb; ++j, ++gb) {
           const int s = gb % kStages;
           if (gb >= (uint32_t)kStages)
@@ -310,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
         Tile t;
         pair_coords(p, u, t);
-        pair_ranges_warp<kCsa>(p, t, lane);
+        pair_ranges_warp<kCsa>(p, cp, t, lane);
         uniform_tile(t);
         const int nb = t.nb;
         if (nb == 0) continue;
@@ -404,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (long long u = blockIdx.x; ok && !poisoned && u < p.npairs; u += gridDim.x) {
       Tile t;
       pair_coords(p, u, t);
-      pair_ranges_warp<kCsa>(p, t, lane);
+      pair_ranges_warp<kCsa>(p, cp, t, lane);
       const int nb = t.nb;
       if (nb == 0) continue;
       for (int x = 0; ok && x < 2; ++x) {
@@ -466,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
       Tile t;
       pair_coords(p, u, t);
-      pair_ranges_warp<kCsa>(p, t, lane);
+      pair_ranges_warp<kCsa>(p, cp, t, lane);
       const int nb = t.nb;
       const int pq = r % Q.Pq, hh = r / Q.Pq;
       const int ppos = x * Q.Pq + pq;  // this row's position in the pair (CSA bits)
@@ -496,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S_X(j) ready; since S_X(j) was issued after PV_X(j-1), O_X is stable
         if (!wait_warp(&bars.s_full[x], scnt & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         uint32_t cbits[4] = {0u, 0u, 0u, 0u};
-        if (kCsa) {
+        if constexpr (kCsa) {
           // the block's key tile (with the gather warps' bits) has landed:
           // the MMA waited for it before S; this wait orders the bits' reads
           const uint32_t sst = scnt % kStages;
@@ -536,20 +541,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
             if (c0 < nk) {
-              uint32_t vm;
-              bool whole;
-              if (kCsa) {
+              if constexpr (kCsa) {
                 // compressed columns: this position's selection bits; raw: its window
-                vm = cbits[c0 >> 5] | (uint32_t)range_mask64(a2, b2, c0);
-                whole = vm == 0xffffffffu;
-              } else {
-                whole = (c0 >= a1 && c0 + 31 <= b1) || (c0 >= a2 && c0 + 31 <= b2);
-              }
-              if (!__all_sync(0xffffffffu, whole)) {
-                if (!kCsa) vm = (uint32_t)(range_mask64(a1, b1, c0) | range_mask64(a2, b2, c0));
+                const uint32_t vm = cbits[c0 >> 5] | (uint32_t)range_mask64(a2, b2, c0);
+                if (!__all_sync(0xffffffffu, vm == 0xffffffffu)) {
 #pragma unroll
-                for (int y = 0; y < 32; ++y)
-                  if (!((vm >> y) & 1u)) sv[c0 + y] = __float_as_uint(ninf);
+                  for (int y = 0; y < 32; ++y)
+                    if (!((vm >> y) & 1u)) sv[c0 + y] = __float_as_uint(ninf);
+                }
+              } else {
+                const bool whole = (c0 >= a1 && c0 + 31 <= b1) || (c0 >= a2 && c0 + 31 <= b2);
+                if (!__all_sync(0xffffffffu, whole)) {
+                  const uint32_t vm = (uint32_t)(range_mask64(a1, b1, c0) | range_mask64(a2, b2, c0));
+#pragma unroll
+                  for (int y = 0; y < 32; ++y)
+                    if (!((vm >> y) & 1u)) sv[c0 + y] = __float_as_uint(ninf);
+                }
               }
 #pragma unroll
               for (int y = 0; y < 32; y += 16) {
@@ -661,11 +668,12 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st, const CsaUnion *csa) {
   const QTiling &q = p.qt;
   p.ntp = (q.ntq + 1) / 2;
   p.npairs = (long long)a.B * q.groups * p.ntp;
-  p.u_cnt = csa ? csa->cnt : nullptr;
-  p.u_ent = csa ? csa->ent : nullptr;
-  p.u_mask = csa ? csa->mask : nullptr;
-  p.u_cap = csa ? csa->cap : 0;
-  p.ckv = static_cast<const __nv_bfloat16 *>(a.ckv);
+  CsaParams cp;
+  cp.u_cnt = csa ? csa->cnt : nullptr;
+  cp.u_ent = csa ? csa->ent : nullptr;
+  cp.u_mask = csa ? csa->mask : nullptr;
+  cp.u_cap = csa ? csa->cap : 0;
+  cp.ckv = static_cast<const __nv_bfloat16 *>(a.ckv);
   CUtensorMap mq, mkv, mckv, mkv16, mckv16, mout;
   if (!make_map_bf16(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mout, a.out, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
@@ -683,7 +691,7 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st, const CsaUnion *csa) {
   const bool pos = p.sl2 > 0.f;
   const int which = (pos ? 1 : 0) + (csa ? 2 : 0);
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
-               const CUtensorMap, const FwdParams) =
+               const CUtensorMap, const FwdParams, const CsaParams) =
       which == 0   ? hca_fwd_tc_kernel<false, false>
       : which == 1 ? hca_fwd_tc_kernel<true, false>
       : which == 2 ? hca_fwd_tc_kernel<false, true>
@@ -696,7 +704,7 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st, const CsaUnion *csa) {
   const long long grid = p.npairs < sms ? p.npairs : sms;
   if (grid == 0) return cudaSuccess;
   ProfScope prof(kKFwdTc, st);
-  kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mkv, mckv, mkv16, mckv16, mout, p);
+  kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(mq, mkv, mckv, mkv16, mckv16, mout, p, cp);
   return cudaGetLastError();
 }
 
