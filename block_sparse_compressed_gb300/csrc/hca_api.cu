@@ -299,7 +299,7 @@ int hca_attn_bwd(const void *q, const void *kv, const void *ckv, const int32_t *
 
 size_t hca_csa_workspace_size(int B, int H, int S, int D, int W, int m, int k, int dtype, int for_backward) {
   if (check_dims(B, H, S, D, W, m, dtype) != HCA_OK || k < 1) return 0;
-  if (dtype != HCA_BF16 || !tc_fwd_supported(H, D, dtype) || !csa_shape_ok(H, k)) return 0;
+  if (dtype != HCA_BF16 || D != 128 || !tc_fwd_supported(H, D, dtype) || !csa_shape_ok(H, k)) return 0;
   return for_backward ? csa_bwd_ws_bytes(B, H, S, D, W, m, k) : csa_fwd_ws_bytes(B, H, S, k);
 }
 
@@ -308,7 +308,7 @@ static int csa_checks(int B, int H, int S, int D, int W, int m, int k, float sca
   if (rc != HCA_OK) return rc;
   if (!std::isfinite(scale) || k < 1) return HCA_ERR_ARG;
   // CSA runs on the tensor-core kernels only (bf16, D = 128, H a multiple of 32)
-  if (dtype != HCA_BF16 || !tc_fwd_supported(H, D, dtype) || !csa_shape_ok(H, k)) return HCA_ERR_UNSUPPORTED;
+  if (dtype != HCA_BF16 || D != 128 || !tc_fwd_supported(H, D, dtype) || !csa_shape_ok(H, k)) return HCA_ERR_UNSUPPORTED;
   return HCA_OK;
 }
 

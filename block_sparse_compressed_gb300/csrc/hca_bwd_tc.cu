@@ -126,7 +126,7 @@ __device__ __forceinline__ bool read_dq_desc(DqBars &bars, uint32_t kd, Tile &t,
   return true;
 }
 
-template <bool kCsa>
+template <bool kCsa, int kD>
 __global__ void __launch_bounds__(dqk::kThreads, 1)
     hca_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                       const __grid_constant__ CUtensorMap map_out,
@@ -134,6 +134,9 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
                       const __grid_constant__ CUtensorMap map_kv16, const __grid_constant__ CUtensorMap map_ckv16,
                       const __grid_constant__ CUtensorMap map_dq, const DqParams p) {
   using namespace dqk;
+  static_assert(kD == 64 || kD == 128, "head dim 64 or 128");
+  static_assert(!kCsa || kD == 128, "CSA gathers 128-dim rows");
+  constexpr int kHalves = kD / 64;   // 64-column (128-byte) halves of a row
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ DqBars bars;
@@ -229,14 +232,14 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         if (lane == 0) {
           if (tw > 0) ok = mbar_wait(&bars.qd_empty, (tw - 1) & 1, abort_flag, p.status, p.wait_ns);
           if (ok) {
-            mbar_arrive_expect_tx(&bars.qd_full, 3 * kTile);
+            mbar_arrive_expect_tx(&bars.qd_full, 3 * kHalves * kHalfTile);
             const int c2 = t.b * Q.H + t.g * Q.HG;
-            tma_load_3d(&map_q, &bars.qd_full, smem + kOffQ, 0, t.i0, c2);
-            tma_load_3d(&map_q, &bars.qd_full, smem + kOffQ + kHalfTile, 64, t.i0, c2);
-            tma_load_3d(&map_do, &bars.qd_full, smem + kOffDO, 0, t.i0, c2);
-            tma_load_3d(&map_do, &bars.qd_full, smem + kOffDO + kHalfTile, 64, t.i0, c2);
-            tma_load_3d(&map_out, &bars.qd_full, smem + kOffO, 0, t.i0, c2);
-            tma_load_3d(&map_out, &bars.qd_full, smem + kOffO + kHalfTile, 64, t.i0, c2);
+#pragma unroll
+            for (int hh = 0; hh < kHalves; ++hh) {
+              tma_load_3d(&map_q, &bars.qd_full, smem + kOffQ + hh * kHalfTile, 64 * hh, t.i0, c2);
+              tma_load_3d(&map_do, &bars.qd_full, smem + kOffDO + hh * kHalfTile, 64 * hh, t.i0, c2);
+              tma_load_3d(&map_out, &bars.qd_full, smem + kOffO + hh * kHalfTile, 64 * hh, t.i0, c2);
+            }
             q_par = tw & 1;
             // this CTA's next tile: its q, dO and out rows go to L2 now, so
             // the loads at the tile boundary do not wait on HBM
@@ -246,7 +249,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
               tile_coords(Q, un, tn);
               const int cn = tn.b * Q.H + tn.g * Q.HG;
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
+              for (int hh = 0; hh < kHalves; ++hh) {
                 tma_prefetch_3d(&map_q, 64 * hh, tn.i0, cn);
                 tma_prefetch_3d(&map_do, 64 * hh, tn.i0, cn);
                 tma_prefetch_3d(&map_out, 64 * hh, tn.i0, cn);
@@ -265,9 +268,9 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
               mbar_arrive_expect_tx(&bars.kv_full[s], nc == n ? 0u : raw_load_bytes(n, nc));
               if (nc < n) load_block_raw(t, j, n, nc, &map_kv, &map_kv16, &bars.kv_full[s], smem + kOffKV + s * kTile);
             } else {
-              mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes(n, nc));
-              load_block(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
-                         smem + kOffKV + s * kTile);
+              mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes<kHalves>(n, nc));
+              load_block<kHalves>(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
+                                  smem + kOffKV + s * kTile);
             }
             last_par[s] = (gb / kStages) & 1;
           }
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       const uint64_t dDO = smem_desc_sw128(smem_u32(smem + kOffDO), 16, 1024);
       const uint64_t dK0 = smem_desc_sw128(smem_u32(smem + kOffKV), 16, 1024);
       const uint64_t dV0 = smem_desc_sw128(smem_u32(smem + kOffKV), kHalfTile, 1024);
-      const uint32_t id_dq = idesc_bf16_f32(kRows, kHeadDim, false, true);
+      const uint32_t id_dq = idesc_bf16_f32(kRows, kD, false, true);
       uint32_t gb = 0, tw = 0, kd = 0;
       bool ok = true, issued = false;
       if (!poisoned && p.stall) {
@@ -320,7 +323,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
           const uint32_t d = tmem + (x ? kColDP : kColS);
           if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, da + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
+            for (int k = 0; k < kD / 16; ++k) mma_ss(d, da + kmaj_step(k), bk + kmaj_step(k), idesc, k > 0);
             mma_commit(x ? &bars.dp_full : &bars.s_full);
             if (last_q_use) mma_commit(&bars.qd_empty);
           }
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         const long long grp = (long long)t.b * Q.ntq + t.i0 / Q.Pq;
         const int32_t *ent = p.u_ent + grp * p.u_cap;
         const uint32_t *msk = p.u_mask + grp * p.u_cap;
-        const __nv_bfloat16 *ckv_b = p.ckv + (size_t)t.b * Q.Sc * kHeadDim;
+        const __nv_bfloat16 *ckv_b = p.ckv + (size_t)t.b * Q.Sc * kD;
         for (int j = 0; ok && j < t.nb; ++j, ++gb) {
           const int s = gb % kStages;
           if (gb >= (uint32_t)kStages)
@@ -440,7 +443,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
           dl[h] = 0.f;
           const int r = dt + (kRows / kRowsPerLane) * h;
 #pragma unroll 4
-          for (int ch = 0; ch < 16; ++ch) {
+          for (int ch = 0; ch < kD / 8; ++ch) {
             const uint4 ov = *reinterpret_cast<const uint4 *>(outbuf + sw128_offset(r, ch));
             const uint4 gv = *reinterpret_cast<const uint4 *>(dobuf + sw128_offset(r, ch));
             const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
@@ -469,7 +472,8 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
     // thread r of warpgroup wg owns row r (TMEM lane r) and key columns
     // [64 wg, 64 wg + 64) of every block (and dq columns [64 wg, 64 wg + 64))
     const int r = tid & (kRows - 1), wg = tid >> 7;
-    const int cb = wg * 64;
+    const int cb = wg * 64;            // key columns of a block
+    const int cbq = wg * (kD / 2);     // dq columns
     const int pq = r & (Q.Pq - 1), hh = r >> p.pq_shift;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     uint8_t *obuf = smem + kOffOut;
@@ -497,9 +501,9 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         if (i < Q.S) {
           const float v = poisoned ? __int_as_float(0x7fc00000) : 0.f;
           const uint32_t w2 = pack_bf16x2(v, v);
-          uint4 *grow = reinterpret_cast<uint4 *>(p.dq + lrow * kHeadDim + cb);
+          uint4 *grow = reinterpret_cast<uint4 *>(p.dq + lrow * kD + cbq);
 #pragma unroll
-          for (int c = 0; c < kHeadDim / 16; ++c) grow[c] = make_uint4(w2, w2, w2, w2);
+          for (int c = 0; c < kD / 16; ++c) grow[c] = make_uint4(w2, w2, w2, w2);
         }
         if (wg == 0) {
           rs[r] = 0.f;
@@ -618,7 +622,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       {
         uint32_t o[32];
 #pragma unroll
-        for (int c0 = cb; c0 < cb + 64; c0 += 32) {
+        for (int c0 = cbq; c0 < cbq + kD / 2; c0 += 32) {
           tmem_ld32(lane_addr + kColDQ + c0, o);
           tmem_wait_ld();
 #pragma unroll
@@ -637,8 +641,8 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       if (!rendezvous()) { ok = false; break; }
       if (tid == 0) {
         const int c2 = t.b * Q.H + t.g * Q.HG;
-        tma_store_3d(&map_dq, obuf, 0, t.i0, c2);
-        tma_store_3d(&map_dq, obuf + kHalfTile, 64, t.i0, c2);
+#pragma unroll
+        for (int hh = 0; hh < kHalves; ++hh) tma_store_3d(&map_dq, obuf + hh * kHalfTile, 64 * hh, t.i0, c2);
         bulk_commit();
       }
       store_pending = true;
@@ -851,11 +855,15 @@ struct DkvBars {
   int abort;
 };
 
+template <int kD>
 __global__ void __launch_bounds__(dkk::kThreads, 1)
     hca_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_qs, const __grid_constant__ CUtensorMap map_dos,
                        const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_ckv,
                        const DkvParams p) {
   using namespace dkk;
+  static_assert(kD == 64 || kD == 128, "head dim 64 or 128");
+  constexpr int kHalves = kD / 64;   // 64-column (128-byte) halves of a row
+  constexpr int kAccCols = kD / 2;   // accumulator columns per warpgroup in the item epilogue
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ DkvBars bars;
@@ -933,11 +941,11 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
           if (iw > 0) ok = mbar_wait(&bars.k_empty, (iw - 1) & 1, abort_flag, p.status, p.wait_ns);
           if (ok) {
             const CUtensorMap *mp = it.comp ? &map_ckv : &map_kv;
-            mbar_arrive_expect_tx(&bars.k_full, it.nkb * kTile);
+            mbar_arrive_expect_tx(&bars.k_full, it.nkb * kHalves * kHalfTile);
             for (int a = 0; a < it.nkb; ++a) {
               uint8_t *dst = smem + kOffK + a * kTile;
-              tma_load_3d(mp, &bars.k_full, dst, 0, it.k0[a], it.b);
-              tma_load_3d(mp, &bars.k_full, dst + kHalfTile, 64, it.k0[a], it.b);
+#pragma unroll
+              for (int hh = 0; hh < kHalves; ++hh) tma_load_3d(mp, &bars.k_full, dst + hh * kHalfTile, 64 * hh, it.k0[a], it.b);
             }
             k_par = iw & 1;
           }
@@ -963,9 +971,9 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
           }
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive_expect_tx(&bars.st_full[s], kSubBytes + 512);
+            mbar_arrive_expect_tx(&bars.st_full[s], kHalves * kHalfTile + 512);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < kHalves; ++h) {
               tma_load_3d(&map_qs, &bars.st_full[s], st + h * kHalfTile, 64 * h, pos0, hd);
               tma_load_3d(&map_dos, &bars.st_full[s], st + h * kHalfTile + kHalfRows * 128, 64 * h, pos0, hd);
             }
@@ -1002,7 +1010,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
       const uint64_t dR0 = smem_desc_sw128(smem_u32(smem + kOffStage), 16, 1024);          // R, K-major
       const uint64_t dM0 = smem_desc_sw128(smem_u32(smem + kOffStage), kHalfTile, 1024);   // R rows, MN-major
       const uint32_t id_sd = idesc_bf16_f32(kRows, kRows, false, false);
-      const uint32_t id_acc = idesc_bf16_f32(kRows, kHeadDim, false, true);
+      const uint32_t id_acc = idesc_bf16_f32(kRows, kD, false, true);
       uint32_t gsub = 0, gu = 0, iw = 0;  // sub-tiles, units and items with work so far
       bool ok = true, issued = false;
       if (p.stall && !poisoned) {
@@ -1042,7 +1050,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
           const uint32_t d = tmem + col_buf(gu + w);
           if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, bk + kmaj_step(k), br + kmaj_step(k), id_sd, k > 0);
+            for (int k = 0; k < kD / 16; ++k) mma_ss(d, bk + kmaj_step(k), br + kmaj_step(k), id_sd, k > 0);
             mma_commit(&bars.s_full[(gu + w) & 1]);
             if (w == nu - 1) mma_commit(&bars.k_empty);  // the key tiles are read by these MMAs only
           }
@@ -1122,7 +1130,7 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
         const size_t rows = it.comp ? (size_t)p.Sc_pad : (size_t)p.S_pad;
         float *base = it.comp ? p.cpart : p.rpart;
         const int sl = (it.comp || !p.raw_atomic) ? it.slot[a] : 0;
-        prow[a] = a < nkb ? base + (((size_t)sl * Q.B + it.b) * rows + it.k0[a] + kr) * kHeadDim + wg * 64 : nullptr;
+        prow[a] = a < nkb ? base + (((size_t)sl * Q.B + it.b) * rows + it.k0[a] + kr) * kD + wg * kAccCols : nullptr;
       }
       const bool atomic_rows = !it.comp && p.raw_atomic;
       if (poisoned || nsub <= 0) {
@@ -1131,10 +1139,10 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
           float4 *dst = reinterpret_cast<float4 *>(prow[a]);
           if (atomic_rows) {
             if (poisoned)
-              for (int c = 0; c < 16; ++c) atomicAdd(dst + c, make_float4(val, val, val, val));
+              for (int c = 0; c < kAccCols / 4; ++c) atomicAdd(dst + c, make_float4(val, val, val, val));
           } else {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) dst[c] = make_float4(val, val, val, val);
+            for (int c = 0; c < kAccCols / 4; ++c) dst[c] = make_float4(val, val, val, val);
           }
         }
         continue;
@@ -1210,10 +1218,10 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
       if (!wait_warp(&bars.acc_full, iw & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
       tc_fence_after();
       for (int a = 0; a < nkb; ++a) {
-        uint32_t o[64];
-        const uint32_t ab = lane_addr + col_acc(a) + wg * 64;
-        tmem_ld32(ab, *reinterpret_cast<uint32_t(*)[32]>(o));
-        tmem_ld32(ab + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+        uint32_t o[kAccCols];
+        const uint32_t ab = lane_addr + col_acc(a) + wg * kAccCols;
+#pragma unroll
+        for (int c0 = 0; c0 < kAccCols; c0 += 32) tmem_ld32(ab + c0, *reinterpret_cast<uint32_t(*)[32]>(o + c0));
         tmem_wait_ld();
         if (a == nkb - 1) {
           tc_fence_before();
@@ -1222,12 +1230,12 @@ __global__ void __launch_bounds__(dkk::kThreads, 1)
         float4 *dst = reinterpret_cast<float4 *>(prow[a]);
         if (atomic_rows) {
 #pragma unroll
-          for (int x = 0; x < 16; ++x)
+          for (int x = 0; x < kAccCols / 4; ++x)
             atomicAdd(dst + x, make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
                                            __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3])));
         } else {
 #pragma unroll
-          for (int x = 0; x < 16; ++x)
+          for (int x = 0; x < kAccCols / 4; ++x)
             dst[x] = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]), __uint_as_float(o[4 * x + 2]),
                                  __uint_as_float(o[4 * x + 3]));
         }
@@ -1255,15 +1263,16 @@ struct ReduceParams {
   int with_comp;  // 0: dkv only (CSA writes dckv itself)
 };
 
+template <int kD>
 __global__ void hca_bwd_reduce_kernel(const ReduceParams p) {
-  const long long nraw4 = (long long)p.B * p.S * (kHeadDim / 4);
-  const long long ncomp4 = p.with_comp ? (long long)p.B * p.Sc * (kHeadDim / 4) : 0;
+  const long long nraw4 = (long long)p.B * p.S * (kD / 4);
+  const long long ncomp4 = p.with_comp ? (long long)p.B * p.Sc * (kD / 4) : 0;
   for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nraw4 + ncomp4;
        v += (long long)gridDim.x * blockDim.x) {
     const bool comp = v >= nraw4;
     const long long x = comp ? v - nraw4 : v;
-    const int d4 = (int)(x % (kHeadDim / 4));
-    const long long row = x / (kHeadDim / 4);
+    const int d4 = (int)(x % (kD / 4));
+    const long long row = x / (kD / 4);
     const int rows = comp ? p.Sc : p.S;
     const int b = (int)(row / rows), key = (int)(row % rows);
     const int kb = key / kBlockKeys;
@@ -1275,15 +1284,15 @@ __global__ void hca_bwd_reduce_kernel(const ReduceParams p) {
       // when their odd partner exists, pair slots
       s_lo = (kb & 1) ? dkk::kSplitLead : 0;
       s_hi = ((kb & 1) || kb + 1 < p.nkb_comp) ? dkk::kSlotsComp : dkk::kSplitLead;
-      stride = (size_t)p.B * p.Sc_pad * kHeadDim;
-      off = ((size_t)b * p.Sc_pad + key) * kHeadDim + d4 * 4;
+      stride = (size_t)p.B * p.Sc_pad * kD;
+      off = ((size_t)b * p.Sc_pad + key) * kD + d4 * 4;
       base = p.cpart;
     } else {
       // slot s holds query range kb + s; ranges past the sequence do not exist
       s_lo = 0;
       s_hi = p.raw_atomic ? 1 : min(p.nslot, p.nrb - kb);
-      stride = (size_t)p.B * p.S_pad * kHeadDim;
-      off = ((size_t)b * p.S_pad + key) * kHeadDim + d4 * 4;
+      stride = (size_t)p.B * p.S_pad * kD;
+      off = ((size_t)b * p.S_pad + key) * kD + d4 * 4;
       base = p.rpart;
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1294,7 +1303,7 @@ __global__ void hca_bwd_reduce_kernel(const ReduceParams p) {
     uint2 o;
     o.x = pack_bf16x2(acc.x, acc.y);
     o.y = pack_bf16x2(acc.z, acc.w);
-    __nv_bfloat16 *dst = comp ? p.dckv + ((size_t)b * p.Sc + key) * kHeadDim : p.dkv + ((size_t)b * p.S + key) * kHeadDim;
+    __nv_bfloat16 *dst = comp ? p.dckv + ((size_t)b * p.Sc + key) * kD : p.dkv + ((size_t)b * p.S + key) * kD;
     *reinterpret_cast<uint2 *>(dst + d4 * 4) = o;
   }
 }
@@ -1322,10 +1331,10 @@ RawGeom raw_geom(int S, int W) {
   g.atomic = ns > kMaxRawSlots;
   return g;
 }
-size_t rpart_bytes(int B, const RawGeom &g) {
-  return align_up((size_t)(g.atomic ? 1 : g.nslot) * B * g.S_pad * kHeadDim * sizeof(float));
+size_t rpart_bytes(int B, const RawGeom &g, int D) {
+  return align_up((size_t)(g.atomic ? 1 : g.nslot) * B * g.S_pad * D * sizeof(float));
 }
-size_t cpart_bytes(int B, int Sc) { return align_up((size_t)dkk::kSlotsComp * B * sc_pad(Sc) * kHeadDim * sizeof(float)); }
+size_t cpart_bytes(int B, int Sc, int D) { return align_up((size_t)dkk::kSlotsComp * B * sc_pad(Sc) * D * sizeof(float)); }
 
 }  // namespace
 
@@ -1335,7 +1344,7 @@ size_t tc_bwd_scratch_bytes(int B, int H, int S, int D, int W, int m, int dtype,
   if (!tc_shape_ok(H, D, dtype)) return 0;
   QTiling q = make_qtiling(nullptr, B, H, S, W, m);
   // CSA keeps no compressed partial slots: its dckv is accumulated query-major
-  return rowstat_bytes(q) + (csa ? 0 : cpart_bytes(B, q.Sc)) + rpart_bytes(B, raw_geom(S, W));
+  return rowstat_bytes(q) + (csa ? 0 : cpart_bytes(B, q.Sc, D)) + rpart_bytes(B, raw_geom(S, W), D);
 }
 
 cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st, const CsaBwd *csa) {
@@ -1345,28 +1354,33 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st, const CsaBwd *csa) {
   char *ws = static_cast<char *>(a.scratch);
   float *rowstat = reinterpret_cast<float *>(ws);
   float *cpart = csa ? nullptr : reinterpret_cast<float *>(ws + rowstat_bytes(q));
-  float *rpart = reinterpret_cast<float *>(ws + rowstat_bytes(q) + (csa ? 0 : cpart_bytes(a.B, q.Sc)));
+  float *rpart = reinterpret_cast<float *>(ws + rowstat_bytes(q) + (csa ? 0 : cpart_bytes(a.B, q.Sc, a.D)));
   // dkv kernel: a 64-row half of a query tile is a head range when HG >= 2,
   // a position range when one head fills the tile
   const int sub_hg = q.HG >= 2 ? q.HG / 2 : 1;
   const int sub_pq = q.HG >= 2 ? q.Pq : q.Pq / 2;
   CUtensorMap mq, mdo, mout, mkv, mckv, mkv16, mckv16, mdq, mqs, mdos;
-  if (!make_map_bf16(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
-      !make_map_bf16(&mout, a.out, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
-      !make_map_bf16(&mdo, a.dout, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
-      !make_map_bf16(&mdq, a.dq, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
-      !make_map_bf16(&mqs, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, sub_pq, sub_hg) ||
-      !make_map_bf16(&mdos, a.dout, kHeadDim, a.S, (uint64_t)a.B * a.H, sub_pq, sub_hg) ||
-      !make_map_bf16(&mkv, a.kv, kHeadDim, a.S, a.B, kBlockKeys, 1) ||
-      !make_map_bf16(&mckv, a.ckv, kHeadDim, q.Sc, a.B, kBlockKeys, 1) ||
-      !make_map_bf16(&mkv16, a.kv, kHeadDim, a.S, a.B, 16, 1) ||
-      !make_map_bf16(&mckv16, a.ckv, kHeadDim, q.Sc, a.B, 16, 1))
+  const uint64_t D = (uint64_t)a.D;
+  if (!make_map_bf16(&mq, a.q, D, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mout, a.out, D, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mdo, a.dout, D, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mdq, a.dq, D, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mqs, a.q, D, a.S, (uint64_t)a.B * a.H, sub_pq, sub_hg) ||
+      !make_map_bf16(&mdos, a.dout, D, a.S, (uint64_t)a.B * a.H, sub_pq, sub_hg) ||
+      !make_map_bf16(&mkv, a.kv, D, a.S, a.B, kBlockKeys, 1) ||
+      !make_map_bf16(&mckv, a.ckv, D, q.Sc, a.B, kBlockKeys, 1) ||
+      !make_map_bf16(&mkv16, a.kv, D, a.S, a.B, 16, 1) ||
+      !make_map_bf16(&mckv16, a.ckv, D, q.Sc, a.B, 16, 1))
     return cudaErrorInvalidValue;
-  auto dq_kern = csa ? hca_bwd_dq_kernel<true> : hca_bwd_dq_kernel<false>;
-  static SmemAttrOnce attr_dq[2], attr_dkv;
+  if (csa && a.D != 128) return cudaErrorInvalidValue;
+  const bool d64 = a.D == 64;
+  auto dq_kern = csa ? hca_bwd_dq_kernel<true, 128> : (d64 ? hca_bwd_dq_kernel<false, 64> : hca_bwd_dq_kernel<false, 128>);
+  auto dkv_kern = d64 ? hca_bwd_dkv_kernel<64> : hca_bwd_dkv_kernel<128>;
+  auto reduce_kern = d64 ? hca_bwd_reduce_kernel<64> : hca_bwd_reduce_kernel<128>;
+  static SmemAttrOnce attr_dq[3], attr_dkv[2];
   {
-    cudaError_t e = attr_dq[csa ? 1 : 0].ensure(reinterpret_cast<const void *>(dq_kern), dqk::kSmemBytes);
-    if (e == cudaSuccess) e = attr_dkv.ensure(reinterpret_cast<const void *>(hca_bwd_dkv_kernel), dkk::kSmemBytes);
+    cudaError_t e = attr_dq[csa ? 2 : (d64 ? 1 : 0)].ensure(reinterpret_cast<const void *>(dq_kern), dqk::kSmemBytes);
+    if (e == cudaSuccess) e = attr_dkv[d64 ? 1 : 0].ensure(reinterpret_cast<const void *>(dkv_kern), dkk::kSmemBytes);
     if (e != cudaSuccess) return e;
   }
   const int sms = sm_count();
@@ -1426,11 +1440,11 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st, const CsaBwd *csa) {
   kp.stall = (a.stall & HCA_STALL_DKV) != 0;
   const long long g2 = kp.nitems < sms ? kp.nitems : sms;
   e = cudaMemsetAsync(kp.next_item, 0, sizeof(int32_t), st);
-  if (e == cudaSuccess && rg.atomic) e = cudaMemsetAsync(rpart, 0, rpart_bytes(a.B, rg), st);
+  if (e == cudaSuccess && rg.atomic) e = cudaMemsetAsync(rpart, 0, rpart_bytes(a.B, rg, a.D), st);
   if (e != cudaSuccess) return e;
   {
     ProfScope prof(kKBwdDkv, st);
-    hca_bwd_dkv_kernel<<<(unsigned)g2, dkk::kThreads, dkk::kSmemBytes, st>>>(mqs, mdos, mkv, mckv, kp);
+    dkv_kern<<<(unsigned)g2, dkk::kThreads, dkk::kSmemBytes, st>>>(mqs, mdos, mkv, mckv, kp);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;
@@ -1450,12 +1464,12 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st, const CsaBwd *csa) {
   rp.nkb_comp = kp.nkb_comp;
   rp.raw_atomic = rg.atomic;
   rp.with_comp = csa ? 0 : 1;
-  const long long n4 = (long long)a.B * (a.S + (csa ? 0 : q.Sc)) * (kHeadDim / 4);
+  const long long n4 = (long long)a.B * (a.S + (csa ? 0 : q.Sc)) * (a.D / 4);
   if (n4 > 0) {
     int blocks = (int)((n4 + 255) / 256);
     if (blocks > 8 * sms) blocks = 8 * sms;
     ProfScope prof(kKBwdReduce, st);
-    hca_bwd_reduce_kernel<<<blocks, 256, 0, st>>>(rp);
+    reduce_kern<<<blocks, 256, 0, st>>>(rp);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess || !csa) return e;

@@ -136,12 +136,15 @@ struct Bars {
   int abort;
 };
 
-template <bool kPosScale, bool kCsa>
+template <bool kPosScale, bool kCsa, int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     hca_fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
                       const __grid_constant__ CUtensorMap map_ckv, const __grid_constant__ CUtensorMap map_kv16,
                       const __grid_constant__ CUtensorMap map_ckv16, const __grid_constant__ CUtensorMap map_out,
                       const FwdParams p, const CsaParams cp) {
+  static_assert(kD == 64 || kD == 128, "head dim 64 or 128");
+  static_assert(!kCsa || kD == 128, "CSA gathers 128-dim rows");
+  constexpr int kHalves = kD / 64;   // 64-column (128-byte) halves of a row
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Bars bars;
@@ -207,13 +210,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (gq > 0) ok = mbar_wait(&bars.q_empty, (gq - 1) & 1, abort_flag, p.status, p.wait_ns);
           if (ok) {
             const bool has_b = t.i0 + Q.Pq < Q.S;
-            mbar_arrive_expect_tx(&bars.q_full, has_b ? 2 * kTile : kTile);
+            mbar_arrive_expect_tx(&bars.q_full, (has_b ? 2 : 1) * kHalves * kHalfTile);
             const int c2 = t.b * Q.H + t.g * Q.HG;
-            tma_load_3d(&map_q, &bars.q_full, smem + kOffQ, 0, t.i0, c2);
-            tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + kHalfTile, 64, t.i0, c2);
-            if (has_b) {
-              tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + kTile, 0, t.i0 + Q.Pq, c2);
-              tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + kTile + kHalfTile, 64, t.i0 + Q.Pq, c2);
+#pragma unroll
+            for (int hh = 0; hh < kHalves; ++hh) {
+              tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + hh * kHalfTile, 64 * hh, t.i0, c2);
+              if (has_b)
+                tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + kTile + hh * kHalfTile, 64 * hh, t.i0 + Q.Pq, c2);
             }
             q_par = gq & 1;
             // this CTA's next pair: its q rows go to L2 now
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               pair_coords(p, un, tn);
               const int cn = tn.b * Q.H + tn.g * Q.HG;
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
+              for (int hh = 0; hh < kHalves; ++hh) {
                 tma_prefetch_3d(&map_q, 64 * hh, tn.i0, cn);
                 if (tn.i0 + Q.Pq < Q.S) tma_prefetch_3d(&map_q, 64 * hh, tn.i0 + Q.Pq, cn);
               }
@@ -241,9 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive_expect_tx(&bars.kv_full[s], nc == n ? 0u : raw_load_bytes(n, nc));
               if (nc < n) load_block_raw(t, j, n, nc, &map_kv, &map_kv16, &bars.kv_full[s], smem + kOffKV + s * kTile);
             } else {
-              mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes(n, nc));
-              load_block(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
-                         smem + kOffKV + s * kTile);
+              mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes<kHalves>(n, nc));
+              load_block<kHalves>(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
+                                  smem + kOffKV + s * kTile);
             }
             issued = (issued | (1u << s)) & ~(1u << (8 + s));
             issued |= ((gb / kStages) & 1u) << (8 + s);
@@ -305,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dq1 = smem_desc_sw128(smem_u32(smem + kOffQ + kTile), 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(smem + kOffKV), 16, 1024);         // K view of stage 0
       const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + kOffKV), kHalfTile, 1024);  // V view of stage 0
-      const uint32_t id_pv = idesc_bf16_f32(kRows, kHeadDim, false, true);
+      const uint32_t id_pv = idesc_bf16_f32(kRows, kD, false, true);
       uint32_t gb = 0, gq = 0, pcnt = 0;
       bool ok = !poisoned, issued = false;
       if (ok && p.stall) {
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d = tmem + col_s(x);
           if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < kHeadDim / 16; ++k) mma_ss(d, da + kmaj_step(k), db + kmaj_step(k), idesc, k > 0);
+            for (int k = 0; k < kD / 16; ++k) mma_ss(d, da + kmaj_step(k), db + kmaj_step(k), idesc, k > 0);
             mma_commit(&bars.s_full[x]);
             if (extra) mma_commit(extra);
           }
@@ -428,10 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint32_t o[32];
 #pragma unroll
-        for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+        for (int c0 = 0; c0 < kD; c0 += 32) {
           tmem_ld32(lane_addr + col_o(x) + c0, o);
           tmem_wait_ld();
-          if (c0 == kHeadDim - 32) {
+          if (c0 == kD - 32) {
             tc_fence_before();
             mbar_arrive(&bars.o_free[x]);  // O_X may now be overwritten
           }
@@ -450,8 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i0 < Q.S) {
           if (r == 0) {
             const int c2 = t.b * Q.H + t.g * Q.HG;
-            tma_store_3d(&map_out, obuf, 0, i0, c2);
-            tma_store_3d(&map_out, obuf + kHalfTile, 64, i0, c2);
+#pragma unroll
+            for (int hh = 0; hh < kHalves; ++hh) tma_store_3d(&map_out, obuf + hh * kHalfTile, 64 * hh, i0, c2);
           }
         }
         if (r == 0) bulk_commit();  // one group per staging tile (possibly empty)
@@ -483,9 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i < Q.S) {
           const float v = poisoned ? __int_as_float(0x7fc00000) : 0.f;
           const uint32_t w2 = pack_bf16x2(v, v);
-          uint4 *orow = reinterpret_cast<uint4 *>(p.out + lrow * kHeadDim);
+          uint4 *orow = reinterpret_cast<uint4 *>(p.out + lrow * kD);
 #pragma unroll
-          for (int c = 0; c < kHeadDim / 8; ++c) orow[c] = make_uint4(w2, w2, w2, w2);
+          for (int c = 0; c < kD / 8; ++c) orow[c] = make_uint4(w2, w2, w2, w2);
           p.lse[lrow] = poisoned ? v : -INFINITY;
         }
         continue;
@@ -618,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__any_sync(0xffffffffu, rescale_o)) {
           uint32_t o[32];
 #pragma unroll
-          for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+          for (int c0 = 0; c0 < kD; c0 += 32) {
             tmem_ld32(lane_addr + col_o(x) + c0, o);
             tmem_wait_ld();
 #pragma unroll
@@ -675,12 +678,13 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st, const CsaUnion *csa) {
   cp.u_cap = csa ? csa->cap : 0;
   cp.ckv = static_cast<const __nv_bfloat16 *>(a.ckv);
   CUtensorMap mq, mkv, mckv, mkv16, mckv16, mout;
-  if (!make_map_bf16(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
-      !make_map_bf16(&mout, a.out, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
-      !make_map_bf16(&mkv, a.kv, kHeadDim, a.S, a.B, kBlockKeys, 1) ||
-      !make_map_bf16(&mckv, a.ckv, kHeadDim, q.Sc, a.B, kBlockKeys, 1) ||
-      !make_map_bf16(&mkv16, a.kv, kHeadDim, a.S, a.B, 16, 1) ||
-      !make_map_bf16(&mckv16, a.ckv, kHeadDim, q.Sc, a.B, 16, 1))
+  const uint64_t D = (uint64_t)a.D;
+  if (!make_map_bf16(&mq, a.q, D, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mout, a.out, D, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_bf16(&mkv, a.kv, D, a.S, a.B, kBlockKeys, 1) ||
+      !make_map_bf16(&mckv, a.ckv, D, q.Sc, a.B, kBlockKeys, 1) ||
+      !make_map_bf16(&mkv16, a.kv, D, a.S, a.B, 16, 1) ||
+      !make_map_bf16(&mckv16, a.ckv, D, q.Sc, a.B, 16, 1))
     return cudaErrorInvalidValue;
   p.status = a.status_rw;
   p.lse = a.lse;
@@ -689,14 +693,17 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st, const CsaUnion *csa) {
   p.wait_ns = a.wait_ns;
   p.stall = a.stall;
   const bool pos = p.sl2 > 0.f;
-  const int which = (pos ? 1 : 0) + (csa ? 2 : 0);
+  if (csa && a.D != 128) return cudaErrorInvalidValue;
+  const int which = (pos ? 1 : 0) + (csa ? 2 : 0) + (a.D == 64 ? 4 : 0);
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                const CUtensorMap, const FwdParams, const CsaParams) =
-      which == 0   ? hca_fwd_tc_kernel<false, false>
-      : which == 1 ? hca_fwd_tc_kernel<true, false>
-      : which == 2 ? hca_fwd_tc_kernel<false, true>
-                   : hca_fwd_tc_kernel<true, true>;
-  static SmemAttrOnce attr[4];
+      which == 0   ? hca_fwd_tc_kernel<false, false, 128>
+      : which == 1 ? hca_fwd_tc_kernel<true, false, 128>
+      : which == 2 ? hca_fwd_tc_kernel<false, true, 128>
+      : which == 3 ? hca_fwd_tc_kernel<true, true, 128>
+      : which == 4 ? hca_fwd_tc_kernel<false, false, 64>
+                   : hca_fwd_tc_kernel<true, false, 64>;
+  static SmemAttrOnce attr[6];
   cudaError_t e = attr[which].ensure(reinterpret_cast<const void *>(kern), kSmemBytes);
   if (e != cudaSuccess) return e;
   const int sms = sm_count();

@@ -123,35 +123,40 @@ __device__ __forceinline__ void row_cols(const Tile &t, const RowIv &iv, int j, 
   b2 = min(iv.rhi - off, n - 1);
 }
 
-// Bytes that load_block delivers for a block of n columns, nc compressed.
+// Bytes that load_block delivers for a block of n columns, nc compressed,
+// of rows with kHalves 64-column halves (head dim 64 * kHalves).
+template <int kHalves = 2>
 __device__ __forceinline__ uint32_t block_load_bytes(int n, int nc) {
-  if (nc == n || nc == 0) return (uint32_t)kTile;
-  return (uint32_t)(nc / 16 + (n - nc + 15) / 16) * 16u * 256u;
+  if (nc == n || nc == 0) return (uint32_t)(kHalves * kHalfTile);
+  return (uint32_t)(nc / 16 + (n - nc + 15) / 16) * 16u * 128u * kHalves;
 }
 
 // TMA loads of block j's key rows into a 128-row tile at dst (two 64-column
 // swizzled halves).  A block of one kind is one 128-row box per half; a block
 // that holds both kinds is loaded in 16-row boxes (2 KB, so every box starts
 // on a 1 KB swizzle atom), compressed rows first.
+template <int kHalves = 2>
 __device__ __forceinline__ void load_block(const Tile &t, int j, int n, int nc, const CUtensorMap *kv,
                                            const CUtensorMap *ckv, const CUtensorMap *kv16, const CUtensorMap *ckv16,
                                            uint64_t *bar, uint8_t *dst) {
   const int c0 = j * kBlockKeys;
   const int off = t.rlo + c0 - t.cpad;
   if (nc == n) {
-    tma_load_3d(ckv, bar, dst, 0, t.clo + c0, t.b);
-    tma_load_3d(ckv, bar, dst + kHalfTile, 64, t.clo + c0, t.b);
+#pragma unroll
+    for (int hh = 0; hh < kHalves; ++hh) tma_load_3d(ckv, bar, dst + hh * kHalfTile, 64 * hh, t.clo + c0, t.b);
   } else if (nc == 0) {
-    tma_load_3d(kv, bar, dst, 0, off, t.b);
-    tma_load_3d(kv, bar, dst + kHalfTile, 64, off, t.b);
+#pragma unroll
+    for (int hh = 0; hh < kHalves; ++hh) tma_load_3d(kv, bar, dst + hh * kHalfTile, 64 * hh, off, t.b);
   } else {
     for (int r = 0; r < nc; r += 16) {
-      tma_load_3d(ckv16, bar, dst + r * 128, 0, t.clo + c0 + r, t.b);
-      tma_load_3d(ckv16, bar, dst + kHalfTile + r * 128, 64, t.clo + c0 + r, t.b);
+#pragma unroll
+      for (int hh = 0; hh < kHalves; ++hh)
+        tma_load_3d(ckv16, bar, dst + hh * kHalfTile + r * 128, 64 * hh, t.clo + c0 + r, t.b);
     }
     for (int r = nc; r < n; r += 16) {
-      tma_load_3d(kv16, bar, dst + r * 128, 0, off + r, t.b);
-      tma_load_3d(kv16, bar, dst + kHalfTile + r * 128, 64, off + r, t.b);
+#pragma unroll
+      for (int hh = 0; hh < kHalves; ++hh)
+        tma_load_3d(kv16, bar, dst + hh * kHalfTile + r * 128, 64 * hh, off + r, t.b);
     }
   }
 }
@@ -308,7 +313,7 @@ inline int heads_per_tile(int H) {
   return hg;
 }
 
-inline bool tc_shape_ok(int H, int D, int dtype) { return dtype == HCA_BF16 && D == kHeadDim && H >= 1; }
+inline bool tc_shape_ok(int H, int D, int dtype) { return dtype == HCA_BF16 && (D == 64 || D == 128) && H >= 1; }
 
 // Dynamic shared-memory limit of a kernel, raised once per device: the
 // attribute belongs to the (function, device) pair, so a process that drives

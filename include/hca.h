@@ -26,7 +26,8 @@
  *            lse: [B,H,S] fp32.  All contiguous, row-major.
  *   dtype    HCA_BF16: q/kv/ckv/out/dout/dq/dkv/dckv are bfloat16, the
  *            arithmetic is bf16 tensor-core products with fp32 accumulation
- *            and fp32 softmax.  HCA_F32: everything fp32, fp32 arithmetic.
+ *            and fp32 softmax; D = 64 or 128 (other D: HCA_ERR_UNSUPPORTED).
+ *            HCA_F32: everything fp32, fp32 arithmetic, any D.
  *            lse is fp32 in both.
  *   seg      NULL means one segment per batch row.  Otherwise non-negative
  *            ids must be non-decreasing along S and negative ids (padding)
@@ -71,7 +72,7 @@ typedef enum {
   HCA_ERR_SEG = 6,         /* segment ids out of order (device-side check)     */
   HCA_ERR_WORKSPACE = 7,   /* workspace NULL, misaligned or too small          */
   HCA_ERR_UNSUPPORTED = 8, /* no kernel for this dtype / D combination (bf16
-                              runs on tensor cores only, for D = 128)        */
+                              runs on tensor cores only, for D = 64 or 128)  */
   HCA_ERR_CUDA = 9,        /* a CUDA runtime call or launch failed             */
   HCA_ERR_TIMEOUT = 10     /* a bounded on-device wait gave up                 */
 } hca_status;

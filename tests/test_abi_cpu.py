@@ -88,11 +88,15 @@ def test_argument_errors_are_caught_on_the_host(lib):
     assert _fwd(lib, wsb=16) == E_WS               # too small
     assert _fwd(lib, B=0) == OK                     # empty problem: nothing to do
     assert _fwd(lib, S=0) == OK
-    # bf16 runs on the tensor-core kernels only (D = 128): other head dims
-    # are rejected before anything is enqueued, never sent to CUDA cores
-    assert _fwd(lib, D=64) == E_UNSUP
+    # bf16 runs on the tensor-core kernels only (D = 64 or 128): other head
+    # dims are rejected before anything is enqueued, never sent to CUDA cores
+    assert _fwd(lib, D=32) == E_UNSUP
     assert _fwd(lib, D=256) == E_UNSUP
-    assert _fwd(lib, D=64, dt=1) != E_UNSUP         # fp32 runs every D
+    # supported shapes pass that check and stop at the (too small) workspace,
+    # still before any CUDA call
+    assert _fwd(lib, D=64, wsb=16) == E_WS
+    assert _fwd(lib, D=128, wsb=16) == E_WS
+    assert _fwd(lib, D=256, dt=1, wsb=16) == E_WS   # fp32 runs every D
 
 
 def test_backward_argument_errors(lib):

@@ -89,7 +89,22 @@ def test_any_head_count_on_tensor_cores(H):
     run_case(1, H, 300, 128, 48, 16, torch.bfloat16)
 
 
-@pytest.mark.parametrize("D", [64, 32, 256])
+@pytest.mark.parametrize("H,S,W,m,layout", [(64, 700, 128, 16, False), (16, 489, 333, 64, True),
+                                             (48, 300, 48, 1, False), (128, 260, 600, 8, True)])
+def test_head_dim_64_bf16(H, S, W, m, layout):
+    # D = 64 runs its own instantiation of the tensor-core kernels (one
+    # 128-byte half per row instead of two): several query tiles and key
+    # blocks with a ragged tail, multi-block windows, the atomic raw partials
+    # (W = 600) and documents with padding
+    seg = None
+    if layout:
+        rng = np.random.Generator(np.random.PCG64(S))
+        seg = I.random_layout(S, rng, allow_pad=True)[None]
+    assert hca.hca_query_tile_positions(H, 64, torch.bfloat16) == 128 // math.gcd(H, 128)
+    run_case(1, H, S, 64, W, m, torch.bfloat16, seg)
+
+
+@pytest.mark.parametrize("D", [32, 256])
 def test_bf16_head_dims_without_a_tensor_core_tile_are_rejected(D):
     # bf16 runs on the tensor-core kernels only: other head dims are an
     # error, never a silent CUDA-core fallback
