@@ -16,27 +16,32 @@
 // ranges are never loaded and no mask exists in memory; inside a block every
 // row masks by its own two intervals.
 //
-// Per key block j and tile X in {A, B}:
-//   S_X = Q_X K^T            tcgen05 SS, fp32 accumulator in TMEM
+// Per half-block k (64 keys of a key block) and tile X in {A, B}:
+//   S_X = Q_X K^T            tcgen05 SS, fp32 accumulator in TMEM buffer
+//                            (k mod 2) of S_X
 //   softmax warpgroup X      loads S_X, masks, online softmax in fp32 with
 //                            exp2 (the running max is raised only when a
-//                            block beats it by more than 2^8, so O_X is
+//                            half-block beats it by more than 2^8, so O_X is
 //                            rarely rescaled), writes P_X (bf16) back into
-//                            the first half of S_X's TMEM columns
+//                            the first half of the buffer's columns
 //   O_X += P_X V             tcgen05 TS: A = P_X from TMEM, B = the same kv
-//                            tile through an MN-major descriptor (K = V)
-// The MMA warp interleaves S_A, S_B, PV_A, PV_B so that each softmax
-// warpgroup works while the tensor core runs the other tile's GEMMs.  The
-// tensor pipe executes one thread's MMAs in order, so the commit of S_X(j+1)
-// also means PV_X(j) is done: that is what lets P alias S and lets the
-// softmax rescale O_X right after S_X(j+1) arrives.
+//                            rows through an MN-major descriptor (K = V)
+// S_X is double-buffered: S_X(k+1) is computed while the softmax works on
+// k, and S_X(k+2) is issued right after PV_X(k).  The tensor pipe executes
+// one thread's MMAs in order, so S_X(k+2) cannot overwrite P_X(k) before
+// PV_X(k) has read it.  The MMA warp interleaves the two tiles so that the
+// tensor core runs one tile's GEMMs while the other's softmax works.  A
+// softmax that must rescale O_X first waits for PV_X(k-1) (a barrier the
+// MMA warp commits after every PV).
 //
 // Warp roles (512 threads, persistent CTAs; registers rebalanced with
 // setmaxnreg to 176 / 176 / 72 / 88 per thread):
 //   warpgroup 0   softmax of tile A (thread r owns row r = TMEM lane r)
 //   warpgroup 1   softmax of tile B
 //   warpgroup 2   epilogue: O_X * (1/l) -> bf16 -> swizzled smem -> TMA store
-//   warpgroup 3   warp 12 TMA producer, warp 13 MMA issuer, warps 14-15 idle
+//   warpgroup 3   warp 12 TMA producer, warps 13 and 14 MMA issuers (tile A,
+//                 tile B), warp 15 idle; with CSA warp 13 issues for both
+//                 tiles and warps 14-15 gather the selected rows
 // Every wait is bounded (tc_ptx.cuh): on a timeout the CTA records
 // HCA_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -55,6 +60,7 @@ constexpr int kStages = 3;        // kv ring depth
 constexpr int kWG = 128;          // threads per warpgroup
 constexpr int kThreads = 4 * kWG;
 constexpr int kTmemCols = 512;    // S_A | S_B | O_A | O_B, 128 columns each
+constexpr int kHalfKeys = 64;     // keys of a half-block: S_X is two buffers of 64 columns
 __host__ __device__ constexpr uint32_t col_s(int x) { return (uint32_t)x * 128u; }        // S_X (P_X aliases it)
 __host__ __device__ constexpr uint32_t col_o(int x) { return 256u + (uint32_t)x * 128u; }  // O_X
 constexpr float kRescaleLog2 = 8.0f;
@@ -119,6 +125,12 @@ __device__ __forceinline__ void pair_ranges_warp(const FwdParams &p, const CsaPa
   }
 }
 
+// Half-blocks of a pair's key list: two per block, one for a last block of
+// at most 64 columns.
+__device__ __forceinline__ int half_blocks(const Tile &t) {
+  return 2 * (t.nb - 1) + (t.ncols - (t.nb - 1) * kBlockKeys > kHalfKeys ? 2 : 1);
+}
+
 __device__ __forceinline__ void setmaxnreg_inc_softmax() { asm volatile("setmaxnreg.inc.sync.aligned.u32 176;"); }
 __device__ __forceinline__ void setmaxnreg_dec_epilogue() { asm volatile("setmaxnreg.dec.sync.aligned.u32 72;"); }
 __device__ __forceinline__ void setmaxnreg_dec_producer() { asm volatile("setmaxnreg.dec.sync.aligned.u32 88;"); }
@@ -126,10 +138,10 @@ __device__ __forceinline__ void setmaxnreg_dec_producer() { asm volatile("setmax
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2], p_full[2];
+  uint64_t s_full[2][2], p_full[2][2], pv_done[2];  // [tile][buffer]: the softmax may finish k + 1 before the MMA waits for k
   uint64_t o_final[2], o_free[2];
   uint64_t st_full[2], st_free[2];
-  uint64_t epi, drain, never;
+  uint64_t epi, drain[2], never;
   float inv_l[2][kRows];
   uint32_t vis[kStages][kCsaMaxPos][4];  // CSA: per block, each pair position's bits of the compressed columns
   uint32_t tmem_base;
@@ -145,6 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(kD == 64 || kD == 128, "head dim 64 or 128");
   static_assert(!kCsa || kD == 128, "CSA gathers 128-dim rows");
   constexpr int kHalves = kD / 64;   // 64-column (128-byte) halves of a row
+  // MMA issue: warp 13 for tile A and warp 14 for tile B; with CSA, whose
+  // gather warps are 14-15, warp 13 issues for both tiles
+  constexpr int kMmaWarps = kCsa ? 1 : 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Bars bars;
@@ -155,22 +170,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&bars.q_full, 1);
-    mbar_init(&bars.q_empty, 1);
+    mbar_init(&bars.q_empty, kMmaWarps);
     for (int s = 0; s < kStages; ++s) {
       // CSA: the gather warps also arrive once their rows have landed
       mbar_init(&bars.kv_full[s], kCsa ? 1 + kGatherThreads : 1);
-      mbar_init(&bars.kv_empty[s], 1);
+      mbar_init(&bars.kv_empty[s], kMmaWarps);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&bars.s_full[x], 1);
-      mbar_init(&bars.p_full[x], kWG);
+      mbar_init(&bars.s_full[x][0], 1);
+      mbar_init(&bars.s_full[x][1], 1);
+      mbar_init(&bars.pv_done[x], 1);
+      mbar_init(&bars.p_full[x][0], kWG);
+      mbar_init(&bars.p_full[x][1], kWG);
       mbar_init(&bars.o_final[x], 1);
       mbar_init(&bars.o_free[x], kWG);
       mbar_init(&bars.st_full[x], kWG);
       mbar_init(&bars.st_free[x], kWG);
     }
     mbar_init(&bars.epi, kWG);
-    mbar_init(&bars.drain, 1);
+    mbar_init(&bars.drain[0], 1);
+    mbar_init(&bars.drain[1], 1);
     mbar_init(&bars.never, 1);
     bars.abort = 0;
     fence_mbar_init();
@@ -295,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars.kv_full[s]);
         }
       }
-    } else if (warp == 13) {
+    } else if (warp == 13 || (!kCsa && warp == 14)) {
       // ---------------------------------------------------------- MMA
       // The whole warp runs this loop on warp-uniform values (the pair's
       // ranges are broadcast from lane 0) and one elect.sync lane issues each
@@ -304,12 +323,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // same MMAs issued from a lane-0 branch cost 50-80 cycles, more than
       // the tensor pipe needs to execute an M=128, N=128, K=16 step (~65).
       // Descriptors are built once; an MMA only adds a constant offset.
+      //
+      // Half-block k of a pair is keys [64 (k & 1), 64 (k & 1) + 64) of block
+      // k >> 1.  Its S_X goes to TMEM buffer (hb + k) & 1 of tile X, so S_X of
+      // half-block k + 1 is ready while the softmax works on k; the order
+      //   S_A(0) S_B(0) S_A(1) S_B(1) | PV_A(0) S_A(2) PV_B(0) S_B(2) | ...
+      // issues S_X(k + 2) right after PV_X(k), which reads P_X(k) from the
+      // same buffer (the tensor pipe runs one thread's MMAs in order).
       const uint64_t dq0 = smem_desc_sw128(smem_u32(smem + kOffQ), 16, 1024);
       const uint64_t dq1 = smem_desc_sw128(smem_u32(smem + kOffQ + kTile), 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(smem + kOffKV), 16, 1024);         // K view of stage 0
       const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + kOffKV), kHalfTile, 1024);  // V view of stage 0
       const uint32_t id_pv = idesc_bf16_f32(kRows, kD, false, true);
-      uint32_t gb = 0, gq = 0, pcnt = 0;
+      const int x0 = kCsa ? 0 : warp - 13, x1 = kCsa ? 2 : x0 + 1;  // tiles this warp issues for
+      uint32_t gb = 0, gq = 0, hb = 0;  // blocks, pairs and half-blocks before this pair
       bool ok = !poisoned, issued = false;
       if (ok && p.stall) {
         injected_stall(&bars.never, abort_flag, p.status, p.wait_ns);
@@ -322,76 +349,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         uniform_tile(t);
         const int nb = t.nb;
         if (nb == 0) continue;
-        auto issue_s = [&](int x, int j, uint32_t g, uint64_t *extra) {
+        const int nh = half_blocks(t);
+        auto issue_s = [&](int x, int k) {
           int n, nc;
-          block_cols(t, j, n, nc);
-          const uint32_t idesc = idesc_bf16_f32(kRows, (n + 15) & ~15, false, false);
+          block_cols(t, k >> 1, n, nc);
+          const int h = k & 1;
+          const int w = h ? n - kHalfKeys : min(n, kHalfKeys);
+          const uint32_t idesc = idesc_bf16_f32(kRows, (w + 15) & ~15, false, false);
           const uint64_t da = x ? dq1 : dq0;
-          const uint64_t db = dk0 + desc_bytes((g % kStages) * kTile);
-          const uint32_t d = tmem + col_s(x);
+          const uint64_t db = dk0 + desc_bytes(((gb + (k >> 1)) % kStages) * kTile + h * kHalfKeys * 128);
+          const uint32_t buf = (hb + k) & 1;
+          const uint32_t d = tmem + col_s(x) + buf * kHalfKeys;
           if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < kD / 16; ++k) mma_ss(d, da + kmaj_step(k), db + kmaj_step(k), idesc, k > 0);
-            mma_commit(&bars.s_full[x]);
-            if (extra) mma_commit(extra);
+            for (int kk = 0; kk < kD / 16; ++kk) mma_ss(d, da + kmaj_step(kk), db + kmaj_step(kk), idesc, kk > 0);
+            mma_commit(&bars.s_full[x][buf]);
+            if (x == x1 - 1 && k == nh - 1) mma_commit(&bars.q_empty);
           }
           __syncwarp();
           issued = true;
+        };
+        auto issue_pv = [&](int x, int k) {
+          int n, nc;
+          block_cols(t, k >> 1, n, nc);
+          const int h = k & 1;
+          const int w = h ? n - kHalfKeys : min(n, kHalfKeys);
+          const int nks = (w + 15) >> 4;
+          const uint32_t st = (gb + (k >> 1)) % kStages;
+          const uint64_t dbv = dv0 + desc_bytes(st * kTile) + mnmaj_step(h * (kHalfKeys / 16));
+          const uint32_t d = tmem + col_o(x), a = tmem + col_s(x) + ((hb + k) & 1) * kHalfKeys;
+          const uint32_t acc0 = k > 0 ? 1u : 0u;
+          if (elect_one()) {
+            // a full half goes out as one straight run of MMAs: a branch
+            // between tcgen05.mma instructions slows their issue
+            if (nks == kHalfKeys / 16) {
+              mma_ts(d, a, dbv, id_pv, acc0);
+#pragma unroll
+              for (int kk = 1; kk < kHalfKeys / 16; ++kk) mma_ts(d, a + kk * 8, dbv + mnmaj_step(kk), id_pv, 1u);
+            } else {
+              for (int kk = 0; kk < nks; ++kk) mma_ts(d, a + kk * 8, dbv + mnmaj_step(kk), id_pv, kk > 0 ? 1u : acc0);
+            }
+            mma_commit(&bars.pv_done[x]);
+            if (k == nh - 1) mma_commit(&bars.o_final[x]);
+            if (x == x1 - 1 && (h == 1 || k == nh - 1)) mma_commit(&bars.kv_empty[st]);
+          }
+          __syncwarp();
         };
         ok = wait_warp(&bars.q_full, gq & 1, abort_flag, p.status, p.wait_ns);
         if (ok) ok = wait_warp(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status, p.wait_ns);
         if (ok) {
           tc_fence_after();
-          issue_s(0, 0, gb, nullptr);
-          issue_s(1, 0, gb, nb == 1 ? &bars.q_empty : nullptr);
+          for (int x = x0; x < x1; ++x) issue_s(x, 0);
+          if (nh > 1)
+            for (int x = x0; x < x1; ++x) issue_s(x, 1);
         }
-        for (int j = 0; ok && j < nb; ++j) {
-          const uint32_t g = gb + j;
-          const bool next = j + 1 < nb;
-          int n, nc;
-          block_cols(t, j, n, nc);
-          const int nks = (n + 15) >> 4;
-          const uint64_t dbv = dv0 + desc_bytes((g % kStages) * kTile);
-          for (int x = 0; ok && x < 2; ++x) {
-            ok = wait_warp(&bars.p_full[x], pcnt & 1, abort_flag, p.status, p.wait_ns);
-            if (ok && j == 0 && gq > 0) ok = wait_warp(&bars.o_free[x], (gq - 1) & 1, abort_flag, p.status, p.wait_ns);
+        for (int k = 0; ok && k < nh; ++k) {
+          const int k2 = k + 2;
+          for (int x = x0; ok && x < x1; ++x) {
+            ok = wait_warp(&bars.p_full[x][(hb + k) & 1], ((hb + k) >> 1) & 1, abort_flag, p.status, p.wait_ns);
+            if (ok && k == 0 && gq > 0) ok = wait_warp(&bars.o_free[x], (gq - 1) & 1, abort_flag, p.status, p.wait_ns);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t d = tmem + col_o(x), a = tmem + col_s(x);
-            const uint32_t acc0 = j > 0 ? 1u : 0u;
-            if (elect_one()) {
-              // a full block goes out as one straight run of MMAs: a branch
-              // between tcgen05.mma instructions slows their issue
-              if (nks == kBlockKeys / 16) {
-                mma_ts(d, a, dbv, id_pv, acc0);
-#pragma unroll
-                for (int kk = 1; kk < kBlockKeys / 16; ++kk) mma_ts(d, a + kk * 8, dbv + mnmaj_step(kk), id_pv, 1u);
-              } else {
-                for (int kk = 0; kk < nks; ++kk) mma_ts(d, a + kk * 8, dbv + mnmaj_step(kk), id_pv, kk > 0 ? 1u : acc0);
-              }
-              if (j == nb - 1) mma_commit(&bars.o_final[x]);
-              if (x == 1) mma_commit(&bars.kv_empty[g % kStages]);
-            }
-            __syncwarp();
-            if (next) {
-              if (x == 0) {
-                ok = wait_warp(&bars.kv_full[(g + 1) % kStages], ((g + 1) / kStages) & 1, abort_flag, p.status, p.wait_ns);
+            issue_pv(x, k);
+            if (k2 < nh) {
+              if (x == x0 && (k2 & 1) == 0) {
+                const uint32_t g2 = gb + (k2 >> 1);
+                ok = wait_warp(&bars.kv_full[g2 % kStages], (g2 / kStages) & 1, abort_flag, p.status, p.wait_ns);
                 if (!ok) break;
                 tc_fence_after();
               }
-              issue_s(x, j + 1, g + 1, (x == 1 && j + 1 == nb - 1) ? &bars.q_empty : nullptr);
+              issue_s(x, k2);
             }
           }
-          ++pcnt;
         }
         gb += nb;
+        hb += nh;
         ++gq;
       }
       if (!ok && issued) {
         volatile int never = 0;
-        if (elect_one()) mma_commit(&bars.drain);
+        if (elect_one()) mma_commit(&bars.drain[x0]);
         __syncwarp();
-        if (lane == 0) mbar_wait(&bars.drain, 0, &never, p.status, 100000000ull);
+        if (lane == 0) mbar_wait(&bars.drain[x0], 0, &never, p.status, 100000000ull);
         __syncwarp();
       }
     }
@@ -469,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int x = wg;  // 0: tile A, 1: tile B
     const int r = tid - x * kWG;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    uint32_t scnt = 0, gq = 0;
+    uint32_t hb = 0, gq = 0, scnt = 0;  // half-blocks and pairs before this one; blocks (CSA bits)
     bool ok = true;
     for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
       Tile t;
@@ -493,46 +532,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
+      const int nh = half_blocks(t);
       float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < nb; ++j) {
+      int a1 = 0, b1 = -1, a2 = 0, b2 = -1;  // the row's visible columns of the block: [a1, b1] compressed, [a2, b2] raw
+      uint32_t cbits[4] = {0u, 0u, 0u, 0u};
+      for (int k = 0; k < nh; ++k) {
+        const int j = k >> 1, h = k & 1;
         int n, nc;
         block_cols(t, j, n, nc);
-        const int nk = (n + 15) & ~15;
-        // the row's visible columns: [a1, b1] compressed, [a2, b2] raw
-        int a1, b1, a2, b2;
-        row_cols(t, iv, j, n, nc, a1, b1, a2, b2);
-        // S_X(j) ready; since S_X(j) was issued after PV_X(j-1), O_X is stable
-        if (!wait_warp(&bars.s_full[x], scnt & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
-        uint32_t cbits[4] = {0u, 0u, 0u, 0u};
+        const int nk = ((h ? n - kHalfKeys : min(n, kHalfKeys)) + 15) & ~15;
+        if (h == 0) row_cols(t, iv, j, n, nc, a1, b1, a2, b2);
+        const uint32_t buf = (hb + k) & 1;
+        if (!wait_warp(&bars.s_full[x][buf], ((hb + k) >> 1) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         if constexpr (kCsa) {
-          // the block's key tile (with the gather warps' bits) has landed:
-          // the MMA waited for it before S; this wait orders the bits' reads
-          const uint32_t sst = scnt % kStages;
-          if (!wait_warp(&bars.kv_full[sst], (scnt / kStages) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
-          if (iv.valid) {
+          if (h == 0) {
+            // the block's key tile (with the gather warps' bits) has landed:
+            // the MMA waited for it before S; this wait orders the bits' reads
+            const uint32_t sst = scnt % kStages;
+            if (!wait_warp(&bars.kv_full[sst], (scnt / kStages) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
 #pragma unroll
-            for (int w = 0; w < 4; ++w) cbits[w] = bars.vis[sst][ppos][w];
+            for (int w = 0; w < 4; ++w) cbits[w] = iv.valid ? bars.vis[sst][ppos][w] : 0u;
+            ++scnt;
           }
         }
-        ++scnt;
         tc_fence_after();
-        // One TMEM round trip brings the row's nk scores into registers; the
-        // masked row max, then exp2 / row sum / bf16 packing 32 columns at a
-        // time.  P_X overwrites the first nk/2 columns of S_X.  Columns outside
-        // the row's two ranges are masked -- that also covers the padding
-        // entries and the columns past n of a short block -- and a chunk that
-        // every row of the warp sees whole skips the per-element test
-        // (warp-uniform).
-        const uint32_t sbase = lane_addr + col_s(x);
-        uint32_t sv[kBlockKeys];
-        {
-          uint32_t* c0p = sv;
-          tmem_ld32(sbase, *reinterpret_cast<uint32_t(*)[32]>(c0p));
-          if (32 < nk) tmem_ld32(sbase + 32, *reinterpret_cast<uint32_t(*)[32]>(c0p + 32));
-          if (64 < nk) tmem_ld32(sbase + 64, *reinterpret_cast<uint32_t(*)[32]>(c0p + 64));
-          if (96 < nk) tmem_ld32(sbase + 96, *reinterpret_cast<uint32_t(*)[32]>(c0p + 96));
-          tmem_wait_ld();
-        }
+        // One TMEM round trip brings the row's nk scores of this half into
+        // registers; the masked row max, then exp2 / row sum / bf16 packing
+        // 32 columns at a time.  P_X overwrites the first nk/2 columns of the
+        // buffer.  Columns outside the row's two ranges are masked -- that
+        // also covers the padding entries and the columns past n of a short
+        // block -- and a chunk that every row of the warp sees whole skips
+        // the per-element test (warp-uniform).
+        const uint32_t sbase = lane_addr + col_s(x) + buf * kHalfKeys;
+        uint32_t sv[kHalfKeys];
+        tmem_ld32(sbase, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        if (32 < nk) tmem_ld32(sbase + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+        tmem_wait_ld();
         float mx;
         {
           // kPosScale: max of s, scaled after; otherwise min of s (scale < 0)
@@ -540,17 +575,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           // eight independent 3-input max chains keep the dependency depth short
           float mc[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) mc[k] = ninf;
+          for (int q = 0; q < 8; ++q) mc[q] = ninf;
 #pragma unroll
-          for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
-            if (c0 < nk) {
+          for (int cc = 0; cc < kHalfKeys; cc += 32) {
+            if (cc < nk) {
+              const int c0 = h * kHalfKeys + cc;  // column in the block
               if constexpr (kCsa) {
                 // compressed columns: this position's selection bits; raw: its window
                 const uint32_t vm = cbits[c0 >> 5] | (uint32_t)range_mask64(a2, b2, c0);
                 if (!__all_sync(0xffffffffu, vm == 0xffffffffu)) {
 #pragma unroll
                   for (int y = 0; y < 32; ++y)
-                    if (!((vm >> y) & 1u)) sv[c0 + y] = __float_as_uint(ninf);
+                    if (!((vm >> y) & 1u)) sv[cc + y] = __float_as_uint(ninf);
                 }
               } else {
                 const bool whole = (c0 >= a1 && c0 + 31 <= b1) || (c0 >= a2 && c0 + 31 <= b2);
@@ -558,15 +594,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const uint32_t vm = (uint32_t)(range_mask64(a1, b1, c0) | range_mask64(a2, b2, c0));
 #pragma unroll
                   for (int y = 0; y < 32; ++y)
-                    if (!((vm >> y) & 1u)) sv[c0 + y] = __float_as_uint(ninf);
+                    if (!((vm >> y) & 1u)) sv[cc + y] = __float_as_uint(ninf);
                 }
               }
 #pragma unroll
               for (int y = 0; y < 32; y += 16) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                  const float a0 = __uint_as_float(sv[c0 + y + 2 * k]), a1 = __uint_as_float(sv[c0 + y + 2 * k + 1]);
-                  mc[k] = kPosScale ? fmax3(mc[k], a0, a1) : fmin3(mc[k], a0, a1);
+                for (int q = 0; q < 8; ++q) {
+                  const float e0 = __uint_as_float(sv[cc + y + 2 * q]), e1 = __uint_as_float(sv[cc + y + 2 * q + 1]);
+                  mc[q] = kPosScale ? fmax3(mc[q], e0, e1) : fmin3(mc[q], e0, e1);
                 }
               }
             }
@@ -587,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (m_run > -INFINITY) {
             f = ex2_approx(m_run - mx);
             l_run *= f;
-            rescale_o = j > 0;
+            rescale_o = true;  // an earlier half-block of this pair had visible keys
           }
           m_run = mx;
         }
@@ -597,28 +633,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t nm2 = f32x2(__float_as_uint(-m_use), __float_as_uint(-m_use));
           uint64_t acc[4] = {0, 0, 0, 0};  // packed row sums (+0.0f bit patterns), four chains
 #pragma unroll
-          for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
-            if (c0 < nk) {
+          for (int cc = 0; cc < kHalfKeys; cc += 32) {
+            if (cc < nk) {
               uint32_t pk[16];
 #pragma unroll
               for (int y = 0; y < 32; y += 2) {
                 // masked scores are already +-inf, so exp2 gives exactly 0
                 float t0, t1;
-                f32x2_split(ffma2(f32x2(sv[c0 + y], sv[c0 + y + 1]), sl2x2, nm2), t0, t1);
+                f32x2_split(ffma2(f32x2(sv[cc + y], sv[cc + y + 1]), sl2x2, nm2), t0, t1);
                 const float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
                 const uint64_t e2 = f32x2(__float_as_uint(e0), __float_as_uint(e1));
                 acc[(y >> 1) & 3] = fadd2(acc[(y >> 1) & 3], e2);
                 pk[y >> 1] = pack_bf16x2(e0, e1);
               }
-              tmem_st16(lane_addr + col_s(x) + c0 / 2, pk);
+              tmem_st16(sbase + cc / 2, pk);
             }
           }
-          float a0, a1, b0, b1;
-          f32x2_split(fadd2(acc[0], acc[1]), a0, a1);
-          f32x2_split(fadd2(acc[2], acc[3]), b0, b1);
-          l_run += (a0 + a1) + (b0 + b1);
+          float a0, a1s, b0, b1s;
+          f32x2_split(fadd2(acc[0], acc[1]), a0, a1s);
+          f32x2_split(fadd2(acc[2], acc[3]), b0, b1s);
+          l_run += (a0 + a1s) + (b0 + b1s);
         }
         if (__any_sync(0xffffffffu, rescale_o)) {
+          // O_X holds the sum up to half-block k - 1 once that PV completes
+          // (S_X(k) only implies PV_X(k - 2))
+          if (!wait_warp(&bars.pv_done[x], (hb + k - 1) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+          tc_fence_after();
           uint32_t o[32];
 #pragma unroll
           for (int c0 = 0; c0 < kD; c0 += 32) {
@@ -631,9 +671,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars.p_full[x]);
+        mbar_arrive(&bars.p_full[x][buf]);
       }
       if (!ok) break;
+      hb += nh;
       // row statistics: lse to global, 1/l to the epilogue
       if (gq > 0 && !wait_warp(&bars.st_free[x], (gq - 1) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
       bars.inv_l[x][r] = l_run > 0.f ? 1.f / l_run : 0.f;
