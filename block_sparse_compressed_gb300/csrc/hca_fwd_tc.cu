@@ -35,7 +35,7 @@
 // MMA warp commits after every PV).
 //
 // Warp roles (512 threads, persistent CTAs; registers rebalanced with
-// setmaxnreg to 176 / 176 / 72 / 88 per thread):
+// setmaxnreg to 160 / 160 / 104 / 88 per thread):
 //   warpgroup 0   softmax of tile A (thread r owns row r = TMEM lane r)
 //   warpgroup 1   softmax of tile B
 //   warpgroup 2   epilogue: O_X * (1/l) -> bf16 -> swizzled smem -> TMA store
@@ -64,7 +64,7 @@ constexpr int kHalfKeys = 64;     // keys of a half-block: S_X is two buffers of
 __host__ __device__ constexpr uint32_t col_s(int x) { return (uint32_t)x * 128u; }        // S_X (P_X aliases it)
 __host__ __device__ constexpr uint32_t col_o(int x) { return 256u + (uint32_t)x * 128u; }  // O_X
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kRegSoftmax = 176, kRegEpilogue = 72, kRegProducer = 88;
+constexpr int kRegSoftmax = 160, kRegEpilogue = 104, kRegProducer = 88;
 static_assert(2 * kRegSoftmax + kRegEpilogue + kRegProducer == 512, "register split must fit the launch");
 
 // dynamic shared memory: Q_A | Q_B | kv ring | out staging A | B (+1 KB align)
@@ -131,8 +131,8 @@ __device__ __forceinline__ int half_blocks(const Tile &t) {
   return 2 * (t.nb - 1) + (t.ncols - (t.nb - 1) * kBlockKeys > kHalfKeys ? 2 : 1);
 }
 
-__device__ __forceinline__ void setmaxnreg_inc_softmax() { asm volatile("setmaxnreg.inc.sync.aligned.u32 176;"); }
-__device__ __forceinline__ void setmaxnreg_dec_epilogue() { asm volatile("setmaxnreg.dec.sync.aligned.u32 72;"); }
+__device__ __forceinline__ void setmaxnreg_inc_softmax() { asm volatile("setmaxnreg.inc.sync.aligned.u32 160;"); }
+__device__ __forceinline__ void setmaxnreg_dec_epilogue() { asm volatile("setmaxnreg.dec.sync.aligned.u32 104;"); }
 __device__ __forceinline__ void setmaxnreg_dec_producer() { asm volatile("setmaxnreg.dec.sync.aligned.u32 88;"); }
 
 struct Bars {
