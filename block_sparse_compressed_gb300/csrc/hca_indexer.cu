@@ -375,20 +375,44 @@ __global__ void __launch_bounds__(kTopkThreads) hca_index_topk_kernel(const Topk
     __syncthreads();
   }
   // prefix is the k-th largest key; rem of the keys equal to it are taken,
-  // the ones with the smallest entry index.  Ordered compaction:
-  int placed = 0, ties = 0;
-  for (int t0 = 0; t0 < n; t0 += kTopkThreads) {
-    const int t = t0 + tid;
-    const uint32_t kv = t < n ? keys[t] : 0u;
-    const bool eq = t < n && kv == prefix;
-    int eq_before;
-    const int eq_total = block_excl_scan(eq ? 1 : 0, eq_before, wsum);
-    const bool take = t < n && (kv > prefix || (eq && ties + eq_before < rem));
-    int pos;
-    const int take_total = block_excl_scan(take ? 1 : 0, pos, wsum);
-    if (take) out[placed + pos] = lo + t;
-    placed += take_total;
-    ties += eq_total;
+  // the ones with the smallest entry index.  Ordered compaction: warp w owns
+  // the keys [w L, (w + 1) L), swept 32 at a time.  A first sweep counts the
+  // warp's keys above and equal to prefix, one scan over the warps gives each
+  // its output and tie offsets, and a second sweep writes with ballots.
+  constexpr int kWarps = kTopkThreads / 32;
+  __shared__ int wgt[kWarps], weq[kWarps];
+  const int wid = tid >> 5;
+  const int L = ((n + kWarps - 1) / kWarps + 31) & ~31;
+  const int s0 = min(wid * L, n), s1 = min(s0 + L, n);
+  int gt = 0, eqc = 0;
+  for (int t0 = s0; t0 < s1; t0 += 32) {
+    const int t = t0 + lane;
+    const uint32_t kv = t < s1 ? keys[t] : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, t < s1 && kv > prefix));
+    eqc += __popc(__ballot_sync(0xffffffffu, t < s1 && kv == prefix));
+  }
+  if (lane == 0) {
+    wgt[wid] = gt;
+    weq[wid] = eqc;
+  }
+  __syncthreads();
+  int gt_run = 0, eq_run = 0;
+  for (int w = 0; w < wid; ++w) {
+    gt_run += wgt[w];
+    eq_run += weq[w];
+  }
+  int placed = gt_run + min(eq_run, rem);  // winners with a smaller entry index
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int t0 = s0; t0 < s1; t0 += 32) {
+    const int t = t0 + lane;
+    const uint32_t kv = t < s1 ? keys[t] : 0u;
+    const bool eq = t < s1 && kv == prefix;
+    const uint32_t beq = __ballot_sync(0xffffffffu, eq);
+    const bool take = t < s1 && (kv > prefix || (eq && eq_run + __popc(beq & lt) < rem));
+    const uint32_t btake = __ballot_sync(0xffffffffu, take);
+    if (take) out[placed + __popc(btake & lt)] = lo + t;
+    placed += __popc(btake);
+    eq_run += __popc(beq);
   }
 }
 
