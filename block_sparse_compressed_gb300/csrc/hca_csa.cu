@@ -274,9 +274,23 @@ __global__ void __launch_bounds__(ckk::kThreads, 1)
           const int c0 = j * kBlockKeys;
           const int n = min(kBlockKeys, ((cnt + 15) & ~15) - c0);
           uint8_t *dst = smem + kOffKV + s * kTile;
+          // entry ids first (lane holds rows lane + 32 jj), so that each
+          // copy's address is a shuffle away instead of a load's latency
+          int32_t eid[kBlockKeys / 32];
+#pragma unroll
+          for (int jj = 0; jj < kBlockKeys / 32; ++jj) {
+            const int r = lane + 32 * jj;
+            eid[jj] = r < n ? ent[c0 + r] : 0;
+          }
           for (int q = lane; q < n * 16; q += 32) {
             const int r = q >> 4, ch = q & 15;
-            const __nv_bfloat16 *src = p.ckv + ((size_t)t.b * Q.Sc + ent[c0 + r]) * kHeadDim + ch * 8;
+            int32_t e = 0;
+#pragma unroll
+            for (int jj = 0; jj < kBlockKeys / 32; ++jj) {
+              const int32_t ej = __shfl_sync(0xffffffffu, eid[jj], r & 31);
+              if ((r >> 5) == jj) e = ej;
+            }
+            const __nv_bfloat16 *src = p.ckv + ((size_t)t.b * Q.Sc + e) * kHeadDim + ch * 8;
             cp_async16(smem_u32(dst + sw128_offset(r, ch)), src);
           }
           // visibility bits: word w of position pp = columns [32 w, 32 w + 32)

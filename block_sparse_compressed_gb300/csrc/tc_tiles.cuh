@@ -221,9 +221,23 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __device__ __forceinline__ void gather_block(const int32_t *ent, const uint32_t *msk, int cnt, int c0, int nc,
                                              const __nv_bfloat16 *ckv_b, uint8_t *dst, int part, int nparts,
                                              int npos, int wlo, int whi, uint32_t *vis /* [npos][4] */, int lane) {
+  // the block's entry ids, loaded together (lane holds rows lane + 32 j), so
+  // that each copy's address is a shuffle away instead of a load's latency
+  int32_t eid[kBlockKeys / 32];
+#pragma unroll
+  for (int j = 0; j < kBlockKeys / 32; ++j) {
+    const int r = lane + 32 * j;
+    eid[j] = r < nc ? ent[c0 + r] : 0;
+  }
   for (int q = lane; q < 16 * ((nc + nparts - 1) / nparts); q += 32) {
     const int r = part + nparts * (q >> 4), ch = q & 15;
-    if (r < nc) cp_async16(smem_u32(dst + sw128_offset(r, ch)), ckv_b + (size_t)ent[c0 + r] * kHeadDim + ch * 8);
+    int32_t e = 0;
+#pragma unroll
+    for (int j = 0; j < kBlockKeys / 32; ++j) {
+      const int32_t ej = __shfl_sync(0xffffffffu, eid[j], r & 31);
+      if ((r >> 5) == j) e = ej;
+    }
+    if (r < nc) cp_async16(smem_u32(dst + sw128_offset(r, ch)), ckv_b + (size_t)e * kHeadDim + ch * 8);
   }
   for (int w = wlo; w < whi; ++w) {
     const int c = 32 * w + lane;
