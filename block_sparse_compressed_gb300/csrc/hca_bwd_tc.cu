@@ -62,7 +62,7 @@ constexpr int kOffQ = 0, kOffDO = kTile, kOffO = 2 * kTile, kOffKV = 3 * kTile;
 constexpr int kOffOut = kOffKV + kStages * kTile;
 constexpr int kSmemBytes = kOffOut + kTile + 1024;
 constexpr int kDescSlots = 8;
-constexpr int kDescReaders = 11;  // dS warps 0-7, MMA warp 9, Delta warps 10-11 (CSA: gather warp 10, Delta warp 11)
+constexpr int kDescReaders = 11;  // dS warps 0-7, MMA warp 9, Delta warps 10-11 (CSA: warp 10 gathers, warp 11 gathers and forms Delta)
 constexpr int kDeltaThreads = 64;
 constexpr int kCsaMaxPos = 4;     // CSA: positions per tile whose bits are kept (Pq <= 4)
 }  // namespace dqk
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
     mbar_init(&bars.qd_empty, 1 + (kCsa ? 32 : kDeltaThreads));
     for (int s = 0; s < kStages; ++s) {
       // CSA: the gather warp also arrives once its rows have landed
-      mbar_init(&bars.kv_full[s], kCsa ? 1 + 32 : 1);
+      mbar_init(&bars.kv_full[s], kCsa ? 1 + 64 : 1);  // CSA: both gather warps' lanes arrive too
       mbar_init(&bars.kv_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
           if (!ok) break;
           int n, nc;
           block_cols(t, j, n, nc);
-          gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, 0, 1, Q.Pq, 0, 4,
+          gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, 0, 2, Q.Pq, 0, 2,
                        &bars.vis[s][0][0], lane);
           cp_async_wait_all();
           fence_async_smem();
@@ -426,8 +426,28 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       // memory and, as -scale*Delta, in the row records the dkv kernel reads.
       constexpr int kRowsPerLane = kCsa ? 4 : 2;
       const int dt = kCsa ? lane : tid - (kEW + 64);
-      uint32_t tw = 0, kd = 0;
+      uint32_t tw = 0, kd = 0, gb = 0;
       bool ok = true;
+      // CSA: this warp also copies every other gathered row (part 1 of 2):
+      // a tile's block 0 before its Delta (it does not wait for the tile's
+      // q / dO / out), the other blocks after
+      auto gather_share = [&](const Tile &t, int j) -> bool {
+        const int s = gb % kStages;
+        if (gb >= (uint32_t)kStages &&
+            !wait_warp(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns))
+          return false;
+        const long long grp = (long long)t.b * Q.ntq + t.i0 / Q.Pq;
+        int n, nc;
+        block_cols(t, j, n, nc);
+        gather_block(p.u_ent + grp * p.u_cap, p.u_mask + grp * p.u_cap, t.chi, j * kBlockKeys, nc,
+                     p.ckv + (size_t)t.b * Q.Sc * kD, smem + kOffKV + s * kTile, 1, 2, Q.Pq, 2, 4, &bars.vis[s][0][0],
+                     lane);
+        cp_async_wait_all();
+        fence_async_smem();
+        mbar_arrive(&bars.kv_full[s]);
+        ++gb;
+        return true;
+      };
       const uint8_t *dobuf = smem + kOffDO;
       const uint8_t *outbuf = smem + kOffO;
       while (ok) {
@@ -436,6 +456,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         ok = read_dq_desc(bars, kd++, t, u, abort_flag, p.status, p.wait_ns);
         if (!ok || u < 0) break;
         if (poisoned || t.nb == 0) continue;
+        if (kCsa && !gather_share(t, 0)) { ok = false; break; }
         if (!wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         float dl[kRowsPerLane];
 #pragma unroll
@@ -464,6 +485,8 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         for (int h = 0; h < kRowsPerLane; ++h) bars.delta[dt + (kRows / kRowsPerLane) * h] = dl[h];
         mbar_arrive(&bars.stat_full);
         ++tw;
+        if (kCsa)
+          for (int j = 1; ok && j < t.nb; ++j) ok = gather_share(t, j);
       }
     }
   } else {
