@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kUnionThreads) csa_union_kernel(const UnionArg
 namespace ckk {
 constexpr int kStages = 2;
 constexpr int kEW = 256;                  // two warpgroups, 64 key columns each
-constexpr int kThreads = kEW + 128;       // + TMA warp, MMA warp, gather warp, idle warp
+constexpr int kThreads = kEW + 128;       // + TMA warp, MMA warp, two gather warps
 constexpr int kRegEW = 192, kRegProducer = 120;
 static_assert(2 * 128 * kRegEW + 128 * kRegProducer <= kThreads * 168, "register split must fit the launch");
 constexpr uint32_t kColS = 0, kColDP = 128, kColD = 256;  // D: two 128-column buffers
@@ -144,7 +144,7 @@ constexpr int kOffQ = 0, kOffDO = kTile, kOffKV = 2 * kTile;
 constexpr int kOffP = kOffKV + kStages * kTile, kOffDS = kOffP + kTile;
 constexpr int kSmemBytes = kOffDS + kTile + 1024;
 constexpr int kMaxPos = 4;                // positions per tile (H a multiple of 32)
-constexpr int kGather = 32;               // gather threads
+constexpr int kGather = 64;               // gather threads (two warps, alternate rows)
 }  // namespace ckk
 
 struct DckvParams {
@@ -252,11 +252,14 @@ __global__ void __launch_bounds__(ckk::kThreads, 1)
         volatile int never = 0;
         mbar_wait(&bars.q_full, q_par, &never, p.status, 100000000ull);
       }
-    } else if (warp == kEW / 32 + 2) {
+    } else if (warp >= kEW / 32 + 2) {
       // ------------------------------------------------------------ gather: the union's ckv rows
       // Each block's entries are copied 16 bytes at a time into the 128B-
       // swizzled tile layout the MMA descriptors read; the per-position
-      // visibility bits of the block go to shared memory beside them.
+      // visibility bits of the block go to shared memory beside them.  Two
+      // warps: `part` copies rows part, part + 2, ... and bit words 2 part,
+      // 2 part + 1 (one warp's copies are issue-bound).
+      const int part = warp - (kEW / 32 + 2);
       uint32_t gb = 0;
       bool ok = !poisoned;
       for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
@@ -282,19 +285,21 @@ __global__ void __launch_bounds__(ckk::kThreads, 1)
             const int r = lane + 32 * jj;
             eid[jj] = r < n ? ent[c0 + r] : 0;
           }
-          for (int q = lane; q < n * 16; q += 32) {
-            const int r = q >> 4, ch = q & 15;
+          for (int q = lane; q < ((n + 1) / 2) * 16; q += 32) {
+            const int r = part + 2 * (q >> 4), ch = q & 15;
             int32_t e = 0;
 #pragma unroll
             for (int jj = 0; jj < kBlockKeys / 32; ++jj) {
               const int32_t ej = __shfl_sync(0xffffffffu, eid[jj], r & 31);
               if ((r >> 5) == jj) e = ej;
             }
-            const __nv_bfloat16 *src = p.ckv + ((size_t)t.b * Q.Sc + e) * kHeadDim + ch * 8;
-            cp_async16(smem_u32(dst + sw128_offset(r, ch)), src);
+            if (r < n) {
+              const __nv_bfloat16 *src = p.ckv + ((size_t)t.b * Q.Sc + e) * kHeadDim + ch * 8;
+              cp_async16(smem_u32(dst + sw128_offset(r, ch)), src);
+            }
           }
           // visibility bits: word w of position pp = columns [32 w, 32 w + 32)
-          for (int w = 0; w < 4; ++w) {
+          for (int w = 2 * part; w < 2 * part + 2; ++w) {
             const int c = c0 + 32 * w + lane;
             const uint32_t mk = (32 * w + lane < n && c < cnt) ? msk[c] : 0u;
             for (int pp = 0; pp < Q.Pq; ++pp) {
