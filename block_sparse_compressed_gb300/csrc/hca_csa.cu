@@ -285,7 +285,8 @@ __global__ void __launch_bounds__(ckk::kThreads, 1)
             const int r = lane + 32 * jj;
             eid[jj] = r < n ? ent[c0 + r] : 0;
           }
-          for (int q = lane; q < ((n + 1) / 2) * 16; q += 32) {
+          // the same number of passes for every lane (whole-warp shuffles)
+          for (int q = lane; q < ((((n + 1) / 2) * 16 + 31) & ~31); q += 32) {
             const int r = part + 2 * (q >> 4), ch = q & 15;
             int32_t e = 0;
 #pragma unroll

@@ -173,7 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.q_empty, kMmaWarps);
     for (int s = 0; s < kStages; ++s) {
       // CSA: the gather warps also arrive once their rows have landed
-      mbar_init(&bars.kv_full[s], kCsa ? 1 + kGatherThreads : 1);
+      // CSA: every lane of the TMA warp and of the two gather warps arrives
+      mbar_init(&bars.kv_full[s], kCsa ? 32 + kGatherThreads : 1);
       mbar_init(&bars.kv_empty[s], kMmaWarps);
     }
     for (int x = 0; x < 2; ++x) {
@@ -251,28 +252,50 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-          for (int j = 0; ok && j < nb; ++j, ++gb) {
+          for (int j = 0; !kCsa && ok && j < nb; ++j, ++gb) {
             const int s = gb % kStages;
             if (gb >= (uint32_t)kStages)
               ok = mbar_wait(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
             if (!ok) break;
             int n, nc;
             block_cols(t, j, n, nc);
-            if (kCsa) {
-              // raw rows only: the gather warps bring the compressed ones
-              mbar_arrive_expect_tx(&bars.kv_full[s], nc == n ? 0u : raw_load_bytes(n, nc));
-              if (nc < n) load_block_raw(t, j, n, nc, &map_kv, &map_kv16, &bars.kv_full[s], smem + kOffKV + s * kTile);
-            } else {
-              mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes<kHalves>(n, nc));
-              load_block<kHalves>(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
-                                  smem + kOffKV + s * kTile);
-            }
+            mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes<kHalves>(n, nc));
+            load_block<kHalves>(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
+                                smem + kOffKV + s * kTile);
             issued = (issued | (1u << s)) & ~(1u << (8 + s));
             issued |= ((gb / kStages) & 1u) << (8 + s);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         gb = __shfl_sync(0xffffffffu, gb, 0);
+        if constexpr (kCsa) {
+          // CSA: lane 0 loads the raw rows by TMA and the whole warp copies a
+          // third of the gathered rows (the gather is issue-bound per warp);
+          // every lane joins the block's kv_full arrival once its copies land
+          const long long grp = (long long)t.b * p.ntp + t.i0 / (2 * Q.Pq);
+          const int32_t *ent = cp.u_ent + grp * cp.u_cap;
+          const uint32_t *msk = cp.u_mask + grp * cp.u_cap;
+          const __nv_bfloat16 *ckv_b = cp.ckv + (size_t)t.b * Q.Sc * kHeadDim;
+          for (int j = 0; ok && j < nb; ++j, ++gb) {
+            const int s = gb % kStages;
+            if (gb >= (uint32_t)kStages)
+              ok = wait_warp(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
+            if (!ok) break;
+            int n, nc;
+            block_cols(t, j, n, nc);
+            if (lane == 0) {
+              mbar_expect_tx(&bars.kv_full[s], nc == n ? 0u : raw_load_bytes(n, nc));
+              if (nc < n) load_block_raw(t, j, n, nc, &map_kv, &map_kv16, &bars.kv_full[s], smem + kOffKV + s * kTile);
+              issued = (issued | (1u << s)) & ~(1u << (8 + s));
+              issued |= ((gb / kStages) & 1u) << (8 + s);
+            }
+            gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, 2, 3, 2 * Q.Pq, 0,
+                         0, &bars.vis[s][0][0], lane);
+            cp_async_wait_all();
+            fence_async_smem();
+            mbar_arrive(&bars.kv_full[s]);
+          }
+        }
         ++gq;
       }
       if (!ok && !poisoned && lane == 0) {
@@ -307,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           int n, nc;
           block_cols(t, j, n, nc);
-          gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, part, 2,
+          gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, part, 3,
                        2 * Q.Pq, 2 * part, 2 * part + 2, &bars.vis[s][0][0], lane);
           cp_async_wait_all();
           fence_async_smem();

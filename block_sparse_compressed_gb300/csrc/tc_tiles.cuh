@@ -229,7 +229,10 @@ __device__ __forceinline__ void gather_block(const int32_t *ent, const uint32_t 
     const int r = lane + 32 * j;
     eid[j] = r < nc ? ent[c0 + r] : 0;
   }
-  for (int q = lane; q < 16 * ((nc + nparts - 1) / nparts); q += 32) {
+  // every lane runs the same number of passes (the shuffles below need the
+  // whole warp): the bound is rounded up to a multiple of 32
+  const int nq = (16 * ((nc + nparts - 1) / nparts) + 31) & ~31;
+  for (int q = lane; q < nq; q += 32) {
     const int r = part + nparts * (q >> 4), ch = q & 15;
     int32_t e = 0;
 #pragma unroll
