@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
     mbar_init(&bars.qd_empty, 1 + (kCsa ? 32 : kDeltaThreads));
     for (int s = 0; s < kStages; ++s) {
       // CSA: the gather warp also arrives once its rows have landed
-      mbar_init(&bars.kv_full[s], kCsa ? 1 + 64 : 1);  // CSA: both gather warps' lanes arrive too
+      mbar_init(&bars.kv_full[s], kCsa ? 96 : 1);  // CSA: every lane of the TMA warp and the two gather warps
       mbar_init(&bars.kv_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
@@ -256,27 +256,48 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
               }
             }
           }
-          for (int j = 0; ok && j < nb; ++j, ++gb) {
+          for (int j = 0; !kCsa && ok && j < nb; ++j, ++gb) {
             const int s = gb % kStages;
             if (gb >= (uint32_t)kStages)
               ok = mbar_wait(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
             if (!ok) break;
             int n, nc;
             block_cols(t, j, n, nc);
-            if (kCsa) {
-              // raw rows only: the gather warp brings the compressed ones
-              mbar_arrive_expect_tx(&bars.kv_full[s], nc == n ? 0u : raw_load_bytes(n, nc));
-              if (nc < n) load_block_raw(t, j, n, nc, &map_kv, &map_kv16, &bars.kv_full[s], smem + kOffKV + s * kTile);
-            } else {
-              mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes<kHalves>(n, nc));
-              load_block<kHalves>(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
-                                  smem + kOffKV + s * kTile);
-            }
+            mbar_arrive_expect_tx(&bars.kv_full[s], block_load_bytes<kHalves>(n, nc));
+            load_block<kHalves>(t, j, n, nc, &map_kv, &map_ckv, &map_kv16, &map_ckv16, &bars.kv_full[s],
+                                smem + kOffKV + s * kTile);
             last_par[s] = (gb / kStages) & 1;
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         gb = __shfl_sync(0xffffffffu, gb, 0);
+        if constexpr (kCsa) {
+          // CSA: lane 0 loads the raw rows by TMA and the whole warp copies a
+          // third of the gathered rows (the gather is issue-bound per warp);
+          // every lane joins the block's kv_full arrival once its copies land
+          const long long grp = (long long)t.b * Q.ntq + t.i0 / Q.Pq;
+          const int32_t *ent = p.u_ent + grp * p.u_cap;
+          const uint32_t *msk = p.u_mask + grp * p.u_cap;
+          const __nv_bfloat16 *ckv_b = p.ckv + (size_t)t.b * Q.Sc * kD;
+          for (int j = 0; ok && j < nb; ++j, ++gb) {
+            const int s = gb % kStages;
+            if (gb >= (uint32_t)kStages)
+              ok = wait_warp(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
+            if (!ok) break;
+            int n, nc;
+            block_cols(t, j, n, nc);
+            if (lane == 0) {
+              mbar_expect_tx(&bars.kv_full[s], nc == n ? 0u : raw_load_bytes(n, nc));
+              if (nc < n) load_block_raw(t, j, n, nc, &map_kv, &map_kv16, &bars.kv_full[s], smem + kOffKV + s * kTile);
+              last_par[s] = (gb / kStages) & 1;
+            }
+            gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, 2, 3, Q.Pq, 0, 0,
+                         &bars.vis[s][0][0], lane);
+            cp_async_wait_all();
+            fence_async_smem();
+            mbar_arrive(&bars.kv_full[s]);
+          }
+        }
         ++tw;
       }
       if (!ok && !poisoned && lane == 0) {
@@ -411,7 +432,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
           if (!ok) break;
           int n, nc;
           block_cols(t, j, n, nc);
-          gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, 0, 2, Q.Pq, 0, 2,
+          gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, 0, 3, Q.Pq, 0, 2,
                        &bars.vis[s][0][0], lane);
           cp_async_wait_all();
           fence_async_smem();
@@ -428,7 +449,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       const int dt = kCsa ? lane : tid - (kEW + 64);
       uint32_t tw = 0, kd = 0, gb = 0;
       bool ok = true;
-      // CSA: this warp also copies every other gathered row (part 1 of 2):
+      // CSA: this warp also copies a third of the gathered rows (part 1 of 3):
       // a tile's block 0 before its Delta (it does not wait for the tile's
       // q / dO / out), the other blocks after
       auto gather_share = [&](const Tile &t, int j) -> bool {
@@ -440,7 +461,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         int n, nc;
         block_cols(t, j, n, nc);
         gather_block(p.u_ent + grp * p.u_cap, p.u_mask + grp * p.u_cap, t.chi, j * kBlockKeys, nc,
-                     p.ckv + (size_t)t.b * Q.Sc * kD, smem + kOffKV + s * kTile, 1, 2, Q.Pq, 2, 4, &bars.vis[s][0][0],
+                     p.ckv + (size_t)t.b * Q.Sc * kD, smem + kOffKV + s * kTile, 1, 3, Q.Pq, 2, 4, &bars.vis[s][0][0],
                      lane);
         cp_async_wait_all();
         fence_async_smem();
