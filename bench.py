@@ -701,9 +701,45 @@ def run_csa(args):
 
 
 def run_ncu_case(args):
+    """One small run of a path for a profiler capture (S = --ncu-case): the
+    HCA fwd+bwd by default, else the path --mode names."""
     import torch
     from block_sparse_compressed_gb300 import hca
     from block_sparse_compressed_gb300 import inputs as I
+    S = args.ncu_case
+    dev = torch.device("cuda", 0)
+    if args.mode == "compress":
+        B, D, m = 4, 128, 128
+        x = I.normal((B, S, D), 1, torch.bfloat16, dev)
+        g = I.normal((B, S), 2, torch.float32, dev)
+        bias = I.normal((m,), 3, torch.float32, dev)
+        for _ in range(args.warmup + 1):
+            ckv = hca.hca_compress_fwd(x, g, bias, None, m)
+            hca.hca_compress_bwd(x, g, bias, None, m, ckv)
+        torch.cuda.synchronize()
+        print(json.dumps({"ncu_case": f"compressor B{B} S{S} D{D} m{m}", "ok": True}))
+        return 0
+    if args.mode == "indexer":
+        Hi, m, k = 64, 4, 512
+        qi = I.normal((1, S, Hi, 128), 1, torch.bfloat16, dev)
+        ki = I.normal((1, (S + m - 1) // m, 128), 2, torch.bfloat16, dev)
+        wt = I.normal((1, S, Hi), 3, torch.float32, dev)
+        for _ in range(args.warmup + 1):
+            hca.hca_indexer_topk(qi, ki, wt, None, m, k)
+        torch.cuda.synchronize()
+        print(json.dumps({"ncu_case": f"indexer B1 S{S} Hi{Hi} Di128 m{m} k{k}", "ok": True}))
+        return 0
+    if args.mode == "csa":
+        H, D, W, m, k = 64, 128, 128, 4, 256
+        w = I.Workload(f"csa fwd+bwd bf16 B1 H{H} S{S} D{D} W{W} m{m} k{k}", 1, H, S, D, W, m, torch.bfloat16)
+        q, kv, ckv, _, dout = I.tensors(w, device=dev)
+        sel = I.random_selection(1, S, m, k, 77, extra=0).to(dev)
+        for _ in range(args.warmup + 1):
+            out, lse = hca.hca_csa_attn_fwd(q, kv, ckv, None, sel, W, m, w.scale)
+            hca.hca_csa_attn_bwd(q, kv, ckv, None, sel, out, lse, dout, W, m, w.scale)
+        torch.cuda.synchronize()
+        print(json.dumps({"ncu_case": w.name, "ok": True}))
+        return 0
     base = workload()
     w = I.Workload(f"fwd+bwd bf16 B1 H64 S{args.ncu_case} D128 W128 m128", base.B, base.H, args.ncu_case, base.D,
                    base.W, base.m, base.dtype)
