@@ -335,13 +335,21 @@ __global__ void __launch_bounds__(kTopkThreads) hca_index_topk_kernel(const Topk
     const uint32_t dmask = (1u << bits) - 1u;
     for (int d = tid; d < kRadixBins; d += kTopkThreads) hist[d] = 0;
     __syncthreads();
-    for (int t0 = 0; t0 < n; t0 += kTopkThreads) {
-      const int t = t0 + tid;
-      const uint32_t kv = t < n ? keys[t] : 0u;
-      const bool in = t < n && (kv & mask) == prefix;
-      const uint32_t dg = in ? (kv >> shift) & dmask : 0xffffffffu;
-      const unsigned peers = __match_any_sync(0xffffffffu, dg);
-      if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
+    if (pass == 0) {
+      for (int t0 = 0; t0 < n; t0 += kTopkThreads) {
+        const int t = t0 + tid;
+        const uint32_t kv = t < n ? keys[t] : 0u;
+        const uint32_t dg = t < n ? (kv >> shift) & dmask : 0xffffffffu;
+        const unsigned peers = __match_any_sync(0xffffffffu, dg);
+        if (t < n && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
+      }
+    } else {
+      // only the keys under the prefix count, a few percent of them, with
+      // digits spread over the bins: plain atomics
+      for (int t = tid; t < n; t += kTopkThreads) {
+        const uint32_t kv = keys[t];
+        if ((kv & mask) == prefix) atomicAdd(&hist[(kv >> shift) & dmask], 1);
+      }
     }
     __syncthreads();
     // digit from the top where the running count reaches rem: thread t owns
