@@ -34,11 +34,19 @@
 // softmax that must rescale O_X first waits for PV_X(k-1) (a barrier the
 // MMA warp commits after every PV).
 //
+// q is double-buffered over a CTA's pairs: the next pair's q tiles are
+// requested while the current pair runs (their load takes several thousand
+// cycles, which a single buffer exposed at every pair boundary).  The buffer
+// of a finished pair holds no live q any more -- O_X is final only after
+// every MMA of tile X -- so the epilogue stages the pair's output there, and
+// the buffer is reloaded once the output stores have read it.
+//
 // Warp roles (512 threads, persistent CTAs; registers rebalanced with
 // setmaxnreg to 160 / 160 / 104 / 88 per thread):
 //   warpgroup 0   softmax of tile A (thread r owns row r = TMEM lane r)
 //   warpgroup 1   softmax of tile B
-//   warpgroup 2   epilogue: O_X * (1/l) -> bf16 -> swizzled smem -> TMA store
+//   warpgroup 2   epilogue: O_X * (1/l) -> bf16 -> swizzled smem (the pair's
+//                 q buffer) -> TMA store
 //   warpgroup 3   warp 12 TMA producer, warps 13 and 14 MMA issuers (tile A,
 //                 tile B), warp 15 idle; with CSA warp 13 issues for both
 //                 tiles and warps 14-15 gather the selected rows
@@ -67,11 +75,12 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr int kRegSoftmax = 160, kRegEpilogue = 104, kRegProducer = 88;
 static_assert(2 * kRegSoftmax + kRegEpilogue + kRegProducer == 512, "register split must fit the launch");
 
-// dynamic shared memory: Q_A | Q_B | kv ring | out staging A | B (+1 KB align)
+// dynamic shared memory: q ring of two pairs (Q_A | Q_B each; a finished
+// pair's q buffer becomes its output staging) | kv ring (+1 KB align)
 constexpr int kOffQ = 0;
-constexpr int kOffKV = 2 * kTile;
-constexpr int kOffOut = kOffKV + kStages * kTile;
-constexpr int kSmemBytes = kOffOut + 2 * kTile + 1024;
+constexpr int kQBuf = 2 * kTile;  // one pair's q tiles, later its output tiles
+constexpr int kOffKV = kOffQ + 2 * kQBuf;
+constexpr int kSmemBytes = kOffKV + kStages * kTile + 1024;
 constexpr int kCsaMaxPos = 8;     // positions of a pair whose bits CSA keeps (Pq <= 4)
 constexpr int kGatherThreads = 64;  // CSA: warps 14 and 15 gather the compressed rows
 
@@ -136,7 +145,8 @@ __device__ __forceinline__ void setmaxnreg_dec_epilogue() { asm volatile("setmax
 __device__ __forceinline__ void setmaxnreg_dec_producer() { asm volatile("setmaxnreg.dec.sync.aligned.u32 88;"); }
 
 struct Bars {
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];  // q ring; a buffer is empty once the pair's output stores have read it
+  Tile tile[2];                    // geometry of the pair in each q buffer (nb < 0: end of the schedule)
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2][2], p_full[2][2], pv_done[2];  // [tile][buffer]: the softmax may finish k + 1 before the MMA waits for k
   uint64_t o_final[2], o_free[2];
@@ -169,8 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const QTiling &Q = p.qt;
 
   if (tid == 0) {
-    mbar_init(&bars.q_full, 1);
-    mbar_init(&bars.q_empty, kMmaWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars.q_full[b], 1);
+      mbar_init(&bars.q_empty[b], 1);
+    }
     for (int s = 0; s < kStages; ++s) {
       // CSA: the gather warps also arrive once their rows have landed
       // CSA: every lane of the TMA warp and of the two gather warps arrives
@@ -217,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&map_ckv16);
       }
       uint32_t gb = 0, gq = 0;
-      uint32_t issued = 0;  // bit s: stage s loaded at least once; bit 8+s: parity of its last load
-      int q_par = -1;
+      uint32_t issued = 0;    // bit s: stage s loaded at least once; bit 8+s: parity of its last load
+      uint32_t q_issued = 0;  // the same for the two q buffers
       bool ok = !poisoned;
       for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
         Tile t;
@@ -227,18 +239,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nb = t.nb;
         if (nb == 0) continue;
         if (lane == 0) {
-          if (gq > 0) ok = mbar_wait(&bars.q_empty, (gq - 1) & 1, abort_flag, p.status, p.wait_ns);
+          // q buffer gq mod 2: free once pair gq - 2's output has left it, so
+          // a pair's q is requested while the pair before it still runs
+          const uint32_t qb = gq & 1;
+          if (gq >= 2) ok = mbar_wait(&bars.q_empty[qb], ((gq >> 1) - 1) & 1, abort_flag, p.status, p.wait_ns);
           if (ok) {
+            // the MMA warps take the pair's geometry from here once q_full completes
+            bars.tile[qb] = t;
             const bool has_b = t.i0 + Q.Pq < Q.S;
-            mbar_arrive_expect_tx(&bars.q_full, (has_b ? 2 : 1) * kHalves * kHalfTile);
+            mbar_arrive_expect_tx(&bars.q_full[qb], (has_b ? 2 : 1) * kHalves * kHalfTile);
             const int c2 = t.b * Q.H + t.g * Q.HG;
+            uint8_t *qdst = smem + kOffQ + qb * kQBuf;
 #pragma unroll
             for (int hh = 0; hh < kHalves; ++hh) {
-              tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + hh * kHalfTile, 64 * hh, t.i0, c2);
-              if (has_b)
-                tma_load_3d(&map_q, &bars.q_full, smem + kOffQ + kTile + hh * kHalfTile, 64 * hh, t.i0 + Q.Pq, c2);
+              tma_load_3d(&map_q, &bars.q_full[qb], qdst + hh * kHalfTile, 64 * hh, t.i0, c2);
+              if (has_b) tma_load_3d(&map_q, &bars.q_full[qb], qdst + kTile + hh * kHalfTile, 64 * hh, t.i0 + Q.Pq, c2);
             }
-            q_par = gq & 1;
+            q_issued = (q_issued | (1u << qb)) & ~(1u << (8 + qb));
+            q_issued |= ((gq >> 1) & 1u) << (8 + qb);
             // this CTA's next pair: its q rows go to L2 now
             const long long un = u + gridDim.x;
             if (un < p.npairs) {
@@ -298,11 +316,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++gq;
       }
+      if (ok && lane == 0) {
+        // end of the schedule: a pair with nb < 0 in the next slot
+        const uint32_t qb = gq & 1;
+        if (gq >= 2) ok = mbar_wait(&bars.q_empty[qb], ((gq >> 1) - 1) & 1, abort_flag, p.status, p.wait_ns);
+        if (ok) {
+          bars.tile[qb].nb = -1;
+          mbar_arrive(&bars.q_full[qb]);
+        }
+      }
       if (!ok && !poisoned && lane == 0) {
         volatile int never = 0;
         for (int s = 0; s < kStages; ++s)
           if (issued & (1u << s)) mbar_wait(&bars.kv_full[s], (issued >> (8 + s)) & 1u, &never, p.status, 100000000ull);
-        if (q_par >= 0) mbar_wait(&bars.q_full, q_par, &never, p.status, 100000000ull);
+        for (int b = 0; b < 2; ++b)
+          if (q_issued & (1u << b)) mbar_wait(&bars.q_full[b], (q_issued >> (8 + b)) & 1u, &never, p.status, 100000000ull);
       }
     } else if (kCsa && warp >= 14) {
       // ---------------------------------------------------------- CSA gather
@@ -365,21 +393,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         injected_stall(&bars.never, abort_flag, p.status, p.wait_ns);
         ok = false;
       }
-      for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
-        Tile t;
-        pair_coords(p, u, t);
-        pair_ranges_warp<kCsa>(p, cp, t, lane);
+      while (ok) {
+        // The pairs with keys, in the TMA warp's order: each one's geometry
+        // sits beside its q buffer, so none of it is computed here between
+        // two pairs (the range arithmetic took ~2000 cycles of this warp's
+        // critical path at every pair boundary).
+        ok = wait_warp(&bars.q_full[gq & 1], (gq >> 1) & 1, abort_flag, p.status, p.wait_ns);
+        if (!ok) break;
+        Tile t = bars.tile[gq & 1];
         uniform_tile(t);
+        if (t.nb < 0) break;
         const int nb = t.nb;
-        if (nb == 0) continue;
         const int nh = half_blocks(t);
+        const uint64_t qoff = desc_bytes((gq & 1) * kQBuf);  // this pair's q buffer
         auto issue_s = [&](int x, int k) {
           int n, nc;
           block_cols(t, k >> 1, n, nc);
           const int h = k & 1;
           const int w = h ? n - kHalfKeys : min(n, kHalfKeys);
           const uint32_t idesc = idesc_bf16_f32(kRows, (w + 15) & ~15, false, false);
-          const uint64_t da = x ? dq1 : dq0;
+          const uint64_t da = (x ? dq1 : dq0) + qoff;
           const uint64_t db = dk0 + desc_bytes(((gb + (k >> 1)) % kStages) * kTile + h * kHalfKeys * 128);
           const uint32_t buf = (hb + k) & 1;
           const uint32_t d = tmem + col_s(x) + buf * kHalfKeys;
@@ -387,7 +420,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) mma_ss(d, da + kmaj_step(kk), db + kmaj_step(kk), idesc, kk > 0);
             mma_commit(&bars.s_full[x][buf]);
-            if (x == x1 - 1 && k == nh - 1) mma_commit(&bars.q_empty);
           }
           __syncwarp();
           issued = true;
@@ -418,8 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         };
-        ok = wait_warp(&bars.q_full, gq & 1, abort_flag, p.status, p.wait_ns);
-        if (ok) ok = wait_warp(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status, p.wait_ns);
+        ok = wait_warp(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status, p.wait_ns);
         if (ok) {
           tc_fence_after();
           for (int x = x0; x < x1; ++x) issue_s(x, 0);
@@ -464,7 +495,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     uint32_t gq = 0, epi_phase = 0;
     bool ok = true;
-    uint32_t pending = 0;  // bit x: a store from staging tile x may still be reading it
     auto rendezvous = [&]() -> bool {
       mbar_arrive(&bars.epi);
       const bool rr = wait_warp(&bars.epi, epi_phase & 1, abort_flag, p.status, p.wait_ns);
@@ -479,18 +509,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nb == 0) continue;
       for (int x = 0; ok && x < 2; ++x) {
         const int i0 = t.i0 + x * Q.Pq;
-        uint8_t *obuf = smem + kOffOut + x * kTile;
+        // tile X's output is staged where its q was: O_X is final only after
+        // every MMA of tile X, the S MMAs that read Q_X included, has completed
+        uint8_t *obuf = smem + kOffQ + (gq & 1) * kQBuf + x * kTile;
         if (!wait_warp(&bars.o_final[x], gq & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         if (!wait_warp(&bars.st_full[x], gq & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         const float inv = bars.inv_l[x][r];
         mbar_arrive(&bars.st_free[x]);
         tc_fence_after();
-        if (pending & (1u << x)) {
-          // the store issued from this staging tile one pair ago must have read it
-          if (r == 0) bulk_wait_read1();
-          if (!rendezvous()) { ok = false; break; }
-          pending &= ~(1u << x);
-        }
         uint32_t o[32];
 #pragma unroll
         for (int c0 = 0; c0 < kD; c0 += 32) {
@@ -520,7 +546,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (r == 0) bulk_commit();  // one group per staging tile (possibly empty)
-        pending |= 1u << x;
+      }
+      if (!ok) break;
+      // the q buffer is free for pair gq + 2 once both stores have read it
+      if (r == 0) {
+        bulk_wait_read0();
+        mbar_arrive(&bars.q_empty[gq & 1]);
       }
       ++gq;
     }
