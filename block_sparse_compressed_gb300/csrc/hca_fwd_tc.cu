@@ -237,7 +237,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         pair_coords(p, u, t);
         pair_ranges_warp<kCsa>(p, cp, t, lane);
         const int nb = t.nb;
-        if (nb == 0) continue;
+        if (nb == 0) {
+          // no position of the pair has keys (all padding): zero output, lse -inf
+          for (int e = lane; e < 2 * Q.Pq * Q.HG; e += 32) {
+            const int i = t.i0 + e % (2 * Q.Pq);
+            if (i >= Q.S) continue;
+            const size_t lrow = ((size_t)t.b * Q.H + t.g * Q.HG + e / (2 * Q.Pq)) * Q.S + i;
+            uint4 *orow = reinterpret_cast<uint4 *>(p.out + lrow * kD);
+            for (int c = 0; c < kD / 8; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+            p.lse[lrow] = -INFINITY;
+          }
+          continue;
+        }
         if (lane == 0) {
           // q buffer gq mod 2: free once pair gq - 2's output has left it, so
           // a pair's q is requested while the pair before it still runs
@@ -563,29 +574,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = tid - x * kWG;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     uint32_t hb = 0, gq = 0, scnt = 0;  // half-blocks and pairs before this one; blocks (CSA bits)
-    bool ok = true;
-    for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
-      Tile t;
-      pair_coords(p, u, t);
-      pair_ranges_warp<kCsa>(p, cp, t, lane);
-      const int nb = t.nb;
-      const int pq = r % Q.Pq, hh = r / Q.Pq;
-      const int ppos = x * Q.Pq + pq;  // this row's position in the pair (CSA bits)
-      const int head = t.g * Q.HG + hh;
-      const int i = t.i0 + x * Q.Pq + pq;
-      const RowIv iv = row_interval(Q.sstart, t.b, Q.S, i, Q.W, Q.m);
-      const size_t lrow = ((size_t)t.b * Q.H + head) * Q.S + i;
-      if (poisoned || nb == 0) {
+    const int pq = r % Q.Pq, hh = r / Q.Pq;
+    const int ppos = x * Q.Pq + pq;  // this row's position in the pair (CSA bits)
+    if (poisoned) {
+      // the ordering check failed: every row is NaN
+      for (long long u = blockIdx.x; u < p.npairs; u += gridDim.x) {
+        Tile t;
+        pair_coords(p, u, t);
+        const int i = t.i0 + x * Q.Pq + pq;
         if (i < Q.S) {
-          const float v = poisoned ? __int_as_float(0x7fc00000) : 0.f;
+          const size_t lrow = ((size_t)t.b * Q.H + t.g * Q.HG + hh) * Q.S + i;
+          const float v = __int_as_float(0x7fc00000);
           const uint32_t w2 = pack_bf16x2(v, v);
           uint4 *orow = reinterpret_cast<uint4 *>(p.out + lrow * kD);
 #pragma unroll
           for (int c = 0; c < kD / 8; ++c) orow[c] = make_uint4(w2, w2, w2, w2);
-          p.lse[lrow] = poisoned ? v : -INFINITY;
+          p.lse[lrow] = v;
         }
-        continue;
       }
+    }
+    bool ok = !poisoned;
+    while (ok) {
+      // the pairs with keys, in the TMA warp's order, with their geometry
+      // (a pair's ranges took this warpgroup ~2000 cycles to work out)
+      if (!wait_warp(&bars.q_full[gq & 1], (gq >> 1) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
+      const Tile t = bars.tile[gq & 1];
+      const int nb = t.nb;
+      if (nb < 0) break;
+      const int head = t.g * Q.HG + hh;
+      const int i = t.i0 + x * Q.Pq + pq;
+      const RowIv iv = row_interval(Q.sstart, t.b, Q.S, i, Q.W, Q.m);
+      const size_t lrow = ((size_t)t.b * Q.H + head) * Q.S + i;
       const int nh = half_blocks(t);
       float m_run = -INFINITY, l_run = 0.f;
       int a1 = 0, b1 = -1, a2 = 0, b2 = -1;  // the row's visible columns of the block: [a1, b1] compressed, [a2, b2] raw
