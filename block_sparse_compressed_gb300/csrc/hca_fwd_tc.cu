@@ -400,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int x0 = kCsa ? 0 : warp - 13, x1 = kCsa ? 2 : x0 + 1;  // tiles this warp issues for
       uint32_t gb = 0, gq = 0, hb = 0;  // blocks, pairs and half-blocks before this pair
       bool ok = !poisoned, issued = false;
+      bool ahead = false;  // this pair's S(0) and S(1) went out during the previous pair
       if (ok && p.stall) {
         injected_stall(&bars.never, abort_flag, p.status, p.wait_ns);
         ok = false;
@@ -416,16 +417,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t.nb < 0) break;
         const int nb = t.nb;
         const int nh = half_blocks(t);
-        const uint64_t qoff = desc_bytes((gq & 1) * kQBuf);  // this pair's q buffer
-        auto issue_s = [&](int x, int k) {
-          int n, nc;
-          block_cols(t, k >> 1, n, nc);
+        // S_X of half-block k of a pair whose key list has ncols columns, whose
+        // q sits in buffer qbuf and whose blocks / half-blocks start at gbb / hbb
+        auto issue_s_at = [&](int ncols, uint32_t qbuf, uint32_t gbb, uint32_t hbb, int x, int k) {
+          const int n = min(kBlockKeys, ncols - (k >> 1) * kBlockKeys);
           const int h = k & 1;
           const int w = h ? n - kHalfKeys : min(n, kHalfKeys);
           const uint32_t idesc = idesc_bf16_f32(kRows, (w + 15) & ~15, false, false);
-          const uint64_t da = (x ? dq1 : dq0) + qoff;
-          const uint64_t db = dk0 + desc_bytes(((gb + (k >> 1)) % kStages) * kTile + h * kHalfKeys * 128);
-          const uint32_t buf = (hb + k) & 1;
+          const uint64_t da = (x ? dq1 : dq0) + desc_bytes(qbuf * kQBuf);
+          const uint64_t db = dk0 + desc_bytes(((gbb + (k >> 1)) % kStages) * kTile + h * kHalfKeys * 128);
+          const uint32_t buf = (hbb + k) & 1;
           const uint32_t d = tmem + col_s(x) + buf * kHalfKeys;
           if (elect_one()) {
 #pragma unroll
@@ -435,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           issued = true;
         };
+        auto issue_s = [&](int x, int k) { issue_s_at(t.ncols, gq & 1, gb, hb, x, k); };
         auto issue_pv = [&](int x, int k) {
           int n, nc;
           block_cols(t, k >> 1, n, nc);
@@ -461,15 +463,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         };
-        ok = wait_warp(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status, p.wait_ns);
-        if (ok) {
-          tc_fence_after();
-          for (int x = x0; x < x1; ++x) issue_s(x, 0);
-          if (nh > 1)
-            for (int x = x0; x < x1; ++x) issue_s(x, 1);
+        if (!ahead) {
+          ok = wait_warp(&bars.kv_full[gb % kStages], (gb / kStages) & 1, abort_flag, p.status, p.wait_ns);
+          if (ok) {
+            tc_fence_after();
+            for (int x = x0; x < x1; ++x) issue_s(x, 0);
+            if (nh > 1)
+              for (int x = x0; x < x1; ++x) issue_s(x, 1);
+          }
         }
+        // The next pair's first two S go out during this pair's last two
+        // half-blocks (their buffers are free once PV(nh-2) and PV(nh-1) are
+        // issued), so its softmax can start as soon as this pair ends -- if
+        // its q and first key block have already landed (checked without
+        // waiting; otherwise it starts the usual way).
+        int nx_cols = 0;
         for (int k = 0; ok && k < nh; ++k) {
           const int k2 = k + 2;
+          if (k2 == nh) {
+            const uint32_t gn = gq + 1, bn = gb + nb;
+            bool rdy = mbar_test(&bars.q_full[gn & 1], (gn >> 1) & 1);
+            const int c = rdy ? bars.tile[gn & 1].ncols : 0;
+            rdy = rdy && bars.tile[gn & 1].nb > 0 && mbar_test(&bars.kv_full[bn % kStages], (bn / kStages) & 1);
+            nx_cols = __all_sync(0xffffffffu, rdy) ? __shfl_sync(0xffffffffu, c, 0) : 0;
+          }
           for (int x = x0; ok && x < x1; ++x) {
             ok = wait_warp(&bars.p_full[x][(hb + k) & 1], ((hb + k) >> 1) & 1, abort_flag, p.status, p.wait_ns);
             if (ok && k == 0 && gq > 0) ok = wait_warp(&bars.o_free[x], (gq - 1) & 1, abort_flag, p.status, p.wait_ns);
@@ -484,9 +501,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
               }
               issue_s(x, k2);
+            } else if (nx_cols > 0 && k2 - nh < 2 && (k2 - nh) * kHalfKeys < nx_cols) {
+              tc_fence_after();
+              issue_s_at(nx_cols, (gq + 1) & 1, gb + nb, hb + nh, x, k2 - nh);
             }
           }
         }
+        ahead = nx_cols > 0;
         gb += nb;
         hb += nh;
         ++gq;
