@@ -62,7 +62,7 @@ constexpr int kOffQ = 0, kOffDO = kTile, kOffO = 2 * kTile, kOffKV = 3 * kTile;
 constexpr int kOffOut = kOffKV + kStages * kTile;
 constexpr int kSmemBytes = kOffOut + kTile + 1024;
 constexpr int kDescSlots = 8;
-constexpr int kDescReaders = 11;  // dS warps 0-7, MMA warp 9, Delta warps 10-11 (CSA: warp 10 gathers, warp 11 gathers and forms Delta)
+constexpr int kDescReaders = 11;  // dS warps 0-7, MMA warp 9, Delta warps 10-11 (CSA: warp 11 alone forms Delta)
 constexpr int kDeltaThreads = 64;
 constexpr int kCsaMaxPos = 4;     // CSA: positions per tile whose bits are kept (Pq <= 4)
 }  // namespace dqk
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
     mbar_init(&bars.qd_empty, 1 + (kCsa ? 32 : kDeltaThreads));
     for (int s = 0; s < kStages; ++s) {
       // CSA: the gather warp also arrives once its rows have landed
-      mbar_init(&bars.kv_full[s], kCsa ? 96 : 1);  // CSA: every lane of the TMA warp and the two gather warps
+      mbar_init(&bars.kv_full[s], kCsa ? 32 : 1);  // CSA: every lane of the TMA warp
       mbar_init(&bars.kv_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
     mbar_init(&bars.stat_empty, kEW);
     for (int s = 0; s < kDescSlots; ++s) {
       mbar_init(&bars.desc_full[s], 32);
-      mbar_init(&bars.desc_empty[s], kDescReaders);
+      mbar_init(&bars.desc_empty[s], kCsa ? kDescReaders - 1 : kDescReaders);
     }
     mbar_init(&bars.epi, kEW);
     mbar_init(&bars.drain, 1);
@@ -272,29 +272,53 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         gb = __shfl_sync(0xffffffffu, gb, 0);
         if constexpr (kCsa) {
-          // CSA: lane 0 loads the raw rows by TMA and the whole warp copies a
-          // third of the gathered rows (the gather is issue-bound per warp);
-          // every lane joins the block's kv_full arrival once its copies land
+          // CSA: lane 0 loads the raw rows by TMA; the compressed columns are
+          // the tile's union of selected entries, gathered four rows per TMA
+          // load (the row view of ckv in map_ckv); every lane joins the
+          // block's kv_full arrival once its loads are issued and the
+          // positions' visibility bits are written
           const long long grp = (long long)t.b * Q.ntq + t.i0 / Q.Pq;
           const int32_t *ent = p.u_ent + grp * p.u_cap;
           const uint32_t *msk = p.u_mask + grp * p.u_cap;
-          const __nv_bfloat16 *ckv_b = p.ckv + (size_t)t.b * Q.Sc * kD;
+          const int rb = t.b * Q.Sc;  // row of ckv[b][0] in the row view
           for (int j = 0; ok && j < nb; ++j, ++gb) {
             const int s = gb % kStages;
+            int n, nc;
+            block_cols(t, j, n, nc);
+            // entry ids and selection masks, loaded before the wait for a stage
+            const int4 e4 = 4 * lane < nc ? *reinterpret_cast<const int4 *>(ent + j * kBlockKeys + 4 * lane)
+                                          : make_int4(0, 0, 0, 0);
+            uint32_t mk[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const int c = 32 * w + lane;
+              mk[w] = (c < nc && j * kBlockKeys + c < t.chi) ? msk[j * kBlockKeys + c] : 0u;
+            }
             if (gb >= (uint32_t)kStages)
               ok = wait_warp(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
             if (!ok) break;
-            int n, nc;
-            block_cols(t, j, n, nc);
+            uint8_t *dst = smem + kOffKV + s * kTile;
             if (lane == 0) {
-              mbar_expect_tx(&bars.kv_full[s], nc == n ? 0u : raw_load_bytes(n, nc));
-              if (nc < n) load_block_raw(t, j, n, nc, &map_kv, &map_kv16, &bars.kv_full[s], smem + kOffKV + s * kTile);
+              mbar_expect_tx(&bars.kv_full[s], (nc == n ? 0u : raw_load_bytes(n, nc)) + (uint32_t)nc * 128u * kHalves);
+              if (nc < n) load_block_raw(t, j, n, nc, &map_kv, &map_kv16, &bars.kv_full[s], dst);
               last_par[s] = (gb / kStages) & 1;
             }
-            gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, 2, 3, Q.Pq, 0, 0,
-                         &bars.vis[s][0][0], lane);
-            cp_async_wait_all();
-            fence_async_smem();
+            __syncwarp();  // the expected bytes are set before any gathered row lands
+            // nc is a multiple of 16: lane l gathers rows 4l .. 4l + 3 (padding
+            // entries are row 0, which no position sees)
+            if (4 * lane < nc) {
+#pragma unroll
+              for (int hh = 0; hh < kHalves; ++hh)
+                tma_gather4(&map_ckv, &bars.kv_full[s], dst + hh * kHalfTile + 4 * lane * 128, 64 * hh, rb + e4.x,
+                            rb + e4.y, rb + e4.z, rb + e4.w);
+            }
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              for (int pp = 0; pp < Q.Pq; ++pp) {
+                const uint32_t bits = __ballot_sync(0xffffffffu, (mk[w] >> pp) & 1u);
+                if (lane == 0) bars.vis[s][pp][w] = bits;
+              }
+            }
             mbar_arrive(&bars.kv_full[s]);
           }
         }
@@ -408,37 +432,8 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         __syncwarp();
       }
     } else if (kCsa && warp == kEW / 32 + 2) {
-      // ------------------------------------------------------------ CSA gather
-      // The compressed columns of every block are the tile's union of
-      // selected entries: their ckv rows go into the key tile in the swizzled
-      // layout the TMA gives the raw rows, each position's bits for them to
-      // shared memory, then the warp joins the block's kv_full arrival.
-      uint32_t gb = 0, kd = 0;
-      bool ok = true;
-      while (ok) {
-        Tile t;
-        long long u;
-        ok = read_dq_desc(bars, kd++, t, u, abort_flag, p.status, p.wait_ns);
-        if (!ok || u < 0) break;
-        if (poisoned || t.nb == 0) continue;
-        const long long grp = (long long)t.b * Q.ntq + t.i0 / Q.Pq;
-        const int32_t *ent = p.u_ent + grp * p.u_cap;
-        const uint32_t *msk = p.u_mask + grp * p.u_cap;
-        const __nv_bfloat16 *ckv_b = p.ckv + (size_t)t.b * Q.Sc * kD;
-        for (int j = 0; ok && j < t.nb; ++j, ++gb) {
-          const int s = gb % kStages;
-          if (gb >= (uint32_t)kStages)
-            ok = wait_warp(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
-          if (!ok) break;
-          int n, nc;
-          block_cols(t, j, n, nc);
-          gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, 0, 3, Q.Pq, 0, 2,
-                       &bars.vis[s][0][0], lane);
-          cp_async_wait_all();
-          fence_async_smem();
-          mbar_arrive(&bars.kv_full[s]);
-        }
-      }
+      // CSA: idle (the TMA warp gathers the selected rows); it is not counted
+      // among the tile descriptors' readers
     } else {
       // ------------------------------------------------------------ Delta
       // Delta = <dO, out> of every tile row from the staged dO and out tiles
@@ -447,28 +442,8 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
       // memory and, as -scale*Delta, in the row records the dkv kernel reads.
       constexpr int kRowsPerLane = kCsa ? 4 : 2;
       const int dt = kCsa ? lane : tid - (kEW + 64);
-      uint32_t tw = 0, kd = 0, gb = 0;
+      uint32_t tw = 0, kd = 0;
       bool ok = true;
-      // CSA: this warp also copies a third of the gathered rows (part 1 of 3):
-      // a tile's block 0 before its Delta (it does not wait for the tile's
-      // q / dO / out), the other blocks after
-      auto gather_share = [&](const Tile &t, int j) -> bool {
-        const int s = gb % kStages;
-        if (gb >= (uint32_t)kStages &&
-            !wait_warp(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns))
-          return false;
-        const long long grp = (long long)t.b * Q.ntq + t.i0 / Q.Pq;
-        int n, nc;
-        block_cols(t, j, n, nc);
-        gather_block(p.u_ent + grp * p.u_cap, p.u_mask + grp * p.u_cap, t.chi, j * kBlockKeys, nc,
-                     p.ckv + (size_t)t.b * Q.Sc * kD, smem + kOffKV + s * kTile, 1, 3, Q.Pq, 2, 4, &bars.vis[s][0][0],
-                     lane);
-        cp_async_wait_all();
-        fence_async_smem();
-        mbar_arrive(&bars.kv_full[s]);
-        ++gb;
-        return true;
-      };
       const uint8_t *dobuf = smem + kOffDO;
       const uint8_t *outbuf = smem + kOffO;
       while (ok) {
@@ -477,7 +452,6 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         ok = read_dq_desc(bars, kd++, t, u, abort_flag, p.status, p.wait_ns);
         if (!ok || u < 0) break;
         if (poisoned || t.nb == 0) continue;
-        if (kCsa && !gather_share(t, 0)) { ok = false; break; }
         if (!wait_warp(&bars.qd_full, tw & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         float dl[kRowsPerLane];
 #pragma unroll
@@ -506,8 +480,6 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         for (int h = 0; h < kRowsPerLane; ++h) bars.delta[dt + (kRows / kRowsPerLane) * h] = dl[h];
         mbar_arrive(&bars.stat_full);
         ++tw;
-        if (kCsa)
-          for (int j = 1; ok && j < t.nb; ++j) ok = gather_share(t, j);
       }
     }
   } else {
@@ -1403,7 +1375,7 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st, const CsaBwd *csa) {
   // a position range when one head fills the tile
   const int sub_hg = q.HG >= 2 ? q.HG / 2 : 1;
   const int sub_pq = q.HG >= 2 ? q.Pq : q.Pq / 2;
-  CUtensorMap mq, mdo, mout, mkv, mckv, mkv16, mckv16, mdq, mqs, mdos;
+  CUtensorMap mq, mdo, mout, mkv, mckv, mkv16, mckv16, mdq, mqs, mdos, mckvg;
   const uint64_t D = (uint64_t)a.D;
   if (!make_map_bf16(&mq, a.q, D, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mout, a.out, D, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
@@ -1417,6 +1389,8 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st, const CsaBwd *csa) {
       !make_map_bf16(&mckv16, a.ckv, D, q.Sc, a.B, 16, 1))
     return cudaErrorInvalidValue;
   if (csa && a.D != 128) return cudaErrorInvalidValue;
+  // CSA: the dq kernel gathers its compressed rows through the row view of ckv
+  if (csa && !make_map_rows_bf16(&mckvg, a.ckv, D, (uint64_t)q.Sc * a.B)) return cudaErrorInvalidValue;
   const bool d64 = a.D == 64;
   auto dq_kern = csa ? hca_bwd_dq_kernel<true, 128> : (d64 ? hca_bwd_dq_kernel<false, 64> : hca_bwd_dq_kernel<false, 128>);
   auto dkv_kern = d64 ? hca_bwd_dkv_kernel<64> : hca_bwd_dkv_kernel<128>;
@@ -1453,7 +1427,7 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st, const CsaBwd *csa) {
   cudaError_t e;
   {
     ProfScope prof(kKBwdDq, st);
-    dq_kern<<<(unsigned)g1, dqk::kThreads, dqk::kSmemBytes, st>>>(mq, mdo, mout, mkv, mckv, mkv16, mckv16, mdq, dp);
+    dq_kern<<<(unsigned)g1, dqk::kThreads, dqk::kSmemBytes, st>>>(mq, mdo, mout, mkv, csa ? mckvg : mckv, mkv16, mckv16, mdq, dp);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;

@@ -144,12 +144,11 @@ constexpr int kOffQ = 0, kOffDO = kTile, kOffKV = 2 * kTile;
 constexpr int kOffP = kOffKV + kStages * kTile, kOffDS = kOffP + kTile;
 constexpr int kSmemBytes = kOffDS + kTile + 1024;
 constexpr int kMaxPos = 4;                // positions per tile (H a multiple of 32)
-constexpr int kGather = 64;               // gather threads (two warps, alternate rows)
+constexpr int kGather = 32;               // the gather warp's lanes (each issues TMA gather4 loads)
 }  // namespace ckk
 
 struct DckvParams {
   QTiling qt;
-  const __nv_bfloat16 *ckv;
   const float *rowstat;       // [ntiles][2][128] from the dq kernel
   const int32_t *u_cnt, *u_ent;
   const uint32_t *u_mask;
@@ -175,7 +174,7 @@ struct DckvBars {
 
 __global__ void __launch_bounds__(ckk::kThreads, 1)
     hca_csa_dckv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
-                        const DckvParams p) {
+                        const __grid_constant__ CUtensorMap map_ckv, const DckvParams p) {
   using namespace ckk;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -252,15 +251,15 @@ __global__ void __launch_bounds__(ckk::kThreads, 1)
         volatile int never = 0;
         mbar_wait(&bars.q_full, q_par, &never, p.status, 100000000ull);
       }
-    } else if (warp >= kEW / 32 + 2) {
+    } else if (warp == kEW / 32 + 2) {
       // ------------------------------------------------------------ gather: the union's ckv rows
-      // Each block's entries are copied 16 bytes at a time into the 128B-
-      // swizzled tile layout the MMA descriptors read; the per-position
-      // visibility bits of the block go to shared memory beside them.  Two
-      // warps: `part` copies rows part, part + 2, ... and bit words 2 part,
-      // 2 part + 1 (one warp's copies are issue-bound).
-      const int part = warp - (kEW / 32 + 2);
+      // Each block's entries land in the 128B-swizzled tile layout the MMA
+      // descriptors read, four rows per TMA gather4 load through the row view
+      // of ckv (lane l takes rows 4l .. 4l + 3; 16-byte copies made one warp's
+      // issue the limit); the per-position visibility bits of the block go to
+      // shared memory beside them.  Warp kEW/32 + 3 is idle.
       uint32_t gb = 0;
+      uint32_t issued = 0;  // bit s: stage s loaded at least once; bit 8+s: parity of its last load
       bool ok = !poisoned;
       for (long long u = blockIdx.x; ok && u < Q.ntiles; u += gridDim.x) {
         Tile t;
@@ -269,49 +268,49 @@ __global__ void __launch_bounds__(ckk::kThreads, 1)
         const long long grp = (long long)t.b * Q.ntq + t.i0 / Q.Pq;
         const int32_t *ent = p.u_ent + grp * p.u_cap;
         const uint32_t *msk = p.u_mask + grp * p.u_cap;
+        const int rb = t.b * Q.Sc;  // row of ckv[b][0] in the row view
         for (int j = 0; ok && j < nb; ++j, ++gb) {
           const int s = gb % kStages;
+          const int c0 = j * kBlockKeys;
+          const int n = min(kBlockKeys, ((cnt + 15) & ~15) - c0);  // a multiple of 16
+          // entry ids and selection masks, loaded before the wait for a stage
+          const int4 e4 = 4 * lane < n ? *reinterpret_cast<const int4 *>(ent + c0 + 4 * lane) : make_int4(0, 0, 0, 0);
+          uint32_t mk[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int c = c0 + 32 * w + lane;
+            mk[w] = (32 * w + lane < n && c < cnt) ? msk[c] : 0u;
+          }
           if (gb >= (uint32_t)kStages)
             ok = wait_warp(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
           if (!ok) break;
-          const int c0 = j * kBlockKeys;
-          const int n = min(kBlockKeys, ((cnt + 15) & ~15) - c0);
           uint8_t *dst = smem + kOffKV + s * kTile;
-          // entry ids first (lane holds rows lane + 32 jj), so that each
-          // copy's address is a shuffle away instead of a load's latency
-          int32_t eid[kBlockKeys / 32];
+          if (lane == 0) mbar_expect_tx(&bars.kv_full[s], (uint32_t)n * 256u);
+          __syncwarp();  // the expected bytes are set before any row lands
+          if (4 * lane < n) {
 #pragma unroll
-          for (int jj = 0; jj < kBlockKeys / 32; ++jj) {
-            const int r = lane + 32 * jj;
-            eid[jj] = r < n ? ent[c0 + r] : 0;
-          }
-          // the same number of passes for every lane (whole-warp shuffles)
-          for (int q = lane; q < ((((n + 1) / 2) * 16 + 31) & ~31); q += 32) {
-            const int r = part + 2 * (q >> 4), ch = q & 15;
-            int32_t e = 0;
-#pragma unroll
-            for (int jj = 0; jj < kBlockKeys / 32; ++jj) {
-              const int32_t ej = __shfl_sync(0xffffffffu, eid[jj], r & 31);
-              if ((r >> 5) == jj) e = ej;
-            }
-            if (r < n) {
-              const __nv_bfloat16 *src = p.ckv + ((size_t)t.b * Q.Sc + e) * kHeadDim + ch * 8;
-              cp_async16(smem_u32(dst + sw128_offset(r, ch)), src);
-            }
+            for (int hh = 0; hh < 2; ++hh)
+              tma_gather4(&map_ckv, &bars.kv_full[s], dst + hh * kHalfTile + 4 * lane * 128, 64 * hh, rb + e4.x,
+                          rb + e4.y, rb + e4.z, rb + e4.w);
           }
           // visibility bits: word w of position pp = columns [32 w, 32 w + 32)
-          for (int w = 2 * part; w < 2 * part + 2; ++w) {
-            const int c = c0 + 32 * w + lane;
-            const uint32_t mk = (32 * w + lane < n && c < cnt) ? msk[c] : 0u;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
             for (int pp = 0; pp < Q.Pq; ++pp) {
-              const uint32_t bits = __ballot_sync(0xffffffffu, (mk >> pp) & 1u);
+              const uint32_t bits = __ballot_sync(0xffffffffu, (mk[w] >> pp) & 1u);
               if (lane == 0) bars.vis[s][pp][w] = bits;
             }
           }
-          cp_async_wait_all();
-          fence_async_smem();
           mbar_arrive(&bars.kv_full[s]);
+          issued = (issued | (1u << s)) & ~(1u << (8 + s));
+          issued |= ((gb / kStages) & 1u) << (8 + s);
         }
+      }
+      if (!ok && !poisoned && lane == 0) {
+        // the loads already issued land before the CTA can exit
+        volatile int never = 0;
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s)) mbar_wait(&bars.kv_full[s], (issued >> (8 + s)) & 1u, &never, p.status, 100000000ull);
       }
     } else if (warp == kEW / 32 + 1) {
       // ------------------------------------------------------------ MMA
@@ -553,9 +552,10 @@ size_t csa_dckv_acc_bytes(int B, int Sc) { return align_up((size_t)B * Sc * kHea
 
 cudaError_t csa_dckv(const BwdArgs &a, const CsaUnion &u, const float *rowstat, float *acc, cudaStream_t st) {
   const QTiling q = make_qtiling(a.sstart, a.B, a.H, a.S, a.W, a.m);
-  CUtensorMap mq, mdo;
+  CUtensorMap mq, mdo, mckv;
   if (!make_map_bf16(&mq, a.q, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
-      !make_map_bf16(&mdo, a.dout, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG))
+      !make_map_bf16(&mdo, a.dout, kHeadDim, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
+      !make_map_rows_bf16(&mckv, a.ckv, kHeadDim, (uint64_t)q.Sc * a.B))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaMemsetAsync(acc, 0, (size_t)a.B * q.Sc * kHeadDim * sizeof(float), st);
   if (e != cudaSuccess) return e;
@@ -564,7 +564,6 @@ cudaError_t csa_dckv(const BwdArgs &a, const CsaUnion &u, const float *rowstat, 
   if (e != cudaSuccess) return e;
   DckvParams p;
   p.qt = q;
-  p.ckv = static_cast<const __nv_bfloat16 *>(a.ckv);
   p.rowstat = rowstat;
   p.u_cnt = u.cnt; p.u_ent = u.ent; p.u_mask = u.mask; p.u_cap = u.cap;
   p.acc = acc;
@@ -579,7 +578,7 @@ cudaError_t csa_dckv(const BwdArgs &a, const CsaUnion &u, const float *rowstat, 
   const long long grid = q.ntiles < sms ? q.ntiles : sms;
   if (grid > 0) {
     ProfScope prof(kKCsaDckv, st);
-    hca_csa_dckv_kernel<<<(unsigned)grid, ckk::kThreads, ckk::kSmemBytes, st>>>(mq, mdo, p);
+    hca_csa_dckv_kernel<<<(unsigned)grid, ckk::kThreads, ckk::kSmemBytes, st>>>(mq, mdo, mckv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

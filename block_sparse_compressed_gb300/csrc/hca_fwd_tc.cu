@@ -49,7 +49,8 @@
 //                 q buffer) -> TMA store
 //   warpgroup 3   warp 12 TMA producer, warps 13 and 14 MMA issuers (tile A,
 //                 tile B), warp 15 idle; with CSA warp 13 issues for both
-//                 tiles and warps 14-15 gather the selected rows
+//                 tiles and warps 14-15 are idle (the TMA warp gathers the
+//                 selected rows with TMA gather4 loads)
 // Every wait is bounded (tc_ptx.cuh): on a timeout the CTA records
 // HCA_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -82,7 +83,6 @@ constexpr int kQBuf = 2 * kTile;  // one pair's q tiles, later its output tiles
 constexpr int kOffKV = kOffQ + 2 * kQBuf;
 constexpr int kSmemBytes = kOffKV + kStages * kTile + 1024;
 constexpr int kCsaMaxPos = 8;     // positions of a pair whose bits CSA keeps (Pq <= 4)
-constexpr int kGatherThreads = 64;  // CSA: warps 14 and 15 gather the compressed rows
 
 // CSA: per pair, the union of its positions' selected entries (hca_csa.cu).
 // A kernel argument of its own: growing FwdParams changes how the HCA
@@ -184,9 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.q_empty[b], 1);
     }
     for (int s = 0; s < kStages; ++s) {
-      // CSA: the gather warps also arrive once their rows have landed
-      // CSA: every lane of the TMA warp and of the two gather warps arrives
-      mbar_init(&bars.kv_full[s], kCsa ? 32 + kGatherThreads : 1);
+      // CSA: every lane of the TMA warp arrives once it has issued its
+      // gather loads and the visibility bits are written
+      mbar_init(&bars.kv_full[s], kCsa ? 32 : 1);
       mbar_init(&bars.kv_empty[s], kMmaWarps);
     }
     for (int x = 0; x < 2; ++x) {
@@ -298,30 +298,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         gb = __shfl_sync(0xffffffffu, gb, 0);
         if constexpr (kCsa) {
-          // CSA: lane 0 loads the raw rows by TMA and the whole warp copies a
-          // third of the gathered rows (the gather is issue-bound per warp);
-          // every lane joins the block's kv_full arrival once its copies land
+          // CSA: lane 0 loads the raw rows by TMA; the compressed columns are
+          // the pair's union of selected entries, gathered four rows per TMA
+          // load (one 16-byte copy per lane and instruction took a warp ~8000
+          // cycles per block); every lane joins the block's kv_full arrival
           const long long grp = (long long)t.b * p.ntp + t.i0 / (2 * Q.Pq);
           const int32_t *ent = cp.u_ent + grp * cp.u_cap;
           const uint32_t *msk = cp.u_mask + grp * cp.u_cap;
-          const __nv_bfloat16 *ckv_b = cp.ckv + (size_t)t.b * Q.Sc * kHeadDim;
+          const int rb = t.b * Q.Sc;  // row of ckv[b][0] in the row view of map_ckv
           for (int j = 0; ok && j < nb; ++j, ++gb) {
             const int s = gb % kStages;
+            int n, nc;
+            block_cols(t, j, n, nc);
+            // the block's entry ids and selection masks: global loads issued
+            // before the wait for a free stage, which hides their latency
+            const int4 e4 = 4 * lane < nc ? *reinterpret_cast<const int4 *>(ent + j * kBlockKeys + 4 * lane)
+                                          : make_int4(0, 0, 0, 0);
+            uint32_t mk[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const int c = 32 * w + lane;
+              mk[w] = (c < nc && j * kBlockKeys + c < t.chi) ? msk[j * kBlockKeys + c] : 0u;
+            }
             if (gb >= (uint32_t)kStages)
               ok = wait_warp(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
             if (!ok) break;
-            int n, nc;
-            block_cols(t, j, n, nc);
+            uint8_t *dst = smem + kOffKV + s * kTile;
             if (lane == 0) {
-              mbar_expect_tx(&bars.kv_full[s], nc == n ? 0u : raw_load_bytes(n, nc));
-              if (nc < n) load_block_raw(t, j, n, nc, &map_kv, &map_kv16, &bars.kv_full[s], smem + kOffKV + s * kTile);
+              mbar_expect_tx(&bars.kv_full[s], (nc == n ? 0u : raw_load_bytes(n, nc)) + (uint32_t)nc * 128u * kHalves);
+              if (nc < n) load_block_raw(t, j, n, nc, &map_kv, &map_kv16, &bars.kv_full[s], dst);
               issued = (issued | (1u << s)) & ~(1u << (8 + s));
               issued |= ((gb / kStages) & 1u) << (8 + s);
             }
-            gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, 2, 3, 2 * Q.Pq, 0,
-                         0, &bars.vis[s][0][0], lane);
-            cp_async_wait_all();
-            fence_async_smem();
+            __syncwarp();  // the expected bytes are set before any gathered row lands
+            // compressed columns (nc is a multiple of 16): lane l gathers rows
+            // 4l .. 4l + 3, the union's entries, with one TMA gather4 load per
+            // 64-column half; padding entries are row 0, which no position sees
+            if (4 * lane < nc) {
+#pragma unroll
+              for (int hh = 0; hh < kHalves; ++hh)
+                tma_gather4(&map_ckv, &bars.kv_full[s], dst + hh * kHalfTile + 4 * lane * 128, 64 * hh, rb + e4.x,
+                            rb + e4.y, rb + e4.z, rb + e4.w);
+            }
+            // each pair position's bits for the block's compressed columns
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              for (int pp = 0; pp < 2 * Q.Pq; ++pp) {
+                const uint32_t bits = __ballot_sync(0xffffffffu, (mk[w] >> pp) & 1u);
+                if (lane == 0) bars.vis[s][pp][w] = bits;
+              }
+            }
             mbar_arrive(&bars.kv_full[s]);
           }
         }
@@ -342,39 +368,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (issued & (1u << s)) mbar_wait(&bars.kv_full[s], (issued >> (8 + s)) & 1u, &never, p.status, 100000000ull);
         for (int b = 0; b < 2; ++b)
           if (q_issued & (1u << b)) mbar_wait(&bars.q_full[b], (q_issued >> (8 + b)) & 1u, &never, p.status, 100000000ull);
-      }
-    } else if (kCsa && warp >= 14) {
-      // ---------------------------------------------------------- CSA gather
-      // The compressed columns of every block are the pair's union of
-      // selected entries: their ckv rows are copied into the key tile (the
-      // swizzled layout the TMA gives the raw rows) and each pair position's
-      // bits for them go to shared memory; the warps then join the block's
-      // kv_full arrival.  They follow the TMA warp's schedule.
-      const int part = warp - 14;
-      uint32_t gb = 0;
-      bool ok = !poisoned;
-      for (long long u = blockIdx.x; ok && u < p.npairs; u += gridDim.x) {
-        Tile t;
-        pair_coords(p, u, t);
-        pair_ranges_warp<kCsa>(p, cp, t, lane);
-        const int nb = t.nb;
-        const long long grp = (long long)t.b * p.ntp + t.i0 / (2 * Q.Pq);
-        const int32_t *ent = cp.u_ent + grp * cp.u_cap;
-        const uint32_t *msk = cp.u_mask + grp * cp.u_cap;
-        const __nv_bfloat16 *ckv_b = cp.ckv + (size_t)t.b * Q.Sc * kHeadDim;
-        for (int j = 0; ok && j < nb; ++j, ++gb) {
-          const int s = gb % kStages;
-          if (gb >= (uint32_t)kStages)
-            ok = wait_warp(&bars.kv_empty[s], ((gb / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
-          if (!ok) break;
-          int n, nc;
-          block_cols(t, j, n, nc);
-          gather_block(ent, msk, t.chi, j * kBlockKeys, nc, ckv_b, smem + kOffKV + s * kTile, part, 3,
-                       2 * Q.Pq, 2 * part, 2 * part + 2, &bars.vis[s][0][0], lane);
-          cp_async_wait_all();
-          fence_async_smem();
-          mbar_arrive(&bars.kv_full[s]);
-        }
       }
     } else if (warp == 13 || (!kCsa && warp == 14)) {
       // ---------------------------------------------------------- MMA
@@ -817,7 +810,9 @@ cudaError_t tc_fwd(const FwdArgs &a, cudaStream_t st, const CsaUnion *csa) {
   if (!make_map_bf16(&mq, a.q, D, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mout, a.out, D, a.S, (uint64_t)a.B * a.H, q.Pq, q.HG) ||
       !make_map_bf16(&mkv, a.kv, D, a.S, a.B, kBlockKeys, 1) ||
-      !make_map_bf16(&mckv, a.ckv, D, q.Sc, a.B, kBlockKeys, 1) ||
+      // CSA gathers its compressed rows through the 2-D row view of ckv
+      !(csa ? make_map_rows_bf16(&mckv, a.ckv, D, (uint64_t)q.Sc * a.B)
+            : make_map_bf16(&mckv, a.ckv, D, q.Sc, a.B, kBlockKeys, 1)) ||
       !make_map_bf16(&mkv16, a.kv, D, a.S, a.B, 16, 1) ||
       !make_map_bf16(&mckv16, a.ckv, D, q.Sc, a.B, 16, 1))
     return cudaErrorInvalidValue;

@@ -109,6 +109,18 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap *m, uint64_t *bar,
       : "memory");
 }
 
+// Four rows of a 2-D tensor (rows y0..y3, columns [x, x + box width)) into
+// four consecutive 128-byte rows of shared memory, completing on bar.  The
+// tensor map's box is one row high.
+__device__ __forceinline__ void tma_gather4(const CUtensorMap *m, uint64_t *bar, void *dst, int x, int y0, int y1,
+                                            int y2, int y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
+      "%5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
+
 // L2 prefetch of one tensor box (no shared memory, no completion): warms the
 // rows of a later tile while the current one computes.
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int c0, int c1, int c2) {
