@@ -8,7 +8,8 @@ bullet: unsupported or failing cases are reported as errors, not crashes).
   arrives at, with the bounded-wait limit shortened to 30 ms.  The wait gives
   up, every CTA drains its own copies and MMAs, frees its tensor memory and
   exits; the workspace status reads HCA_ERR_TIMEOUT, the context stays usable
-  and the next ordinary call matches the oracle.
+  and the next ordinary call matches the oracle.  The CSA instantiations of
+  the forward and dq kernels are stalled the same way.
 """
 import math
 
@@ -106,6 +107,41 @@ def test_backward_wait_gives_up_and_context_stays_usable(mask):
     assert hca.hca_workspace_status(ws) == TIMEOUT
     hca.hca_test_inject(hca.INJECT_RESET)
     _check_ordinary_call(cpu, W, m, scale, backward=True)
+
+
+@pytest.mark.parametrize("mask", [STALL_FWD, STALL_DQ])
+def test_csa_wait_gives_up_and_context_stays_usable(mask):
+    # the CSA instantiations give up the same way; their TMA warp has TMA
+    # gather4 loads of the selected rows in flight, which land before the CTA
+    # exits and frees its tensor memory
+    B, H, S, W, m, k, D = 1, 64, 600, 64, 4, 16, 128
+    scale = 1.0 / math.sqrt(D)
+    q, kv, ckv, _, dout = I.small(B, H, S, D, W, m, dtype=torch.bfloat16, seed=11)
+    sel = I.random_selection(B, S, m, k, 61)
+    g = [x.to(DEV) for x in (q, kv, ckv, dout, sel)]
+    hca.hca_test_inject(hca.INJECT_WAIT_LIMIT_NS, 30_000_000)
+    if mask == STALL_FWD:
+        ws = hca.csa_workspace(B, H, S, D, W, m, k, torch.bfloat16, False, DEV)
+        hca.hca_test_inject(hca.INJECT_STALL, mask)
+        hca.hca_csa_attn_fwd(g[0], g[1], g[2], None, g[4], W, m, scale, ws=ws)
+    else:
+        out, lse = hca.hca_csa_attn_fwd(g[0], g[1], g[2], None, g[4], W, m, scale, check=True)
+        ws = hca.csa_workspace(B, H, S, D, W, m, k, torch.bfloat16, True, DEV)
+        hca.hca_test_inject(hca.INJECT_STALL, mask)
+        hca.hca_csa_attn_bwd(g[0], g[1], g[2], None, g[4], out, lse, g[3], W, m, scale, ws=ws)
+    assert hca.hca_workspace_status(ws) == TIMEOUT
+    hca.hca_test_inject(hca.INJECT_RESET)
+    # ordinary calls afterwards match the oracle
+    keep = oracle.topk_mask(sel, -(-S // m))
+    out, lse = hca.hca_csa_attn_fwd(g[0], g[1], g[2], None, g[4], W, m, scale, check=True)
+    ro, rl = oracle.csa_fwd(q, kv, ckv, None, keep, W, m, scale)
+    assert_close("out", out, ro, torch.bfloat16)
+    assert_close("lse", lse, rl, torch.bfloat16)
+    dq, dkv, dckv = hca.hca_csa_attn_bwd(g[0], g[1], g[2], None, g[4], out, lse, g[3], W, m, scale, check=True)
+    rdq, rdkv, rdckv = oracle.csa_bwd(q, kv, ckv, None, keep, dout, W, m, scale)
+    assert_close("dq", dq, rdq, torch.bfloat16)
+    assert_close("dkv", dkv, rdkv, torch.bfloat16)
+    assert_close("dckv", dckv, rdckv, torch.bfloat16)
 
 
 def test_stall_mask_is_consumed_by_one_call():
