@@ -150,8 +150,9 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
     // it has read the staged dO and out tiles
     mbar_init(&bars.qd_empty, 1 + (kCsa ? 32 : kDeltaThreads));
     for (int s = 0; s < kStages; ++s) {
-      // CSA: the gather warp also arrives once its rows have landed
-      mbar_init(&bars.kv_full[s], kCsa ? 32 : 1);  // CSA: every lane of the TMA warp
+      // CSA: every lane of the TMA warp arrives once its gather loads are
+      // issued and the visibility bits written
+      mbar_init(&bars.kv_full[s], kCsa ? 32 : 1);
       mbar_init(&bars.kv_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
@@ -541,7 +542,7 @@ __global__ void __launch_bounds__(dqk::kThreads, 1)
         uint64_t vis = kCsa ? range_mask64(a2, b2, cb) : (range_mask64(a1, b1, cb) | range_mask64(a2, b2, cb));
         if (!wait_warp(&bars.s_full, gb & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         if (kCsa) {
-          // the block's key tile (with the gather warp's bits) has landed;
+          // the block's key tile (with the TMA warp's bits) has landed;
           // this wait orders the bits' reads
           const int s = gb % kStages;
           if (!wait_warp(&bars.kv_full[s], (gb / kStages) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }

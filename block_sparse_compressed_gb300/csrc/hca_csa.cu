@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kUnionThreads) csa_union_kernel(const UnionArg
 namespace ckk {
 constexpr int kStages = 2;
 constexpr int kEW = 256;                  // two warpgroups, 64 key columns each
-constexpr int kThreads = kEW + 128;       // + TMA warp, MMA warp, two gather warps
+constexpr int kThreads = kEW + 128;       // + TMA warp, MMA warp, gather warp, one idle warp
 constexpr int kRegEW = 192, kRegProducer = 120;
 static_assert(2 * 128 * kRegEW + 128 * kRegProducer <= kThreads * 168, "register split must fit the launch");
 constexpr uint32_t kColS = 0, kColDP = 128, kColD = 256;  // D: two 128-column buffers

@@ -167,8 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(kD == 64 || kD == 128, "head dim 64 or 128");
   static_assert(!kCsa || kD == 128, "CSA gathers 128-dim rows");
   constexpr int kHalves = kD / 64;   // 64-column (128-byte) halves of a row
-  // MMA issue: warp 13 for tile A and warp 14 for tile B; with CSA, whose
-  // gather warps are 14-15, warp 13 issues for both tiles
+  // MMA issue: warp 13 for tile A and warp 14 for tile B; with CSA warp 13
+  // issues for both tiles
   constexpr int kMmaWarps = kCsa ? 1 : 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(&bars.s_full[x][buf], ((hb + k) >> 1) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
         if constexpr (kCsa) {
           if (h == 0) {
-            // the block's key tile (with the gather warps' bits) has landed:
+            // the block's key tile (with the TMA warp's bits) has landed:
             // the MMA waited for it before S; this wait orders the bits' reads
             const uint32_t sst = scnt % kStages;
             if (!wait_warp(&bars.kv_full[sst], (scnt / kStages) & 1, abort_flag, p.status, p.wait_ns)) { ok = false; break; }

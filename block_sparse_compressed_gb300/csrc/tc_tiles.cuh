@@ -206,53 +206,6 @@ __device__ __forceinline__ void load_block_raw(const Tile &t, int j, int n, int 
   }
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// One gather warp's share of block j's compressed columns [c0, c0 + nc):
-// rows ent[c0 + r] of ckv[b] copied 16 bytes at a time into the swizzled
-// tile at dst (warp `part` of `nparts` takes rows r = part, part + nparts,
-// ...), and words [wlo, whi) of the per-position visibility bits: word w of
-// position p holds bit (c - 32 w) for the block's columns c in [32 w, 32 w +
-// 32) that position p selected.  The caller waits for the copies
-// (cp_async_wait_all) and fences them for the tensor core before it signals.
-__device__ __forceinline__ void gather_block(const int32_t *ent, const uint32_t *msk, int cnt, int c0, int nc,
-                                             const __nv_bfloat16 *ckv_b, uint8_t *dst, int part, int nparts,
-                                             int npos, int wlo, int whi, uint32_t *vis /* [npos][4] */, int lane) {
-  // the block's entry ids, loaded together (lane holds rows lane + 32 j), so
-  // that each copy's address is a shuffle away instead of a load's latency
-  int32_t eid[kBlockKeys / 32];
-#pragma unroll
-  for (int j = 0; j < kBlockKeys / 32; ++j) {
-    const int r = lane + 32 * j;
-    eid[j] = r < nc ? ent[c0 + r] : 0;
-  }
-  // every lane runs the same number of passes (the shuffles below need the
-  // whole warp): the bound is rounded up to a multiple of 32
-  const int nq = (16 * ((nc + nparts - 1) / nparts) + 31) & ~31;
-  for (int q = lane; q < nq; q += 32) {
-    const int r = part + nparts * (q >> 4), ch = q & 15;
-    int32_t e = 0;
-#pragma unroll
-    for (int j = 0; j < kBlockKeys / 32; ++j) {
-      const int32_t ej = __shfl_sync(0xffffffffu, eid[j], r & 31);
-      if ((r >> 5) == j) e = ej;
-    }
-    if (r < nc) cp_async16(smem_u32(dst + sw128_offset(r, ch)), ckv_b + (size_t)e * kHeadDim + ch * 8);
-  }
-  for (int w = wlo; w < whi; ++w) {
-    const int c = 32 * w + lane;
-    const uint32_t mk = (c < nc && c0 + c < cnt) ? msk[c0 + c] : 0u;
-    for (int pp = 0; pp < npos; ++pp) {
-      const uint32_t bits = __ballot_sync(0xffffffffu, (mk >> pp) & 1u);
-      if (lane == 0) vis[pp * 4 + w] = bits;
-    }
-  }
-}
-
-
 // UMMA descriptor offsets (in the descriptor's 16-byte units) of k-step k
 // (16 bf16 of K) inside a 128-row tile stored as two 128B-swizzled halves:
 // K-major operands advance 32 bytes inside a half, then jump to the next half;
