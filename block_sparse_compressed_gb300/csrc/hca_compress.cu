@@ -70,10 +70,31 @@ __device__ __forceinline__ void load_cols(const T *row, int lane, float (&v)[NC]
   }
 }
 
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// NC consecutive columns of a row per lane: one vector store.
 template <typename T, int NC>
 __device__ __forceinline__ void store_cols(T *row, int lane, const float (&v)[NC]) {
+  if constexpr (sizeof(T) == 4 && NC == 4) {
+    *reinterpret_cast<float4 *>(row + NC * lane) = make_float4(v[0], v[1], v[2], v[3]);
+  } else if constexpr (sizeof(T) == 4 && NC == 8) {
+    float4 *q = reinterpret_cast<float4 *>(row + NC * lane);
+    q[0] = make_float4(v[0], v[1], v[2], v[3]);
+    q[1] = make_float4(v[4], v[5], v[6], v[7]);
+  } else if constexpr (sizeof(T) == 2 && NC == 2) {
+    *reinterpret_cast<uint32_t *>(row + NC * lane) = bf16x2_bits(v[0], v[1]);
+  } else if constexpr (sizeof(T) == 2 && NC == 4) {
+    *reinterpret_cast<uint2 *>(row + NC * lane) = make_uint2(bf16x2_bits(v[0], v[1]), bf16x2_bits(v[2], v[3]));
+  } else if constexpr (sizeof(T) == 2 && NC == 8) {
+    *reinterpret_cast<uint4 *>(row + NC * lane) = make_uint4(bf16x2_bits(v[0], v[1]), bf16x2_bits(v[2], v[3]),
+                                                             bf16x2_bits(v[4], v[5]), bf16x2_bits(v[6], v[7]));
+  } else {
 #pragma unroll
-  for (int c = 0; c < NC; ++c) stf(row + NC * lane + c, v[c]);
+    for (int c = 0; c < NC; ++c) stf(row + NC * lane + c, v[c]);
+  }
 }
 
 __device__ __forceinline__ float warp_max(float v) {
