@@ -1280,27 +1280,40 @@ struct ReduceParams {
   int with_comp;  // 0: dkv only (CSA writes dckv itself)
 };
 
+// Raw rows: one thread per four columns (a few slots each).  Compressed rows
+// have up to kSlotsComp slots: kReduceLanes lanes per four columns, lane l
+// summing slots s_lo + l, s_lo + l + kReduceLanes, ... in order, then a fixed
+// butterfly over the lanes; both orders are fixed, so the sums are the same
+// run to run.  The compressed index range starts at a multiple of 32 (the raw
+// range is padded with idle threads), so no warp mixes the two and every
+// shuffle has the whole warp.
+constexpr int kReduceLanes = 8;
+
 template <int kD>
 __global__ void hca_bwd_reduce_kernel(const ReduceParams p) {
   const long long nraw4 = (long long)p.B * p.S * (kD / 4);
-  const long long ncomp4 = p.with_comp ? (long long)p.B * p.Sc * (kD / 4) : 0;
-  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nraw4 + ncomp4;
+  const long long nraw_pad = (nraw4 + 31) & ~31LL;
+  const long long ncomp = p.with_comp ? (long long)p.B * p.Sc * (kD / 4) * kReduceLanes : 0;
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nraw_pad + ncomp;
        v += (long long)gridDim.x * blockDim.x) {
-    const bool comp = v >= nraw4;
-    const long long x = comp ? v - nraw4 : v;
+    if (v >= nraw4 && v < nraw_pad) continue;  // padding of the raw range
+    const bool comp = v >= nraw_pad;
+    const int part = comp ? (int)((v - nraw_pad) % kReduceLanes) : 0;
+    const long long x = comp ? (v - nraw_pad) / kReduceLanes : v;
     const int d4 = (int)(x % (kD / 4));
     const long long row = x / (kD / 4);
     const int rows = comp ? p.Sc : p.S;
     const int b = (int)(row / rows), key = (int)(row % rows);
     const int kb = key / kBlockKeys;
-    int s_lo, s_hi;
+    int s_lo, s_hi, s_step;
     size_t stride, off;
     const float *base;
     if (comp) {
       // odd blocks only have pair slots; even blocks have lead slots and,
       // when their odd partner exists, pair slots
-      s_lo = (kb & 1) ? dkk::kSplitLead : 0;
+      s_lo = ((kb & 1) ? dkk::kSplitLead : 0) + part;
       s_hi = ((kb & 1) || kb + 1 < p.nkb_comp) ? dkk::kSlotsComp : dkk::kSplitLead;
+      s_step = kReduceLanes;
       stride = (size_t)p.B * p.Sc_pad * kD;
       off = ((size_t)b * p.Sc_pad + key) * kD + d4 * 4;
       base = p.cpart;
@@ -1308,14 +1321,25 @@ __global__ void hca_bwd_reduce_kernel(const ReduceParams p) {
       // slot s holds query range kb + s; ranges past the sequence do not exist
       s_lo = 0;
       s_hi = p.raw_atomic ? 1 : min(p.nslot, p.nrb - kb);
+      s_step = 1;
       stride = (size_t)p.B * p.S_pad * kD;
       off = ((size_t)b * p.S_pad + key) * kD + d4 * 4;
       base = p.rpart;
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = s_lo; s < s_hi; ++s) {
+    for (int s = s_lo; s < s_hi; s += s_step) {
       const float4 y = *reinterpret_cast<const float4 *>(base + s * stride + off);
       acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
+    }
+    if (comp) {
+#pragma unroll
+      for (int o = kReduceLanes / 2; o > 0; o >>= 1) {
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
+      }
+      if (part != 0) continue;
     }
     uint2 o;
     o.x = pack_bf16x2(acc.x, acc.y);
@@ -1483,7 +1507,8 @@ cudaError_t tc_bwd(const BwdArgs &a, cudaStream_t st, const CsaBwd *csa) {
   rp.nkb_comp = kp.nkb_comp;
   rp.raw_atomic = rg.atomic;
   rp.with_comp = csa ? 0 : 1;
-  const long long n4 = (long long)a.B * (a.S + (csa ? 0 : q.Sc)) * (a.D / 4);
+  const long long n4 = (((long long)a.B * a.S * (a.D / 4) + 31) & ~31LL) +
+                       (csa ? 0 : (long long)a.B * q.Sc * (a.D / 4) * kReduceLanes);
   if (n4 > 0) {
     int blocks = (int)((n4 + 255) / 256);
     if (blocks > 8 * sms) blocks = 8 * sms;
