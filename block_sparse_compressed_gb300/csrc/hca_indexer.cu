@@ -84,6 +84,7 @@ struct ScoreParams {
   const int32_t *sstart;  // NULL = one document per row
   float *buf;             // [B][rows][ld] fp32 chunk buffer
   int B, S, m, Sc, row0, rows, ld;
+  int groups;             // CTAs per query tile, each taking a share of its entry blocks
   int32_t *status;
   uint64_t wait_ns;
 };
@@ -109,13 +110,19 @@ __global__ void __launch_bounds__(isk::kThreads, 1)
   __shared__ ScoreBars bars;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   volatile int *abort_flag = &bars.abort;
-  // tile: batch row b, positions [p0, p0 + 128) of the chunk
+  // tile: batch row b, positions [p0, p0 + 128) of the chunk; this CTA takes
+  // the entry blocks [j0, j0 + nblk) of it (group g of p.groups), so that a
+  // chunk of few tiles still fills the GPU
   const int tiles_per_b = (p.rows + kRows - 1) / kRows;
-  const int b = blockIdx.x / tiles_per_b;
-  const int p0 = p.row0 + (blockIdx.x % tiles_per_b) * kRows;
+  const int tile = blockIdx.x / p.groups, grp = blockIdx.x % p.groups;
+  const int b = tile / tiles_per_b;
+  const int p0 = p.row0 + (tile % tiles_per_b) * kRows;
   const int p1 = min(p0 + kRows, min(p.row0 + p.rows, p.S));
   const int nent = min(entries_upto(p1, p.m), p.Sc);
-  const int nblk = (nent + kBlockKeys - 1) / kBlockKeys;
+  const int nblk_tile = (nent + kBlockKeys - 1) / kBlockKeys;
+  const int per = (nblk_tile + p.groups - 1) / p.groups;
+  const int j0 = min(grp * per, nblk_tile);
+  const int nblk = min(j0 + per, nblk_tile) - j0;  // local block j is entry block j0 + j
 
   if (tid == 0) {
     mbar_init(&bars.a_full, 1);
@@ -154,8 +161,8 @@ __global__ void __launch_bounds__(isk::kThreads, 1)
         if (j >= kStages) ok = mbar_wait(&bars.b_empty[s], ((j / kStages) - 1) & 1, abort_flag, p.status, p.wait_ns);
         if (!ok) break;
         mbar_arrive_expect_tx(&bars.b_full[s], kTile);
-        tma_load_3d(&map_k, &bars.b_full[s], smem + kOffB + s * kTile, 0, j * kBlockKeys, b);
-        tma_load_3d(&map_k, &bars.b_full[s], smem + kOffB + s * kTile + kHalfTile, 64, j * kBlockKeys, b);
+        tma_load_3d(&map_k, &bars.b_full[s], smem + kOffB + s * kTile, 0, (j0 + j) * kBlockKeys, b);
+        tma_load_3d(&map_k, &bars.b_full[s], smem + kOffB + s * kTile + kHalfTile, 64, (j0 + j) * kBlockKeys, b);
         b_par[s] = (j / kStages) & 1;
       }
       if (!ok) {
@@ -233,7 +240,7 @@ __global__ void __launch_bounds__(isk::kThreads, 1)
       for (int rr = warp * 32; rr < warp * 32 + 32; ++rr) {
         if (p0 + rr >= p1) break;
         const float4 v = reinterpret_cast<const float4 *>(stage + rr * kStageLd)[lane];
-        float *dst = p.buf + ((size_t)b * p.rows + (p0 + rr - p.row0)) * p.ld + j * kBlockKeys;
+        float *dst = p.buf + ((size_t)b * p.rows + (p0 + rr - p.row0)) * p.ld + (j0 + j) * kBlockKeys;
         reinterpret_cast<float4 *>(dst)[lane] = v;
       }
       if (!rendezvous()) break;
@@ -475,9 +482,12 @@ cudaError_t indexer_topk(const IndexerArgs &a, cudaStream_t st) {
     sp.sstart = a.sstart; sp.buf = a.buf; sp.B = a.B; sp.S = a.S; sp.m = a.m; sp.Sc = Sc;
     sp.row0 = row0; sp.rows = rows; sp.ld = ld; sp.status = a.status; sp.wait_ns = a.wait_ns;
     const int tiles = a.B * ((rows + kRows - 1) / kRows);
+    // enough CTAs for two per SM, each with at least two entry blocks
+    const int max_blk = (Sc + kBlockKeys - 1) / kBlockKeys;
+    sp.groups = max(1, min((2 * sm_count() + tiles - 1) / tiles, max_blk / 2));
     {
       ProfScope prof(kKIndexScore, st);
-      hca_index_score_kernel<<<tiles, isk::kThreads, isk::kSmemBytes, st>>>(mq, mk, sp);
+      hca_index_score_kernel<<<tiles * sp.groups, isk::kThreads, isk::kSmemBytes, st>>>(mq, mk, sp);
       e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
