@@ -81,6 +81,7 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
 std::atomic<long long> g_inject_launch_failures{0};
 std::atomic<int> g_inject_stall_mask{0};
 std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_csa_union{0};
 
 bool take_counter(std::atomic<long long> &c) {
   long long v = c.load();
@@ -95,6 +96,7 @@ namespace hca {
 bool take_launch_failure() { return take_counter(g_inject_launch_failures); }
 int take_stall_mask() { return g_inject_stall_mask.exchange(0); }
 uint64_t wait_limit_ns() { return g_wait_ns.load(); }
+int csa_union_setting() { return g_csa_union.load(); }
 }  // namespace hca
 
 extern "C" {
@@ -130,6 +132,7 @@ int hca_test_inject(int what, long long value) {
       g_inject_launch_failures = 0;
       g_inject_stall_mask = 0;
       g_wait_ns = kDefaultWaitNs;
+      g_csa_union = 0;
       return HCA_OK;
     case HCA_INJECT_LAUNCH_FAILURE: g_inject_launch_failures = value; return HCA_OK;
     case HCA_INJECT_STALL:
@@ -137,6 +140,10 @@ int hca_test_inject(int what, long long value) {
       g_inject_stall_mask = (int)value;
       return HCA_OK;
     case HCA_INJECT_WAIT_LIMIT_NS: g_wait_ns = value == 0 ? kDefaultWaitNs : (unsigned long long)value; return HCA_OK;
+    case HCA_INJECT_CSA_UNION:
+      if (value > 16384 || (value > 1 && value % 64 != 0)) return HCA_ERR_ARG;
+      g_csa_union = (int)value;
+      return HCA_OK;
     default: return HCA_ERR_ARG;
   }
 }

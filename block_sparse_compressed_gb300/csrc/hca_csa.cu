@@ -11,9 +11,11 @@
 // selections outside that set, repeats and -1 padding are ignored.
 //
 // This file holds the CSA-only parts:
-//   - csa_union_kernel: per group of P consecutive positions (a forward
-//     pair or a dq tile), the sorted set of entries any of them selected
-//     and may see, each with the bit mask of the positions that selected it.
+//   - csa_union_mask_kernel / csa_union_kernel: per group of P consecutive
+//     positions (a forward pair or a dq tile), the sorted set of entries any
+//     of them selected and may see, each with the bit mask of the positions
+//     that selected it (from byte masks over the group's entry range, or from
+//     a sort of the selections, whichever moves fewer bytes).
 //     The attention kernels gather those ckv rows into their key blocks and
 //     mask each row by its position's bit.
 //   - hca_csa_dckv_kernel: dckv, query-major.  Per query tile and block of
@@ -49,6 +51,7 @@ struct UnionArgs {
   int32_t *ent;           // [B*ngroups][cap]
   uint32_t *mask;         // [B*ngroups][cap]
   int B, S, m, Sc, k, P, ngroups, cap, sortn;
+  int chunk;  // byte-mask kernel: entries per shared-memory chunk (a multiple of 64)
 };
 
 __global__ void __launch_bounds__(kUnionThreads) csa_union_kernel(const UnionArgs a) {
@@ -125,6 +128,128 @@ __global__ void __launch_bounds__(kUnionThreads) csa_union_kernel(const UnionArg
   for (int t = out + tid; t < padded; t += kUnionThreads) {
     a.ent[base + t] = 0;
     a.mask[base + t] = 0u;
+  }
+  if (tid == 0) a.cnt[g] = out;
+}
+
+// The same union from one byte of position bits per entry.  The group's
+// entries lie in [lo, hi] (the union of its positions' visible compressed
+// ranges); a chunk of that range is zeroed in shared memory, every selection
+// inside the chunk ORs its position's bit into its entry's byte (a shared
+// atomic on the containing word), and the non-zero bytes are compacted in
+// entry order.  Its cost follows the range (zeroing and one pass over it)
+// instead of the bitonic sort's P k log^2(P k) steps; the output is the same
+// sorted list.  Needs P <= 8.
+constexpr int kMaskPositions = 8;
+constexpr int kMaskChunk = 16384;  // default entries (bytes) per chunk
+
+__global__ void __launch_bounds__(kUnionThreads) csa_union_mask_kernel(const UnionArgs a) {
+  extern __shared__ uint4 words4[];  // a.chunk bytes: the chunk's entries
+  uint32_t *words = reinterpret_cast<uint32_t *>(words4);
+  __shared__ int wsum[kUnionThreads / 32];
+  __shared__ int2 civ[kMaskPositions];  // visible compressed range per position (empty: x > y)
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int g = blockIdx.x;
+  const int b = g / a.ngroups, pos0 = (g % a.ngroups) * a.P;
+  if (tid < a.P) {
+    const int i = pos0 + tid;
+    int2 r = make_int2(1, 0);
+    if (i < a.S) {
+      const RowIv iv = row_interval(a.sstart, b, a.S, i, 1, a.m);
+      if (iv.valid) r = make_int2(iv.clo, min(iv.chi, a.Sc - 1));
+    }
+    civ[tid] = r;
+  }
+  __syncthreads();
+  int lo = 0x7fffffff, hi = -1;
+  for (int p = 0; p < a.P; ++p)
+    if (civ[p].x <= civ[p].y) {
+      lo = min(lo, civ[p].x);
+      hi = max(hi, civ[p].y);
+    }
+  int32_t *ent = a.ent + (size_t)g * a.cap;
+  uint32_t *msk = a.mask + (size_t)g * a.cap;
+  // each thread's first selection of every position, loaded together (the
+  // rest, for k > kUnionThreads, are read per chunk)
+  const size_t row0 = (size_t)b * a.S + pos0;
+  int ev[kMaskPositions];
+#pragma unroll
+  for (int p = 0; p < kMaskPositions; ++p) {
+    ev[p] = -1;
+    if (p < a.P && civ[p].x <= civ[p].y && tid < a.k) ev[p] = a.sel[(row0 + p) * a.k + tid];
+  }
+  int out = 0;
+  for (int c0 = lo; c0 <= hi; c0 += a.chunk) {
+    const int width = min(a.chunk, hi - c0 + 1);
+    const int n4 = (width + 15) >> 4;  // 16 entries per uint4
+    for (int w = tid; w < n4; w += kUnionThreads) words4[w] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    // a selection e of position p counts when it is visible to p and in
+    // this chunk: e in [max(clo, c0), min(chi, c0 + width - 1)]
+#pragma unroll
+    for (int p = 0; p < kMaskPositions; ++p) {
+      if (p < a.P) {
+        const int elo = max(civ[p].x, c0), ehi = min(civ[p].y, c0 + width - 1);
+        const int e = ev[p];
+        if (e >= elo && e <= ehi) atomicOr(&words[(e - c0) >> 2], (1u << p) << (8 * ((e - c0) & 3)));
+        for (int j = tid + kUnionThreads; j < a.k && elo <= ehi; j += kUnionThreads) {
+          const int e2 = a.sel[(row0 + p) * a.k + j];
+          if (e2 >= elo && e2 <= ehi) atomicOr(&words[(e2 - c0) >> 2], (1u << p) << (8 * ((e2 - c0) & 3)));
+        }
+      }
+    }
+    __syncthreads();
+    // ordered compaction: thread tid of round q takes entries
+    // [16 (q*256 + tid), +16) of the chunk
+    for (int q0 = 0; q0 < n4; q0 += kUnionThreads) {
+      const int q = q0 + tid;
+      const uint4 v = q < n4 ? words4[q] : make_uint4(0u, 0u, 0u, 0u);
+      // bit 4x + y of nz: byte y of word x is non-zero (the byte's high bit
+      // after adding 0x7f to its low seven bits, or its own high bit; the
+      // four high bits then gathered into a nibble by one multiply whose
+      // partial products do not overlap)
+      uint32_t nz = 0;
+      {
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const uint32_t hb = (((wv[x] & 0x7f7f7f7fu) + 0x7f7f7f7fu) | wv[x]) & 0x80808080u;
+          nz |= (((hb >> 7) * 0x01020408u) >> 24) << (4 * x);
+        }
+      }
+      const int cnt = __popc(nz);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) wsum[wid] = incl;
+      __syncthreads();
+      int before = 0, total = 0;
+#pragma unroll
+      for (int w = 0; w < kUnionThreads / 32; ++w) {
+        if (w < wid) before += wsum[w];
+        total += wsum[w];
+      }
+      __syncthreads();
+      int pos = out + before + incl - cnt;
+      while (nz != 0u) {
+        const int bi = __ffs(nz) - 1;
+        nz &= nz - 1u;
+        const uint32_t wsel = (bi & 8) ? ((bi & 4) ? v.w : v.z) : ((bi & 4) ? v.y : v.x);
+        ent[pos] = c0 + 16 * q + bi;
+        msk[pos] = (wsel >> (8 * (bi & 3))) & 0xffu;
+        ++pos;
+      }
+      out += total;
+    }
+  }
+  // pad to a multiple of 16 with a loadable row that no position sees
+  const int padded = (out + 15) & ~15;
+  for (int t = out + tid; t < padded; t += kUnionThreads) {
+    ent[t] = 0;
+    msk[t] = 0u;
   }
   if (tid == 0) a.cnt[g] = out;
 }
@@ -540,11 +665,31 @@ cudaError_t csa_build_union(const int32_t *sel, const int32_t *sstart, int B, in
   a.B = B; a.S = S; a.m = m; a.Sc = (S + m - 1) / m; a.k = k; a.P = P; a.ngroups = ng; a.cap = u.cap;
   a.sortn = next_pow2(P * k);
   if (a.sortn < 2) a.sortn = 2;
-  static SmemAttrOnce attr;
-  cudaError_t e = attr.ensure(reinterpret_cast<const void *>(csa_union_kernel), 32768 * (int)sizeof(uint32_t));
-  if (e != cudaSuccess) return e;
+  a.chunk = kMaskChunk;
+  // shared-memory bytes moved per group: the sort's compare-exchange stages
+  // (two loads, up to two stores each) against zeroing and scanning the
+  // entry range (Sc/2 on average) plus one atomic per selection
+  int lg = 0;
+  while ((1 << lg) < a.sortn) ++lg;
+  const long long sort_cost = (long long)a.sortn * (lg * (lg + 1) / 2) * 6;
+  const long long mask_cost = (long long)a.Sc + 4LL * P * k;
+  bool use_mask = P <= kMaskPositions && mask_cost < sort_cost;
+  const int setting = csa_union_setting();
+  if (setting == 1) use_mask = false;
+  if (setting >= 64) {
+    if (P > kMaskPositions) return cudaErrorInvalidValue;
+    use_mask = true;
+    a.chunk = setting;
+  }
   ProfScope prof(kKCsaUnion, st);
-  csa_union_kernel<<<B * ng, kUnionThreads, a.sortn * sizeof(uint32_t), st>>>(a);
+  if (use_mask) {
+    csa_union_mask_kernel<<<B * ng, kUnionThreads, a.chunk, st>>>(a);
+  } else {
+    static SmemAttrOnce attr;
+    cudaError_t e = attr.ensure(reinterpret_cast<const void *>(csa_union_kernel), 32768 * (int)sizeof(uint32_t));
+    if (e != cudaSuccess) return e;
+    csa_union_kernel<<<B * ng, kUnionThreads, a.sortn * sizeof(uint32_t), st>>>(a);
+  }
   return cudaGetLastError();
 }
 

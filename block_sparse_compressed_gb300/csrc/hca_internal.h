@@ -68,6 +68,9 @@ struct BwdArgs {
 bool take_launch_failure();
 int take_stall_mask();
 uint64_t wait_limit_ns();
+// How the CSA union is built (HCA_INJECT_CSA_UNION): 0 automatic, 1 the
+// sorting kernel, c >= 64 the byte-mask kernel with chunks of c entries.
+int csa_union_setting();
 
 cudaError_t launch_prep(const int32_t *seg, int B, int S, int32_t *sstart, int32_t *status, cudaStream_t st);
 cudaError_t launch_visible_pairs(const int32_t *sstart, int B, int S, int W, int m, int64_t *raw, int64_t *comp,

@@ -34,7 +34,7 @@ EXPORTS = ("hca_status_string", "hca_version", "hca_workspace_size", "hca_query_
            "hca_indexer_topk", "hca_csa_workspace_size", "hca_csa_attn_fwd", "hca_csa_attn_bwd")
 
 # failure-path test hooks (hca_test_inject)
-INJECT_RESET, INJECT_LAUNCH_FAILURE, INJECT_STALL, INJECT_WAIT_LIMIT_NS = 0, 1, 2, 3
+INJECT_RESET, INJECT_LAUNCH_FAILURE, INJECT_STALL, INJECT_WAIT_LIMIT_NS, INJECT_CSA_UNION = 0, 1, 2, 3, 4
 
 
 class HCAError(RuntimeError):

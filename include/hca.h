@@ -281,13 +281,21 @@ HCA_API int hca_indexer_topk(const void *qi, const void *ki, const float *w, con
  *                             their outputs, and the call's workspace status
  *                             reads HCA_ERR_TIMEOUT;
  *   HCA_INJECT_WAIT_LIMIT_NS  limit of every bounded on-device wait, in ns,
- *                             for later launches (0 restores the default 2 s).
+ *                             for later launches (0 restores the default 2 s);
+ *   HCA_INJECT_CSA_UNION      how later CSA calls build each query group's
+ *                             union of selected entries: 0 picks the cheaper
+ *                             of the two kernels (the default), 1 forces the
+ *                             sorting kernel, a multiple of 64 up to 16384
+ *                             forces the byte-mask kernel with chunks of that
+ *                             many entries (so small cases reach its
+ *                             several-chunk path).  Both give the same union.
  * The settings are process-wide.  Returns HCA_OK, or HCA_ERR_ARG for an
- * unknown `what` or a negative value. */
+ * unknown `what`, a negative value or a value out of its range. */
 #define HCA_INJECT_RESET 0
 #define HCA_INJECT_LAUNCH_FAILURE 1
 #define HCA_INJECT_STALL 2
 #define HCA_INJECT_WAIT_LIMIT_NS 3
+#define HCA_INJECT_CSA_UNION 4
 #define HCA_STALL_FWD 1
 #define HCA_STALL_DQ 2
 #define HCA_STALL_DKV 4

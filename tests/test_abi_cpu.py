@@ -127,6 +127,10 @@ def test_test_hooks_argument_checks(lib):
     assert lib.hca_test_inject(2, 8) == E_ARG       # not a mask of the three kernels
     assert lib.hca_test_inject(99, 0) == E_ARG
     assert lib.hca_test_inject(3, 1000) == OK
+    assert lib.hca_test_inject(4, 1) == OK          # CSA union: sorting kernel
+    assert lib.hca_test_inject(4, 128) == OK        # byte-mask kernel, 128-entry chunks
+    assert lib.hca_test_inject(4, 63) == E_ARG      # chunks are multiples of 64
+    assert lib.hca_test_inject(4, 16384 + 64) == E_ARG
     assert lib.hca_test_inject(0, 0) == OK
 
 

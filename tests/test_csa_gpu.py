@@ -51,6 +51,46 @@ def test_csa_matches_oracle(B, H, S, W, m, k):
     run_csa(B, H, S, W, m, k)
 
 
+@pytest.fixture
+def union_setting():
+    yield lambda v: hca.hca_test_inject(hca.INJECT_CSA_UNION, v)
+    hca.hca_test_inject(hca.INJECT_RESET)
+
+
+@pytest.mark.parametrize("setting", [1, 64, 0])
+def test_csa_union_kernels_agree(union_setting, setting):
+    # the per-group union of selections comes from a bitonic sort (1) or from
+    # byte masks over the group's entry range (64: 64-entry chunks, so a
+    # group's range spans several); both against the oracle, and the
+    # forward and dq (no atomics) bit-identical to the automatic choice
+    B, H, S, W, m, k = 1, 64, 1100, 128, 4, 96
+    seed = 11
+    q, kv, ckv, _, dout = I.small(B, H, S, 128, W, m, dtype=torch.bfloat16, seed=seed)
+    sel = I.random_selection(B, S, m, k, seed + 50).to(DEV)
+    g = [x.to(DEV) for x in (q, kv, ckv, dout)]
+    scale = 1 / math.sqrt(128)
+
+    def call():
+        o, l = hca.hca_csa_attn_fwd(g[0], g[1], g[2], None, sel, W, m, scale, check=True)
+        d = hca.hca_csa_attn_bwd(g[0], g[1], g[2], None, sel, o, l, g[3], W, m, scale, check=True)
+        return o, l, d[0]
+
+    ref = call()
+    union_setting(setting)
+    got = call()
+    for name, a, b in zip(("out", "lse", "dq"), got, ref):
+        assert torch.equal(a, b), name
+    run_csa(B, H, S, W, m, k, seed=seed)
+
+
+def test_csa_union_chunks_with_documents(union_setting):
+    union_setting(64)
+    S = 700
+    seg = torch.cat([I.segments_from_lengths([250, 300, 100], S, pad=50),
+                     I.segments_from_lengths([699], S, pad=1)])
+    run_csa(2, 64, S, 96, 4, 24, seg=seg)
+
+
 def test_csa_documents_and_padding():
     S = 700
     seg = torch.cat([I.segments_from_lengths([250, 300, 100], S, pad=50),
