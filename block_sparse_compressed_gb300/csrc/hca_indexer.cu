@@ -301,12 +301,53 @@ struct TopkParams {
   int B, S, m, Sc, row0, rows, ld, k;
 };
 
+// Digit of a radix pass: scanning the histogram h (nbins = dmask + 1 bins)
+// from the top, the bin where the running count reaches rem.  Thread t owns
+// the 8 bins [top - 8t - 7, top - 8t]; the thread holding the crossing bin
+// writes the digit, the winners still to place inside it and the bin's size.
+__device__ __forceinline__ void select_digit(const int *h, int dmask, int rem, int *wsum, int *sh) {
+  const int tid = threadIdx.x;
+  int c[8], sum = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int d = dmask - (tid * 8 + q);
+    c[q] = d >= 0 ? h[d] : 0;
+    sum += c[q];
+  }
+  int before;
+  block_excl_scan(sum, before, wsum);
+  if (before < rem && before + sum >= rem) {
+    int run = before;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (run + c[q] >= rem) {
+        sh[0] = dmask - (tid * 8 + q);
+        sh[1] = rem - run;
+        sh[2] = c[q];
+        break;
+      }
+      run += c[q];
+    }
+  }
+  __syncthreads();
+}
+
+// Candidates: entries whose top digit is the k-th largest key's, when they
+// fit beside the small histogram in the top digit's histogram space.
+constexpr int kSmallBins = 128;  // 7-bit digits over the candidates
+constexpr int kCandCap = kRadixBins - kSmallBins;
+
 __global__ void __launch_bounds__(kTopkThreads) hca_index_topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t keys[];
-  __shared__ int hist[kRadixBins];
+  // the top digit's histogram; afterwards a small histogram and the
+  // candidate list, or (too many candidates) the wide histogram again
+  __shared__ int area[kRadixBins];
   __shared__ int wsum[kTopkThreads / 32];
-  __shared__ int sh_digit, sh_rem;
-  const int tid = threadIdx.x, lane = tid & 31;
+  __shared__ int sh[3];
+  __shared__ int ncand;
+  constexpr int kWarps = kTopkThreads / 32;
+  __shared__ int wgt[kWarps], weq[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int b = blockIdx.x / p.rows;
   const int i = p.row0 + blockIdx.x % p.rows;
   if (i >= p.S) return;
@@ -328,96 +369,132 @@ __global__ void __launch_bounds__(kTopkThreads) hca_index_topk_kernel(const Topk
     for (int t = tid; t < p.k; t += kTopkThreads) out[t] = t < n ? lo + t : -1;
     return;
   }
-  for (int t = tid; t < n; t += kTopkThreads) keys[t] = fkey(row[lo + t]);
-  // radix select of the k-th largest key: digits of 11, 11 and 10 bits from
-  // the top.  Lanes whose digit agrees add to the histogram once per group
-  // (match.any), so bins that most keys share (the exponent bits of similar
-  // scores) do not serialise the block on one shared-memory address.
-  uint32_t prefix = 0, mask = 0;
-  int rem = p.k;  // winners still to place at or below the current prefix
-#pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const int bits = pass == 2 ? 10 : 11;
-    const uint32_t dmask = (1u << bits) - 1u;
-    for (int d = tid; d < kRadixBins; d += kTopkThreads) hist[d] = 0;
-    __syncthreads();
-    if (pass == 0) {
-      for (int t0 = 0; t0 < n; t0 += kTopkThreads) {
-        const int t = t0 + tid;
-        const uint32_t kv = t < n ? keys[t] : 0u;
-        const uint32_t dg = t < n ? (kv >> shift) & dmask : 0xffffffffu;
-        const unsigned peers = __match_any_sync(0xffffffffu, dg);
-        if (t < n && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
-      }
-    } else {
-      // only the keys under the prefix count, a few percent of them, with
-      // digits spread over the bins: plain atomics
-      for (int t = tid; t < n; t += kTopkThreads) {
-        const uint32_t kv = keys[t];
-        if ((kv & mask) == prefix) atomicAdd(&hist[(kv >> shift) & dmask], 1);
-      }
-    }
-    __syncthreads();
-    // digit from the top where the running count reaches rem: thread t owns
-    // the 8 bins [top - 8t - 7, top - 8t] (top = 2^bits - 1)
-    const int top = (int)dmask;
-    int c[8], sum = 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int d = top - (tid * 8 + q);
-      c[q] = d >= 0 ? hist[d] : 0;
-      sum += c[q];
-    }
-    int before;
-    block_excl_scan(sum, before, wsum);
-    if (before < rem && before + sum >= rem) {
-      int run = before;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (run + c[q] >= rem) {
-          sh_digit = top - (tid * 8 + q);
-          sh_rem = rem - run;
-          break;
-        }
-        run += c[q];
-      }
-    }
-    __syncthreads();
-    prefix |= (uint32_t)sh_digit << shift;
-    mask |= dmask << shift;
-    rem = sh_rem;
-    __syncthreads();
-  }
-  // prefix is the k-th largest key; rem of the keys equal to it are taken,
-  // the ones with the smallest entry index.  Ordered compaction: warp w owns
-  // the keys [w L, (w + 1) L), swept 32 at a time.  A first sweep counts the
-  // warp's keys above and equal to prefix, one scan over the warps gives each
-  // its output and tie offsets, and a second sweep writes with ballots.
-  constexpr int kWarps = kTopkThreads / 32;
-  __shared__ int wgt[kWarps], weq[kWarps];
-  const int wid = tid >> 5;
-  const int L = ((n + kWarps - 1) / kWarps + 31) & ~31;
-  const int s0 = min(wid * L, n), s1 = min(s0 + L, n);
-  int gt = 0, eqc = 0;
-  for (int t0 = s0; t0 < s1; t0 += 32) {
-    const int t = t0 + lane;
-    const uint32_t kv = t < s1 ? keys[t] : 0u;
-    gt += __popc(__ballot_sync(0xffffffffu, t < s1 && kv > prefix));
-    eqc += __popc(__ballot_sync(0xffffffffu, t < s1 && kv == prefix));
-  }
-  if (lane == 0) {
-    wgt[wid] = gt;
-    weq[wid] = eqc;
+  // Radix select of the k-th largest key, top digit 11 bits.  Its histogram
+  // is built while the keys are staged (eight loads in flight per thread);
+  // lanes whose digit agrees add once per group (match.any), so bins that
+  // most keys share (the exponent bits of similar scores) do not serialise
+  // the block on one shared-memory address.
+  for (int d = tid; d < kRadixBins; d += kTopkThreads) area[d] = 0;
+  if (tid == 0) ncand = 0;
+  if (tid < kWarps) {
+    wgt[tid] = 0;
+    weq[tid] = 0;
   }
   __syncthreads();
+  constexpr int kInFlight = 8;
+  const float *src = row + lo;
+  for (int t0 = 0; t0 < n; t0 += kInFlight * kTopkThreads) {
+    uint32_t kv[kInFlight];
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      const int t = t0 + u * kTopkThreads + tid;
+      kv[u] = t < n ? fkey(src[t]) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      const int t = t0 + u * kTopkThreads + tid;
+      if (t < n) keys[t] = kv[u];
+      const uint32_t dg = t < n ? kv[u] >> 21 : 0xffffffffu;
+      const unsigned peers = __match_any_sync(0xffffffffu, dg);
+      if (t < n && lane == __ffs(peers) - 1) atomicAdd(&area[dg], __popc(peers));
+    }
+  }
+  __syncthreads();
+  select_digit(area, kRadixBins - 1, p.k, wsum, sh);
+  const uint32_t d0 = (uint32_t)sh[0];
+  uint32_t prefix = d0 << 21, mask = 0x7ffu << 21;
+  int rem = sh[1];  // winners still to place at or below the current prefix
+  const bool use_cand = sh[2] <= kCandCap;
+  __syncthreads();  // everyone has read sh and the histogram
+  // Winners are the keys above prefix plus the rem keys equal to it with the
+  // smallest entry index.  Warp w owns the keys [w L, (w + 1) L) for the
+  // ordered output (and for the per-warp counts).
+  const int L = ((n + kWarps - 1) / kWarps + 31) & ~31;
+  const int s0 = min(wid * L, n), s1 = min(s0 + L, n);
+  const uint32_t lt = (1u << lane) - 1u;
+  if (use_cand) {
+    int *hs = area;
+    int *cand = area + kSmallBins;
+    // one sweep: keys above the top digit per warp, candidates listed
+    int above = 0;
+    for (int t0 = s0; t0 < s1; t0 += 32) {
+      const int t = t0 + lane;
+      const uint32_t dg = t < s1 ? keys[t] >> 21 : 0u;
+      above += __popc(__ballot_sync(0xffffffffu, t < s1 && dg > d0));
+      const bool c = t < s1 && dg == d0;
+      const unsigned bc = __ballot_sync(0xffffffffu, c);
+      int cb = 0;
+      if (lane == 0 && bc) cb = atomicAdd(&ncand, __popc(bc));
+      cb = __shfl_sync(0xffffffffu, cb, 0);
+      if (c) cand[cb + __popc(bc & lt)] = t;
+    }
+    if (lane == 0) wgt[wid] = above;
+    // the remaining 21 bits in three 7-bit digits, over the candidates only
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = 14 - 7 * pass;
+      for (int d = tid; d < kSmallBins; d += kTopkThreads) hs[d] = 0;
+      __syncthreads();
+      const int nc = ncand;
+      for (int c = tid; c < nc; c += kTopkThreads) {
+        const uint32_t kv = keys[cand[c]];
+        if ((kv & mask) == prefix) atomicAdd(&hs[(kv >> shift) & (kSmallBins - 1)], 1);
+      }
+      __syncthreads();
+      select_digit(hs, kSmallBins - 1, rem, wsum, sh);
+      prefix |= (uint32_t)sh[0] << shift;
+      mask |= (uint32_t)(kSmallBins - 1) << shift;
+      rem = sh[1];
+      __syncthreads();
+    }
+    // the candidates above and equal to the k-th key, per owning warp
+    const int nc = ncand;
+    for (int c = tid; c < nc; c += kTopkThreads) {
+      const int t = cand[c];
+      const uint32_t kv = keys[t];
+      if (kv > prefix) atomicAdd(&wgt[t / L], 1);
+      else if (kv == prefix) atomicAdd(&weq[t / L], 1);
+    }
+  } else {
+    // too many candidates: digits of 11 and 10 bits over every key
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+      const int shift = pass == 0 ? 10 : 0;
+      const uint32_t dmask = pass == 0 ? 0x7ffu : 0x3ffu;
+      for (int d = tid; d < kRadixBins; d += kTopkThreads) area[d] = 0;
+      __syncthreads();
+      for (int t = tid; t < n; t += kTopkThreads) {
+        const uint32_t kv = keys[t];
+        if ((kv & mask) == prefix) atomicAdd(&area[(kv >> shift) & dmask], 1);
+      }
+      __syncthreads();
+      select_digit(area, (int)dmask, rem, wsum, sh);
+      prefix |= (uint32_t)sh[0] << shift;
+      mask |= dmask << shift;
+      rem = sh[1];
+      __syncthreads();
+    }
+    int gt = 0, eqc = 0;
+    for (int t0 = s0; t0 < s1; t0 += 32) {
+      const int t = t0 + lane;
+      const uint32_t kv = t < s1 ? keys[t] : 0u;
+      gt += __popc(__ballot_sync(0xffffffffu, t < s1 && kv > prefix));
+      eqc += __popc(__ballot_sync(0xffffffffu, t < s1 && kv == prefix));
+    }
+    if (lane == 0) {
+      wgt[wid] = gt;
+      weq[wid] = eqc;
+    }
+  }
+  __syncthreads();
+  // ordered write: one scan over the warps' counts gives each warp its
+  // output and tie offsets, then a sweep with ballots
   int gt_run = 0, eq_run = 0;
   for (int w = 0; w < wid; ++w) {
     gt_run += wgt[w];
     eq_run += weq[w];
   }
   int placed = gt_run + min(eq_run, rem);  // winners with a smaller entry index
-  const uint32_t lt = (1u << lane) - 1u;
   for (int t0 = s0; t0 < s1; t0 += 32) {
     const int t = t0 + lane;
     const uint32_t kv = t < s1 ? keys[t] : 0u;

@@ -87,6 +87,23 @@ def test_indexer_full_size_sampled_rows():
         _check_rows(sel_c[0, r0:r0 + 8], sc_c[0, r0:r0 + 8].astype(np.float64), ref[0], k)
 
 
+def test_indexer_ties():
+    # the entries repeat three key vectors, so every row's scores take three
+    # values: the k-th largest is a heavy tie (smaller entry index first);
+    # early rows resolve it from the list of keys sharing the k-th key's top
+    # digit, late rows (more than the list holds) from passes over every key
+    B, S, Hi, m, k = 1, 8192, 2, 1, 100
+    qi, ki, w = _inputs(B, S, Hi, m, 51)
+    pick = torch.from_numpy(np.random.Generator(np.random.PCG64(5)).integers(0, 3, S))
+    ki = ki[:, :3][:, pick].contiguous()
+    sel, sc = hca.hca_indexer_topk(qi.to(DEV), ki.to(DEV), w.to(DEV), None, m, k, with_scores=True, check=True)
+    sel_c, sc_c = sel.cpu().numpy(), sc.cpu().numpy()
+    for r0 in (0, 96, 3000, 6000, S - 8):
+        rows = (r0, r0 + 8)
+        ref = CI.index_scores(qi, ki, w, None, m, rows=rows)
+        _check_rows(sel_c[0, r0:r0 + 8], sc_c[0, r0:r0 + 8].astype(np.float64), ref[0], k)
+
+
 def test_indexer_bad_segments_select_nothing():
     qi, ki, w = _inputs(1, 64, 2, 4, 3)
     seg = torch.zeros(1, 64, dtype=torch.int32)
