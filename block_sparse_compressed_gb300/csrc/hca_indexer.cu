@@ -332,12 +332,51 @@ __device__ __forceinline__ void select_digit(const int *h, int dmask, int rem, i
   __syncthreads();
 }
 
+// The same for a histogram of at most 256 bins, by warp 0 alone (eight bins
+// per lane, one warp scan): the other warps only wait at the barrier.
+__device__ __forceinline__ void select_digit_warp(const int *h, int dmask, int rem, int *sh) {
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    int c[8], sum = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int d = dmask - (tid * 8 + q);
+      c[q] = d >= 0 ? h[d] : 0;
+      sum += c[q];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (tid >= o) incl += y;
+    }
+    const int before = incl - sum;
+    if (before < rem && incl >= rem) {
+      int run = before;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (run + c[q] >= rem) {
+          sh[0] = dmask - (tid * 8 + q);
+          sh[1] = rem - run;
+          sh[2] = c[q];
+          break;
+        }
+        run += c[q];
+      }
+    }
+  }
+  __syncthreads();
+}
+
 // Candidates: entries whose top digit is the k-th largest key's, when they
 // fit beside the small histogram in the top digit's histogram space.
 constexpr int kSmallBins = 128;  // 7-bit digits over the candidates
 constexpr int kCandCap = kRadixBins - kSmallBins;
+// keys at or above a sampled threshold: 8-bit digits over them
+constexpr int kByteBins = 256;
+constexpr int kTauCap = kRadixBins - kByteBins;
 
-__global__ void __launch_bounds__(kTopkThreads) hca_index_topk_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kTopkThreads, 6) hca_index_topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t keys[];
   // the top digit's histogram; afterwards a small histogram and the
   // candidate list, or (too many candidates) the wide histogram again
@@ -369,11 +408,9 @@ __global__ void __launch_bounds__(kTopkThreads) hca_index_topk_kernel(const Topk
     for (int t = tid; t < p.k; t += kTopkThreads) out[t] = t < n ? lo + t : -1;
     return;
   }
-  // Radix select of the k-th largest key, top digit 11 bits.  Its histogram
-  // is built while the keys are staged (eight loads in flight per thread);
-  // lanes whose digit agrees add once per group (match.any), so bins that
-  // most keys share (the exponent bits of similar scores) do not serialise
-  // the block on one shared-memory address.
+  // The keys are staged in shared memory (eight loads in flight per
+  // thread) while every eighth one (by entry index: at most four lanes of a
+  // warp per atomic) goes into a histogram of the top 11-bit digit.
   for (int d = tid; d < kRadixBins; d += kTopkThreads) area[d] = 0;
   if (tid == 0) ncand = 0;
   if (tid < kWarps) {
@@ -393,18 +430,22 @@ __global__ void __launch_bounds__(kTopkThreads) hca_index_topk_kernel(const Topk
 #pragma unroll
     for (int u = 0; u < kInFlight; ++u) {
       const int t = t0 + u * kTopkThreads + tid;
-      if (t < n) keys[t] = kv[u];
-      const uint32_t dg = t < n ? kv[u] >> 21 : 0xffffffffu;
-      const unsigned peers = __match_any_sync(0xffffffffu, dg);
-      if (t < n && lane == __ffs(peers) - 1) atomicAdd(&area[dg], __popc(peers));
+      if (t < n) {
+        keys[t] = kv[u];
+        if ((t & 7) == 0) atomicAdd(&area[kv[u] >> 21], 1);
+      }
     }
   }
   __syncthreads();
-  select_digit(area, kRadixBins - 1, p.k, wsum, sh);
-  const uint32_t d0 = (uint32_t)sh[0];
-  uint32_t prefix = d0 << 21, mask = 0x7ffu << 21;
-  int rem = sh[1];  // winners still to place at or below the current prefix
-  const bool use_cand = sh[2] <= kCandCap;
+  // Threshold: the lower edge of the top-digit bin where the sample's count
+  // from the top reaches its share of k plus a margin (about three standard
+  // deviations of that count), so that normally at least k keys lie at or
+  // above it; the sample's own digits are exact, only the count is an
+  // estimate.
+  const int ns = (n + 7) >> 3;
+  const int want = min(ns, (int)(((long long)p.k * 115 * ns + 100LL * n - 1) / (100LL * n)) + 16);
+  select_digit(area, kRadixBins - 1, want, wsum, sh);
+  const uint32_t tau = (uint32_t)sh[0] << 21;
   __syncthreads();  // everyone has read sh and the histogram
   // Winners are the keys above prefix plus the rem keys equal to it with the
   // smallest entry index.  Warp w owns the keys [w L, (w + 1) L) for the
@@ -412,78 +453,148 @@ __global__ void __launch_bounds__(kTopkThreads) hca_index_topk_kernel(const Topk
   const int L = ((n + kWarps - 1) / kWarps + 31) & ~31;
   const int s0 = min(wid * L, n), s1 = min(s0 + L, n);
   const uint32_t lt = (1u << lane) - 1u;
-  if (use_cand) {
-    int *hs = area;
-    int *cand = area + kSmallBins;
-    // one sweep: keys above the top digit per warp, candidates listed
-    int above = 0;
+  uint32_t prefix = 0, mask = 0;
+  int rem = p.k;  // winners still to place at or below the current prefix
+  {
+    // one sweep: the keys at or above the threshold, listed if they fit
+    int *cand = area + kByteBins;
     for (int t0 = s0; t0 < s1; t0 += 32) {
       const int t = t0 + lane;
-      const uint32_t dg = t < s1 ? keys[t] >> 21 : 0u;
-      above += __popc(__ballot_sync(0xffffffffu, t < s1 && dg > d0));
-      const bool c = t < s1 && dg == d0;
+      const bool c = t < s1 && keys[t] >= tau;
       const unsigned bc = __ballot_sync(0xffffffffu, c);
-      int cb = 0;
-      if (lane == 0 && bc) cb = atomicAdd(&ncand, __popc(bc));
-      cb = __shfl_sync(0xffffffffu, cb, 0);
-      if (c) cand[cb + __popc(bc & lt)] = t;
+      if (bc) {
+        int cb = 0;
+        if (lane == 0) cb = atomicAdd(&ncand, __popc(bc));
+        cb = __shfl_sync(0xffffffffu, cb, 0);
+        const int slot = cb + __popc(bc & lt);
+        if (c && slot < kTauCap) cand[slot] = t;
+      }
     }
-    if (lane == 0) wgt[wid] = above;
-    // the remaining 21 bits in three 7-bit digits, over the candidates only
+  }
+  __syncthreads();
+  const int nlisted = ncand;
+  __syncthreads();  // read by everyone before the exact path may reset it
+  if (nlisted >= p.k && nlisted <= kTauCap) {
+    // the k-th largest key is among the listed ones (every other key is
+    // below the threshold): four 8-bit digits over the list
+    int *hs = area;
+    const int *cand = area + kByteBins;
 #pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-      const int shift = 14 - 7 * pass;
-      for (int d = tid; d < kSmallBins; d += kTopkThreads) hs[d] = 0;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int d = tid; d < kByteBins; d += kTopkThreads) hs[d] = 0;
       __syncthreads();
-      const int nc = ncand;
-      for (int c = tid; c < nc; c += kTopkThreads) {
+      for (int c = tid; c < nlisted; c += kTopkThreads) {
         const uint32_t kv = keys[cand[c]];
-        if ((kv & mask) == prefix) atomicAdd(&hs[(kv >> shift) & (kSmallBins - 1)], 1);
+        if ((kv & mask) == prefix) atomicAdd(&hs[(kv >> shift) & (kByteBins - 1)], 1);
       }
       __syncthreads();
-      select_digit(hs, kSmallBins - 1, rem, wsum, sh);
+      // the next pass zeroes hs only after two more barriers, and sh is
+      // rewritten only after them: no barrier after reading sh
+      select_digit_warp(hs, kByteBins - 1, rem, sh);
       prefix |= (uint32_t)sh[0] << shift;
-      mask |= (uint32_t)(kSmallBins - 1) << shift;
+      mask |= (uint32_t)(kByteBins - 1) << shift;
       rem = sh[1];
-      __syncthreads();
     }
-    // the candidates above and equal to the k-th key, per owning warp
-    const int nc = ncand;
-    for (int c = tid; c < nc; c += kTopkThreads) {
+    for (int c = tid; c < nlisted; c += kTopkThreads) {
       const int t = cand[c];
       const uint32_t kv = keys[t];
       if (kv > prefix) atomicAdd(&wgt[t / L], 1);
       else if (kv == prefix) atomicAdd(&weq[t / L], 1);
     }
   } else {
-    // too many candidates: digits of 11 and 10 bits over every key
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-      const int shift = pass == 0 ? 10 : 0;
-      const uint32_t dmask = pass == 0 ? 0x7ffu : 0x3ffu;
-      for (int d = tid; d < kRadixBins; d += kTopkThreads) area[d] = 0;
-      __syncthreads();
-      for (int t = tid; t < n; t += kTopkThreads) {
-        const uint32_t kv = keys[t];
-        if ((kv & mask) == prefix) atomicAdd(&area[(kv >> shift) & dmask], 1);
+    // the sample missed: the exact top digit from every key
+    for (int d = tid; d < kRadixBins; d += kTopkThreads) area[d] = 0;
+    if (tid == 0) ncand = 0;
+    __syncthreads();
+    for (int t0 = 0; t0 < n; t0 += kTopkThreads) {
+      const int t = t0 + tid;
+      const uint32_t dg = t < n ? keys[t] >> 21 : 0xffffffffu;
+      // lanes whose digit agrees add once per group (match.any): bins that
+      // most keys share do not serialise the block on one address
+      const unsigned peers = __match_any_sync(0xffffffffu, dg);
+      if (t < n && lane == __ffs(peers) - 1) atomicAdd(&area[dg], __popc(peers));
+    }
+    __syncthreads();
+    select_digit(area, kRadixBins - 1, p.k, wsum, sh);
+    const uint32_t d0 = (uint32_t)sh[0];
+    prefix = d0 << 21;
+    mask = 0x7ffu << 21;
+    rem = sh[1];
+    const bool use_cand = sh[2] <= kCandCap;
+    __syncthreads();  // everyone has read sh and the histogram
+    if (use_cand) {
+      int *hs = area;
+      int *cand = area + kSmallBins;
+      // one sweep: keys above the top digit per warp, the bin's keys listed
+      int above = 0;
+      for (int t0 = s0; t0 < s1; t0 += 32) {
+        const int t = t0 + lane;
+        const uint32_t dg = t < s1 ? keys[t] >> 21 : 0u;
+        above += __popc(__ballot_sync(0xffffffffu, t < s1 && dg > d0));
+        const bool c = t < s1 && dg == d0;
+        const unsigned bc = __ballot_sync(0xffffffffu, c);
+        int cb = 0;
+        if (lane == 0 && bc) cb = atomicAdd(&ncand, __popc(bc));
+        cb = __shfl_sync(0xffffffffu, cb, 0);
+        if (c) cand[cb + __popc(bc & lt)] = t;
       }
-      __syncthreads();
-      select_digit(area, (int)dmask, rem, wsum, sh);
-      prefix |= (uint32_t)sh[0] << shift;
-      mask |= dmask << shift;
-      rem = sh[1];
-      __syncthreads();
-    }
-    int gt = 0, eqc = 0;
-    for (int t0 = s0; t0 < s1; t0 += 32) {
-      const int t = t0 + lane;
-      const uint32_t kv = t < s1 ? keys[t] : 0u;
-      gt += __popc(__ballot_sync(0xffffffffu, t < s1 && kv > prefix));
-      eqc += __popc(__ballot_sync(0xffffffffu, t < s1 && kv == prefix));
-    }
-    if (lane == 0) {
-      wgt[wid] = gt;
-      weq[wid] = eqc;
+      if (lane == 0) wgt[wid] = above;
+      // the remaining 21 bits in three 7-bit digits, over the bin only
+#pragma unroll 1
+      for (int pass = 0; pass < 3; ++pass) {
+        const int shift = 14 - 7 * pass;
+        for (int d = tid; d < kSmallBins; d += kTopkThreads) hs[d] = 0;
+        __syncthreads();
+        const int nc = ncand;
+        for (int c = tid; c < nc; c += kTopkThreads) {
+          const uint32_t kv = keys[cand[c]];
+          if ((kv & mask) == prefix) atomicAdd(&hs[(kv >> shift) & (kSmallBins - 1)], 1);
+        }
+        __syncthreads();
+        select_digit_warp(hs, kSmallBins - 1, rem, sh);
+        prefix |= (uint32_t)sh[0] << shift;
+        mask |= (uint32_t)(kSmallBins - 1) << shift;
+        rem = sh[1];
+      }
+      // the bin's keys above and equal to the k-th key, per owning warp
+      const int nc = ncand;
+      for (int c = tid; c < nc; c += kTopkThreads) {
+        const int t = cand[c];
+        const uint32_t kv = keys[t];
+        if (kv > prefix) atomicAdd(&wgt[t / L], 1);
+        else if (kv == prefix) atomicAdd(&weq[t / L], 1);
+      }
+    } else {
+      // too many keys in the bin: digits of 11 and 10 bits over every key
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
+        const int shift = pass == 0 ? 10 : 0;
+        const uint32_t dmask = pass == 0 ? 0x7ffu : 0x3ffu;
+        for (int d = tid; d < kRadixBins; d += kTopkThreads) area[d] = 0;
+        __syncthreads();
+        for (int t = tid; t < n; t += kTopkThreads) {
+          const uint32_t kv = keys[t];
+          if ((kv & mask) == prefix) atomicAdd(&area[(kv >> shift) & dmask], 1);
+        }
+        __syncthreads();
+        select_digit(area, (int)dmask, rem, wsum, sh);
+        prefix |= (uint32_t)sh[0] << shift;
+        mask |= dmask << shift;
+        rem = sh[1];
+        __syncthreads();
+      }
+      int gt = 0, eqc = 0;
+      for (int t0 = s0; t0 < s1; t0 += 32) {
+        const int t = t0 + lane;
+        const uint32_t kv = t < s1 ? keys[t] : 0u;
+        gt += __popc(__ballot_sync(0xffffffffu, t < s1 && kv > prefix));
+        eqc += __popc(__ballot_sync(0xffffffffu, t < s1 && kv == prefix));
+      }
+      if (lane == 0) {
+        wgt[wid] = gt;
+        weq[wid] = eqc;
+      }
     }
   }
   __syncthreads();

@@ -98,7 +98,7 @@ def test_indexer_ties():
     ki = ki[:, :3][:, pick].contiguous()
     sel, sc = hca.hca_indexer_topk(qi.to(DEV), ki.to(DEV), w.to(DEV), None, m, k, with_scores=True, check=True)
     sel_c, sc_c = sel.cpu().numpy(), sc.cpu().numpy()
-    for r0 in (0, 96, 3000, 6000, S - 8):
+    for r0 in (0, 96, 3000, 5500, 5600, 6000, S - 8):
         rows = (r0, r0 + 8)
         ref = CI.index_scores(qi, ki, w, None, m, rows=rows)
         _check_rows(sel_c[0, r0:r0 + 8], sc_c[0, r0:r0 + 8].astype(np.float64), ref[0], k)
