@@ -596,12 +596,39 @@ __global__ void __launch_bounds__(ckk::kThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&bars.d_free[x]);
-        if (c0 + r < cnt) {
-          float4 *dst = reinterpret_cast<float4 *>(p.acc + ((size_t)t.b * Q.Sc + ent[c0 + r]) * kHeadDim + cb);
+        // The block's D MMAs (done: d_full) were the last readers of its P
+        // and dS tiles, and this warp alone writes their rows [32 (warp & 3),
+        // +32) of half wg: 4 KB in each tile, the room for the warp's 32 rows
+        // of 64 fp32 values.  Staged there (float4 index XOR row, so no two
+        // lanes of an 8-lane phase share banks) and read back transposed,
+        // each atomic instruction adds two whole 256-byte row pieces instead
+        // of 32 scattered 16-byte pieces.
+        {
+          const int wl = warp & 3;
+          uint8_t *stg_p = smem + kOffP + wg * kHalfTile + wl * 32 * 128;
+          uint8_t *stg_d = smem + kOffDS + wg * kHalfTile + wl * 32 * 128;
 #pragma unroll
-          for (int q = 0; q < 16; ++q)
-            atomicAdd(dst + q, make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
-                                           __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3])));
+          for (int q = 0; q < 16; ++q) {
+            uint8_t *base = q < 8 ? stg_p : stg_d;
+            const int col = (q & 7) ^ (lane & 7);
+            *reinterpret_cast<float4 *>(base + lane * 128 + col * 16) =
+                make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]), __uint_as_float(o[4 * q + 2]),
+                            __uint_as_float(o[4 * q + 3]));
+          }
+          __syncwarp();
+          const int f = lane & 15;
+          const uint8_t *rbase = f < 8 ? stg_p : stg_d;
+#pragma unroll 2
+          for (int q = 0; q < 16; ++q) {
+            const int ri = 2 * q + (lane >> 4);  // the warp's row this lane adds to
+            const int e = c0 + wl * 32 + ri;       // its position in the union
+            if (e < cnt) {
+              const float4 v = *reinterpret_cast<const float4 *>(rbase + ri * 128 + (((f & 7) ^ (ri & 7)) * 16));
+              float4 *dst = reinterpret_cast<float4 *>(p.acc + ((size_t)t.b * Q.Sc + ent[e]) * kHeadDim + cb);
+              atomicAdd(dst + f, v);
+            }
+          }
+          __syncwarp();  // staging read before the next block's P and dS go there
         }
       }
     }
