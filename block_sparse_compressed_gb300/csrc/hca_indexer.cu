@@ -372,20 +372,22 @@ __device__ __forceinline__ void select_digit_warp(const int *h, int dmask, int r
 // fit beside the small histogram in the top digit's histogram space.
 constexpr int kSmallBins = 128;  // 7-bit digits over the candidates
 constexpr int kCandCap = kRadixBins - kSmallBins;
-// keys at or above a sampled threshold: 8-bit digits over them
+// keys at or above a sampled threshold, listed per warp: 8-bit digits over them
 constexpr int kByteBins = 256;
-constexpr int kTauCap = kRadixBins - kByteBins;
+constexpr int kListCap = (kRadixBins - kByteBins) / (kTopkThreads / 32);
 
 __global__ void __launch_bounds__(kTopkThreads, 6) hca_index_topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t keys[];
-  // the top digit's histogram; afterwards a small histogram and the
-  // candidate list, or (too many candidates) the wide histogram again
+  // the sample's top-digit histogram; then a small histogram and the
+  // warps' lists of keys at or above the threshold; on the exact path the
+  // top-digit histogram of every key, then a small histogram and the list of
+  // its bin's keys, or the wide histogram again
   __shared__ int area[kRadixBins];
   __shared__ int wsum[kTopkThreads / 32];
   __shared__ int sh[3];
   __shared__ int ncand;
   constexpr int kWarps = kTopkThreads / 32;
-  __shared__ int wgt[kWarps], weq[kWarps];
+  __shared__ int wgt[kWarps], weq[kWarps], wlist[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int b = blockIdx.x / p.rows;
   const int i = p.row0 + blockIdx.x % p.rows;
@@ -408,9 +410,9 @@ __global__ void __launch_bounds__(kTopkThreads, 6) hca_index_topk_kernel(const T
     for (int t = tid; t < p.k; t += kTopkThreads) out[t] = t < n ? lo + t : -1;
     return;
   }
-  // The keys are staged in shared memory (eight loads in flight per
-  // thread) while every eighth one (by entry index: at most four lanes of a
-  // warp per atomic) goes into a histogram of the top 11-bit digit.
+  // Every eighth key (by entry index) first, into a histogram of the top
+  // 11-bit digit: eight strided loads in flight per thread; they touch every
+  // 32-byte sector of the row once, so the staging below reads it from L2.
   for (int d = tid; d < kRadixBins; d += kTopkThreads) area[d] = 0;
   if (tid == 0) ncand = 0;
   if (tid < kWarps) {
@@ -420,21 +422,17 @@ __global__ void __launch_bounds__(kTopkThreads, 6) hca_index_topk_kernel(const T
   __syncthreads();
   constexpr int kInFlight = 8;
   const float *src = row + lo;
-  for (int t0 = 0; t0 < n; t0 += kInFlight * kTopkThreads) {
+  const int ns = (n + 7) >> 3;
+  for (int j0 = 0; j0 < ns; j0 += kInFlight * kTopkThreads) {
     uint32_t kv[kInFlight];
 #pragma unroll
     for (int u = 0; u < kInFlight; ++u) {
-      const int t = t0 + u * kTopkThreads + tid;
-      kv[u] = t < n ? fkey(src[t]) : 0u;
+      const int j = j0 + u * kTopkThreads + tid;
+      kv[u] = j < ns ? fkey(src[8 * j]) : 0u;
     }
 #pragma unroll
-    for (int u = 0; u < kInFlight; ++u) {
-      const int t = t0 + u * kTopkThreads + tid;
-      if (t < n) {
-        keys[t] = kv[u];
-        if ((t & 7) == 0) atomicAdd(&area[kv[u] >> 21], 1);
-      }
-    }
+    for (int u = 0; u < kInFlight; ++u)
+      if (j0 + u * kTopkThreads + tid < ns) atomicAdd(&area[kv[u] >> 21], 1);
   }
   __syncthreads();
   // Threshold: the lower edge of the top-digit bin where the sample's count
@@ -442,51 +440,63 @@ __global__ void __launch_bounds__(kTopkThreads, 6) hca_index_topk_kernel(const T
   // deviations of that count), so that normally at least k keys lie at or
   // above it; the sample's own digits are exact, only the count is an
   // estimate.
-  const int ns = (n + 7) >> 3;
   const int want = min(ns, (int)(((long long)p.k * 115 * ns + 100LL * n - 1) / (100LL * n)) + 16);
   select_digit(area, kRadixBins - 1, want, wsum, sh);
   const uint32_t tau = (uint32_t)sh[0] << 21;
   __syncthreads();  // everyone has read sh and the histogram
-  // Winners are the keys above prefix plus the rem keys equal to it with the
-  // smallest entry index.  Warp w owns the keys [w L, (w + 1) L) for the
-  // ordered output (and for the per-warp counts).
+  // Warp w owns the keys [w L, (w + 1) L): it stages them (eight loads in
+  // flight per lane, 128 bytes per warp load) and lists the ones at or above
+  // the threshold, in entry order, in its own part of the area.
   const int L = ((n + kWarps - 1) / kWarps + 31) & ~31;
   const int s0 = min(wid * L, n), s1 = min(s0 + L, n);
   const uint32_t lt = (1u << lane) - 1u;
-  uint32_t prefix = 0, mask = 0;
-  int rem = p.k;  // winners still to place at or below the current prefix
-  {
-    // one sweep: the keys at or above the threshold, listed if they fit
-    int *cand = area + kByteBins;
-    for (int t0 = s0; t0 < s1; t0 += 32) {
-      const int t = t0 + lane;
-      const bool c = t < s1 && keys[t] >= tau;
+  int *lists = area + kByteBins;
+  int *mine = lists + wid * kListCap;
+  int wn = 0;
+  for (int c0 = s0; c0 < s1; c0 += kInFlight * 32) {
+    uint32_t kv[kInFlight];
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      const int t = c0 + u * 32 + lane;
+      kv[u] = t < s1 ? fkey(src[t]) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      const int t = c0 + u * 32 + lane;
+      const bool c = t < s1 && kv[u] >= tau;
+      if (t < s1) keys[t] = kv[u];
       const unsigned bc = __ballot_sync(0xffffffffu, c);
-      if (bc) {
-        int cb = 0;
-        if (lane == 0) cb = atomicAdd(&ncand, __popc(bc));
-        cb = __shfl_sync(0xffffffffu, cb, 0);
-        const int slot = cb + __popc(bc & lt);
-        if (c && slot < kTauCap) cand[slot] = t;
-      }
+      const int slot = wn + __popc(bc & lt);
+      if (c && slot < kListCap) mine[slot] = t;
+      wn += __popc(bc);
     }
   }
+  if (lane == 0) wlist[wid] = wn;
   __syncthreads();
-  const int nlisted = ncand;
-  __syncthreads();  // read by everyone before the exact path may reset it
-  if (nlisted >= p.k && nlisted <= kTauCap) {
+  int nlisted = 0;
+  bool fits = true;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    nlisted += wlist[w];
+    fits = fits && wlist[w] <= kListCap;
+  }
+  uint32_t prefix = 0, mask = 0;
+  int rem = p.k;  // winners still to place at or below the current prefix
+  if (fits && nlisted >= p.k) {
     // the k-th largest key is among the listed ones (every other key is
-    // below the threshold): four 8-bit digits over the list
+    // below the threshold): four 8-bit digits over the lists
     int *hs = area;
-    const int *cand = area + kByteBins;
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
       for (int d = tid; d < kByteBins; d += kTopkThreads) hs[d] = 0;
       __syncthreads();
-      for (int c = tid; c < nlisted; c += kTopkThreads) {
-        const uint32_t kv = keys[cand[c]];
-        if ((kv & mask) == prefix) atomicAdd(&hs[(kv >> shift) & (kByteBins - 1)], 1);
+      for (int w = 0; w < kWarps; ++w) {
+        const int nw = wlist[w];
+        for (int c = tid; c < nw; c += kTopkThreads) {
+          const uint32_t kv = keys[lists[w * kListCap + c]];
+          if ((kv & mask) == prefix) atomicAdd(&hs[(kv >> shift) & (kByteBins - 1)], 1);
+        }
       }
       __syncthreads();
       // the next pass zeroes hs only after two more barriers, and sh is
@@ -496,12 +506,39 @@ __global__ void __launch_bounds__(kTopkThreads, 6) hca_index_topk_kernel(const T
       mask |= (uint32_t)(kByteBins - 1) << shift;
       rem = sh[1];
     }
-    for (int c = tid; c < nlisted; c += kTopkThreads) {
-      const int t = cand[c];
-      const uint32_t kv = keys[t];
-      if (kv > prefix) atomicAdd(&wgt[t / L], 1);
-      else if (kv == prefix) atomicAdd(&weq[t / L], 1);
+    // ordered write from the lists: winners are the listed keys above
+    // prefix plus the rem keys equal to it with the smallest entry index
+    int gt = 0, eqc = 0;
+    for (int c0 = 0; c0 < wn; c0 += 32) {
+      const int c = c0 + lane;
+      const uint32_t kv = c < wn ? keys[mine[c]] : 0u;
+      gt += __popc(__ballot_sync(0xffffffffu, c < wn && kv > prefix));
+      eqc += __popc(__ballot_sync(0xffffffffu, c < wn && kv == prefix));
     }
+    if (lane == 0) {
+      wgt[wid] = gt;
+      weq[wid] = eqc;
+    }
+    __syncthreads();
+    int gt_run = 0, eq_run = 0;
+    for (int w = 0; w < wid; ++w) {
+      gt_run += wgt[w];
+      eq_run += weq[w];
+    }
+    int placed = gt_run + min(eq_run, rem);
+    for (int c0 = 0; c0 < wn; c0 += 32) {
+      const int c = c0 + lane;
+      const int t = c < wn ? mine[c] : 0;
+      const uint32_t kv = c < wn ? keys[t] : 0u;
+      const bool eq = c < wn && kv == prefix;
+      const uint32_t beq = __ballot_sync(0xffffffffu, eq);
+      const bool take = c < wn && (kv > prefix || (eq && eq_run + __popc(beq & lt) < rem));
+      const uint32_t btake = __ballot_sync(0xffffffffu, take);
+      if (take) out[placed + __popc(btake & lt)] = lo + t;
+      placed += __popc(btake);
+      eq_run += __popc(beq);
+    }
+    return;
   } else {
     // the sample missed: the exact top digit from every key
     for (int d = tid; d < kRadixBins; d += kTopkThreads) area[d] = 0;
