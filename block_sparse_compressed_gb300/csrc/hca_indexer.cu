@@ -376,7 +376,7 @@ constexpr int kCandCap = kRadixBins - kSmallBins;
 constexpr int kByteBins = 256;
 constexpr int kListCap = (kRadixBins - kByteBins) / (kTopkThreads / 32);
 
-__global__ void __launch_bounds__(kTopkThreads, 6) hca_index_topk_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kTopkThreads, 5) hca_index_topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t keys[];
   // the sample's top-digit histogram; then a small histogram and the
   // warps' lists of keys at or above the threshold; on the exact path the
@@ -486,17 +486,32 @@ __global__ void __launch_bounds__(kTopkThreads, 6) hca_index_topk_kernel(const T
     // the k-th largest key is among the listed ones (every other key is
     // below the threshold): four 8-bit digits over the lists
     int *hs = area;
+    // listed key c of the concatenated lists: warp w = the last with
+    // start[w] <= c, slot c - start[w] (all threads share every pass evenly)
+    int start[kWarps];
+    {
+      int run = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        start[w] = run;
+        run += wlist[w];
+      }
+    }
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
       for (int d = tid; d < kByteBins; d += kTopkThreads) hs[d] = 0;
       __syncthreads();
-      for (int w = 0; w < kWarps; ++w) {
-        const int nw = wlist[w];
-        for (int c = tid; c < nw; c += kTopkThreads) {
-          const uint32_t kv = keys[lists[w * kListCap + c]];
-          if ((kv & mask) == prefix) atomicAdd(&hs[(kv >> shift) & (kByteBins - 1)], 1);
-        }
+      for (int c = tid; c < nlisted; c += kTopkThreads) {
+        int w = 0, sw = 0;
+#pragma unroll
+        for (int x = 1; x < kWarps; ++x)
+          if (c >= start[x]) {
+            w = x;
+            sw = start[x];
+          }
+        const uint32_t kv = keys[lists[w * kListCap + (c - sw)]];
+        if ((kv & mask) == prefix) atomicAdd(&hs[(kv >> shift) & (kByteBins - 1)], 1);
       }
       __syncthreads();
       // the next pass zeroes hs only after two more barriers, and sh is
