@@ -74,11 +74,28 @@ namespace isk {
 constexpr int kStages = 2;
 constexpr int kThreads = 192;  // warps 0-3 epilogue (one TMEM lane quarter each), 4 TMA, 5 MMA
 constexpr int kOffA = 0, kOffB = kTile;
-constexpr int kStageLd = kBlockKeys + 4;  // staging row pitch in floats (bank-conflict padding)
+// output staging: two buffers (one per accumulator), each four 32-column
+// fp32 quarters of 128 rows x 128 bytes, 128B-swizzled for the TMA store
+constexpr int kQuarter = kRows * 128;
+constexpr int kStageBuf = 4 * kQuarter;
 constexpr int kOffStage = kTile + kStages * kTile;
-constexpr int kSmemBytes = kOffStage + kRows * kStageLd * 4 + 1024;
+constexpr int kSmemBytes = kOffStage + 2 * kStageBuf + 1024;
 constexpr int kTmemCols = 256;  // two 128-column accumulators
 }  // namespace isk
+
+// 3-D view {ld, rows, B} of the fp32 score chunk with a 32-column, 128-row
+// box (128 bytes per row, 128B-swizzled): the map of the score stores.
+static bool make_map_scores(CUtensorMap *m, float *buf, uint64_t ld, uint64_t rows, uint64_t B) {
+  tc::EncodeTiledFn enc = tc::encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {ld, rows, B};
+  cuuint64_t strides[2] = {ld * 4, ld * rows * 4};
+  cuuint32_t box[3] = {32, (cuuint32_t)kRows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, buf, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
 
 struct ScoreParams {
   const int32_t *sstart;  // NULL = one document per row
@@ -103,7 +120,7 @@ __device__ __forceinline__ int entries_upto(int p1, int m) { return p1 / m; }
 
 __global__ void __launch_bounds__(isk::kThreads, 1)
     hca_index_score_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                           const ScoreParams p) {
+                           const __grid_constant__ CUtensorMap map_s, const ScoreParams p) {
   using namespace isk;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -206,11 +223,13 @@ __global__ void __launch_bounds__(isk::kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     // thread r = row r of the tile (TMEM lane r) stages its 128 scores of a
-    // block in shared memory; then every warp writes whole rows, so each
-    // store instruction covers one contiguous 512-byte row segment
+    // block (four 128B-swizzled quarters, conflict-free); thread 0 stores the
+    // block with four TMA tensor stores (rows past the chunk are clipped).
+    // Staging buffer j & 1 is written again two blocks later: before the
+    // rendezvous of block j, thread 0 waits until block j - 1's stores have
+    // read their buffer, so every thread may write it in block j + 1.
     const int r = tid;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    float *stage = reinterpret_cast<float *>(smem + kOffStage);
     uint32_t epi_phase = 0;
     // bounded rendezvous of the four epilogue warps (an abort ends it too)
     auto rendezvous = [&]() -> bool {
@@ -223,28 +242,30 @@ __global__ void __launch_bounds__(isk::kThreads, 1)
       const int x = j & 1;
       if (!wait_warp(&bars.acc_full[x], (j / 2) & 1, abort_flag, p.status, p.wait_ns)) break;
       tc_fence_after();
+      uint8_t *buf = smem + kOffStage + x * kStageBuf;
 #pragma unroll
-      for (int c0 = 0; c0 < kBlockKeys; c0 += 32) {
+      for (int q = 0; q < 4; ++q) {
         uint32_t v[32];
-        tmem_ld32(lane_addr + x * 128 + c0, v);
+        tmem_ld32(lane_addr + x * 128 + 32 * q, v);
         tmem_wait_ld();
-        float4 *d4 = reinterpret_cast<float4 *>(stage + r * kStageLd + c0);
+        uint8_t *rowp = buf + q * kQuarter + r * 128;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
-                              __uint_as_float(v[4 * q + 3]));
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4 *>(rowp + ((c ^ (r & 7)) << 4)) = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
       }
       tc_fence_before();
       mbar_arrive(&bars.acc_free[x]);
+      fence_async_smem();
+      if (tid == 0) bulk_wait_read0();  // block j - 1's stores have read the other buffer
       if (!rendezvous()) break;
-      for (int rr = warp * 32; rr < warp * 32 + 32; ++rr) {
-        if (p0 + rr >= p1) break;
-        const float4 v = reinterpret_cast<const float4 *>(stage + rr * kStageLd)[lane];
-        float *dst = p.buf + ((size_t)b * p.rows + (p0 + rr - p.row0)) * p.ld + (j0 + j) * kBlockKeys;
-        reinterpret_cast<float4 *>(dst)[lane] = v;
+      if (tid == 0) {
+        const int cx = (j0 + j) * kBlockKeys, cy = p0 - p.row0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tma_store_3d(&map_s, buf + q * kQuarter, cx + 32 * q, cy, b);
+        bulk_commit();
       }
-      if (!rendezvous()) break;
     }
+    if (tid == 0) bulk_wait0();
   }
   tc_fence_before();
   __syncthreads();
@@ -708,7 +729,7 @@ cudaError_t indexer_topk(const IndexerArgs &a, cudaStream_t st) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  CUtensorMap mq, mk;
+  CUtensorMap mq, mk, ms;
   if (!make_map_bf16(&mq, qc, kHeadDim, a.S, a.B, kRows, 1) || !make_map_bf16(&mk, a.ki, kHeadDim, Sc, a.B, kBlockKeys, 1))
     return cudaErrorInvalidValue;
   static SmemAttrOnce attr_s, attr_t;
@@ -725,9 +746,11 @@ cudaError_t indexer_topk(const IndexerArgs &a, cudaStream_t st) {
     // enough CTAs for two per SM, each with at least two entry blocks
     const int max_blk = (Sc + kBlockKeys - 1) / kBlockKeys;
     sp.groups = max(1, min((2 * sm_count() + tiles - 1) / tiles, max_blk / 2));
+    // the chunk buffer holds `rows` rows at pitch ld (16-byte aligned rows: ld is a multiple of 128)
+    if (!make_map_scores(&ms, a.buf, (uint64_t)ld, (uint64_t)rows, (uint64_t)a.B)) return cudaErrorInvalidValue;
     {
       ProfScope prof(kKIndexScore, st);
-      hca_index_score_kernel<<<tiles * sp.groups, isk::kThreads, isk::kSmemBytes, st>>>(mq, mk, sp);
+      hca_index_score_kernel<<<tiles * sp.groups, isk::kThreads, isk::kSmemBytes, st>>>(mq, mk, ms, sp);
       e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
