@@ -117,6 +117,42 @@ def test_csa_selecting_everything_is_hca():
         assert_close(name, a, to_np(b), torch.bfloat16)
 
 
+def test_csa_full_size_sampled_rows():
+    # the CSA bench workload, B1 H64 S65536 D128 W128 m4 k256 with random
+    # selections: out, lse and dq on sampled rows; exactly, the gradients of
+    # the last 32 raw keys and the last 8 compressed entries (only the last 64
+    # positions see them, and those positions are made to select the 8
+    # entries); and, over every key, the sum identity (the gradients of all
+    # keys add up to the sum of dO, since each row's softmax sums to one and
+    # its dS sums to zero)
+    B, H, S, D, W, m, k = 1, 64, 65536, 128, 128, 4, 256
+    Sc = S // m
+    scale = 1.0 / math.sqrt(D)
+    q, kv, ckv, _, dout = I.small(B, H, S, D, W, m, dtype=torch.bfloat16, seed=21, device=DEV)
+    sel = I.random_selection(B, S, m, k, 71)
+    sel[0, S - 64:, :8] = torch.arange(Sc - 8, Sc, dtype=torch.int32)
+    out, lse = hca.hca_csa_attn_fwd(q, kv, ckv, None, sel.to(DEV), W, m, scale, check=True)
+    dq, dkv, dckv = hca.hca_csa_attn_bwd(q, kv, ckv, None, sel.to(DEV), out, lse, dout, W, m, scale, check=True)
+    torch.cuda.synchronize()
+    keep = oracle.topk_mask(sel, Sc)
+    qc, kvc, ckvc, dc = q.cpu(), kv.cpu(), ckv.cpu(), dout.cpu()
+    out_c, lse_c, dq_c = to_np(out)[0], to_np(lse)[0], to_np(dq)[0]
+    for lo in (0, 1022, 20000, 40962, S - 66):
+        hi = lo + 2
+        ro, rl = oracle.csa_fwd(qc, kvc, ckvc, None, keep, W, m, scale, rows=(lo, hi))
+        assert_close(f"out [{lo},{hi})", out_c[:, lo:hi], ro[0][:, lo:hi], torch.bfloat16)
+        assert_close(f"lse [{lo},{hi})", lse_c[:, lo:hi], rl[0][:, lo:hi], torch.bfloat16)
+        rdq, _, _ = oracle.csa_bwd(qc, kvc, ckvc, None, keep, dc, W, m, scale, rows=(lo, hi))
+        assert_close(f"dq [{lo},{hi})", dq_c[:, lo:hi], rdq[0][:, lo:hi], torch.bfloat16)
+    _, rdkv, rdckv = oracle.csa_bwd(qc, kvc, ckvc, None, keep, dc, W, m, scale, rows=(S - 64, S))
+    dkv_c, dckv_c = to_np(dkv)[0], to_np(dckv)[0]
+    assert_close("dkv, last 32 keys", dkv_c[S - 32:], rdkv[0][S - 32:], torch.bfloat16)
+    assert np.abs(rdckv[0][Sc - 8:]).max() > 0
+    assert_close("dckv, last 8 entries", dckv_c[Sc - 8:], rdckv[0][Sc - 8:], torch.bfloat16)
+    total = dkv_c.astype(np.float64).sum(0) + dckv_c.astype(np.float64).sum(0)
+    assert_close("sum identity", total, to_np(dout[0].float().sum((0, 1))), torch.bfloat16)
+
+
 def test_csa_fed_by_the_indexer():
     # the indexer's top-k selection drives the attention (the CSA chain)
     B, H, S, W, m, k = 1, 64, 512, 64, 4, 12
