@@ -48,6 +48,26 @@ def test_compressor_matches_oracle(B, S, D, m, dtype):
     assert torch.equal(dx, dx2) and torch.equal(dg, dg2) and torch.equal(db, db2)
 
 
+def test_compressor_bench_size_exact():
+    # the bench workload, B16 S65536 D128 m128 bf16 with the bench's seeds:
+    # every output against the oracle (the windows are independent, so the
+    # whole tensor is cheap to check)
+    B, S, D, m = 16, 65536, 128, 128
+    x = I.normal((B, S, D), 1, torch.bfloat16)
+    g = I.normal((B, S), 2, torch.float32)
+    bias = I.normal((m,), 3, torch.float32)
+    dck = I.normal((B, S // m, D), 4, torch.bfloat16)
+    gd = [t.to(DEV) for t in (x, g, bias, dck)]
+    ckv = hca.hca_compress_fwd(gd[0], gd[1], gd[2], None, m)
+    dx, dg, db = hca.hca_compress_bwd(gd[0], gd[1], gd[2], None, m, gd[3])
+    torch.cuda.synchronize()
+    assert_close("ckv", ckv, CI.compress_fwd(x, g, bias, None, m), torch.bfloat16)
+    rdx, rdg, rdb = CI.compress_bwd(x, g, bias, None, m, dck)
+    assert_close("dx", dx, rdx, torch.bfloat16)
+    assert_close("dg", dg, rdg, torch.bfloat16)
+    assert_close("dbias", db, rdb, torch.bfloat16)
+
+
 def test_compressor_without_segments_and_unsupported_dim():
     x, g, bias, _ = _inputs(1, 512, 128, 16, torch.bfloat16, 5)
     ckv = hca.hca_compress_fwd(x.to(DEV), g.to(DEV), bias.to(DEV), None, 16)
