@@ -69,3 +69,28 @@ def test_local_f32():
 
 def test_local_s8192_one_document():
     run_local(1, 64, 8192, 128, 128, torch.bfloat16)
+
+
+def test_local_full_size_sampled_rows():
+    # the local bench workload, B1 H64 S65536 D128 W128: out, lse and dq on
+    # sampled rows; dkv exactly for a few key ranges (key j is seen by the W
+    # queries [j, j + W) alone, so those rows give its whole gradient)
+    B, H, S, D, W = 1, 64, 65536, 128, 128
+    m = S + 1
+    scale = 1.0 / math.sqrt(D)
+    q, kv, ckv, _, dout = I.small(B, H, S, D, W, m, dtype=torch.bfloat16, seed=31, device=DEV)
+    out, lse = hca.hca_local_attn_fwd(q, kv, None, W, scale, check=True)
+    dq, dkv = hca.hca_local_attn_bwd(q, kv, None, out, lse, dout, W, scale, check=True)
+    torch.cuda.synchronize()
+    qc, kvc, ckvc, dc = q.cpu(), kv.cpu(), ckv.cpu(), dout.cpu()
+    out_c, lse_c, dq_c, dkv_c = to_np(out)[0], to_np(lse)[0], to_np(dq)[0], to_np(dkv)[0]
+    for lo in (0, 127, 33000, S - 2):
+        hi = lo + 2
+        ro, rl = oracle.fwd(qc, kvc, ckvc, None, W, m, scale, rows=(lo, hi))
+        assert_close(f"out [{lo},{hi})", out_c[:, lo:hi], ro[0][:, lo:hi], torch.bfloat16)
+        assert_close(f"lse [{lo},{hi})", lse_c[:, lo:hi], rl[0][:, lo:hi], torch.bfloat16)
+        rdq, _, _ = oracle.bwd(qc, kvc, ckvc, None, dc, W, m, scale, rows=(lo, hi))
+        assert_close(f"dq [{lo},{hi})", dq_c[:, lo:hi], rdq[0][:, lo:hi], torch.bfloat16)
+    for j0 in (0, 40000, S - 4):
+        _, rdkv, _ = oracle.bwd(qc, kvc, ckvc, None, dc, W, m, scale, rows=(j0, min(S, j0 + 3 + W)))
+        assert_close(f"dkv [{j0},{j0 + 4})", dkv_c[j0:j0 + 4], rdkv[0][j0:j0 + 4], torch.bfloat16)
